@@ -1,0 +1,586 @@
+// C ABI of libh3: argument validation (fail closed, before any launch), TMA
+// tensor maps, the block's workspace plan and the stage composition.
+#include "h3.h"
+#include "h3_device.cuh"
+#include "h3_internal.h"
+
+#include <chrono>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <thread>
+
+#include <cudaTypedefs.h>
+
+namespace h3 {
+
+// Device error word: set by kernels on bad metadata or a wait that ran out,
+// read and cleared by h3_sync_check.
+__device__ uint32_t g_error_word = 0;
+
+namespace {
+thread_local char g_info[512] = "";
+constexpr int kMaxDevices = 64;
+int g_sms[kMaxDevices] = {0};
+uint32_t* g_err_ptr[kMaxDevices] = {nullptr};
+std::mutex g_mu;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int current_device() {
+  int d = 0;
+  cudaGetDevice(&d);
+  return d < 0 || d >= kMaxDevices ? 0 : d;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  return g_encode;
+}
+}  // namespace
+
+void set_kernel_info(const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_info, sizeof(g_info), fmt, ap);
+  va_end(ap);
+}
+
+int num_sms() {
+  const int d = current_device();
+  if (!g_sms[d]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, d);
+    g_sms[d] = n > 0 ? n : 1;
+  }
+  return g_sms[d];
+}
+
+uint32_t* device_error_word() {
+  const int d = current_device();
+  if (!g_err_ptr[d]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_error_word) == cudaSuccess) g_err_ptr[d] = static_cast<uint32_t*>(p);
+  }
+  return g_err_ptr[d];
+}
+
+bool make_tmap_2d(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t cols, uint64_t ld,
+                  uint32_t box_rows) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {ld * 2};
+  const cuuint32_t box[2] = {64, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_tmap_qkv(CUtensorMap* tm, const void* base, uint64_t n_rows, uint64_t n_heads, uint64_t row_stride,
+                   uint64_t head_stride, uint32_t box_rows) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {128, n_heads, n_rows};
+  const cuuint64_t strides[2] = {head_stride * 2, row_stride * 2};
+  const cuuint32_t box[3] = {64, 1, box_rows};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace h3
+
+using namespace h3;
+
+// ===========================================================================
+// validation helpers
+// ===========================================================================
+namespace {
+
+inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool al16n(const void* p) { return p == nullptr || al16(p); }
+inline size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
+
+h3_status check_cfg(const h3_block_config* c) {
+  if (!c) return H3_ERR_NULL;
+  if (c->head_dim != 128 || c->rope_freqs_per_axis != 16 || c->rope_channels != 96) return H3_ERR_UNSUPPORTED;
+  if (c->dim < 64 || c->dim % 64 || c->dim > 8192) return H3_ERR_UNSUPPORTED;
+  if (c->cond_dim < 64 || c->cond_dim % 64 || c->cond_dim > 2816) return H3_ERR_UNSUPPORTED;
+  if (c->ffn_dim < 128 || c->ffn_dim % 128) return H3_ERR_UNSUPPORTED;
+  if (c->n_heads < 1 || c->n_heads > 1024) return H3_ERR_UNSUPPORTED;
+  if (!(c->eps > 0.0f) || !std::isfinite(c->eps)) return H3_ERR_SHAPE;
+  if (!(c->rope_theta > 1.0f) || !std::isfinite(c->rope_theta)) return H3_ERR_SHAPE;
+  return H3_OK;
+}
+
+h3_status check_meta(const h3_packed_meta* m, bool need_tables) {
+  if (!m) return H3_ERR_NULL;
+  if (m->n_rows < 1) return H3_ERR_SHAPE;
+  if (!m->token_tag || !m->timestep_index || !m->pos_thw) return H3_ERR_NULL;
+  if (need_tables) {
+    if (m->n_timesteps < 1 || m->n_timesteps > 16) return H3_ERR_UNSUPPORTED;
+    if (!m->t_cond) return H3_ERR_NULL;
+  }
+  return H3_OK;
+}
+
+h3_status cuda_st(cudaError_t e) { return e == cudaSuccess ? H3_OK : H3_ERR_CUDA; }
+
+void fill_omega(float* omega, float theta) {
+  for (int i = 0; i < 16; ++i) omega[i] = (float)std::pow((double)theta, -(double)i / 16.0);
+}
+
+struct WsLayout {
+  size_t table, h, qkv, o, x1, total;
+};
+WsLayout ws_layout(const h3_block_config& c, int64_t S, int64_t T) {
+  const size_t D = (size_t)c.dim, I = (size_t)c.n_heads * 128, F = (size_t)c.ffn_dim;
+  WsLayout L{};
+  size_t off = 0;
+  L.table = off;
+  off = al256(off + (size_t)T * 18 * D * 2);
+  L.h = off;
+  off = al256(off + (size_t)S * D * 2);
+  L.qkv = off;   // qkv [S][3I], later the SwiGLU activations [S][F]
+  off = al256(off + (size_t)S * (3 * I > F ? 3 * I : F) * 2);
+  L.o = off;
+  off = al256(off + (size_t)S * I * 2);
+  L.x1 = off;
+  off = al256(off + (size_t)S * D * 2);
+  L.total = off;
+  return L;
+}
+
+// ---------------------------------------------------------------------------
+// stage launchers (arguments already validated)
+// ---------------------------------------------------------------------------
+h3_status run_adaln_table(const h3_block_config& c, const void* w_ada, const void* b_ada, const float* t_cond,
+                          int T, void* out, cudaStream_t st) {
+  CUtensorMap tm;
+  if (!make_tmap_2d(&tm, w_ada, (uint64_t)18 * c.dim, (uint64_t)c.cond_dim, (uint64_t)c.cond_dim, 128))
+    return H3_ERR_CUDA;
+  AdalnArgs a{};
+  a.C = c.cond_dim;
+  a.T = T;
+  a.NW = 18 * c.dim;
+  a.t_cond = t_cond;
+  a.bias = static_cast<const __nv_bfloat16*>(b_ada);
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.err = device_error_word();
+  return cuda_st(launch_adaln_table(tm, a, st));
+}
+
+h3_status run_modulate(const h3_block_config& c, const h3_packed_meta& m, const void* table, int branch,
+                       const void* x, const void* g, void* h, cudaStream_t st) {
+  ModulateArgs a{};
+  a.S = m.n_rows;
+  a.D = c.dim;
+  a.T = m.n_timesteps;
+  a.x = static_cast<const __nv_bfloat16*>(x);
+  a.gain = static_cast<const __nv_bfloat16*>(g);
+  a.table = static_cast<const __nv_bfloat16*>(table);
+  a.chunk_shift = branch == 0 ? 0 : 3;
+  a.chunk_scale = branch == 0 ? 1 : 4;
+  a.tag = m.token_tag;
+  a.tidx = m.timestep_index;
+  a.eps = c.eps;
+  a.h = static_cast<__nv_bfloat16*>(h);
+  a.err = device_error_word();
+  return cuda_st(launch_modulate(a, st));
+}
+
+void gemm_common(GemmArgs& a, int M, int K, int num_n) {
+  a.M = M;
+  a.K = K;
+  a.num_m = (M + 127) / 128;
+  a.num_n = num_n;
+  a.num_k = K / 64;
+  a.err = device_error_word();
+}
+
+h3_status run_qkv(const h3_block_config& c, const h3_packed_meta& m, const void* h, const void* w_qkv,
+                  const void* b_qkv, const void* qg, const void* kg, void* out, cudaStream_t st) {
+  const int S = m.n_rows, D = c.dim, H = c.n_heads;
+  CUtensorMap tA, tB;
+  if (!make_tmap_2d(&tA, h, S, D, D, 128) || !make_tmap_2d(&tB, w_qkv, (uint64_t)3 * H * 128, D, D, 128))
+    return H3_ERR_CUDA;
+  GemmArgs a{};
+  gemm_common(a, S, D, H + (H + 1) / 2);
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.ldo = 3 * H * 128;
+  a.bias = static_cast<const __nv_bfloat16*>(b_qkv);
+  a.H = H;
+  a.q_gain = static_cast<const __nv_bfloat16*>(qg);
+  a.k_gain = static_cast<const __nv_bfloat16*>(kg);
+  a.pos = m.pos_thw;
+  a.eps = c.eps;
+  fill_omega(a.omega, c.rope_theta);
+  return cuda_st(launch_gemm(EPI_QKV, tA, tB, a, st));
+}
+
+h3_status run_attention(int S, int H, const void* q, const void* k, const void* v, int64_t rs, int64_t hs,
+                        void* o, float* lse, cudaStream_t st) {
+  CUtensorMap tq, tk, tv;
+  if (!make_tmap_qkv(&tq, q, S, H, rs, hs, 128) || !make_tmap_qkv(&tk, k, S, H, rs, hs, 128) ||
+      !make_tmap_qkv(&tv, v, S, H, rs, hs, 128))
+    return H3_ERR_CUDA;
+  AttnArgs a{};
+  a.S = S;
+  a.H = H;
+  a.o = static_cast<__nv_bfloat16*>(o);
+  a.lse = lse;
+  a.scale_log2 = (float)(1.4426950408889634 / std::sqrt(128.0));
+  a.err = device_error_word();
+  return cuda_st(launch_attention(tq, tk, tv, a, st));
+}
+
+h3_status run_resid_gemm(const h3_block_config& c, const h3_packed_meta& m, const void* table, int chunk,
+                         const void* act, int K, const void* w, const void* b, const void* x, void* out,
+                         cudaStream_t st) {
+  const int S = m.n_rows, D = c.dim;
+  CUtensorMap tA, tB;
+  if (!make_tmap_2d(&tA, act, S, K, K, 128) || !make_tmap_2d(&tB, w, D, K, K, 128)) return H3_ERR_CUDA;
+  GemmArgs a{};
+  gemm_common(a, S, K, (D + 255) / 256);
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.ldo = D;
+  a.bias = static_cast<const __nv_bfloat16*>(b);
+  a.n_valid = D;
+  a.resid = static_cast<const __nv_bfloat16*>(x);
+  a.ldr = D;
+  a.table = static_cast<const __nv_bfloat16*>(table);
+  a.D = D;
+  a.chunk = chunk;
+  a.T = m.n_timesteps;
+  a.tag = m.token_tag;
+  a.tidx = m.timestep_index;
+  return cuda_st(launch_gemm(EPI_RESID, tA, tB, a, st));
+}
+
+h3_status run_ffn_up(const h3_block_config& c, int S, const void* h, const void* w1, const void* b1, void* out,
+                     cudaStream_t st) {
+  const int D = c.dim, F = c.ffn_dim;
+  CUtensorMap tA, tB;
+  if (!make_tmap_2d(&tA, h, S, D, D, 128) || !make_tmap_2d(&tB, w1, (uint64_t)2 * F, D, D, 128))
+    return H3_ERR_CUDA;
+  GemmArgs a{};
+  gemm_common(a, S, D, F / 128);
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.ldo = F;
+  a.bias = static_cast<const __nv_bfloat16*>(b1);
+  a.F = F;
+  return cuda_st(launch_gemm(EPI_SWIGLU, tA, tB, a, st));
+}
+
+h3_status check_block_weights(const h3_block_weights* w) {
+  if (!w) return H3_ERR_NULL;
+  if (!w->w_ada || !w->norm1_g || !w->norm2_g || !w->w_qkv || !w->q_norm_g || !w->k_norm_g || !w->w_o ||
+      !w->w_fc1 || !w->w_fc2)
+    return H3_ERR_NULL;
+  const void* req[] = {w->w_ada, w->norm1_g, w->norm2_g, w->w_qkv, w->q_norm_g, w->k_norm_g,
+                       w->w_o, w->w_fc1, w->w_fc2};
+  for (const void* p : req)
+    if (!al16(p)) return H3_ERR_ALIGN;
+  const void* opt[] = {w->b_ada, w->b_qkv, w->b_o, w->b_fc1, w->b_fc2};
+  for (const void* p : opt)
+    if (!al16n(p)) return H3_ERR_ALIGN;
+  return H3_OK;
+}
+
+h3_status block_impl(const h3_block_config* cfg, const h3_block_weights* w, const h3_packed_meta* meta,
+                     const void* x_in, void* x_out, void* ws, size_t ws_bytes, cudaStream_t st,
+                     void* const* events, int n_events) {
+  const int S = meta->n_rows, T = meta->n_timesteps;
+  const WsLayout L = ws_layout(*cfg, S, T);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  void* table = base + L.table;
+  void* h = base + L.h;
+  void* qkv = base + L.qkv;
+  void* o = base + L.o;
+  void* x1 = base + L.x1;
+  const int I = cfg->n_heads * 128;
+  int stage = 0;
+  auto mark = [&]() -> h3_status {
+    if (events && stage < n_events && events[stage]) {
+      if (cudaEventRecord(static_cast<cudaEvent_t>(events[stage]), st) != cudaSuccess) return H3_ERR_CUDA;
+    }
+    ++stage;
+    return H3_OK;
+  };
+  h3_status s;
+#define H3_TRY(expr)            \
+  if ((s = (expr)) != H3_OK) return s; \
+  if ((s = mark()) != H3_OK) return s;
+  H3_TRY(run_adaln_table(*cfg, w->w_ada, w->b_ada, meta->t_cond, T, table, st));
+  H3_TRY(run_modulate(*cfg, *meta, table, 0, x_in, w->norm1_g, h, st));
+  H3_TRY(run_qkv(*cfg, *meta, h, w->w_qkv, w->b_qkv, w->q_norm_g, w->k_norm_g, qkv, st));
+  {
+    const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(qkv);
+    H3_TRY(run_attention(S, cfg->n_heads, q, q + 128, q + 256, 3 * I, 384, o, nullptr, st));
+  }
+  H3_TRY(run_resid_gemm(*cfg, *meta, table, 2, o, I, w->w_o, w->b_o, x_in, x1, st));
+  H3_TRY(run_modulate(*cfg, *meta, table, 1, x1, w->norm2_g, h, st));
+  H3_TRY(run_ffn_up(*cfg, S, h, w->w_fc1, w->b_fc1, qkv, st));
+  H3_TRY(run_resid_gemm(*cfg, *meta, table, 5, qkv, cfg->ffn_dim, w->w_fc2, w->b_fc2, x1, x_out, st));
+#undef H3_TRY
+  return H3_OK;
+}
+
+h3_status check_block_args(const h3_block_config* cfg, const h3_block_weights* w, const h3_packed_meta* meta,
+                           const void* x_in, void* x_out, void* ws, size_t ws_bytes) {
+  h3_status s;
+  if ((s = check_cfg(cfg)) != H3_OK) return s;
+  if ((s = check_meta(meta, true)) != H3_OK) return s;
+  if ((s = check_block_weights(w)) != H3_OK) return s;
+  if (!x_in || !x_out || !ws) return H3_ERR_NULL;
+  if (!al16(x_in) || !al16(x_out) || (reinterpret_cast<uintptr_t>(ws) & 255u)) return H3_ERR_ALIGN;
+  if (ws_bytes < ws_layout(*cfg, meta->n_rows, meta->n_timesteps).total) return H3_ERR_WORKSPACE;
+  return H3_OK;
+}
+
+}  // namespace
+
+// ===========================================================================
+// exported C ABI
+// ===========================================================================
+extern "C" {
+
+size_t h3_block_workspace_bytes(const h3_block_config* cfg, int32_t n_rows, int32_t n_timesteps) {
+  if (check_cfg(cfg) != H3_OK || n_rows < 1 || n_timesteps < 1 || n_timesteps > 16) return 0;
+  return ws_layout(*cfg, n_rows, n_timesteps).total;
+}
+
+h3_status h3_block_forward(const h3_block_config* cfg, const h3_block_weights* w, const h3_packed_meta* meta,
+                           const void* x_in, void* x_out, void* workspace, size_t ws_bytes,
+                           cudaStream_t stream) {
+  h3_status s = check_block_args(cfg, w, meta, x_in, x_out, workspace, ws_bytes);
+  if (s != H3_OK) return s;
+  return block_impl(cfg, w, meta, x_in, x_out, workspace, ws_bytes, stream, nullptr, 0);
+}
+
+h3_status h3_block_forward_profiled(const h3_block_config* cfg, const h3_block_weights* w,
+                                    const h3_packed_meta* meta, const void* x_in, void* x_out, void* workspace,
+                                    size_t ws_bytes, cudaStream_t stream, void* const* events,
+                                    int32_t n_events) {
+  h3_status s = check_block_args(cfg, w, meta, x_in, x_out, workspace, ws_bytes);
+  if (s != H3_OK) return s;
+  if (n_events < 0) return H3_ERR_SHAPE;
+  return block_impl(cfg, w, meta, x_in, x_out, workspace, ws_bytes, stream, events, n_events);
+}
+
+h3_status h3_blocks_forward(const h3_block_config* cfg, int32_t n_blocks, const h3_block_weights* w,
+                            const h3_packed_meta* meta, const void* x_in, void* x_out, void* workspace,
+                            size_t ws_bytes, cudaStream_t stream) {
+  if (!w) return H3_ERR_NULL;
+  if (n_blocks < 1) return H3_ERR_SHAPE;
+  for (int b = 0; b < n_blocks; ++b) {
+    h3_status s = check_block_args(cfg, &w[b], meta, x_in, x_out, workspace, ws_bytes);
+    if (s != H3_OK) return s;
+  }
+  for (int b = 0; b < n_blocks; ++b) {
+    h3_status s = block_impl(cfg, &w[b], meta, b == 0 ? x_in : x_out, x_out, workspace, ws_bytes, stream,
+                             nullptr, 0);
+    if (s != H3_OK) return s;
+  }
+  return H3_OK;
+}
+
+h3_status h3_adaln_table(const h3_block_config* cfg, const void* w_ada, const void* b_ada, const float* t_cond,
+                         int32_t n_timesteps, void* table_out, cudaStream_t stream) {
+  h3_status s = check_cfg(cfg);
+  if (s != H3_OK) return s;
+  if (!w_ada || !t_cond || !table_out) return H3_ERR_NULL;
+  if (n_timesteps < 1 || n_timesteps > 16) return H3_ERR_UNSUPPORTED;
+  if (!al16(w_ada) || !al16n(b_ada) || !al16(table_out) || (reinterpret_cast<uintptr_t>(t_cond) & 3u))
+    return H3_ERR_ALIGN;
+  return run_adaln_table(*cfg, w_ada, b_ada, t_cond, n_timesteps, table_out, stream);
+}
+
+h3_status h3_adaln_modulate(const h3_block_config* cfg, const h3_packed_meta* meta, const void* table,
+                            int32_t branch, const void* x, const void* norm_g, void* h_out, cudaStream_t stream) {
+  h3_status s = check_cfg(cfg);
+  if (s != H3_OK) return s;
+  if (!meta) return H3_ERR_NULL;
+  if (meta->n_rows < 1) return H3_ERR_SHAPE;
+  if (!meta->token_tag || !meta->timestep_index) return H3_ERR_NULL;
+  if (meta->n_timesteps < 1 || meta->n_timesteps > 16) return H3_ERR_UNSUPPORTED;
+  if (branch != 0 && branch != 1) return H3_ERR_SHAPE;
+  if (!table || !x || !norm_g || !h_out) return H3_ERR_NULL;
+  if (!al16(table) || !al16(x) || !al16(norm_g) || !al16(h_out)) return H3_ERR_ALIGN;
+  return run_modulate(*cfg, *meta, table, branch, x, norm_g, h_out, stream);
+}
+
+h3_status h3_qkv_projection(const h3_block_config* cfg, const h3_packed_meta* meta, const void* h,
+                            const void* w_qkv, const void* b_qkv, const void* q_norm_g, const void* k_norm_g,
+                            void* qkv_out, cudaStream_t stream) {
+  h3_status s = check_cfg(cfg);
+  if (s != H3_OK) return s;
+  if ((s = check_meta(meta, false)) != H3_OK) return s;
+  if (!h || !w_qkv || !q_norm_g || !k_norm_g || !qkv_out) return H3_ERR_NULL;
+  if (!al16(h) || !al16(w_qkv) || !al16n(b_qkv) || !al16(q_norm_g) || !al16(k_norm_g) || !al16(qkv_out))
+    return H3_ERR_ALIGN;
+  return run_qkv(*cfg, *meta, h, w_qkv, b_qkv, q_norm_g, k_norm_g, qkv_out, stream);
+}
+
+h3_status h3_rope_qknorm(const h3_block_config* cfg, int32_t n_rows, const int32_t* pos_thw, void* q, void* k,
+                         int64_t row_stride_elems, int64_t head_stride_elems, const void* q_norm_g,
+                         const void* k_norm_g, cudaStream_t stream) {
+  h3_status s = check_cfg(cfg);
+  if (s != H3_OK) return s;
+  if (n_rows < 1) return H3_ERR_SHAPE;
+  if (!pos_thw || !q || !k || !q_norm_g || !k_norm_g) return H3_ERR_NULL;
+  if (row_stride_elems < 128 || head_stride_elems < 128) return H3_ERR_SHAPE;
+  if ((row_stride_elems & 7) || (head_stride_elems & 7)) return H3_ERR_ALIGN;
+  if (!al16(q) || !al16(k) || !al16(q_norm_g) || !al16(k_norm_g)) return H3_ERR_ALIGN;
+  RopeArgs a{};
+  a.S = n_rows;
+  a.H = cfg->n_heads;
+  a.q = static_cast<__nv_bfloat16*>(q);
+  a.k = static_cast<__nv_bfloat16*>(k);
+  a.row_stride = row_stride_elems;
+  a.head_stride = head_stride_elems;
+  a.q_gain = static_cast<const __nv_bfloat16*>(q_norm_g);
+  a.k_gain = static_cast<const __nv_bfloat16*>(k_norm_g);
+  a.pos = pos_thw;
+  a.eps = cfg->eps;
+  fill_omega(a.omega, cfg->rope_theta);
+  a.err = device_error_word();
+  return cuda_st(launch_rope_qknorm(a, stream));
+}
+
+h3_status h3_attention(int32_t n_rows, int32_t n_heads, const void* q, const void* k, const void* v,
+                       int64_t row_stride_elems, int64_t head_stride_elems, void* o, float* lse_opt,
+                       cudaStream_t stream) {
+  if (n_rows < 1 || n_heads < 1 || n_heads > 65535) return H3_ERR_SHAPE;
+  if (!q || !k || !v || !o) return H3_ERR_NULL;
+  if (row_stride_elems < 128 || head_stride_elems < 128) return H3_ERR_SHAPE;
+  if ((row_stride_elems & 7) || (head_stride_elems & 7)) return H3_ERR_ALIGN;
+  if (!al16(q) || !al16(k) || !al16(v) || !al16(o) || (reinterpret_cast<uintptr_t>(lse_opt) & 3u))
+    return H3_ERR_ALIGN;
+  return run_attention(n_rows, n_heads, q, k, v, row_stride_elems, head_stride_elems, o, lse_opt, stream);
+}
+
+h3_status h3_out_projection(const h3_block_config* cfg, const h3_packed_meta* meta, const void* table,
+                            const void* o, const void* w_o, const void* b_o, const void* x, void* x_out,
+                            cudaStream_t stream) {
+  h3_status s = check_cfg(cfg);
+  if (s != H3_OK) return s;
+  if (!meta) return H3_ERR_NULL;
+  if (meta->n_rows < 1) return H3_ERR_SHAPE;
+  if (!meta->token_tag || !meta->timestep_index) return H3_ERR_NULL;
+  if (meta->n_timesteps < 1 || meta->n_timesteps > 16) return H3_ERR_UNSUPPORTED;
+  if (!table || !o || !w_o || !x || !x_out) return H3_ERR_NULL;
+  if (!al16(table) || !al16(o) || !al16(w_o) || !al16n(b_o) || !al16(x) || !al16(x_out)) return H3_ERR_ALIGN;
+  return run_resid_gemm(*cfg, *meta, table, 2, o, cfg->n_heads * 128, w_o, b_o, x, x_out, stream);
+}
+
+h3_status h3_ffn_up_swiglu(const h3_block_config* cfg, int32_t n_rows, const void* h, const void* w_fc1,
+                           const void* b_fc1, void* a_out, cudaStream_t stream) {
+  h3_status s = check_cfg(cfg);
+  if (s != H3_OK) return s;
+  if (n_rows < 1) return H3_ERR_SHAPE;
+  if (!h || !w_fc1 || !a_out) return H3_ERR_NULL;
+  if (!al16(h) || !al16(w_fc1) || !al16n(b_fc1) || !al16(a_out)) return H3_ERR_ALIGN;
+  return run_ffn_up(*cfg, n_rows, h, w_fc1, b_fc1, a_out, stream);
+}
+
+h3_status h3_ffn_down_residual(const h3_block_config* cfg, const h3_packed_meta* meta, const void* table,
+                               const void* a, const void* w_fc2, const void* b_fc2, const void* x1, void* y_out,
+                               cudaStream_t stream) {
+  h3_status s = check_cfg(cfg);
+  if (s != H3_OK) return s;
+  if (!meta) return H3_ERR_NULL;
+  if (meta->n_rows < 1) return H3_ERR_SHAPE;
+  if (!meta->token_tag || !meta->timestep_index) return H3_ERR_NULL;
+  if (meta->n_timesteps < 1 || meta->n_timesteps > 16) return H3_ERR_UNSUPPORTED;
+  if (!table || !a || !w_fc2 || !x1 || !y_out) return H3_ERR_NULL;
+  if (!al16(table) || !al16(a) || !al16(w_fc2) || !al16n(b_fc2) || !al16(x1) || !al16(y_out)) return H3_ERR_ALIGN;
+  return run_resid_gemm(*cfg, *meta, table, 5, a, cfg->ffn_dim, w_fc2, b_fc2, x1, y_out, stream);
+}
+
+h3_status h3_linear(int32_t M, int32_t N, int32_t K, const void* x, const void* w, const void* b, void* y,
+                    cudaStream_t stream) {
+  if (M < 1 || N < 1 || K < 64) return H3_ERR_SHAPE;
+  if (K % 64 || N % 8) return H3_ERR_UNSUPPORTED;
+  if (!x || !w || !y) return H3_ERR_NULL;
+  if (!al16(x) || !al16(w) || !al16n(b) || !al16(y)) return H3_ERR_ALIGN;
+  CUtensorMap tA, tB;
+  if (!make_tmap_2d(&tA, x, M, K, K, 128) || !make_tmap_2d(&tB, w, N, K, K, 128)) return H3_ERR_CUDA;
+  GemmArgs a{};
+  gemm_common(a, M, K, (N + 255) / 256);
+  a.out = static_cast<__nv_bfloat16*>(y);
+  a.ldo = N;
+  a.bias = static_cast<const __nv_bfloat16*>(b);
+  a.n_valid = N;
+  return cuda_st(launch_gemm(EPI_PLAIN, tA, tB, a, stream));
+}
+
+h3_status h3_sync_check(cudaStream_t stream, int32_t timeout_ms) {
+  cudaEvent_t ev;
+  if (cudaEventCreateWithFlags(&ev, cudaEventDisableTiming) != cudaSuccess) return H3_ERR_CUDA;
+  if (cudaEventRecord(ev, stream) != cudaSuccess) {
+    cudaEventDestroy(ev);
+    return H3_ERR_CUDA;
+  }
+  const auto t0 = std::chrono::steady_clock::now();
+  cudaError_t e;
+  while ((e = cudaEventQuery(ev)) == cudaErrorNotReady) {
+    const auto ms =
+        std::chrono::duration_cast<std::chrono::milliseconds>(std::chrono::steady_clock::now() - t0).count();
+    if (ms > timeout_ms) {
+      cudaEventDestroy(ev);
+      return H3_ERR_TIMEOUT;
+    }
+    std::this_thread::sleep_for(std::chrono::microseconds(50));
+  }
+  cudaEventDestroy(ev);
+  if (e != cudaSuccess) return H3_ERR_CUDA;
+  uint32_t* p = device_error_word();
+  if (!p) return H3_ERR_CUDA;
+  uint32_t bits = 0;
+  if (cudaMemcpy(&bits, p, sizeof(bits), cudaMemcpyDeviceToHost) != cudaSuccess) return H3_ERR_CUDA;
+  if (bits) {
+    if (cudaMemset(p, 0, sizeof(uint32_t)) != cudaSuccess) return H3_ERR_CUDA;
+    if (cudaDeviceSynchronize() != cudaSuccess) return H3_ERR_CUDA;
+  }
+  if (bits & DEVERR_TIMEOUT) return H3_ERR_TIMEOUT;
+  if (bits & DEVERR_INDEX) return H3_ERR_INDEX;
+  return H3_OK;
+}
+
+const char* h3_status_string(h3_status s) {
+  switch (s) {
+    case H3_OK: return "ok";
+    case H3_ERR_NULL: return "null pointer argument";
+    case H3_ERR_SHAPE: return "size out of range";
+    case H3_ERR_ALIGN: return "pointer or stride not 16-byte aligned";
+    case H3_ERR_UNSUPPORTED: return "unsupported configuration (fails closed)";
+    case H3_ERR_INDEX: return "device saw a bad tag, timestep index or position";
+    case H3_ERR_CUDA: return "CUDA runtime error";
+    case H3_ERR_TIMEOUT: return "device wait or stream synchronisation timed out";
+    case H3_ERR_WORKSPACE: return "workspace too small";
+  }
+  return "unknown status";
+}
+
+h3_status h3_last_kernel_info(char* buf, size_t len) {
+  if (!buf || len == 0) return H3_ERR_NULL;
+  snprintf(buf, len, "%s", g_info);
+  return H3_OK;
+}
+
+const char* h3_version(void) { return "libh3 0.1 sm_103a tcgen05"; }
+
+}  // extern "C"

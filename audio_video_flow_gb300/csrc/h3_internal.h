@@ -1,0 +1,125 @@
+// Host-side declarations shared by the translation units of libh3: kernel
+// argument blocks, launchers and the tensor-map helper.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace h3 {
+
+// ---------------------------------------------------------------------------
+// tensor maps (cuTensorMapEncodeTiled through the runtime's driver entry point)
+// ---------------------------------------------------------------------------
+// 2-D bf16 tensor [rows][cols] with row stride `ld` elements, box
+// [box_rows][64] (64 bf16 = 128 bytes), 128-byte swizzle, zero OOB fill.
+bool make_tmap_2d(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t cols, uint64_t ld,
+                  uint32_t box_rows);
+// 3-D bf16 tensor (channel c < 128, head h < H, row i < S) at
+// base + i*row_stride + h*head_stride + c, box (64, 1, box_rows).
+bool make_tmap_qkv(CUtensorMap* tm, const void* base, uint64_t n_rows, uint64_t n_heads,
+                   uint64_t row_stride, uint64_t head_stride, uint32_t box_rows);
+
+int num_sms();
+uint32_t* device_error_word();   // device address of the error word (current device)
+void set_kernel_info(const char* fmt, ...);
+
+// ---------------------------------------------------------------------------
+// GEMM (tcgen05, 128 x 256 x 64 tiles, persistent, warp-specialised)
+// ---------------------------------------------------------------------------
+enum GemmEpilogue : int {
+  EPI_PLAIN = 0,   // y = bf16(acc + b)
+  EPI_QKV = 1,     // per-head Q/K RMSNorm + MM-RoPE on q|k tiles, plain v tiles
+  EPI_RESID = 2,   // y = bf16(x + gate[r] * bf16(acc + b))
+  EPI_SWIGLU = 3,  // a = bf16(SiLU(bf16(acc_g + b_g)) * bf16(acc_u + b_u))
+};
+
+struct GemmArgs {
+  int M;                 // rows of the activation operand (packed rows S)
+  int K;                 // reduction length (multiple of 64)
+  int num_m, num_n, num_k;
+  __nv_bfloat16* out;    // output, row stride ldo elements
+  int ldo;
+  const __nv_bfloat16* bias;  // nullable; indexed by the weight row
+  int n_valid;           // PLAIN / RESID: number of output columns
+  // RESID: gate chunk of the AdaLN table and the residual input
+  const __nv_bfloat16* resid;
+  int ldr;
+  const __nv_bfloat16* table;  // [3T][6][D]
+  int D, chunk, T;
+  const int32_t* tag;
+  const int32_t* tidx;
+  // SWIGLU
+  int F;
+  // QKV
+  int H;
+  const __nv_bfloat16* q_gain;
+  const __nv_bfloat16* k_gain;
+  const int32_t* pos;
+  float eps;
+  float omega[16];
+  uint32_t* err;
+};
+
+cudaError_t launch_gemm(int epi, const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
+                        cudaStream_t stream);
+
+// AdaLN table: SiLU prologue + skinny tcgen05 GEMM with the weights as the M
+// operand (128 x 16 tiles), output transposed to [T][18D].
+struct AdalnArgs {
+  int C;                  // cond width (multiple of 64, <= 2816)
+  int T;                  // timestep rows (1..16)
+  int NW;                 // 18*D output channels (multiple of 128)
+  const float* t_cond;    // [T][C]
+  const __nv_bfloat16* bias;  // [NW] nullable
+  __nv_bfloat16* out;     // [T][NW]
+  uint32_t* err;
+};
+cudaError_t launch_adaln_table(const CUtensorMap& tmW, const AdalnArgs& a, cudaStream_t stream);
+
+// ---------------------------------------------------------------------------
+// attention (tcgen05 flash attention, one 128-row query tile per CTA)
+// ---------------------------------------------------------------------------
+struct AttnArgs {
+  int S, H;
+  __nv_bfloat16* o;       // [S][H*128]
+  float* lse;             // [H][S] or null
+  float scale_log2;       // log2(e) / sqrt(128)
+  uint32_t* err;
+};
+cudaError_t launch_attention(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                             const AttnArgs& a, cudaStream_t stream);
+
+// ---------------------------------------------------------------------------
+// row-wise kernels
+// ---------------------------------------------------------------------------
+struct ModulateArgs {
+  int S, D, T;
+  const __nv_bfloat16* x;
+  const __nv_bfloat16* gain;
+  const __nv_bfloat16* table;  // [3T][6][D]
+  int chunk_shift, chunk_scale;
+  const int32_t* tag;
+  const int32_t* tidx;
+  float eps;
+  __nv_bfloat16* h;
+  uint32_t* err;
+};
+cudaError_t launch_modulate(const ModulateArgs& a, cudaStream_t stream);
+
+struct RopeArgs {
+  int S, H;
+  __nv_bfloat16* q;
+  __nv_bfloat16* k;
+  int64_t row_stride, head_stride;
+  const __nv_bfloat16* q_gain;
+  const __nv_bfloat16* k_gain;
+  const int32_t* pos;
+  float eps;
+  float omega[16];
+  uint32_t* err;
+};
+cudaError_t launch_rope_qknorm(const RopeArgs& a, cudaStream_t stream);
+
+}  // namespace h3

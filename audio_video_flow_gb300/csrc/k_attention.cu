@@ -1,0 +1,311 @@
+// Full non-causal attention over one packed document (RFC section 4: every row
+// attends to every row, no mask), 128-wide heads, fp32 online softmax, on the
+// 5th-generation tensor cores.
+//
+// One CTA computes one 128-row query tile of one head:
+//   warp 0      TMA producer: Q once, then K_j and V_j tiles (128 rows x 128
+//               channels, two 64-channel 128-byte-swizzled boxes each) into a
+//               2-deep ring per operand;
+//   warp 1      MMA issuer (one thread): S_j = Q K_j^T into one of two TMEM
+//               score buffers, and O += P_j V_j into the TMEM output
+//               accumulator (V is read MN-major straight from its TMA tile);
+//   warps 4-7   softmax, one query row per thread: tcgen05.ld of the score
+//               row, running max and sum in fp32 (base-2 exponent with the
+//               1/sqrt(128) scale folded in), P_j as bf16 into shared memory
+//               in the tensor core's K-major layout, and the O rescale in TMEM
+//               when the running max grows.
+// S_{j+1} is computed while the softmax of tile j runs.  Keys past the end of
+// the sequence (zero-filled by TMA) get probability 0; query rows past the end
+// are computed and not stored.  Every sum runs in a fixed order, so the result
+// does not depend on the grid or on other rows.
+#include "h3_device.cuh"
+#include "h3_internal.h"
+
+#include <cmath>
+
+namespace h3 {
+
+namespace {
+constexpr int AT_THREADS = 256;
+constexpr int KV_TILE = 128;
+constexpr int KST = 2, VST = 2;
+constexpr int TILE_BYTES = 128 * 128 * 2;   // 32 KB: two 16 KB boxes
+constexpr int BOX_BYTES = 128 * 64 * 2;     // 16 KB
+constexpr int AT_SMEM = 1024 + TILE_BYTES * (1 + KST + VST + 1) + 512;
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  const uint32_t s = smem_u32(p);
+  return p + (((s + 1023u) & ~1023u) - s);
+}
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer() - t0 > kWaitLimitNs) return;
+  }
+}
+}  // namespace
+
+__global__ void __launch_bounds__(AT_THREADS, 1)
+    attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, const AttnArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint8_t* sQ = smem;
+  uint8_t* sK = sQ + TILE_BYTES;
+  uint8_t* sV = sK + KST * TILE_BYTES;
+  uint8_t* sP = sV + VST * TILE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + TILE_BYTES);
+  uint64_t* q_full = bars;
+  uint64_t* k_full = bars + 1;
+  uint64_t* k_empty = k_full + KST;
+  uint64_t* v_full = k_empty + KST;
+  uint64_t* v_empty = v_full + VST;
+  uint64_t* s_full = v_empty + VST;
+  uint64_t* s_empty = s_full + 2;
+  uint64_t* p_full = s_empty + 2;
+  uint64_t* o_done = p_full + 1;
+  uint64_t* drain = o_done + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int q_tile = blockIdx.x, head = blockIdx.y;
+  const int S = args.S;
+  const int n_kv = (S + KV_TILE - 1) / KV_TILE;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < KST; ++s) { mbar_init(&k_full[s], 1); mbar_init(&k_empty[s], 1); }
+    for (int s = 0; s < VST; ++s) { mbar_init(&v_full[s], 1); mbar_init(&v_empty[s], 1); }
+    for (int b = 0; b < 2; ++b) { mbar_init(&s_full[b], 1); mbar_init(&s_empty[b], 4); }
+    mbar_init(p_full, 4);
+    mbar_init(o_done, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;   // S0: cols [0,128), S1: [128,256), O: [256,384)
+  volatile int* abort_v = abort_flag;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      bool ok = true;
+      int issued_k = 0, issued_v = 0;
+      mbar_arrive_expect_tx(q_full, TILE_BYTES);
+      tma_load_3d(sQ, &tmQ, q_full, 0, head, q_tile * 128);
+      tma_load_3d(sQ + BOX_BYTES, &tmQ, q_full, 64, head, q_tile * 128);
+      for (int j = 0; j < n_kv && ok; ++j) {
+        const int ks = j % KST;
+        const uint32_t kph = (uint32_t)(j / KST) & 1u;
+        if (!mbar_wait(&k_empty[ks], kph ^ 1u, abort_v)) { ok = false; break; }
+        mbar_arrive_expect_tx(&k_full[ks], TILE_BYTES);
+        tma_load_3d(sK + ks * TILE_BYTES, &tmK, &k_full[ks], 0, head, j * KV_TILE);
+        tma_load_3d(sK + ks * TILE_BYTES + BOX_BYTES, &tmK, &k_full[ks], 64, head, j * KV_TILE);
+        ++issued_k;
+        const int vs = j % VST;
+        const uint32_t vph = (uint32_t)(j / VST) & 1u;
+        if (!mbar_wait(&v_empty[vs], vph ^ 1u, abort_v)) { ok = false; break; }
+        mbar_arrive_expect_tx(&v_full[vs], TILE_BYTES);
+        tma_load_3d(sV + vs * TILE_BYTES, &tmV, &v_full[vs], 0, head, j * KV_TILE);
+        tma_load_3d(sV + vs * TILE_BYTES + BOX_BYTES, &tmV, &v_full[vs], 64, head, j * KV_TILE);
+        ++issued_v;
+      }
+      if (!ok) {  // let issued loads land before the CTA exits
+        drain_wait(q_full, 0);
+        for (int j = (issued_k > KST ? issued_k - KST : 0); j < issued_k; ++j)
+          drain_wait(&k_full[j % KST], (uint32_t)(j / KST) & 1u);
+        for (int j = (issued_v > VST ? issued_v - VST : 0); j < issued_v; ++j)
+          drain_wait(&v_full[j % VST], (uint32_t)(j / VST) & 1u);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t idesc_o = idesc_bf16(128, 128, false, true);   // V is MN-major
+      const uint32_t q0 = smem_u32(sQ), k0 = smem_u32(sK), v0 = smem_u32(sV), p0 = smem_u32(sP);
+      const uint32_t o_tmem = tmem_base + 256u;
+      bool ok = mbar_wait(q_full, 0, abort_v);
+      auto issue_s = [&](int j) -> bool {
+        const int ks = j % KST;
+        if (!mbar_wait(&k_full[ks], (uint32_t)(j / KST) & 1u, abort_v)) return false;
+        const int b = j & 1;
+        if (!mbar_wait(&s_empty[b], ((uint32_t)(j >> 1) & 1u) ^ 1u, abort_v)) return false;
+        tc_fence_after();
+        const uint32_t kb = k0 + (uint32_t)(ks * TILE_BYTES);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t off = (uint32_t)((k >> 2) * BOX_BYTES + (k & 3) * 32);
+          mma_bf16_ss(tmem_base + (uint32_t)(b * 128), sdesc_kmajor(q0 + off), sdesc_kmajor(kb + off), idesc_s,
+                      k != 0 ? 1u : 0u);
+        }
+        mma_commit(&s_full[b]);
+        mma_commit(&k_empty[ks]);
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      for (int j = 0; j < n_kv && ok; ++j) {
+        if (j + 1 < n_kv && !issue_s(j + 1)) { ok = false; break; }
+        if (!mbar_wait(p_full, (uint32_t)j & 1u, abort_v)) { ok = false; break; }
+        const int vs = j % VST;
+        if (!mbar_wait(&v_full[vs], (uint32_t)(j / VST) & 1u, abort_v)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t vb = v0 + (uint32_t)(vs * TILE_BYTES);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint64_t a_desc = sdesc_kmajor(p0 + (uint32_t)((k >> 2) * BOX_BYTES + (k & 3) * 32));
+          // V tile: 128 key rows x 128 B per 64-channel box; 16 keys = 2048 B;
+          // next 64 channels one box (16 KB) further: LBO = 16 KB, SBO = 1 KB.
+          const uint64_t b_desc = sdesc_sw128(vb + (uint32_t)(k * 2048), BOX_BYTES, 1024);
+          mma_bf16_ss(o_tmem, a_desc, b_desc, idesc_o, (j | k) != 0 ? 1u : 0u);
+        }
+        mma_commit(o_done);
+        mma_commit(&v_empty[vs]);
+      }
+      if (!ok) {
+        mma_commit(drain);
+        drain_wait(drain, 0);
+      }
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax
+    const int qq = warp & 3;
+    const int row = qq * 32 + lane;
+    const int grow = q_tile * 128 + row;
+    const uint32_t lane_base = tmem_addr(tmem_base, (uint32_t)(qq * 32), 0);
+    const float sl2 = args.scale_log2;
+    float m_run = -INFINITY, l_run = 0.0f;
+    bool ok = true;
+    for (int j = 0; j < n_kv; ++j) {
+      const int b = j & 1;
+      if (!mbar_wait(&s_full[b], (uint32_t)(j >> 1) & 1u, abort_v)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t s0[32], s1[32], s2[32], s3[32];
+      tmem_ld32(lane_base + (uint32_t)(b * 128 + 0), s0);
+      tmem_ld32(lane_base + (uint32_t)(b * 128 + 32), s1);
+      tmem_ld32(lane_base + (uint32_t)(b * 128 + 64), s2);
+      tmem_ld32(lane_base + (uint32_t)(b * 128 + 96), s3);
+      tmem_ld_wait(s0);
+      tmem_ld_wait(s1);
+      tmem_ld_wait(s2);
+      tmem_ld_wait(s3);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_empty[b]);
+      float sc[128];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        sc[c] = __uint_as_float(s0[c]);
+        sc[32 + c] = __uint_as_float(s1[c]);
+        sc[64 + c] = __uint_as_float(s2[c]);
+        sc[96 + c] = __uint_as_float(s3[c]);
+      }
+      if (j == n_kv - 1) {
+        const int valid = S - j * KV_TILE;
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (c >= valid) sc[c] = -INFINITY;
+      }
+      float mx = sc[0];
+#pragma unroll
+      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, sc[c]);
+      const float m_new = fmaxf(m_run, mx * sl2);
+      uint32_t pk[64];
+      float rs = 0.0f;
+#pragma unroll
+      for (int c = 0; c < 128; c += 2) {
+        const float e0 = exp2f(__fmaf_rn(sc[c], sl2, -m_new));
+        const float e1 = exp2f(__fmaf_rn(sc[c + 1], sl2, -m_new));
+        rs += e0;
+        rs += e1;
+        pk[c >> 1] = pack_bf16x2(e0, e1);
+      }
+      const float alpha = exp2f(m_run - m_new);
+      l_run = __fmaf_rn(l_run, alpha, rs);
+      if (j > 0) {
+        if (!mbar_wait(o_done, (uint32_t)(j - 1) & 1u, abort_v)) { ok = false; break; }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, m_new > m_run)) {
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            uint32_t o[32];
+            const uint32_t ta = lane_base + 256u + (uint32_t)(c * 32);
+            tmem_ld32(ta, o);
+            tmem_ld_wait(o);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st32(ta, o);
+          }
+          tmem_st_wait();
+        }
+      }
+      // P_j (bf16) into the K-major 128-byte-swizzled operand tile
+#pragma unroll
+      for (int cc = 0; cc < 16; ++cc) {
+        const uint32_t off = (uint32_t)((cc >> 3) * BOX_BYTES) + sw128_offset((uint32_t)row, (uint32_t)(cc & 7));
+        *reinterpret_cast<uint4*>(sP + off) = make_uint4(pk[cc * 4], pk[cc * 4 + 1], pk[cc * 4 + 2], pk[cc * 4 + 3]);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full);
+      m_run = m_new;
+    }
+    if (ok && mbar_wait(o_done, (uint32_t)(n_kv - 1) & 1u, abort_v)) {
+      tc_fence_after();
+      const float inv_l = 1.0f / l_run;
+      const int HD = args.H * 128;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t o[32];
+        tmem_ld32(lane_base + 256u + (uint32_t)(c * 32), o);
+        tmem_ld_wait(o);
+        if (grow < S) {
+          uint4* dst = reinterpret_cast<uint4*>(args.o + (size_t)grow * HD + head * 128 + c * 32);
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            dst[g] = make_uint4(pack_bf16x2(__uint_as_float(o[g * 8 + 0]) * inv_l, __uint_as_float(o[g * 8 + 1]) * inv_l),
+                                pack_bf16x2(__uint_as_float(o[g * 8 + 2]) * inv_l, __uint_as_float(o[g * 8 + 3]) * inv_l),
+                                pack_bf16x2(__uint_as_float(o[g * 8 + 4]) * inv_l, __uint_as_float(o[g * 8 + 5]) * inv_l),
+                                pack_bf16x2(__uint_as_float(o[g * 8 + 6]) * inv_l, __uint_as_float(o[g * 8 + 7]) * inv_l));
+          }
+        }
+      }
+      if (args.lse != nullptr && grow < S)
+        args.lse[(size_t)head * S + grow] = (m_run + log2f(l_run)) * 0.69314718055994530942f;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0 && *abort_v) record_error(args.err, DEVERR_TIMEOUT);
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 512);
+  }
+}
+
+cudaError_t launch_attention(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                             const AttnArgs& a, cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, AT_SMEM);
+  if (e != cudaSuccess) return e;
+  const dim3 grid((unsigned)((a.S + 127) / 128), (unsigned)a.H);
+  attention_kernel<<<grid, AT_THREADS, AT_SMEM, stream>>>(tmQ, tmK, tmV, a);
+  set_kernel_info("attention_kernel tcgen05.mma.cta_group::1.kind::f16 q_tile=128 kv_tile=128 k_stages=%d "
+                  "v_stages=%d acc=f32 tmem=S0,S1,O softmax=fp32-online grid=%ux%u",
+                  KST, VST, grid.x, grid.y);
+  return cudaGetLastError();
+}
+
+}  // namespace h3

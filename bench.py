@@ -1,0 +1,471 @@
+"""Benchmark of the H3 block forward on GB300.
+
+One step = one pass of the whole hot path over one packed document: the AdaLN
+table, norm1/modulate, QKV + QK-norm + MM-RoPE, attention, O projection +
+gated residual, norm2/modulate, FC1 + SwiGLU, FC2 + gated residual (and, for
+the 50-block denoiser workload, all 50 blocks).  Default workload: one
+full-width block over 505 packed rows (17 text + 360 video + 128 audio, 12
+timestep rows).
+
+Prints ONE JSON line (rank 0).  `value` is whole-job TFLOP/s of algorithmic
+work (dense GEMMs, full attention, AdaLN projection) measured with CUDA events
+on the launching stream, max over ranks; `e2e` is the same metric with the
+inputs copied host->device and the output device->host inside the timed
+region.  `--impl reference` times the CPU oracle on the host cores instead.
+Multi-GPU (torchrun): every rank runs an independent replica (the batch axis
+is pure replication), so scaling is weak and no data-path collective exists.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "H3 block fwd TFLOP/s & packed tokens/s (bf16, 1 GB300); % of tensor/HBM roofline"
+STAGES = ("adaln_table", "norm1_modulate", "qkv_qknorm_rope", "attention", "out_proj_residual",
+          "norm2_modulate", "fc1_swiglu", "fc2_residual")
+# dram__bytes_read.sum + dram__bytes_write.sum per launch from an ncu capture
+# of the current kernel build, keyed "stage@workload"; None when not captured.
+TRAFFIC = {}
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work
+# ---------------------------------------------------------------------------
+
+def stage_work(shape, S: int, T: int):
+    """(flops, bytes) per stage of one block: the method's own dense work and
+    the bytes each kernel must move at least once."""
+    D, I, F, C = shape.dim, shape.n_heads * shape.head_dim, shape.ffn_dim, shape.cond_dim
+    b = 2  # bf16
+    return {
+        "adaln_table": (2.0 * T * C * 18 * D, 18 * D * C * b + T * C * 4 + T * 18 * D * b),
+        "norm1_modulate": (0.0, 2.0 * S * D * b),
+        "qkv_qknorm_rope": (2.0 * S * D * 3 * I, 3 * I * D * b + S * D * b + S * 3 * I * b),
+        "attention": (4.0 * S * S * I, 4.0 * S * I * b),
+        "out_proj_residual": (2.0 * S * I * D, D * I * b + S * I * b + 2 * S * D * b),
+        "norm2_modulate": (0.0, 2.0 * S * D * b),
+        "fc1_swiglu": (2.0 * S * D * 2 * F, 2 * F * D * b + S * D * b + S * F * b),
+        "fc2_residual": (2.0 * S * F * D, D * F * b + S * F * b + 2 * S * D * b),
+    }
+
+
+def weight_bytes(shape):
+    D, I, F, C = shape.dim, shape.n_heads * shape.head_dim, shape.ffn_dim, shape.cond_dim
+    return 2 * (18 * D * C + 3 * I * D + D * I + 2 * F * D + D * F)
+
+
+BOUND = {"adaln_table": "hbm", "norm1_modulate": "hbm", "norm2_modulate": "hbm", "qkv_qknorm_rope": "tensor",
+         "attention": "tensor", "out_proj_residual": "tensor", "fc1_swiglu": "tensor", "fc2_residual": "tensor"}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ---------------------------------------------------------------------------
+# ranks (replicas): timing aggregation is the only cross-rank step
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def aggregate(elapsed_ms: float, units: float, world_size: int):
+    """Max elapsed time and summed work over ranks (host-side timing reduction)."""
+    if world_size <= 1:
+        return elapsed_ms, units
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
+    u = torch.tensor([units], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def barrier(world_size: int):
+    if world_size > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.25)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args, ws_n: int, rank: int, local: int):
+    import torch
+    import audio_video_flow_gb300 as h3
+    import h3_inputs as hi
+
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    wl = hi.WORKLOADS[args.workload]
+    shape, S, T, NB = wl.shape, wl.layout.n_rows, wl.n_timesteps, wl.n_blocks
+    cfg = h3.make_config(shape.dim, shape.n_heads, shape.ffn_dim, shape.cond_dim)
+    meta_c, acts_c, _ = hi.workload_inputs(wl, seed=args.seed, device="cpu", block=0) if NB == 1 else \
+        (hi.packed_metadata(wl.layout, T, args.seed), hi.activations(shape, S, T, args.seed), None)
+    if NB == 1:
+        wts = [hi.block_weights(shape, args.seed, 0, device=dev)]
+    else:   # 50 blocks: generated on the device (about 1.3 GB each)
+        wts = [hi.block_weights(shape, args.seed, b, device=dev) for b in range(NB)]
+    cw = [h3.make_weights(w) for w in wts]
+    meta_d = {k: v.to(dev) for k, v in meta_c.items()}
+    x = acts_c["x"].to(dev)
+    tc = acts_c["t_cond"].to(dev)
+    y = torch.empty_like(x)
+    meta = h3.make_meta(meta_d["token_tag"], meta_d["timestep_index"], meta_d["pos_thw"], tc, T)
+    wsp = torch.empty(h3.h3_block_workspace_bytes(cfg, S, T), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    # one set of stage events per timed step and block: the per-kernel launch
+    # durations are read from the timed region itself
+    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(len(STAGES) + 1)] for _ in range(NB)]
+          for _ in range(args.steps)]
+
+    def step(i=None):
+        for b in range(NB):
+            xin = x if b == 0 else y
+            if i is not None:
+                ev[i][b][0].record(stream)
+                h3.h3_block_forward_profiled(cfg, cw[b], meta, xin, y, wsp, ev[i][b][1:])
+            else:
+                h3.h3_block_forward(cfg, cw[b], meta, xin, y, wsp)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if h3.h3_sync_check(timeout_ms=60000) != 0:
+        raise RuntimeError("device error during warm-up")
+
+    work = stage_work(shape, S, T)
+    flops_step = NB * sum(f for f, _ in work.values())
+
+    # ---- timed region (device time on the launching stream)
+    with ClockSampler(local) as clk:
+        barrier(ws_n)
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        host0 = time.perf_counter()
+        for i in range(args.steps):
+            step(i)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        host1 = time.perf_counter()
+        barrier(ws_n)
+    elapsed_ms = t0.elapsed_time(t1)
+    status = h3.h3_sync_check(timeout_ms=60000)
+    if status != 0:
+        raise RuntimeError(f"device error in the timed region: {h3.status_string(status)}")
+    stage_ms = {}
+    for k, s in enumerate(STAGES):
+        stage_ms[s] = statistics.mean(ev[i][b][k].elapsed_time(ev[i][b][k + 1])
+                                      for i in range(args.steps) for b in range(NB))
+
+    elapsed_ms, units = aggregate(elapsed_ms, float(args.steps) * flops_step, ws_n)
+    ms_per_step = elapsed_ms / args.steps
+    tflops = units / (elapsed_ms * 1e-3) / 1e12
+    tokens_per_s = ws_n * S * args.steps / (elapsed_ms * 1e-3)
+
+    # ---- end to end: pinned host inputs -> device, block(s), output -> host
+    e2e = None
+    if not args.no_e2e:
+        h_x = acts_c["x"].pin_memory()
+        h_meta = {k: v.pin_memory() for k, v in meta_c.items()}
+        h_tc = acts_c["t_cond"].pin_memory()
+        h_y = torch.empty_like(acts_c["x"]).pin_memory()
+        bi = h_x.numel() * 2 + h_tc.numel() * 4 + sum(v.numel() * 4 for v in h_meta.values())
+        bo = h_y.numel() * 2
+        n_e2e = max(3, min(args.steps, 200))
+
+        def e2e_step():
+            x.copy_(h_x, non_blocking=True)
+            tc.copy_(h_tc, non_blocking=True)
+            for k in h_meta:
+                meta_d[k].copy_(h_meta[k], non_blocking=True)
+            step()
+            h_y.copy_(y, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        barrier(ws_n)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(ws_n)
+        e_ms, e_units = aggregate(e0.elapsed_time(e1), float(n_e2e) * flops_step, ws_n)
+        e2e = {"value": round(e_units / (e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+               "h2d_bytes_per_step": int(bi), "d2h_bytes_per_step": int(bo),
+               "ms_per_step": round(e_ms / n_e2e, 4), "steps": n_e2e}
+
+    # ---- roofline of the dominant kernel
+    peaks = load_peaks()
+    dom = max(STAGES, key=lambda s: stage_ms[s])
+    fl, by = work[dom]
+    d_ms = stage_ms[dom]
+    if BOUND[dom] == "tensor":
+        achieved, peak, unit = fl / (d_ms * 1e-3) / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+    else:
+        achieved, peak, unit = by / (d_ms * 1e-3) / 1e9, peaks["hbm_gbs"], "GB/s"
+    stages_out = {}
+    for s in STAGES:
+        f, bts = work[s]
+        ms = stage_ms[s]
+        stages_out[s] = {"us": round(ms * 1e3, 2), "share": round(ms / sum(stage_ms.values()), 4),
+                         "tflops": round(f / (ms * 1e-3) / 1e12, 1) if f else None,
+                         "gbs": round(bts / (ms * 1e-3) / 1e9, 1)}
+    clocks = clk.summary()
+    line = {
+        "metric": METRIC, "value": round(tflops, 3), "unit": "TFLOP/s", "n_gpus": ws_n, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "tokens_per_s": round(tokens_per_s, 1),
+        "config": {"workload": wl.name, "description": wl.description, "rows": S, "timestep_rows": T,
+                   "blocks": NB, "dim": shape.dim, "heads": shape.n_heads, "ffn": shape.ffn_dim,
+                   "cond": shape.cond_dim, "flop_per_step": flops_step,
+                   "l2": "inputs larger than L2: %.2f GB of block weights re-read every step" %
+                         (NB * weight_bytes(shape) / 1e9),
+                   "parallelism": f"replicas x{ws_n}"},
+        "e2e": e2e,
+        "gpu_launches": args.steps * NB * len(STAGES),
+        "roofline": {"kernel": dom, "bound": BOUND[dom], "achieved": round(achieved, 1), "peak": peak,
+                     "unit": unit, "frac": round(achieved / peak, 4),
+                     "peak_source": peaks["source"] + (" bf16 burst" if BOUND[dom] == "tensor" else " hbm copy"),
+                     "traffic": TRAFFIC.get(f"{dom}@{wl.name}")},
+        "stages": stages_out,
+        "clocks": clocks,
+        "host_ms_per_step": round((host1 - host0) * 1e3 / args.steps, 4),
+    }
+    if rank == 0 and not args.no_cpu_baseline and ws_n == 1:
+        line["cpu_baseline"] = cpu_baseline(wl, args.seed, args.cpu_seconds)
+    return line
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (the reference arm and the cpu_baseline leg)
+# ---------------------------------------------------------------------------
+
+class OracleRowStepper:
+    """Times the CPU oracle one packed row at a time.  Before timing: the AdaLN
+    table and every row's q/k/v (the keys and values all rows attend to).
+    Each step then evaluates one row's share of the block: its QKV projection
+    and QK-norm/RoPE, its attention over all keys, the O projection and
+    residual, norm2, FC1/SwiGLU and FC2/residual."""
+
+    def __init__(self, wl, seed):
+        import numpy as np
+        import torch
+        import h3_inputs as hi
+        from oracle import h3_oracle as O
+        if wl.n_blocks != 1 or wl.layout.n_rows > 4096:
+            raise ValueError("the oracle row sampler covers single-block workloads up to 4096 rows")
+        self.O, self.np = O, np
+        meta, acts, wts = hi.workload_inputs(wl, seed=seed)
+        f64 = lambda t: t.to(torch.float64).numpy()
+        self.w = {k: (f64(v) if v is not None else None) for k, v in wts.items()}
+        self.x = f64(acts["x"])
+        self.tag, self.tidx, self.pos = (meta[k].numpy() for k in ("token_tag", "timestep_index", "pos_thw"))
+        tc = acts["t_cond"].numpy().astype(np.float64)
+        self.table = O.adaln_table(tc, self.w["w_ada"], self.w["b_ada"], wl.shape.dim)
+        self.mod = self.table[O.adaln_rows(self.tag, self.tidx)]
+        h1 = O.rmsnorm_modulate(self.x, self.w["norm1_g"], self.mod[:, 0], self.mod[:, 1])
+        qkv = O.linear(h1, self.w["w_qkv"]).reshape(wl.layout.n_rows, wl.shape.n_heads, 3, 128)
+        _, self.k, self.v = O.qk_norm_rope(qkv, self.pos, self.w["q_norm_g"], self.w["k_norm_g"])
+        self.S, self.shape = wl.layout.n_rows, wl.shape
+        self.row_flops = sum(f for f, _ in stage_work(wl.shape, wl.layout.n_rows, wl.n_timesteps).values()) \
+            / wl.layout.n_rows
+        self.i = 0
+
+    def step(self):
+        O, np = self.O, self.np
+        i = self.i % self.S
+        self.i += 1
+        r = slice(i, i + 1)
+        mod = self.mod[r]
+        h1 = O.rmsnorm_modulate(self.x[r], self.w["norm1_g"], mod[:, 0], mod[:, 1])
+        qkv = O.linear(h1, self.w["w_qkv"]).reshape(1, self.shape.n_heads, 3, 128)
+        q, _, _ = O.qk_norm_rope(qkv, self.pos[r], self.w["q_norm_g"], self.w["k_norm_g"])
+        o = np.empty((1, self.shape.n_heads * 128))
+        for h in range(self.shape.n_heads):
+            o[:, h * 128:(h + 1) * 128] = O.attention_head(q[:, h], self.k[:, h], self.v[:, h])
+        o = O.bf16_round(o)
+        x1 = O.gated_residual(self.x[r], mod[:, 2], O.linear(o, self.w["w_o"]))
+        h2 = O.rmsnorm_modulate(x1, self.w["norm2_g"], mod[:, 3], mod[:, 4])
+        gu = O.linear(h2, self.w["w_fc1"])
+        F = gu.shape[1] // 2
+        return O.gated_residual(x1, mod[:, 5], O.linear(O.swiglu(gu[:, :F], gu[:, F:]), self.w["w_fc2"]))
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(wl, seed, seconds: float):
+    st = OracleRowStepper(wl, seed)
+    st.step()
+    n, t0 = 0, time.perf_counter()
+    while time.perf_counter() - t0 < seconds:
+        st.step()
+        n += 1
+    dt = time.perf_counter() - t0
+    tflops = n * st.row_flops / dt / 1e12
+    return {"value": round(tflops, 6), "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+            "tokens_per_s": round(n / dt, 2),
+            "sample": f"{n} packed rows of {wl.name}, one row's block work per step in fp64 numpy "
+                      f"(AdaLN table and all rows' K/V computed before timing), {dt:.1f} s"}
+
+
+def run_reference(args, ws_n: int, rank: int):
+    import h3_inputs as hi
+    wl = hi.WORKLOADS[args.workload]
+    if rank != 0:
+        return None
+    try:
+        st = OracleRowStepper(wl, args.seed)
+    except ValueError as e:
+        return {"impl": "reference", "unavailable": f"CPU oracle too slow for {wl.name}: {e}"}
+    for _ in range(args.warmup):
+        st.step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        st.step()
+    dt = time.perf_counter() - t0
+    flops_step = st.row_flops
+    value = args.steps * flops_step / dt / 1e12
+    return {"metric": METRIC, "impl": "reference", "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": ws_n,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / args.steps, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "tokens_per_s": round(args.steps / dt, 3),
+            "config": {"workload": wl.name, "rows": wl.layout.n_rows, "sample": "one packed row per step"},
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+                             "sample": "one packed row's block work per step (AdaLN table and all rows' K/V "
+                                       "computed before timing)"},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="block505")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    ws_n, rank, local = dist_env()
+    if args.impl == "reference":
+        line = run_reference(args, ws_n, rank)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return 0
+    if ws_n > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
+    line = run_ours(args, ws_n, rank, local)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws_n > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

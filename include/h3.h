@@ -1,0 +1,268 @@
+/*
+ * libh3 -- MiniMax-H3 Omni-Transformer block forward on one GB300 (sm_103a).
+ *
+ * The operations are defined by the RL-Kernel RFC "[MiniMax-H3][CUDA/ROCm]
+ * WS1/WS2 kernel roadmap, ablation matrix and integration plan" ("the RFC"):
+ * section 2 (Omni-Transformer and mixed-precision fingerprint tables),
+ * section 3 (figure 2, one H3 block), section 4 (the H3-specific arithmetic
+ * rules) and the work items of section 5.  The checkpoint layout of the QKV
+ * rows follows the "h3-metal" README, section "Checkpoint layout and media
+ * pipeline".
+ *
+ * Conventions shared by every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller.  The
+ *     library never allocates or frees device memory; where scratch space is
+ *     needed the caller passes a workspace sized by the matching *_bytes call.
+ *   - bf16 tensors are row-major, 16-byte aligned, with every row stride a
+ *     multiple of 16 bytes.  Weights are [out][in].
+ *   - Calls are stream-ordered and asynchronous.  Argument errors are returned
+ *     synchronously, before anything is launched, and nothing is launched
+ *     then.  Unsupported geometry fails closed (H3_ERR_UNSUPPORTED); there is
+ *     no fallback path.
+ *   - Bad metadata values found on the device (a tag outside {0,1,2}, a
+ *     timestep index outside [0,T), a position outside [0, 2^24)) do not
+ *     fault: the kernel records the error in a device error word, leaves the
+ *     row's output unwritten and carries on.  h3_sync_check reads and clears
+ *     that word.  A device-side wait that exceeds its time limit is recorded
+ *     the same way (H3_ERR_TIMEOUT).
+ *   - Results are deterministic: every reduction has a fixed order that does
+ *     not depend on the row count, the launch geometry or the SM count (RFC
+ *     section 4, numerical contract items 1-3).  There is no split-K.
+ */
+#ifndef H3_H_
+#define H3_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  H3_OK = 0,
+  H3_ERR_NULL = 1,         /* a required pointer is NULL */
+  H3_ERR_SHAPE = 2,        /* a size is out of range (e.g. n_rows < 1) */
+  H3_ERR_ALIGN = 3,        /* a pointer or stride breaks the 16-byte rule */
+  H3_ERR_UNSUPPORTED = 4,  /* a configuration this library does not implement */
+  H3_ERR_INDEX = 5,        /* the device saw a bad tag / timestep index / position */
+  H3_ERR_CUDA = 6,         /* a CUDA runtime call failed */
+  H3_ERR_TIMEOUT = 7,      /* a device-side wait or h3_sync_check timed out */
+  H3_ERR_WORKSPACE = 8     /* the workspace is smaller than required */
+} h3_status;
+
+/* Block widths (RFC s2, "Omni-Transformer fingerprint").  Supported:
+ * head_dim == 128, rope_freqs_per_axis == 16, rope_channels == 96,
+ * dim, cond_dim multiples of 64 (cond_dim <= 2816), ffn_dim a multiple of
+ * 128, n_heads in [1, 1024].  H3 itself: dim 5376, n_heads 56, ffn_dim 14336,
+ * cond_dim 2688, eps 1e-5, rope_theta 10000. */
+typedef struct {
+  int32_t dim;                  /* D, residual width */
+  int32_t n_heads;              /* H */
+  int32_t head_dim;             /* 128 */
+  int32_t ffn_dim;              /* F, SwiGLU hidden width */
+  int32_t cond_dim;             /* C, timestep embedding width into the AdaLN projection */
+  int32_t rope_freqs_per_axis;  /* 16 */
+  int32_t rope_channels;        /* 96 */
+  float eps;                    /* RMSNorm epsilon (block and Q/K norms) */
+  float rope_theta;             /* 10000 */
+} h3_block_config;
+
+/* One block's weights, all bf16 device pointers.  Biases may be NULL.
+ *   w_ada  [18*D][C], b_ada [18*D]: AdaLN projection.  Output channel
+ *          n = m*6*D + c*D + d is (modality m, chunk c, channel d), chunks
+ *          in the order shift_msa, scale_msa, gate_msa, shift_mlp, scale_mlp,
+ *          gate_mlp.
+ *   norm1_g, norm2_g [D]: block RMSNorm gains.
+ *   w_qkv  [H*3*128][D], b_qkv [H*3*128]: rows interleaved per head,
+ *          head h owning rows h*384 .. h*384+383 as q(128), k(128), v(128).
+ *   q_norm_g, k_norm_g [128]: per-head Q/K RMSNorm gains, shared by heads.
+ *   w_o    [D][H*128], b_o [D]
+ *   w_fc1  [2F][D], b_fc1 [2F]: rows 0..F-1 gate (SiLU'd), F..2F-1 value.
+ *   w_fc2  [D][F], b_fc2 [D]                                               */
+typedef struct {
+  const void *w_ada, *b_ada;
+  const void *norm1_g, *norm2_g;
+  const void *w_qkv, *b_qkv;
+  const void *q_norm_g, *k_norm_g;
+  const void *w_o, *b_o;
+  const void *w_fc1, *b_fc1;
+  const void *w_fc2, *b_fc2;
+} h3_block_weights;
+
+/* Packed-row metadata of one document (RFC s3: the row identity tuple; s4:
+ * the index tensors, tags and positions carry meaning and are inputs of the
+ * arithmetic, not incidental metadata).  Device pointers:
+ *   token_tag [S] int32 in {0 video, 1 text, 2 audio}
+ *   timestep_index [S] int32 in [0, T)
+ *   pos_thw [S][3] int32 (t, h, w) in [0, 2^24)
+ *   t_cond [T][C] fp32, the timestep embedding before the AdaLN SiLU.       */
+typedef struct {
+  int32_t n_rows;        /* S >= 1 */
+  int32_t n_timesteps;   /* T in [1, 16] */
+  const int32_t *token_tag;
+  const int32_t *timestep_index;
+  const int32_t *pos_thw;
+  const float *t_cond;
+} h3_packed_meta;
+
+/* ----------------------------------------------------------------------- */
+/* The block                                                                */
+/* ----------------------------------------------------------------------- */
+
+/* Bytes of workspace h3_block_forward / h3_blocks_forward need for S rows and
+ * T timestep rows.  Returns 0 for an invalid configuration. */
+size_t h3_block_workspace_bytes(const h3_block_config *cfg, int32_t n_rows, int32_t n_timesteps);
+
+/* One Omni-Transformer block forward (RFC s3 figure 2; s5 work items
+ * adaln_projection_3mod through h3_ffn_down_gemm, composed as in
+ * ws1_one_h3_block):
+ *   table = bf16(SiLU(t_cond) W_ada^T + b_ada)            as [3T][6][D]
+ *   r     = timestep_index*3 + token_tag
+ *   h1    = bf16(rms(x) g1 (1 + scale_msa[r]) + shift_msa[r])
+ *   qkv   = bf16(h1 W_qkv^T + b_qkv);  q,k <- RoPE(bf16(rms_128(.) g))
+ *   o     = bf16(softmax(q k^T / sqrt(128)) v)             (no mask)
+ *   x1    = bf16(x + gate_msa[r] bf16(o W_o^T + b_o))
+ *   h2    = bf16(rms(x1) g2 (1 + scale_mlp[r]) + shift_mlp[r])
+ *   a     = bf16(SiLU(g) u),  [g | u] = bf16(h2 W_fc1^T + b_fc1)
+ *   y     = bf16(x1 + gate_mlp[r] bf16(a W_fc2^T + b_fc2))
+ * x_in, x_out: bf16 [S][D]; x_out may alias x_in.  The workspace (device,
+ * 256-byte aligned, >= h3_block_workspace_bytes) is scratch: its contents on
+ * return are the block's intermediates (layout not part of the ABI). */
+h3_status h3_block_forward(const h3_block_config *cfg, const h3_block_weights *w,
+                           const h3_packed_meta *meta, const void *x_in, void *x_out,
+                           void *workspace, size_t ws_bytes, cudaStream_t stream);
+
+/* As h3_block_forward, recording cudaEvent_t events[k] on the stream after
+ * launch stage k, for k = 0..n_events-1, stages in order: 0 AdaLN table,
+ * 1 norm1/modulate, 2 QKV + QK-norm + RoPE, 3 attention, 4 O projection +
+ * gated residual, 5 norm2/modulate, 6 FC1 + SwiGLU, 7 FC2 + gated residual.
+ * events may be NULL (then identical to h3_block_forward). */
+h3_status h3_block_forward_profiled(const h3_block_config *cfg, const h3_block_weights *w,
+                                    const h3_packed_meta *meta, const void *x_in, void *x_out,
+                                    void *workspace, size_t ws_bytes, cudaStream_t stream,
+                                    void *const *events, int32_t n_events);
+
+/* A chain of n_blocks blocks (RFC s2 fingerprint row "Transformer layers"; s5
+ * ws1_full_h3_transformer, without the refiner and heads): block b reads the
+ * output of block b-1 and uses weights w[b] (a HOST array of n_blocks
+ * structs of device pointers).  x_out may alias x_in.  Same workspace as one
+ * block. */
+h3_status h3_blocks_forward(const h3_block_config *cfg, int32_t n_blocks,
+                            const h3_block_weights *w, const h3_packed_meta *meta,
+                            const void *x_in, void *x_out, void *workspace, size_t ws_bytes,
+                            cudaStream_t stream);
+
+/* ----------------------------------------------------------------------- */
+/* Stages (each is one kernel launch)                                       */
+/* ----------------------------------------------------------------------- */
+
+/* AdaLN modulation table (RFC s5 adaln_projection_3mod; s4: the SiLU runs at
+ * the timestep-embedding precision and only its result is cast to bf16): table[t][n] = bf16(sum_k bf16(SiLU(t_cond[t][k]))
+ * w_ada[n][k] + b_ada[n]) for n < 18*D, stored [T][18*D] bf16 (= [3T][6][D]).
+ * t_cond fp32 [T][C] with 1 <= T <= 16.  b_ada may be NULL. */
+h3_status h3_adaln_table(const h3_block_config *cfg, const void *w_ada, const void *b_ada,
+                         const float *t_cond, int32_t n_timesteps, void *table_out,
+                         cudaStream_t stream);
+
+/* RMSNorm + AdaLN modulation of one branch (RFC s2 fingerprint row "Block
+ * norm", eps 1e-5; s5 h3_rmsnorm and adaln_row_gather):
+ *   h[i] = bf16(x[i] / sqrt(mean(x[i]^2) + eps) * g * (1 + scale[r_i]) + shift[r_i])
+ * with r_i = timestep_index[i]*3 + token_tag[i], shift/scale the chunks of
+ * branch 0 (attention: shift_msa, scale_msa) or 1 (MLP: shift_mlp,
+ * scale_mlp) of table [3T][6][D].  x, h_out bf16 [S][D]; norm_g bf16 [D]. */
+h3_status h3_adaln_modulate(const h3_block_config *cfg, const h3_packed_meta *meta,
+                            const void *table, int32_t branch, const void *x, const void *norm_g,
+                            void *h_out, cudaStream_t stream);
+
+/* QKV projection with the per-head Q/K RMSNorm and MM-RoPE in its epilogue
+ * (RFC s5 h3_qkv_gemm, h3_qk_rmsnorm_d128, h3_mm_rope_3axis_partial; s4: the
+ * Q/K norm precedes RoPE, whose frequencies are built in FP32 and which
+ * rotates 96 channels and no more).  h bf16 [S][D]; qkv_out bf16
+ * [S][H][3][128]: q and k slots hold the normed, rotated values, the v slot
+ * bf16(h W_v^T + b_v).  RoPE as in h3_rope_qknorm. */
+h3_status h3_qkv_projection(const h3_block_config *cfg, const h3_packed_meta *meta,
+                            const void *h, const void *w_qkv, const void *b_qkv,
+                            const void *q_norm_g, const void *k_norm_g, void *qkv_out,
+                            cudaStream_t stream);
+
+/* Standalone per-head Q/K RMSNorm + partial three-axis MM-RoPE, in place
+ * (RFC s2 rows "Q/K preprocessing", "Position encoding", "RoPE frequencies",
+ * "Rotary channels").  For every row i and head h, on the 128 channels at
+ *   q + i*row_stride + h*head_stride   (and the same for k):
+ *   n_j = bf16(x_j / sqrt(mean(x^2) + eps) * g_j)
+ *   for j < 48, with band a = j/16 (t, h, w) and f = j%16:
+ *     theta = fp32(pos_thw[i][a]) * fp32(rope_theta^(-f/16))    (fp32)
+ *     out_j    = bf16(n_j cos(theta) - n_{j+48} sin(theta))
+ *     out_j+48 = bf16(n_{j+48} cos(theta) + n_j sin(theta))
+ *   out_j = n_j for j in [96, 128).
+ * Strides are in elements, multiples of 8.  q and k bf16. */
+h3_status h3_rope_qknorm(const h3_block_config *cfg, int32_t n_rows, const int32_t *pos_thw,
+                         void *q, void *k, int64_t row_stride_elems, int64_t head_stride_elems,
+                         const void *q_norm_g, const void *k_norm_g, cudaStream_t stream);
+
+/* Full non-causal, unmasked multi-head attention over one packed document
+ * (RFC s2 fingerprint row "Attention"; s4: no causal, padding or
+ * per-modality mask in the released path; s5 h3_full_attention):  o[i][h*128 + c] = bf16(sum_j P_ij v[j][h][c]) with
+ * P = softmax_j(q_i . k_j / sqrt(128)) in fp32.  q, k, v bf16, element
+ * (row i, head h, channel c) at ptr + i*row_stride + h*head_stride + c
+ * (strides in elements, multiples of 8).  o bf16 [S][H*128].  lse_opt: NULL
+ * or fp32 [H][S] receiving log(sum_j exp(q_i.k_j/sqrt(128))). */
+h3_status h3_attention(int32_t n_rows, int32_t n_heads, const void *q, const void *k,
+                       const void *v, int64_t row_stride_elems, int64_t head_stride_elems,
+                       void *o, float *lse_opt, cudaStream_t stream);
+
+/* Output projection + gated residual of the attention branch (RFC s5
+ * h3_attention_o_gemm and adaln_gate_residual; s4: residual plus the row's
+ * gate times the sublayer output, in that order):  x_out = bf16(x + gate_msa[r] bf16(o W_o^T + b_o)).
+ * o bf16 [S][H*128]; x, x_out bf16 [S][D] (may alias); table [3T][6][D]. */
+h3_status h3_out_projection(const h3_block_config *cfg, const h3_packed_meta *meta,
+                            const void *table, const void *o, const void *w_o, const void *b_o,
+                            const void *x, void *x_out, cudaStream_t stream);
+
+/* FC1 with SwiGLU in its epilogue (RFC s5 h3_ffn_gate_up_gemm and h3_swiglu):
+ * a = bf16(SiLU(g) u) in fp32, [g | u] = bf16(h W_fc1^T + b_fc1).
+ * h bf16 [S][D]; a_out bf16 [S][F]. */
+h3_status h3_ffn_up_swiglu(const h3_block_config *cfg, int32_t n_rows, const void *h,
+                           const void *w_fc1, const void *b_fc1, void *a_out,
+                           cudaStream_t stream);
+
+/* FC2 + gated residual of the MLP branch (RFC s5 h3_ffn_down_gemm and
+ * adaln_gate_residual): y = bf16(x1 + gate_mlp[r] bf16(a W_fc2^T + b_fc2)).
+ * a bf16 [S][F]; x1, y_out bf16 [S][D] (may alias). */
+h3_status h3_ffn_down_residual(const h3_block_config *cfg, const h3_packed_meta *meta,
+                               const void *table, const void *a, const void *w_fc2,
+                               const void *b_fc2, const void *x1, void *y_out,
+                               cudaStream_t stream);
+
+/* Plain bf16 projection y = bf16(x W^T + b) with fp32 accumulation (a BF16
+ * module of the RFC s2 mixed-precision table, with its output cast).  x [M][K], W [N][K],
+ * y [M][N]; K a multiple of 64, N a multiple of 8; b may be NULL. */
+h3_status h3_linear(int32_t M, int32_t N, int32_t K, const void *x, const void *w,
+                    const void *b, void *y, cudaStream_t stream);
+
+/* ----------------------------------------------------------------------- */
+/* Status, errors, provenance                                               */
+/* ----------------------------------------------------------------------- */
+
+/* Waits for the stream's work (polling, at most timeout_ms; never blocks
+ * forever), then reads and clears the device error word.  Returns H3_OK,
+ * H3_ERR_INDEX (bad metadata was seen), H3_ERR_TIMEOUT (a device wait gave up,
+ * or the stream did not finish within timeout_ms) or H3_ERR_CUDA. */
+h3_status h3_sync_check(cudaStream_t stream, int32_t timeout_ms);
+
+const char *h3_status_string(h3_status s);
+
+/* Provenance of the most recent launch from this host thread (RFC s4 item 10,
+ * s5 h3_operator_trace): kernel id, tile shape, pipeline depth, accumulator
+ * type, grid.  Writes a NUL-terminated string of at most len bytes. */
+h3_status h3_last_kernel_info(char *buf, size_t len);
+
+/* Library version string. */
+const char *h3_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* H3_H_ */

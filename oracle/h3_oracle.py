@@ -24,7 +24,7 @@ Sources (web pages; each function names the passage it follows):
          halves).
 
 Readings taken where the pages are silent (each is one argument or constant
-below; all are listed in the design notes of the repository):
+below):
   R1 AdaLN projection output per timestep is [3 modality][6 chunk][D], so table
      row t*3+m is a plain reshape; chunk order shift_msa, scale_msa, gate_msa,
      shift_mlp, scale_mlp, gate_mlp.
@@ -98,10 +98,12 @@ def adaln_table(t_cond: np.ndarray, w_ada: np.ndarray, b_ada: Optional[np.ndarra
                 dim: int) -> np.ndarray:
     """AdaLN modulation table of one block, shape [3T][6][D].
 
-    [RFC] s2 fingerprint, row "AdaLN projection": 2688 -> 6*3*5376 per block;
-    s4 "AdaLN projection activation runs at the timestep embedding precision,
-    then casts for the BF16 projection": u = bf16(SiLU(t_cond)); the projection
-    is a BF16 module, its output cast to bf16 (s2 mixed-precision table).
+    [RFC] s2 fingerprint table, row "AdaLN projection" (2688 inputs to
+    6*3*5376 outputs per block); s4 arithmetic rules: the SiLU is evaluated at
+    the precision of the timestep embedding and only its result is cast to
+    bf16 for the projection, so u = bf16(SiLU(t_cond)).  The projection itself
+    is listed among the BF16 modules (s2 mixed-precision table), so its output
+    is cast to bf16.
     Layout per timestep is [modality][chunk][D] (reading R1), i.e. table row
     t*3 + m, the "[t0m0, t0m1, t0m2, ...]" order of probe H4 (s6.2).
     """
@@ -117,9 +119,9 @@ def adaln_table(t_cond: np.ndarray, w_ada: np.ndarray, b_ada: Optional[np.ndarra
 def adaln_rows(token_tag: np.ndarray, timestep_index: np.ndarray) -> np.ndarray:
     """Modulation row of each packed row.
 
-    [RFC] s2 fingerprint, row "AdaLN conditioning": row = timestep_index*3 +
-    token_tag, with modalities video=0, text=1, audio=2 (row "AdaLN
-    modalities"); work item adaln_row_gather (s5).
+    [RFC] s2 fingerprint table, rows "AdaLN conditioning" (the row index is
+    three times the timestep index plus the tag) and "AdaLN modalities" (tags
+    0 video, 1 text, 2 audio); work item adaln_row_gather (s5).
     """
     return np.asarray(timestep_index, np.int64) * N_MODALITIES + np.asarray(token_tag, np.int64)
 
@@ -129,8 +131,8 @@ def adaln_rows(token_tag: np.ndarray, timestep_index: np.ndarray) -> np.ndarray:
 # ---------------------------------------------------------------------------
 
 def rms_inv(x: np.ndarray, eps: float = EPS) -> np.ndarray:
-    """1/sqrt(mean(x^2) + eps) over the last axis ([RFC] s2 "Block norm:
-    RMSNorm, epsilon 1e-5")."""
+    """1/sqrt(mean(x^2) + eps) over the last axis ([RFC] s2 fingerprint
+    table, row "Block norm": an RMSNorm with eps 1e-5)."""
     x = np.asarray(x, np.float64)
     return 1.0 / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps)
 
@@ -139,7 +141,7 @@ def rmsnorm_modulate(x: np.ndarray, gain: np.ndarray, shift: np.ndarray,
                      scale: np.ndarray, eps: float = EPS) -> np.ndarray:
     """h = bf16( rms(x) * g * (1 + scale) + shift ), one cast at the end.
 
-    [RFC] s2 "Block norm: RMSNorm, epsilon 1e-5"; work items h3_rmsnorm and
+    [RFC] s2 fingerprint table, row "Block norm"; work items h3_rmsnorm and
     adaln_row_gather (s5).  Modulation form norm*(1+scale)+shift is reading R3;
     the per-channel gain is reading R4.  shift/scale are per-row [S][D].
     """
@@ -151,9 +153,9 @@ def rmsnorm_modulate(x: np.ndarray, gain: np.ndarray, shift: np.ndarray,
 def head_rmsnorm(v: np.ndarray, gain: np.ndarray, eps: float = EPS) -> np.ndarray:
     """Per-head RMSNorm over the 128 head channels, cast to bf16.
 
-    [RFC] s2 "Q/K preprocessing: per-head RMSNorm, epsilon 1e-5"; s2
-    mixed-precision table: "RMSNorm and Q/K norm outputs after declared casts"
-    (reading R7).  v has shape [..., 128]; one gain shared across heads (R5).
+    [RFC] s2 fingerprint table, row "Q/K preprocessing" (an RMSNorm per head,
+    eps 1e-5); the s2 mixed-precision table puts the norm outputs on the BF16
+    side, after their cast (reading R7).  v has shape [..., 128]; one gain shared across heads (R5).
     """
     v = np.asarray(v, np.float64)
     return bf16_round(v * rms_inv(v, eps) * np.asarray(gain, np.float64))
@@ -166,8 +168,9 @@ def head_rmsnorm(v: np.ndarray, gain: np.ndarray, eps: float = EPS) -> np.ndarra
 def rope_frequencies(n_freq: int = ROPE_FREQS_PER_AXIS, theta: float = ROPE_THETA) -> np.ndarray:
     """omega_i = theta^(-i/n_freq), i = 0..n_freq-1, rounded once to fp32.
 
-    [RFC] s2 "RoPE frequencies: 16 per axis, theta 10000"; s2 mixed-precision
-    table "RoPE frequency construction" is an FP32 path.
+    [RFC] s2 fingerprint table, row "RoPE frequencies" (16 per axis, base
+    10000); the s2 mixed-precision table lists the frequency construction as
+    an FP32 path.
     """
     i = np.arange(n_freq, dtype=np.float64)
     return fp32(theta ** (-i / n_freq))
@@ -178,8 +181,8 @@ def rope_angles(pos_thw: np.ndarray, n_freq: int = ROPE_FREQS_PER_AXIS,
     """fp32 angles [S][3*n_freq]: band a (t, h, w in that order) holds
     fp32(pos[:, a]) * omega_i computed in fp32.
 
-    [RFC] s2 "three-axis (t, h, w) MM-RoPE"; s4 "MM-RoPE constructs
-    frequencies in FP32".
+    [RFC] s2 fingerprint table, row "Position encoding" (three axes, t then h
+    then w); s4 arithmetic rules: the frequencies are built in FP32.
     """
     om = rope_frequencies(n_freq, theta)
     p = fp32(np.asarray(pos_thw))                                   # [S][3]
@@ -191,9 +194,10 @@ def mm_rope(xhat: np.ndarray, pos_thw: np.ndarray, n_freq: int = ROPE_FREQS_PER_
             theta: float = ROPE_THETA) -> np.ndarray:
     """Partial three-axis rotary embedding on [S][H][128] (bf16 values in).
 
-    [RFC] s2 "Rotary channels: 96 of 128 head channels; remaining 32 pass
-    through"; s5 h3_mm_rope_3axis_partial "rotate-half on 96/128 channels";
-    [LEDGER] "split-half RoPE".  Reading R6: with half = 48, channel j < 48
+    [RFC] s2 fingerprint table, row "Rotary channels" (96 of the 128 head
+    channels rotate, the other 32 are left as they are); s5 work item
+    h3_mm_rope_3axis_partial (a rotate-half rotation); [LEDGER] names the
+    pairing split-half.  Reading R6: with half = 48, channel j < 48
     pairs with j + 48 and uses angle column j:
         out_j      = x_j cos - x_{j+48} sin
         out_{j+48} = x_{j+48} cos + x_j sin
@@ -218,7 +222,8 @@ def mm_rope(xhat: np.ndarray, pos_thw: np.ndarray, n_freq: int = ROPE_FREQS_PER_
 
 def linear(x: np.ndarray, w: np.ndarray, b: Optional[np.ndarray] = None) -> np.ndarray:
     """bf16(x @ w^T + b): a BF16 projection with its declared output cast
-    ([RFC] s2 mixed-precision table, "Q/K/V/O and FFN projections")."""
+    ([RFC] s2 mixed-precision table, BF16 column: the Q/K/V/O and FFN
+    projections)."""
     y = np.asarray(x, np.float64) @ np.asarray(w, np.float64).T
     if b is not None:
         y = y + np.asarray(b, np.float64)[None, :]
@@ -229,7 +234,8 @@ def qk_norm_rope(qkv: np.ndarray, pos_thw: np.ndarray, q_gain: np.ndarray,
                  k_gain: np.ndarray, eps: float = EPS):
     """From the projected [S][H][3][128] buffer, return (q_hat, k_hat, v).
 
-    [RFC] s4 "Q/K RMSNorm happens before MM-RoPE"; v is untouched.
+    [RFC] s4 arithmetic rules: the Q/K norm comes first, RoPE second; v is
+    not touched.
     """
     q = head_rmsnorm(qkv[:, :, 0, :], q_gain, eps)
     k = head_rmsnorm(qkv[:, :, 1, :], k_gain, eps)
@@ -239,8 +245,9 @@ def qk_norm_rope(qkv: np.ndarray, pos_thw: np.ndarray, q_gain: np.ndarray,
 def attention_head(q: np.ndarray, k: np.ndarray, v: np.ndarray) -> np.ndarray:
     """softmax(q k^T / sqrt(128)) v for one head, exact exp, no mask.
 
-    [RFC] s2 "full bidirectional self-attention"; s4 "Full attention is
-    non-causal and unmasked over one packed document".  q: [R][128] query rows
+    [RFC] s2 fingerprint table, row "Attention" (bidirectional
+    self-attention); s4 arithmetic rules: every packed row attends to every
+    row of the document, with no causal or padding mask.  q: [R][128] query rows
     (any subset), k, v: [S][128].  Returns float64 (uncast) [R][128].
     """
     s = (np.asarray(q, np.float64) @ np.asarray(k, np.float64).T) / math.sqrt(q.shape[-1])
@@ -271,15 +278,16 @@ def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray,
 
 
 def gated_residual(x: np.ndarray, gate: np.ndarray, y: np.ndarray) -> np.ndarray:
-    """bf16(x + gate * y), in that order ([RFC] s4 "Residual gates are applied
-    in the declared order: residual + gate[row] * sublayer_output"; s5
+    """bf16(x + gate * y), in that order ([RFC] s4 arithmetic rules: the
+    residual plus the row's gate times the sublayer output; s5
     adaln_gate_residual)."""
     return bf16_round(np.asarray(x, np.float64) + np.asarray(gate, np.float64) * np.asarray(y, np.float64))
 
 
 def swiglu(g: np.ndarray, u: np.ndarray) -> np.ndarray:
-    """a = bf16(SiLU(g) * u) ([RFC] s2 "FFN activation: SwiGLU"; s5 h3_swiglu
-    "FP32-math SwiGLU"; gate/value order is reading R9)."""
+    """a = bf16(SiLU(g) * u) ([RFC] s2 fingerprint table, row "FFN
+    activation"; s5 work item h3_swiglu, computed in FP32; gate/value order is
+    reading R9)."""
     return bf16_round(silu(g) * np.asarray(u, np.float64))
 
 
@@ -290,13 +298,12 @@ def swiglu(g: np.ndarray, u: np.ndarray) -> np.ndarray:
 def block_forward(x: np.ndarray, token_tag: np.ndarray, timestep_index: np.ndarray,
                   pos_thw: np.ndarray, t_cond: np.ndarray, w: Dict[str, Optional[np.ndarray]],
                   eps: float = EPS, rows: Optional[np.ndarray] = None) -> Dict[str, np.ndarray]:
-    """One Omni-Transformer block ([RFC] s3 "One Omni-Transformer block", s5
+    """One Omni-Transformer block ([RFC] s3 figure 2, s5
     work items adaln_projection_3mod .. h3_ffn_down_gemm in that order).
 
     All inputs are float arrays holding bf16 values (t_cond: fp32 values),
     weights keyed as in the input generator.  Returns every intermediate so a
-    comparison can localise the first drift ([RFC] s4 "first-drift
-    localization").  With `rows` given, every row-wise stage after attention is
+    comparison can localise the first drift ([RFC] s4, comparison hierarchy).  With `rows` given, every row-wise stage after attention is
     evaluated for those query rows only (keys and values still use all rows).
     """
     S, D = x.shape
@@ -326,8 +333,9 @@ def block_forward(x: np.ndarray, token_tag: np.ndarray, timestep_index: np.ndarr
 
 
 def blocks_forward(x, token_tag, timestep_index, pos_thw, t_cond, weights_list, eps: float = EPS):
-    """A chain of blocks, each with its own weights ([RFC] s2 "Transformer
-    layers: 50"); the output of block b is the input of block b+1."""
+    """A chain of blocks, each with its own weights ([RFC] s2 fingerprint
+    table, row "Transformer layers": 50); the output of block b is the input
+    of block b+1."""
     for w in weights_list:
         x = block_forward(x, token_tag, timestep_index, pos_thw, t_cond, w, eps)["y"]
     return x

@@ -1,0 +1,313 @@
+"""GPU parity: every stage of the CUDA path, called through the C ABI, against
+the CPU oracle on the same seeded inputs.
+
+Per-stage tests feed each kernel the oracle's own input of that stage, so each
+comparison measures one operator.  The block tests run h3_block_forward end to
+end.  Sizes: the tiny H3-shaped block (72 rows: several tiles of every kernel
+but one M tile), a ragged small block (205 rows, odd head count: two M tiles, a
+ragged tail, a half-empty v tile), and the full-width 505-row block.
+"""
+import numpy as np
+import pytest
+import torch
+
+import h3_inputs as hi
+from oracle import h3_oracle as O
+from h3_testutil import (CHAIN_MAX_E, CHAIN_MEAN_E, MAX_E, MEAN_E, assert_close, errors, to_bf16,
+                         to_np)
+
+pytestmark = pytest.mark.gpu
+
+RAGGED = hi.custom_workload(hi.BlockShape(dim=640, n_heads=3, head_dim=128, ffn_dim=1024, cond_dim=192),
+                            n_text=13, video_grid=(2, 5, 9), n_audio=102, n_timesteps=7, name="ragged205")
+
+
+@pytest.fixture(scope="session")
+def h3():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    import audio_video_flow_gb300 as m
+    m.lib()   # raises if libh3.so is missing: no fallback path exists
+    return m
+
+
+class Case:
+    """Inputs of one workload on the CPU (numpy, for the oracle) and on the GPU."""
+
+    def __init__(self, w: hi.Workload, seed: int = 0, rows=None):
+        self.w = w
+        meta, acts, wts = hi.workload_inputs(w, seed=seed)
+        self.S = w.layout.n_rows
+        self.T = w.n_timesteps
+        self.np_w = {k: (to_np(v) if v is not None else None) for k, v in wts.items()}
+        self.np_x = to_np(acts["x"])
+        self.np_tc = acts["t_cond"].numpy().astype(np.float64)
+        self.np_meta = {k: v.numpy() for k, v in meta.items()}
+        self.ref = O.block_forward(self.np_x, self.np_meta["token_tag"], self.np_meta["timestep_index"],
+                                   self.np_meta["pos_thw"], self.np_tc, self.np_w, rows=rows)
+        self.d_w = {k: (v.cuda() if v is not None else None) for k, v in wts.items()}
+        self.d_x = acts["x"].cuda()
+        self.d_tc = acts["t_cond"].cuda()
+        self.d_meta = {k: v.cuda() for k, v in meta.items()}
+
+    def cfg(self, h3):
+        s = self.w.shape
+        return h3.make_config(s.dim, s.n_heads, s.ffn_dim, s.cond_dim)
+
+    def meta(self, h3):
+        m = self.d_meta
+        return h3.make_meta(m["token_tag"], m["timestep_index"], m["pos_thw"], self.d_tc, self.T)
+
+
+_CASES = {}
+
+
+def get_case(name):
+    if name not in _CASES:
+        w = RAGGED if name == "ragged205" else hi.WORKLOADS[name]
+        _CASES[name] = Case(w)
+    return _CASES[name]
+
+
+CASE_NAMES = ["tiny72", "ragged205", "block505"]
+
+
+def table_tensor(case):
+    return to_bf16(case.ref["table"].reshape(case.T, -1))
+
+
+# ---------------------------------------------------------------------------
+# stages
+# ---------------------------------------------------------------------------
+
+def test_linear_plain(h3):
+    g = torch.Generator().manual_seed(5)
+    M, N, K = 200, 264, 320
+    x = torch.randn(M, K, generator=g).to(torch.bfloat16)
+    w = (torch.randn(N, K, generator=g) * 0.05).to(torch.bfloat16)
+    b = (torch.randn(N, generator=g) * 0.1).to(torch.bfloat16)
+    y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    h3.h3_linear(M, N, K, x.cuda(), w.cuda(), b.cuda(), y)
+    torch.cuda.synchronize()
+    assert_close(to_np(y), O.linear(to_np(x), to_np(w), to_np(b)), "linear")
+
+
+@pytest.mark.parametrize("name", CASE_NAMES)
+def test_adaln_table(h3, name):
+    c = get_case(name)
+    out = torch.empty(c.T, 18 * c.w.shape.dim, dtype=torch.bfloat16, device="cuda")
+    h3.h3_adaln_table(c.cfg(h3), c.d_w["w_ada"], c.d_w["b_ada"], c.d_tc, out)
+    assert h3.h3_sync_check() == 0
+    assert_close(to_np(out), c.ref["table"].reshape(c.T, -1), f"adaln_table[{name}]")
+
+
+@pytest.mark.parametrize("name", CASE_NAMES)
+@pytest.mark.parametrize("branch", [0, 1])
+def test_adaln_modulate(h3, name, branch):
+    c = get_case(name)
+    x_np = c.np_x if branch == 0 else c.ref["x1"]
+    g_key = "norm1_g" if branch == 0 else "norm2_g"
+    mod = c.ref["table"][c.ref["rows"]]
+    ref = O.rmsnorm_modulate(x_np, c.np_w[g_key], mod[:, 3 * branch], mod[:, 3 * branch + 1])
+    h = torch.empty(c.S, c.w.shape.dim, dtype=torch.bfloat16, device="cuda")
+    h3.h3_adaln_modulate(c.cfg(h3), c.meta(h3), table_tensor(c), branch, to_bf16(x_np), c.d_w[g_key], h)
+    assert h3.h3_sync_check() == 0
+    assert_close(to_np(h), ref, f"modulate[{name},{branch}]")
+
+
+@pytest.mark.parametrize("name", CASE_NAMES)
+def test_qkv_projection(h3, name):
+    c = get_case(name)
+    H = c.w.shape.n_heads
+    out = torch.zeros(c.S, H, 3, 128, dtype=torch.bfloat16, device="cuda")
+    h3.h3_qkv_projection(c.cfg(h3), c.meta(h3), to_bf16(c.ref["h1"]), c.d_w["w_qkv"], None,
+                         c.d_w["q_norm_g"], c.d_w["k_norm_g"], out)
+    assert h3.h3_sync_check() == 0
+    o = to_np(out)
+    assert_close(o[:, :, 2], c.ref["v"], f"qkv.v[{name}]")
+    assert_close(o[:, :, 0], c.ref["q"], f"qkv.q[{name}]")
+    assert_close(o[:, :, 1], c.ref["k"], f"qkv.k[{name}]")
+
+
+@pytest.mark.parametrize("name", CASE_NAMES)
+def test_rope_qknorm_standalone(h3, name):
+    c = get_case(name)
+    H = c.w.shape.n_heads
+    buf = to_bf16(c.ref["qkv"].reshape(c.S, H, 3, 128))
+    h3.h3_rope_qknorm(c.cfg(h3), c.S, c.d_meta["pos_thw"], buf[:, :, 0], buf[:, :, 1], H * 384, 384,
+                      c.d_w["q_norm_g"], c.d_w["k_norm_g"])
+    assert h3.h3_sync_check() == 0
+    o = to_np(buf)
+    assert_close(o[:, :, 0], c.ref["q"], f"rope.q[{name}]")
+    assert_close(o[:, :, 1], c.ref["k"], f"rope.k[{name}]")
+    np.testing.assert_array_equal(o[:, :, 2], c.ref["v"])   # v untouched
+
+
+@pytest.mark.parametrize("name", CASE_NAMES)
+def test_attention(h3, name):
+    c = get_case(name)
+    H, S = c.w.shape.n_heads, c.S
+    buf = torch.stack([to_bf16(c.ref["q"]), to_bf16(c.ref["k"]), to_bf16(c.ref["v"])], dim=2).contiguous()
+    o = torch.empty(S, H * 128, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(H, S, dtype=torch.float32, device="cuda")
+    h3.h3_attention(S, H, buf[:, :, 0], buf[:, :, 1], buf[:, :, 2], H * 384, 384, o, lse)
+    assert h3.h3_sync_check() == 0
+    assert_close(to_np(o), c.ref["o"], f"attention[{name}]")
+    # probabilities within 1e-3: P from the exported LSE vs the oracle's P
+    lse_np = lse.cpu().numpy().astype(np.float64)
+    rows = np.unique(np.linspace(0, S - 1, 24).astype(int))
+    for h in range(H):
+        q, k = c.ref["q"][rows, h], c.ref["k"][:, h]
+        p_gpu = np.exp(q @ k.T / np.sqrt(128.0) - lse_np[h, rows][:, None])
+        p_ref = O.attention_probs(q, k)
+        assert np.abs(p_gpu - p_ref).max() <= 1e-3, f"probabilities head {h}"
+
+
+@pytest.mark.parametrize("name", CASE_NAMES)
+def test_out_projection(h3, name):
+    c = get_case(name)
+    D = c.w.shape.dim
+    x1 = torch.empty(c.S, D, dtype=torch.bfloat16, device="cuda")
+    h3.h3_out_projection(c.cfg(h3), c.meta(h3), table_tensor(c), to_bf16(c.ref["o"]), c.d_w["w_o"], None,
+                         c.d_x, x1)
+    assert h3.h3_sync_check() == 0
+    assert_close(to_np(x1), c.ref["x1"], f"out_projection[{name}]")
+
+
+@pytest.mark.parametrize("name", CASE_NAMES)
+def test_ffn_up_swiglu(h3, name):
+    c = get_case(name)
+    a = torch.empty(c.S, c.w.shape.ffn_dim, dtype=torch.bfloat16, device="cuda")
+    h3.h3_ffn_up_swiglu(c.cfg(h3), c.S, to_bf16(c.ref["h2"]), c.d_w["w_fc1"], None, a)
+    assert h3.h3_sync_check() == 0
+    assert_close(to_np(a), c.ref["a"], f"ffn_up_swiglu[{name}]")
+
+
+@pytest.mark.parametrize("name", CASE_NAMES)
+def test_ffn_down_residual(h3, name):
+    c = get_case(name)
+    y = torch.empty(c.S, c.w.shape.dim, dtype=torch.bfloat16, device="cuda")
+    h3.h3_ffn_down_residual(c.cfg(h3), c.meta(h3), table_tensor(c), to_bf16(c.ref["a"]), c.d_w["w_fc2"], None,
+                            to_bf16(c.ref["x1"]), y)
+    assert h3.h3_sync_check() == 0
+    assert_close(to_np(y), c.ref["y"], f"ffn_down_residual[{name}]")
+
+
+# ---------------------------------------------------------------------------
+# the block
+# ---------------------------------------------------------------------------
+
+def run_block(h3, c, x=None, meta=None, ws=None):
+    cfg = c.cfg(h3)
+    nbytes = h3.h3_block_workspace_bytes(cfg, c.S, c.T)
+    assert nbytes > 0
+    if ws is None:
+        ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    y = torch.empty(c.S, c.w.shape.dim, dtype=torch.bfloat16, device="cuda")
+    h3.h3_block_forward(cfg, h3.make_weights(c.d_w), meta or c.meta(h3), c.d_x if x is None else x, y, ws)
+    assert h3.h3_sync_check() == 0
+    return y
+
+
+@pytest.mark.parametrize("name", ["tiny72", "ragged205"])
+def test_block_forward_small(h3, name):
+    c = get_case(name)
+    y = run_block(h3, c)
+    assert_close(to_np(y), c.ref["y"], f"block[{name}]")
+
+
+def test_block_forward_505(h3):
+    c = get_case("block505")
+    y = run_block(h3, c)
+    mx, mn = errors(to_np(y), c.ref["y"])
+    print(f"block505 end-to-end: max_e={mx:.4f} mean_e={mn:.5f}")
+    assert_close(to_np(y), c.ref["y"], "block505 end to end", CHAIN_MAX_E, CHAIN_MEAN_E)
+
+
+def test_block_repeatable_and_inplace(h3):
+    """Control H-C0 (repeated call: bitwise equal), a fresh workspace, and
+    x_out aliasing x_in."""
+    c = get_case("ragged205")
+    y1 = run_block(h3, c)
+    y2 = run_block(h3, c)
+    assert torch.equal(y1, y2)
+    x = c.d_x.clone()
+    cfg = c.cfg(h3)
+    ws = torch.empty(h3.h3_block_workspace_bytes(cfg, c.S, c.T), dtype=torch.uint8, device="cuda")
+    h3.h3_block_forward(cfg, h3.make_weights(c.d_w), c.meta(h3), x, x, ws)
+    assert h3.h3_sync_check() == 0
+    assert torch.equal(x, y1)
+
+
+def test_block_permutation_equivariance(h3):
+    """Control H-C3: a consistent permutation of rows and metadata permutes the
+    output (keys are summed in another order, so equal within tolerance)."""
+    c = get_case("ragged205")
+    y = to_np(run_block(h3, c))
+    perm = torch.randperm(c.S, generator=torch.Generator().manual_seed(3))
+    pd = perm.cuda()
+    m = c.d_meta
+    tag, tidx, pos = (m[k][pd].contiguous() for k in ("token_tag", "timestep_index", "pos_thw"))
+    meta = h3.make_meta(tag, tidx, pos, c.d_tc, c.T)
+    x_p = c.d_x[pd].contiguous()
+    yp = to_np(run_block(h3, c, x=x_p, meta=meta))
+    assert_close(yp, y[perm.numpy()], "permuted block")
+
+
+def test_chain_two_blocks(h3):
+    c = get_case("tiny72")
+    cfg = c.cfg(h3)
+    ws = torch.empty(h3.h3_block_workspace_bytes(cfg, c.S, c.T), dtype=torch.uint8, device="cuda")
+    y = torch.empty_like(c.d_x)
+    wts = h3.make_weights(c.d_w)
+    h3.h3_blocks_forward(cfg, [wts, wts], c.meta(h3), c.d_x, y, ws)
+    assert h3.h3_sync_check() == 0
+    y1 = run_block(h3, c)
+    y2 = run_block(h3, c, x=y1)
+    assert torch.equal(y, y2)
+    ref = O.block_forward(c.ref["y"], c.np_meta["token_tag"], c.np_meta["timestep_index"], c.np_meta["pos_thw"],
+                          c.np_tc, c.np_w)["y"]
+    assert_close(to_np(y), ref, "two-block chain")
+
+
+def test_single_row_block(h3):
+    w = hi.custom_workload(hi.TINY_SHAPE, n_text=1, video_grid=(0, 0, 0), n_audio=0, n_timesteps=1)
+    c = Case(w)
+    y = run_block(h3, c)
+    assert_close(to_np(y), c.ref["y"], "block S=1")
+
+
+# ---------------------------------------------------------------------------
+# failure handling (host-detected and device-detected; nothing faults)
+# ---------------------------------------------------------------------------
+
+def test_bad_metadata_is_reported_not_faulted(h3):
+    c = get_case("tiny72")
+    bad = c.d_meta["token_tag"].clone()
+    bad[5] = 7
+    meta = h3.make_meta(bad, c.d_meta["timestep_index"], c.d_meta["pos_thw"], c.d_tc, c.T)
+    cfg = c.cfg(h3)
+    ws = torch.empty(h3.h3_block_workspace_bytes(cfg, c.S, c.T), dtype=torch.uint8, device="cuda")
+    y = torch.zeros_like(c.d_x)
+    h3.h3_block_forward(cfg, h3.make_weights(c.d_w), meta, c.d_x, y, ws)
+    assert h3.h3_sync_check() == h3.H3_ERR_INDEX
+    assert h3.h3_sync_check() == 0          # the word was cleared
+    run_block(h3, c)                        # the context is still usable
+
+
+def test_host_validation_launches_nothing(h3):
+    c = get_case("tiny72")
+    cfg = c.cfg(h3)
+    bad_cfg = h3.make_config(c.w.shape.dim, c.w.shape.n_heads, c.w.shape.ffn_dim, c.w.shape.cond_dim,
+                             head_dim=64)
+    ws = torch.empty(16, dtype=torch.uint8, device="cuda")
+    y = torch.empty_like(c.d_x)
+    with pytest.raises(h3.H3Error) as e:
+        h3.h3_block_forward(bad_cfg, h3.make_weights(c.d_w), c.meta(h3), c.d_x, y, ws)
+    assert e.value.status == h3.H3_ERR_UNSUPPORTED
+    with pytest.raises(h3.H3Error) as e:
+        h3.h3_block_forward(cfg, h3.make_weights(c.d_w), c.meta(h3), c.d_x, y, ws)
+    assert e.value.status == h3.H3_ERR_WORKSPACE
+    with pytest.raises(h3.H3Error) as e:
+        h3.h3_attention(c.S, 4, c.d_x, c.d_x, c.d_x, 1540, 384, y)
+    assert e.value.status == h3.H3_ERR_ALIGN
+    assert "tcgen05" in h3.h3_last_kernel_info() or h3.h3_last_kernel_info() != ""
