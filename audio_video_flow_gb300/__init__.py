@@ -68,7 +68,8 @@ def lib() -> ctypes.CDLL:
             "h3_block_forward": (i32, [cfgp, wp, mp, vp, vp, vp, sz, vp]),
             "h3_block_forward_profiled": (i32, [cfgp, wp, mp, vp, vp, vp, sz, vp, vp, i32]),
             "h3_blocks_forward": (i32, [cfgp, i32, wp, mp, vp, vp, vp, sz, vp]),
-            "h3_adaln_table": (i32, [cfgp, vp, vp, vp, i32, vp, vp]),
+            "h3_adaln_table_workspace_bytes": (sz, [cfgp]),
+            "h3_adaln_table": (i32, [cfgp, vp, vp, vp, i32, vp, vp, sz, vp]),
             "h3_adaln_modulate": (i32, [cfgp, mp, vp, i32, vp, vp, vp, vp]),
             "h3_qkv_projection": (i32, [cfgp, mp, vp, vp, vp, vp, vp, vp, vp]),
             "h3_rope_qknorm": (i32, [cfgp, i32, vp, vp, vp, c_int64, c_int64, vp, vp, vp]),
@@ -179,9 +180,14 @@ def h3_blocks_forward(cfg, weights_list: Sequence[BlockWeights], meta, x_in, x_o
                                    _stream(stream)), "h3_blocks_forward")
 
 
-def h3_adaln_table(cfg, w_ada, b_ada, t_cond, table_out, stream=None) -> None:
+def h3_adaln_table_workspace_bytes(cfg: BlockConfig) -> int:
+    return int(lib().h3_adaln_table_workspace_bytes(ctypes.byref(cfg)))
+
+
+def h3_adaln_table(cfg, w_ada, b_ada, t_cond, table_out, workspace, stream=None) -> None:
     _check(lib().h3_adaln_table(ctypes.byref(cfg), _ptr(w_ada), _ptr(b_ada), _ptr(t_cond), int(t_cond.shape[0]),
-                                _ptr(table_out), _stream(stream)), "h3_adaln_table")
+                                _ptr(table_out), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                _stream(stream)), "h3_adaln_table")
 
 
 def h3_adaln_modulate(cfg, meta, table, branch: int, x, norm_g, h_out, stream=None) -> None:

@@ -142,13 +142,17 @@ void fill_omega(float* omega, float theta) {
   for (int i = 0; i < 16; ++i) omega[i] = (float)std::pow((double)theta, -(double)i / 16.0);
 }
 
+size_t adaln_scratch_bytes(const h3_block_config& c) { return al256((size_t)kAdalnRows * c.cond_dim * 2); }
+
 struct WsLayout {
-  size_t table, h, qkv, o, x1, total;
+  size_t u, table, h, qkv, o, x1, total;
 };
 WsLayout ws_layout(const h3_block_config& c, int64_t S, int64_t T) {
   const size_t D = (size_t)c.dim, I = (size_t)c.n_heads * 128, F = (size_t)c.ffn_dim;
   WsLayout L{};
   size_t off = 0;
+  L.u = off;     // bf16(SiLU(t_cond)), [16][C]
+  off = al256(off + adaln_scratch_bytes(c));
   L.table = off;
   off = al256(off + (size_t)T * 18 * D * 2);
   L.h = off;
@@ -167,10 +171,13 @@ WsLayout ws_layout(const h3_block_config& c, int64_t S, int64_t T) {
 // stage launchers (arguments already validated)
 // ---------------------------------------------------------------------------
 h3_status run_adaln_table(const h3_block_config& c, const void* w_ada, const void* b_ada, const float* t_cond,
-                          int T, void* out, cudaStream_t st) {
-  CUtensorMap tm;
-  if (!make_tmap_2d(&tm, w_ada, (uint64_t)18 * c.dim, (uint64_t)c.cond_dim, (uint64_t)c.cond_dim, 128))
+                          int T, void* out, void* u_scratch, cudaStream_t st) {
+  CUtensorMap tm, tu;
+  if (!make_tmap_2d(&tm, w_ada, (uint64_t)18 * c.dim, (uint64_t)c.cond_dim, (uint64_t)c.cond_dim, 128) ||
+      !make_tmap_2d(&tu, u_scratch, kAdalnRows, (uint64_t)c.cond_dim, (uint64_t)c.cond_dim, kAdalnRows))
     return H3_ERR_CUDA;
+  h3_status s0 = cuda_st(launch_silu_rows(t_cond, T, c.cond_dim, static_cast<__nv_bfloat16*>(u_scratch), st));
+  if (s0 != H3_OK) return s0;
   AdalnArgs a{};
   a.C = c.cond_dim;
   a.T = T;
@@ -179,7 +186,7 @@ h3_status run_adaln_table(const h3_block_config& c, const void* w_ada, const voi
   a.bias = static_cast<const __nv_bfloat16*>(b_ada);
   a.out = static_cast<__nv_bfloat16*>(out);
   a.err = device_error_word();
-  return cuda_st(launch_adaln_table(tm, a, st));
+  return cuda_st(launch_adaln_table(tm, tu, a, st));
 }
 
 h3_status run_modulate(const h3_block_config& c, const h3_packed_meta& m, const void* table, int branch,
@@ -213,11 +220,13 @@ void gemm_common(GemmArgs& a, int M, int K, int num_n) {
 h3_status run_qkv(const h3_block_config& c, const h3_packed_meta& m, const void* h, const void* w_qkv,
                   const void* b_qkv, const void* qg, const void* kg, void* out, cudaStream_t st) {
   const int S = m.n_rows, D = c.dim, H = c.n_heads;
+  const int bn = gemm_choose_bn(EPI_QKV, S, 3 * H * 128, H, 0);
   CUtensorMap tA, tB;
-  if (!make_tmap_2d(&tA, h, S, D, D, 128) || !make_tmap_2d(&tB, w_qkv, (uint64_t)3 * H * 128, D, D, 128))
+  if (!make_tmap_2d(&tA, h, S, D, D, 128) ||
+      !make_tmap_2d(&tB, w_qkv, (uint64_t)3 * H * 128, D, D, (uint32_t)gemm_b_box_rows(EPI_QKV, bn)))
     return H3_ERR_CUDA;
   GemmArgs a{};
-  gemm_common(a, S, D, H + (H + 1) / 2);
+  gemm_common(a, S, D, gemm_num_n(EPI_QKV, bn, 3 * H * 128, H, 0));
   a.out = static_cast<__nv_bfloat16*>(out);
   a.ldo = 3 * H * 128;
   a.bias = static_cast<const __nv_bfloat16*>(b_qkv);
@@ -227,7 +236,7 @@ h3_status run_qkv(const h3_block_config& c, const h3_packed_meta& m, const void*
   a.pos = m.pos_thw;
   a.eps = c.eps;
   fill_omega(a.omega, c.rope_theta);
-  return cuda_st(launch_gemm(EPI_QKV, tA, tB, a, st));
+  return cuda_st(launch_gemm(EPI_QKV, bn, tA, tB, a, st));
 }
 
 h3_status run_attention(int S, int H, const void* q, const void* k, const void* v, int64_t rs, int64_t hs,
@@ -250,10 +259,13 @@ h3_status run_resid_gemm(const h3_block_config& c, const h3_packed_meta& m, cons
                          const void* act, int K, const void* w, const void* b, const void* x, void* out,
                          cudaStream_t st) {
   const int S = m.n_rows, D = c.dim;
+  const int bn = gemm_choose_bn(EPI_RESID, S, D, 0, 0);
   CUtensorMap tA, tB;
-  if (!make_tmap_2d(&tA, act, S, K, K, 128) || !make_tmap_2d(&tB, w, D, K, K, 128)) return H3_ERR_CUDA;
+  if (!make_tmap_2d(&tA, act, S, K, K, 128) ||
+      !make_tmap_2d(&tB, w, D, K, K, (uint32_t)gemm_b_box_rows(EPI_RESID, bn)))
+    return H3_ERR_CUDA;
   GemmArgs a{};
-  gemm_common(a, S, K, (D + 255) / 256);
+  gemm_common(a, S, K, gemm_num_n(EPI_RESID, bn, D, 0, 0));
   a.out = static_cast<__nv_bfloat16*>(out);
   a.ldo = D;
   a.bias = static_cast<const __nv_bfloat16*>(b);
@@ -266,7 +278,7 @@ h3_status run_resid_gemm(const h3_block_config& c, const h3_packed_meta& m, cons
   a.T = m.n_timesteps;
   a.tag = m.token_tag;
   a.tidx = m.timestep_index;
-  return cuda_st(launch_gemm(EPI_RESID, tA, tB, a, st));
+  return cuda_st(launch_gemm(EPI_RESID, bn, tA, tB, a, st));
 }
 
 h3_status run_ffn_up(const h3_block_config& c, int S, const void* h, const void* w1, const void* b1, void* out,
@@ -276,12 +288,12 @@ h3_status run_ffn_up(const h3_block_config& c, int S, const void* h, const void*
   if (!make_tmap_2d(&tA, h, S, D, D, 128) || !make_tmap_2d(&tB, w1, (uint64_t)2 * F, D, D, 128))
     return H3_ERR_CUDA;
   GemmArgs a{};
-  gemm_common(a, S, D, F / 128);
+  gemm_common(a, S, D, gemm_num_n(EPI_SWIGLU, 256, 0, 0, F));
   a.out = static_cast<__nv_bfloat16*>(out);
   a.ldo = F;
   a.bias = static_cast<const __nv_bfloat16*>(b1);
   a.F = F;
-  return cuda_st(launch_gemm(EPI_SWIGLU, tA, tB, a, st));
+  return cuda_st(launch_gemm(EPI_SWIGLU, 256, tA, tB, a, st));
 }
 
 h3_status check_block_weights(const h3_block_weights* w) {
@@ -305,6 +317,7 @@ h3_status block_impl(const h3_block_config* cfg, const h3_block_weights* w, cons
   const int S = meta->n_rows, T = meta->n_timesteps;
   const WsLayout L = ws_layout(*cfg, S, T);
   uint8_t* base = static_cast<uint8_t*>(ws);
+  void* u = base + L.u;
   void* table = base + L.table;
   void* h = base + L.h;
   void* qkv = base + L.qkv;
@@ -323,7 +336,7 @@ h3_status block_impl(const h3_block_config* cfg, const h3_block_weights* w, cons
 #define H3_TRY(expr)            \
   if ((s = (expr)) != H3_OK) return s; \
   if ((s = mark()) != H3_OK) return s;
-  H3_TRY(run_adaln_table(*cfg, w->w_ada, w->b_ada, meta->t_cond, T, table, st));
+  H3_TRY(run_adaln_table(*cfg, w->w_ada, w->b_ada, meta->t_cond, T, table, u, st));
   H3_TRY(run_modulate(*cfg, *meta, table, 0, x_in, w->norm1_g, h, st));
   H3_TRY(run_qkv(*cfg, *meta, h, w->w_qkv, w->b_qkv, w->q_norm_g, w->k_norm_g, qkv, st));
   {
@@ -397,15 +410,23 @@ h3_status h3_blocks_forward(const h3_block_config* cfg, int32_t n_blocks, const 
   return H3_OK;
 }
 
+size_t h3_adaln_table_workspace_bytes(const h3_block_config* cfg) {
+  if (check_cfg(cfg) != H3_OK) return 0;
+  return adaln_scratch_bytes(*cfg);
+}
+
 h3_status h3_adaln_table(const h3_block_config* cfg, const void* w_ada, const void* b_ada, const float* t_cond,
-                         int32_t n_timesteps, void* table_out, cudaStream_t stream) {
+                         int32_t n_timesteps, void* table_out, void* workspace, size_t ws_bytes,
+                         cudaStream_t stream) {
   h3_status s = check_cfg(cfg);
   if (s != H3_OK) return s;
-  if (!w_ada || !t_cond || !table_out) return H3_ERR_NULL;
+  if (!w_ada || !t_cond || !table_out || !workspace) return H3_ERR_NULL;
   if (n_timesteps < 1 || n_timesteps > 16) return H3_ERR_UNSUPPORTED;
-  if (!al16(w_ada) || !al16n(b_ada) || !al16(table_out) || (reinterpret_cast<uintptr_t>(t_cond) & 3u))
+  if (!al16(w_ada) || !al16n(b_ada) || !al16(table_out) || (reinterpret_cast<uintptr_t>(t_cond) & 3u) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return H3_ERR_ALIGN;
-  return run_adaln_table(*cfg, w_ada, b_ada, t_cond, n_timesteps, table_out, stream);
+  if (ws_bytes < adaln_scratch_bytes(*cfg)) return H3_ERR_WORKSPACE;
+  return run_adaln_table(*cfg, w_ada, b_ada, t_cond, n_timesteps, table_out, workspace, stream);
 }
 
 h3_status h3_adaln_modulate(const h3_block_config* cfg, const h3_packed_meta* meta, const void* table,
@@ -516,15 +537,18 @@ h3_status h3_linear(int32_t M, int32_t N, int32_t K, const void* x, const void* 
   if (K % 64 || N % 8) return H3_ERR_UNSUPPORTED;
   if (!x || !w || !y) return H3_ERR_NULL;
   if (!al16(x) || !al16(w) || !al16n(b) || !al16(y)) return H3_ERR_ALIGN;
+  const int bn = gemm_choose_bn(EPI_PLAIN, M, N, 0, 0);
   CUtensorMap tA, tB;
-  if (!make_tmap_2d(&tA, x, M, K, K, 128) || !make_tmap_2d(&tB, w, N, K, K, 128)) return H3_ERR_CUDA;
+  if (!make_tmap_2d(&tA, x, M, K, K, 128) ||
+      !make_tmap_2d(&tB, w, N, K, K, (uint32_t)gemm_b_box_rows(EPI_PLAIN, bn)))
+    return H3_ERR_CUDA;
   GemmArgs a{};
-  gemm_common(a, M, K, (N + 255) / 256);
+  gemm_common(a, M, K, gemm_num_n(EPI_PLAIN, bn, N, 0, 0));
   a.out = static_cast<__nv_bfloat16*>(y);
   a.ldo = N;
   a.bias = static_cast<const __nv_bfloat16*>(b);
   a.n_valid = N;
-  return cuda_st(launch_gemm(EPI_PLAIN, tA, tB, a, stream));
+  return cuda_st(launch_gemm(EPI_PLAIN, bn, tA, tB, a, stream));
 }
 
 h3_status h3_sync_check(cudaStream_t stream, int32_t timeout_ms) {

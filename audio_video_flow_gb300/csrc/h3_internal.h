@@ -62,11 +62,17 @@ struct GemmArgs {
   uint32_t* err;
 };
 
-cudaError_t launch_gemm(int epi, const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
+// Tile width (256, 192 or 128 columns) for a GEMM of M rows; the number of N
+// tiles and the row count of one B box (for the tensor map) at that width.
+int gemm_choose_bn(int epi, int M, int N, int H, int F);
+int gemm_num_n(int epi, int bn, int N, int H, int F);
+int gemm_b_box_rows(int epi, int bn);
+cudaError_t launch_gemm(int epi, int bn, const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
                         cudaStream_t stream);
 
-// AdaLN table: SiLU prologue + skinny tcgen05 GEMM with the weights as the M
-// operand (128 x 16 tiles), output transposed to [T][18D].
+// AdaLN table: u = bf16(SiLU(t_cond)) into a [16][C] scratch (rows >= T zero),
+// then a skinny tcgen05 GEMM with the weights as the M operand (128 x 16
+// tiles), output transposed to [T][18D].
 struct AdalnArgs {
   int C;                  // cond width (multiple of 64, <= 2816)
   int T;                  // timestep rows (1..16)
@@ -76,7 +82,10 @@ struct AdalnArgs {
   __nv_bfloat16* out;     // [T][NW]
   uint32_t* err;
 };
-cudaError_t launch_adaln_table(const CUtensorMap& tmW, const AdalnArgs& a, cudaStream_t stream);
+cudaError_t launch_silu_rows(const float* t_cond, int T, int C, __nv_bfloat16* u, cudaStream_t stream);
+cudaError_t launch_adaln_table(const CUtensorMap& tmW, const CUtensorMap& tmU, const AdalnArgs& a,
+                               cudaStream_t stream);
+constexpr int kAdalnRows = 16;   // rows of the u scratch (T <= 16, zero padded)
 
 // ---------------------------------------------------------------------------
 // attention (tcgen05 flash attention, one 128-row query tile per CTA)

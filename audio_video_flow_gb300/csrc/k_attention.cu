@@ -22,6 +22,7 @@
 #include "h3_internal.h"
 
 #include <cmath>
+#include <cstdlib>
 
 namespace h3 {
 
@@ -296,15 +297,338 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   }
 }
 
+
+// ---------------------------------------------------------------------------
+// Two query tiles per CTA (for long sequences): tiles A and B of one head
+// share every K/V tile.  The MMA warp alternates S_A = Q_A K^T, P_A V,
+// S_B = Q_B K^T, P_B V, so the tensor core works on one tile while the
+// softmax warpgroup of the other runs.  TMEM: S_A [0,128), S_B [128,256),
+// O_A [256,384), O_B [384,512).  The softmax writes P (bf16, two per
+// column) over the first 64 columns of its S buffer and the P V product
+// reads its A operand from TMEM.  Each softmax thread reads its score row
+// twice (maximum, then exponentials), so it holds at most 64 scores.  O is
+// rescaled only when a row maximum grows by more than 8 (base 2): the
+// running maximum used for the exponent then lags the true one by at most 8,
+// so probabilities before normalisation stay below 2^8; the final division
+// by the running sum uses the same maximum, so the result is unchanged.
+// ---------------------------------------------------------------------------
+namespace {
+constexpr int AT2_THREADS = 384;   // warp 0 TMA, warp 1 MMA, warps 4-7 tile A, 8-11 tile B
+constexpr int AT2_SMEM = 1024 + TILE_BYTES * (2 + KST + VST) + 512;
+constexpr float kRescaleThreshold = 8.0f;
+
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// D[tmem] (+)= A[tmem] * B[smem], bf16, fp32 accumulate.
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+}  // namespace
+
+__global__ void __launch_bounds__(AT2_THREADS, 1)
+    attention_kernel_2q(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmV, const AttnArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint8_t* sQ = smem;                       // Q_A, Q_B: 32 KB each
+  uint8_t* sK = sQ + 2 * TILE_BYTES;
+  uint8_t* sV = sK + KST * TILE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + VST * TILE_BYTES);
+  uint64_t* q_full = bars;
+  uint64_t* k_full = bars + 1;
+  uint64_t* k_empty = k_full + KST;
+  uint64_t* v_full = k_empty + KST;
+  uint64_t* v_empty = v_full + VST;
+  uint64_t* s_full = v_empty + VST;    // [2]: tile A, tile B
+  uint64_t* p_full = s_full + 2;       // [2]
+  uint64_t* o_final = p_full + 2;      // [2]
+  uint64_t* drain = o_final + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int pair = blockIdx.x, head = blockIdx.y;
+  const int S = args.S;
+  const int n_kv = (S + KV_TILE - 1) / KV_TILE;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < KST; ++s) { mbar_init(&k_full[s], 1); mbar_init(&k_empty[s], 1); }
+    for (int s = 0; s < VST; ++s) { mbar_init(&v_full[s], 1); mbar_init(&v_empty[s], 1); }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&s_full[t], 1);
+      mbar_init(&p_full[t], 4);
+      mbar_init(&o_final[t], 1);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  volatile int* abort_v = abort_flag;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      bool ok = true;
+      int issued_k = 0, issued_v = 0;
+      mbar_arrive_expect_tx(q_full, 2 * TILE_BYTES);
+      for (int t = 0; t < 2; ++t) {
+        tma_load_3d(sQ + t * TILE_BYTES, &tmQ, q_full, 0, head, pair * 256 + t * 128);
+        tma_load_3d(sQ + t * TILE_BYTES + BOX_BYTES, &tmQ, q_full, 64, head, pair * 256 + t * 128);
+      }
+      for (int j = 0; j < n_kv && ok; ++j) {
+        const int ks = j % KST;
+        if (!mbar_wait(&k_empty[ks], ((uint32_t)(j / KST) & 1u) ^ 1u, abort_v)) { ok = false; break; }
+        mbar_arrive_expect_tx(&k_full[ks], TILE_BYTES);
+        tma_load_3d(sK + ks * TILE_BYTES, &tmK, &k_full[ks], 0, head, j * KV_TILE);
+        tma_load_3d(sK + ks * TILE_BYTES + BOX_BYTES, &tmK, &k_full[ks], 64, head, j * KV_TILE);
+        ++issued_k;
+        const int vs = j % VST;
+        if (!mbar_wait(&v_empty[vs], ((uint32_t)(j / VST) & 1u) ^ 1u, abort_v)) { ok = false; break; }
+        mbar_arrive_expect_tx(&v_full[vs], TILE_BYTES);
+        tma_load_3d(sV + vs * TILE_BYTES, &tmV, &v_full[vs], 0, head, j * KV_TILE);
+        tma_load_3d(sV + vs * TILE_BYTES + BOX_BYTES, &tmV, &v_full[vs], 64, head, j * KV_TILE);
+        ++issued_v;
+      }
+      if (!ok) {
+        drain_wait(q_full, 0);
+        for (int j = (issued_k > KST ? issued_k - KST : 0); j < issued_k; ++j)
+          drain_wait(&k_full[j % KST], (uint32_t)(j / KST) & 1u);
+        for (int j = (issued_v > VST ? issued_v - VST : 0); j < issued_v; ++j)
+          drain_wait(&v_full[j % VST], (uint32_t)(j / VST) & 1u);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t idesc_o = idesc_bf16(128, 128, false, true);   // V is MN-major
+      const uint32_t q0 = smem_u32(sQ), k0 = smem_u32(sK), v0 = smem_u32(sV);
+      bool ok = mbar_wait(q_full, 0, abort_v);
+      // S_t = Q_t K_j^T into TMEM columns [128 t, 128 t + 128)
+      auto issue_s = [&](int t, int j) {
+        const uint32_t kb = k0 + (uint32_t)((j % KST) * TILE_BYTES);
+        const uint32_t qb = q0 + (uint32_t)(t * TILE_BYTES);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t off = (uint32_t)((k >> 2) * BOX_BYTES + (k & 3) * 32);
+          mma_bf16_ss(tmem_base + (uint32_t)(t * 128), sdesc_kmajor(qb + off), sdesc_kmajor(kb + off), idesc_s,
+                      k != 0 ? 1u : 0u);
+        }
+      };
+      // O_t += P_t V_j, P_t in TMEM over S_t (16 keys = 8 columns per step)
+      auto issue_pv = [&](int t, int j) {
+        const uint32_t vb = v0 + (uint32_t)((j % VST) * TILE_BYTES);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint64_t b_desc = sdesc_sw128(vb + (uint32_t)(k * 2048), BOX_BYTES, 1024);
+          mma_bf16_ts(tmem_base + 256u + (uint32_t)(t * 128), tmem_base + (uint32_t)(t * 128 + k * 8), b_desc,
+                      idesc_o, (j | k) != 0 ? 1u : 0u);
+        }
+      };
+      if (ok) ok = mbar_wait(&k_full[0], 0, abort_v);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0, 0);
+        mma_commit(&s_full[0]);
+        issue_s(1, 0);
+        mma_commit(&s_full[1]);
+      }
+      for (int j = 0; j < n_kv && ok; ++j) {
+        const bool more = j + 1 < n_kv;
+        const int ks = j % KST, vs = j % VST;
+        if (!mbar_wait(&v_full[vs], (uint32_t)(j / VST) & 1u, abort_v)) { ok = false; break; }
+        if (more && !mbar_wait(&k_full[(j + 1) % KST], (uint32_t)((j + 1) / KST) & 1u, abort_v)) { ok = false; break; }
+        for (int t = 0; t < 2; ++t) {
+          if (!mbar_wait(&p_full[t], (uint32_t)j & 1u, abort_v)) { ok = false; break; }
+          tc_fence_after();
+          issue_pv(t, j);
+          if (more) issue_s(t, j + 1);     // overwrites S_t / P_t after P_t V_j (in order)
+          if (t == 1) {
+            mma_commit(&k_empty[ks]);
+            mma_commit(&v_empty[vs]);
+          }
+          mma_commit(more ? &s_full[t] : &o_final[t]);
+        }
+      }
+      if (!ok) {
+        mma_commit(drain);
+        drain_wait(drain, 0);
+      }
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax
+    const int t = (warp - 4) >> 2;             // query tile A (0) or B (1)
+    const int qq = warp & 3;
+    const int row = qq * 32 + lane;
+    const int grow = pair * 256 + t * 128 + row;
+    const uint32_t s_base = tmem_addr(tmem_base, (uint32_t)(qq * 32), (uint32_t)(t * 128));
+    const uint32_t o_base = s_base + 256u;
+    const float sl2 = args.scale_log2;
+    float m_used = -INFINITY, l_run = 0.0f;
+    bool ok = true;
+    for (int j = 0; j < n_kv; ++j) {
+      if (!mbar_wait(&s_full[t], (uint32_t)j & 1u, abort_v)) { ok = false; break; }
+      tc_fence_after();
+      const int valid = S - j * KV_TILE;     // keys of this tile that exist (>= 1)
+      // pass 1: row maximum
+      float mx = -INFINITY;
+#pragma unroll 1
+      for (int h2 = 0; h2 < 2; ++h2) {
+        uint32_t a[32], b[32];
+        tmem_ld32(s_base + (uint32_t)(h2 * 64), a);
+        tmem_ld32(s_base + (uint32_t)(h2 * 64 + 32), b);
+        tmem_ld_wait(a);
+        tmem_ld_wait(b);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const float va = (h2 * 64 + c < valid) ? __uint_as_float(a[c]) : -INFINITY;
+          const float vb = (h2 * 64 + 32 + c < valid) ? __uint_as_float(b[c]) : -INFINITY;
+          mx = fmaxf(mx, fmaxf(va, vb));
+        }
+      }
+      const float m_tile = mx * sl2;
+      // lazy rescale: move the running maximum only when it grows by > 8
+      const bool need = m_tile > m_used + kRescaleThreshold;
+      if (__any_sync(0xffffffffu, need)) {
+        const float m_new = need ? fmaxf(m_tile, m_used) : m_used;
+        const float alpha = ex2_approx(m_used - m_new);   // 0 when m_used = -inf
+        l_run *= alpha;
+        if (j > 0) {
+          // O_t is final for tiles < j (the S_t(j) commit covers P_t V_{j-1})
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            uint32_t o[32];
+            tmem_ld32(o_base + (uint32_t)(c * 32), o);
+            tmem_ld_wait(o);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st32(o_base + (uint32_t)(c * 32), o);
+          }
+        }
+        m_used = m_new;
+      }
+      // pass 2: P = 2^(s * scale_log2 - m_used) as bf16 over the S columns
+      float rs = 0.0f;
+#pragma unroll 1
+      for (int h2 = 0; h2 < 2; ++h2) {
+        uint32_t a[32], b[32];
+        tmem_ld32(s_base + (uint32_t)(h2 * 64), a);
+        tmem_ld32(s_base + (uint32_t)(h2 * 64 + 32), b);
+        tmem_ld_wait(a);
+        tmem_ld_wait(b);
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const int k0 = h2 * 64 + 2 * c;
+          const float e0 = k0 < valid ? ex2_approx(__fmaf_rn(__uint_as_float(a[2 * c]), sl2, -m_used)) : 0.0f;
+          const float e1 = k0 + 1 < valid ? ex2_approx(__fmaf_rn(__uint_as_float(a[2 * c + 1]), sl2, -m_used)) : 0.0f;
+          rs += e0;
+          rs += e1;
+          pk[c] = pack_bf16x2(e0, e1);
+        }
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const int k0 = h2 * 64 + 32 + 2 * c;
+          const float e0 = k0 < valid ? ex2_approx(__fmaf_rn(__uint_as_float(b[2 * c]), sl2, -m_used)) : 0.0f;
+          const float e1 = k0 + 1 < valid ? ex2_approx(__fmaf_rn(__uint_as_float(b[2 * c + 1]), sl2, -m_used)) : 0.0f;
+          rs += e0;
+          rs += e1;
+          pk[16 + c] = pack_bf16x2(e0, e1);
+        }
+        // keys [64 h2, 64 h2 + 64) -> packed columns [32 h2, 32 h2 + 32): only
+        // columns this thread has already read are overwritten
+        tmem_st32(s_base + (uint32_t)(h2 * 32), pk);
+      }
+      l_run += rs;
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[t]);
+    }
+    if (ok && mbar_wait(&o_final[t], 0, abort_v)) {
+      tc_fence_after();
+      const float inv_l = 1.0f / l_run;
+      const int HD = args.H * 128;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t o[32];
+        tmem_ld32(o_base + (uint32_t)(c * 32), o);
+        tmem_ld_wait(o);
+        if (grow < S) {
+          uint4* dst = reinterpret_cast<uint4*>(args.o + (size_t)grow * HD + head * 128 + c * 32);
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            dst[g] = make_uint4(pack_bf16x2(__uint_as_float(o[g * 8 + 0]) * inv_l, __uint_as_float(o[g * 8 + 1]) * inv_l),
+                                pack_bf16x2(__uint_as_float(o[g * 8 + 2]) * inv_l, __uint_as_float(o[g * 8 + 3]) * inv_l),
+                                pack_bf16x2(__uint_as_float(o[g * 8 + 4]) * inv_l, __uint_as_float(o[g * 8 + 5]) * inv_l),
+                                pack_bf16x2(__uint_as_float(o[g * 8 + 6]) * inv_l, __uint_as_float(o[g * 8 + 7]) * inv_l));
+          }
+        }
+      }
+      if (args.lse != nullptr && grow < S)
+        args.lse[(size_t)head * S + grow] = (m_used + log2f(l_run)) * 0.69314718055994530942f;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0 && *abort_v) record_error(args.err, DEVERR_TIMEOUT);
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 512);
+  }
+}
+
+// One query tile per CTA while that is needed to fill the SMs (short
+// sequences), two otherwise.  H3_ATTN_QTILES=1|2 in the environment forces one
+// (tests cover both).
 cudaError_t launch_attention(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                              const AttnArgs& a, cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, AT_SMEM);
-  if (e != cudaSuccess) return e;
-  const dim3 grid((unsigned)((a.S + 127) / 128), (unsigned)a.H);
-  attention_kernel<<<grid, AT_THREADS, AT_SMEM, stream>>>(tmQ, tmK, tmV, a);
-  set_kernel_info("attention_kernel tcgen05.mma.cta_group::1.kind::f16 q_tile=128 kv_tile=128 k_stages=%d "
-                  "v_stages=%d acc=f32 tmem=S0,S1,O softmax=fp32-online grid=%ux%u",
-                  KST, VST, grid.x, grid.y);
+  int qtiles = ((a.S + 255) / 256) * a.H >= num_sms() ? 2 : 1;
+  if (const char* env = getenv("H3_ATTN_QTILES")) {
+    const int f = atoi(env);
+    if (f == 1 || f == 2) qtiles = f;
+  }
+  cudaError_t e;
+  if (qtiles == 2) {
+    e = cudaFuncSetAttribute(attention_kernel_2q, cudaFuncAttributeMaxDynamicSharedMemorySize, AT2_SMEM);
+    if (e != cudaSuccess) return e;
+    const dim3 grid((unsigned)((a.S + 255) / 256), (unsigned)a.H);
+    attention_kernel_2q<<<grid, AT2_THREADS, AT2_SMEM, stream>>>(tmQ, tmK, tmV, a);
+    set_kernel_info("attention_kernel_2q tcgen05.mma.cta_group::1.kind::f16 q_tiles=2x128 kv_tile=128 "
+                    "k_stages=%d v_stages=%d acc=f32 tmem=S_A,S_B,O_A,O_B P-in-TMEM lazy-rescale=%g grid=%ux%u",
+                    KST, VST, (double)kRescaleThreshold, grid.x, grid.y);
+  } else {
+    e = cudaFuncSetAttribute(attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, AT_SMEM);
+    if (e != cudaSuccess) return e;
+    const dim3 grid((unsigned)((a.S + 127) / 128), (unsigned)a.H);
+    attention_kernel<<<grid, AT_THREADS, AT_SMEM, stream>>>(tmQ, tmK, tmV, a);
+    set_kernel_info("attention_kernel tcgen05.mma.cta_group::1.kind::f16 q_tile=128 kv_tile=128 k_stages=%d "
+                    "v_stages=%d acc=f32 tmem=S0,S1,O softmax=fp32-online grid=%ux%u",
+                    KST, VST, grid.x, grid.y);
+  }
   return cudaGetLastError();
 }
 

@@ -1,54 +1,53 @@
 // tcgen05 GEMMs for the H3 block projections.
 //
-// gemm_bf16_tc<EPI>: D[128 x 256] tiles of  act[M][K] . W[rows][K]^T, bf16 in,
-// fp32 accumulate in TMEM, with the epilogue fused per projection:
+// gemm_bf16_tc<EPI, BN>: D[128 x BN] tiles of act[M][K] . W[rows][K]^T, bf16
+// in, fp32 accumulate in TMEM, with the epilogue fused per projection:
 //   EPI_PLAIN   y = bf16(acc + b)
-//   EPI_QKV     q|k tiles of one head: per-head Q/K RMSNorm, then the partial
-//               three-axis MM-RoPE on 96 of the 128 channels (RFC section 4:
-//               norm before RoPE); v tiles plain
+//   EPI_QKV     q and k columns of a head: per-head Q/K RMSNorm, then the
+//               partial three-axis MM-RoPE on 96 of the 128 channels (RFC
+//               section 4: norm before RoPE); v columns plain
 //   EPI_RESID   y = bf16(x + gate[r] * bf16(acc + b))   (RFC s4 residual order)
 //   EPI_SWIGLU  a = bf16(SiLU(g) * u) with g, u the paired gate / value tiles
 //               (the h3-metal README, section "Metal 4 and TensorOps paths",
 //               pairs the FC1 gate and up tiles so SwiGLU happens before the
 //               store)
-// Structure: persistent CTAs (one per SM), static tile order (m fastest so CTAs
-// running together share the weight tile through L2), warp 0 issues TMA loads
-// into a 4-stage mbarrier ring, warp 1 issues tcgen05.mma from one thread into
-// one of two TMEM accumulators (2 x 256 columns), warps 2-5 drain the other
-// accumulator through tcgen05.ld and run the epilogue.  The K loop of a tile
-// is a fixed sequence of 16-deep MMAs: no split-K, so the reduction order is
-// independent of M and of the grid.
+// Structure: persistent CTAs (one per SM), static tile order (m fastest, so
+// the CTAs running together share each weight tile through L2); warp 0 issues
+// TMA loads into an mbarrier ring (4-6 stages depending on BN) and L2
+// prefetches further ahead; warp 1 issues tcgen05.mma from one thread into one
+// of two TMEM accumulators (2 x BN columns); warps 2-5 drain the other
+// accumulator through tcgen05.ld and run the epilogue.  BN (256, 192 or 128)
+// is chosen per launch to fill the SMs; it changes the tiling, never the
+// reduction: every output element is the same fixed sequence of 16-deep MMAs
+// over K, so the result does not depend on M, BN or the grid (no split-K).
 //
 // adaln_table_kernel: the AdaLN projection.  Its M dimension is only T <= 16
-// timestep rows, so the GEMM is run transposed: the 18*D weight rows are the
-// 128-row M operand streamed by TMA, and bf16(SiLU(t_cond)) -- computed by the
-// CTA itself into shared memory -- is the resident N = 16 operand.  The
-// kernel is bound by the weight stream from HBM.
+// timestep rows, so the GEMM runs transposed: the 18*D weight rows are the
+// 128-row M operand streamed by TMA (two 64-column boxes per stage, 256
+// contiguous bytes of every row), and u = bf16(SiLU(t_cond)), written once by
+// silu_rows_kernel and TMA-loaded into shared memory by every CTA, is the
+// resident N = 16 operand.  The kernel is bound by the weight stream from HBM.
 #include "h3_device.cuh"
 #include "h3_internal.h"
 
 #include <cstdio>
+#include <cstdlib>
 
 namespace h3 {
 
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int BM = 128, BK = 64;
 constexpr int A_STAGE_BYTES = BM * BK * 2;   // 16 KB
-constexpr int B_STAGE_BYTES = BN * BK * 2;   // 32 KB
 constexpr int GEMM_THREADS = 192;
-constexpr int GEMM_SMEM = 1024 + STAGES * (A_STAGE_BYTES + B_STAGE_BYTES) + 256;
 
-struct GemmSmem {
-  uint8_t* a;
-  uint8_t* b;
-  uint64_t* full;
-  uint64_t* empty;
-  uint64_t* acc_full;
-  uint64_t* acc_empty;
-  uint64_t* drain;
-  uint32_t* tmem_slot;
-  int* abort_flag;
+template <int BN>
+struct GemmCfg {
+  static constexpr int STAGES = BN == 256 ? 4 : (BN == 192 ? 5 : 6);
+  static constexpr int B_STAGE_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + 256;
+  static constexpr int PREFETCH = STAGES;   // k-blocks of L2 prefetch beyond the ring
 };
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
@@ -64,6 +63,12 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
+__device__ __forceinline__ void tma_prefetch_l2(const CUtensorMap* tm, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(tm)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
 __device__ __forceinline__ void tmem_ld_wait16(uint32_t (&r)[16]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;"
                : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
@@ -75,26 +80,34 @@ __device__ __forceinline__ float bias_at(const __nv_bfloat16* b, int i) {
   return b ? __bfloat162float(b[i]) : 0.0f;
 }
 
-// Weight rows of the two 128-row halves of the B tile n_blk.
-template <int EPI>
-__device__ __forceinline__ void b_rows(const GemmArgs& a, int n_blk, int& r0, int& r1) {
-  if (EPI == EPI_SWIGLU) {
-    r0 = n_blk * 128;            // gate rows
-    r1 = a.F + n_blk * 128;      // value rows
-  } else if (EPI == EPI_QKV) {
-    if (n_blk < a.H) {           // q | k of head n_blk
-      r0 = n_blk * 384;
-      r1 = r0 + 128;
-    } else {                     // v of heads 2p, 2p+1
-      const int p = n_blk - a.H;
-      r0 = (2 * p) * 384 + 256;
-      r1 = (2 * p + 1) * 384 + 256;
+// Weight-row origins of the B boxes of tile n_blk (one box of BN rows, or two
+// boxes of 128 rows when the two halves come from different places).
+template <int EPI, int BN>
+struct BTile {
+  static constexpr int BOXES = (EPI == EPI_SWIGLU || (EPI == EPI_QKV && BN == 256)) ? 2 : 1;
+  static constexpr int BOX_ROWS = BN / BOXES;
+  __device__ static void rows(const GemmArgs& a, int n_blk, int (&r)[2]) {
+    if (EPI == EPI_SWIGLU) {
+      r[0] = n_blk * 128;              // gate rows
+      r[1] = a.F + n_blk * 128;        // value rows
+    } else if (EPI == EPI_QKV && BN == 256) {
+      if (n_blk < a.H) {               // q | k of head n_blk
+        r[0] = n_blk * 384;
+        r[1] = r[0] + 128;
+      } else {                         // v of heads 2p, 2p+1
+        const int p = n_blk - a.H;
+        r[0] = (2 * p) * 384 + 256;
+        r[1] = (2 * p + 1) * 384 + 256;
+      }
+    } else if (EPI == EPI_QKV) {       // BN == 128: q, k or v of one head
+      r[0] = (n_blk / 3) * 384 + (n_blk % 3) * 128;
+      r[1] = r[0];
+    } else {
+      r[0] = n_blk * BN;
+      r[1] = r[0];
     }
-  } else {
-    r0 = n_blk * 256;
-    r1 = r0 + 128;
   }
-}
+};
 
 // ---------------------------------------------------------------------------
 // epilogues (4 warps, thread = one accumulator row)
@@ -124,6 +137,7 @@ __device__ __forceinline__ void store16_bf16(__nv_bfloat16* dst, const float (&v
   }
 }
 
+template <int BN>
 __device__ __forceinline__ void epi_plain(const GemmArgs& a, uint32_t tacc, int m, bool valid, int n_blk) {
 #pragma unroll 1
   for (int c = 0; c < BN / 32; ++c) {
@@ -152,6 +166,7 @@ __device__ __forceinline__ void epi_plain(const GemmArgs& a, uint32_t tacc, int 
   }
 }
 
+template <int BN>
 __device__ __forceinline__ void epi_resid(const GemmArgs& a, uint32_t tacc, int m, bool valid, int n_blk) {
   const __nv_bfloat16* gate = nullptr;
   if (valid) {
@@ -216,8 +231,85 @@ __device__ __forceinline__ void epi_swiglu(const GemmArgs& a, uint32_t tacc, int
   }
 }
 
-// q|k tile of head h: columns [0,128) q, [128,256) k.
-__device__ __forceinline__ void epi_qk(const GemmArgs& a, uint32_t tacc, int m, bool valid, int h) {
+// Q or K columns of head h (128 accumulator columns at tpart): per-head
+// RMSNorm of the bf16-cast projection, then the rotation of channels 0..95
+// (channel j < 48 with j + 48, band j/16 = t, h, w), channels 96..127 normed only.
+__device__ __forceinline__ void epi_qk_part(const GemmArgs& a, uint32_t tpart, int m, bool valid, int h,
+                                            int part, const float (&pos)[3]) {
+  const int cb = h * 384 + part * 128;       // output / weight column of channel 0
+  const __nv_bfloat16* gain = part ? a.k_gain : a.q_gain;
+  float ss = 0.f;
+#pragma unroll 1
+  for (int c = 0; c < 4; ++c) {
+    uint32_t r[32];
+    tmem_ld32(tpart + c * 32, r);
+    tmem_ld_wait(r);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const float v = bf16_round(__uint_as_float(r[j]) + bias_at(a.bias, cb + c * 32 + j));
+      ss = __fmaf_rn(v, v, ss);
+    }
+  }
+  const float inv = 1.0f / sqrtf(ss * (1.0f / 128.0f) + a.eps);
+#pragma unroll 1
+  for (int band = 0; band < 3; ++band) {
+    const float p = band == 0 ? pos[0] : (band == 1 ? pos[1] : pos[2]);
+    uint32_t lo[16], hi[16];
+    tmem_ld16(tpart + band * 16, lo);
+    tmem_ld16(tpart + 48 + band * 16, hi);
+    tmem_ld_wait(lo, hi);
+    if (valid) {
+      float o1[16], o2[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int j = band * 16 + i;
+        float sn, cs;
+        sincosf(p * a.omega[i], &sn, &cs);
+        const float v1 = bf16_round(__uint_as_float(lo[i]) + bias_at(a.bias, cb + j));
+        const float v2 = bf16_round(__uint_as_float(hi[i]) + bias_at(a.bias, cb + 48 + j));
+        const float x1 = bf16_round(v1 * inv * __bfloat162float(gain[j]));
+        const float x2 = bf16_round(v2 * inv * __bfloat162float(gain[48 + j]));
+        o1[i] = __fmaf_rn(x1, cs, -(x2 * sn));
+        o2[i] = __fmaf_rn(x2, cs, x1 * sn);
+      }
+      __nv_bfloat16* dst = a.out + (size_t)m * a.ldo + cb;
+      store16_bf16(dst + band * 16, o1);
+      store16_bf16(dst + 48 + band * 16, o2);
+    }
+  }
+  uint32_t r[32];
+  tmem_ld32(tpart + 96, r);
+  tmem_ld_wait(r);
+  if (valid) {
+    float v[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const float x = bf16_round(__uint_as_float(r[j]) + bias_at(a.bias, cb + 96 + j));
+      v[j] = x * inv * __bfloat162float(gain[96 + j]);
+    }
+    store32_bf16(a.out + (size_t)m * a.ldo + cb + 96, v);
+  }
+}
+
+// V columns of one head (128 accumulator columns at tpart).
+__device__ __forceinline__ void epi_v_head(const GemmArgs& a, uint32_t tpart, int m, bool valid, int head) {
+#pragma unroll 1
+  for (int c = 0; c < 4; ++c) {
+    uint32_t r[32];
+    tmem_ld32(tpart + c * 32, r);
+    tmem_ld_wait(r);
+    if (valid && head < a.H) {
+      const int cb = head * 384 + 256 + c * 32;
+      float v[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]) + bias_at(a.bias, cb + j);
+      store32_bf16(a.out + (size_t)m * a.ldo + cb, v);
+    }
+  }
+}
+
+template <int BN>
+__device__ __forceinline__ void epi_qkv(const GemmArgs& a, uint32_t tacc, int m, bool valid, int n_blk) {
   float pos[3] = {0.f, 0.f, 0.f};
   if (valid) {
 #pragma unroll
@@ -230,125 +322,46 @@ __device__ __forceinline__ void epi_qk(const GemmArgs& a, uint32_t tacc, int m, 
       pos[ax] = (float)p;
     }
   }
-  const int colq = h * 384;  // output column of q; k at +128
-  // pass 1: per-head sums of squares of the bf16-cast projections
-  float ss[2] = {0.f, 0.f};
-#pragma unroll 1
-  for (int part = 0; part < 2; ++part) {
-#pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
-      uint32_t r[32];
-      tmem_ld32(tacc + part * 128 + c * 32, r);
-      tmem_ld_wait(r);
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const float v = bf16_round(__uint_as_float(r[j]) + bias_at(a.bias, colq + part * 128 + c * 32 + j));
-        ss[part] = __fmaf_rn(v, v, ss[part]);
-      }
+  if (BN == 256) {
+    if (n_blk < a.H) {
+      epi_qk_part(a, tacc, m, valid, n_blk, 0, pos);
+      epi_qk_part(a, tacc + 128, m, valid, n_blk, 1, pos);
+    } else {
+      const int p = n_blk - a.H;
+      epi_v_head(a, tacc, m, valid, 2 * p);
+      epi_v_head(a, tacc + 128, m, valid, 2 * p + 1);
     }
-  }
-  float inv[2];
-  inv[0] = 1.0f / sqrtf(ss[0] * (1.0f / 128.0f) + a.eps);
-  inv[1] = 1.0f / sqrtf(ss[1] * (1.0f / 128.0f) + a.eps);
-  // pass 2: normalise, rotate the 96 rotary channels, pass 32 through
-#pragma unroll 1
-  for (int band = 0; band < 3; ++band) {
-    float cs[16], sn[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const float ang = pos[band] * a.omega[i];
-      sincosf(ang, &sn[i], &cs[i]);
-    }
-#pragma unroll 1
-    for (int part = 0; part < 2; ++part) {
-      const __nv_bfloat16* gain = part ? a.k_gain : a.q_gain;
-      uint32_t lo[16], hi[16];
-      tmem_ld16(tacc + part * 128 + band * 16, lo);
-      tmem_ld16(tacc + part * 128 + 48 + band * 16, hi);
-      tmem_ld_wait(lo, hi);
-      if (valid) {
-        float o1[16], o2[16];
-        const int cb = colq + part * 128;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int j = band * 16 + i;
-          const float v1 = bf16_round(__uint_as_float(lo[i]) + bias_at(a.bias, cb + j));
-          const float v2 = bf16_round(__uint_as_float(hi[i]) + bias_at(a.bias, cb + 48 + j));
-          const float x1 = bf16_round(v1 * inv[part] * __bfloat162float(gain[j]));
-          const float x2 = bf16_round(v2 * inv[part] * __bfloat162float(gain[48 + j]));
-          o1[i] = __fmaf_rn(x1, cs[i], -(x2 * sn[i]));
-          o2[i] = __fmaf_rn(x2, cs[i], x1 * sn[i]);
-        }
-        __nv_bfloat16* dst = a.out + (size_t)m * a.ldo + cb;
-        store16_bf16(dst + band * 16, o1);
-        store16_bf16(dst + 48 + band * 16, o2);
-      }
-    }
-  }
-#pragma unroll 1
-  for (int part = 0; part < 2; ++part) {
-    const __nv_bfloat16* gain = part ? a.k_gain : a.q_gain;
-    uint32_t r[32];
-    tmem_ld32(tacc + part * 128 + 96, r);
-    tmem_ld_wait(r);
-    if (valid) {
-      const int cb = colq + part * 128;
-      float v[32];
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const float x = bf16_round(__uint_as_float(r[j]) + bias_at(a.bias, cb + 96 + j));
-        v[j] = x * inv[part] * __bfloat162float(gain[96 + j]);
-      }
-      store32_bf16(a.out + (size_t)m * a.ldo + cb + 96, v);
-    }
+  } else {
+    const int head = n_blk / 3, part = n_blk % 3;
+    if (part < 2) epi_qk_part(a, tacc, m, valid, head, part, pos);
+    else epi_v_head(a, tacc, m, valid, head);
   }
 }
 
-// v tile: columns [0,128) v of head 2p, [128,256) v of head 2p+1.
-__device__ __forceinline__ void epi_v(const GemmArgs& a, uint32_t tacc, int m, bool valid, int p) {
-#pragma unroll 1
-  for (int half = 0; half < 2; ++half) {
-    const int head = 2 * p + half;
-#pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
-      uint32_t r[32];
-      tmem_ld32(tacc + half * 128 + c * 32, r);
-      tmem_ld_wait(r);
-      if (valid && head < a.H) {
-        const int cb = head * 384 + 256 + c * 32;
-        float v[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]) + bias_at(a.bias, cb + j);
-        store32_bf16(a.out + (size_t)m * a.ldo + cb, v);
-      }
-    }
-  }
-}
-
-template <int EPI>
+template <int EPI, int BN>
 __device__ __forceinline__ void run_epilogue(const GemmArgs& a, uint32_t tacc, int m_blk, int n_blk, int row) {
   const int m = m_blk * BM + row;
   const bool valid = m < a.M;
-  if (EPI == EPI_PLAIN) epi_plain(a, tacc, m, valid, n_blk);
-  if (EPI == EPI_RESID) epi_resid(a, tacc, m, valid, n_blk);
+  if (EPI == EPI_PLAIN) epi_plain<BN>(a, tacc, m, valid, n_blk);
+  if (EPI == EPI_RESID) epi_resid<BN>(a, tacc, m, valid, n_blk);
   if (EPI == EPI_SWIGLU) epi_swiglu(a, tacc, m, valid, n_blk);
-  if (EPI == EPI_QKV) {
-    if (n_blk < a.H) epi_qk(a, tacc, m, valid, n_blk);
-    else epi_v(a, tacc, m, valid, n_blk - a.H);
-  }
+  if (EPI == EPI_QKV) epi_qkv<BN>(a, tacc, m, valid, n_blk);
 }
 
 }  // namespace
 
-template <int EPI>
+template <int EPI, int BN>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     gemm_bf16_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const GemmArgs args) {
+  using C = GemmCfg<BN>;
+  using BT = BTile<EPI, BN>;
+  constexpr int STAGES = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * A_STAGE_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * B_STAGE_BYTES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * C::B_STAGE_BYTES);
   uint64_t* full = bars;
   uint64_t* empty = bars + STAGES;
   uint64_t* acc_full = bars + 2 * STAGES;
@@ -384,6 +397,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   volatile int* abort_v = abort_flag;
 
   if (warp == 0) {
+    // ---------------------------------------------------------- TMA producer
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
@@ -392,17 +406,21 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       bool ok = true;
       for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
         const int m_blk = tile % args.num_m, n_blk = tile / args.num_m;
-        int r0, r1;
-        b_rows<EPI>(args, n_blk, r0, r1);
+        int r[2];
+        BT::rows(args, n_blk, r);
         for (int kb = 0; kb < args.num_k; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_v)) { ok = false; break; }
-          mbar_arrive_expect_tx(&full[stage], A_STAGE_BYTES + B_STAGE_BYTES);
-          uint8_t* b = sB + stage * B_STAGE_BYTES;
+          mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+          uint8_t* b = sB + stage * C::B_STAGE_BYTES;
           tma_load_2d(sA + stage * A_STAGE_BYTES, &tmA, &full[stage], kb * BK, m_blk * BM);
-          tma_load_2d(b, &tmB, &full[stage], kb * BK, r0);
-          tma_load_2d(b + B_STAGE_BYTES / 2, &tmB, &full[stage], kb * BK, r1);
+          for (int bx = 0; bx < BT::BOXES; ++bx)
+            tma_load_2d(b + bx * BT::BOX_ROWS * 128, &tmB, &full[stage], kb * BK, r[bx]);
           last_phase[stage] = (int)phase;
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          const int pk = kb + C::PREFETCH;
+          if (pk < args.num_k) {
+            for (int bx = 0; bx < BT::BOXES; ++bx) tma_prefetch_l2(&tmB, pk * BK, r[bx]);
+          }
         }
       }
       if (!ok) {  // let every load already issued land before the CTA exits
@@ -412,6 +430,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
     __syncwarp();
   } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16(BM, BN);
       int stage = 0;
@@ -428,7 +447,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           if (!mbar_wait(&full[stage], phase, abort_v)) { ok = false; break; }
           tc_fence_after();
           const uint32_t a0 = smem_u32(sA + stage * A_STAGE_BYTES);
-          const uint32_t b0 = smem_u32(sB + stage * B_STAGE_BYTES);
+          const uint32_t b0 = smem_u32(sB + stage * C::B_STAGE_BYTES);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
             mma_bf16_ss(d_tmem, sdesc_kmajor(a0 + k * 32), sdesc_kmajor(b0 + k * 32), idesc,
@@ -447,6 +466,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
     __syncwarp();
   } else {
+    // ---------------------------------------------------------- epilogue
     const int q = warp & 3;
     const int row = q * 32 + lane;
     int it = 0;
@@ -457,7 +477,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       tc_fence_after();
       const int m_blk = tile % args.num_m, n_blk = tile / args.num_m;
       const uint32_t tacc = tmem_addr(tmem_base, (uint32_t)(q * 32), (uint32_t)(acc * BN));
-      run_epilogue<EPI>(args, tacc, m_blk, n_blk, row);
+      run_epilogue<EPI, BN>(args, tacc, m_blk, n_blk, row);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[acc]);
@@ -472,31 +492,85 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   }
 }
 
-cudaError_t launch_gemm(int epi, const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
+// ---------------------------------------------------------------------------
+// host side: tile width choice and launch
+// ---------------------------------------------------------------------------
+int gemm_num_n(int epi, int bn, int N, int H, int F) {
+  if (epi == EPI_SWIGLU) return F / 128;
+  if (epi == EPI_QKV) return bn == 256 ? H + (H + 1) / 2 : 3 * H;
+  return (N + bn - 1) / bn;
+}
+
+int gemm_b_box_rows(int epi, int bn) {
+  if (epi == EPI_SWIGLU || (epi == EPI_QKV && bn == 256)) return 128;
+  return bn;
+}
+
+// Pick the tile width that minimises (waves x per-tile time) on this GPU.  A
+// tile's time is its width over the per-SM efficiency measured for that width
+// on GB300 (128-wide tiles feed the tensor core at about 65 % of the rate of
+// 192- and 256-wide ones: each 128 x 128 x 16 MMA needs as many operand bytes
+// per FLOP as the shared-memory port supplies).
+// H3_GEMM_BN=256|192|128 in the environment forces one width where the
+// epilogue supports it (tests sweep every width with it).
+int gemm_choose_bn(int epi, int M, int N, int H, int F) {
+  if (epi == EPI_SWIGLU) return 256;
+  if (const char* env = getenv("H3_GEMM_BN")) {
+    const int f = atoi(env);
+    if (f == 256 || f == 128 || (f == 192 && epi != EPI_QKV)) return f;
+  }
+  const int sms = num_sms();
+  const int num_m = (M + 127) / 128;
+  const int cands[3] = {256, 192, 128};
+  int best = 256;
+  long long best_cost = -1;
+  for (int bn : cands) {
+    if (epi == EPI_QKV && bn == 192) continue;
+    const long long tiles = (long long)num_m * gemm_num_n(epi, bn, N, H, F);
+    const long long waves = (tiles + sms - 1) / sms;
+    const long long eff_pct = bn == 256 ? 100 : (bn == 192 ? 95 : 65);
+    const long long cost = waves * bn * 100 / eff_pct;
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = bn;
+    }
+  }
+  return best;
+}
+
+template <int EPI, int BN>
+static cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, int grid,
+                              cudaStream_t stream) {
+  constexpr int smem = GemmCfg<BN>::SMEM;
+  cudaError_t e = cudaFuncSetAttribute(gemm_bf16_tc<EPI, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  gemm_bf16_tc<EPI, BN><<<grid, GEMM_THREADS, smem, stream>>>(tmA, tmB, a);
+  return cudaSuccess;
+}
+
+cudaError_t launch_gemm(int epi, int bn, const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
                         cudaStream_t stream) {
   const int tiles = a.num_m * a.num_n;
   const int grid = tiles < num_sms() ? tiles : num_sms();
   const char* names[4] = {"plain", "qkv_qknorm_rope", "gated_residual", "swiglu"};
-  cudaError_t e = cudaSuccess;
-#define H3_LAUNCH_GEMM(E)                                                                          \
-  case E: {                                                                                        \
-    e = cudaFuncSetAttribute(gemm_bf16_tc<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM); \
-    if (e != cudaSuccess) return e;                                                                \
-    gemm_bf16_tc<E><<<grid, GEMM_THREADS, GEMM_SMEM, stream>>>(tmA, tmB, a);                       \
-    break;                                                                                         \
+  cudaError_t e = cudaErrorInvalidValue;
+  switch (epi * 1000 + bn) {
+    case EPI_PLAIN * 1000 + 256: e = launch_one<EPI_PLAIN, 256>(tmA, tmB, a, grid, stream); break;
+    case EPI_PLAIN * 1000 + 192: e = launch_one<EPI_PLAIN, 192>(tmA, tmB, a, grid, stream); break;
+    case EPI_PLAIN * 1000 + 128: e = launch_one<EPI_PLAIN, 128>(tmA, tmB, a, grid, stream); break;
+    case EPI_RESID * 1000 + 256: e = launch_one<EPI_RESID, 256>(tmA, tmB, a, grid, stream); break;
+    case EPI_RESID * 1000 + 192: e = launch_one<EPI_RESID, 192>(tmA, tmB, a, grid, stream); break;
+    case EPI_RESID * 1000 + 128: e = launch_one<EPI_RESID, 128>(tmA, tmB, a, grid, stream); break;
+    case EPI_QKV * 1000 + 256: e = launch_one<EPI_QKV, 256>(tmA, tmB, a, grid, stream); break;
+    case EPI_QKV * 1000 + 128: e = launch_one<EPI_QKV, 128>(tmA, tmB, a, grid, stream); break;
+    case EPI_SWIGLU * 1000 + 256: e = launch_one<EPI_SWIGLU, 256>(tmA, tmB, a, grid, stream); break;
+    default: return cudaErrorInvalidValue;
   }
-  switch (epi) {
-    H3_LAUNCH_GEMM(EPI_PLAIN)
-    H3_LAUNCH_GEMM(EPI_QKV)
-    H3_LAUNCH_GEMM(EPI_RESID)
-    H3_LAUNCH_GEMM(EPI_SWIGLU)
-    default:
-      return cudaErrorInvalidValue;
-  }
-#undef H3_LAUNCH_GEMM
-  set_kernel_info("gemm_bf16_tc<%s> tcgen05.mma.cta_group::1.kind::f16 tile=%dx%dx%d stages=%d acc=f32 "
-                  "tmem=2x%d grid=%d tiles=%dx%d k_blocks=%d",
-                  names[epi], BM, BN, BK, STAGES, BN, grid, a.num_m, a.num_n, a.num_k);
+  if (e != cudaSuccess) return e;
+  const int stages = bn == 256 ? GemmCfg<256>::STAGES : (bn == 192 ? GemmCfg<192>::STAGES : GemmCfg<128>::STAGES);
+  set_kernel_info("gemm_bf16_tc<%s,%d> tcgen05.mma.cta_group::1.kind::f16 tile=%dx%dx%d stages=%d acc=f32 "
+                  "tmem=2x%d grid=%d tiles=%dx%d k_blocks=%d l2_prefetch=%d",
+                  names[epi], bn, BM, bn, BK, stages, bn, grid, a.num_m, a.num_n, a.num_k, stages);
   return cudaGetLastError();
 }
 
@@ -504,26 +578,47 @@ cudaError_t launch_gemm(int epi, const CUtensorMap& tmA, const CUtensorMap& tmB,
 // AdaLN table
 // ---------------------------------------------------------------------------
 namespace {
-constexpr int AD_STAGES = 8;
+constexpr int AD_KPS = 2;       // 64-column boxes per stage (256 contiguous bytes of each weight row)
+constexpr int AD_STAGES = 4;
+constexpr int AD_STAGE_BYTES = AD_KPS * A_STAGE_BYTES;
 constexpr int AD_BN = 16;
 constexpr int AD_THREADS = 192;
 constexpr int AD_U_MAX_KB = 44;  // cond_dim <= 44 * 64 = 2816
-constexpr int AD_SMEM = 1024 + AD_U_MAX_KB * 2048 + AD_STAGES * A_STAGE_BYTES + 256;
+constexpr int AD_SMEM = 1024 + AD_U_MAX_KB * 2048 + AD_STAGES * AD_STAGE_BYTES + 256;
+constexpr int AD_PREFETCH = 2 * AD_STAGES;   // stages of L2 prefetch beyond the ring
 }  // namespace
 
+// u[t][k] = bf16(SiLU(t_cond[t][k])) in fp32 for t < T, zero for T <= t < 16.
+__global__ void __launch_bounds__(256) silu_rows_kernel(const float* __restrict__ t_cond, int T, int C,
+                                                        __nv_bfloat16* __restrict__ u) {
+  const int n = AD_BN * C;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+    const int t = i / C;
+    float v = 0.0f;
+    if (t < T) {
+      const float x = t_cond[i];
+      v = x / (1.0f + expf(-x));
+    }
+    u[i] = __float2bfloat16_rn(v);
+  }
+}
+
 __global__ void __launch_bounds__(AD_THREADS, 1)
-    adaln_table_kernel(const __grid_constant__ CUtensorMap tmW, const AdalnArgs args) {
+    adaln_table_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmU,
+                       const AdalnArgs args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
-  const int nkb = args.C / BK;
-  uint8_t* sU = smem;                         // nkb blocks of 16 rows x 128 B
-  uint8_t* sA = smem + nkb * 2048;            // 1024-aligned (2048 multiple)
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sA + AD_STAGES * A_STAGE_BYTES);
+  const int nkb = args.C / BK;                 // 64-column blocks of K
+  const int nst = (nkb + AD_KPS - 1) / AD_KPS; // stages per tile
+  uint8_t* sU = smem;                          // nkb blocks of 16 rows x 128 B
+  uint8_t* sA = smem + nkb * 2048;             // 1024-aligned (2048 multiple)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sA + AD_STAGES * AD_STAGE_BYTES);
   uint64_t* full = bars;
   uint64_t* empty = bars + AD_STAGES;
   uint64_t* acc_full = bars + 2 * AD_STAGES;
   uint64_t* acc_empty = acc_full + 2;
-  uint64_t* drain = acc_empty + 2;
+  uint64_t* u_full = acc_empty + 2;
+  uint64_t* drain = u_full + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
@@ -537,11 +632,15 @@ __global__ void __launch_bounds__(AD_THREADS, 1)
       mbar_init(&acc_full[i], 1);
       mbar_init(&acc_empty[i], 4);
     }
+    mbar_init(u_full, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 0 && lane == 0) tma_prefetch_desc(&tmW);
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmW);
+    tma_prefetch_desc(&tmU);
+  }
   if (warp == 1) tmem_alloc(tmem_slot, 32);
   tc_fence_before();
   __syncthreads();
@@ -549,42 +648,37 @@ __global__ void __launch_bounds__(AD_THREADS, 1)
   const uint32_t tmem_base = *tmem_slot;
   const int num_tiles = args.NW / BM;
   volatile int* abort_v = abort_flag;
-  if (warp != 0) {
-    // Warps 1-5: u = bf16(SiLU(t_cond)) in fp32, rows >= T zero, written in
-    // the K-major 128-byte-swizzled layout the tensor core reads, while warp 0
-    // already streams weight tiles.
-    for (int idx = threadIdx.x - 32; idx < AD_BN * args.C; idx += AD_THREADS - 32) {
-      const int t = idx / args.C, k = idx - t * args.C;
-      float v = 0.0f;
-      if (t < args.T) {
-        const float x = args.t_cond[(size_t)t * args.C + k];
-        v = x / (1.0f + expf(-x));
-      }
-      const uint32_t off = (uint32_t)(k >> 6) * 2048u +
-                           sw128_offset((uint32_t)t, (uint32_t)((k & 63) >> 3)) + (uint32_t)(k & 7) * 2u;
-      *reinterpret_cast<__nv_bfloat16*>(sU + off) = __float2bfloat16_rn(v);
-    }
-    fence_proxy_async_smem();
-    asm volatile("bar.sync 1, %0;" ::"n"(AD_THREADS - 32) : "memory");
-  }
 
   if (warp == 0) {
     if (lane == 0) {
+      // the resident N = 16 operand, one 2 KB box per 64 columns of K
+      mbar_arrive_expect_tx(u_full, (uint32_t)nkb * 2048u);
+      for (int kb = 0; kb < nkb; ++kb) tma_load_2d(sU + kb * 2048, &tmU, u_full, kb * BK, 0);
       int stage = 0;
       uint32_t phase = 0;
       int last_phase[AD_STAGES];
       for (int s = 0; s < AD_STAGES; ++s) last_phase[s] = -1;
       bool ok = true;
       for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-        for (int kb = 0; kb < nkb; ++kb) {
+        for (int kb = 0; kb < AD_PREFETCH * AD_KPS && kb < nkb; ++kb) tma_prefetch_l2(&tmW, kb * BK, tile * BM);
+        for (int st = 0; st < nst; ++st) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_v)) { ok = false; break; }
-          mbar_arrive_expect_tx(&full[stage], A_STAGE_BYTES);
-          tma_load_2d(sA + stage * A_STAGE_BYTES, &tmW, &full[stage], kb * BK, tile * BM);
+          const int k0 = st * AD_KPS;
+          const int nb = nkb - k0 < AD_KPS ? nkb - k0 : AD_KPS;
+          mbar_arrive_expect_tx(&full[stage], (uint32_t)(nb * A_STAGE_BYTES));
+          for (int b = 0; b < nb; ++b)
+            tma_load_2d(sA + stage * AD_STAGE_BYTES + b * A_STAGE_BYTES, &tmW, &full[stage], (k0 + b) * BK,
+                        tile * BM);
           last_phase[stage] = (int)phase;
           if (++stage == AD_STAGES) { stage = 0; phase ^= 1u; }
+          for (int b = 0; b < AD_KPS; ++b) {
+            const int pk = (st + AD_PREFETCH) * AD_KPS + b;
+            if (pk < nkb) tma_prefetch_l2(&tmW, pk * BK, tile * BM);
+          }
         }
       }
       if (!ok) {
+        drain_wait(u_full, 0);
         for (int s = 0; s < AD_STAGES; ++s)
           if (last_phase[s] >= 0) drain_wait(&full[s], (uint32_t)last_phase[s]);
       }
@@ -595,7 +689,7 @@ __global__ void __launch_bounds__(AD_THREADS, 1)
       constexpr uint32_t idesc = idesc_bf16(BM, AD_BN);
       int stage = 0;
       uint32_t phase = 0;
-      bool ok = true;
+      bool ok = mbar_wait(u_full, 0, abort_v);
       int it = 0;
       const uint32_t u0 = smem_u32(sU);
       for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++it) {
@@ -604,15 +698,19 @@ __global__ void __launch_bounds__(AD_THREADS, 1)
         if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, abort_v)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * AD_BN);
-        for (int kb = 0; kb < nkb; ++kb) {
+        for (int st = 0; st < nst; ++st) {
           if (!mbar_wait(&full[stage], phase, abort_v)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t a0 = smem_u32(sA + stage * A_STAGE_BYTES);
-          const uint32_t b0 = u0 + (uint32_t)kb * 2048u;
+          const int k0 = st * AD_KPS;
+          const int nb = nkb - k0 < AD_KPS ? nkb - k0 : AD_KPS;
+          for (int b = 0; b < nb; ++b) {
+            const uint32_t a0 = smem_u32(sA + stage * AD_STAGE_BYTES + b * A_STAGE_BYTES);
+            const uint32_t b0 = u0 + (uint32_t)(k0 + b) * 2048u;
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k) {
-            mma_bf16_ss(d_tmem, sdesc_kmajor(a0 + k * 32), sdesc_kmajor(b0 + k * 32), idesc,
-                        (kb | k) != 0 ? 1u : 0u);
+            for (int k = 0; k < BK / 16; ++k) {
+              mma_bf16_ss(d_tmem, sdesc_kmajor(a0 + k * 32), sdesc_kmajor(b0 + k * 32), idesc,
+                          ((k0 + b) | k) != 0 ? 1u : 0u);
+            }
           }
           mma_commit(&empty[stage]);
           if (++stage == AD_STAGES) { stage = 0; phase ^= 1u; }
@@ -658,15 +756,23 @@ __global__ void __launch_bounds__(AD_THREADS, 1)
   }
 }
 
-cudaError_t launch_adaln_table(const CUtensorMap& tmW, const AdalnArgs& a, cudaStream_t stream) {
+cudaError_t launch_silu_rows(const float* t_cond, int T, int C, __nv_bfloat16* u, cudaStream_t stream) {
+  const int n = AD_BN * C;
+  const int blocks = (n + 255) / 256 < 1024 ? (n + 255) / 256 : 1024;
+  silu_rows_kernel<<<blocks, 256, 0, stream>>>(t_cond, T, C, u);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_adaln_table(const CUtensorMap& tmW, const CUtensorMap& tmU, const AdalnArgs& a,
+                               cudaStream_t stream) {
   const int tiles = a.NW / BM;
   const int grid = tiles < num_sms() ? tiles : num_sms();
   cudaError_t e = cudaFuncSetAttribute(adaln_table_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, AD_SMEM);
   if (e != cudaSuccess) return e;
-  adaln_table_kernel<<<grid, AD_THREADS, AD_SMEM, stream>>>(tmW, a);
-  set_kernel_info("adaln_table_kernel tcgen05.mma.cta_group::1.kind::f16 tile=%dx%dx%d stages=%d acc=f32 "
-                  "tmem=2x%d grid=%d tiles=%d k_blocks=%d (SiLU prologue in smem)",
-                  BM, AD_BN, BK, AD_STAGES, AD_BN, grid, tiles, a.C / BK);
+  adaln_table_kernel<<<grid, AD_THREADS, AD_SMEM, stream>>>(tmW, tmU, a);
+  set_kernel_info("adaln_table_kernel tcgen05.mma.cta_group::1.kind::f16 tile=%dx%dx%d stages=%dx%d acc=f32 "
+                  "tmem=2x%d grid=%d tiles=%d k_blocks=%d l2_prefetch=%d stages",
+                  BM, AD_BN, BK, AD_STAGES, AD_KPS, AD_BN, grid, tiles, a.C / BK, AD_PREFETCH);
   return cudaGetLastError();
 }
 

@@ -31,6 +31,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "H3 block fwd TFLOP/s & packed tokens/s (bf16, 1 GB300); % of tensor/HBM roofline"
+KERNELS_PER_BLOCK = 9   # SiLU rows + AdaLN table + the seven stage kernels below
 STAGES = ("adaln_table", "norm1_modulate", "qkv_qknorm_rope", "attention", "out_proj_residual",
           "norm2_modulate", "fc1_swiglu", "fc2_residual")
 # dram__bytes_read.sum + dram__bytes_write.sum per launch from an ncu capture
@@ -173,6 +174,85 @@ class ClockSampler:
 # our arm
 # ---------------------------------------------------------------------------
 
+def run_attention_core(args, ws_n: int, rank: int, local: int):
+    """Attention core alone: per-head Q/K RMSNorm + MM-RoPE prologue (in place)
+    and full non-causal attention over S packed rows, 56 heads."""
+    import torch
+    import audio_video_flow_gb300 as h3
+    import h3_inputs as hi
+
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    wl = hi.WORKLOADS[args.workload]
+    shape, S = wl.shape, wl.layout.n_rows
+    H = shape.n_heads
+    cfg = h3.make_config(shape.dim, H, shape.ffn_dim, shape.cond_dim)
+    meta = hi.packed_metadata(wl.layout, 1, args.seed)
+    ins = hi.attention_inputs(shape, S, args.seed, device=dev)
+    qkv, qg, kg = ins["qkv"], ins["q_norm_g"], ins["k_norm_g"]
+    pos = meta["pos_thw"].to(dev)
+    o = torch.empty(S, H * 128, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+    q, k, v = qkv[:, :, 0], qkv[:, :, 1], qkv[:, :, 2]
+    rs, hs = H * 384, 384
+    n = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+
+    def step(i=None):
+        if i is not None:
+            ev[i][0].record(stream)
+        h3.h3_rope_qknorm(cfg, S, pos, q, k, rs, hs, qg, kg)
+        if i is not None:
+            ev[i][1].record(stream)
+        h3.h3_attention(S, H, q, k, v, rs, hs, o)
+        if i is not None:
+            ev[i][2].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    flops = 4.0 * S * S * H * 128
+    rope_bytes = 2.0 * 2 * S * H * 128 * 2
+    with ClockSampler(local) as clk:
+        barrier(ws_n)
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for i in range(n):
+            step(i)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        barrier(ws_n)
+    status = h3.h3_sync_check(timeout_ms=60000)
+    if status != 0:
+        raise RuntimeError(f"device error: {h3.status_string(status)}")
+    elapsed_ms, units = aggregate(t0.elapsed_time(t1), n * flops, ws_n)
+    rope_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    attn_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    peaks = load_peaks()
+    achieved = flops / (attn_ms * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": round(units / (elapsed_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+        "n_gpus": ws_n, "steps": n, "warmup": args.warmup, "ms_per_step": round(elapsed_ms / n, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "tokens_per_s": round(ws_n * S * n / (elapsed_ms * 1e-3), 1),
+        "config": {"workload": wl.name, "description": wl.description, "rows": S, "heads": H,
+                   "l2": "inputs larger than L2" if S * H * 384 * 2 > 129e6 else "inputs L2-resident",
+                   "parallelism": f"replicas x{ws_n}"},
+        "e2e": None, "gpu_launches": 2 * n,
+        "roofline": {"kernel": "attention", "bound": "tensor", "achieved": round(achieved, 1),
+                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": round(achieved / peaks["bf16_tflops"], 4), "peak_source": peaks["source"] + " bf16 burst",
+                     "traffic": TRAFFIC.get(f"attention@{wl.name}")},
+        "stages": {"rope_qknorm": {"us": round(rope_ms * 1e3, 2),
+                                   "gbs": round(rope_bytes / (rope_ms * 1e-3) / 1e9, 1),
+                                   "hbm_frac": round(rope_bytes / (rope_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)},
+                   "attention": {"us": round(attn_ms * 1e3, 2), "tflops": round(achieved, 1)}},
+        "clocks": clk.summary(),
+    }
+    return line
+
+
 def run_ours(args, ws_n: int, rank: int, local: int):
     import torch
     import audio_video_flow_gb300 as h3
@@ -181,6 +261,8 @@ def run_ours(args, ws_n: int, rank: int, local: int):
     torch.cuda.set_device(local)
     dev = f"cuda:{local}"
     wl = hi.WORKLOADS[args.workload]
+    if wl.name.startswith("attn"):
+        return run_attention_core(args, ws_n, rank, local)
     shape, S, T, NB = wl.shape, wl.layout.n_rows, wl.n_timesteps, wl.n_blocks
     cfg = h3.make_config(shape.dim, shape.n_heads, shape.ffn_dim, shape.cond_dim)
     meta_c, acts_c, _ = hi.workload_inputs(wl, seed=args.seed, device="cpu", block=0) if NB == 1 else \
@@ -202,6 +284,13 @@ def run_ours(args, ws_n: int, rank: int, local: int):
     # durations are read from the timed region itself
     ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(len(STAGES) + 1)] for _ in range(NB)]
           for _ in range(args.steps)]
+    # torch only reports elapsed time between events it has recorded itself:
+    # record each once here; inside the timed region the library re-records
+    # the stage events after each launch (the latest record is what counts).
+    for e3 in ev:
+        for e2 in e3:
+            for e in e2:
+                e.record(stream)
 
     def step(i=None):
         for b in range(NB):
@@ -314,7 +403,7 @@ def run_ours(args, ws_n: int, rank: int, local: int):
                          (NB * weight_bytes(shape) / 1e9),
                    "parallelism": f"replicas x{ws_n}"},
         "e2e": e2e,
-        "gpu_launches": args.steps * NB * len(STAGES),
+        "gpu_launches": args.steps * NB * KERNELS_PER_BLOCK,
         "roofline": {"kernel": dom, "bound": BOUND[dom], "achieved": round(achieved, 1), "peak": peak,
                      "unit": unit, "frac": round(achieved / peak, 4),
                      "peak_source": peaks["source"] + (" bf16 burst" if BOUND[dom] == "tensor" else " hbm copy"),
@@ -333,13 +422,13 @@ def run_ours(args, ws_n: int, rank: int, local: int):
 # ---------------------------------------------------------------------------
 
 class OracleRowStepper:
-    """Times the CPU oracle one packed row at a time.  Before timing: the AdaLN
-    table and every row's q/k/v (the keys and values all rows attend to).
-    Each step then evaluates one row's share of the block: its QKV projection
-    and QK-norm/RoPE, its attention over all keys, the O projection and
-    residual, norm2, FC1/SwiGLU and FC2/residual."""
+    """Times the CPU oracle a few packed rows at a time.  Before timing: the
+    AdaLN table and every row's q/k/v (the keys and values all rows attend
+    to).  Each step then evaluates the block's work for `rows` packed rows:
+    their QKV projection and QK-norm/RoPE, attention over all keys, the O
+    projection and residual, norm2, FC1/SwiGLU and FC2/residual."""
 
-    def __init__(self, wl, seed):
+    def __init__(self, wl, seed, rows: int = 8):
         import numpy as np
         import torch
         import h3_inputs as hi
@@ -359,20 +448,21 @@ class OracleRowStepper:
         qkv = O.linear(h1, self.w["w_qkv"]).reshape(wl.layout.n_rows, wl.shape.n_heads, 3, 128)
         _, self.k, self.v = O.qk_norm_rope(qkv, self.pos, self.w["q_norm_g"], self.w["k_norm_g"])
         self.S, self.shape = wl.layout.n_rows, wl.shape
+        self.rows = rows
         self.row_flops = sum(f for f, _ in stage_work(wl.shape, wl.layout.n_rows, wl.n_timesteps).values()) \
             / wl.layout.n_rows
+        self.step_flops = rows * self.row_flops
         self.i = 0
 
     def step(self):
         O, np = self.O, self.np
-        i = self.i % self.S
-        self.i += 1
-        r = slice(i, i + 1)
+        r = (np.arange(self.rows) + self.i) % self.S
+        self.i += self.rows
         mod = self.mod[r]
         h1 = O.rmsnorm_modulate(self.x[r], self.w["norm1_g"], mod[:, 0], mod[:, 1])
-        qkv = O.linear(h1, self.w["w_qkv"]).reshape(1, self.shape.n_heads, 3, 128)
+        qkv = O.linear(h1, self.w["w_qkv"]).reshape(self.rows, self.shape.n_heads, 3, 128)
         q, _, _ = O.qk_norm_rope(qkv, self.pos[r], self.w["q_norm_g"], self.w["k_norm_g"])
-        o = np.empty((1, self.shape.n_heads * 128))
+        o = np.empty((self.rows, self.shape.n_heads * 128))
         for h in range(self.shape.n_heads):
             o[:, h * 128:(h + 1) * 128] = O.attention_head(q[:, h], self.k[:, h], self.v[:, h])
         o = O.bf16_round(o)
@@ -398,11 +488,11 @@ def cpu_baseline(wl, seed, seconds: float):
         st.step()
         n += 1
     dt = time.perf_counter() - t0
-    tflops = n * st.row_flops / dt / 1e12
+    tflops = n * st.step_flops / dt / 1e12
     return {"value": round(tflops, 6), "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
-            "tokens_per_s": round(n / dt, 2),
-            "sample": f"{n} packed rows of {wl.name}, one row's block work per step in fp64 numpy "
-                      f"(AdaLN table and all rows' K/V computed before timing), {dt:.1f} s"}
+            "tokens_per_s": round(n * st.rows / dt, 2),
+            "sample": f"{n * st.rows} packed rows of {wl.name}, {st.rows} rows' block work per step in fp64 "
+                      f"numpy (AdaLN table and all rows' K/V computed before timing), {dt:.1f} s"}
 
 
 def run_reference(args, ws_n: int, rank: int):
@@ -420,16 +510,16 @@ def run_reference(args, ws_n: int, rank: int):
     for _ in range(args.steps):
         st.step()
     dt = time.perf_counter() - t0
-    flops_step = st.row_flops
+    flops_step = st.step_flops
     value = args.steps * flops_step / dt / 1e12
     return {"metric": METRIC, "impl": "reference", "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": ws_n,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / args.steps, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "tokens_per_s": round(args.steps / dt, 3),
-            "config": {"workload": wl.name, "rows": wl.layout.n_rows, "sample": "one packed row per step"},
+            "tokens_per_s": round(args.steps * st.rows / dt, 3),
+            "config": {"workload": wl.name, "rows": wl.layout.n_rows, "sample": f"{st.rows} packed rows per step"},
             "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
-                             "sample": "one packed row's block work per step (AdaLN table and all rows' K/V "
-                                       "computed before timing)"},
+                             "sample": f"{st.rows} packed rows' block work per step (AdaLN table and all rows' "
+                                       "K/V computed before timing)"},
             "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 

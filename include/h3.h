@@ -159,12 +159,16 @@ h3_status h3_blocks_forward(const h3_block_config *cfg, int32_t n_blocks,
 /* ----------------------------------------------------------------------- */
 
 /* AdaLN modulation table (RFC s5 adaln_projection_3mod; s4: the SiLU runs at
- * the timestep-embedding precision and only its result is cast to bf16): table[t][n] = bf16(sum_k bf16(SiLU(t_cond[t][k]))
- * w_ada[n][k] + b_ada[n]) for n < 18*D, stored [T][18*D] bf16 (= [3T][6][D]).
- * t_cond fp32 [T][C] with 1 <= T <= 16.  b_ada may be NULL. */
+ * the timestep-embedding precision and only its result is cast to bf16):
+ * table[t][n] = bf16(sum_k bf16(SiLU(t_cond[t][k])) w_ada[n][k] + b_ada[n])
+ * for n < 18*D, stored [T][18*D] bf16 (= [3T][6][D]).  t_cond fp32 [T][C]
+ * with 1 <= T <= 16.  b_ada may be NULL.  workspace: device scratch of at
+ * least h3_adaln_table_workspace_bytes bytes, 256-byte aligned (holds the
+ * bf16 SiLU rows). */
+size_t h3_adaln_table_workspace_bytes(const h3_block_config *cfg);
 h3_status h3_adaln_table(const h3_block_config *cfg, const void *w_ada, const void *b_ada,
                          const float *t_cond, int32_t n_timesteps, void *table_out,
-                         cudaStream_t stream);
+                         void *workspace, size_t ws_bytes, cudaStream_t stream);
 
 /* RMSNorm + AdaLN modulation of one branch (RFC s2 fingerprint row "Block
  * norm", eps 1e-5; s5 h3_rmsnorm and adaln_row_gather):

@@ -35,8 +35,8 @@ def test_workspace_bytes_and_config_validation(lib):
     cfg = h3.make_config(5376, 56, 14336, 2688)
     n = h3.h3_block_workspace_bytes(cfg, 505, 12)
     D, I, F, S, T = 5376, 7168, 14336, 505, 12
-    at_least = 2 * (T * 18 * D + S * D + S * max(3 * I, F) + S * I + S * D)
-    assert at_least <= n < at_least + 5 * 256
+    at_least = 2 * (16 * 2688 + T * 18 * D + S * D + S * max(3 * I, F) + S * I + S * D)
+    assert at_least <= n < at_least + 6 * 256
     assert h3.h3_block_workspace_bytes(cfg, 0, 12) == 0
     assert h3.h3_block_workspace_bytes(cfg, 10, 17) == 0
     for bad in [h3.make_config(5376, 56, 14336, 2688, head_dim=64),
@@ -72,7 +72,9 @@ def test_host_rejections_return_before_any_launch(lib):
     assert L.h3_linear(0, 8, 64, 16, 16, None, 16, None) == h3.H3_ERR_SHAPE
     assert L.h3_linear(8, 8, 96, 16, 16, None, 16, None) == h3.H3_ERR_UNSUPPORTED
     assert L.h3_adaln_modulate(ctypes.byref(cfg), ctypes.byref(meta), 16, 2, 16, 16, 16, None) == h3.H3_ERR_SHAPE
-    assert L.h3_adaln_table(ctypes.byref(cfg), 16, None, 16, 17, 16, None) == h3.H3_ERR_UNSUPPORTED
+    assert L.h3_adaln_table(ctypes.byref(cfg), 16, None, 16, 17, 16, 256, 1 << 20, None) == h3.H3_ERR_UNSUPPORTED
+    assert L.h3_adaln_table(ctypes.byref(cfg), 16, None, 16, 4, 16, 256, 16, None) == h3.H3_ERR_WORKSPACE
+    assert L.h3_adaln_table_workspace_bytes(ctypes.byref(cfg)) == 16 * 256 * 2
     buf = ctypes.create_string_buffer(64)
     assert L.h3_last_kernel_info(None, 0) == h3.H3_ERR_NULL
     assert L.h3_last_kernel_info(buf, 64) == h3.H3_OK

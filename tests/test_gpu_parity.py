@@ -79,7 +79,7 @@ def table_tensor(case):
 # stages
 # ---------------------------------------------------------------------------
 
-def test_linear_plain(h3):
+def test_linear_plain(h3, gemm_bn):
     g = torch.Generator().manual_seed(5)
     M, N, K = 200, 264, 320
     x = torch.randn(M, K, generator=g).to(torch.bfloat16)
@@ -95,7 +95,8 @@ def test_linear_plain(h3):
 def test_adaln_table(h3, name):
     c = get_case(name)
     out = torch.empty(c.T, 18 * c.w.shape.dim, dtype=torch.bfloat16, device="cuda")
-    h3.h3_adaln_table(c.cfg(h3), c.d_w["w_ada"], c.d_w["b_ada"], c.d_tc, out)
+    ws = torch.empty(h3.h3_adaln_table_workspace_bytes(c.cfg(h3)), dtype=torch.uint8, device="cuda")
+    h3.h3_adaln_table(c.cfg(h3), c.d_w["w_ada"], c.d_w["b_ada"], c.d_tc, out, ws)
     assert h3.h3_sync_check() == 0
     assert_close(to_np(out), c.ref["table"].reshape(c.T, -1), f"adaln_table[{name}]")
 
@@ -114,8 +115,18 @@ def test_adaln_modulate(h3, name, branch):
     assert_close(to_np(h), ref, f"modulate[{name},{branch}]")
 
 
+@pytest.fixture(params=["auto", "256", "192", "128"])
+def gemm_bn(request, monkeypatch):
+    """Every GEMM tile width: the library picks one per launch; H3_GEMM_BN forces it."""
+    if request.param == "auto":
+        monkeypatch.delenv("H3_GEMM_BN", raising=False)
+    else:
+        monkeypatch.setenv("H3_GEMM_BN", request.param)
+    return request.param
+
+
 @pytest.mark.parametrize("name", CASE_NAMES)
-def test_qkv_projection(h3, name):
+def test_qkv_projection(h3, name, gemm_bn):
     c = get_case(name)
     H = c.w.shape.n_heads
     out = torch.zeros(c.S, H, 3, 128, dtype=torch.bfloat16, device="cuda")
@@ -142,8 +153,18 @@ def test_rope_qknorm_standalone(h3, name):
     np.testing.assert_array_equal(o[:, :, 2], c.ref["v"])   # v untouched
 
 
+@pytest.fixture(params=["auto", "1", "2"])
+def attn_qtiles(request, monkeypatch):
+    """Both attention kernels (one or two query tiles per CTA); H3_ATTN_QTILES forces one."""
+    if request.param == "auto":
+        monkeypatch.delenv("H3_ATTN_QTILES", raising=False)
+    else:
+        monkeypatch.setenv("H3_ATTN_QTILES", request.param)
+    return request.param
+
+
 @pytest.mark.parametrize("name", CASE_NAMES)
-def test_attention(h3, name):
+def test_attention(h3, name, attn_qtiles):
     c = get_case(name)
     H, S = c.w.shape.n_heads, c.S
     buf = torch.stack([to_bf16(c.ref["q"]), to_bf16(c.ref["k"]), to_bf16(c.ref["v"])], dim=2).contiguous()
@@ -163,7 +184,7 @@ def test_attention(h3, name):
 
 
 @pytest.mark.parametrize("name", CASE_NAMES)
-def test_out_projection(h3, name):
+def test_out_projection(h3, name, gemm_bn):
     c = get_case(name)
     D = c.w.shape.dim
     x1 = torch.empty(c.S, D, dtype=torch.bfloat16, device="cuda")
@@ -183,7 +204,7 @@ def test_ffn_up_swiglu(h3, name):
 
 
 @pytest.mark.parametrize("name", CASE_NAMES)
-def test_ffn_down_residual(h3, name):
+def test_ffn_down_residual(h3, name, gemm_bn):
     c = get_case(name)
     y = torch.empty(c.S, c.w.shape.dim, dtype=torch.bfloat16, device="cuda")
     h3.h3_ffn_down_residual(c.cfg(h3), c.meta(h3), table_tensor(c), to_bf16(c.ref["a"]), c.d_w["w_fc2"], None,
@@ -311,3 +332,52 @@ def test_host_validation_launches_nothing(h3):
         h3.h3_attention(c.S, 4, c.d_x, c.d_x, c.d_x, 1540, 384, y)
     assert e.value.status == h3.H3_ERR_ALIGN
     assert "tcgen05" in h3.h3_last_kernel_info() or h3.h3_last_kernel_info() != ""
+
+
+# ---------------------------------------------------------------------------
+# attention core at 4096 packed rows (56 heads): QK-norm + RoPE prologue on the
+# GPU against the oracle, then attention on sampled query rows
+# ---------------------------------------------------------------------------
+
+@pytest.fixture(scope="module")
+def attn4096():
+    w = hi.WORKLOADS["attn4096"]
+    meta = hi.packed_metadata(w.layout, 1, 0)
+    ins = hi.attention_inputs(w.shape, w.layout.n_rows, 0)
+    qkv = to_np(ins["qkv"])
+    gq, gk = to_np(ins["q_norm_g"]), to_np(ins["k_norm_g"])
+    pos = meta["pos_thw"].numpy()
+    q, k, v = O.qk_norm_rope(qkv, pos, gq, gk)
+    return {"w": w, "ins": ins, "pos": meta["pos_thw"], "q": q, "k": k, "v": v}
+
+
+def test_rope_qknorm_4096(h3, attn4096):
+    d = attn4096
+    w = d["w"]
+    S, H = w.layout.n_rows, w.shape.n_heads
+    cfg = h3.make_config(w.shape.dim, H, w.shape.ffn_dim, w.shape.cond_dim)
+    buf = d["ins"]["qkv"].cuda()
+    h3.h3_rope_qknorm(cfg, S, d["pos"].cuda(), buf[:, :, 0], buf[:, :, 1], H * 384, 384,
+                      d["ins"]["q_norm_g"].cuda(), d["ins"]["k_norm_g"].cuda())
+    assert h3.h3_sync_check() == 0
+    o = to_np(buf)
+    assert_close(o[:, :, 0], d["q"], "rope4096.q")
+    assert_close(o[:, :, 1], d["k"], "rope4096.k")
+
+
+def test_attention_4096_sampled_rows(h3, attn4096, attn_qtiles):
+    d = attn4096
+    S, H = d["w"].layout.n_rows, d["w"].shape.n_heads
+    buf = torch.stack([to_bf16(d["q"]), to_bf16(d["k"]), to_bf16(d["v"])], dim=2).contiguous()
+    o = torch.empty(S, H * 128, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(H, S, dtype=torch.float32, device="cuda")
+    h3.h3_attention(S, H, buf[:, :, 0], buf[:, :, 1], buf[:, :, 2], H * 384, 384, o, lse)
+    assert h3.h3_sync_check() == 0
+    rows = np.unique(np.concatenate([np.arange(0, 3), np.linspace(0, S - 1, 93).astype(int), [S - 1]]))
+    ref = O.attention(d["q"], d["k"], d["v"], rows)
+    assert_close(to_np(o)[rows], ref, f"attention4096[{attn_qtiles}]")
+    lse_np = lse.cpu().numpy().astype(np.float64)
+    for h in range(0, H, 5):
+        q, k = d["q"][rows[:16], h], d["k"][:, h]
+        p_gpu = np.exp(q @ k.T / np.sqrt(128.0) - lse_np[h, rows[:16]][:, None])
+        assert np.abs(p_gpu - O.attention_probs(q, k)).max() <= 1e-3
