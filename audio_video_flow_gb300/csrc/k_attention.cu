@@ -219,20 +219,27 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         for (int c = 0; c < 128; ++c)
           if (c >= valid) sc[c] = -INFINITY;
       }
-      float mx = sc[0];
+      // eight independent partial maxima / sums (element c goes to partial
+      // c % 8), combined in a fixed tree: short dependency chains, fixed order
+      float mp[8];
 #pragma unroll
-      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, sc[c]);
+      for (int e = 0; e < 8; ++e) mp[e] = sc[e];
+#pragma unroll
+      for (int c = 8; c < 128; ++c) mp[c & 7] = fmaxf(mp[c & 7], sc[c]);
+      const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                             fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
       const float m_new = fmaxf(m_run, mx * sl2);
       uint32_t pk[64];
-      float rs = 0.0f;
+      float sp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c = 0; c < 128; c += 2) {
         const float e0 = exp2f(__fmaf_rn(sc[c], sl2, -m_new));
         const float e1 = exp2f(__fmaf_rn(sc[c + 1], sl2, -m_new));
-        rs += e0;
-        rs += e1;
+        sp[c & 7] += e0;
+        sp[(c + 1) & 7] += e1;
         pk[c >> 1] = pack_bf16x2(e0, e1);
       }
+      const float rs = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
       const float alpha = exp2f(m_run - m_new);
       l_run = __fmaf_rn(l_run, alpha, rs);
       if (j > 0) {
@@ -494,7 +501,11 @@ __global__ void __launch_bounds__(AT2_THREADS, 1)
       tc_fence_after();
       const int valid = S - j * KV_TILE;     // keys of this tile that exist (>= 1)
       // pass 1: row maximum
-      float mx = -INFINITY;
+      // eight independent partial maxima (fixed combination order)
+      float mp[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) mp[e] = -INFINITY;
+      const bool full_tile = valid >= KV_TILE;
 #pragma unroll 1
       for (int h2 = 0; h2 < 2; ++h2) {
         uint32_t a[32], b[32];
@@ -502,13 +513,21 @@ __global__ void __launch_bounds__(AT2_THREADS, 1)
         tmem_ld32(s_base + (uint32_t)(h2 * 64 + 32), b);
         tmem_ld_wait(a);
         tmem_ld_wait(b);
+        if (full_tile) {
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const float va = (h2 * 64 + c < valid) ? __uint_as_float(a[c]) : -INFINITY;
-          const float vb = (h2 * 64 + 32 + c < valid) ? __uint_as_float(b[c]) : -INFINITY;
-          mx = fmaxf(mx, fmaxf(va, vb));
+          for (int c = 0; c < 32; ++c)
+            mp[c & 7] = fmaxf(mp[c & 7], fmaxf(__uint_as_float(a[c]), __uint_as_float(b[c])));
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const float va = (h2 * 64 + c < valid) ? __uint_as_float(a[c]) : -INFINITY;
+            const float vb = (h2 * 64 + 32 + c < valid) ? __uint_as_float(b[c]) : -INFINITY;
+            mp[c & 7] = fmaxf(mp[c & 7], fmaxf(va, vb));
+          }
         }
       }
+      const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                             fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
       const float m_tile = mx * sl2;
       // lazy rescale: move the running maximum only when it grows by > 8
       const bool need = m_tile > m_used + kRescaleThreshold;
@@ -531,7 +550,7 @@ __global__ void __launch_bounds__(AT2_THREADS, 1)
         m_used = m_new;
       }
       // pass 2: P = 2^(s * scale_log2 - m_used) as bf16 over the S columns
-      float rs = 0.0f;
+      float sp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
       for (int h2 = 0; h2 < 2; ++h2) {
         uint32_t a[32], b[32];
@@ -539,30 +558,35 @@ __global__ void __launch_bounds__(AT2_THREADS, 1)
         tmem_ld32(s_base + (uint32_t)(h2 * 64 + 32), b);
         tmem_ld_wait(a);
         tmem_ld_wait(b);
+        if (!full_tile) {   // keys past the end of the sequence get probability 0
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            if (h2 * 64 + c >= valid) a[c] = __float_as_uint(-INFINITY);
+            if (h2 * 64 + 32 + c >= valid) b[c] = __float_as_uint(-INFINITY);
+          }
+        }
         uint32_t pk[32];
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
-          const int k0 = h2 * 64 + 2 * c;
-          const float e0 = k0 < valid ? ex2_approx(__fmaf_rn(__uint_as_float(a[2 * c]), sl2, -m_used)) : 0.0f;
-          const float e1 = k0 + 1 < valid ? ex2_approx(__fmaf_rn(__uint_as_float(a[2 * c + 1]), sl2, -m_used)) : 0.0f;
-          rs += e0;
-          rs += e1;
+          const float e0 = ex2_approx(__fmaf_rn(__uint_as_float(a[2 * c]), sl2, -m_used));
+          const float e1 = ex2_approx(__fmaf_rn(__uint_as_float(a[2 * c + 1]), sl2, -m_used));
+          sp[(2 * c) & 7] += e0;
+          sp[(2 * c + 1) & 7] += e1;
           pk[c] = pack_bf16x2(e0, e1);
         }
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
-          const int k0 = h2 * 64 + 32 + 2 * c;
-          const float e0 = k0 < valid ? ex2_approx(__fmaf_rn(__uint_as_float(b[2 * c]), sl2, -m_used)) : 0.0f;
-          const float e1 = k0 + 1 < valid ? ex2_approx(__fmaf_rn(__uint_as_float(b[2 * c + 1]), sl2, -m_used)) : 0.0f;
-          rs += e0;
-          rs += e1;
+          const float e0 = ex2_approx(__fmaf_rn(__uint_as_float(b[2 * c]), sl2, -m_used));
+          const float e1 = ex2_approx(__fmaf_rn(__uint_as_float(b[2 * c + 1]), sl2, -m_used));
+          sp[(2 * c) & 7] += e0;
+          sp[(2 * c + 1) & 7] += e1;
           pk[16 + c] = pack_bf16x2(e0, e1);
         }
         // keys [64 h2, 64 h2 + 64) -> packed columns [32 h2, 32 h2 + 32): only
         // columns this thread has already read are overwritten
         tmem_st32(s_base + (uint32_t)(h2 * 32), pk);
       }
-      l_run += rs;
+      l_run += ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();

@@ -11,8 +11,8 @@
 //               (the h3-metal README, section "Metal 4 and TensorOps paths",
 //               pairs the FC1 gate and up tiles so SwiGLU happens before the
 //               store)
-// Structure: persistent CTAs (one per SM), static tile order (m fastest, so
-// the CTAs running together share each weight tile through L2); warp 0 issues
+// Structure: persistent CTAs (one per SM), static grouped tile order (see
+// tile_coords); warp 0 issues
 // TMA loads into an mbarrier ring (4-6 stages depending on BN) and L2
 // prefetches further ahead; warp 1 issues tcgen05.mma from one thread into one
 // of two TMEM accumulators (2 x BN columns); warps 2-5 drain the other
@@ -108,6 +108,21 @@ struct BTile {
     }
   }
 };
+
+// Tile order: groups of GROUP_M m-tiles; inside a group m runs fastest, then
+// n.  The CTAs running at one time then share a few weight tiles and a group
+// of activation rows that both stay in L2 (with m fastest over all of M, a
+// tall activation matrix would be streamed from HBM once per weight column).
+constexpr int GROUP_M = 32;
+__device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int& m_blk, int& n_blk) {
+  const int per_group = GROUP_M * num_n;
+  const int g = tile / per_group;
+  const int m0 = g * GROUP_M;
+  const int gm = num_m - m0 < GROUP_M ? num_m - m0 : GROUP_M;
+  const int r = tile - g * per_group;
+  m_blk = m0 + r % gm;
+  n_blk = r / gm;
+}
 
 // ---------------------------------------------------------------------------
 // epilogues (4 warps, thread = one accumulator row)
@@ -405,7 +420,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       for (int s = 0; s < STAGES; ++s) last_phase[s] = -1;
       bool ok = true;
       for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-        const int m_blk = tile % args.num_m, n_blk = tile / args.num_m;
+        int m_blk, n_blk;
+        tile_coords(tile, args.num_m, args.num_n, m_blk, n_blk);
         int r[2];
         BT::rows(args, n_blk, r);
         for (int kb = 0; kb < args.num_k; ++kb) {
@@ -475,7 +491,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
       if (!mbar_wait(&acc_full[acc], acc_phase, abort_v)) break;
       tc_fence_after();
-      const int m_blk = tile % args.num_m, n_blk = tile / args.num_m;
+      int m_blk, n_blk;
+        tile_coords(tile, args.num_m, args.num_n, m_blk, n_blk);
       const uint32_t tacc = tmem_addr(tmem_base, (uint32_t)(q * 32), (uint32_t)(acc * BN));
       run_epilogue<EPI, BN>(args, tacc, m_blk, n_blk, row);
       tc_fence_before();

@@ -10,10 +10,7 @@
 //
 // rope_qknorm_kernel: standalone per-head Q/K RMSNorm + partial three-axis
 // MM-RoPE, in place (RFC section 2 rows "Q/K preprocessing", "Rotary
-// channels").  One warp per (row, head): lane l holds channels 4l..4l+3; lanes
-// 0-11 hold the first half of the 96 rotary channels and exchange with lanes
-// 12-23, which hold the partners j+48; lanes 24-31 hold the 32 pass-through
-// channels.
+// channels"); layout described at the kernel.
 #include "h3_device.cuh"
 #include "h3_internal.h"
 
@@ -95,68 +92,92 @@ cudaError_t launch_modulate(const ModulateArgs& a, cudaStream_t stream) {
 }
 
 // ---------------------------------------------------------------------------
+// One CTA per packed row.  The row's 48 rotation angles (bands t, h, w x 16
+// frequencies, fp32(pos) * omega_f in fp32) are computed once into shared
+// memory; then each warp takes whole heads: lanes 0-15 hold q, lanes 16-31
+// hold k, lane l of a half owning channels 8l..8l+7 (16-byte accesses).  The
+// rotation pairs channel j < 48 with j + 48, i.e. half-lane l < 6 with l + 6;
+// half-lanes 12-15 carry the 32 pass-through channels.  A warp issues the
+// loads of all its heads (up to 8 x 512 bytes) before it computes.
 __global__ void __launch_bounds__(256) rope_qknorm_kernel(const RopeArgs a) {
+  const int i = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long gw = (long long)blockIdx.x * 8 + warp;
-  if (gw >= (long long)a.S * a.H) return;
-  const int i = (int)(gw / a.H), h = (int)(gw % a.H);
-  float pos[3];
-  bool valid = true;
-#pragma unroll
-  for (int ax = 0; ax < 3; ++ax) {
-    const int p = a.pos[(size_t)i * 3 + ax];
-    if ((unsigned)p >= (1u << 24)) valid = false;
-    pos[ax] = (float)p;
+  __shared__ float s_cos[48], s_sin[48];
+  __shared__ int s_bad;
+  if (threadIdx.x == 0) s_bad = 0;
+  __syncthreads();
+  if (threadIdx.x < 48) {
+    const int band = threadIdx.x >> 4, f = threadIdx.x & 15;
+    const int p = a.pos[(size_t)i * 3 + band];
+    if ((unsigned)p >= (1u << 24)) s_bad = 1;
+    float sn, cs;
+    sincosf((float)p * a.omega[f], &sn, &cs);
+    s_cos[threadIdx.x] = cs;
+    s_sin[threadIdx.x] = sn;
   }
-  if (!valid) {
-    if (lane == 0) record_error(a.err, DEVERR_INDEX);
+  __syncthreads();
+  if (s_bad) {
+    if (threadIdx.x == 0) record_error(a.err, DEVERR_INDEX);
     return;
   }
-  // angles of this lane's four channels (lanes 0-23; both partners compute
-  // the same j = 4*(lane mod 12) + e)
-  float cs[4], sn[4];
-  const int jl = (lane < 12 ? lane : lane - 12) * 4;
+  const int hl = lane & 15;                 // lane within the q or k half
+  const bool is_k = lane >= 16;
+  const int partner = hl < 6 ? lane + 6 : (hl < 12 ? lane - 6 : lane);
+  float cs[8], sn[8], g[8];
 #pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const int j = jl + e;
-    const int band = j >> 4;
-    const float p = band == 0 ? pos[0] : (band == 1 ? pos[1] : pos[2]);
-    sincosf(p * a.omega[j & 15], &sn[e], &cs[e]);
+  for (int e = 0; e < 8; ++e) {
+    const int j = (hl < 12 ? (hl % 6) : 0) * 8 + e;   // rotation column of this channel
+    cs[e] = s_cos[j];
+    sn[e] = s_sin[j];
+    g[e] = __bfloat162float((is_k ? a.k_gain : a.q_gain)[hl * 8 + e]);
   }
-  const int partner = lane < 12 ? lane + 12 : (lane < 24 ? lane - 12 : lane);
+  __nv_bfloat16* base = (is_k ? a.k : a.q) + (size_t)i * a.row_stride + hl * 8;
+  // heads warp, warp + 8, ...: issue every load of this warp first
+  constexpr int kMaxHeadsPerWarp = 8;   // H <= 64 in one pass
+  for (int hb = 0; hb < a.H; hb += 8 * kMaxHeadsPerWarp) {
+    uint4 r[kMaxHeadsPerWarp];
 #pragma unroll
-  for (int part = 0; part < 2; ++part) {
-    __nv_bfloat16* base = (part ? a.k : a.q) + (size_t)i * a.row_stride + (size_t)h * a.head_stride;
-    const __nv_bfloat16* gain = part ? a.k_gain : a.q_gain;
-    uint2 raw = *reinterpret_cast<const uint2*>(base + lane * 4);
-    float v[4] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y)};
-    float ss = 0.0f;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) ss = __fmaf_rn(v[e], v[e], ss);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    const float inv = 1.0f / sqrtf(ss * (1.0f / 128.0f) + a.eps);
-    float n[4], out[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) n[e] = bf16_round((v[e] * inv) * __bfloat162float(gain[lane * 4 + e]));
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float other = __shfl_sync(0xffffffffu, n[e], partner);
-      if (lane < 12) out[e] = __fmaf_rn(n[e], cs[e], -(other * sn[e]));
-      else if (lane < 24) out[e] = __fmaf_rn(n[e], cs[e], other * sn[e]);
-      else out[e] = n[e];
+    for (int u = 0; u < kMaxHeadsPerWarp; ++u) {
+      const int h = hb + warp + 8 * u;
+      if (h < a.H) r[u] = *reinterpret_cast<const uint4*>(base + (size_t)h * a.head_stride);
     }
-    raw.x = pack_bf16x2(out[0], out[1]);
-    raw.y = pack_bf16x2(out[2], out[3]);
-    *reinterpret_cast<uint2*>(base + lane * 4) = raw;
+#pragma unroll
+    for (int u = 0; u < kMaxHeadsPerWarp; ++u) {
+      const int h = hb + warp + 8 * u;
+      if (h >= a.H) break;
+      const uint32_t w[4] = {r[u].x, r[u].y, r[u].z, r[u].w};
+      float v[8];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        v[2 * e] = bf16_lo(w[e]);
+        v[2 * e + 1] = bf16_hi(w[e]);
+      }
+      float ss = 0.0f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) ss = __fmaf_rn(v[e], v[e], ss);
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);   // within the half
+      const float inv = 1.0f / sqrtf(ss * (1.0f / 128.0f) + a.eps);
+      float n[8], out[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) n[e] = bf16_round((v[e] * inv) * g[e]);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float other = __shfl_sync(0xffffffffu, n[e], partner);
+        if (hl < 6) out[e] = __fmaf_rn(n[e], cs[e], -(other * sn[e]));
+        else if (hl < 12) out[e] = __fmaf_rn(n[e], cs[e], other * sn[e]);
+        else out[e] = n[e];
+      }
+      *reinterpret_cast<uint4*>(base + (size_t)h * a.head_stride) =
+          make_uint4(pack_bf16x2(out[0], out[1]), pack_bf16x2(out[2], out[3]), pack_bf16x2(out[4], out[5]),
+                     pack_bf16x2(out[6], out[7]));
+    }
   }
 }
 
 cudaError_t launch_rope_qknorm(const RopeArgs& a, cudaStream_t stream) {
-  const long long warps = (long long)a.S * a.H;
-  const unsigned blocks = (unsigned)((warps + 7) / 8);
-  rope_qknorm_kernel<<<blocks, 256, 0, stream>>>(a);
-  set_kernel_info("rope_qknorm_kernel warp-per-(row,head) rows=%d heads=%d", a.S, a.H);
+  rope_qknorm_kernel<<<a.S, 256, 0, stream>>>(a);
+  set_kernel_info("rope_qknorm_kernel cta-per-row angles-in-smem vec=16B rows=%d heads=%d", a.S, a.H);
   return cudaGetLastError();
 }
 
