@@ -70,6 +70,7 @@ def lib() -> ctypes.CDLL:
             "h3_blocks_forward": (i32, [cfgp, i32, wp, mp, vp, vp, vp, sz, vp]),
             "h3_adaln_table_workspace_bytes": (sz, [cfgp]),
             "h3_adaln_table": (i32, [cfgp, vp, vp, vp, i32, vp, vp, sz, vp]),
+            "h3_adaln_table_noalloc": (i32, [cfgp, vp, vp, vp, i32, vp, vp]),
             "h3_adaln_modulate": (i32, [cfgp, mp, vp, i32, vp, vp, vp, vp]),
             "h3_qkv_projection": (i32, [cfgp, mp, vp, vp, vp, vp, vp, vp, vp]),
             "h3_rope_qknorm": (i32, [cfgp, i32, vp, vp, vp, c_int64, c_int64, vp, vp, vp]),
@@ -188,6 +189,14 @@ def h3_adaln_table(cfg, w_ada, b_ada, t_cond, table_out, workspace, stream=None)
     _check(lib().h3_adaln_table(ctypes.byref(cfg), _ptr(w_ada), _ptr(b_ada), _ptr(t_cond), int(t_cond.shape[0]),
                                 _ptr(table_out), _ptr(workspace), workspace.numel() * workspace.element_size(),
                                 _stream(stream)), "h3_adaln_table")
+
+
+def h3_adaln_table_noalloc(cfg, w_ada, b_ada, t_cond, table_out, stream=None) -> None:
+    """h3_adaln_table for callers that cannot allocate device memory: the
+    library's own static scratch replaces the workspace (serialise calls)."""
+    _check(lib().h3_adaln_table_noalloc(ctypes.byref(cfg), _ptr(w_ada), _ptr(b_ada), _ptr(t_cond),
+                                        int(t_cond.shape[0]), _ptr(table_out), _stream(stream)),
+           "h3_adaln_table_noalloc")
 
 
 def h3_adaln_modulate(cfg, meta, table, branch: int, x, norm_g, h_out, stream=None) -> None:

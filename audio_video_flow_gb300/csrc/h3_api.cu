@@ -112,6 +112,7 @@ namespace {
 inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline bool al16n(const void* p) { return p == nullptr || al16(p); }
 inline size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
+constexpr int kMaxDevicesApi = 64;
 
 h3_status check_cfg(const h3_block_config* c) {
   if (!c) return H3_ERR_NULL;
@@ -363,6 +364,37 @@ h3_status check_block_args(const h3_block_config* cfg, const h3_block_weights* w
   return H3_OK;
 }
 
+// ---------------------------------------------------------------------------
+// Scratch of h3_adaln_table_noalloc: the bf16 SiLU rows [16][cond_dim] live in
+// a file-scope device array instead of caller memory.  Every GPU that loads
+// the library holds it (16 x 2816 x 2 = 90,112 bytes) until the process exits.
+// Host code may not pass the array's name to a kernel (on the host it is only
+// a stand-in symbol): its device address is looked up once per device.
+// ---------------------------------------------------------------------------
+constexpr int kNoAllocMaxCond = 2816;
+void* g_noalloc_scratch[kMaxDevicesApi] = {nullptr};
+std::mutex g_noalloc_mu;
+
+}  // namespace
+
+static __device__ __align__(256) __nv_bfloat16 h3_noalloc_silu_rows[kAdalnRows * kNoAllocMaxCond];
+
+namespace {
+// Device address of the array for the current device; the first call on a
+// device (made with that device current) performs the lookup.
+h3_status noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return H3_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevicesApi) return H3_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_scratch[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, h3_noalloc_silu_rows) != cudaSuccess || p == nullptr) return H3_ERR_CUDA;
+    g_noalloc_scratch[dev] = p;
+  }
+  *out = g_noalloc_scratch[dev];
+  return H3_OK;
+}
 }  // namespace
 
 // ===========================================================================
@@ -427,6 +459,22 @@ h3_status h3_adaln_table(const h3_block_config* cfg, const void* w_ada, const vo
     return H3_ERR_ALIGN;
   if (ws_bytes < adaln_scratch_bytes(*cfg)) return H3_ERR_WORKSPACE;
   return run_adaln_table(*cfg, w_ada, b_ada, t_cond, n_timesteps, table_out, workspace, stream);
+}
+
+h3_status h3_adaln_table_noalloc(const h3_block_config* cfg, const void* w_ada, const void* b_ada,
+                                 const float* t_cond, int32_t n_timesteps, void* table_out, cudaStream_t stream) {
+  h3_status s = check_cfg(cfg);
+  if (s != H3_OK) return s;
+  if (cfg->cond_dim > kNoAllocMaxCond) return H3_ERR_UNSUPPORTED;
+  if (!w_ada || !t_cond || !table_out) return H3_ERR_NULL;
+  if (n_timesteps < 1 || n_timesteps > kAdalnRows) return H3_ERR_UNSUPPORTED;
+  if (!al16(w_ada) || !al16n(b_ada) || !al16(table_out) || (reinterpret_cast<uintptr_t>(t_cond) & 3u))
+    return H3_ERR_ALIGN;
+  void* u = nullptr;
+  if ((s = noalloc_scratch(&u)) != H3_OK) return s;
+  // the SiLU kernel rewrites every row of the scratch (zeros beyond T), so no
+  // contents of an earlier call are read
+  return run_adaln_table(*cfg, w_ada, b_ada, t_cond, n_timesteps, table_out, u, stream);
 }
 
 h3_status h3_adaln_modulate(const h3_block_config* cfg, const h3_packed_meta* meta, const void* table,

@@ -170,6 +170,27 @@ h3_status h3_adaln_table(const h3_block_config *cfg, const void *w_ada, const vo
                          const float *t_cond, int32_t n_timesteps, void *table_out,
                          void *workspace, size_t ws_bytes, cudaStream_t stream);
 
+/* The AdaLN table of h3_adaln_table without any caller-provided scratch.
+ * The pages have no counterpart: this entry point exists for callers that
+ * cannot allocate device memory themselves (code handed only its input and
+ * output buffers by a host framework that owns the allocator, or a
+ * latency-critical loop that must not call cudaMalloc, which can synchronise
+ * the device).  Same arguments and result as h3_adaln_table, minus the
+ * workspace.  The scratch is a file-scope device array of 16 x 2816 bf16
+ * (90,112 bytes) that every GPU loading the library holds until exit; configs
+ * with cond_dim > 2816 or n_timesteps > 16 are rejected (H3_ERR_UNSUPPORTED).
+ * The first call on a device looks up the array's device address with that
+ * device current; make that first call before any stream capture.  Each
+ * GPU has its own copy of the array, and on one GPU every call shares it:
+ * calls that can overlap on the GPU (for example on two streams with no
+ * ordering between them) race, so serialise them.  Each call keeps its
+ * contents until the next; nothing has to be cleared first, because a call
+ * rewrites every scratch row it reads (rows past n_timesteps with zeros).
+ * Allocates nothing. */
+h3_status h3_adaln_table_noalloc(const h3_block_config *cfg, const void *w_ada, const void *b_ada,
+                                 const float *t_cond, int32_t n_timesteps, void *table_out,
+                                 cudaStream_t stream);
+
 /* RMSNorm + AdaLN modulation of one branch (RFC s2 fingerprint row "Block
  * norm", eps 1e-5; s5 h3_rmsnorm and adaln_row_gather):
  *   h[i] = bf16(x[i] / sqrt(mean(x[i]^2) + eps) * g * (1 + scale[r_i]) + shift[r_i])
