@@ -47,7 +47,7 @@ struct GemmCfg {
   static constexpr int B_STAGE_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
   static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + 256;
-  static constexpr int PREFETCH = STAGES;   // k-blocks of L2 prefetch beyond the ring
+  static constexpr int PREFETCH = 2 * STAGES;   // k-blocks of L2 prefetch ahead of the ring
 };
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {

@@ -102,8 +102,20 @@ cudaError_t launch_modulate(const ModulateArgs& a, cudaStream_t stream) {
 __global__ void __launch_bounds__(256) rope_qknorm_kernel(const RopeArgs a) {
   const int i = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int hl = lane & 15;                 // lane within the q or k half
+  const bool is_k = lane >= 16;
   __shared__ float s_cos[48], s_sin[48];
   __shared__ int s_bad;
+  // heads warp, warp + 8, ...: issue this warp's loads first (up to 8 x 512
+  // bytes), so their latency overlaps the angle set-up below
+  constexpr int kMaxHeadsPerWarp = 8;   // H <= 64 per pass
+  __nv_bfloat16* base = (is_k ? a.k : a.q) + (size_t)i * a.row_stride + hl * 8;
+  uint4 r[kMaxHeadsPerWarp];
+#pragma unroll
+  for (int u = 0; u < kMaxHeadsPerWarp; ++u) {
+    const int h = warp + 8 * u;
+    if (h < a.H) r[u] = *reinterpret_cast<const uint4*>(base + (size_t)h * a.head_stride);
+  }
   if (threadIdx.x == 0) s_bad = 0;
   __syncthreads();
   if (threadIdx.x < 48) {
@@ -120,8 +132,6 @@ __global__ void __launch_bounds__(256) rope_qknorm_kernel(const RopeArgs a) {
     if (threadIdx.x == 0) record_error(a.err, DEVERR_INDEX);
     return;
   }
-  const int hl = lane & 15;                 // lane within the q or k half
-  const bool is_k = lane >= 16;
   const int partner = hl < 6 ? lane + 6 : (hl < 12 ? lane - 6 : lane);
   float cs[8], sn[8], g[8];
 #pragma unroll
@@ -131,15 +141,13 @@ __global__ void __launch_bounds__(256) rope_qknorm_kernel(const RopeArgs a) {
     sn[e] = s_sin[j];
     g[e] = __bfloat162float((is_k ? a.k_gain : a.q_gain)[hl * 8 + e]);
   }
-  __nv_bfloat16* base = (is_k ? a.k : a.q) + (size_t)i * a.row_stride + hl * 8;
-  // heads warp, warp + 8, ...: issue every load of this warp first
-  constexpr int kMaxHeadsPerWarp = 8;   // H <= 64 in one pass
   for (int hb = 0; hb < a.H; hb += 8 * kMaxHeadsPerWarp) {
-    uint4 r[kMaxHeadsPerWarp];
+    if (hb > 0) {
 #pragma unroll
-    for (int u = 0; u < kMaxHeadsPerWarp; ++u) {
-      const int h = hb + warp + 8 * u;
-      if (h < a.H) r[u] = *reinterpret_cast<const uint4*>(base + (size_t)h * a.head_stride);
+      for (int u = 0; u < kMaxHeadsPerWarp; ++u) {
+        const int h = hb + warp + 8 * u;
+        if (h < a.H) r[u] = *reinterpret_cast<const uint4*>(base + (size_t)h * a.head_stride);
+      }
     }
 #pragma unroll
     for (int u = 0; u < kMaxHeadsPerWarp; ++u) {

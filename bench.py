@@ -35,8 +35,22 @@ KERNELS_PER_BLOCK = 9   # SiLU rows + AdaLN table + the seven stage kernels belo
 STAGES = ("adaln_table", "norm1_modulate", "qkv_qknorm_rope", "attention", "out_proj_residual",
           "norm2_modulate", "fc1_swiglu", "fc2_residual")
 # dram__bytes_read.sum + dram__bytes_write.sum per launch from an ncu capture
-# of the current kernel build, keyed "stage@workload"; None when not captured.
-TRAFFIC = {}
+# of the current kernel build (profiles/block505_kernels.md,
+# profiles/attention_attn4096.md), keyed "stage@workload"; absent when not
+# captured.  The 15,860-row attention value is the 4,096-row capture scaled by
+# the row count (its DRAM traffic is reading q, k, v and writing o once).
+TRAFFIC = {
+    "adaln_table@block505": 527_491_584,
+    "norm1_modulate@block505": 6_146_816,
+    "qkv_qknorm_rope@block505": 252_032_000,
+    "attention@block505": 21_766_656,
+    "out_proj_residual@block505": 93_319_936,
+    "norm2_modulate@block505": 6_146_816,
+    "fc1_swiglu@block505": 335_214_336,
+    "fc2_residual@block505": 177_720_064,
+    "attention@attn4096": 213_602_816,
+    "attention@denoiser15860": int(213_602_816 * 15860 / 4096),
+}
 
 
 # ---------------------------------------------------------------------------
