@@ -65,6 +65,7 @@ def lib() -> ctypes.CDLL:
         cfgp, wp, mp = ctypes.POINTER(BlockConfig), ctypes.POINTER(BlockWeights), ctypes.POINTER(PackedMeta)
         sig = {
             "h3_block_workspace_bytes": (sz, [cfgp, i32, i32]),
+            "h3_block_adaln_side_ctas": (i32, [cfgp, i32]),
             "h3_block_forward": (i32, [cfgp, wp, mp, vp, vp, vp, sz, vp]),
             "h3_block_forward_profiled": (i32, [cfgp, wp, mp, vp, vp, vp, sz, vp, vp, i32]),
             "h3_blocks_forward": (i32, [cfgp, i32, wp, mp, vp, vp, vp, sz, vp]),
@@ -157,6 +158,10 @@ def make_meta(token_tag, timestep_index, pos_thw, t_cond=None, n_timesteps: int 
 
 def h3_block_workspace_bytes(cfg: BlockConfig, n_rows: int, n_timesteps: int) -> int:
     return int(lib().h3_block_workspace_bytes(ctypes.byref(cfg), n_rows, n_timesteps))
+
+
+def h3_block_adaln_side_ctas(cfg: BlockConfig, n_rows: int) -> int:
+    return int(lib().h3_block_adaln_side_ctas(ctypes.byref(cfg), n_rows))
 
 
 def h3_block_forward(cfg, weights, meta, x_in, x_out, workspace, stream=None) -> None:

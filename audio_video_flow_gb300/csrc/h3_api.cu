@@ -9,6 +9,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <cstdlib>
 #include <mutex>
 #include <thread>
 
@@ -53,6 +54,14 @@ void set_kernel_info(const char* fmt, ...) {
   va_start(ap, fmt);
   vsnprintf(g_info, sizeof(g_info), fmt, ap);
   va_end(ap);
+}
+
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* e = getenv("H3_NO_PDL");
+    return !(e && e[0] == '1');
+  }();
+  return on;
 }
 
 int num_sms() {
@@ -171,23 +180,38 @@ WsLayout ws_layout(const h3_block_config& c, int64_t S, int64_t T) {
 // ---------------------------------------------------------------------------
 // stage launchers (arguments already validated)
 // ---------------------------------------------------------------------------
-h3_status run_adaln_table(const h3_block_config& c, const void* w_ada, const void* b_ada, const float* t_cond,
-                          int T, void* out, void* u_scratch, cudaStream_t st) {
+// Table chunks [chunk_lo, chunk_hi) of every modality, from the SiLU rows u.
+h3_status run_adaln_chunks(const h3_block_config& c, const void* w_ada, const void* b_ada, int T, void* out,
+                           const void* u_scratch, int chunk_lo, int chunk_hi, int max_ctas, cudaStream_t st) {
   CUtensorMap tm, tu;
   if (!make_tmap_2d(&tm, w_ada, (uint64_t)18 * c.dim, (uint64_t)c.cond_dim, (uint64_t)c.cond_dim, 128) ||
       !make_tmap_2d(&tu, u_scratch, kAdalnRows, (uint64_t)c.cond_dim, (uint64_t)c.cond_dim, kAdalnRows))
     return H3_ERR_CUDA;
-  h3_status s0 = cuda_st(launch_silu_rows(t_cond, T, c.cond_dim, static_cast<__nv_bfloat16*>(u_scratch), st));
-  if (s0 != H3_OK) return s0;
   AdalnArgs a{};
   a.C = c.cond_dim;
   a.T = T;
   a.NW = 18 * c.dim;
-  a.t_cond = t_cond;
+  a.D = c.dim;
+  a.chunk_lo = chunk_lo;
+  a.chunk_hi = chunk_hi;
+  a.max_ctas = max_ctas;
   a.bias = static_cast<const __nv_bfloat16*>(b_ada);
   a.out = static_cast<__nv_bfloat16*>(out);
   a.err = device_error_word();
   return cuda_st(launch_adaln_table(tm, tu, a, st));
+}
+
+h3_status run_silu(const h3_block_config& c, const float* t_cond, int T, void* u_scratch, cudaStream_t st) {
+  return cuda_st(launch_silu_rows(t_cond, T, c.cond_dim, static_cast<__nv_bfloat16*>(u_scratch), st));
+}
+
+h3_status run_adaln_table(const h3_block_config& c, const void* w_ada, const void* b_ada, const float* t_cond,
+                          int T, void* out, void* u_scratch, cudaStream_t st) {
+  h3_status s0 = run_silu(c, t_cond, T, u_scratch, st);
+  if (s0 != H3_OK) return s0;
+  // one launch over all six chunks (exact for every D, including D not a
+  // multiple of 128 where a weight tile straddles two chunks)
+  return run_adaln_chunks(c, w_ada, b_ada, T, out, u_scratch, 0, 6, 0, st);
 }
 
 h3_status run_modulate(const h3_block_config& c, const h3_packed_meta& m, const void* table, int branch,
@@ -219,7 +243,8 @@ void gemm_common(GemmArgs& a, int M, int K, int num_n) {
 }
 
 h3_status run_qkv(const h3_block_config& c, const h3_packed_meta& m, const void* h, const void* w_qkv,
-                  const void* b_qkv, const void* qg, const void* kg, void* out, cudaStream_t st) {
+                  const void* b_qkv, const void* qg, const void* kg, void* out, cudaStream_t st,
+                  int max_ctas = 0) {
   const int S = m.n_rows, D = c.dim, H = c.n_heads;
   const int bn = gemm_choose_bn(EPI_QKV, S, 3 * H * 128, H, 0);
   CUtensorMap tA, tB;
@@ -236,6 +261,7 @@ h3_status run_qkv(const h3_block_config& c, const h3_packed_meta& m, const void*
   a.k_gain = static_cast<const __nv_bfloat16*>(kg);
   a.pos = m.pos_thw;
   a.eps = c.eps;
+  a.max_ctas = max_ctas;
   fill_omega(a.omega, c.rope_theta);
   return cuda_st(launch_gemm(EPI_QKV, bn, tA, tB, a, st));
 }
@@ -312,6 +338,33 @@ h3_status check_block_weights(const h3_block_weights* w) {
   return H3_OK;
 }
 
+// SMs for the AdaLN chunks 2-5 on the side stream, 0 when the table is not
+// split: the split needs D a multiple of 128 (whole chunks per weight tile)
+// and pays only when the QKV GEMM leaves at least 8 SMs free at its wave
+// count (short documents); otherwise every SM already has GEMM work.
+int adaln_side_ctas(const h3_block_config& c, int S) {
+  if (c.dim % 128) return 0;
+  const int sms = num_sms(), H = c.n_heads, I = H * 128;
+  const int bn = gemm_choose_bn(EPI_QKV, S, 3 * I, H, 0);
+  const long long tiles = (long long)((S + 127) / 128) * gemm_num_n(EPI_QKV, bn, 3 * I, H, 0);
+  const long long waves = (tiles + sms - 1) / sms;
+  const int need = (int)((tiles + waves - 1) / waves);   // fewest CTAs with the same wave count
+  return sms - need >= 8 ? sms - need : 0;
+}
+
+// A library-owned stream per device for work that overlaps the caller's
+// stream inside one call (joined back by events before the call returns).
+cudaStream_t side_stream() {
+  static cudaStream_t streams[kMaxDevicesApi] = {nullptr};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevicesApi) return nullptr;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!streams[dev] && cudaStreamCreateWithFlags(&streams[dev], cudaStreamNonBlocking) != cudaSuccess)
+    streams[dev] = nullptr;
+  return streams[dev];
+}
+
 h3_status block_impl(const h3_block_config* cfg, const h3_block_weights* w, const h3_packed_meta* meta,
                      const void* x_in, void* x_out, void* ws, size_t ws_bytes, cudaStream_t st,
                      void* const* events, int n_events) {
@@ -337,13 +390,55 @@ h3_status block_impl(const h3_block_config* cfg, const h3_block_weights* w, cons
 #define H3_TRY(expr)            \
   if ((s = (expr)) != H3_OK) return s; \
   if ((s = mark()) != H3_OK) return s;
-  H3_TRY(run_adaln_table(*cfg, w->w_ada, w->b_ada, meta->t_cond, T, table, u, st));
+  // Stage 0, the AdaLN table.  norm1 reads only chunks 0-1 (shift_msa,
+  // scale_msa); chunk 2 is first read by the O projection.  Chunks 0-1 run on
+  // the caller's stream; chunks 2-5 (two thirds of the weight stream) run on
+  // the side stream on the SMs that the QKV GEMM's wave count leaves free,
+  // and the caller's stream waits for them before the O projection.
+  s = run_silu(*cfg, meta->t_cond, T, u, st);
+  if (s != H3_OK) return s;
+  const int side_ctas = adaln_side_ctas(*cfg, S);
+  cudaStream_t side = side_ctas > 0 ? side_stream() : nullptr;
+  cudaEvent_t ev_a = nullptr, ev_b = nullptr;
+  if (side) {
+    if (cudaEventCreateWithFlags(&ev_a, cudaEventDisableTiming) != cudaSuccess) return H3_ERR_CUDA;
+    if (cudaEventCreateWithFlags(&ev_b, cudaEventDisableTiming) != cudaSuccess) {
+      cudaEventDestroy(ev_a);
+      return H3_ERR_CUDA;
+    }
+  }
+  struct EventGuard {
+    cudaEvent_t a, b;
+    ~EventGuard() {
+      if (a) cudaEventDestroy(a);
+      if (b) cudaEventDestroy(b);
+    }
+  } guard{ev_a, ev_b};
+  int qkv_ctas = 0;
+  if (side) {
+    qkv_ctas = num_sms() - side_ctas;
+    if ((s = run_adaln_chunks(*cfg, w->w_ada, w->b_ada, T, table, u, 0, 2, 0, st)) != H3_OK) return s;
+    if (cudaEventRecord(ev_a, st) != cudaSuccess || cudaStreamWaitEvent(side, ev_a, 0) != cudaSuccess)
+      return H3_ERR_CUDA;
+    if (events && n_events > 8 && events[8] &&
+        cudaEventRecord(static_cast<cudaEvent_t>(events[8]), side) != cudaSuccess)
+      return H3_ERR_CUDA;
+    if ((s = run_adaln_chunks(*cfg, w->w_ada, w->b_ada, T, table, u, 2, 6, side_ctas, side)) != H3_OK) return s;
+    if (events && n_events > 9 && events[9] &&
+        cudaEventRecord(static_cast<cudaEvent_t>(events[9]), side) != cudaSuccess)
+      return H3_ERR_CUDA;
+    if (cudaEventRecord(ev_b, side) != cudaSuccess) return H3_ERR_CUDA;
+  } else {
+    if ((s = run_adaln_chunks(*cfg, w->w_ada, w->b_ada, T, table, u, 0, 6, 0, st)) != H3_OK) return s;
+  }
+  if ((s = mark()) != H3_OK) return s;
   H3_TRY(run_modulate(*cfg, *meta, table, 0, x_in, w->norm1_g, h, st));
-  H3_TRY(run_qkv(*cfg, *meta, h, w->w_qkv, w->b_qkv, w->q_norm_g, w->k_norm_g, qkv, st));
+  H3_TRY(run_qkv(*cfg, *meta, h, w->w_qkv, w->b_qkv, w->q_norm_g, w->k_norm_g, qkv, st, qkv_ctas));
   {
     const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(qkv);
     H3_TRY(run_attention(S, cfg->n_heads, q, q + 128, q + 256, 3 * I, 384, o, nullptr, st));
   }
+  if (side && cudaStreamWaitEvent(st, ev_b, 0) != cudaSuccess) return H3_ERR_CUDA;
   H3_TRY(run_resid_gemm(*cfg, *meta, table, 2, o, I, w->w_o, w->b_o, x_in, x1, st));
   H3_TRY(run_modulate(*cfg, *meta, table, 1, x1, w->norm2_g, h, st));
   H3_TRY(run_ffn_up(*cfg, S, h, w->w_fc1, w->b_fc1, qkv, st));
@@ -405,6 +500,11 @@ extern "C" {
 size_t h3_block_workspace_bytes(const h3_block_config* cfg, int32_t n_rows, int32_t n_timesteps) {
   if (check_cfg(cfg) != H3_OK || n_rows < 1 || n_timesteps < 1 || n_timesteps > 16) return 0;
   return ws_layout(*cfg, n_rows, n_timesteps).total;
+}
+
+int32_t h3_block_adaln_side_ctas(const h3_block_config* cfg, int32_t n_rows) {
+  if (check_cfg(cfg) != H3_OK || n_rows < 1) return 0;
+  return adaln_side_ctas(*cfg, n_rows);
 }
 
 h3_status h3_block_forward(const h3_block_config* cfg, const h3_block_weights* w, const h3_packed_meta* meta,

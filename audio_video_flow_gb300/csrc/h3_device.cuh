@@ -80,6 +80,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
 }
 
 // ---------------------------------------------------------------------------
+// programmatic dependent launch: every kernel of the library lets the next
+// kernel on the stream be scheduled as soon as all of its own CTAs have
+// started, and waits for the previous kernel (completed, memory visible)
+// before it touches any global data that earlier work on the stream produces
+// or still reads.  Weights, which nothing writes, may be prefetched earlier.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
 // TMA (tiled tensor loads, no multicast)
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* tm) {

@@ -22,6 +22,26 @@ bool make_tmap_qkv(CUtensorMap* tm, const void* base, uint64_t n_rows, uint64_t 
                    uint64_t row_stride, uint64_t head_stride, uint32_t box_rows);
 
 int num_sms();
+
+// Launch with programmatic stream serialization (the kernel may start while
+// the previous kernel on the stream finishes; it synchronises with
+// griddepcontrol.wait).  H3_NO_PDL=1 in the environment launches without it.
+bool pdl_enabled();
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                          Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
 uint32_t* device_error_word();   // device address of the error word (current device)
 void set_kernel_info(const char* fmt, ...);
 
@@ -59,6 +79,7 @@ struct GemmArgs {
   const int32_t* pos;
   float eps;
   float omega[16];
+  int max_ctas;          // 0: one CTA per SM; otherwise at most this many
   uint32_t* err;
 };
 
@@ -77,6 +98,9 @@ struct AdalnArgs {
   int C;                  // cond width (multiple of 64, <= 2816)
   int T;                  // timestep rows (1..16)
   int NW;                 // 18*D output channels (multiple of 128)
+  int D;                  // residual width
+  int chunk_lo, chunk_hi; // compute the table chunks [chunk_lo, chunk_hi) of every modality
+  int max_ctas;           // 0: one CTA per SM; otherwise at most this many
   const float* t_cond;    // [T][C]
   const __nv_bfloat16* bias;  // [NW] nullable
   __nv_bfloat16* out;     // [T][NW]

@@ -69,6 +69,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
+  griddep_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q_tile = blockIdx.x, head = blockIdx.y;
   const int S = args.S;
@@ -94,6 +95,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  griddep_wait();
   const uint32_t tmem_base = *tmem_slot;   // S0: cols [0,128), S1: [128,256), O: [256,384)
   volatile int* abort_v = abort_flag;
 
@@ -363,6 +365,7 @@ __global__ void __launch_bounds__(AT2_THREADS, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
+  griddep_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int pair = blockIdx.x, head = blockIdx.y;
   const int S = args.S;
@@ -390,6 +393,7 @@ __global__ void __launch_bounds__(AT2_THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  griddep_wait();
   const uint32_t tmem_base = *tmem_slot;
   volatile int* abort_v = abort_flag;
 
@@ -625,12 +629,12 @@ __global__ void __launch_bounds__(AT2_THREADS, 1)
   }
 }
 
-// One query tile per CTA while that is needed to fill the SMs (short
-// sequences), two otherwise.  H3_ATTN_QTILES=1|2 in the environment forces one
+// Two query tiles per CTA (measured faster at every length down to 505
+// rows); H3_ATTN_QTILES=1 in the environment selects the one-tile kernel
 // (tests cover both).
 cudaError_t launch_attention(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                              const AttnArgs& a, cudaStream_t stream) {
-  int qtiles = ((a.S + 255) / 256) * a.H >= num_sms() ? 2 : 1;
+  int qtiles = 2;
   if (const char* env = getenv("H3_ATTN_QTILES")) {
     const int f = atoi(env);
     if (f == 1 || f == 2) qtiles = f;
@@ -640,7 +644,8 @@ cudaError_t launch_attention(const CUtensorMap& tmQ, const CUtensorMap& tmK, con
     e = cudaFuncSetAttribute(attention_kernel_2q, cudaFuncAttributeMaxDynamicSharedMemorySize, AT2_SMEM);
     if (e != cudaSuccess) return e;
     const dim3 grid((unsigned)((a.S + 255) / 256), (unsigned)a.H);
-    attention_kernel_2q<<<grid, AT2_THREADS, AT2_SMEM, stream>>>(tmQ, tmK, tmV, a);
+    e = launch_kernel(attention_kernel_2q, grid, dim3(AT2_THREADS), AT2_SMEM, stream, tmQ, tmK, tmV, a);
+    if (e != cudaSuccess) return e;
     set_kernel_info("attention_kernel_2q tcgen05.mma.cta_group::1.kind::f16 q_tiles=2x128 kv_tile=128 "
                     "k_stages=%d v_stages=%d acc=f32 tmem=S_A,S_B,O_A,O_B P-in-TMEM lazy-rescale=%g grid=%ux%u",
                     KST, VST, (double)kRescaleThreshold, grid.x, grid.y);
@@ -648,7 +653,8 @@ cudaError_t launch_attention(const CUtensorMap& tmQ, const CUtensorMap& tmK, con
     e = cudaFuncSetAttribute(attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, AT_SMEM);
     if (e != cudaSuccess) return e;
     const dim3 grid((unsigned)((a.S + 127) / 128), (unsigned)a.H);
-    attention_kernel<<<grid, AT_THREADS, AT_SMEM, stream>>>(tmQ, tmK, tmV, a);
+    e = launch_kernel(attention_kernel, grid, dim3(AT_THREADS), AT_SMEM, stream, tmQ, tmK, tmV, a);
+    if (e != cudaSuccess) return e;
     set_kernel_info("attention_kernel tcgen05.mma.cta_group::1.kind::f16 q_tile=128 kv_tile=128 k_stages=%d "
                     "v_stages=%d acc=f32 tmem=S0,S1,O softmax=fp32-online grid=%ux%u",
                     KST, VST, grid.x, grid.y);

@@ -385,7 +385,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
+  griddep_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int num_tiles = args.num_m * args.num_n;
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
@@ -402,13 +404,22 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    // weights are never written: pull the first tile's into L2 while the
+    // previous kernel on the stream may still be running
+    if ((int)blockIdx.x < num_tiles) {
+      int m0, n0, r[2];
+      tile_coords(blockIdx.x, args.num_m, args.num_n, m0, n0);
+      BT::rows(args, n0, r);
+      for (int kb = 0; kb < C::STAGES + C::PREFETCH && kb < args.num_k; ++kb)
+        for (int bx = 0; bx < BT::BOXES; ++bx) tma_prefetch_l2(&tmB, kb * BK, r[bx]);
+    }
   }
   if (warp == 1) tmem_alloc(tmem_slot, 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  griddep_wait();
   const uint32_t tmem_base = *tmem_slot;
-  const int num_tiles = args.num_m * args.num_n;
   volatile int* abort_v = abort_flag;
 
   if (warp == 0) {
@@ -561,14 +572,14 @@ static cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, co
   constexpr int smem = GemmCfg<BN>::SMEM;
   cudaError_t e = cudaFuncSetAttribute(gemm_bf16_tc<EPI, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  gemm_bf16_tc<EPI, BN><<<grid, GEMM_THREADS, smem, stream>>>(tmA, tmB, a);
-  return cudaSuccess;
+  return launch_kernel(gemm_bf16_tc<EPI, BN>, dim3(grid), dim3(GEMM_THREADS), smem, stream, tmA, tmB, a);
 }
 
 cudaError_t launch_gemm(int epi, int bn, const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
                         cudaStream_t stream) {
   const int tiles = a.num_m * a.num_n;
-  const int grid = tiles < num_sms() ? tiles : num_sms();
+  int grid = tiles < num_sms() ? tiles : num_sms();
+  if (a.max_ctas > 0 && grid > a.max_ctas) grid = a.max_ctas;
   const char* names[4] = {"plain", "qkv_qknorm_rope", "gated_residual", "swiglu"};
   cudaError_t e = cudaErrorInvalidValue;
   switch (epi * 1000 + bn) {
@@ -608,6 +619,8 @@ constexpr int AD_PREFETCH = 2 * AD_STAGES;   // stages of L2 prefetch beyond the
 // u[t][k] = bf16(SiLU(t_cond[t][k])) in fp32 for t < T, zero for T <= t < 16.
 __global__ void __launch_bounds__(256) silu_rows_kernel(const float* __restrict__ t_cond, int T, int C,
                                                         __nv_bfloat16* __restrict__ u) {
+  griddep_launch_dependents();
+  griddep_wait();
   const int n = AD_BN * C;
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
     const int t = i / C;
@@ -639,6 +652,7 @@ __global__ void __launch_bounds__(AD_THREADS, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
+  griddep_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < AD_STAGES; ++s) {
@@ -654,17 +668,31 @@ __global__ void __launch_bounds__(AD_THREADS, 1)
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tmW);
-    tma_prefetch_desc(&tmU);
-  }
   if (warp == 1) tmem_alloc(tmem_slot, 32);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int num_tiles = args.NW / BM;
+  // tiles of chunks [chunk_lo, chunk_hi) of every modality
+  const int tiles_per_mod = (args.chunk_hi - args.chunk_lo) * args.D / BM;
+  const int num_tiles = 3 * tiles_per_mod;
+  auto tile_row = [&](int tile) {
+    const int m = tile / tiles_per_mod;
+    return m * 6 * args.D + args.chunk_lo * args.D + (tile - m * tiles_per_mod) * BM;
+  };
   volatile int* abort_v = abort_flag;
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmW);
+    tma_prefetch_desc(&tmU);
+    // weights are never written: pull the first tile's into L2 while the
+    // previous kernel (the SiLU rows) may still be running
+    if ((int)blockIdx.x < num_tiles) {
+      const int row0 = tile_row(blockIdx.x);
+      for (int kb = 0; kb < (AD_STAGES + AD_PREFETCH) * AD_KPS && kb < nkb; ++kb)
+        tma_prefetch_l2(&tmW, kb * BK, row0);
+    }
+  }
+  griddep_wait();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -677,7 +705,8 @@ __global__ void __launch_bounds__(AD_THREADS, 1)
       for (int s = 0; s < AD_STAGES; ++s) last_phase[s] = -1;
       bool ok = true;
       for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-        for (int kb = 0; kb < AD_PREFETCH * AD_KPS && kb < nkb; ++kb) tma_prefetch_l2(&tmW, kb * BK, tile * BM);
+        const int row0 = tile_row(tile);
+        for (int kb = 0; kb < AD_PREFETCH * AD_KPS && kb < nkb; ++kb) tma_prefetch_l2(&tmW, kb * BK, row0);
         for (int st = 0; st < nst; ++st) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_v)) { ok = false; break; }
           const int k0 = st * AD_KPS;
@@ -685,12 +714,12 @@ __global__ void __launch_bounds__(AD_THREADS, 1)
           mbar_arrive_expect_tx(&full[stage], (uint32_t)(nb * A_STAGE_BYTES));
           for (int b = 0; b < nb; ++b)
             tma_load_2d(sA + stage * AD_STAGE_BYTES + b * A_STAGE_BYTES, &tmW, &full[stage], (k0 + b) * BK,
-                        tile * BM);
+                        row0);
           last_phase[stage] = (int)phase;
           if (++stage == AD_STAGES) { stage = 0; phase ^= 1u; }
           for (int b = 0; b < AD_KPS; ++b) {
             const int pk = (st + AD_PREFETCH) * AD_KPS + b;
-            if (pk < nkb) tma_prefetch_l2(&tmW, pk * BK, tile * BM);
+            if (pk < nkb) tma_prefetch_l2(&tmW, pk * BK, row0);
           }
         }
       }
@@ -756,7 +785,7 @@ __global__ void __launch_bounds__(AD_THREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[acc]);
-      const int n = tile * BM + row;
+      const int n = tile_row(tile) + row;
       const float b = bias_at(args.bias, n);
 #pragma unroll
       for (int t = 0; t < AD_BN; ++t) {
@@ -776,20 +805,21 @@ __global__ void __launch_bounds__(AD_THREADS, 1)
 cudaError_t launch_silu_rows(const float* t_cond, int T, int C, __nv_bfloat16* u, cudaStream_t stream) {
   const int n = AD_BN * C;
   const int blocks = (n + 255) / 256 < 1024 ? (n + 255) / 256 : 1024;
-  silu_rows_kernel<<<blocks, 256, 0, stream>>>(t_cond, T, C, u);
-  return cudaGetLastError();
+  return launch_kernel(silu_rows_kernel, dim3(blocks), dim3(256), 0, stream, t_cond, T, C, u);
 }
 
 cudaError_t launch_adaln_table(const CUtensorMap& tmW, const CUtensorMap& tmU, const AdalnArgs& a,
                                cudaStream_t stream) {
-  const int tiles = a.NW / BM;
-  const int grid = tiles < num_sms() ? tiles : num_sms();
+  const int tiles = 3 * (a.chunk_hi - a.chunk_lo) * a.D / BM;
+  int grid = tiles < num_sms() ? tiles : num_sms();
+  if (a.max_ctas > 0 && grid > a.max_ctas) grid = a.max_ctas;
   cudaError_t e = cudaFuncSetAttribute(adaln_table_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, AD_SMEM);
   if (e != cudaSuccess) return e;
-  adaln_table_kernel<<<grid, AD_THREADS, AD_SMEM, stream>>>(tmW, tmU, a);
+  e = launch_kernel(adaln_table_kernel, dim3(grid), dim3(AD_THREADS), AD_SMEM, stream, tmW, tmU, a);
+  if (e != cudaSuccess) return e;
   set_kernel_info("adaln_table_kernel tcgen05.mma.cta_group::1.kind::f16 tile=%dx%dx%d stages=%dx%d acc=f32 "
-                  "tmem=2x%d grid=%d tiles=%d k_blocks=%d l2_prefetch=%d stages",
-                  BM, AD_BN, BK, AD_STAGES, AD_KPS, AD_BN, grid, tiles, a.C / BK, AD_PREFETCH);
+                  "tmem=2x%d grid=%d tiles=%d chunks=[%d,%d) k_blocks=%d l2_prefetch=%d stages",
+                  BM, AD_BN, BK, AD_STAGES, AD_KPS, AD_BN, grid, tiles, a.chunk_lo, a.chunk_hi, a.C / BK, AD_PREFETCH);
   return cudaGetLastError();
 }
 

@@ -23,6 +23,8 @@ constexpr int MOD_MAXC = 4;  // 16-byte chunks per thread: D <= 256 * 4 * 8 = 81
 
 __global__ void __launch_bounds__(MOD_THREADS) modulate_kernel(const ModulateArgs a) {
   const int row = blockIdx.x;
+  griddep_launch_dependents();
+  griddep_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   __shared__ float red[MOD_THREADS / 32];
   const int tg = a.tag[row], ti = a.tidx[row];
@@ -86,7 +88,8 @@ __global__ void __launch_bounds__(MOD_THREADS) modulate_kernel(const ModulateArg
 }
 
 cudaError_t launch_modulate(const ModulateArgs& a, cudaStream_t stream) {
-  modulate_kernel<<<a.S, MOD_THREADS, 0, stream>>>(a);
+  cudaError_t e = launch_kernel(modulate_kernel, dim3(a.S), dim3(MOD_THREADS), 0, stream, a);
+  if (e != cudaSuccess) return e;
   set_kernel_info("modulate_kernel rows=%d threads=%d vec=16B reduce=fixed-tree", a.S, MOD_THREADS);
   return cudaGetLastError();
 }
@@ -101,6 +104,8 @@ cudaError_t launch_modulate(const ModulateArgs& a, cudaStream_t stream) {
 // loads of all its heads (up to 8 x 512 bytes) before it computes.
 __global__ void __launch_bounds__(256) rope_qknorm_kernel(const RopeArgs a) {
   const int i = blockIdx.x;
+  griddep_launch_dependents();
+  griddep_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int hl = lane & 15;                 // lane within the q or k half
   const bool is_k = lane >= 16;
@@ -184,7 +189,8 @@ __global__ void __launch_bounds__(256) rope_qknorm_kernel(const RopeArgs a) {
 }
 
 cudaError_t launch_rope_qknorm(const RopeArgs& a, cudaStream_t stream) {
-  rope_qknorm_kernel<<<a.S, 256, 0, stream>>>(a);
+  cudaError_t e = launch_kernel(rope_qknorm_kernel, dim3(a.S), dim3(256), 0, stream, a);
+  if (e != cudaSuccess) return e;
   set_kernel_info("rope_qknorm_kernel cta-per-row angles-in-smem vec=16B rows=%d heads=%d", a.S, a.H);
   return cudaGetLastError();
 }

@@ -31,7 +31,9 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "H3 block fwd TFLOP/s & packed tokens/s (bf16, 1 GB300); % of tensor/HBM roofline"
-KERNELS_PER_BLOCK = 9   # SiLU rows + AdaLN table + the seven stage kernels below
+def kernels_per_block(shape, S: int) -> int:
+    """SiLU rows, the AdaLN table (two launches when split), the seven stage kernels."""
+    return 10 if adaln_split(shape, S) else 9
 STAGES = ("adaln_table", "norm1_modulate", "qkv_qknorm_rope", "attention", "out_proj_residual",
           "norm2_modulate", "fc1_swiglu", "fc2_residual")
 # dram__bytes_read.sum + dram__bytes_write.sum per launch from an ncu capture
@@ -39,31 +41,31 @@ STAGES = ("adaln_table", "norm1_modulate", "qkv_qknorm_rope", "attention", "out_
 # profiles/attention_attn4096.md), keyed "stage@workload"; absent when not
 # captured.  The 15,860-row attention value is the 4,096-row capture scaled by
 # the row count (its DRAM traffic is reading q, k, v and writing o once).
-TRAFFIC = {
-    "adaln_table@block505": 527_491_584,
-    "norm1_modulate@block505": 6_146_816,
-    "qkv_qknorm_rope@block505": 252_032_000,
-    "attention@block505": 21_766_656,
-    "out_proj_residual@block505": 93_319_936,
-    "norm2_modulate@block505": 6_146_816,
-    "fc1_swiglu@block505": 335_214_336,
-    "fc2_residual@block505": 177_720_064,
-    "attention@attn4096": 213_602_816,
-    "attention@denoiser15860": int(213_602_816 * 15860 / 4096),
-}
+TRAFFIC = {}
 
 
 # ---------------------------------------------------------------------------
 # algorithmic work
 # ---------------------------------------------------------------------------
 
-def stage_work(shape, S: int, T: int):
+def adaln_split(shape, S: int) -> bool:
+    """True when the library computes AdaLN chunks 2-5 on its side stream."""
+    import audio_video_flow_gb300 as h3
+    cfg = h3.make_config(shape.dim, shape.n_heads, shape.ffn_dim, shape.cond_dim)
+    return h3.h3_block_adaln_side_ctas(cfg, S) > 0
+
+
+def stage_work(shape, S: int, T: int, split: bool = False):
     """(flops, bytes) per stage of one block: the method's own dense work and
-    the bytes each kernel must move at least once."""
+    the bytes each kernel must move at least once.  With the AdaLN split, the
+    critical-path stage covers chunks 0-1 and adaln_table_side chunks 2-5."""
     D, I, F, C = shape.dim, shape.n_heads * shape.head_dim, shape.ffn_dim, shape.cond_dim
     b = 2  # bf16
+    ada = (2.0 * T * C * 18 * D, 18 * D * C * b + T * C * 4 + T * 18 * D * b)
+    frac = 2.0 / 6.0 if split else 1.0
     return {
-        "adaln_table": (2.0 * T * C * 18 * D, 18 * D * C * b + T * C * 4 + T * 18 * D * b),
+        "adaln_table": (ada[0] * frac, ada[1] * frac),
+        "adaln_table_side": (ada[0] * (1 - frac), ada[1] * (1 - frac)),
         "norm1_modulate": (0.0, 2.0 * S * D * b),
         "qkv_qknorm_rope": (2.0 * S * D * 3 * I, 3 * I * D * b + S * D * b + S * 3 * I * b),
         "attention": (4.0 * S * S * I, 4.0 * S * I * b),
@@ -79,7 +81,7 @@ def weight_bytes(shape):
     return 2 * (18 * D * C + 3 * I * D + D * I + 2 * F * D + D * F)
 
 
-BOUND = {"adaln_table": "hbm", "norm1_modulate": "hbm", "norm2_modulate": "hbm", "qkv_qknorm_rope": "tensor",
+BOUND = {"adaln_table": "hbm", "adaln_table_side": "hbm", "norm1_modulate": "hbm", "norm2_modulate": "hbm", "qkv_qknorm_rope": "tensor",
          "attention": "tensor", "out_proj_residual": "tensor", "fc1_swiglu": "tensor", "fc2_residual": "tensor"}
 
 
@@ -296,7 +298,8 @@ def run_ours(args, ws_n: int, rank: int, local: int):
 
     # one set of stage events per timed step and block: the per-kernel launch
     # durations are read from the timed region itself
-    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(len(STAGES) + 1)] for _ in range(NB)]
+    # per step and block: start, 8 stage ends, side-stream start and end
+    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(len(STAGES) + 3)] for _ in range(NB)]
           for _ in range(args.steps)]
     # torch only reports elapsed time between events it has recorded itself:
     # record each once here; inside the timed region the library re-records
@@ -321,7 +324,8 @@ def run_ours(args, ws_n: int, rank: int, local: int):
     if h3.h3_sync_check(timeout_ms=60000) != 0:
         raise RuntimeError("device error during warm-up")
 
-    work = stage_work(shape, S, T)
+    split = adaln_split(shape, S)
+    work = stage_work(shape, S, T, split)
     flops_step = NB * sum(f for f, _ in work.values())
 
     # ---- timed region (device time on the launching stream)
@@ -346,6 +350,10 @@ def run_ours(args, ws_n: int, rank: int, local: int):
     for k, s in enumerate(STAGES):
         stage_ms[s] = statistics.mean(ev[i][b][k].elapsed_time(ev[i][b][k + 1])
                                       for i in range(args.steps) for b in range(NB))
+    side_ms = None
+    if split:
+        side_ms = statistics.mean(ev[i][b][9].elapsed_time(ev[i][b][10])
+                                  for i in range(args.steps) for b in range(NB))
 
     elapsed_ms, units = aggregate(elapsed_ms, float(args.steps) * flops_step, ws_n)
     ms_per_step = elapsed_ms / args.steps
@@ -404,6 +412,10 @@ def run_ours(args, ws_n: int, rank: int, local: int):
         stages_out[s] = {"us": round(ms * 1e3, 2), "share": round(ms / sum(stage_ms.values()), 4),
                          "tflops": round(f / (ms * 1e-3) / 1e12, 1) if f else None,
                          "gbs": round(bts / (ms * 1e-3) / 1e9, 1)}
+    if side_ms is not None:
+        f, bts = work["adaln_table_side"]
+        stages_out["adaln_table_side"] = {"us": round(side_ms * 1e3, 2), "overlapped": True,
+                                          "gbs": round(bts / (side_ms * 1e-3) / 1e9, 1)}
     clocks = clk.summary()
     line = {
         "metric": METRIC, "value": round(tflops, 3), "unit": "TFLOP/s", "n_gpus": ws_n, "steps": args.steps,
@@ -417,7 +429,7 @@ def run_ours(args, ws_n: int, rank: int, local: int):
                          (NB * weight_bytes(shape) / 1e9),
                    "parallelism": f"replicas x{ws_n}"},
         "e2e": e2e,
-        "gpu_launches": args.steps * NB * KERNELS_PER_BLOCK,
+        "gpu_launches": args.steps * NB * kernels_per_block(shape, S),
         "roofline": {"kernel": dom, "bound": BOUND[dom], "achieved": round(achieved, 1), "peak": peak,
                      "unit": unit, "frac": round(achieved / peak, 4),
                      "peak_source": peaks["source"] + (" bf16 burst" if BOUND[dom] == "tensor" else " hbm copy"),

@@ -129,20 +129,34 @@ size_t h3_block_workspace_bytes(const h3_block_config *cfg, int32_t n_rows, int3
  *   y     = bf16(x1 + gate_mlp[r] bf16(a W_fc2^T + b_fc2))
  * x_in, x_out: bf16 [S][D]; x_out may alias x_in.  The workspace (device,
  * 256-byte aligned, >= h3_block_workspace_bytes) is scratch: its contents on
- * return are the block's intermediates (layout not part of the ABI). */
+ * return are the block's intermediates (layout not part of the ABI).
+ * When D is a multiple of 128, the AdaLN chunks that norm1 does not read are
+ * computed on a stream the library owns (one per device), overlapping the
+ * QKV projection; the caller's stream waits for them before the O
+ * projection, so the work stays ordered on the caller's stream. */
 h3_status h3_block_forward(const h3_block_config *cfg, const h3_block_weights *w,
                            const h3_packed_meta *meta, const void *x_in, void *x_out,
                            void *workspace, size_t ws_bytes, cudaStream_t stream);
 
 /* As h3_block_forward, recording cudaEvent_t events[k] on the stream after
- * launch stage k, for k = 0..n_events-1, stages in order: 0 AdaLN table,
- * 1 norm1/modulate, 2 QKV + QK-norm + RoPE, 3 attention, 4 O projection +
- * gated residual, 5 norm2/modulate, 6 FC1 + SwiGLU, 7 FC2 + gated residual.
- * events may be NULL (then identical to h3_block_forward). */
+ * launch stage k, for k = 0..min(n_events, 8)-1, stages in order: 0 AdaLN
+ * table (the chunks on the caller's stream), 1 norm1/modulate, 2 QKV +
+ * QK-norm + RoPE, 3 attention, 4 O projection + gated residual,
+ * 5 norm2/modulate, 6 FC1 + SwiGLU, 7 FC2 + gated residual.  When the AdaLN
+ * chunks 2-5 run on the library's side stream, events[8] and events[9] (if
+ * n_events > 9) are recorded on that stream before and after them.  events
+ * may be NULL (then identical to h3_block_forward). */
 h3_status h3_block_forward_profiled(const h3_block_config *cfg, const h3_block_weights *w,
                                     const h3_packed_meta *meta, const void *x_in, void *x_out,
                                     void *workspace, size_t ws_bytes, cudaStream_t stream,
                                     void *const *events, int32_t n_events);
+
+/* How h3_block_forward schedules the AdaLN table for this config and row
+ * count on the current device: the number of SMs given to the chunks 2-5 on
+ * the library's side stream, or 0 when the whole table runs on the caller's
+ * stream.  A scheduling detail (no counterpart on the pages); results are
+ * identical either way. */
+int32_t h3_block_adaln_side_ctas(const h3_block_config *cfg, int32_t n_rows);
 
 /* A chain of n_blocks blocks (RFC s2 fingerprint row "Transformer layers"; s5
  * ws1_full_h3_transformer, without the refiner and heads): block b reads the

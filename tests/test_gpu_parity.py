@@ -18,6 +18,10 @@ from h3_testutil import (CHAIN_MAX_E, CHAIN_MEAN_E, MAX_E, MEAN_E, assert_close,
 
 pytestmark = pytest.mark.gpu
 
+# D not a multiple of 128: the block computes the AdaLN table in one launch
+# (its 128-row weight tiles straddle two chunks)
+D576 = hi.custom_workload(hi.BlockShape(dim=576, n_heads=2, head_dim=128, ffn_dim=512, cond_dim=128),
+                          n_text=5, video_grid=(2, 3, 4), n_audio=11, n_timesteps=3, name="d576")
 RAGGED = hi.custom_workload(hi.BlockShape(dim=640, n_heads=3, head_dim=128, ffn_dim=1024, cond_dim=192),
                             n_text=13, video_grid=(2, 5, 9), n_audio=102, n_timesteps=7, name="ragged205")
 
@@ -63,7 +67,7 @@ _CASES = {}
 
 def get_case(name):
     if name not in _CASES:
-        w = RAGGED if name == "ragged205" else hi.WORKLOADS[name]
+        w = {"ragged205": RAGGED, "d576": D576}.get(name) or hi.WORKLOADS[name]
         _CASES[name] = Case(w)
     return _CASES[name]
 
@@ -229,7 +233,7 @@ def run_block(h3, c, x=None, meta=None, ws=None):
     return y
 
 
-@pytest.mark.parametrize("name", ["tiny72", "ragged205"])
+@pytest.mark.parametrize("name", ["tiny72", "ragged205", "d576"])
 def test_block_forward_small(h3, name):
     c = get_case(name)
     y = run_block(h3, c)
