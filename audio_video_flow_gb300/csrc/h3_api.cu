@@ -109,6 +109,21 @@ bool make_tmap_qkv(CUtensorMap* tm, const void* base, uint64_t n_rows, uint64_t 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// [S][H][128] bf16 view with the caller's row and head strides, unswizzled
+// boxes of {128 channels, box_heads heads, 1 row}.
+bool make_tmap_rope(CUtensorMap* tm, const void* base, uint64_t n_rows, uint64_t n_heads, uint64_t row_stride,
+                    uint64_t head_stride, uint32_t box_heads) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {128, n_heads, n_rows};
+  const cuuint64_t strides[2] = {head_stride * 2, row_stride * 2};
+  const cuuint32_t box[3] = {128, box_heads, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace h3
 
 using namespace h3;
@@ -236,7 +251,7 @@ h3_status run_modulate(const h3_block_config& c, const h3_packed_meta& m, const 
 void gemm_common(GemmArgs& a, int M, int K, int num_n) {
   a.M = M;
   a.K = K;
-  a.num_m = (M + 127) / 128;
+  a.num_m = gemm_m_tiles(M);
   a.num_n = num_n;
   a.num_k = K / 64;
   a.err = device_error_word();
@@ -345,10 +360,11 @@ h3_status check_block_weights(const h3_block_weights* w) {
 int adaln_side_ctas(const h3_block_config& c, int S) {
   if (c.dim % 128) return 0;
   const int sms = num_sms(), H = c.n_heads, I = H * 128;
+  const int slots = gemm_pair_slots();
   const int bn = gemm_choose_bn(EPI_QKV, S, 3 * I, H, 0);
-  const long long tiles = (long long)((S + 127) / 128) * gemm_num_n(EPI_QKV, bn, 3 * I, H, 0);
-  const long long waves = (tiles + sms - 1) / sms;
-  const int need = (int)((tiles + waves - 1) / waves);   // fewest CTAs with the same wave count
+  const long long tiles = (long long)gemm_m_tiles(S) * gemm_num_n(EPI_QKV, bn, 3 * I, H, 0);
+  const long long waves = (tiles + slots - 1) / slots;
+  const int need = 2 * (int)((tiles + waves - 1) / waves);   // fewest CTAs (pairs x 2) with the same wave count
   return sms - need >= 8 ? sms - need : 0;
 }
 
@@ -626,7 +642,14 @@ h3_status h3_rope_qknorm(const h3_block_config* cfg, int32_t n_rows, const int32
   a.eps = cfg->eps;
   fill_omega(a.omega, cfg->rope_theta);
   a.err = device_error_word();
-  return cuda_st(launch_rope_qknorm(a, stream));
+  CUtensorMap tq, tk;
+  const uint32_t hb = (uint32_t)rope_qknorm_heads_per_unit(a.H);
+  if (!make_tmap_rope(&tq, q, (uint64_t)n_rows, (uint64_t)a.H, (uint64_t)row_stride_elems,
+                      (uint64_t)head_stride_elems, hb) ||
+      !make_tmap_rope(&tk, k, (uint64_t)n_rows, (uint64_t)a.H, (uint64_t)row_stride_elems,
+                      (uint64_t)head_stride_elems, hb))
+    return H3_ERR_CUDA;
+  return cuda_st(launch_rope_qknorm(tq, tk, a, num_sms(), stream));
 }
 
 h3_status h3_attention(int32_t n_rows, int32_t n_heads, const void* q, const void* k, const void* v,

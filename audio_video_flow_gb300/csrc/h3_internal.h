@@ -27,26 +27,43 @@ int num_sms();
 // the previous kernel on the stream finishes; it synchronises with
 // griddepcontrol.wait).  H3_NO_PDL=1 in the environment launches without it.
 bool pdl_enabled();
+// cluster_x > 1 launches clusters of cluster_x CTAs along x.
 template <typename... KArgs, typename... Args>
-cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
-                          Args&&... args) {
+cudaError_t launch_kernel_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                                  int cluster_x, Args&&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (pdl_enabled()) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (cluster_x > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = (unsigned)cluster_x;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  cfg.numAttrs = n;
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                          Args&&... args) {
+  return launch_kernel_cluster(kernel, grid, block, smem, stream, 1, static_cast<Args&&>(args)...);
 }
 uint32_t* device_error_word();   // device address of the error word (current device)
 void set_kernel_info(const char* fmt, ...);
 
 // ---------------------------------------------------------------------------
-// GEMM (tcgen05, 128 x 256 x 64 tiles, persistent, warp-specialised)
+// GEMM (tcgen05 CTA pairs, 256 x BN x 64 tiles, persistent, warp-specialised)
 // ---------------------------------------------------------------------------
 enum GemmEpilogue : int {
   EPI_PLAIN = 0,   // y = bf16(acc + b)
@@ -88,6 +105,8 @@ struct GemmArgs {
 int gemm_choose_bn(int epi, int M, int N, int H, int F);
 int gemm_num_n(int epi, int bn, int N, int H, int F);
 int gemm_b_box_rows(int epi, int bn);
+int gemm_m_tiles(int M);        // 256-row tiles (one per CTA pair)
+int gemm_pair_slots();          // CTA pairs that can be resident at once on this GPU
 cudaError_t launch_gemm(int epi, int bn, const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
                         cudaStream_t stream);
 
@@ -153,6 +172,10 @@ struct RopeArgs {
   float omega[16];
   uint32_t* err;
 };
-cudaError_t launch_rope_qknorm(const RopeArgs& a, cudaStream_t stream);
+// q and k maps: 3-D [S][H][128] views with the caller's strides, box {128, heads per unit, 1}
+int rope_qknorm_heads_per_unit(int H);
+int rope_qknorm_smem_bytes(int H);
+cudaError_t launch_rope_qknorm(const CUtensorMap& tmq, const CUtensorMap& tmk, const RopeArgs& a, int num_sms,
+                               cudaStream_t stream);
 
 }  // namespace h3

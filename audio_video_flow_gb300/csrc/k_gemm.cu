@@ -1,6 +1,6 @@
 // tcgen05 GEMMs for the H3 block projections.
 //
-// gemm_bf16_tc<EPI, BN>: D[128 x BN] tiles of act[M][K] . W[rows][K]^T, bf16
+// gemm_bf16_tc<EPI, BN>: D[256 x BN] tiles of act[M][K] . W[rows][K]^T, bf16
 // in, fp32 accumulate in TMEM, with the epilogue fused per projection:
 //   EPI_PLAIN   y = bf16(acc + b)
 //   EPI_QKV     q and k columns of a head: per-head Q/K RMSNorm, then the
@@ -11,15 +11,22 @@
 //               (the h3-metal README, section "Metal 4 and TensorOps paths",
 //               pairs the FC1 gate and up tiles so SwiGLU happens before the
 //               store)
-// Structure: persistent CTAs (one per SM), static grouped tile order (see
-// tile_coords); warp 0 issues
-// TMA loads into an mbarrier ring (4-6 stages depending on BN) and L2
-// prefetches further ahead; warp 1 issues tcgen05.mma from one thread into one
-// of two TMEM accumulators (2 x BN columns); warps 2-5 drain the other
-// accumulator through tcgen05.ld and run the epilogue.  BN (256, 192 or 128)
-// is chosen per launch to fill the SMs; it changes the tiling, never the
-// reduction: every output element is the same fixed sequence of 16-deep MMAs
-// over K, so the result does not depend on M, BN or the grid (no split-K).
+// Structure: persistent CTA pairs (clusters of two, one CTA per SM), static
+// grouped tile order (see tile_coords).  A pair owns a 256 x BN tile: each CTA
+// stages its 128 rows of A and half (BN/2) of the tile's weight rows, and one
+// thread of the even CTA issues tcgen05.mma.cta_group::2 (M = 256), which
+// reads both CTAs' shared memory and accumulates each CTA's 128 rows in its
+// own TMEM.  Per SM this moves 32 KB of operands per 64-deep k-block instead
+// of the 48 KB a 128 x 256 tile on one SM needs, and leaves room for a deeper
+// ring (6-8 stages).  Warp 0 of each CTA issues its TMA loads (completion
+// counted on the even CTA's barrier) and L2 prefetches further ahead; warp 1
+// of the even CTA issues the MMAs into one of two TMEM accumulators
+// (2 x BN columns) and releases ring stages to both CTAs with a multicast
+// commit; warps 2-5 of each CTA drain the other accumulator through
+// tcgen05.ld and run the epilogue.  BN (256, 192 or 128) is chosen per
+// launch to fill the SMs; it changes the tiling, never the reduction: every
+// output element is the same fixed sequence of 16-deep MMAs over K, so the
+// result does not depend on M, BN or the grid (no split-K).
 //
 // adaln_table_kernel: the AdaLN projection.  Its M dimension is only T <= 16
 // timestep rows, so the GEMM runs transposed: the 18*D weight rows are the
@@ -41,11 +48,13 @@ constexpr int BM = 128, BK = 64;
 constexpr int A_STAGE_BYTES = BM * BK * 2;   // 16 KB
 constexpr int GEMM_THREADS = 192;
 
+// Per CTA of a pair: its 128 rows of A and BN/2 rows of B per 64-deep k-block.
 template <int BN>
 struct GemmCfg {
-  static constexpr int STAGES = BN == 256 ? 4 : (BN == 192 ? 5 : 6);
-  static constexpr int B_STAGE_BYTES = BN * BK * 2;
+  static constexpr int B_ROWS = BN / 2;
+  static constexpr int B_STAGE_BYTES = B_ROWS * BK * 2;
   static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+  static constexpr int STAGES = (196608 / STAGE_BYTES) > 8 ? 8 : (196608 / STAGE_BYTES);   // 6, 7, 8
   static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + 256;
   static constexpr int PREFETCH = 2 * STAGES;   // k-blocks of L2 prefetch ahead of the ring
 };
@@ -80,40 +89,25 @@ __device__ __forceinline__ float bias_at(const __nv_bfloat16* b, int i) {
   return b ? __bfloat162float(b[i]) : 0.0f;
 }
 
-// Weight-row origins of the B boxes of tile n_blk (one box of BN rows, or two
-// boxes of 128 rows when the two halves come from different places).
+// First weight row of the BN/2 B rows that CTA `rank` of the pair loads for
+// tile n_blk.  The tile's N columns are rank 0's rows then rank 1's rows.
 template <int EPI, int BN>
-struct BTile {
-  static constexpr int BOXES = (EPI == EPI_SWIGLU || (EPI == EPI_QKV && BN == 256)) ? 2 : 1;
-  static constexpr int BOX_ROWS = BN / BOXES;
-  __device__ static void rows(const GemmArgs& a, int n_blk, int (&r)[2]) {
-    if (EPI == EPI_SWIGLU) {
-      r[0] = n_blk * 128;              // gate rows
-      r[1] = a.F + n_blk * 128;        // value rows
-    } else if (EPI == EPI_QKV && BN == 256) {
-      if (n_blk < a.H) {               // q | k of head n_blk
-        r[0] = n_blk * 384;
-        r[1] = r[0] + 128;
-      } else {                         // v of heads 2p, 2p+1
-        const int p = n_blk - a.H;
-        r[0] = (2 * p) * 384 + 256;
-        r[1] = (2 * p + 1) * 384 + 256;
-      }
-    } else if (EPI == EPI_QKV) {       // BN == 128: q, k or v of one head
-      r[0] = (n_blk / 3) * 384 + (n_blk % 3) * 128;
-      r[1] = r[0];
-    } else {
-      r[0] = n_blk * BN;
-      r[1] = r[0];
-    }
+__device__ __forceinline__ int b_tile_row(const GemmArgs& a, int n_blk, uint32_t rank) {
+  if (EPI == EPI_SWIGLU) return (rank ? a.F : 0) + n_blk * 128;            // gate rows | value rows
+  if (EPI == EPI_QKV && BN == 256) {
+    if (n_blk < a.H) return n_blk * 384 + (int)rank * 128;                  // q | k of head n_blk
+    const int p = n_blk - a.H;
+    return (2 * p + (int)rank) * 384 + 256;                                 // v of heads 2p | 2p+1
   }
-};
+  if (EPI == EPI_QKV) return (n_blk / 3) * 384 + (n_blk % 3) * 128 + (int)rank * 64;   // q, k or v of a head
+  return n_blk * BN + (int)rank * (BN / 2);
+}
 
-// Tile order: groups of GROUP_M m-tiles; inside a group m runs fastest, then
-// n.  The CTAs running at one time then share a few weight tiles and a group
+// Tile order (tiles of 256 rows, one per CTA pair): groups of GROUP_M
+// m-tiles; inside a group m runs fastest, then n.  The CTAs running at one time then share a few weight tiles and a group
 // of activation rows that both stay in L2 (with m fastest over all of M, a
 // tall activation matrix would be streamed from HBM once per weight column).
-constexpr int GROUP_M = 32;
+constexpr int GROUP_M = 16;
 __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int& m_blk, int& n_blk) {
   const int per_group = GROUP_M * num_n;
   const int g = tile / per_group;
@@ -354,8 +348,7 @@ __device__ __forceinline__ void epi_qkv(const GemmArgs& a, uint32_t tacc, int m,
 }
 
 template <int EPI, int BN>
-__device__ __forceinline__ void run_epilogue(const GemmArgs& a, uint32_t tacc, int m_blk, int n_blk, int row) {
-  const int m = m_blk * BM + row;
+__device__ __forceinline__ void run_epilogue(const GemmArgs& a, uint32_t tacc, int m, int n_blk) {
   const bool valid = m < a.M;
   if (EPI == EPI_PLAIN) epi_plain<BN>(a, tacc, m, valid, n_blk);
   if (EPI == EPI_RESID) epi_resid<BN>(a, tacc, m, valid, n_blk);
@@ -370,23 +363,25 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     gemm_bf16_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const GemmArgs args) {
   using C = GemmCfg<BN>;
-  using BT = BTile<EPI, BN>;
   constexpr int STAGES = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * A_STAGE_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * C::B_STAGE_BYTES);
-  uint64_t* full = bars;
-  uint64_t* empty = bars + STAGES;
+  uint64_t* full = bars;                 // used in the even CTA: both CTAs' loads land on it
+  uint64_t* empty = bars + STAGES;       // both CTAs: released by the pair's MMA commit
   uint64_t* acc_full = bars + 2 * STAGES;
-  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* acc_empty = acc_full + 2;    // even CTA: 4 epilogue warps of each CTA
   uint64_t* drain = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
   griddep_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int pair = (int)(blockIdx.x >> 1), num_pairs = (int)(gridDim.x >> 1);
   const int num_tiles = args.num_m * args.num_n;
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -395,7 +390,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], 4);
+      mbar_init(&acc_empty[i], 8);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -404,119 +399,125 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
-    // weights are never written: pull the first tile's into L2 while the
-    // previous kernel on the stream may still be running
-    if ((int)blockIdx.x < num_tiles) {
-      int m0, n0, r[2];
-      tile_coords(blockIdx.x, args.num_m, args.num_n, m0, n0);
-      BT::rows(args, n0, r);
-      for (int kb = 0; kb < C::STAGES + C::PREFETCH && kb < args.num_k; ++kb)
-        for (int bx = 0; bx < BT::BOXES; ++bx) tma_prefetch_l2(&tmB, kb * BK, r[bx]);
+    // weights are never written: pull this CTA's half of the first tile into
+    // L2 while the previous kernel on the stream may still be running
+    if (pair < num_tiles) {
+      int m0, n0;
+      tile_coords(pair, args.num_m, args.num_n, m0, n0);
+      const int r0 = b_tile_row<EPI, BN>(args, n0, rank);
+      for (int kb = 0; kb < C::STAGES + C::PREFETCH && kb < args.num_k; ++kb) tma_prefetch_l2(&tmB, kb * BK, r0);
     }
   }
-  if (warp == 1) tmem_alloc(tmem_slot, 512);
+  if (warp == 1) tmem_alloc_pair(tmem_slot, 512);
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();          // barriers of both CTAs initialised, TMEM of both allocated
   tc_fence_after();
   griddep_wait();
   const uint32_t tmem_base = *tmem_slot;
   volatile int* abort_v = abort_flag;
 
   if (warp == 0) {
-    // ---------------------------------------------------------- TMA producer
+    // ---------------------------------------------------------- TMA producer (both CTAs)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
       int last_phase[STAGES];
       for (int s = 0; s < STAGES; ++s) last_phase[s] = -1;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+      const uint32_t full0 = mapa_shared(smem_u32(full), 0);   // the even CTA's full[0]
+      for (int tile = pair; tile < num_tiles && ok; tile += num_pairs) {
         int m_blk, n_blk;
         tile_coords(tile, args.num_m, args.num_n, m_blk, n_blk);
-        int r[2];
-        BT::rows(args, n_blk, r);
+        const int rb = b_tile_row<EPI, BN>(args, n_blk, rank);
+        const int ra = m_blk * 2 * BM + (int)rank * BM;
         for (int kb = 0; kb < args.num_k; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_v)) { ok = false; break; }
-          mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
-          uint8_t* b = sB + stage * C::B_STAGE_BYTES;
-          tma_load_2d(sA + stage * A_STAGE_BYTES, &tmA, &full[stage], kb * BK, m_blk * BM);
-          for (int bx = 0; bx < BT::BOXES; ++bx)
-            tma_load_2d(b + bx * BT::BOX_ROWS * 128, &tmB, &full[stage], kb * BK, r[bx]);
+          if (!mbar_wait_cluster(&empty[stage], phase ^ 1u, abort_v)) { ok = false; break; }
+          if (leader) mbar_arrive_expect_tx(&full[stage], 2 * C::STAGE_BYTES);
+          const uint32_t fb = full0 + (uint32_t)stage * 8u;
+          tma_load_2d_pair(sA + stage * A_STAGE_BYTES, &tmA, fb, kb * BK, ra);
+          tma_load_2d_pair(sB + stage * C::B_STAGE_BYTES, &tmB, fb, kb * BK, rb);
           last_phase[stage] = (int)phase;
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
           const int pk = kb + C::PREFETCH;
-          if (pk < args.num_k) {
-            for (int bx = 0; bx < BT::BOXES; ++bx) tma_prefetch_l2(&tmB, pk * BK, r[bx]);
-          }
+          if (pk < args.num_k) tma_prefetch_l2(&tmB, pk * BK, rb);
         }
       }
-      if (!ok) {  // let every load already issued land before the CTA exits
+      if (ok) {
+        // every stage handed out must come back (its release commit has landed)
+        // before the CTA may exit
+        for (int i = 0; i < STAGES && ok; ++i) {
+          if (last_phase[stage] >= 0 && !mbar_wait_cluster(&empty[stage], phase ^ 1u, abort_v)) ok = false;
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+      } else if (leader) {  // let every load already issued land before the pair exits
         for (int s = 0; s < STAGES; ++s)
           if (last_phase[s] >= 0) drain_wait(&full[s], (uint32_t)last_phase[s]);
       }
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16(BM, BN);
+    // ---------------------------------------------------------- MMA issuer (even CTA)
+    if (lane == 0 && leader) {
+      constexpr uint32_t idesc = idesc_bf16(2 * BM, BN);
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
       int it = 0;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++it) {
+      for (int tile = pair; tile < num_tiles && ok; tile += num_pairs, ++it) {
         const int acc = it & 1;
         const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
-        if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, abort_v)) { ok = false; break; }
+        if (!mbar_wait_cluster(&acc_empty[acc], acc_phase ^ 1u, abort_v)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
         for (int kb = 0; kb < args.num_k; ++kb) {
-          if (!mbar_wait(&full[stage], phase, abort_v)) { ok = false; break; }
+          if (!mbar_wait_cluster(&full[stage], phase, abort_v)) { ok = false; break; }
           tc_fence_after();
           const uint32_t a0 = smem_u32(sA + stage * A_STAGE_BYTES);
           const uint32_t b0 = smem_u32(sB + stage * C::B_STAGE_BYTES);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
-            mma_bf16_ss(d_tmem, sdesc_kmajor(a0 + k * 32), sdesc_kmajor(b0 + k * 32), idesc,
-                        (kb | k) != 0 ? 1u : 0u);
+            mma_bf16_ss_pair(d_tmem, sdesc_kmajor(a0 + k * 32), sdesc_kmajor(b0 + k * 32), idesc,
+                             (kb | k) != 0 ? 1u : 0u);
           }
-          mma_commit(&empty[stage]);
+          mma_commit_pair(&empty[stage], 0x3);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
-        mma_commit(&acc_full[acc]);
+        mma_commit_pair(&acc_full[acc], 0x3);
       }
       if (!ok) {  // all MMAs issued so far must finish before TMEM is released
-        mma_commit(drain);
+        mma_commit_pair(drain, 0x1);
         drain_wait(drain, 0);
       }
     }
     __syncwarp();
   } else {
-    // ---------------------------------------------------------- epilogue
+    // ---------------------------------------------------------- epilogue (both CTAs)
     const int q = warp & 3;
     const int row = q * 32 + lane;
+    const uint32_t acc_empty0 = mapa_shared(smem_u32(acc_empty), 0);
     int it = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
+    for (int tile = pair; tile < num_tiles; tile += num_pairs, ++it) {
       const int acc = it & 1;
       const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
-      if (!mbar_wait(&acc_full[acc], acc_phase, abort_v)) break;
+      if (!__all_sync(0xffffffffu, mbar_wait_cluster(&acc_full[acc], acc_phase, abort_v))) break;
       tc_fence_after();
       int m_blk, n_blk;
-        tile_coords(tile, args.num_m, args.num_n, m_blk, n_blk);
+      tile_coords(tile, args.num_m, args.num_n, m_blk, n_blk);
       const uint32_t tacc = tmem_addr(tmem_base, (uint32_t)(q * 32), (uint32_t)(acc * BN));
-      run_epilogue<EPI, BN>(args, tacc, m_blk, n_blk, row);
+      run_epilogue<EPI, BN>(args, tacc, m_blk * 2 * BM + (int)rank * BM + row, n_blk);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[acc]);
+      if (lane == 0) mbar_arrive_cluster(acc_empty0 + (uint32_t)acc * 8u);
     }
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync();          // no CTA of the pair still signals the other's barriers or TMEM
   if (threadIdx.x == 0 && *abort_v) record_error(args.err, DEVERR_TIMEOUT);
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, 512);
+    tmem_dealloc_pair(tmem_base, 512);
   }
 }
 
@@ -530,9 +531,11 @@ int gemm_num_n(int epi, int bn, int N, int H, int F) {
 }
 
 int gemm_b_box_rows(int epi, int bn) {
-  if (epi == EPI_SWIGLU || (epi == EPI_QKV && bn == 256)) return 128;
-  return bn;
+  (void)epi;
+  return bn / 2;   // each CTA of a pair loads half of the tile's weight rows
 }
+
+int gemm_m_tiles(int M) { return (M + 2 * BM - 1) / (2 * BM); }
 
 // Pick the tile width that minimises (waves x per-tile time) on this GPU.  A
 // tile's time is its width over the per-SM efficiency measured for that width
@@ -547,15 +550,15 @@ int gemm_choose_bn(int epi, int M, int N, int H, int F) {
     const int f = atoi(env);
     if (f == 256 || f == 128 || (f == 192 && epi != EPI_QKV)) return f;
   }
-  const int sms = num_sms();
-  const int num_m = (M + 127) / 128;
+  const int slots = gemm_pair_slots();
+  const int num_m = gemm_m_tiles(M);
   const int cands[3] = {256, 192, 128};
   int best = 256;
   long long best_cost = -1;
   for (int bn : cands) {
     if (epi == EPI_QKV && bn == 192) continue;
     const long long tiles = (long long)num_m * gemm_num_n(epi, bn, N, H, F);
-    const long long waves = (tiles + sms - 1) / sms;
+    const long long waves = (tiles + slots - 1) / slots;
     const long long eff_pct = bn == 256 ? 100 : (bn == 192 ? 95 : 65);
     const long long cost = waves * bn * 100 / eff_pct;
     if (best_cost < 0 || cost < best_cost) {
@@ -566,20 +569,52 @@ int gemm_choose_bn(int epi, int M, int N, int H, int F) {
   return best;
 }
 
+int gemm_pair_slots() {
+  static int slots[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+  if (!slots[dev]) {
+    // every instance holds one CTA per SM; the largest shared-memory footprint bounds them all
+    constexpr int smem = GemmCfg<192>::SMEM > GemmCfg<256>::SMEM ? GemmCfg<192>::SMEM : GemmCfg<256>::SMEM;
+    int n = 0;
+    if (cudaFuncSetAttribute(gemm_bf16_tc<EPI_PLAIN, 192>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) ==
+        cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(2 * 1024);
+      cfg.blockDim = dim3(GEMM_THREADS);
+      cfg.dynamicSmemBytes = smem;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&n, gemm_bf16_tc<EPI_PLAIN, 192>, &cfg) != cudaSuccess) n = 0;
+    }
+    cudaGetLastError();
+    slots[dev] = n > 0 ? n : num_sms() / 2;
+  }
+  return slots[dev];
+}
+
 template <int EPI, int BN>
 static cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, int grid,
                               cudaStream_t stream) {
   constexpr int smem = GemmCfg<BN>::SMEM;
   cudaError_t e = cudaFuncSetAttribute(gemm_bf16_tc<EPI, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  return launch_kernel(gemm_bf16_tc<EPI, BN>, dim3(grid), dim3(GEMM_THREADS), smem, stream, tmA, tmB, a);
+  return launch_kernel_cluster(gemm_bf16_tc<EPI, BN>, dim3(grid), dim3(GEMM_THREADS), smem, stream, 2, tmA, tmB,
+                               a);
 }
 
 cudaError_t launch_gemm(int epi, int bn, const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
                         cudaStream_t stream) {
   const int tiles = a.num_m * a.num_n;
-  int grid = tiles < num_sms() ? tiles : num_sms();
-  if (a.max_ctas > 0 && grid > a.max_ctas) grid = a.max_ctas;
+  const int slots = gemm_pair_slots();
+  int pairs = tiles < slots ? tiles : slots;
+  if (a.max_ctas > 0 && pairs > a.max_ctas / 2) pairs = a.max_ctas / 2 > 0 ? a.max_ctas / 2 : 1;
+  const int grid = 2 * pairs;
   const char* names[4] = {"plain", "qkv_qknorm_rope", "gated_residual", "swiglu"};
   cudaError_t e = cudaErrorInvalidValue;
   switch (epi * 1000 + bn) {
@@ -596,9 +631,10 @@ cudaError_t launch_gemm(int epi, int bn, const CUtensorMap& tmA, const CUtensorM
   }
   if (e != cudaSuccess) return e;
   const int stages = bn == 256 ? GemmCfg<256>::STAGES : (bn == 192 ? GemmCfg<192>::STAGES : GemmCfg<128>::STAGES);
-  set_kernel_info("gemm_bf16_tc<%s,%d> tcgen05.mma.cta_group::1.kind::f16 tile=%dx%dx%d stages=%d acc=f32 "
-                  "tmem=2x%d grid=%d tiles=%dx%d k_blocks=%d l2_prefetch=%d",
-                  names[epi], bn, BM, bn, BK, stages, bn, grid, a.num_m, a.num_n, a.num_k, stages);
+  set_kernel_info("gemm_bf16_tc<%s,%d> tcgen05.mma.cta_group::2.kind::f16 pair-tile=%dx%dx%d stages=%d acc=f32 "
+                  "tmem=2x%d grid=%d (pairs=%d of %d) tiles=%dx%d k_blocks=%d l2_prefetch=%d",
+                  names[epi], bn, 2 * BM, bn, BK, stages, bn, grid, pairs, slots, a.num_m, a.num_n, a.num_k,
+                  2 * stages);
   return cudaGetLastError();
 }
 
@@ -812,14 +848,26 @@ cudaError_t launch_adaln_table(const CUtensorMap& tmW, const CUtensorMap& tmU, c
                                cudaStream_t stream) {
   const int tiles = 3 * (a.chunk_hi - a.chunk_lo) * a.D / BM;
   int grid = tiles < num_sms() ? tiles : num_sms();
-  if (a.max_ctas > 0 && grid > a.max_ctas) grid = a.max_ctas;
+  // Sharing the GPU with a GEMM (max_ctas > 0): launch in clusters of two so
+  // that the CTAs take whole SM pairs and leave whole pairs to the GEMM's CTA
+  // pairs (single CTAs spread one per pair would strand the other SM).
+  int cluster = 1;
+  if (a.max_ctas > 0) {
+    if (grid > a.max_ctas) grid = a.max_ctas;
+    if (grid >= 2) {
+      grid &= ~1;
+      cluster = 2;
+    }
+  }
   cudaError_t e = cudaFuncSetAttribute(adaln_table_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, AD_SMEM);
   if (e != cudaSuccess) return e;
-  e = launch_kernel(adaln_table_kernel, dim3(grid), dim3(AD_THREADS), AD_SMEM, stream, tmW, tmU, a);
+  e = launch_kernel_cluster(adaln_table_kernel, dim3(grid), dim3(AD_THREADS), AD_SMEM, stream, cluster, tmW, tmU,
+                            a);
   if (e != cudaSuccess) return e;
   set_kernel_info("adaln_table_kernel tcgen05.mma.cta_group::1.kind::f16 tile=%dx%dx%d stages=%dx%d acc=f32 "
-                  "tmem=2x%d grid=%d tiles=%d chunks=[%d,%d) k_blocks=%d l2_prefetch=%d stages",
-                  BM, AD_BN, BK, AD_STAGES, AD_KPS, AD_BN, grid, tiles, a.chunk_lo, a.chunk_hi, a.C / BK, AD_PREFETCH);
+                  "tmem=2x%d grid=%d cluster=%d tiles=%d chunks=[%d,%d) k_blocks=%d l2_prefetch=%d stages",
+                  BM, AD_BN, BK, AD_STAGES, AD_KPS, AD_BN, grid, cluster, tiles, a.chunk_lo, a.chunk_hi, a.C / BK,
+                  AD_PREFETCH);
   return cudaGetLastError();
 }
 

@@ -10,7 +10,7 @@
 //
 // rope_qknorm_kernel: standalone per-head Q/K RMSNorm + partial three-axis
 // MM-RoPE, in place (RFC section 2 rows "Q/K preprocessing", "Rotary
-// channels"); layout described at the kernel.
+// channels"); a persistent TMA-fed kernel, structure described at the kernel.
 #include "h3_device.cuh"
 #include "h3_internal.h"
 
@@ -95,103 +95,214 @@ cudaError_t launch_modulate(const ModulateArgs& a, cudaStream_t stream) {
 }
 
 // ---------------------------------------------------------------------------
-// One CTA per packed row.  The row's 48 rotation angles (bands t, h, w x 16
-// frequencies, fp32(pos) * omega_f in fp32) are computed once into shared
-// memory; then each warp takes whole heads: lanes 0-15 hold q, lanes 16-31
-// hold k, lane l of a half owning channels 8l..8l+7 (16-byte accesses).  The
-// rotation pairs channel j < 48 with j + 48, i.e. half-lane l < 6 with l + 6;
-// half-lanes 12-15 carry the 32 pass-through channels.  A warp issues the
-// loads of all its heads (up to 8 x 512 bytes) before it computes.
-__global__ void __launch_bounds__(256) rope_qknorm_kernel(const RopeArgs a) {
-  const int i = blockIdx.x;
-  griddep_launch_dependents();
-  griddep_wait();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int hl = lane & 15;                 // lane within the q or k half
-  const bool is_k = lane >= 16;
-  __shared__ float s_cos[48], s_sin[48];
-  __shared__ int s_bad;
-  // heads warp, warp + 8, ...: issue this warp's loads first (up to 8 x 512
-  // bytes), so their latency overlaps the angle set-up below
-  constexpr int kMaxHeadsPerWarp = 8;   // H <= 64 per pass
-  __nv_bfloat16* base = (is_k ? a.k : a.q) + (size_t)i * a.row_stride + hl * 8;
-  uint4 r[kMaxHeadsPerWarp];
-#pragma unroll
-  for (int u = 0; u < kMaxHeadsPerWarp; ++u) {
-    const int h = warp + 8 * u;
-    if (h < a.H) r[u] = *reinterpret_cast<const uint4*>(base + (size_t)h * a.head_stride);
-  }
-  if (threadIdx.x == 0) s_bad = 0;
-  __syncthreads();
-  if (threadIdx.x < 48) {
-    const int band = threadIdx.x >> 4, f = threadIdx.x & 15;
-    const int p = a.pos[(size_t)i * 3 + band];
-    if ((unsigned)p >= (1u << 24)) s_bad = 1;
-    float sn, cs;
-    sincosf((float)p * a.omega[f], &sn, &cs);
-    s_cos[threadIdx.x] = cs;
-    s_sin[threadIdx.x] = sn;
-  }
-  __syncthreads();
-  if (s_bad) {
-    if (threadIdx.x == 0) record_error(a.err, DEVERR_INDEX);
-    return;
-  }
-  const int partner = hl < 6 ? lane + 6 : (hl < 12 ? lane - 6 : lane);
-  float cs[8], sn[8], g[8];
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    const int j = (hl < 12 ? (hl % 6) : 0) * 8 + e;   // rotation column of this channel
-    cs[e] = s_cos[j];
-    sn[e] = s_sin[j];
-    g[e] = __bfloat162float((is_k ? a.k_gain : a.q_gain)[hl * 8 + e]);
-  }
-  for (int hb = 0; hb < a.H; hb += 8 * kMaxHeadsPerWarp) {
-    if (hb > 0) {
-#pragma unroll
-      for (int u = 0; u < kMaxHeadsPerWarp; ++u) {
-        const int h = hb + warp + 8 * u;
-        if (h < a.H) r[u] = *reinterpret_cast<const uint4*>(base + (size_t)h * a.head_stride);
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < kMaxHeadsPerWarp; ++u) {
-      const int h = hb + warp + 8 * u;
-      if (h >= a.H) break;
-      const uint32_t w[4] = {r[u].x, r[u].y, r[u].z, r[u].w};
-      float v[8];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        v[2 * e] = bf16_lo(w[e]);
-        v[2 * e + 1] = bf16_hi(w[e]);
-      }
-      float ss = 0.0f;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) ss = __fmaf_rn(v[e], v[e], ss);
-#pragma unroll
-      for (int o = 8; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);   // within the half
-      const float inv = 1.0f / sqrtf(ss * (1.0f / 128.0f) + a.eps);
-      float n[8], out[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) n[e] = bf16_round((v[e] * inv) * g[e]);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float other = __shfl_sync(0xffffffffu, n[e], partner);
-        if (hl < 6) out[e] = __fmaf_rn(n[e], cs[e], -(other * sn[e]));
-        else if (hl < 12) out[e] = __fmaf_rn(n[e], cs[e], other * sn[e]);
-        else out[e] = n[e];
-      }
-      *reinterpret_cast<uint4*>(base + (size_t)h * a.head_stride) =
-          make_uint4(pack_bf16x2(out[0], out[1]), pack_bf16x2(out[2], out[3]), pack_bf16x2(out[4], out[5]),
-                     pack_bf16x2(out[6], out[7]));
-    }
-  }
+// Persistent CTAs (one per SM); a unit is the q and k of one packed row for a
+// block of up to 64 heads.  Warp 0 streams units through a ring of shared
+// memory stages with two 3-D TMA loads each ([row][head][128] boxes of q and
+// of k) and, while they fly, computes the row's 48 rotation angles (bands
+// t, h, w x 16 frequencies, fp32(pos) * omega_f in fp32) into the stage.
+// Warps 1..16 take whole heads of a stage: lanes 0-15 hold q, lanes 16-31
+// hold k, lane l of a half owning channels 8l..8l+7.  The rotation pairs
+// channel j < 48 with j + 48, i.e. half-lane l < 6 with l + 6 (one shuffle);
+// half-lanes 12-15 carry the 32 pass-through channels.  Results go straight
+// back to global memory (in place) with 16-byte stores.
+constexpr int ROPE_CWARPS = 16;
+constexpr int ROPE_THREADS = 32 * (ROPE_CWARPS + 1);
+constexpr int ROPE_MAX_HB = 64;
+
+__host__ __device__ inline int rope_heads_per_unit(int H) {
+  const int nb = (H + ROPE_MAX_HB - 1) / ROPE_MAX_HB;
+  return (H + nb - 1) / nb;
+}
+__host__ __device__ inline int rope_stage_bytes(int hb) { return 2 * hb * 256; }
+__host__ __device__ inline int rope_stages(int hb) {
+  const int st = (192 * 1024) / rope_stage_bytes(hb);
+  return st > 8 ? 8 : st;
+}
+__host__ __device__ inline int rope_smem_bytes(int hb) {
+  const int st = rope_stages(hb);
+  return 128 + st * rope_stage_bytes(hb) + st * (96 * 4 + 16) + 2 * st * 8 + 16;
 }
 
-cudaError_t launch_rope_qknorm(const RopeArgs& a, cudaStream_t stream) {
-  cudaError_t e = launch_kernel(rope_qknorm_kernel, dim3(a.S), dim3(256), 0, stream, a);
+__global__ void __launch_bounds__(ROPE_THREADS, 1)
+    rope_qknorm_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                       const RopeArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
+  const int HB = rope_heads_per_unit(a.H);
+  const int nhb = (a.H + HB - 1) / HB;
+  const int STAGES = rope_stages(HB);
+  const int SB = rope_stage_bytes(HB);
+  uint8_t* tiles = smem;                                            // [STAGES][q|k][HB][128] bf16
+  float* ang = reinterpret_cast<float*>(tiles + STAGES * SB);        // [STAGES][cos 48 | sin 48]
+  int* bad = reinterpret_cast<int*>(ang + STAGES * 96);              // [STAGES]
+  uint64_t* full = reinterpret_cast<uint64_t*>(
+      reinterpret_cast<uint8_t*>(ang) + STAGES * (96 * 4 + 16));     // 8-byte aligned
+  uint64_t* empty = full + STAGES;
+  int* abort_flag = reinterpret_cast<int*>(empty + STAGES);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long units = (long long)a.S * nhb;
+
+  griddep_launch_dependents();
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < STAGES; ++st) {
+      mbar_init(&full[st], 2);               // expect_tx arrival + angles-ready arrival
+      mbar_init(&empty[st], ROPE_CWARPS);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (threadIdx.x == 32) {
+    tma_prefetch_desc(&tmq);
+    tma_prefetch_desc(&tmk);
+  }
+  __syncthreads();
+  griddep_wait();
+  volatile int* abort_v = abort_flag;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    int stage = 0;
+    uint32_t phase = 0;
+    int last_phase[8];
+    for (int st = 0; st < 8; ++st) last_phase[st] = -1;
+    bool ok = true;
+    for (long long u = blockIdx.x; u < units; u += gridDim.x) {
+      const int row = (int)(u / nhb), h0 = (int)(u % nhb) * HB;
+      // every lane waits (and so acquires the stage); the outcome is made warp-uniform
+      if (!__all_sync(0xffffffffu, mbar_wait(&empty[stage], phase ^ 1u, abort_v))) { ok = false; break; }
+      if (lane == 0) {
+        uint8_t* t = tiles + stage * SB;
+        mbar_arrive_expect_tx(&full[stage], (uint32_t)SB);
+        tma_load_3d(t, &tmq, &full[stage], 0, h0, row);
+        tma_load_3d(t + SB / 2, &tmk, &full[stage], 0, h0, row);
+        last_phase[stage] = (int)phase;
+      }
+      if (lane < 16) {
+        int anybad = 0;
+#pragma unroll
+        for (int band = 0; band < 3; ++band) {
+          const int p = a.pos[(size_t)row * 3 + band];
+          anybad |= (unsigned)p >= (1u << 24);
+          float sn, cs;
+          sincosf((float)p * a.omega[lane], &sn, &cs);
+          ang[stage * 96 + band * 16 + lane] = cs;
+          ang[stage * 96 + 48 + band * 16 + lane] = sn;
+        }
+        anybad = __any_sync(0x0000ffffu, anybad);
+        if (lane == 0) bad[stage] = anybad;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&full[stage]);
+      if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+    }
+    if (!ok && lane == 0) {   // let every load already issued land before the CTA exits
+      const uint64_t t0 = globaltimer();
+      for (int st = 0; st < STAGES; ++st) {
+        if (last_phase[st] < 0) continue;
+        while (!mbar_try_wait(&full[st], (uint32_t)last_phase[st]))
+          if (globaltimer() - t0 > kWaitLimitNs) break;
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ compute
+    const int cw = warp - 1;
+    const int hl = lane & 15;
+    const bool is_k = lane >= 16;
+    const int partner = hl < 6 ? lane + 6 : (hl < 12 ? lane - 6 : lane);
+    const int col = hl < 12 ? (hl % 6) * 8 : 0;                 // first rotation column of the lane
+    const float sgn = hl < 6 ? -1.0f : 1.0f;
+    float g[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) g[e] = __bfloat162float((is_k ? a.k_gain : a.q_gain)[hl * 8 + e]);
+    __nv_bfloat16* gbase = is_k ? a.k : a.q;
+    int stage = 0;
+    uint32_t phase = 0;
+    for (long long u = blockIdx.x; u < units; u += gridDim.x) {
+      const int row = (int)(u / nhb), h0 = (int)(u % nhb) * HB;
+      if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], phase, abort_v))) break;
+      if (bad[stage]) {
+        if (cw == 0 && lane == 0) record_error(a.err, DEVERR_INDEX);
+      } else {
+        float cs[8], sn[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          if (hl < 12) {
+            cs[e] = ang[stage * 96 + col + e];
+            sn[e] = sgn * ang[stage * 96 + 48 + col + e];
+          } else {
+            cs[e] = 1.0f;
+            sn[e] = 0.0f;
+          }
+        }
+        const uint8_t* t = tiles + stage * SB + (is_k ? SB / 2 : 0) + hl * 16;
+        // two heads per pass (h and h + ROPE_CWARPS), interleaved for ILP
+        for (int h = cw; h < HB && h0 + h < a.H; h += 2 * ROPE_CWARPS) {
+          const int hh[2] = {h, h + ROPE_CWARPS};
+          const bool second = hh[1] < HB && h0 + hh[1] < a.H;   // warp-uniform
+          float v[2][8];
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            uint4 r = make_uint4(0u, 0u, 0u, 0u);
+            if (j == 0 || second) r = *reinterpret_cast<const uint4*>(t + hh[j] * 256);
+            const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              v[j][2 * e] = bf16_lo(w[e]);
+              v[j][2 * e + 1] = bf16_hi(w[e]);
+            }
+          }
+          float ss[2] = {0.0f, 0.0f};
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) ss[j] = __fmaf_rn(v[j][e], v[j][e], ss[j]);
+#pragma unroll
+          for (int o = 8; o > 0; o >>= 1)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) ss[j] += __shfl_xor_sync(0xffffffffu, ss[j], o);   // within the half
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const float inv = 1.0f / sqrtf(ss[j] * (1.0f / 128.0f) + a.eps);
+            float n[8], out[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) n[e] = bf16_round((v[j][e] * inv) * g[e]);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const float other = __shfl_sync(0xffffffffu, n[e], partner);
+              out[e] = __fmaf_rn(n[e], cs[e], other * sn[e]);
+            }
+            if (j == 0 || second)
+              *reinterpret_cast<uint4*>(gbase + (size_t)row * a.row_stride + (size_t)(h0 + hh[j]) * a.head_stride +
+                                        hl * 8) =
+                  make_uint4(pack_bf16x2(out[0], out[1]), pack_bf16x2(out[2], out[3]),
+                             pack_bf16x2(out[4], out[5]), pack_bf16x2(out[6], out[7]));
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[stage]);
+      if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && *abort_v) record_error(a.err, DEVERR_TIMEOUT);
+}
+
+int rope_qknorm_smem_bytes(int H) { return rope_smem_bytes(rope_heads_per_unit(H)); }
+int rope_qknorm_heads_per_unit(int H) { return rope_heads_per_unit(H); }
+
+cudaError_t launch_rope_qknorm(const CUtensorMap& tmq, const CUtensorMap& tmk, const RopeArgs& a,
+                               int num_sms, cudaStream_t stream) {
+  const int hb = rope_heads_per_unit(a.H);
+  const int smem = rope_smem_bytes(hb);
+  cudaError_t e = cudaFuncSetAttribute(rope_qknorm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  set_kernel_info("rope_qknorm_kernel cta-per-row angles-in-smem vec=16B rows=%d heads=%d", a.S, a.H);
+  const long long units = (long long)a.S * ((a.H + hb - 1) / hb);
+  const int grid = (int)(units < num_sms ? units : num_sms);
+  e = launch_kernel(rope_qknorm_kernel, dim3(grid), dim3(ROPE_THREADS), smem, stream, tmq, tmk, a);
+  if (e != cudaSuccess) return e;
+  set_kernel_info("rope_qknorm_kernel persistent tma-3d units=%lld heads/unit=%d stages=%d grid=%d", units, hb,
+                  rope_stages(hb), grid);
   return cudaGetLastError();
 }
 

@@ -369,6 +369,41 @@ def test_rope_qknorm_4096(h3, attn4096):
     assert_close(o[:, :, 1], d["k"], "rope4096.k")
 
 
+def test_rope_qknorm_separate_buffers_two_head_blocks(h3):
+    """q and k in separate, row-padded buffers (head stride 128, row stride
+    H*128 + 64) and 70 heads, more than one shared-memory unit holds: the
+    heads of a row are split into two units of 35."""
+    S, H = 301, 70
+    pos = hi.packed_metadata(hi.PackedLayout(9, (4, 6, 11), 28), 1, 3)["pos_thw"]
+    assert pos.shape[0] == S
+    g = torch.Generator().manual_seed(11)
+    q = torch.randn(S, H, 128, generator=g).to(torch.bfloat16)
+    k = torch.randn(S, H, 128, generator=g).to(torch.bfloat16)
+    gq = (1 + 0.1 * torch.randn(128, generator=g)).to(torch.bfloat16)
+    gk = (1 + 0.1 * torch.randn(128, generator=g)).to(torch.bfloat16)
+    qkv = np.stack([to_np(q), to_np(k), np.zeros((S, H, 128))], axis=2)
+    ref_q, ref_k, _ = O.qk_norm_rope(qkv, pos.numpy(), to_np(gq), to_np(gk))
+    rs = H * 128 + 64
+    dq = torch.zeros(S, rs, dtype=torch.bfloat16, device="cuda")
+    dk = torch.zeros(S, rs, dtype=torch.bfloat16, device="cuda")
+    dq[:, :H * 128] = q.reshape(S, -1).cuda()
+    dk[:, :H * 128] = k.reshape(S, -1).cuda()
+    cfg = h3.make_config(512, H, 1536, 256)
+    h3.h3_rope_qknorm(cfg, S, pos.cuda(), dq, dk, rs, 128, gq.cuda(), gk.cuda())
+    assert h3.h3_sync_check() == 0
+    assert "heads/unit=35" in h3.h3_last_kernel_info()
+    assert_close(to_np(dq[:, :H * 128]).reshape(S, H, 128), ref_q, "rope70.q")
+    assert_close(to_np(dk[:, :H * 128]).reshape(S, H, 128), ref_k, "rope70.k")
+    assert not dq[:, H * 128:].any() and not dk[:, H * 128:].any()   # padding untouched
+    # a position out of range is reported and its row is left as it was
+    bad = pos.clone()
+    bad[17, 1] = 1 << 24
+    dq2 = dq.clone()
+    h3.h3_rope_qknorm(cfg, S, bad.cuda(), dq2, dk.clone(), rs, 128, gq.cuda(), gk.cuda())
+    assert h3.h3_sync_check() == h3.H3_ERR_INDEX
+    assert torch.equal(dq2[17], dq[17])
+
+
 def test_attention_4096_sampled_rows(h3, attn4096, attn_qtiles):
     d = attn4096
     S, H = d["w"].layout.n_rows, d["w"].shape.n_heads
