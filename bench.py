@@ -36,12 +36,21 @@ def kernels_per_block(shape, S: int) -> int:
     return 10 if adaln_split(shape, S) else 9
 STAGES = ("adaln_table", "norm1_modulate", "qkv_qknorm_rope", "attention", "out_proj_residual",
           "norm2_modulate", "fc1_swiglu", "fc2_residual")
-# dram__bytes_read.sum + dram__bytes_write.sum per launch from an ncu capture
-# of the current kernel build (profiles/block505_kernels.md,
-# profiles/attention_attn4096.md), keyed "stage@workload"; absent when not
-# captured.  The 15,860-row attention value is the 4,096-row capture scaled by
-# the row count (its DRAM traffic is reading q, k, v and writing o once).
-TRAFFIC = {}
+# dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant
+# kernel, from ncu captures of the current kernel build (profiles/
+# block505_launches.md, block1824_traffic.md, attn16384_traffic.md,
+# attention_attn4096.md), keyed "stage@workload"; absent when not captured.
+# Attention's DRAM traffic is reading q, k, v and writing o once (K/V re-reads
+# hit L2), so the 32,768- and 15,860-row values are the 16,384-row capture
+# scaled by the row count.
+TRAFFIC = {
+    "qkv_qknorm_rope@block505": 252453632,
+    "fc1_swiglu@block1824": 380734720,
+    "attention@attn4096": 214066176,
+    "attention@attn16384": 916994048,
+    "attention@attn32768": 1833988096,
+    "attention@denoiser15860": 887666358,
+}
 
 
 # ---------------------------------------------------------------------------
