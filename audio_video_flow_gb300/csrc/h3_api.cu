@@ -248,6 +248,13 @@ h3_status run_modulate(const h3_block_config& c, const h3_packed_meta& m, const 
   return cuda_st(launch_modulate(a, st));
 }
 
+void gemm_set_plan(GemmArgs& a, const GemmPlan& p) {
+  a.b_rows = p.b_rows;
+  a.nw1 = p.nw1;
+  a.ncnt1 = p.ncnt1;
+  a.nw2 = p.nw2;
+}
+
 void gemm_common(GemmArgs& a, int M, int K, int num_n) {
   a.M = M;
   a.K = K;
@@ -268,6 +275,7 @@ h3_status run_qkv(const h3_block_config& c, const h3_packed_meta& m, const void*
     return H3_ERR_CUDA;
   GemmArgs a{};
   gemm_common(a, S, D, gemm_num_n(EPI_QKV, bn, 3 * H * 128, H, 0));
+  a.b_rows = gemm_b_box_rows(EPI_QKV, bn);
   a.out = static_cast<__nv_bfloat16*>(out);
   a.ldo = 3 * H * 128;
   a.bias = static_cast<const __nv_bfloat16*>(b_qkv);
@@ -301,13 +309,13 @@ h3_status run_resid_gemm(const h3_block_config& c, const h3_packed_meta& m, cons
                          const void* act, int K, const void* w, const void* b, const void* x, void* out,
                          cudaStream_t st) {
   const int S = m.n_rows, D = c.dim;
-  const int bn = gemm_choose_bn(EPI_RESID, S, D, 0, 0);
+  const GemmPlan pl = gemm_plan(EPI_RESID, S, D, 0, 0);
   CUtensorMap tA, tB;
-  if (!make_tmap_2d(&tA, act, S, K, K, 128) ||
-      !make_tmap_2d(&tB, w, D, K, K, (uint32_t)gemm_b_box_rows(EPI_RESID, bn)))
+  if (!make_tmap_2d(&tA, act, S, K, K, 128) || !make_tmap_2d(&tB, w, D, K, K, (uint32_t)pl.b_rows))
     return H3_ERR_CUDA;
   GemmArgs a{};
-  gemm_common(a, S, K, gemm_num_n(EPI_RESID, bn, D, 0, 0));
+  gemm_common(a, S, K, pl.num_n);
+  gemm_set_plan(a, pl);
   a.out = static_cast<__nv_bfloat16*>(out);
   a.ldo = D;
   a.bias = static_cast<const __nv_bfloat16*>(b);
@@ -320,7 +328,7 @@ h3_status run_resid_gemm(const h3_block_config& c, const h3_packed_meta& m, cons
   a.T = m.n_timesteps;
   a.tag = m.token_tag;
   a.tidx = m.timestep_index;
-  return cuda_st(launch_gemm(EPI_RESID, bn, tA, tB, a, st));
+  return cuda_st(launch_gemm(EPI_RESID, pl.bn, tA, tB, a, st));
 }
 
 h3_status run_ffn_up(const h3_block_config& c, int S, const void* h, const void* w1, const void* b1, void* out,
@@ -331,6 +339,7 @@ h3_status run_ffn_up(const h3_block_config& c, int S, const void* h, const void*
     return H3_ERR_CUDA;
   GemmArgs a{};
   gemm_common(a, S, D, gemm_num_n(EPI_SWIGLU, 256, 0, 0, F));
+  a.b_rows = gemm_b_box_rows(EPI_SWIGLU, 256);
   a.out = static_cast<__nv_bfloat16*>(out);
   a.ldo = F;
   a.bias = static_cast<const __nv_bfloat16*>(b1);
@@ -708,18 +717,18 @@ h3_status h3_linear(int32_t M, int32_t N, int32_t K, const void* x, const void* 
   if (K % 64 || N % 8) return H3_ERR_UNSUPPORTED;
   if (!x || !w || !y) return H3_ERR_NULL;
   if (!al16(x) || !al16(w) || !al16n(b) || !al16(y)) return H3_ERR_ALIGN;
-  const int bn = gemm_choose_bn(EPI_PLAIN, M, N, 0, 0);
+  const GemmPlan pl = gemm_plan(EPI_PLAIN, M, N, 0, 0);
   CUtensorMap tA, tB;
-  if (!make_tmap_2d(&tA, x, M, K, K, 128) ||
-      !make_tmap_2d(&tB, w, N, K, K, (uint32_t)gemm_b_box_rows(EPI_PLAIN, bn)))
+  if (!make_tmap_2d(&tA, x, M, K, K, 128) || !make_tmap_2d(&tB, w, N, K, K, (uint32_t)pl.b_rows))
     return H3_ERR_CUDA;
   GemmArgs a{};
-  gemm_common(a, M, K, gemm_num_n(EPI_PLAIN, bn, N, 0, 0));
+  gemm_common(a, M, K, pl.num_n);
+  gemm_set_plan(a, pl);
   a.out = static_cast<__nv_bfloat16*>(y);
   a.ldo = N;
   a.bias = static_cast<const __nv_bfloat16*>(b);
   a.n_valid = N;
-  return cuda_st(launch_gemm(EPI_PLAIN, bn, tA, tB, a, stream));
+  return cuda_st(launch_gemm(EPI_PLAIN, pl.bn, tA, tB, a, stream));
 }
 
 h3_status h3_sync_check(cudaStream_t stream, int32_t timeout_ms) {

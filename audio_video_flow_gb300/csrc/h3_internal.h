@@ -97,11 +97,27 @@ struct GemmArgs {
   float eps;
   float omega[16];
   int max_ctas;          // 0: one CTA per SM; otherwise at most this many
+  // column tiling (see GemmPlan): b_rows weight rows per CTA and k-block;
+  // nw1 = 0 for uniform tiles of BN columns
+  int b_rows;
+  int nw1, ncnt1, nw2;
   uint32_t* err;
 };
 
-// Tile width (256, 192 or 128 columns) for a GEMM of M rows; the number of N
-// tiles and the row count of one B box (for the tensor map) at that width.
+// Column tiling of one GEMM launch.  Uniform: num_n tiles of bn columns.
+// Balanced (plain and residual epilogues, when one wave of uniform tiles
+// would leave CTA pairs idle): the N columns of each 256-row tile are split
+// into ncnt1 tiles of nw1 columns followed by tiles of nw2 = nw1 - 16, as many
+// as the resident pairs allow for all row tiles at once; bn is then the
+// compiled width that holds nw1.  b_rows: weight rows one CTA loads per
+// k-block (the B box of the tensor map).
+struct GemmPlan {
+  int bn, num_n, b_rows;
+  int nw1, ncnt1, nw2;
+};
+GemmPlan gemm_plan(int epi, int M, int N, int H, int F);
+// Tile width (256, 192 or 128 columns) for uniform tiles of a GEMM of M rows;
+// the number of N tiles and the row count of one B box at that width.
 int gemm_choose_bn(int epi, int M, int N, int H, int F);
 int gemm_num_n(int epi, int bn, int N, int H, int F);
 int gemm_b_box_rows(int epi, int bn);

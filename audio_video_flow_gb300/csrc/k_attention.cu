@@ -4,8 +4,8 @@
 //
 // One CTA computes one 128-row query tile of one head:
 //   warp 0      TMA producer: Q once, then K_j and V_j tiles (128 rows x 128
-//               channels, two 64-channel 128-byte-swizzled boxes each) into a
-//               2-deep ring per operand;
+//               channels, two 64-channel 128-byte-swizzled boxes each) into
+//               rings of 3 (K) and 2 (V) tiles;
 //   warp 1      MMA issuer (one thread): S_j = Q K_j^T into one of two TMEM
 //               score buffers, and O += P_j V_j into the TMEM output
 //               accumulator (V is read MN-major straight from its TMA tile);
@@ -29,7 +29,7 @@ namespace h3 {
 namespace {
 constexpr int AT_THREADS = 256;
 constexpr int KV_TILE = 128;
-constexpr int KST = 2, VST = 2;
+constexpr int KST = 3, VST = 2;   // K ring 3 deep: K_{j+1} is loaded two steps ahead of its MMA
 constexpr int TILE_BYTES = 128 * 128 * 2;   // 32 KB: two 16 KB boxes
 constexpr int BOX_BYTES = 128 * 64 * 2;     // 16 KB
 constexpr int AT_SMEM = 1024 + TILE_BYTES * (1 + KST + VST + 1) + 512;
@@ -322,7 +322,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
 // by the running sum uses the same maximum, so the result is unchanged.
 // ---------------------------------------------------------------------------
 namespace {
-constexpr int AT2_THREADS = 384;   // warp 0 TMA, warp 1 MMA, warps 4-7 tile A, 8-11 tile B
+constexpr int AT2_THREADS = 384;   // warp 0 TMA Q/K, warp 1 MMA, warp 2 TMA V, warps 4-7 tile A, 8-11 tile B
 constexpr int AT2_SMEM = 1024 + TILE_BYTES * (2 + KST + VST) + 512;
 constexpr float kRescaleThreshold = 8.0f;
 
@@ -398,10 +398,10 @@ __global__ void __launch_bounds__(AT2_THREADS, 1)
   volatile int* abort_v = abort_flag;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------------------ producer of Q and K
     if (lane == 0) {
       bool ok = true;
-      int issued_k = 0, issued_v = 0;
+      int issued_k = 0;
       mbar_arrive_expect_tx(q_full, 2 * TILE_BYTES);
       for (int t = 0; t < 2; ++t) {
         tma_load_3d(sQ + t * TILE_BYTES, &tmQ, q_full, 0, head, pair * 256 + t * 128);
@@ -414,6 +414,21 @@ __global__ void __launch_bounds__(AT2_THREADS, 1)
         tma_load_3d(sK + ks * TILE_BYTES, &tmK, &k_full[ks], 0, head, j * KV_TILE);
         tma_load_3d(sK + ks * TILE_BYTES + BOX_BYTES, &tmK, &k_full[ks], 64, head, j * KV_TILE);
         ++issued_k;
+      }
+      if (!ok) {
+        drain_wait(q_full, 0);
+        for (int j = (issued_k > KST ? issued_k - KST : 0); j < issued_k; ++j)
+          drain_wait(&k_full[j % KST], (uint32_t)(j / KST) & 1u);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ producer of V (its own thread, so a
+    // V slot that frees up is refilled without waiting behind the K ring)
+    if (lane == 0) {
+      bool ok = true;
+      int issued_v = 0;
+      for (int j = 0; j < n_kv && ok; ++j) {
         const int vs = j % VST;
         if (!mbar_wait(&v_empty[vs], ((uint32_t)(j / VST) & 1u) ^ 1u, abort_v)) { ok = false; break; }
         mbar_arrive_expect_tx(&v_full[vs], TILE_BYTES);
@@ -422,9 +437,6 @@ __global__ void __launch_bounds__(AT2_THREADS, 1)
         ++issued_v;
       }
       if (!ok) {
-        drain_wait(q_full, 0);
-        for (int j = (issued_k > KST ? issued_k - KST : 0); j < issued_k; ++j)
-          drain_wait(&k_full[j % KST], (uint32_t)(j / KST) & 1u);
         for (int j = (issued_v > VST ? issued_v - VST : 0); j < issued_v; ++j)
           drain_wait(&v_full[j % VST], (uint32_t)(j / VST) & 1u);
       }

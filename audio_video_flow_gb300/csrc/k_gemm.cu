@@ -89,8 +89,20 @@ __device__ __forceinline__ float bias_at(const __nv_bfloat16* b, int i) {
   return b ? __bfloat162float(b[i]) : 0.0f;
 }
 
-// First weight row of the BN/2 B rows that CTA `rank` of the pair loads for
-// tile n_blk.  The tile's N columns are rank 0's rows then rank 1's rows.
+// Columns [n0, n0 + w) of tile n_blk (plain and residual epilogues; the
+// others always use uniform BN-wide tiles).
+struct NTile {
+  int n0, w;
+};
+template <int EPI, int BN>
+__device__ __forceinline__ NTile n_tile(const GemmArgs& a, int n_blk) {
+  if ((EPI != EPI_PLAIN && EPI != EPI_RESID) || a.nw1 == 0) return {n_blk * BN, BN};
+  if (n_blk < a.ncnt1) return {n_blk * a.nw1, a.nw1};
+  return {a.ncnt1 * a.nw1 + (n_blk - a.ncnt1) * a.nw2, a.nw2};
+}
+
+// First weight row of the B rows that CTA `rank` of the pair loads for tile
+// n_blk.  The tile's N columns are rank 0's rows then rank 1's rows.
 template <int EPI, int BN>
 __device__ __forceinline__ int b_tile_row(const GemmArgs& a, int n_blk, uint32_t rank) {
   if (EPI == EPI_SWIGLU) return (rank ? a.F : 0) + n_blk * 128;            // gate rows | value rows
@@ -100,7 +112,8 @@ __device__ __forceinline__ int b_tile_row(const GemmArgs& a, int n_blk, uint32_t
     return (2 * p + (int)rank) * 384 + 256;                                 // v of heads 2p | 2p+1
   }
   if (EPI == EPI_QKV) return (n_blk / 3) * 384 + (n_blk % 3) * 128 + (int)rank * 64;   // q, k or v of a head
-  return n_blk * BN + (int)rank * (BN / 2);
+  const NTile t = n_tile<EPI, BN>(a, n_blk);
+  return t.n0 + (int)rank * (t.w / 2);
 }
 
 // Tile order (tiles of 256 rows, one per CTA pair): groups of GROUP_M
@@ -146,37 +159,83 @@ __device__ __forceinline__ void store16_bf16(__nv_bfloat16* dst, const float (&v
   }
 }
 
-template <int BN>
-__device__ __forceinline__ void epi_plain(const GemmArgs& a, uint32_t tacc, int m, bool valid, int n_blk) {
-#pragma unroll 1
-  for (int c = 0; c < BN / 32; ++c) {
-    uint32_t r[32];
-    tmem_ld32(tacc + c * 32, r);
+// Columns [n0, n0 + w) of the tile, w a multiple of 16: 32-column chunks and
+// at most one 16-column tail.
+template <int NC>
+__device__ __forceinline__ void tmem_ld_chunk(uint32_t taddr, uint32_t (&r)[32]) {
+  if (NC == 32) {
+    tmem_ld32(taddr, r);
     tmem_ld_wait(r);
-    const int n0 = n_blk * BN + c * 32;
-    if (valid) {
-      __nv_bfloat16* dst = a.out + (size_t)m * a.ldo + n0;
+  } else {
+    uint32_t h[16];
+    tmem_ld16(taddr, h);
+    tmem_ld_wait16(h);
 #pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        const int n = n0 + g * 8;
-        if (n < a.n_valid) {
-          uint4 w;
-          uint32_t* wp = reinterpret_cast<uint32_t*>(&w);
+    for (int i = 0; i < 16; ++i) r[i] = h[i];
+  }
+}
+
+template <int NC>
+__device__ __forceinline__ void plain_chunk(const GemmArgs& a, uint32_t tc, int m, bool valid, int n0) {
+  uint32_t r[32];
+  tmem_ld_chunk<NC>(tc, r);
+  if (valid) {
+    __nv_bfloat16* dst = a.out + (size_t)m * a.ldo + n0;
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float lo = __uint_as_float(r[g * 8 + 2 * e]) + bias_at(a.bias, n + 2 * e);
-            const float hi = __uint_as_float(r[g * 8 + 2 * e + 1]) + bias_at(a.bias, n + 2 * e + 1);
-            wp[e] = pack_bf16x2(lo, hi);
-          }
-          *reinterpret_cast<uint4*>(dst + g * 8) = w;
+    for (int g = 0; g < NC / 8; ++g) {
+      const int n = n0 + g * 8;
+      if (n < a.n_valid) {
+        uint4 w;
+        uint32_t* wp = reinterpret_cast<uint32_t*>(&w);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float lo = __uint_as_float(r[g * 8 + 2 * e]) + bias_at(a.bias, n + 2 * e);
+          const float hi = __uint_as_float(r[g * 8 + 2 * e + 1]) + bias_at(a.bias, n + 2 * e + 1);
+          wp[e] = pack_bf16x2(lo, hi);
         }
+        *reinterpret_cast<uint4*>(dst + g * 8) = w;
       }
     }
   }
 }
 
-template <int BN>
-__device__ __forceinline__ void epi_resid(const GemmArgs& a, uint32_t tacc, int m, bool valid, int n_blk) {
+__device__ __forceinline__ void epi_plain(const GemmArgs& a, uint32_t tacc, int m, bool valid, NTile t) {
+  int c = 0;
+#pragma unroll 1
+  for (; c + 32 <= t.w; c += 32) plain_chunk<32>(a, tacc + c, m, valid, t.n0 + c);
+  if (c < t.w) plain_chunk<16>(a, tacc + c, m, valid, t.n0 + c);
+}
+
+template <int NC>
+__device__ __forceinline__ void resid_chunk(const GemmArgs& a, uint32_t tc, int m, bool valid,
+                                            const __nv_bfloat16* gate, int n0) {
+  uint32_t r[32];
+  tmem_ld_chunk<NC>(tc, r);
+  if (valid && n0 < a.n_valid) {
+    const uint4* xs = reinterpret_cast<const uint4*>(a.resid + (size_t)m * a.ldr + n0);
+    const uint4* gs = reinterpret_cast<const uint4*>(gate + n0);
+    uint4* dst = reinterpret_cast<uint4*>(a.out + (size_t)m * a.ldo + n0);
+#pragma unroll
+    for (int g = 0; g < NC / 8; ++g) {
+      const uint4 xv = xs[g], gv = gs[g];
+      const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+      const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+      uint32_t ow[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int j = g * 8 + 2 * e;
+        const float flo = bf16_round(__uint_as_float(r[j]) + bias_at(a.bias, n0 + j));
+        const float fhi = bf16_round(__uint_as_float(r[j + 1]) + bias_at(a.bias, n0 + j + 1));
+        const float ylo = __fmaf_rn(bf16_lo(gw[e]), flo, bf16_lo(xw[e]));
+        const float yhi = __fmaf_rn(bf16_hi(gw[e]), fhi, bf16_hi(xw[e]));
+        ow[e] = pack_bf16x2(ylo, yhi);
+      }
+      dst[g] = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+    }
+  }
+}
+
+__device__ __forceinline__ void epi_resid(const GemmArgs& a, uint32_t tacc, int m, bool valid, NTile t) {
   const __nv_bfloat16* gate = nullptr;
   if (valid) {
     const int tg = a.tag[m], ti = a.tidx[m];
@@ -187,35 +246,10 @@ __device__ __forceinline__ void epi_resid(const GemmArgs& a, uint32_t tacc, int 
       gate = a.table + ((size_t)(ti * 3 + tg) * 6 + a.chunk) * a.D;
     }
   }
+  int c = 0;
 #pragma unroll 1
-  for (int c = 0; c < BN / 32; ++c) {
-    uint32_t r[32];
-    tmem_ld32(tacc + c * 32, r);
-    tmem_ld_wait(r);
-    const int n0 = n_blk * BN + c * 32;
-    if (valid && n0 < a.n_valid) {
-      const uint4* xs = reinterpret_cast<const uint4*>(a.resid + (size_t)m * a.ldr + n0);
-      const uint4* gs = reinterpret_cast<const uint4*>(gate + n0);
-      uint4* dst = reinterpret_cast<uint4*>(a.out + (size_t)m * a.ldo + n0);
-#pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        const uint4 xv = xs[g], gv = gs[g];
-        const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-        const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
-        uint32_t ow[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int j = g * 8 + 2 * e;
-          const float flo = bf16_round(__uint_as_float(r[j]) + bias_at(a.bias, n0 + j));
-          const float fhi = bf16_round(__uint_as_float(r[j + 1]) + bias_at(a.bias, n0 + j + 1));
-          const float ylo = __fmaf_rn(bf16_lo(gw[e]), flo, bf16_lo(xw[e]));
-          const float yhi = __fmaf_rn(bf16_hi(gw[e]), fhi, bf16_hi(xw[e]));
-          ow[e] = pack_bf16x2(ylo, yhi);
-        }
-        dst[g] = make_uint4(ow[0], ow[1], ow[2], ow[3]);
-      }
-    }
-  }
+  for (; c + 32 <= t.w; c += 32) resid_chunk<32>(a, tacc + c, m, valid, gate, t.n0 + c);
+  if (c < t.w) resid_chunk<16>(a, tacc + c, m, valid, gate, t.n0 + c);
 }
 
 __device__ __forceinline__ void epi_swiglu(const GemmArgs& a, uint32_t tacc, int m, bool valid, int n_blk) {
@@ -300,6 +334,94 @@ __device__ __forceinline__ void epi_qk_part(const GemmArgs& a, uint32_t tpart, i
   }
 }
 
+// Q and K columns of head h together (q at tq, k at tk, 128 accumulator
+// columns each): the same per-head RMSNorm and rotation as epi_qk_part, with
+// each of the row's 48 rotation angles evaluated once for both parts.
+__device__ __forceinline__ void epi_qk_both(const GemmArgs& a, uint32_t tq, uint32_t tk, int m, bool valid, int h,
+                                            const float (&pos)[3]) {
+  const int cq = h * 384, ck = h * 384 + 128;   // output / weight column of channel 0 of q, k
+  float ssq = 0.f, ssk = 0.f;
+#pragma unroll 1
+  for (int c = 0; c < 4; ++c) {
+    uint32_t rq[16], rk[16], rq2[16], rk2[16];
+    tmem_ld16(tq + c * 32, rq);
+    tmem_ld16(tk + c * 32, rk);
+    tmem_ld_wait(rq, rk);
+    tmem_ld16(tq + c * 32 + 16, rq2);
+    tmem_ld16(tk + c * 32 + 16, rk2);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const float vq = bf16_round(__uint_as_float(rq[j]) + bias_at(a.bias, cq + c * 32 + j));
+      const float vk = bf16_round(__uint_as_float(rk[j]) + bias_at(a.bias, ck + c * 32 + j));
+      ssq = __fmaf_rn(vq, vq, ssq);
+      ssk = __fmaf_rn(vk, vk, ssk);
+    }
+    tmem_ld_wait(rq2, rk2);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const float vq = bf16_round(__uint_as_float(rq2[j]) + bias_at(a.bias, cq + c * 32 + 16 + j));
+      const float vk = bf16_round(__uint_as_float(rk2[j]) + bias_at(a.bias, ck + c * 32 + 16 + j));
+      ssq = __fmaf_rn(vq, vq, ssq);
+      ssk = __fmaf_rn(vk, vk, ssk);
+    }
+  }
+  const float invq = 1.0f / sqrtf(ssq * (1.0f / 128.0f) + a.eps);
+  const float invk = 1.0f / sqrtf(ssk * (1.0f / 128.0f) + a.eps);
+#pragma unroll 1
+  for (int band = 0; band < 3; ++band) {
+    const float p = band == 0 ? pos[0] : (band == 1 ? pos[1] : pos[2]);
+    float cs[16], sn[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) sincosf(p * a.omega[i], &sn[i], &cs[i]);
+#pragma unroll
+    for (int part = 0; part < 2; ++part) {
+      const uint32_t tp = part ? tk : tq;
+      const int cb = part ? ck : cq;
+      const float inv = part ? invk : invq;
+      const __nv_bfloat16* gain = part ? a.k_gain : a.q_gain;
+      uint32_t lo[16], hi[16];
+      tmem_ld16(tp + band * 16, lo);
+      tmem_ld16(tp + 48 + band * 16, hi);
+      tmem_ld_wait(lo, hi);
+      if (valid) {
+        float o1[16], o2[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int j = band * 16 + i;
+          const float v1 = bf16_round(__uint_as_float(lo[i]) + bias_at(a.bias, cb + j));
+          const float v2 = bf16_round(__uint_as_float(hi[i]) + bias_at(a.bias, cb + 48 + j));
+          const float x1 = bf16_round(v1 * inv * __bfloat162float(gain[j]));
+          const float x2 = bf16_round(v2 * inv * __bfloat162float(gain[48 + j]));
+          o1[i] = __fmaf_rn(x1, cs[i], -(x2 * sn[i]));
+          o2[i] = __fmaf_rn(x2, cs[i], x1 * sn[i]);
+        }
+        __nv_bfloat16* dst = a.out + (size_t)m * a.ldo + cb;
+        store16_bf16(dst + band * 16, o1);
+        store16_bf16(dst + 48 + band * 16, o2);
+      }
+    }
+  }
+#pragma unroll 1
+  for (int part = 0; part < 2; ++part) {
+    const uint32_t tp = part ? tk : tq;
+    const int cb = part ? ck : cq;
+    const float inv = part ? invk : invq;
+    const __nv_bfloat16* gain = part ? a.k_gain : a.q_gain;
+    uint32_t r[32];
+    tmem_ld32(tp + 96, r);
+    tmem_ld_wait(r);
+    if (valid) {
+      float v[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float x = bf16_round(__uint_as_float(r[j]) + bias_at(a.bias, cb + 96 + j));
+        v[j] = x * inv * __bfloat162float(gain[96 + j]);
+      }
+      store32_bf16(a.out + (size_t)m * a.ldo + cb + 96, v);
+    }
+  }
+}
+
 // V columns of one head (128 accumulator columns at tpart).
 __device__ __forceinline__ void epi_v_head(const GemmArgs& a, uint32_t tpart, int m, bool valid, int head) {
 #pragma unroll 1
@@ -333,8 +455,7 @@ __device__ __forceinline__ void epi_qkv(const GemmArgs& a, uint32_t tacc, int m,
   }
   if (BN == 256) {
     if (n_blk < a.H) {
-      epi_qk_part(a, tacc, m, valid, n_blk, 0, pos);
-      epi_qk_part(a, tacc + 128, m, valid, n_blk, 1, pos);
+      epi_qk_both(a, tacc, tacc + 128, m, valid, n_blk, pos);
     } else {
       const int p = n_blk - a.H;
       epi_v_head(a, tacc, m, valid, 2 * p);
@@ -350,8 +471,8 @@ __device__ __forceinline__ void epi_qkv(const GemmArgs& a, uint32_t tacc, int m,
 template <int EPI, int BN>
 __device__ __forceinline__ void run_epilogue(const GemmArgs& a, uint32_t tacc, int m, int n_blk) {
   const bool valid = m < a.M;
-  if (EPI == EPI_PLAIN) epi_plain<BN>(a, tacc, m, valid, n_blk);
-  if (EPI == EPI_RESID) epi_resid<BN>(a, tacc, m, valid, n_blk);
+  if (EPI == EPI_PLAIN) epi_plain(a, tacc, m, valid, n_tile<EPI, BN>(a, n_blk));
+  if (EPI == EPI_RESID) epi_resid(a, tacc, m, valid, n_tile<EPI, BN>(a, n_blk));
   if (EPI == EPI_SWIGLU) epi_swiglu(a, tacc, m, valid, n_blk);
   if (EPI == EPI_QKV) epi_qkv<BN>(a, tacc, m, valid, n_blk);
 }
@@ -425,6 +546,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       for (int s = 0; s < STAGES; ++s) last_phase[s] = -1;
       bool ok = true;
       const uint32_t full0 = mapa_shared(smem_u32(full), 0);   // the even CTA's full[0]
+      const uint32_t stage_tx = 2u * (uint32_t)(A_STAGE_BYTES + args.b_rows * BK * 2);   // both CTAs' boxes
       for (int tile = pair; tile < num_tiles && ok; tile += num_pairs) {
         int m_blk, n_blk;
         tile_coords(tile, args.num_m, args.num_n, m_blk, n_blk);
@@ -432,7 +554,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         const int ra = m_blk * 2 * BM + (int)rank * BM;
         for (int kb = 0; kb < args.num_k; ++kb) {
           if (!mbar_wait_cluster(&empty[stage], phase ^ 1u, abort_v)) { ok = false; break; }
-          if (leader) mbar_arrive_expect_tx(&full[stage], 2 * C::STAGE_BYTES);
+          if (leader) mbar_arrive_expect_tx(&full[stage], stage_tx);
           const uint32_t fb = full0 + (uint32_t)stage * 8u;
           tma_load_2d_pair(sA + stage * A_STAGE_BYTES, &tmA, fb, kb * BK, ra);
           tma_load_2d_pair(sB + stage * C::B_STAGE_BYTES, &tmB, fb, kb * BK, rb);
@@ -458,7 +580,6 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer (even CTA)
     if (lane == 0 && leader) {
-      constexpr uint32_t idesc = idesc_bf16(2 * BM, BN);
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -469,6 +590,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         if (!mbar_wait_cluster(&acc_empty[acc], acc_phase ^ 1u, abort_v)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        int m_blk, n_blk;
+        tile_coords(tile, args.num_m, args.num_n, m_blk, n_blk);
+        const uint32_t idesc = idesc_bf16(2 * BM, n_tile<EPI, BN>(args, n_blk).w);
         for (int kb = 0; kb < args.num_k; ++kb) {
           if (!mbar_wait_cluster(&full[stage], phase, abort_v)) { ok = false; break; }
           tc_fence_after();
@@ -569,6 +693,39 @@ int gemm_choose_bn(int epi, int M, int N, int H, int F) {
   return best;
 }
 
+GemmPlan gemm_plan(int epi, int M, int N, int H, int F) {
+  GemmPlan p{};
+  p.bn = gemm_choose_bn(epi, M, N, H, F);
+  p.num_n = gemm_num_n(epi, p.bn, N, H, F);
+  p.b_rows = gemm_b_box_rows(epi, p.bn);
+  if ((epi != EPI_PLAIN && epi != EPI_RESID) || getenv("H3_GEMM_BN") || N % 16) return p;
+  // balanced widths: every row tile gets `per_row` column tiles so that all
+  // of them are resident at once; widths nw1 and nw1 - 16 (multiples of 16)
+  const int slots = gemm_pair_slots(), num_m = gemm_m_tiles(M);
+  const int per_row = slots / num_m;
+  if (per_row < 1) return p;
+  const int units = N / 16;
+  const int u1 = (units + per_row - 1) / per_row;
+  if (u1 < 4 || u1 > 16) return p;            // 64..256 columns
+  const int u2 = u1 - 1;
+  const int cnt1 = units - per_row * u2;       // cnt1 * u1 + (per_row - cnt1) * u2 == units
+  const int cnt2 = per_row - cnt1;
+  if (cnt1 < 1 || cnt1 > per_row) return p;
+  // wave model of the uniform plan against one wave of the balanced one
+  const long long u_tiles = (long long)num_m * p.num_n;
+  const long long u_waves = (u_tiles + slots - 1) / slots;
+  const long long u_cost = u_waves * p.bn * 100 / (p.bn == 256 ? 100 : (p.bn == 192 ? 95 : 65));
+  const long long b_cost = (long long)(16 * u1) * 100 / 95;
+  if (b_cost >= u_cost) return p;
+  p.nw1 = 16 * u1;
+  p.ncnt1 = cnt1;
+  p.nw2 = cnt2 > 0 ? 16 * u2 : 0;
+  p.num_n = per_row;
+  p.bn = p.nw1 <= 128 ? 128 : (p.nw1 <= 192 ? 192 : 256);
+  p.b_rows = p.nw1 / 2;
+  return p;
+}
+
 int gemm_pair_slots() {
   static int slots[64] = {0};
   int dev = 0;
@@ -632,9 +789,9 @@ cudaError_t launch_gemm(int epi, int bn, const CUtensorMap& tmA, const CUtensorM
   if (e != cudaSuccess) return e;
   const int stages = bn == 256 ? GemmCfg<256>::STAGES : (bn == 192 ? GemmCfg<192>::STAGES : GemmCfg<128>::STAGES);
   set_kernel_info("gemm_bf16_tc<%s,%d> tcgen05.mma.cta_group::2.kind::f16 pair-tile=%dx%dx%d stages=%d acc=f32 "
-                  "tmem=2x%d grid=%d (pairs=%d of %d) tiles=%dx%d k_blocks=%d l2_prefetch=%d",
+                  "tmem=2x%d grid=%d (pairs=%d of %d) tiles=%dx%d k_blocks=%d l2_prefetch=%d n-widths=%s%d,%d,%d",
                   names[epi], bn, 2 * BM, bn, BK, stages, bn, grid, pairs, slots, a.num_m, a.num_n, a.num_k,
-                  2 * stages);
+                  2 * stages, a.nw1 ? "balanced:" : "uniform:", a.nw1 ? a.nw1 : bn, a.ncnt1, a.nw2);
   return cudaGetLastError();
 }
 

@@ -211,9 +211,14 @@ __global__ void __launch_bounds__(ROPE_THREADS, 1)
     const int partner = hl < 6 ? lane + 6 : (hl < 12 ? lane - 6 : lane);
     const int col = hl < 12 ? (hl % 6) * 8 : 0;                 // first rotation column of the lane
     const float sgn = hl < 6 ? -1.0f : 1.0f;
-    float g[8];
+    // channel pairs (2e, 2e+1) of the lane's 8 channels travel as float2 so
+    // the per-channel products run as packed fp32 (IEEE, per lane)
+    float2 g2[4];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) g[e] = __bfloat162float((is_k ? a.k_gain : a.q_gain)[hl * 8 + e]);
+    for (int e = 0; e < 4; ++e) {
+      const __nv_bfloat16* gp = (is_k ? a.k_gain : a.q_gain) + hl * 8 + 2 * e;
+      g2[e] = make_float2(__bfloat162float(gp[0]), __bfloat162float(gp[1]));
+    }
     __nv_bfloat16* gbase = is_k ? a.k : a.q;
     int stage = 0;
     uint32_t phase = 0;
@@ -223,15 +228,15 @@ __global__ void __launch_bounds__(ROPE_THREADS, 1)
       if (bad[stage]) {
         if (cw == 0 && lane == 0) record_error(a.err, DEVERR_INDEX);
       } else {
-        float cs[8], sn[8];
+        float2 cs2[4], sn2[4];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
+        for (int e = 0; e < 4; ++e) {
           if (hl < 12) {
-            cs[e] = ang[stage * 96 + col + e];
-            sn[e] = sgn * ang[stage * 96 + 48 + col + e];
+            cs2[e] = make_float2(ang[stage * 96 + col + 2 * e], ang[stage * 96 + col + 2 * e + 1]);
+            sn2[e] = make_float2(sgn * ang[stage * 96 + 48 + col + 2 * e], sgn * ang[stage * 96 + 48 + col + 2 * e + 1]);
           } else {
-            cs[e] = 1.0f;
-            sn[e] = 0.0f;
+            cs2[e] = make_float2(1.0f, 1.0f);
+            sn2[e] = make_float2(0.0f, 0.0f);
           }
         }
         const uint8_t* t = tiles + stage * SB + (is_k ? SB / 2 : 0) + hl * 16;
@@ -239,23 +244,25 @@ __global__ void __launch_bounds__(ROPE_THREADS, 1)
         for (int h = cw; h < HB && h0 + h < a.H; h += 2 * ROPE_CWARPS) {
           const int hh[2] = {h, h + ROPE_CWARPS};
           const bool second = hh[1] < HB && h0 + hh[1] < a.H;   // warp-uniform
-          float v[2][8];
+          float2 v[2][4];
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
             uint4 r = make_uint4(0u, 0u, 0u, 0u);
             if (j == 0 || second) r = *reinterpret_cast<const uint4*>(t + hh[j] * 256);
             const uint32_t w[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              v[j][2 * e] = bf16_lo(w[e]);
-              v[j][2 * e + 1] = bf16_hi(w[e]);
-            }
+            for (int e = 0; e < 4; ++e) v[j][e] = make_float2(bf16_lo(w[e]), bf16_hi(w[e]));
           }
-          float ss[2] = {0.0f, 0.0f};
+          // sum of squares: even and odd channels in two lanes of a float2,
+          // then added, then reduced over the 16 lanes of the half
+          float ss[2];
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
+          for (int j = 0; j < 2; ++j) {
+            float2 acc = make_float2(0.0f, 0.0f);
 #pragma unroll
-            for (int j = 0; j < 2; ++j) ss[j] = __fmaf_rn(v[j][e], v[j][e], ss[j]);
+            for (int e = 0; e < 4; ++e) acc = __ffma2_rn(v[j][e], v[j][e], acc);
+            ss[j] = acc.x + acc.y;
+          }
 #pragma unroll
           for (int o = 8; o > 0; o >>= 1)
 #pragma unroll
@@ -263,19 +270,25 @@ __global__ void __launch_bounds__(ROPE_THREADS, 1)
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
             const float inv = 1.0f / sqrtf(ss[j] * (1.0f / 128.0f) + a.eps);
-            float n[8], out[8];
+            const float2 inv2 = make_float2(inv, inv);
+            uint32_t nb[4], ob[4], outw[4];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) n[e] = bf16_round((v[j][e] * inv) * g[e]);
+            for (int e = 0; e < 4; ++e) {   // normed channels, rounded to bf16 (two per word)
+              const float2 x = __fmul2_rn(__fmul2_rn(v[j][e], inv2), g2[e]);
+              nb[e] = pack_bf16x2(x.x, x.y);
+            }
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const float other = __shfl_sync(0xffffffffu, n[e], partner);
-              out[e] = __fmaf_rn(n[e], cs[e], other * sn[e]);
+            for (int e = 0; e < 4; ++e) ob[e] = __shfl_sync(0xffffffffu, nb[e], partner);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 n = make_float2(bf16_lo(nb[e]), bf16_hi(nb[e]));
+              const float2 other = make_float2(bf16_lo(ob[e]), bf16_hi(ob[e]));
+              const float2 y = __ffma2_rn(n, cs2[e], __fmul2_rn(other, sn2[e]));
+              outw[e] = pack_bf16x2(y.x, y.y);
             }
             if (j == 0 || second)
               *reinterpret_cast<uint4*>(gbase + (size_t)row * a.row_stride + (size_t)(h0 + hh[j]) * a.head_stride +
-                                        hl * 8) =
-                  make_uint4(pack_bf16x2(out[0], out[1]), pack_bf16x2(out[2], out[3]),
-                             pack_bf16x2(out[4], out[5]), pack_bf16x2(out[6], out[7]));
+                                        hl * 8) = make_uint4(outw[0], outw[1], outw[2], outw[3]);
           }
         }
       }

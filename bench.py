@@ -46,10 +46,10 @@ STAGES = ("adaln_table", "norm1_modulate", "qkv_qknorm_rope", "attention", "out_
 TRAFFIC = {
     "qkv_qknorm_rope@block505": 252453632,
     "fc1_swiglu@block1824": 380734720,
-    "attention@attn4096": 214066176,
-    "attention@attn16384": 916994048,
-    "attention@attn32768": 1833988096,
-    "attention@denoiser15860": 887666358,
+    "attention@attn4096": 214684160,
+    "attention@attn16384": 919471872,
+    "attention@attn32768": 1838943744,
+    "attention@denoiser15860": 890064935,
 }
 
 

@@ -95,6 +95,22 @@ def test_linear_plain(h3, gemm_bn):
     assert_close(to_np(y), O.linear(to_np(x), to_np(w), to_np(b)), "linear")
 
 
+@pytest.mark.parametrize("M,N,K", [(505, 2928, 320), (200, 4864, 128)])
+def test_linear_balanced_column_tiles(h3, M, N, K):
+    """Few row tiles and many columns: the columns are split into tiles of two
+    widths (80/64 and 64 columns here) so every CTA pair gets one tile."""
+    g = torch.Generator().manual_seed(6)
+    x = torch.randn(M, K, generator=g).to(torch.bfloat16)
+    w = (torch.randn(N, K, generator=g) * 0.05).to(torch.bfloat16)
+    b = (torch.randn(N, generator=g) * 0.1).to(torch.bfloat16)
+    y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    h3.h3_linear(M, N, K, x.cuda(), w.cuda(), b.cuda(), y)
+    torch.cuda.synchronize()
+    info = h3.h3_last_kernel_info()
+    assert "balanced:" in info, info
+    assert_close(to_np(y), O.linear(to_np(x), to_np(w), to_np(b)), f"linear {M}x{N}x{K}")
+
+
 @pytest.mark.parametrize("name", CASE_NAMES)
 def test_adaln_table(h3, name):
     c = get_case(name)
