@@ -80,6 +80,12 @@ def lib() -> ctypes.CDLL:
             "h3_ffn_up_swiglu": (i32, [cfgp, i32, vp, vp, vp, vp, vp]),
             "h3_ffn_down_residual": (i32, [cfgp, mp, vp, vp, vp, vp, vp, vp, vp]),
             "h3_linear": (i32, [i32, i32, i32, vp, vp, vp, vp, vp]),
+            "h3_sigma_schedule": (i32, [i32, ctypes.c_float, vp, vp, vp]),
+            "h3_ode_step": (i32, [c_int64, vp, vp, ctypes.c_float, ctypes.c_float, vp, vp]),
+            "h3_noise_mix": (i32, [c_int64, vp, vp, ctypes.c_float, vp, vp]),
+            "h3_select_rows": (i32, [i32, vp, i32, vp, vp, vp]),
+            "h3_final_adaln_table": (i32, [cfgp, vp, vp, vp, i32, vp, vp]),
+            "h3_output_head": (i32, [cfgp, i32, i32, vp, vp, i32, vp, vp, vp, vp, i32, vp, vp]),
             "h3_sync_check": (i32, [vp, i32]),
             "h3_status_string": (c_char_p, [i32]),
             "h3_last_kernel_info": (i32, [ctypes.c_char_p, sz]),
@@ -244,6 +250,36 @@ def h3_ffn_down_residual(cfg, meta, table, a, w_fc2, b_fc2, x1, y_out, stream=No
 
 def h3_linear(M: int, N: int, K: int, x, w, b, y, stream=None) -> None:
     _check(lib().h3_linear(M, N, K, _ptr(x), _ptr(w), _ptr(b), _ptr(y), _stream(stream)), "h3_linear")
+
+
+def h3_sigma_schedule(n_points: int, shift: float, sigmas, n_sigmas, stream=None) -> None:
+    _check(lib().h3_sigma_schedule(n_points, shift, _ptr(sigmas), _ptr(n_sigmas), _stream(stream)),
+           "h3_sigma_schedule")
+
+
+def h3_ode_step(n: int, xt, v, sigma: float, sigma_next: float, x_next, stream=None) -> None:
+    _check(lib().h3_ode_step(n, _ptr(xt), _ptr(v), sigma, sigma_next, _ptr(x_next), _stream(stream)), "h3_ode_step")
+
+
+def h3_noise_mix(n: int, x0, noise, t: float, out, stream=None) -> None:
+    _check(lib().h3_noise_mix(n, _ptr(x0), _ptr(noise), t, _ptr(out), _stream(stream)), "h3_noise_mix")
+
+
+def h3_select_rows(n_rows: int, token_tag, tag: int, rows, n_selected, stream=None) -> None:
+    _check(lib().h3_select_rows(n_rows, _ptr(token_tag), tag, _ptr(rows), _ptr(n_selected), _stream(stream)),
+           "h3_select_rows")
+
+
+def h3_final_adaln_table(cfg, w_fin, b_fin, t_cond, n_timesteps: int, table, stream=None) -> None:
+    _check(lib().h3_final_adaln_table(ctypes.byref(cfg), _ptr(w_fin), _ptr(b_fin), _ptr(t_cond), n_timesteps,
+                                      _ptr(table), _stream(stream)), "h3_final_adaln_table")
+
+
+def h3_output_head(cfg, n_rows: int, n_sel: int, rows, timestep_index, n_timesteps: int, x, table, w_head, b_head,
+                   P: int, v_out, stream=None) -> None:
+    _check(lib().h3_output_head(ctypes.byref(cfg), n_rows, n_sel, _ptr(rows), _ptr(timestep_index), n_timesteps,
+                                _ptr(x), _ptr(table), _ptr(w_head), _ptr(b_head), P, _ptr(v_out),
+                                _stream(stream)), "h3_output_head")
 
 
 def h3_sync_check(stream=None, timeout_ms: int = 10000) -> int:

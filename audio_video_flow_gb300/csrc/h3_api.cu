@@ -731,6 +731,79 @@ h3_status h3_linear(int32_t M, int32_t N, int32_t K, const void* x, const void* 
   return cuda_st(launch_gemm(EPI_PLAIN, pl.bn, tA, tB, a, stream));
 }
 
+// ===========================================================================
+// output side and sampler
+// ===========================================================================
+h3_status h3_sigma_schedule(int32_t n_points, float shift, float* sigmas, int32_t* n_sigmas, cudaStream_t stream) {
+  if (!sigmas || !n_sigmas) return H3_ERR_NULL;
+  if (n_points < 2 || n_points > (1 << 20) || !std::isfinite(shift) || !(shift > 0.0f)) return H3_ERR_SHAPE;
+  return cuda_st(launch_sigma_grid(n_points, shift, sigmas, n_sigmas, stream));
+}
+
+h3_status h3_ode_step(int64_t n, const float* xt, const float* v, float sigma, float sigma_next, float* x_next,
+                      cudaStream_t stream) {
+  if (n < 0) return H3_ERR_SHAPE;
+  if (!std::isfinite(sigma) || !(sigma > 0.0f) || !std::isfinite(sigma_next) || sigma_next < 0.0f)
+    return H3_ERR_SHAPE;
+  if (n == 0) return H3_OK;
+  if (!xt || !v || !x_next) return H3_ERR_NULL;
+  if (!al16(xt) || !al16(v) || !al16(x_next)) return H3_ERR_ALIGN;
+  return cuda_st(launch_ode_step((long long)n, xt, v, sigma, sigma_next, x_next, stream));
+}
+
+h3_status h3_noise_mix(int64_t n, const float* x0, const float* noise, float t, float* out, cudaStream_t stream) {
+  if (n < 0 || !std::isfinite(t) || t < 0.0f || t > 1.0f) return H3_ERR_SHAPE;
+  if (n == 0) return H3_OK;
+  if (!x0 || !noise || !out) return H3_ERR_NULL;
+  if (!al16(x0) || !al16(noise) || !al16(out)) return H3_ERR_ALIGN;
+  return cuda_st(launch_noise_mix((long long)n, x0, noise, t, out, stream));
+}
+
+h3_status h3_select_rows(int32_t n_rows, const int32_t* token_tag, int32_t tag, int32_t* rows, int32_t* n_selected,
+                         cudaStream_t stream) {
+  if (n_rows < 0) return H3_ERR_SHAPE;
+  if (!token_tag || !rows || !n_selected) return H3_ERR_NULL;
+  return cuda_st(launch_select_rows(n_rows, token_tag, tag, rows, n_selected, stream));
+}
+
+h3_status h3_final_adaln_table(const h3_block_config* cfg, const float* w_fin, const float* b_fin,
+                               const float* t_cond, int32_t n_timesteps, float* table, cudaStream_t stream) {
+  h3_status s = check_cfg(cfg);
+  if (s != H3_OK) return s;
+  if (n_timesteps < 1 || n_timesteps > 16) return H3_ERR_UNSUPPORTED;
+  if (!w_fin || !t_cond || !table) return H3_ERR_NULL;
+  if (!al16(w_fin) || !al16(t_cond) || !al16n(b_fin) || !al16(table)) return H3_ERR_ALIGN;
+  return cuda_st(launch_final_adaln(w_fin, b_fin, t_cond, n_timesteps, cfg->cond_dim, 2 * cfg->dim, table, stream));
+}
+
+h3_status h3_output_head(const h3_block_config* cfg, int32_t n_rows, int32_t n_sel, const int32_t* rows,
+                         const int32_t* timestep_index, int32_t n_timesteps, const void* x, const float* table,
+                         const float* w_head, const float* b_head, int32_t P, float* v_out, cudaStream_t stream) {
+  h3_status s = check_cfg(cfg);
+  if (s != H3_OK) return s;
+  if (n_rows < 1 || n_sel < 0 || n_sel > n_rows) return H3_ERR_SHAPE;
+  if (P < 1 || P > kOutputHeadMaxP || n_timesteps < 1 || n_timesteps > 16) return H3_ERR_UNSUPPORTED;
+  if (!rows || !timestep_index || !x || !table || !w_head || !v_out) return H3_ERR_NULL;
+  if (!al16(x) || !al16(table) || !al16(w_head)) return H3_ERR_ALIGN;
+  if (n_sel == 0) return H3_OK;
+  OutputHeadArgs a{};
+  a.n_sel = n_sel;
+  a.S = n_rows;
+  a.T = n_timesteps;
+  a.D = cfg->dim;
+  a.P = P;
+  a.rows = rows;
+  a.tidx = timestep_index;
+  a.x = static_cast<const __nv_bfloat16*>(x);
+  a.table = table;
+  a.w = w_head;
+  a.b = b_head;
+  a.out = v_out;
+  a.eps = cfg->eps;
+  a.err = device_error_word();
+  return cuda_st(launch_output_head(a, stream));
+}
+
 h3_status h3_sync_check(cudaStream_t stream, int32_t timeout_ms) {
   cudaEvent_t ev;
   if (cudaEventCreateWithFlags(&ev, cudaEventDisableTiming) != cudaSuccess) return H3_ERR_CUDA;

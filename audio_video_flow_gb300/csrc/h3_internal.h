@@ -194,4 +194,29 @@ int rope_qknorm_smem_bytes(int H);
 cudaError_t launch_rope_qknorm(const CUtensorMap& tmq, const CUtensorMap& tmk, const RopeArgs& a, int num_sms,
                                cudaStream_t stream);
 
+// ---------------------------------------------------------------------------
+// output side and sampler (k_output.cu)
+// ---------------------------------------------------------------------------
+struct OutputHeadArgs {
+  int n_sel, S, T, D, P;
+  const int32_t* rows;
+  const int32_t* tidx;
+  const __nv_bfloat16* x;   // [S][D]
+  const float* table;       // [T][2][D]: shift, scale
+  const float* w;           // [P][D]
+  const float* b;           // [P] or null
+  float* out;               // [n_sel][P]
+  float eps;
+  uint32_t* err;
+};
+constexpr int kOutputHeadMaxP = 128;
+cudaError_t launch_sigma_grid(int n, float s, float* sigmas, int32_t* count, cudaStream_t st);
+cudaError_t launch_ode_step(long long n, const float* xt, const float* v, float sigma, float sigma_next, float* out,
+                            cudaStream_t st);
+cudaError_t launch_noise_mix(long long n, const float* x0, const float* noise, float t, float* out, cudaStream_t st);
+cudaError_t launch_select_rows(int n, const int32_t* tags, int tag, int32_t* rows, int32_t* count, cudaStream_t st);
+cudaError_t launch_final_adaln(const float* w, const float* b, const float* t_cond, int T, int C, int rows,
+                               float* out, cudaStream_t st);
+cudaError_t launch_output_head(const OutputHeadArgs& a, cudaStream_t st);
+
 }  // namespace h3

@@ -44,8 +44,8 @@ STAGES = ("adaln_table", "norm1_modulate", "qkv_qknorm_rope", "attention", "out_
 # hit L2), so the 32,768- and 15,860-row values are the 16,384-row capture
 # scaled by the row count.
 TRAFFIC = {
-    "qkv_qknorm_rope@block505": 252453632,
-    "fc1_swiglu@block1824": 380734720,
+    "qkv_qknorm_rope@block505": 251573760,
+    "fc1_swiglu@block1824": 390174976,
     "attention@attn4096": 214684160,
     "attention@attn16384": 919471872,
     "attention@attn32768": 1838943744,
@@ -287,6 +287,115 @@ def run_attention_core(args, ws_n: int, rank: int, local: int):
     return line
 
 
+FP32_LANES_PER_SM = 128   # fp32 FMA lanes per SM (4 sub-partitions x 32)
+
+
+def alu_fp32_peak_tflops(sm_mhz: float, n_sms: int) -> float:
+    """FP32 FMA peak: SMs x 128 lanes x 2 FLOP x clock."""
+    return n_sms * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12
+
+
+def run_output_side(args, ws_n: int, rank: int, local: int):
+    """One evaluation's output side at the 15,860-row shape: row selection,
+    FP32 final AdaLN table of both modalities, the FP32 velocity heads and the
+    two Euler steps on the patch-packed fp32 latents."""
+    import torch
+    import audio_video_flow_gb300 as h3
+    import h3_inputs as hi
+
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    wl = hi.WORKLOADS[args.workload]
+    shape, S, T = wl.shape, wl.layout.n_rows, wl.n_timesteps
+    D, C = shape.dim, shape.cond_dim
+    cfg = h3.make_config(D, shape.n_heads, shape.ffn_dim, C)
+    meta = {k: v.to(dev) for k, v in hi.packed_metadata(wl.layout, T, args.seed).items()}
+    acts = hi.activations(shape, S, T, args.seed, device=dev)
+    ow = hi.output_weights(shape, args.seed, device=dev)
+    mods = [("video", 0, hi.VIDEO_PATCH, wl.layout.n_video), ("audio", 2, hi.AUDIO_PATCH, wl.layout.n_audio)]
+    rows = {m: torch.empty(S, dtype=torch.int32, device=dev) for m, *_ in mods}
+    cnt = {m: torch.zeros(1, dtype=torch.int32, device=dev) for m, *_ in mods}
+    tab = {m: torch.empty(T, 2, D, dtype=torch.float32, device=dev) for m, *_ in mods}
+    vel = {m: torch.empty(n, P, dtype=torch.float32, device=dev) for m, _, P, n in mods}
+    lat = {m: hi.latents(n, P, args.seed, 74 + i, device=dev) for i, (m, _, P, n) in enumerate(mods)}
+    sig = {"video": (0.9, 0.8), "audio": (0.75, 0.6)}
+    stream = torch.cuda.current_stream()
+    n = args.steps
+    names = ["select_rows", "final_adaln_table", "output_head", "ode_step"]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(n)]
+
+    def step(i=None):
+        rec = (lambda k: ev[i][k].record(stream)) if i is not None else (lambda k: None)
+        rec(0)
+        for m, tag, P, nr in mods:
+            h3.h3_select_rows(S, meta["token_tag"], tag, rows[m], cnt[m])
+        rec(1)
+        for m, tag, P, nr in mods:
+            h3.h3_final_adaln_table(cfg, ow[f"w_fin_{m}"], ow[f"b_fin_{m}"], acts["t_cond"], T, tab[m])
+        rec(2)
+        for m, tag, P, nr in mods:
+            h3.h3_output_head(cfg, S, nr, rows[m], meta["timestep_index"], T, acts["x"], tab[m],
+                              ow[f"w_head_{m}"], ow[f"b_head_{m}"], P, vel[m])
+        rec(3)
+        for m, tag, P, nr in mods:
+            h3.h3_ode_step(lat[m].numel(), lat[m], vel[m], sig[m][0], sig[m][1], lat[m])
+        rec(4)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    for e3 in ev:
+        for e in e3:
+            e.record(stream)
+    head_flops = sum(2.0 * nr * P * D for _, _, P, nr in mods)
+    table_bytes = 2 * (2 * D * C * 4)
+    ode_bytes = sum(3 * 4 * nr * P for _, _, P, nr in mods)
+    with ClockSampler(local) as clk:
+        barrier(ws_n)
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for i in range(n):
+            step(i)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        barrier(ws_n)
+    status = h3.h3_sync_check(timeout_ms=60000)
+    if status != 0:
+        raise RuntimeError(f"device error: {h3.status_string(status)}")
+    elapsed_ms, units = aggregate(t0.elapsed_time(t1), n * head_flops, ws_n)
+    st = {nm: statistics.mean(e[k].elapsed_time(e[k + 1]) for e in ev) for k, nm in enumerate(names)}
+    clocks = clk.summary()
+    peak = alu_fp32_peak_tflops(clocks.get("sm_max_mhz") or 2070.0, torch.cuda.get_device_properties(dev).multi_processor_count)
+    head_tf = head_flops / (st["output_head"] * 1e-3) / 1e12
+    peaks = load_peaks()
+    return {
+        "metric": METRIC, "value": round(units / (elapsed_ms * 1e-3) / 1e12, 4), "unit": "TFLOP/s",
+        "n_gpus": ws_n, "steps": n, "warmup": args.warmup, "ms_per_step": round(elapsed_ms / n, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "tokens_per_s": round(ws_n * S * n / (elapsed_ms * 1e-3), 1),
+        "config": {"workload": wl.name, "description": wl.description, "rows": S,
+                   "video_rows": wl.layout.n_video, "audio_rows": wl.layout.n_audio, "dim": D, "cond": C,
+                   "flop_per_step": head_flops, "l2": "inputs larger than L2: 231 MB of fp32 final-AdaLN "
+                   "weights re-read every step", "parallelism": f"replicas x{ws_n}"},
+        "e2e": None, "gpu_launches": 8 * n,
+        "roofline": {"kernel": "output_head", "bound": "alu", "achieved": round(head_tf, 2),
+                     "peak": round(peak, 1), "unit": "TFLOP/s", "frac": round(head_tf / peak, 4),
+                     "peak_source": "fp32 FMA lanes x 2 x max SM clock", "traffic": None},
+        "stages": {
+            "select_rows": {"us": round(st["select_rows"] * 1e3, 2)},
+            "final_adaln_table": {"us": round(st["final_adaln_table"] * 1e3, 2),
+                                  "gbs": round(table_bytes / (st["final_adaln_table"] * 1e-3) / 1e9, 1),
+                                  "hbm_frac": round(table_bytes / (st["final_adaln_table"] * 1e-3) / 1e9
+                                                    / peaks["hbm_gbs"], 4)},
+            "output_head": {"us": round(st["output_head"] * 1e3, 2), "tflops": round(head_tf, 2)},
+            "ode_step": {"us": round(st["ode_step"] * 1e3, 2),
+                         "gbs": round(ode_bytes / (st["ode_step"] * 1e-3) / 1e9, 1)},
+        },
+        "clocks": clocks,
+    }
+
+
 def run_ours(args, ws_n: int, rank: int, local: int):
     import torch
     import audio_video_flow_gb300 as h3
@@ -297,6 +406,8 @@ def run_ours(args, ws_n: int, rank: int, local: int):
     wl = hi.WORKLOADS[args.workload]
     if wl.name.startswith("attn"):
         return run_attention_core(args, ws_n, rank, local)
+    if wl.name.startswith("output"):
+        return run_output_side(args, ws_n, rank, local)
     shape, S, T, NB = wl.shape, wl.layout.n_rows, wl.n_timesteps, wl.n_blocks
     cfg = h3.make_config(shape.dim, shape.n_heads, shape.ffn_dim, shape.cond_dim)
     meta_c, acts_c, _ = hi.workload_inputs(wl, seed=args.seed, device="cpu", block=0) if NB == 1 else \

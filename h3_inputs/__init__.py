@@ -90,6 +90,10 @@ WORKLOADS: Dict[str, Workload] = {
         "denoiser15860", H3_SHAPE, PackedLayout(256, (36, 15, 27), 1024), n_timesteps=1,
         n_blocks=50,
         description="50-block denoiser forward at the 864x480 141-frame shape, 15860 rows"),
+    "output15860": Workload(
+        "output15860", H3_SHAPE, PackedLayout(256, (36, 15, 27), 1024), n_timesteps=1, n_blocks=0,
+        description="output side of one evaluation at the 15860-row shape: row selection, FP32 final "
+                    "AdaLN of both modalities, FP32 heads (14580 x 96, 1024 x 32), both Euler steps"),
     "attn4096": Workload(
         "attn4096", H3_SHAPE, PackedLayout(86, (9, 20, 20), 410), n_timesteps=1,
         description="attention core alone, 4096 packed rows"),
@@ -205,6 +209,31 @@ def attention_inputs(shape: BlockShape, n_rows: int, seed: int = 0,
         "q_norm_g": normal((d,), 0.1, 1.0, seed, 21, device),
         "k_norm_g": normal((d,), 0.1, 1.0, seed, 22, device),
     }
+
+
+VIDEO_PATCH, AUDIO_PATCH = 96, 32   # latent channels per video / audio row
+
+
+def output_weights(shape: BlockShape, seed: int = 0, device: str = "cpu") -> Dict[str, torch.Tensor]:
+    """Random-init FP32 weights of the final layer: per modality (video, audio)
+    a final AdaLN projection w_fin [2*D][C] (shift rows, then scale rows) with
+    bias b_fin [2*D], and a head w_head [P][D] with bias b_head [P]
+    (P = 96 video, 32 audio); all ~N(0, 0.02) in fp32."""
+    D, C = shape.dim, shape.cond_dim
+    n = lambda shp, k: normal(shp, 0.02, 0.0, seed, 60 + k, device, dtype=torch.float32)
+    return {
+        "w_fin_video": n((2 * D, C), 0), "b_fin_video": n((2 * D,), 1),
+        "w_fin_audio": n((2 * D, C), 2), "b_fin_audio": n((2 * D,), 3),
+        "w_head_video": n((VIDEO_PATCH, D), 4), "b_head_video": n((VIDEO_PATCH,), 5),
+        "w_head_audio": n((AUDIO_PATCH, D), 6), "b_head_audio": n((AUDIO_PATCH,), 7),
+    }
+
+
+def latents(n_rows: int, width: int, seed: int = 0, tensor_id: int = 70,
+            device: str = "cpu") -> torch.Tensor:
+    """Patch-packed fp32 latent rows [n_rows][width] ~N(0, 1) (noisy latents,
+    velocities or noise for the sampler)."""
+    return normal((n_rows, width), 1.0, 0.0, seed, tensor_id, device, dtype=torch.float32)
 
 
 def workload_inputs(w: Workload, seed: int = 0, device: str = "cpu", block: int = 0):

@@ -282,6 +282,74 @@ h3_status h3_linear(int32_t M, int32_t N, int32_t K, const void *x, const void *
                     const void *b, void *y, cudaStream_t stream);
 
 /* ----------------------------------------------------------------------- */
+/* Output side and sampler of one denoiser evaluation                      */
+/* ----------------------------------------------------------------------- */
+
+/* Sigma grid of one modality's scheduler (RFC s2 "Scheduler fingerprint":
+ * sigma transform s*sigma/(1+(s-1)*sigma), grid = shifted linspace(1, 0,
+ * n_points) with consecutive fp32 duplicates removed; s5 h3_sigma_schedule).
+ * Point i is the fp64 value 1 - i/(n_points-1) rounded to fp32, shifted in
+ * fp32 with one rounding per operation (num = s*sigma, den = 1 + (s-1)*sigma,
+ * num/den); a terminal zero is appended and consecutive equal values
+ * collapsed (the linspace's own zero and the terminal zero become one), so
+ * the grid holds n_points values and n_points - 1 model evaluations.  The
+ * video scheduler uses shift 12, the audio one 3.  sigmas: device float
+ * [n_points + 1] (the first *n_sigmas used); n_sigmas: device int32.  Both are
+ * written by the device (read them after the stream).  Errors:
+ * n_points < 2 or > 1048576, shift not finite or <= 0 -> H3_ERR_SHAPE;
+ * NULL -> H3_ERR_NULL. */
+h3_status h3_sigma_schedule(int32_t n_points, float shift, float *sigmas, int32_t *n_sigmas,
+                            cudaStream_t stream);
+
+/* One Euler step of the data-ward flow (RFC s2 "Velocity convention" x0 = xt +
+ * sigma*v and "Euler update" x_next = r*xt + (1-r)*x0 with r =
+ * sigma_next/sigma; s5 h3_ode_step): fp32, one rounding per operation in that
+ * order, no fused multiply-add, so the result is bit-reproducible.  xt, v,
+ * x_next: device float [n], 16-byte aligned; x_next may alias xt.  sigma must
+ * be finite and > 0, sigma_next finite and >= 0 (H3_ERR_SHAPE otherwise);
+ * n = 0 does nothing. */
+h3_status h3_ode_step(int64_t n, const float *xt, const float *v, float sigma, float sigma_next,
+                      float *x_next, cudaStream_t stream);
+
+/* Conditioning-anchor noise mix out = t*x0 + (1-t)*noise (RFC s5
+ * conditioning_noise_mix), fp32 as written.  All arrays device float [n],
+ * 16-byte aligned; out may alias either input.  t finite in [0, 1]. */
+h3_status h3_noise_mix(int64_t n, const float *x0, const float *noise, float t, float *out,
+                       cudaStream_t stream);
+
+/* Rows of one modality in packed order (RFC s5 packed_index_select): rows
+ * receives the indices i < n_rows with token_tag[i] == tag, ascending, and
+ * n_selected their count (both device memory, written by the device).
+ * token_tag and rows: device int32 [n_rows]. */
+h3_status h3_select_rows(int32_t n_rows, const int32_t *token_tag, int32_t tag, int32_t *rows,
+                         int32_t *n_selected, cudaStream_t stream);
+
+/* Final AdaLN table of one modality (RFC s5 final_adaln_out; the ledger's
+ * "H3 final layer"): table[t][0][:] = shift, table[t][1][:] = scale, from
+ * SiLU(t_cond[t]) W_fin^T + b_fin in fp32 (an FP32 module of the RFC s2
+ * mixed-precision table).  w_fin fp32 [2D][C] (rows 0..D-1 shift, D..2D-1
+ * scale), b_fin fp32 [2D] or NULL, t_cond fp32 [T][C], table fp32 [T][2][D];
+ * D = cfg->dim, C = cfg->cond_dim, 1 <= T <= 16.  All device pointers. */
+h3_status h3_final_adaln_table(const h3_block_config *cfg, const float *w_fin, const float *b_fin,
+                               const float *t_cond, int32_t n_timesteps, float *table,
+                               cudaStream_t stream);
+
+/* Velocity head of one modality (RFC s5 video_output_projection_fp32 5376 ->
+ * 96, audio_output_projection_fp32 5376 -> 32): for i < n_sel and r = rows[i],
+ *   m = RMSNorm(x[r]) * (1 + table[tidx[r]][1]) + table[tidx[r]][0]
+ * (plain RMSNorm, no gain, eps cfg->eps, fp32), then v_out[i] = m W_head^T +
+ * b_head in fp32.  x bf16 [n_rows][D]; rows device int32 [n_sel] (e.g. from
+ * h3_select_rows); timestep_index device int32 [n_rows]; table fp32 [T][2][D];
+ * w_head fp32 [P][D]; b_head fp32 [P] or NULL; v_out fp32 [n_sel][P];
+ * 1 <= P <= 128.  A row index or timestep index out of range is reported
+ * through the device error word (h3_sync_check -> H3_ERR_INDEX) and its
+ * output row left unwritten. */
+h3_status h3_output_head(const h3_block_config *cfg, int32_t n_rows, int32_t n_sel,
+                         const int32_t *rows, const int32_t *timestep_index, int32_t n_timesteps,
+                         const void *x, const float *table, const float *w_head, const float *b_head,
+                         int32_t P, float *v_out, cudaStream_t stream);
+
+/* ----------------------------------------------------------------------- */
 /* Status, errors, provenance                                               */
 /* ----------------------------------------------------------------------- */
 
