@@ -39,6 +39,9 @@ below):
   R8 softmax scale 1/sqrt(128), no mask, exact exp.
   R9 FC1 rows 0..F-1 are the gate (SiLU'd), rows F..2F-1 the value.
   R10 QKV weight rows interleaved per head as [H][q,k,v][128].
+  R11 token refiner: the block without AdaLN modulation or RoPE (norm gains,
+      per-head Q/K RMSNorm, SwiGLU kept), residuals without a gate, and a
+      final RMSNorm with its own gain after the last refiner block.
 """
 from __future__ import annotations
 
@@ -339,3 +342,50 @@ def blocks_forward(x, token_tag, timestep_index, pos_thw, t_cond, weights_list, 
     for w in weights_list:
         x = block_forward(x, token_tag, timestep_index, pos_thw, t_cond, w, eps)["y"]
     return x
+
+
+# ---------------------------------------------------------------------------
+# token refiner ([RFC] s2 fingerprint rows "Text-refiner layers" 2 and "Text
+# projection" 5120 -> 5376 then the 2-layer token refiner; s5 work item
+# token_refiner_block: two pre-norm attention/FFN blocks without AdaLN or
+# RoPE; [LEDGER] "Current Runtime Scope": the refiner ends with a final
+# RMSNorm).  Reading R11: everything else is the block above - per-channel
+# norm gains, per-head Q/K RMSNorm, full unmasked attention over the refined
+# rows, SwiGLU - and the residuals carry no gate.
+# ---------------------------------------------------------------------------
+
+def rmsnorm(x: np.ndarray, gain: np.ndarray, eps: float = EPS) -> np.ndarray:
+    """h = bf16(rms(x) * g): the block norm without modulation."""
+    x = np.asarray(x, np.float64)
+    return bf16_round(x * rms_inv(x, eps) * np.asarray(gain, np.float64)[None, :])
+
+
+def refiner_block_forward(x: np.ndarray, w: Dict[str, Optional[np.ndarray]], eps: float = EPS) -> Dict[str, np.ndarray]:
+    """One token-refiner block: pre-norm attention then pre-norm SwiGLU FFN,
+    each added back to the residual stream with one bf16 cast."""
+    S = x.shape[0]
+    x = np.asarray(x, np.float64)
+    h1 = rmsnorm(x, w["norm1_g"], eps)
+    qkv = linear(h1, w["w_qkv"], w.get("b_qkv"))
+    H = qkv.shape[1] // (3 * HEAD_DIM)
+    qkv = qkv.reshape(S, H, 3, HEAD_DIM)
+    q = head_rmsnorm(qkv[:, :, 0, :], w["q_norm_g"], eps)
+    k = head_rmsnorm(qkv[:, :, 1, :], w["k_norm_g"], eps)
+    v = np.asarray(qkv[:, :, 2, :], np.float64)
+    o = attention(q, k, v, np.arange(S))
+    x1 = bf16_round(x + linear(o, w["w_o"], w.get("b_o")))
+    h2 = rmsnorm(x1, w["norm2_g"], eps)
+    gu = linear(h2, w["w_fc1"], w.get("b_fc1"))
+    F = gu.shape[1] // 2
+    a = swiglu(gu[:, :F], gu[:, F:])
+    y = bf16_round(x1 + linear(a, w["w_fc2"], w.get("b_fc2")))
+    return {"h1": h1, "q": q, "k": k, "v": v, "o": o, "x1": x1, "h2": h2, "a": a, "y": y}
+
+
+def refiner_forward(x: np.ndarray, weights_list, final_norm_g: Optional[np.ndarray],
+                    eps: float = EPS) -> np.ndarray:
+    """The refiner blocks in order, then the final RMSNorm (skipped when no
+    gain is given)."""
+    for w in weights_list:
+        x = refiner_block_forward(x, w, eps)["y"]
+    return rmsnorm(x, final_norm_g, eps) if final_norm_g is not None else x

@@ -469,3 +469,39 @@ def test_attention_probs_brute_force(rng):
         e = [math.exp(sum(q[i, c] * k[j, c] for c in range(128)) / math.sqrt(128)) for j in range(S)]
         for j in range(S):
             assert abs(p[i, j] - e[j] / sum(e)) < 1e-14
+
+
+# ---------------------------------------------------------------- token refiner
+
+def _refiner_case(S=11, D=64, H=2, F=96, seed=21):
+    rng = np.random.default_rng(seed)
+    b = lambda a: O.bf16_round(a)
+    w = {"norm1_g": b(1 + 0.1 * rng.standard_normal(D)), "norm2_g": b(1 + 0.1 * rng.standard_normal(D)),
+         "w_qkv": b(0.1 * rng.standard_normal((3 * H * 128, D))), "q_norm_g": b(1 + 0.1 * rng.standard_normal(128)),
+         "k_norm_g": b(1 + 0.1 * rng.standard_normal(128)), "w_o": b(0.05 * rng.standard_normal((D, H * 128))),
+         "w_fc1": b(0.1 * rng.standard_normal((2 * F, D))), "w_fc2": b(0.1 * rng.standard_normal((D, F)))}
+    x = b(rng.standard_normal((S, D)))
+    return x, w
+
+
+def test_refiner_equals_block_with_identity_modulation_and_zero_positions():
+    # the same arithmetic as the block: shift = scale = 0, gates = 1, RoPE at position 0
+    x, w = _refiner_case()
+    S, D = x.shape
+    C = 8
+    wb = dict(w, w_ada=np.zeros((18 * D, C)),
+              b_ada=np.tile(np.repeat(np.array([0, 0, 1, 0, 0, 1], float), D), 3))
+    ref = O.block_forward(x, np.ones(S, np.int32), np.zeros(S, np.int32), np.zeros((S, 3), np.int32),
+                          np.zeros((1, C)), wb)["y"]
+    np.testing.assert_array_equal(O.refiner_block_forward(x, w)["y"], ref)
+
+
+def test_refiner_permutation_equivariant_and_residual_identity():
+    x, w = _refiner_case()
+    y = O.refiner_forward(x, [w, w], w["norm2_g"])
+    perm = np.random.default_rng(2).permutation(x.shape[0])
+    np.testing.assert_allclose(O.refiner_forward(x[perm], [w, w], w["norm2_g"]), y[perm], rtol=0, atol=1e-12)
+    w0 = dict(w, w_o=np.zeros_like(w["w_o"]), w_fc2=np.zeros_like(w["w_fc2"]))
+    np.testing.assert_array_equal(O.refiner_block_forward(x, w0)["y"], x)      # zero sublayers: y = x
+    ones = O.refiner_forward(x, [], np.ones(x.shape[1]))
+    np.testing.assert_allclose(np.sqrt(np.mean(ones ** 2, axis=1)), 1.0, rtol=1e-2)   # final norm: unit RMS
