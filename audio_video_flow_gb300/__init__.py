@@ -80,6 +80,8 @@ def lib() -> ctypes.CDLL:
             "h3_ffn_up_swiglu": (i32, [cfgp, i32, vp, vp, vp, vp, vp]),
             "h3_ffn_down_residual": (i32, [cfgp, mp, vp, vp, vp, vp, vp, vp, vp]),
             "h3_linear": (i32, [i32, i32, i32, vp, vp, vp, vp, vp]),
+            "h3_refiner_workspace_bytes": (sz, [cfgp, i32]),
+            "h3_refiner_forward": (i32, [cfgp, i32, wp, vp, i32, vp, vp, vp, sz, vp]),
             "h3_sigma_schedule": (i32, [i32, ctypes.c_float, vp, vp, vp]),
             "h3_ode_step": (i32, [c_int64, vp, vp, ctypes.c_float, ctypes.c_float, vp, vp]),
             "h3_noise_mix": (i32, [c_int64, vp, vp, ctypes.c_float, vp, vp]),
@@ -250,6 +252,19 @@ def h3_ffn_down_residual(cfg, meta, table, a, w_fc2, b_fc2, x1, y_out, stream=No
 
 def h3_linear(M: int, N: int, K: int, x, w, b, y, stream=None) -> None:
     _check(lib().h3_linear(M, N, K, _ptr(x), _ptr(w), _ptr(b), _ptr(y), _stream(stream)), "h3_linear")
+
+
+def h3_refiner_workspace_bytes(cfg: BlockConfig, n_rows: int) -> int:
+    return int(lib().h3_refiner_workspace_bytes(ctypes.byref(cfg), n_rows))
+
+
+def h3_refiner_forward(cfg, weights_list: Sequence[BlockWeights], final_norm_g, n_rows: int, x_in, x_out,
+                       workspace, stream=None) -> None:
+    arr = (BlockWeights * max(len(weights_list), 1))(*weights_list)
+    _check(lib().h3_refiner_forward(ctypes.byref(cfg), len(weights_list), arr, _ptr(final_norm_g), n_rows,
+                                    _ptr(x_in), _ptr(x_out), _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(), _stream(stream)),
+           "h3_refiner_forward")
 
 
 def h3_sigma_schedule(n_points: int, shift: float, sigmas, n_sigmas, stream=None) -> None:

@@ -567,6 +567,80 @@ h3_status h3_blocks_forward(const h3_block_config* cfg, int32_t n_blocks, const 
   return H3_OK;
 }
 
+// ===========================================================================
+// token refiner: the block's stages with the identity AdaLN table and
+// text / timestep-0 / zero-position metadata written into the workspace
+// ===========================================================================
+namespace {
+size_t refiner_meta_bytes(int64_t S) { return al256((size_t)5 * (size_t)S * 4); }
+
+h3_status check_refiner_weights(const h3_block_weights* w) {
+  if (!w) return H3_ERR_NULL;
+  const void* req[] = {w->norm1_g, w->norm2_g, w->w_qkv, w->q_norm_g, w->k_norm_g, w->w_o, w->w_fc1, w->w_fc2};
+  for (const void* p : req) {
+    if (!p) return H3_ERR_NULL;
+    if (!al16(p)) return H3_ERR_ALIGN;
+  }
+  const void* opt[] = {w->b_qkv, w->b_o, w->b_fc1, w->b_fc2};
+  for (const void* p : opt)
+    if (!al16n(p)) return H3_ERR_ALIGN;
+  return H3_OK;
+}
+}  // namespace
+
+size_t h3_refiner_workspace_bytes(const h3_block_config* cfg, int32_t n_rows) {
+  if (check_cfg(cfg) != H3_OK || n_rows < 1) return 0;
+  return ws_layout(*cfg, n_rows, 1).total + refiner_meta_bytes(n_rows);
+}
+
+h3_status h3_refiner_forward(const h3_block_config* cfg, int32_t n_blocks, const h3_block_weights* w,
+                             const void* final_norm_g, int32_t n_rows, const void* x_in, void* x_out,
+                             void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  h3_status s = check_cfg(cfg);
+  if (s != H3_OK) return s;
+  if (n_rows < 1 || n_blocks < 0 || (n_blocks == 0 && !final_norm_g)) return H3_ERR_SHAPE;
+  if (n_blocks > 0 && !w) return H3_ERR_NULL;
+  for (int b = 0; b < n_blocks; ++b)
+    if ((s = check_refiner_weights(&w[b])) != H3_OK) return s;
+  if (!x_in || !x_out || !workspace) return H3_ERR_NULL;
+  if (!al16(x_in) || !al16(x_out) || !al16n(final_norm_g) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return H3_ERR_ALIGN;
+  const WsLayout L = ws_layout(*cfg, n_rows, 1);
+  if (ws_bytes < L.total + refiner_meta_bytes(n_rows)) return H3_ERR_WORKSPACE;
+  uint8_t* base = static_cast<uint8_t*>(workspace);
+  void* table = base + L.table;
+  void* h = base + L.h;
+  void* qkv = base + L.qkv;
+  void* o = base + L.o;
+  void* x1 = base + L.x1;
+  int32_t* tag = reinterpret_cast<int32_t*>(base + L.total);
+  int32_t* tidx = tag + n_rows;
+  int32_t* pos = tidx + n_rows;
+  const int S = n_rows, I = cfg->n_heads * 128;
+  if ((s = cuda_st(launch_refiner_setup(S, cfg->dim, static_cast<__nv_bfloat16*>(table), tag, tidx, pos,
+                                        stream))) != H3_OK)
+    return s;
+  const h3_packed_meta m{S, 1, tag, tidx, pos, nullptr};
+  for (int b = 0; b < n_blocks; ++b) {
+    const void* xi = b == 0 ? x_in : x_out;
+    const h3_block_weights& wb = w[b];
+    const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(qkv);
+    if ((s = run_modulate(*cfg, m, table, 0, xi, wb.norm1_g, h, stream)) != H3_OK) return s;
+    if ((s = run_qkv(*cfg, m, h, wb.w_qkv, wb.b_qkv, wb.q_norm_g, wb.k_norm_g, qkv, stream)) != H3_OK) return s;
+    if ((s = run_attention(S, cfg->n_heads, q, q + 128, q + 256, 3 * I, 384, o, nullptr, stream)) != H3_OK)
+      return s;
+    if ((s = run_resid_gemm(*cfg, m, table, 2, o, I, wb.w_o, wb.b_o, xi, x1, stream)) != H3_OK) return s;
+    if ((s = run_modulate(*cfg, m, table, 1, x1, wb.norm2_g, h, stream)) != H3_OK) return s;
+    if ((s = run_ffn_up(*cfg, S, h, wb.w_fc1, wb.b_fc1, qkv, stream)) != H3_OK) return s;
+    if ((s = run_resid_gemm(*cfg, m, table, 5, qkv, cfg->ffn_dim, wb.w_fc2, wb.b_fc2, x1, x_out, stream)) != H3_OK)
+      return s;
+  }
+  if (final_norm_g)   // row-local, so in place on x_out
+    if ((s = run_modulate(*cfg, m, table, 0, n_blocks > 0 ? x_out : x_in, final_norm_g, x_out, stream)) != H3_OK)
+      return s;
+  return H3_OK;
+}
+
 size_t h3_adaln_table_workspace_bytes(const h3_block_config* cfg) {
   if (check_cfg(cfg) != H3_OK) return 0;
   return adaln_scratch_bytes(*cfg);

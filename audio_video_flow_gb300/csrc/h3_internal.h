@@ -194,6 +194,10 @@ int rope_qknorm_smem_bytes(int H);
 cudaError_t launch_rope_qknorm(const CUtensorMap& tmq, const CUtensorMap& tmk, const RopeArgs& a, int num_sms,
                                cudaStream_t stream);
 
+// token refiner: identity AdaLN table [3][6][D] and text / timestep-0 / zero-position metadata
+cudaError_t launch_refiner_setup(int S, int D, __nv_bfloat16* table, int32_t* tag, int32_t* tidx, int32_t* pos,
+                                 cudaStream_t st);
+
 // ---------------------------------------------------------------------------
 // output side and sampler (k_output.cu)
 // ---------------------------------------------------------------------------

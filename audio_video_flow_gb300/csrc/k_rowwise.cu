@@ -319,4 +319,41 @@ cudaError_t launch_rope_qknorm(const CUtensorMap& tmq, const CUtensorMap& tmk, c
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// Token refiner set-up: the block's kernels run the refiner when the AdaLN
+// table is the identity modulation (shift 0, scale 0, gate 1 in all six
+// chunks of the three modality rows of timestep 0) and every row is a text
+// row at timestep 0 and position (0, 0, 0), where MM-RoPE is the identity.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) refiner_setup_kernel(int S, int D, __nv_bfloat16* __restrict__ table,
+                                                            int32_t* __restrict__ tag, int32_t* __restrict__ tidx,
+                                                            int32_t* __restrict__ pos) {
+  griddep_launch_dependents();
+  griddep_wait();
+  const int n_tab = 3 * 6 * D;
+  const int n = n_tab + 5 * S;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+    if (i < n_tab) {
+      const int chunk = (i / D) % 6;
+      table[i] = __float2bfloat16_rn((chunk == 2 || chunk == 5) ? 1.0f : 0.0f);
+    } else {
+      const int j = i - n_tab;
+      if (j < S) tag[j] = 1;             // text
+      else if (j < 2 * S) tidx[j - S] = 0;
+      else pos[j - 2 * S] = 0;
+    }
+  }
+}
+
+cudaError_t launch_refiner_setup(int S, int D, __nv_bfloat16* table, int32_t* tag, int32_t* tidx, int32_t* pos,
+                                 cudaStream_t st) {
+  const long long n = 18LL * D + 5LL * S;
+  int grid = (int)((n + 255) / 256);
+  if (grid > 4 * num_sms()) grid = 4 * num_sms();
+  cudaError_t e = launch_kernel(refiner_setup_kernel, dim3(grid), dim3(256), 0, st, S, D, table, tag, tidx, pos);
+  if (e != cudaSuccess) return e;
+  set_kernel_info("refiner_setup_kernel identity-table rows=%d", S);
+  return cudaGetLastError();
+}
+
 }  // namespace h3

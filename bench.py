@@ -396,6 +396,66 @@ def run_output_side(args, ws_n: int, rank: int, local: int):
     }
 
 
+def run_refiner(args, ws_n: int, rank: int, local: int):
+    """The 2-layer token refiner and its final RMSNorm over the text rows."""
+    import torch
+    import audio_video_flow_gb300 as h3
+    import h3_inputs as hi
+
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    wl = hi.WORKLOADS[args.workload]
+    shape, S, NB = wl.shape, wl.layout.n_rows, wl.n_blocks
+    cfg = h3.make_config(shape.dim, shape.n_heads, shape.ffn_dim, shape.cond_dim)
+    wts = [hi.block_weights(shape, args.seed, 60 + b, device=dev) for b in range(NB)]
+    for w in wts:
+        w["w_ada"] = w["b_ada"] = None          # the refiner has no AdaLN
+    cw = [h3.make_weights(w) for w in wts]
+    gfin = hi.normal((shape.dim,), 0.1, 1.0, args.seed, 90, device=dev)
+    x = hi.normal((S, shape.dim), 1.0, 0.0, args.seed, 91, device=dev)
+    y = torch.empty_like(x)
+    ws = torch.empty(h3.h3_refiner_workspace_bytes(cfg, S), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    work = stage_work(shape, S, 1)
+    flops_step = NB * sum(f for k, (f, _) in work.items() if k != "adaln_table")
+    for _ in range(args.warmup):
+        h3.h3_refiner_forward(cfg, cw, gfin, S, x, y, ws)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        barrier(ws_n)
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(args.steps):
+            h3.h3_refiner_forward(cfg, cw, gfin, S, x, y, ws)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        barrier(ws_n)
+    status = h3.h3_sync_check(timeout_ms=60000)
+    if status != 0:
+        raise RuntimeError(f"device error: {h3.status_string(status)}")
+    elapsed_ms, units = aggregate(t0.elapsed_time(t1), args.steps * flops_step, ws_n)
+    peaks = load_peaks()
+    t_peak, t_src = tensor_peak(peaks, elapsed_ms)
+    achieved = units / (elapsed_ms * 1e-3) / 1e12
+    return {
+        "metric": METRIC, "value": round(achieved, 3), "unit": "TFLOP/s", "n_gpus": ws_n, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(elapsed_ms / args.steps, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "tokens_per_s": round(ws_n * S * args.steps / (elapsed_ms * 1e-3), 1),
+        "config": {"workload": wl.name, "description": wl.description, "rows": S, "blocks": NB,
+                   "dim": shape.dim, "heads": shape.n_heads, "ffn": shape.ffn_dim, "flop_per_step": flops_step,
+                   "l2": "inputs larger than L2: %.2f GB of refiner weights re-read every step" %
+                         (NB * (weight_bytes(shape) - 2 * 18 * shape.dim * shape.cond_dim) / 1e9),
+                   "parallelism": f"replicas x{ws_n}"},
+        "e2e": None, "gpu_launches": args.steps * (1 + 7 * NB + 1),
+        "roofline": {"kernel": "refiner_step", "bound": "tensor", "achieved": round(achieved, 1), "peak": t_peak,
+                     "unit": "TFLOP/s", "frac": round(achieved / t_peak, 4), "peak_source": t_src,
+                     "traffic": None, "note": "whole step (all launches), not one kernel"},
+        "clocks": clk.summary(),
+    }
+
+
 def run_ours(args, ws_n: int, rank: int, local: int):
     import torch
     import audio_video_flow_gb300 as h3
@@ -408,6 +468,8 @@ def run_ours(args, ws_n: int, rank: int, local: int):
         return run_attention_core(args, ws_n, rank, local)
     if wl.name.startswith("output"):
         return run_output_side(args, ws_n, rank, local)
+    if wl.name.startswith("refiner"):
+        return run_refiner(args, ws_n, rank, local)
     shape, S, T, NB = wl.shape, wl.layout.n_rows, wl.n_timesteps, wl.n_blocks
     cfg = h3.make_config(shape.dim, shape.n_heads, shape.ffn_dim, shape.cond_dim)
     meta_c, acts_c, _ = hi.workload_inputs(wl, seed=args.seed, device="cpu", block=0) if NB == 1 else \

@@ -90,6 +90,9 @@ WORKLOADS: Dict[str, Workload] = {
         "denoiser15860", H3_SHAPE, PackedLayout(256, (36, 15, 27), 1024), n_timesteps=1,
         n_blocks=50,
         description="50-block denoiser forward at the 864x480 141-frame shape, 15860 rows"),
+    "refiner256": Workload(
+        "refiner256", H3_SHAPE, PackedLayout(256, (0, 0, 0), 0), n_timesteps=1, n_blocks=2,
+        description="2-layer token refiner plus final RMSNorm over 256 projected text rows"),
     "output15860": Workload(
         "output15860", H3_SHAPE, PackedLayout(256, (36, 15, 27), 1024), n_timesteps=1, n_blocks=0,
         description="output side of one evaluation at the 15860-row shape: row selection, FP32 final "

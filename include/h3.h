@@ -282,6 +282,29 @@ h3_status h3_linear(int32_t M, int32_t N, int32_t K, const void *x, const void *
                     const void *b, void *y, cudaStream_t stream);
 
 /* ----------------------------------------------------------------------- */
+/* Token refiner                                                            */
+/* ----------------------------------------------------------------------- */
+
+/* Workspace for h3_refiner_forward over n_rows rows (0 when cfg is unsupported). */
+size_t h3_refiner_workspace_bytes(const h3_block_config *cfg, int32_t n_rows);
+
+/* Token refiner over the projected text rows (RFC s2: "Text projection
+ * 5120 -> 5376, then 2-layer token refiner"; s5 token_refiner_block: pre-norm
+ * attention/FFN blocks without AdaLN or RoPE; the ledger's refiner ends with
+ * a final RMSNorm).  Each of the n_blocks blocks is the Omni-Transformer block
+ * with the modulation removed: h1 = bf16(rms(x) g1), per-head Q/K RMSNorm,
+ * full unmasked attention over the n_rows rows, x1 = bf16(x + bf16(o W_o^T +
+ * b_o)), h2 = bf16(rms(x1) g2), SwiGLU FFN, y = bf16(x1 + bf16(a W_fc2^T +
+ * b_fc2)); then, when final_norm_g is not NULL, x_out = bf16(rms(y) g_final).
+ * weights: array of n_blocks (w_ada and b_ada are not used); final_norm_g bf16
+ * [D] or NULL; x_in, x_out bf16 [n_rows][D] (may alias).  It runs the block's
+ * kernels with an identity modulation table (shift 0, scale 0, gate 1) and
+ * zero positions, written into the workspace. */
+h3_status h3_refiner_forward(const h3_block_config *cfg, int32_t n_blocks, const h3_block_weights *weights,
+                             const void *final_norm_g, int32_t n_rows, const void *x_in, void *x_out,
+                             void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* ----------------------------------------------------------------------- */
 /* Output side and sampler of one denoiser evaluation                      */
 /* ----------------------------------------------------------------------- */
 

@@ -13,8 +13,8 @@ import torch
 
 import h3_inputs as hi
 from oracle import h3_oracle as O
-from h3_testutil import (CHAIN_MAX_E, CHAIN_MEAN_E, MAX_E, MEAN_E, assert_close, errors, to_bf16,
-                         to_np)
+from h3_testutil import (CHAIN_MAX_E, CHAIN_MEAN_E, MAX_E, MEAN_E, REFINER_CHAIN_MAX_E, REFINER_CHAIN_MEAN_E,
+                         assert_close, errors, to_bf16, to_np)
 
 pytestmark = pytest.mark.gpu
 
@@ -315,6 +315,34 @@ def test_single_row_block(h3):
     c = Case(w)
     y = run_block(h3, c)
     assert_close(to_np(y), c.ref["y"], "block S=1")
+
+
+# ---------------------------------------------------------------------------
+# token refiner: two pre-norm blocks without AdaLN or RoPE, then a final norm
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("shape_name,S", [("tiny", 37), ("h3", 256)])
+def test_refiner_forward(h3, shape_name, S):
+    shape = hi.WORKLOADS["tiny72" if shape_name == "tiny" else "block505"].shape
+    wts = [hi.block_weights(shape, 0, b) for b in (7, 8)]
+    gfin = hi.normal((shape.dim,), 0.1, 1.0, 0, 90)
+    x = hi.normal((S, shape.dim), 1.0, 0.0, 0, 91)
+    ref = O.refiner_forward(to_np(x), [{k: (to_np(v) if v is not None else None) for k, v in w.items()} for w in wts],
+                            to_np(gfin))
+    cfg = h3.make_config(shape.dim, shape.n_heads, shape.ffn_dim, shape.cond_dim)
+    d_w = [{k: (v.cuda() if v is not None else None) for k, v in w.items()} for w in wts]
+    ws = torch.empty(h3.h3_refiner_workspace_bytes(cfg, S), dtype=torch.uint8, device="cuda")
+    d_x = x.cuda()
+    y = torch.empty_like(d_x)
+    h3.h3_refiner_forward(cfg, [h3.make_weights(w) for w in d_w], gfin.cuda(), S, d_x, y, ws)
+    assert h3.h3_sync_check() == 0
+    lim = (MAX_E, MEAN_E) if shape_name == "tiny" else (REFINER_CHAIN_MAX_E, REFINER_CHAIN_MEAN_E)
+    mx, mn = assert_close(to_np(y), ref, f"refiner {shape_name} S={S}", *lim)
+    print(f"refiner {shape_name} S={S}: max_e={mx:.4f} mean_e={mn:.5f}")
+    # in place, and repeatable bit for bit
+    h3.h3_refiner_forward(cfg, [h3.make_weights(w) for w in d_w], gfin.cuda(), S, d_x, d_x, ws)
+    assert h3.h3_sync_check() == 0
+    assert torch.equal(d_x, y)
 
 
 # ---------------------------------------------------------------------------
