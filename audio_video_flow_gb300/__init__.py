@@ -80,6 +80,11 @@ def lib() -> ctypes.CDLL:
             "h3_ffn_up_swiglu": (i32, [cfgp, i32, vp, vp, vp, vp, vp]),
             "h3_ffn_down_residual": (i32, [cfgp, mp, vp, vp, vp, vp, vp, vp, vp]),
             "h3_linear": (i32, [i32, i32, i32, vp, vp, vp, vp, vp]),
+            "h3_patch_pack": (i32, [i32, i32, i32, i32, vp, vp, vp]),
+            "h3_patch_unpack": (i32, [i32, i32, i32, i32, vp, vp, vp]),
+            "h3_input_projection": (i32, [cfgp, i32, i32, vp, vp, vp, vp, i32, vp, vp]),
+            "h3_packed_index_copy": (i32, [cfgp, i32, vp, vp, i32, vp, vp]),
+            "h3_timestep_embedding": (i32, [cfgp, i32, vp, vp, vp, vp, vp, vp, vp, vp]),
             "h3_refiner_workspace_bytes": (sz, [cfgp, i32]),
             "h3_refiner_forward": (i32, [cfgp, i32, wp, vp, i32, vp, vp, vp, sz, vp]),
             "h3_sigma_schedule": (i32, [i32, ctypes.c_float, vp, vp, vp]),
@@ -252,6 +257,30 @@ def h3_ffn_down_residual(cfg, meta, table, a, w_fc2, b_fc2, x1, y_out, stream=No
 
 def h3_linear(M: int, N: int, K: int, x, w, b, y, stream=None) -> None:
     _check(lib().h3_linear(M, N, K, _ptr(x), _ptr(w), _ptr(b), _ptr(y), _stream(stream)), "h3_linear")
+
+
+def h3_patch_pack(C: int, T: int, H: int, W: int, latent, rows, stream=None) -> None:
+    _check(lib().h3_patch_pack(C, T, H, W, _ptr(latent), _ptr(rows), _stream(stream)), "h3_patch_pack")
+
+
+def h3_patch_unpack(C: int, T: int, H: int, W: int, rows, latent, stream=None) -> None:
+    _check(lib().h3_patch_unpack(C, T, H, W, _ptr(rows), _ptr(latent), _stream(stream)), "h3_patch_unpack")
+
+
+def h3_input_projection(cfg, n: int, K: int, src, w, b, dst_rows, n_rows: int, x_out, stream=None) -> None:
+    _check(lib().h3_input_projection(ctypes.byref(cfg), n, K, _ptr(src), _ptr(w), _ptr(b), _ptr(dst_rows), n_rows,
+                                     _ptr(x_out), _stream(stream)), "h3_input_projection")
+
+
+def h3_packed_index_copy(cfg, n: int, src, dst_rows, n_rows: int, x_out, stream=None) -> None:
+    _check(lib().h3_packed_index_copy(ctypes.byref(cfg), n, _ptr(src), _ptr(dst_rows), n_rows, _ptr(x_out),
+                                      _stream(stream)), "h3_packed_index_copy")
+
+
+def h3_timestep_embedding(cfg, n_timesteps: int, t, w1, b1, w2, b2, scratch, t_cond, stream=None) -> None:
+    _check(lib().h3_timestep_embedding(ctypes.byref(cfg), n_timesteps, _ptr(t), _ptr(w1), _ptr(b1), _ptr(w2),
+                                       _ptr(b2), _ptr(scratch), _ptr(t_cond), _stream(stream)),
+           "h3_timestep_embedding")
 
 
 def h3_refiner_workspace_bytes(cfg: BlockConfig, n_rows: int) -> int:

@@ -806,6 +806,84 @@ h3_status h3_linear(int32_t M, int32_t N, int32_t K, const void* x, const void* 
 }
 
 // ===========================================================================
+// input side
+// ===========================================================================
+namespace {
+h3_status patch_common(int32_t C, int32_t T, int32_t H, int32_t W, const float* a, const float* b) {
+  if (C < 1 || T < 1 || H < 2 || W < 2 || (H & 1) || (W & 1)) return H3_ERR_SHAPE;
+  if ((long long)C * T * H * W > (1LL << 40)) return H3_ERR_SHAPE;
+  if (!a || !b) return H3_ERR_NULL;
+  return H3_OK;
+}
+}  // namespace
+
+h3_status h3_patch_pack(int32_t C, int32_t T, int32_t H, int32_t W, const float* latent, float* rows,
+                        cudaStream_t stream) {
+  h3_status s = patch_common(C, T, H, W, latent, rows);
+  if (s != H3_OK) return s;
+  return cuda_st(launch_patch_pack(C, T, H, W, latent, rows, false, stream));
+}
+
+h3_status h3_patch_unpack(int32_t C, int32_t T, int32_t H, int32_t W, const float* rows, float* latent,
+                          cudaStream_t stream) {
+  h3_status s = patch_common(C, T, H, W, rows, latent);
+  if (s != H3_OK) return s;
+  return cuda_st(launch_patch_pack(C, T, H, W, rows, latent, true, stream));
+}
+
+h3_status h3_input_projection(const h3_block_config* cfg, int32_t n, int32_t K, const float* src, const float* w,
+                              const float* b, const int32_t* dst_rows, int32_t n_rows, void* x_out,
+                              cudaStream_t stream) {
+  h3_status s = check_cfg(cfg);
+  if (s != H3_OK) return s;
+  if (n < 0 || n_rows < 1) return H3_ERR_SHAPE;
+  if (K < 4 || K > kInputProjMaxK || (K & 3)) return H3_ERR_UNSUPPORTED;
+  if (n == 0) return H3_OK;
+  if (!src || !w || !dst_rows || !x_out) return H3_ERR_NULL;
+  if (!al16(src) || !al16(w) || !al16(x_out)) return H3_ERR_ALIGN;
+  InputProjArgs a{};
+  a.n = n;
+  a.K = K;
+  a.D = cfg->dim;
+  a.n_dst = n_rows;
+  a.src = src;
+  a.w = w;
+  a.b = b;
+  a.dst = dst_rows;
+  a.out = static_cast<__nv_bfloat16*>(x_out);
+  a.err = device_error_word();
+  return cuda_st(launch_input_proj(a, stream));
+}
+
+h3_status h3_packed_index_copy(const h3_block_config* cfg, int32_t n, const void* src, const int32_t* dst_rows,
+                               int32_t n_rows, void* x_out, cudaStream_t stream) {
+  h3_status s = check_cfg(cfg);
+  if (s != H3_OK) return s;
+  if (n < 0 || n_rows < 1) return H3_ERR_SHAPE;
+  if (n == 0) return H3_OK;
+  if (!src || !dst_rows || !x_out) return H3_ERR_NULL;
+  if (!al16(src) || !al16(x_out)) return H3_ERR_ALIGN;
+  return cuda_st(launch_index_copy(n, cfg->dim, static_cast<const __nv_bfloat16*>(src), dst_rows, n_rows,
+                                   static_cast<__nv_bfloat16*>(x_out), device_error_word(), stream));
+}
+
+h3_status h3_timestep_embedding(const h3_block_config* cfg, int32_t n_timesteps, const float* t, const float* w1,
+                                const float* b1, const float* w2, const float* b2, float* scratch, float* t_cond,
+                                cudaStream_t stream) {
+  h3_status s = check_cfg(cfg);
+  if (s != H3_OK) return s;
+  if (n_timesteps < 1 || n_timesteps > 16) return H3_ERR_UNSUPPORTED;
+  if (!t || !w1 || !w2 || !scratch || !t_cond) return H3_ERR_NULL;
+  if (!al16(w1) || !al16(w2) || !al16(scratch) || !al16(t_cond) || !al16n(b1) || !al16n(b2)) return H3_ERR_ALIGN;
+  const int T = n_timesteps, D = cfg->dim, C = cfg->cond_dim;
+  float* e = scratch;                 // [T][256]
+  float* h = scratch + (size_t)T * 256;   // [T][D]
+  if ((s = cuda_st(launch_sinusoid(T, t, e, stream))) != H3_OK) return s;
+  if ((s = cuda_st(launch_rows_linear(T, 256, D, e, w1, b1, 1, h, stream))) != H3_OK) return s;
+  return cuda_st(launch_rows_linear(T, D, C, h, w2, b2, 0, t_cond, stream));
+}
+
+// ===========================================================================
 // output side and sampler
 // ===========================================================================
 h3_status h3_sigma_schedule(int32_t n_points, float shift, float* sigmas, int32_t* n_sigmas, cudaStream_t stream) {

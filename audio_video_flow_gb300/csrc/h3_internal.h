@@ -199,6 +199,28 @@ cudaError_t launch_refiner_setup(int S, int D, __nv_bfloat16* table, int32_t* ta
                                  cudaStream_t st);
 
 // ---------------------------------------------------------------------------
+// input side (k_input.cu)
+// ---------------------------------------------------------------------------
+struct InputProjArgs {
+  int n, K, D, n_dst;
+  const float* src;        // [n][K]
+  const float* w;          // [D][K]
+  const float* b;          // [D] or null
+  const int32_t* dst;      // [n] destination rows
+  __nv_bfloat16* out;      // [n_dst][D]
+  uint32_t* err;
+};
+constexpr int kInputProjMaxK = 128;
+cudaError_t launch_patch_pack(int C, int T, int H, int W, const float* src, float* dst, bool unpack,
+                              cudaStream_t st);
+cudaError_t launch_input_proj(const InputProjArgs& a, cudaStream_t st);
+cudaError_t launch_index_copy(int n, int D, const __nv_bfloat16* src, const int32_t* dst, int n_dst,
+                              __nv_bfloat16* out, uint32_t* err, cudaStream_t st);
+cudaError_t launch_sinusoid(int T, const float* t, float* e_out, cudaStream_t st);
+cudaError_t launch_rows_linear(int T, int K, int N, const float* in, const float* w, const float* b, int act,
+                               float* out, cudaStream_t st);
+
+// ---------------------------------------------------------------------------
 // output side and sampler (k_output.cu)
 // ---------------------------------------------------------------------------
 struct OutputHeadArgs {

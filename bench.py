@@ -396,6 +396,111 @@ def run_output_side(args, ws_n: int, rank: int, local: int):
     }
 
 
+def run_input_side(args, ws_n: int, rank: int, local: int):
+    """One evaluation's input side at the 15,860-row shape: the video patch
+    permutation, the FP32 video and audio input projections scattered into
+    the packed stream, the BF16 text projection of the text rows and its
+    scatter, and the timestep conditioning row."""
+    import torch
+    import audio_video_flow_gb300 as h3
+    import h3_inputs as hi
+
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    wl = hi.WORKLOADS[args.workload]
+    shape, S, T = wl.shape, wl.layout.n_rows, wl.n_timesteps
+    D, C = shape.dim, shape.cond_dim
+    cfg = h3.make_config(D, shape.n_heads, shape.ffn_dim, C)
+    lay = wl.layout
+    gt, gh, gw = lay.video_grid
+    lat = hi.normal((24, gt, 2 * gh, 2 * gw), 1.0, 0.0, args.seed, 95, device=dev, dtype=torch.float32)
+    vrows = torch.empty(lay.n_video, 96, dtype=torch.float32, device=dev)
+    arows = hi.latents(lay.n_audio, 32, args.seed, 97, device=dev)
+    text = hi.normal((lay.n_text, 5120), 1.0, 0.0, args.seed, 99, device=dev)
+    w_text = hi.normal((D, 5120), 0.02, 0.0, args.seed, 100, device=dev)
+    iw = hi.input_weights(shape, args.seed, device=dev)
+    idx = torch.arange(S, dtype=torch.int32, device=dev)
+    i_text, i_vid, i_aud = idx[:lay.n_text], idx[lay.n_text:lay.n_text + lay.n_video], idx[lay.n_text + lay.n_video:]
+    t = torch.full((T,), 0.5, dtype=torch.float32, device=dev)
+    x = torch.zeros(S, D, dtype=torch.bfloat16, device=dev)
+    tproj = torch.empty(lay.n_text, D, dtype=torch.bfloat16, device=dev)
+    scratch = torch.empty(T * (256 + D), dtype=torch.float32, device=dev)
+    tc = torch.empty(T, C, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    names = ["patch_pack", "input_projection", "text_projection", "timestep_embedding"]
+    n = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(n)]
+
+    def step(i=None):
+        rec = (lambda k: ev[i][k].record(stream)) if i is not None else (lambda k: None)
+        rec(0)
+        h3.h3_patch_pack(24, gt, 2 * gh, 2 * gw, lat, vrows)
+        rec(1)
+        h3.h3_input_projection(cfg, lay.n_video, 96, vrows, iw["w_in_video"], iw["b_in_video"], i_vid, S, x)
+        h3.h3_input_projection(cfg, lay.n_audio, 32, arows, iw["w_in_audio"], iw["b_in_audio"], i_aud, S, x)
+        rec(2)
+        h3.h3_linear(lay.n_text, D, 5120, text, w_text, None, tproj)
+        h3.h3_packed_index_copy(cfg, lay.n_text, tproj, i_text, S, x)
+        rec(3)
+        h3.h3_timestep_embedding(cfg, T, t, iw["w_t1"], iw["b_t1"], iw["w_t2"], iw["b_t2"], scratch, tc)
+        rec(4)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    for e3 in ev:
+        for e in e3:
+            e.record(stream)
+    proj_flops = 2.0 * D * (lay.n_video * 96 + lay.n_audio * 32)
+    text_flops = 2.0 * lay.n_text * 5120 * D
+    mlp_bytes = 4 * (D * 256 + C * D)
+    with ClockSampler(local) as clk:
+        barrier(ws_n)
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for i in range(n):
+            step(i)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        barrier(ws_n)
+    status = h3.h3_sync_check(timeout_ms=60000)
+    if status != 0:
+        raise RuntimeError(f"device error: {h3.status_string(status)}")
+    elapsed_ms, units = aggregate(t0.elapsed_time(t1), n * (proj_flops + text_flops), ws_n)
+    st = {nm: statistics.mean(e[k].elapsed_time(e[k + 1]) for e in ev) for k, nm in enumerate(names)}
+    clocks = clk.summary()
+    peak = alu_fp32_peak_tflops(clocks.get("sm_max_mhz") or 2070.0,
+                                torch.cuda.get_device_properties(dev).multi_processor_count)
+    proj_tf = proj_flops / (st["input_projection"] * 1e-3) / 1e12
+    peaks = load_peaks()
+    return {
+        "metric": METRIC, "value": round(units / (elapsed_ms * 1e-3) / 1e12, 4), "unit": "TFLOP/s",
+        "n_gpus": ws_n, "steps": n, "warmup": args.warmup, "ms_per_step": round(elapsed_ms / n, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "tokens_per_s": round(ws_n * S * n / (elapsed_ms * 1e-3), 1),
+        "config": {"workload": wl.name, "description": wl.description, "rows": S, "dim": D,
+                   "flop_per_step": proj_flops + text_flops, "l2": "video latent and projections written "
+                   "every step (157 MB of bf16 rows)", "parallelism": f"replicas x{ws_n}"},
+        "e2e": None, "gpu_launches": 7 * n,
+        "roofline": {"kernel": "input_projection", "bound": "alu", "achieved": round(proj_tf, 2),
+                     "peak": round(peak, 1), "unit": "TFLOP/s", "frac": round(proj_tf / peak, 4),
+                     "peak_source": "fp32 FMA lanes x 2 x max SM clock", "traffic": None},
+        "stages": {
+            "patch_pack": {"us": round(st["patch_pack"] * 1e3, 2),
+                           "gbs": round(2 * 4 * lat.numel() / (st["patch_pack"] * 1e-3) / 1e9, 1)},
+            "input_projection": {"us": round(st["input_projection"] * 1e3, 2), "tflops": round(proj_tf, 2)},
+            "text_projection": {"us": round(st["text_projection"] * 1e3, 2),
+                                "tflops": round(text_flops / (st["text_projection"] * 1e-3) / 1e12, 1)},
+            "timestep_embedding": {"us": round(st["timestep_embedding"] * 1e3, 2),
+                                   "gbs": round(mlp_bytes / (st["timestep_embedding"] * 1e-3) / 1e9, 1),
+                                   "hbm_frac": round(mlp_bytes / (st["timestep_embedding"] * 1e-3) / 1e9
+                                                     / peaks["hbm_gbs"], 4)},
+        },
+        "clocks": clocks,
+    }
+
+
 def run_refiner(args, ws_n: int, rank: int, local: int):
     """The 2-layer token refiner and its final RMSNorm over the text rows."""
     import torch
@@ -470,6 +575,8 @@ def run_ours(args, ws_n: int, rank: int, local: int):
         return run_output_side(args, ws_n, rank, local)
     if wl.name.startswith("refiner"):
         return run_refiner(args, ws_n, rank, local)
+    if wl.name.startswith("input"):
+        return run_input_side(args, ws_n, rank, local)
     shape, S, T, NB = wl.shape, wl.layout.n_rows, wl.n_timesteps, wl.n_blocks
     cfg = h3.make_config(shape.dim, shape.n_heads, shape.ffn_dim, shape.cond_dim)
     meta_c, acts_c, _ = hi.workload_inputs(wl, seed=args.seed, device="cpu", block=0) if NB == 1 else \

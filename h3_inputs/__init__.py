@@ -90,6 +90,11 @@ WORKLOADS: Dict[str, Workload] = {
         "denoiser15860", H3_SHAPE, PackedLayout(256, (36, 15, 27), 1024), n_timesteps=1,
         n_blocks=50,
         description="50-block denoiser forward at the 864x480 141-frame shape, 15860 rows"),
+    "input15860": Workload(
+        "input15860", H3_SHAPE, PackedLayout(256, (36, 15, 27), 1024), n_timesteps=1, n_blocks=0,
+        description="input side of one evaluation at the 15860-row shape: video patch packing "
+                    "(24 x 36 x 30 x 54 latent), FP32 video/audio input projections into the packed "
+                    "stream, BF16 text projection 5120 -> 5376, timestep sinusoid and FP32 MLP"),
     "refiner256": Workload(
         "refiner256", H3_SHAPE, PackedLayout(256, (0, 0, 0), 0), n_timesteps=1, n_blocks=2,
         description="2-layer token refiner plus final RMSNorm over 256 projected text rows"),
@@ -229,6 +234,21 @@ def output_weights(shape: BlockShape, seed: int = 0, device: str = "cpu") -> Dic
         "w_fin_audio": n((2 * D, C), 2), "b_fin_audio": n((2 * D,), 3),
         "w_head_video": n((VIDEO_PATCH, D), 4), "b_head_video": n((VIDEO_PATCH,), 5),
         "w_head_audio": n((AUDIO_PATCH, D), 6), "b_head_audio": n((AUDIO_PATCH,), 7),
+    }
+
+
+def input_weights(shape: BlockShape, seed: int = 0, device: str = "cpu") -> Dict[str, torch.Tensor]:
+    """Random-init FP32 weights of the input side, all ~N(0, 0.02): the video
+    and audio input projections w_in_video [D][96], w_in_audio [D][32] with
+    biases [D], and the timestep MLP w_t1 [D][256], b_t1 [D], w_t2 [C][D],
+    b_t2 [C]."""
+    D, C = shape.dim, shape.cond_dim
+    n = lambda shp, k: normal(shp, 0.02, 0.0, seed, 80 + k, device, dtype=torch.float32)
+    return {
+        "w_in_video": n((D, VIDEO_PATCH), 0), "b_in_video": n((D,), 1),
+        "w_in_audio": n((D, AUDIO_PATCH), 2), "b_in_audio": n((D,), 3),
+        "w_t1": n((D, 256), 4), "b_t1": n((D,), 5),
+        "w_t2": n((C, D), 6), "b_t2": n((C,), 7),
     }
 
 

@@ -282,6 +282,52 @@ h3_status h3_linear(int32_t M, int32_t N, int32_t K, const void *x, const void *
                     const void *b, void *y, cudaStream_t stream);
 
 /* ----------------------------------------------------------------------- */
+/* Input side of one denoiser evaluation                                   */
+/* ----------------------------------------------------------------------- */
+
+/* Video latent to patch rows (RFC s2: visual VAE latent of C = 24 channels,
+ * transformer video patch (1, 2, 2), flattened width 96; s5
+ * video_patch_pack_unpack).  latent fp32 [C][T][H][W] (one batch row), rows
+ * fp32 [T*(H/2)*(W/2)][4C]: row (t, h/2, w/2) with t slowest (the order of the
+ * video positions), feature (c, dh, dw) with c slowest.  H and W even; both
+ * device pointers.  h3_patch_unpack is the exact inverse. */
+h3_status h3_patch_pack(int32_t C, int32_t T, int32_t H, int32_t W, const float *latent, float *rows,
+                        cudaStream_t stream);
+h3_status h3_patch_unpack(int32_t C, int32_t T, int32_t H, int32_t W, const float *rows, float *latent,
+                          cudaStream_t stream);
+
+/* FP32 input projection of one modality (RFC s5
+ * video_input_projection_fp32 96 -> 5376, audio_input_projection_fp32
+ * 32 -> 5376): x_out[dst_rows[i]] = bf16(src[i] W^T + b), fp32 inputs,
+ * weights and accumulation, one rounding to bf16 (the h3-metal README's patch
+ * projection), written straight into the packed residual stream.  src fp32
+ * [n][K], w fp32 [D][K], b fp32 [D] or NULL, dst_rows int32 [n] (device),
+ * x_out bf16 [n_rows][D]; K a multiple of 4, 4 <= K <= 128; D = cfg->dim.  A
+ * destination outside [0, n_rows) is reported (H3_ERR_INDEX) and skipped. */
+h3_status h3_input_projection(const h3_block_config *cfg, int32_t n, int32_t K, const float *src,
+                              const float *w, const float *b, const int32_t *dst_rows, int32_t n_rows,
+                              void *x_out, cudaStream_t stream);
+
+/* Row scatter into the packed stream (RFC s5 packed_index_copy):
+ * x_out[dst_rows[i]] = src[i] for bf16 rows of D = cfg->dim (e.g. the refined
+ * text rows).  Zero-initialising the stream first is the caller's memset;
+ * rows no modality writes stay zero.  Bad destinations are reported and
+ * skipped. */
+h3_status h3_packed_index_copy(const h3_block_config *cfg, int32_t n, const void *src, const int32_t *dst_rows,
+                               int32_t n_rows, void *x_out, cudaStream_t stream);
+
+/* Timestep conditioning rows (RFC s2: sinusoid width 256, timestep MLP
+ * 256 -> 5376 -> 2688, FP32; s5 timestep_sinusoid_h3, timestep_mlp_fp32):
+ * e = [cos(t f_i) | sin(t f_i)], f_i = exp(-ln(10000) i / 128), i < 128, with
+ * t = 1 - sigma as given (no 0..1000 scaling); h = SiLU(e W1^T + b1);
+ * t_cond = h W2^T + b2.  t fp32 [T]; w1 fp32 [D][256]; w2 fp32 [C][D]; b1, b2
+ * or NULL; scratch fp32 [T][256 + D]; t_cond fp32 [T][C]; 1 <= T <= 16,
+ * D = cfg->dim, C = cfg->cond_dim.  All device pointers. */
+h3_status h3_timestep_embedding(const h3_block_config *cfg, int32_t n_timesteps, const float *t,
+                                const float *w1, const float *b1, const float *w2, const float *b2,
+                                float *scratch, float *t_cond, cudaStream_t stream);
+
+/* ----------------------------------------------------------------------- */
 /* Token refiner                                                            */
 /* ----------------------------------------------------------------------- */
 
