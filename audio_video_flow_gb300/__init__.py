@@ -80,6 +80,9 @@ def lib() -> ctypes.CDLL:
             "h3_ffn_up_swiglu": (i32, [cfgp, i32, vp, vp, vp, vp, vp]),
             "h3_ffn_down_residual": (i32, [cfgp, mp, vp, vp, vp, vp, vp, vp, vp]),
             "h3_linear": (i32, [i32, i32, i32, vp, vp, vp, vp, vp]),
+            "h3_blocks_graph_create": (i32, [cfgp, i32, wp, mp, vp, vp, vp, sz, ctypes.POINTER(vp)]),
+            "h3_graph_launch": (i32, [vp, vp]),
+            "h3_graph_destroy": (i32, [vp]),
             "h3_patch_pack": (i32, [i32, i32, i32, i32, vp, vp, vp]),
             "h3_patch_unpack": (i32, [i32, i32, i32, i32, vp, vp, vp]),
             "h3_input_projection": (i32, [cfgp, i32, i32, vp, vp, vp, vp, i32, vp, vp]),
@@ -197,6 +200,36 @@ def h3_blocks_forward(cfg, weights_list: Sequence[BlockWeights], meta, x_in, x_o
     _check(lib().h3_blocks_forward(ctypes.byref(cfg), len(weights_list), arr, ctypes.byref(meta), _ptr(x_in),
                                    _ptr(x_out), _ptr(workspace), workspace.numel() * workspace.element_size(),
                                    _stream(stream)), "h3_blocks_forward")
+
+
+class BlocksGraph:
+    """A captured chain of blocks (h3_blocks_graph_create); launch() replays it.
+    Keeps the weight structs and tensors it was captured with alive."""
+
+    def __init__(self, cfg, weights_list: Sequence[BlockWeights], meta, x_in, x_out, workspace):
+        self._keep = (cfg, list(weights_list), meta, x_in, x_out, workspace)
+        arr = (BlockWeights * len(weights_list))(*weights_list)
+        self._arr = arr
+        h = c_void_p()
+        _check(lib().h3_blocks_graph_create(ctypes.byref(cfg), len(weights_list), arr, ctypes.byref(meta),
+                                            _ptr(x_in), _ptr(x_out), _ptr(workspace),
+                                            workspace.numel() * workspace.element_size(), ctypes.byref(h)),
+               "h3_blocks_graph_create")
+        self._h = h
+
+    def launch(self, stream=None) -> None:
+        _check(lib().h3_graph_launch(self._h, _stream(stream)), "h3_graph_launch")
+
+    def close(self) -> None:
+        if self._h is not None and self._h.value:
+            lib().h3_graph_destroy(self._h)
+        self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def h3_adaln_table_workspace_bytes(cfg: BlockConfig) -> int:

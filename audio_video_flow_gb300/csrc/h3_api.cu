@@ -6,6 +6,7 @@
 
 #include <chrono>
 #include <cmath>
+#include <new>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -564,6 +565,75 @@ h3_status h3_blocks_forward(const h3_block_config* cfg, int32_t n_blocks, const 
                              nullptr, 0);
     if (s != H3_OK) return s;
   }
+  return H3_OK;
+}
+
+// ===========================================================================
+// the chain as one CUDA graph
+// ===========================================================================
+struct h3_graph {
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+};
+
+h3_status h3_blocks_graph_create(const h3_block_config* cfg, int32_t n_blocks, const h3_block_weights* w,
+                                 const h3_packed_meta* meta, const void* x_in, void* x_out, void* workspace,
+                                 size_t ws_bytes, h3_graph** out) {
+  if (!out) return H3_ERR_NULL;
+  *out = nullptr;
+  if (!w) return H3_ERR_NULL;
+  if (n_blocks < 1) return H3_ERR_SHAPE;
+  for (int b = 0; b < n_blocks; ++b) {
+    h3_status s = check_block_args(cfg, &w[b], meta, x_in, x_out, workspace, ws_bytes);
+    if (s != H3_OK) return s;
+  }
+  cudaStream_t cap = nullptr;
+  if (cudaStreamCreateWithFlags(&cap, cudaStreamNonBlocking) != cudaSuccess) return H3_ERR_CUDA;
+  h3_status s = H3_OK;
+  if (cudaStreamBeginCapture(cap, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+    cudaStreamDestroy(cap);
+    return H3_ERR_CUDA;
+  }
+  for (int b = 0; b < n_blocks && s == H3_OK; ++b)
+    s = block_impl(cfg, &w[b], meta, b == 0 ? x_in : x_out, x_out, workspace, ws_bytes, cap, nullptr, 0);
+  cudaGraph_t g = nullptr;
+  const cudaError_t e_end = cudaStreamEndCapture(cap, &g);
+  cudaStreamDestroy(cap);
+  if (s != H3_OK || e_end != cudaSuccess || !g) {
+    if (g) cudaGraphDestroy(g);
+    cudaGetLastError();
+    return s != H3_OK ? s : H3_ERR_CUDA;
+  }
+  cudaGraphExec_t ex = nullptr;
+  if (cudaGraphInstantiate(&ex, g, 0) != cudaSuccess) {
+    cudaGraphDestroy(g);
+    cudaGetLastError();
+    return H3_ERR_CUDA;
+  }
+  h3_graph* hg = new (std::nothrow) h3_graph;
+  if (!hg) {
+    cudaGraphExecDestroy(ex);
+    cudaGraphDestroy(g);
+    return H3_ERR_CUDA;
+  }
+  hg->graph = g;
+  hg->exec = ex;
+  *out = hg;
+  set_kernel_info("blocks graph: %d blocks captured (side-stream fork/join and programmatic launches as edges)",
+                  n_blocks);
+  return H3_OK;
+}
+
+h3_status h3_graph_launch(h3_graph* g, cudaStream_t stream) {
+  if (!g || !g->exec) return H3_ERR_NULL;
+  return cudaGraphLaunch(g->exec, stream) == cudaSuccess ? H3_OK : H3_ERR_CUDA;
+}
+
+h3_status h3_graph_destroy(h3_graph* g) {
+  if (!g) return H3_ERR_NULL;
+  if (g->exec) cudaGraphExecDestroy(g->exec);
+  if (g->graph) cudaGraphDestroy(g->graph);
+  delete g;
   return H3_OK;
 }
 

@@ -626,7 +626,11 @@ def run_ours(args, ws_n: int, rank: int, local: int):
     work = stage_work(shape, S, T, split)
     flops_step = NB * sum(f for f, _ in work.values())
 
-    # ---- timed region (device time on the launching stream)
+    # ---- timed region (device time on the launching stream).  The headline
+    # value comes from K plain steps: an event recorded between two launches
+    # would cut the programmatic overlap of consecutive kernels.  A second
+    # timed pass of K steps records an event after every launch and gives the
+    # per-kernel times (and the dominant kernel's roofline).
     with ClockSampler(local) as clk:
         barrier(ws_n)
         torch.cuda.synchronize()
@@ -634,13 +638,23 @@ def run_ours(args, ws_n: int, rank: int, local: int):
         t1 = torch.cuda.Event(enable_timing=True)
         t0.record(stream)
         host0 = time.perf_counter()
-        for i in range(args.steps):
-            step(i)
+        for _ in range(args.steps):
+            step()
         t1.record(stream)
         torch.cuda.synchronize()
         host1 = time.perf_counter()
         barrier(ws_n)
+        torch.cuda.synchronize()
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for i in range(args.steps):
+            step(i)
+        s1.record(stream)
+        torch.cuda.synchronize()
+        barrier(ws_n)
     elapsed_ms = t0.elapsed_time(t1)
+    instrumented_ms = s0.elapsed_time(s1)
     status = h3.h3_sync_check(timeout_ms=60000)
     if status != 0:
         raise RuntimeError(f"device error in the timed region: {h3.status_string(status)}")
@@ -726,7 +740,9 @@ def run_ours(args, ws_n: int, rank: int, local: int):
                    "cond": shape.cond_dim, "flop_per_step": flops_step,
                    "l2": "inputs larger than L2: %.2f GB of block weights re-read every step" %
                          (NB * weight_bytes(shape) / 1e9),
-                   "parallelism": f"replicas x{ws_n}"},
+                   "parallelism": f"replicas x{ws_n}",
+                   "timing": "value from K plain steps; stage times from K more steps with an event after "
+                             "every launch (those events cut the overlap of consecutive launches)"},
         "e2e": e2e,
         "gpu_launches": args.steps * NB * kernels_per_block(shape, S),
         "roofline": {"kernel": dom, "bound": BOUND[dom], "achieved": round(achieved, 1), "peak": peak,
@@ -734,9 +750,30 @@ def run_ours(args, ws_n: int, rank: int, local: int):
                      "peak_source": src,
                      "traffic": TRAFFIC.get(f"{dom}@{wl.name}")},
         "stages": stages_out,
+        "instrumented_ms_per_step": round(instrumented_ms / args.steps, 5),
         "clocks": clocks,
         "host_ms_per_step": round((host1 - host0) * 1e3 / args.steps, 4),
     }
+    if args.graph:
+        # the same steps replayed from one captured CUDA graph (no stage events)
+        g = h3.BlocksGraph(cfg, cw, meta, x, y, wsp)
+        for _ in range(args.warmup):
+            g.launch()
+        torch.cuda.synchronize()
+        barrier(ws_n)
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for _ in range(args.steps):
+            g.launch()
+        g1.record(stream)
+        torch.cuda.synchronize()
+        barrier(ws_n)
+        if h3.h3_sync_check(timeout_ms=60000) != 0:
+            raise RuntimeError("device error in the graph replays")
+        g_ms, g_units = aggregate(g0.elapsed_time(g1), float(args.steps) * flops_step, ws_n)
+        line["graph"] = {"ms_per_step": round(g_ms / args.steps, 5),
+                         "value": round(g_units / (g_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s"}
+        g.close()
     if rank == 0 and not args.no_cpu_baseline and ws_n == 1:
         line["cpu_baseline"] = cpu_baseline(wl, args.seed, args.cpu_seconds)
     return line
@@ -859,6 +896,7 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--graph", action="store_true", help="also time the block chain replayed from one CUDA graph")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -168,6 +168,23 @@ h3_status h3_blocks_forward(const h3_block_config *cfg, int32_t n_blocks,
                             const void *x_in, void *x_out, void *workspace, size_t ws_bytes,
                             cudaStream_t stream);
 
+/* The same chain captured once into a CUDA graph and replayed with one launch
+ * (SURVEY "next" item 1: one graph per evaluation).  h3_blocks_graph_create
+ * records the launches h3_blocks_forward would make for these arguments
+ * (pointers and sizes are baked in; the buffers' contents are read at each
+ * replay) and instantiates the graph; h3_graph_launch replays it on a
+ * stream; h3_graph_destroy frees it.  The block's side-stream fork and join
+ * and the programmatic dependent launches become edges of the graph.
+ * Validation errors as for h3_blocks_forward; H3_ERR_CUDA if capture or
+ * instantiation fails.  *graph is NULL on error. */
+typedef struct h3_graph h3_graph;
+h3_status h3_blocks_graph_create(const h3_block_config *cfg, int32_t n_blocks,
+                                 const h3_block_weights *weights, const h3_packed_meta *meta,
+                                 const void *x_in, void *x_out, void *workspace,
+                                 size_t workspace_bytes, h3_graph **graph);
+h3_status h3_graph_launch(h3_graph *graph, cudaStream_t stream);
+h3_status h3_graph_destroy(h3_graph *graph);
+
 /* ----------------------------------------------------------------------- */
 /* Stages (each is one kernel launch)                                       */
 /* ----------------------------------------------------------------------- */

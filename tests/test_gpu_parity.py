@@ -318,6 +318,39 @@ def test_single_row_block(h3):
 
 
 # ---------------------------------------------------------------------------
+# the chain as one CUDA graph: replays equal direct calls bit for bit
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name,nb", [("tiny72", 3), ("block505", 2)])
+def test_blocks_graph_replay_matches_direct(h3, name, nb):
+    w = hi.WORKLOADS[name]
+    shape, S, T = w.shape, w.layout.n_rows, w.n_timesteps
+    meta = {k: v.cuda() for k, v in hi.packed_metadata(w.layout, T, 0).items()}
+    acts = hi.activations(shape, S, T, 0, device="cuda")
+    wts = [{k: (v.cuda() if v is not None else None) for k, v in hi.block_weights(shape, 0, b).items()}
+           for b in range(nb)]
+    cfg = h3.make_config(shape.dim, shape.n_heads, shape.ffn_dim, shape.cond_dim)
+    cw = [h3.make_weights(x) for x in wts]
+    m = h3.make_meta(meta["token_tag"], meta["timestep_index"], meta["pos_thw"], acts["t_cond"], T)
+    ws = torch.empty(h3.h3_block_workspace_bytes(cfg, S, T), dtype=torch.uint8, device="cuda")
+    x = acts["x"].clone()
+    y_direct = torch.empty_like(x)
+    h3.h3_blocks_forward(cfg, cw, m, x, y_direct, ws)
+    y_graph = torch.zeros_like(x)
+    g = h3.BlocksGraph(cfg, cw, m, x, y_graph, ws)
+    g.launch()
+    assert h3.h3_sync_check() == 0
+    assert torch.equal(y_graph, y_direct)
+    # a replay reads the buffers' current contents
+    x.copy_(hi.normal((S, shape.dim), 1.0, 0.0, 5, 1, device="cuda"))
+    h3.h3_blocks_forward(cfg, cw, m, x, y_direct, ws)
+    g.launch()
+    assert h3.h3_sync_check() == 0
+    assert torch.equal(y_graph, y_direct)
+    g.close()
+
+
+# ---------------------------------------------------------------------------
 # token refiner: two pre-norm blocks without AdaLN or RoPE, then a final norm
 # ---------------------------------------------------------------------------
 
