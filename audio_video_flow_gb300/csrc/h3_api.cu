@@ -269,14 +269,14 @@ h3_status run_qkv(const h3_block_config& c, const h3_packed_meta& m, const void*
                   const void* b_qkv, const void* qg, const void* kg, void* out, cudaStream_t st,
                   int max_ctas = 0) {
   const int S = m.n_rows, D = c.dim, H = c.n_heads;
-  const int bn = gemm_choose_bn(EPI_QKV, S, 3 * H * 128, H, 0);
+  const GemmPlan pl = gemm_plan(EPI_QKV, S, 3 * H * 128, H, 0);
   CUtensorMap tA, tB;
-  if (!make_tmap_2d(&tA, h, S, D, D, 128) ||
-      !make_tmap_2d(&tB, w_qkv, (uint64_t)3 * H * 128, D, D, (uint32_t)gemm_b_box_rows(EPI_QKV, bn)))
+  if (!make_tmap_2d(&tA, h, S, D, D, (uint32_t)pl.a_box) ||
+      !make_tmap_2d(&tB, w_qkv, (uint64_t)3 * H * 128, D, D, (uint32_t)pl.b_box))
     return H3_ERR_CUDA;
   GemmArgs a{};
-  gemm_common(a, S, D, gemm_num_n(EPI_QKV, bn, 3 * H * 128, H, 0));
-  a.b_rows = gemm_b_box_rows(EPI_QKV, bn);
+  gemm_common(a, S, D, pl.num_n);
+  gemm_set_plan(a, pl);
   a.out = static_cast<__nv_bfloat16*>(out);
   a.ldo = 3 * H * 128;
   a.bias = static_cast<const __nv_bfloat16*>(b_qkv);
@@ -287,7 +287,7 @@ h3_status run_qkv(const h3_block_config& c, const h3_packed_meta& m, const void*
   a.eps = c.eps;
   a.max_ctas = max_ctas;
   fill_omega(a.omega, c.rope_theta);
-  return cuda_st(launch_gemm(EPI_QKV, bn, tA, tB, a, st));
+  return cuda_st(launch_gemm(EPI_QKV, pl.bn, pl.mc, tA, tB, a, st));
 }
 
 h3_status run_attention(int S, int H, const void* q, const void* k, const void* v, int64_t rs, int64_t hs,
@@ -312,7 +312,7 @@ h3_status run_resid_gemm(const h3_block_config& c, const h3_packed_meta& m, cons
   const int S = m.n_rows, D = c.dim;
   const GemmPlan pl = gemm_plan(EPI_RESID, S, D, 0, 0);
   CUtensorMap tA, tB;
-  if (!make_tmap_2d(&tA, act, S, K, K, 128) || !make_tmap_2d(&tB, w, D, K, K, (uint32_t)pl.b_rows))
+  if (!make_tmap_2d(&tA, act, S, K, K, (uint32_t)pl.a_box) || !make_tmap_2d(&tB, w, D, K, K, (uint32_t)pl.b_box))
     return H3_ERR_CUDA;
   GemmArgs a{};
   gemm_common(a, S, K, pl.num_n);
@@ -329,23 +329,24 @@ h3_status run_resid_gemm(const h3_block_config& c, const h3_packed_meta& m, cons
   a.T = m.n_timesteps;
   a.tag = m.token_tag;
   a.tidx = m.timestep_index;
-  return cuda_st(launch_gemm(EPI_RESID, pl.bn, tA, tB, a, st));
+  return cuda_st(launch_gemm(EPI_RESID, pl.bn, pl.mc, tA, tB, a, st));
 }
 
 h3_status run_ffn_up(const h3_block_config& c, int S, const void* h, const void* w1, const void* b1, void* out,
                      cudaStream_t st) {
   const int D = c.dim, F = c.ffn_dim;
+  const GemmPlan pl = gemm_plan(EPI_SWIGLU, S, 2 * F, 0, F);
   CUtensorMap tA, tB;
-  if (!make_tmap_2d(&tA, h, S, D, D, 128) || !make_tmap_2d(&tB, w1, (uint64_t)2 * F, D, D, 128))
+  if (!make_tmap_2d(&tA, h, S, D, D, (uint32_t)pl.a_box) || !make_tmap_2d(&tB, w1, (uint64_t)2 * F, D, D, (uint32_t)pl.b_box))
     return H3_ERR_CUDA;
   GemmArgs a{};
-  gemm_common(a, S, D, gemm_num_n(EPI_SWIGLU, 256, 0, 0, F));
-  a.b_rows = gemm_b_box_rows(EPI_SWIGLU, 256);
+  gemm_common(a, S, D, pl.num_n);
+  gemm_set_plan(a, pl);
   a.out = static_cast<__nv_bfloat16*>(out);
   a.ldo = F;
   a.bias = static_cast<const __nv_bfloat16*>(b1);
   a.F = F;
-  return cuda_st(launch_gemm(EPI_SWIGLU, 256, tA, tB, a, st));
+  return cuda_st(launch_gemm(EPI_SWIGLU, pl.bn, pl.mc, tA, tB, a, st));
 }
 
 h3_status check_block_weights(const h3_block_weights* w) {
@@ -370,11 +371,14 @@ h3_status check_block_weights(const h3_block_weights* w) {
 int adaln_side_ctas(const h3_block_config& c, int S) {
   if (c.dim % 128) return 0;
   const int sms = num_sms(), H = c.n_heads, I = H * 128;
-  const int slots = gemm_pair_slots();
-  const int bn = gemm_choose_bn(EPI_QKV, S, 3 * I, H, 0);
-  const long long tiles = (long long)gemm_m_tiles(S) * gemm_num_n(EPI_QKV, bn, 3 * I, H, 0);
-  const long long waves = (tiles + slots - 1) / slots;
-  const int need = 2 * (int)((tiles + waves - 1) / waves);   // fewest CTAs (pairs x 2) with the same wave count
+  const GemmPlan pl = gemm_plan(EPI_QKV, S, 3 * I, H, 0);
+  const int cl = pl.mc ? 4 : 2;
+  const int slots = pl.mc ? gemm_quad_slots() : gemm_pair_slots();
+  const long long units = pl.mc == 1 ? (long long)(gemm_m_tiles(S) / 2) * pl.num_n
+                        : pl.mc == 2 ? (long long)gemm_m_tiles(S) * (pl.num_n / 2)
+                                     : (long long)gemm_m_tiles(S) * pl.num_n;
+  const long long waves = (units + slots - 1) / slots;
+  const int need = cl * (int)((units + waves - 1) / waves);   // fewest CTAs (clusters x size) with the same wave count
   return sms - need >= 8 ? sms - need : 0;
 }
 
@@ -863,7 +867,7 @@ h3_status h3_linear(int32_t M, int32_t N, int32_t K, const void* x, const void* 
   if (!al16(x) || !al16(w) || !al16n(b) || !al16(y)) return H3_ERR_ALIGN;
   const GemmPlan pl = gemm_plan(EPI_PLAIN, M, N, 0, 0);
   CUtensorMap tA, tB;
-  if (!make_tmap_2d(&tA, x, M, K, K, 128) || !make_tmap_2d(&tB, w, N, K, K, (uint32_t)pl.b_rows))
+  if (!make_tmap_2d(&tA, x, M, K, K, (uint32_t)pl.a_box) || !make_tmap_2d(&tB, w, N, K, K, (uint32_t)pl.b_box))
     return H3_ERR_CUDA;
   GemmArgs a{};
   gemm_common(a, M, K, pl.num_n);
@@ -872,7 +876,7 @@ h3_status h3_linear(int32_t M, int32_t N, int32_t K, const void* x, const void* 
   a.ldo = N;
   a.bias = static_cast<const __nv_bfloat16*>(b);
   a.n_valid = N;
-  return cuda_st(launch_gemm(EPI_PLAIN, pl.bn, tA, tB, a, stream));
+  return cuda_st(launch_gemm(EPI_PLAIN, pl.bn, pl.mc, tA, tB, a, stream));
 }
 
 // ===========================================================================

@@ -35,6 +35,8 @@
 // silu_rows_kernel and TMA-loaded into shared memory by every CTA, is the
 // resident N = 16 operand.  The kernel is bound by the weight stream from HBM.
 #include "h3_device.cuh"
+
+#include <string>
 #include "h3_internal.h"
 
 #include <cstdio>
@@ -479,7 +481,16 @@ __device__ __forceinline__ void run_epilogue(const GemmArgs& a, uint32_t tacc, i
 
 }  // namespace
 
-template <int EPI, int BN>
+// MC = 1: clusters of four CTAs, two pairs on the two 256-row halves (m =
+// 2 mp, 2 mp + 1) of one column tile.  Each CTA loads one half of its weight
+// rows and multicasts it to the CTA with the same rank in the other pair, so
+// each SM fetches 16 KB of activations and BN/4 rows of weights per k-block.
+// A ring stage of a CTA is then written by both pairs: its release needs the
+// MMA commits of both pairs (empty barriers count 2, commits go to all four
+// CTAs).  Everything else (full barriers, accumulators, epilogue) stays per
+// pair.  Both pairs walk the same tiles and k-blocks, so their rings advance
+// together.
+template <int EPI, int BN, int MC>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     gemm_bf16_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const GemmArgs args) {
@@ -500,14 +511,33 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 
   griddep_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_ctarank();
+  const uint32_t crank = cluster_ctarank();
+  const uint32_t rank = crank & 1u;                 // rank inside the CTA pair
+  const uint32_t pic = MC ? (crank >> 1) : 0u;      // pair inside the cluster
+  const uint32_t lead = crank & ~1u;                // cluster rank of this pair's even CTA
   const bool leader = rank == 0;
-  const int pair = (int)(blockIdx.x >> 1), num_pairs = (int)(gridDim.x >> 1);
-  const int num_tiles = args.num_m * args.num_n;
+  constexpr int CL = MC ? 4 : 2;
+  const int unit = (int)(blockIdx.x / CL), num_units = (int)(gridDim.x / CL);
+  // MC == 1: the cluster's two pairs take m-tiles 2u, 2u+1 of one column tile
+  // and share its weight tile; MC == 2: they take column tiles 2v, 2v+1 of one
+  // m-tile and share its activation tile.  Each pair loads half of the shared
+  // tile and multicasts it to the same rank of the other pair.
+  const int num_mu = MC == 1 ? (args.num_m + 1) / 2 : args.num_m;
+  const int num_nu = MC == 2 ? (args.num_n + 1) / 2 : args.num_n;
+  const int num_tiles = num_mu * num_nu;
+  const uint16_t all_mask = MC ? 0xF : 0x3;
+  const uint16_t pair_mask = (uint16_t)(0x3u << lead);
+  // tile `t` of this unit's walk -> (m_blk, n_blk) of this pair
+  auto my_tile = [&](int t, int& m_blk, int& n_blk) {
+    int mu, nu;
+    tile_coords(t, num_mu, num_nu, mu, nu);
+    m_blk = MC == 1 ? 2 * mu + (int)pic : mu;
+    n_blk = MC == 2 ? 2 * nu + (int)pic : nu;
+  };
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], MC ? 2 : 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&acc_full[i], 1);
@@ -522,10 +552,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     tma_prefetch_desc(&tmB);
     // weights are never written: pull this CTA's half of the first tile into
     // L2 while the previous kernel on the stream may still be running
-    if (pair < num_tiles) {
+    if (unit < num_tiles) {
       int m0, n0;
-      tile_coords(pair, args.num_m, args.num_n, m0, n0);
-      const int r0 = b_tile_row<EPI, BN>(args, n0, rank);
+      my_tile(unit, m0, n0);
+      const int r0 = b_tile_row<EPI, BN>(args, n0, rank) + (MC == 1 ? (int)pic * (args.b_rows / 2) : 0);
       for (int kb = 0; kb < C::STAGES + C::PREFETCH && kb < args.num_k; ++kb) tma_prefetch_l2(&tmB, kb * BK, r0);
     }
   }
@@ -545,19 +575,27 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       int last_phase[STAGES];
       for (int s = 0; s < STAGES; ++s) last_phase[s] = -1;
       bool ok = true;
-      const uint32_t full0 = mapa_shared(smem_u32(full), 0);   // the even CTA's full[0]
+      const uint32_t full0 = mapa_shared(smem_u32(full), lead);   // this pair's even CTA's full[0]
       const uint32_t stage_tx = 2u * (uint32_t)(A_STAGE_BYTES + args.b_rows * BK * 2);   // both CTAs' boxes
-      for (int tile = pair; tile < num_tiles && ok; tile += num_pairs) {
+      const uint16_t mc_mask = (uint16_t)((1u << rank) | (1u << (rank + 2)));   // same rank in both pairs
+      for (int tile = unit; tile < num_tiles && ok; tile += num_units) {
         int m_blk, n_blk;
-        tile_coords(tile, args.num_m, args.num_n, m_blk, n_blk);
-        const int rb = b_tile_row<EPI, BN>(args, n_blk, rank);
-        const int ra = m_blk * 2 * BM + (int)rank * BM;
+        my_tile(tile, m_blk, n_blk);
+        const int rb = b_tile_row<EPI, BN>(args, n_blk, rank) + (MC == 1 ? (int)pic * (args.b_rows / 2) : 0);
+        const int ra = m_blk * 2 * BM + (int)rank * BM + (MC == 2 ? (int)pic * (BM / 2) : 0);
         for (int kb = 0; kb < args.num_k; ++kb) {
           if (!mbar_wait_cluster(&empty[stage], phase ^ 1u, abort_v)) { ok = false; break; }
           if (leader) mbar_arrive_expect_tx(&full[stage], stage_tx);
           const uint32_t fb = full0 + (uint32_t)stage * 8u;
-          tma_load_2d_pair(sA + stage * A_STAGE_BYTES, &tmA, fb, kb * BK, ra);
-          tma_load_2d_pair(sB + stage * C::B_STAGE_BYTES, &tmB, fb, kb * BK, rb);
+          if (MC == 2)
+            tma_load_2d_pair_mc(sA + stage * A_STAGE_BYTES + (int)pic * (BM / 2) * 128, &tmA, fb, kb * BK, ra, mc_mask);
+          else
+            tma_load_2d_pair(sA + stage * A_STAGE_BYTES, &tmA, fb, kb * BK, ra);
+          if (MC == 1)
+            tma_load_2d_pair_mc(sB + stage * C::B_STAGE_BYTES + (int)pic * (args.b_rows / 2) * 128, &tmB, fb, kb * BK, rb,
+                                mc_mask);
+          else
+            tma_load_2d_pair(sB + stage * C::B_STAGE_BYTES, &tmB, fb, kb * BK, rb);
           last_phase[stage] = (int)phase;
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
           const int pk = kb + C::PREFETCH;
@@ -584,14 +622,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       uint32_t phase = 0;
       bool ok = true;
       int it = 0;
-      for (int tile = pair; tile < num_tiles && ok; tile += num_pairs, ++it) {
+      for (int tile = unit; tile < num_tiles && ok; tile += num_units, ++it) {
         const int acc = it & 1;
         const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
         if (!mbar_wait_cluster(&acc_empty[acc], acc_phase ^ 1u, abort_v)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
         int m_blk, n_blk;
-        tile_coords(tile, args.num_m, args.num_n, m_blk, n_blk);
+        my_tile(tile, m_blk, n_blk);
         const uint32_t idesc = idesc_bf16(2 * BM, n_tile<EPI, BN>(args, n_blk).w);
         for (int kb = 0; kb < args.num_k; ++kb) {
           if (!mbar_wait_cluster(&full[stage], phase, abort_v)) { ok = false; break; }
@@ -603,14 +641,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             mma_bf16_ss_pair(d_tmem, sdesc_kmajor(a0 + k * 32), sdesc_kmajor(b0 + k * 32), idesc,
                              (kb | k) != 0 ? 1u : 0u);
           }
-          mma_commit_pair(&empty[stage], 0x3);
+          mma_commit_pair(&empty[stage], all_mask);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
-        mma_commit_pair(&acc_full[acc], 0x3);
+        mma_commit_pair(&acc_full[acc], pair_mask);
       }
       if (!ok) {  // all MMAs issued so far must finish before TMEM is released
-        mma_commit_pair(drain, 0x1);
+        mma_commit_pair(drain, (uint16_t)(1u << lead));
         drain_wait(drain, 0);
       }
     }
@@ -619,15 +657,15 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     // ---------------------------------------------------------- epilogue (both CTAs)
     const int q = warp & 3;
     const int row = q * 32 + lane;
-    const uint32_t acc_empty0 = mapa_shared(smem_u32(acc_empty), 0);
+    const uint32_t acc_empty0 = mapa_shared(smem_u32(acc_empty), lead);
     int it = 0;
-    for (int tile = pair; tile < num_tiles; tile += num_pairs, ++it) {
+    for (int tile = unit; tile < num_tiles; tile += num_units, ++it) {
       const int acc = it & 1;
       const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
       if (!__all_sync(0xffffffffu, mbar_wait_cluster(&acc_full[acc], acc_phase, abort_v))) break;
       tc_fence_after();
       int m_blk, n_blk;
-      tile_coords(tile, args.num_m, args.num_n, m_blk, n_blk);
+      my_tile(tile, m_blk, n_blk);
       const uint32_t tacc = tmem_addr(tmem_base, (uint32_t)(q * 32), (uint32_t)(acc * BN));
       run_epilogue<EPI, BN>(args, tacc, m_blk * 2 * BM + (int)rank * BM + row, n_blk);
       tc_fence_before();
@@ -637,7 +675,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   }
   tc_fence_before();
   __syncthreads();
-  cluster_sync();          // no CTA of the pair still signals the other's barriers or TMEM
+  cluster_sync();          // no CTA of the cluster still signals another's barriers or TMEM
   if (threadIdx.x == 0 && *abort_v) record_error(args.err, DEVERR_TIMEOUT);
   if (warp == 1) {
     tc_fence_after();
@@ -693,105 +731,175 @@ int gemm_choose_bn(int epi, int M, int N, int H, int F) {
   return best;
 }
 
-GemmPlan gemm_plan(int epi, int M, int N, int H, int F) {
-  GemmPlan p{};
-  p.bn = gemm_choose_bn(epi, M, N, H, F);
-  p.num_n = gemm_num_n(epi, p.bn, N, H, F);
-  p.b_rows = gemm_b_box_rows(epi, p.bn);
-  if ((epi != EPI_PLAIN && epi != EPI_RESID) || getenv("H3_GEMM_BN") || N % 16) return p;
-  // balanced widths: every row tile gets `per_row` column tiles so that all
-  // of them are resident at once; widths nw1 and nw1 - 16 (multiples of 16)
-  const int slots = gemm_pair_slots(), num_m = gemm_m_tiles(M);
-  const int per_row = slots / num_m;
-  if (per_row < 1) return p;
+// Balanced column widths: every row of tiles gets `per_row` column tiles so
+// that all of them are resident at once, widths nw1 and nw1 - 16 (multiples
+// of 16).  mc as in GemmPlan.  Returns false when the uniform plan's wave
+// model is at least as good.
+static bool balance_columns(GemmPlan& p, int N, int num_m, int mc) {
+  const int slots = mc ? gemm_quad_slots() : gemm_pair_slots();
+  int per_row;
+  if (mc == 1) {
+    if (num_m % 2) return false;
+    per_row = slots / (num_m / 2);        // one row unit = two m-tiles
+  } else if (mc == 2) {
+    per_row = 2 * (slots / num_m);        // column tiles come in pairs
+  } else {
+    per_row = slots / num_m;
+  }
+  if (per_row < 1) return false;
   const int units = N / 16;
   const int u1 = (units + per_row - 1) / per_row;
-  if (u1 < 4 || u1 > 16) return p;            // 64..256 columns
+  if (u1 < 4 || u1 > 16) return false;         // 64..256 columns
   const int u2 = u1 - 1;
   const int cnt1 = units - per_row * u2;       // cnt1 * u1 + (per_row - cnt1) * u2 == units
   const int cnt2 = per_row - cnt1;
-  if (cnt1 < 1 || cnt1 > per_row) return p;
-  // wave model of the uniform plan against one wave of the balanced one
+  if (cnt1 < 1 || cnt1 > per_row) return false;
+  // wave model of the uniform (pair) plan against one wave of the balanced one
+  const int pair_slots = gemm_pair_slots();
   const long long u_tiles = (long long)num_m * p.num_n;
-  const long long u_waves = (u_tiles + slots - 1) / slots;
+  const long long u_waves = (u_tiles + pair_slots - 1) / pair_slots;
   const long long u_cost = u_waves * p.bn * 100 / (p.bn == 256 ? 100 : (p.bn == 192 ? 95 : 65));
   const long long b_cost = (long long)(16 * u1) * 100 / 95;
-  if (b_cost >= u_cost) return p;
+  if (b_cost >= u_cost) return false;
   p.nw1 = 16 * u1;
   p.ncnt1 = cnt1;
   p.nw2 = cnt2 > 0 ? 16 * u2 : 0;
   p.num_n = per_row;
   p.bn = p.nw1 <= 128 ? 128 : (p.nw1 <= 192 ? 192 : 256);
-  p.b_rows = p.nw1 / 2;
+  p.mc = mc;
+  // a weight half-box starts on a 1024-byte swizzle atom (8 weight rows), so
+  // with mc == 1 the CTA's box is rounded up to 16 rows; the extra rows go unused
+  p.b_rows = mc == 1 ? (p.nw1 / 2 + 15) / 16 * 16 : p.nw1 / 2;
+  p.b_box = mc == 1 ? p.b_rows / 2 : p.b_rows;
+  p.a_box = mc == 2 ? BM / 2 : BM;
+  return true;
+}
+
+// Uniform tiles with multicast: mc == 1 needs an even number of m-tiles,
+// mc == 2 an even number of column tiles.
+static bool uniform_mc(GemmPlan& p, int num_m, int mc) {
+  if (mc == 1 ? num_m % 2 != 0 : p.num_n % 2 != 0) return false;
+  p.mc = mc;
+  p.b_box = mc == 1 ? p.b_rows / 2 : p.b_rows;
+  p.a_box = mc == 2 ? BM / 2 : BM;
+  return true;
+}
+
+GemmPlan gemm_plan(int epi, int M, int N, int H, int F) {
+  GemmPlan p{};
+  p.bn = gemm_choose_bn(epi, M, N, H, F);
+  p.num_n = gemm_num_n(epi, p.bn, N, H, F);
+  p.b_rows = gemm_b_box_rows(epi, p.bn);
+  p.b_box = p.b_rows;
+  p.a_box = BM;
+  const int num_m = gemm_m_tiles(M);
+  // Multicast (two pairs of a 4-CTA cluster sharing one operand tile) is a
+  // selectable mode, off by default: on GB300 only 36 such clusters fit (144
+  // of 152 SMs), and at 505-4096 rows it measured within a few percent of
+  // independent pairs either way, slower inside the block where the AdaLN
+  // side kernel fragments the SMs.  H3_GEMM_MC selects it: w / a weight /
+  // activation multicast on uniform tiles, bw / ba the same on balanced tiles.
+  const char* env = getenv("H3_GEMM_MC");
+  const std::string mode = env ? env : "";
+  const bool can_balance = (epi == EPI_PLAIN || epi == EPI_RESID) && !getenv("H3_GEMM_BN") && N % 16 == 0;
+  GemmPlan q = p;
+  if (mode == "w" || mode == "a") {
+    if (uniform_mc(q, num_m, mode == "w" ? 1 : 2)) return q;
+    return p;
+  }
+  if (mode == "bw" || mode == "ba") {
+    if (can_balance && balance_columns(q, N, num_m, mode == "bw" ? 1 : 2)) return q;
+    return p;
+  }
+  if (!can_balance) return p;
+  if (balance_columns(q, N, num_m, 0)) return q;
   return p;
 }
 
-int gemm_pair_slots() {
-  static int slots[64] = {0};
+// Clusters of `cl` CTAs (2: pairs, 4: multicast pairs) resident at once.
+static int cluster_slots(int cl) {
+  static int slots[64][2] = {{0}};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
-  if (!slots[dev]) {
+  const int k = cl == 4 ? 1 : 0;
+  if (!slots[dev][k]) {
     // every instance holds one CTA per SM; the largest shared-memory footprint bounds them all
     constexpr int smem = GemmCfg<192>::SMEM > GemmCfg<256>::SMEM ? GemmCfg<192>::SMEM : GemmCfg<256>::SMEM;
     int n = 0;
-    if (cudaFuncSetAttribute(gemm_bf16_tc<EPI_PLAIN, 192>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) ==
+    if (cudaFuncSetAttribute(gemm_bf16_tc<EPI_PLAIN, 192, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) ==
         cudaSuccess) {
       cudaLaunchConfig_t cfg = {};
-      cfg.gridDim = dim3(2 * 1024);
+      cfg.gridDim = dim3(4 * 1024);
       cfg.blockDim = dim3(GEMM_THREADS);
       cfg.dynamicSmemBytes = smem;
       cudaLaunchAttribute attr[1];
       attr[0].id = cudaLaunchAttributeClusterDimension;
-      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.x = (unsigned)cl;
       attr[0].val.clusterDim.y = 1;
       attr[0].val.clusterDim.z = 1;
       cfg.attrs = attr;
       cfg.numAttrs = 1;
-      if (cudaOccupancyMaxActiveClusters(&n, gemm_bf16_tc<EPI_PLAIN, 192>, &cfg) != cudaSuccess) n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, gemm_bf16_tc<EPI_PLAIN, 192, 0>, &cfg) != cudaSuccess) n = 0;
     }
     cudaGetLastError();
-    slots[dev] = n > 0 ? n : num_sms() / 2;
+    slots[dev][k] = n > 0 ? n : num_sms() / cl;
   }
-  return slots[dev];
+  return slots[dev][k];
 }
 
-template <int EPI, int BN>
+int gemm_pair_slots() { return cluster_slots(2); }
+int gemm_quad_slots() { return cluster_slots(4); }
+
+template <int EPI, int BN, int MC>
 static cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, int grid,
                               cudaStream_t stream) {
   constexpr int smem = GemmCfg<BN>::SMEM;
-  cudaError_t e = cudaFuncSetAttribute(gemm_bf16_tc<EPI, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e =
+      cudaFuncSetAttribute(gemm_bf16_tc<EPI, BN, MC>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  return launch_kernel_cluster(gemm_bf16_tc<EPI, BN>, dim3(grid), dim3(GEMM_THREADS), smem, stream, 2, tmA, tmB,
-                               a);
+  return launch_kernel_cluster(gemm_bf16_tc<EPI, BN, MC>, dim3(grid), dim3(GEMM_THREADS), smem, stream,
+                               MC ? 4 : 2, tmA, tmB, a);
 }
 
-cudaError_t launch_gemm(int epi, int bn, const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
-                        cudaStream_t stream) {
-  const int tiles = a.num_m * a.num_n;
-  const int slots = gemm_pair_slots();
-  int pairs = tiles < slots ? tiles : slots;
-  if (a.max_ctas > 0 && pairs > a.max_ctas / 2) pairs = a.max_ctas / 2 > 0 ? a.max_ctas / 2 : 1;
-  const int grid = 2 * pairs;
+cudaError_t launch_gemm(int epi, int bn, int mc, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                        const GemmArgs& a, cudaStream_t stream) {
+  const int cl = mc ? 4 : 2;
+  const int units = mc == 1 ? ((a.num_m + 1) / 2) * a.num_n
+                  : mc == 2 ? a.num_m * ((a.num_n + 1) / 2)
+                            : a.num_m * a.num_n;
+  const int slots = mc ? gemm_quad_slots() : gemm_pair_slots();
+  int n_cl = units < slots ? units : slots;
+  if (a.max_ctas > 0 && n_cl > a.max_ctas / cl) n_cl = a.max_ctas / cl > 0 ? a.max_ctas / cl : 1;
+  const int grid = cl * n_cl;
   const char* names[4] = {"plain", "qkv_qknorm_rope", "gated_residual", "swiglu"};
   cudaError_t e = cudaErrorInvalidValue;
+#define H3_GEMM_CASE(E, B)                                                                       \
+  case E * 1000 + B:                                                                             \
+    e = mc == 2   ? launch_one<E, B, 2>(tmA, tmB, a, grid, stream)                                 \
+        : mc == 1 ? launch_one<E, B, 1>(tmA, tmB, a, grid, stream)                                 \
+                  : launch_one<E, B, 0>(tmA, tmB, a, grid, stream);                                \
+    break;
   switch (epi * 1000 + bn) {
-    case EPI_PLAIN * 1000 + 256: e = launch_one<EPI_PLAIN, 256>(tmA, tmB, a, grid, stream); break;
-    case EPI_PLAIN * 1000 + 192: e = launch_one<EPI_PLAIN, 192>(tmA, tmB, a, grid, stream); break;
-    case EPI_PLAIN * 1000 + 128: e = launch_one<EPI_PLAIN, 128>(tmA, tmB, a, grid, stream); break;
-    case EPI_RESID * 1000 + 256: e = launch_one<EPI_RESID, 256>(tmA, tmB, a, grid, stream); break;
-    case EPI_RESID * 1000 + 192: e = launch_one<EPI_RESID, 192>(tmA, tmB, a, grid, stream); break;
-    case EPI_RESID * 1000 + 128: e = launch_one<EPI_RESID, 128>(tmA, tmB, a, grid, stream); break;
-    case EPI_QKV * 1000 + 256: e = launch_one<EPI_QKV, 256>(tmA, tmB, a, grid, stream); break;
-    case EPI_QKV * 1000 + 128: e = launch_one<EPI_QKV, 128>(tmA, tmB, a, grid, stream); break;
-    case EPI_SWIGLU * 1000 + 256: e = launch_one<EPI_SWIGLU, 256>(tmA, tmB, a, grid, stream); break;
+    H3_GEMM_CASE(EPI_PLAIN, 256)
+    H3_GEMM_CASE(EPI_PLAIN, 192)
+    H3_GEMM_CASE(EPI_PLAIN, 128)
+    H3_GEMM_CASE(EPI_RESID, 256)
+    H3_GEMM_CASE(EPI_RESID, 192)
+    H3_GEMM_CASE(EPI_RESID, 128)
+    H3_GEMM_CASE(EPI_QKV, 256)
+    H3_GEMM_CASE(EPI_QKV, 128)
+    H3_GEMM_CASE(EPI_SWIGLU, 256)
     default: return cudaErrorInvalidValue;
   }
+#undef H3_GEMM_CASE
   if (e != cudaSuccess) return e;
   const int stages = bn == 256 ? GemmCfg<256>::STAGES : (bn == 192 ? GemmCfg<192>::STAGES : GemmCfg<128>::STAGES);
   set_kernel_info("gemm_bf16_tc<%s,%d> tcgen05.mma.cta_group::2.kind::f16 pair-tile=%dx%dx%d stages=%d acc=f32 "
-                  "tmem=2x%d grid=%d (pairs=%d of %d) tiles=%dx%d k_blocks=%d l2_prefetch=%d n-widths=%s%d,%d,%d",
-                  names[epi], bn, 2 * BM, bn, BK, stages, bn, grid, pairs, slots, a.num_m, a.num_n, a.num_k,
-                  2 * stages, a.nw1 ? "balanced:" : "uniform:", a.nw1 ? a.nw1 : bn, a.ncnt1, a.nw2);
+                  "tmem=2x%d grid=%d (%s=%d of %d) tiles=%dx%d k_blocks=%d l2_prefetch=%d n-widths=%s%d,%d,%d",
+                  names[epi], bn, 2 * BM, bn, BK, stages, bn, grid,
+                  mc == 1 ? "weight-multicast quads" : (mc == 2 ? "activation-multicast quads" : "pairs"), n_cl,
+                  slots, a.num_m, a.num_n, a.num_k, 2 * stages, a.nw1 ? "balanced:" : "uniform:",
+                  a.nw1 ? a.nw1 : bn, a.ncnt1, a.nw2);
   return cudaGetLastError();
 }
 
