@@ -171,7 +171,7 @@ void fill_omega(float* omega, float theta) {
 size_t adaln_scratch_bytes(const h3_block_config& c) { return al256((size_t)kAdalnRows * c.cond_dim * 2); }
 
 struct WsLayout {
-  size_t u, table, h, qkv, o, x1, total;
+  size_t u, table, h, qkv, o, x1, sk_part, sk_flags, total;
 };
 WsLayout ws_layout(const h3_block_config& c, int64_t S, int64_t T) {
   const size_t D = (size_t)c.dim, I = (size_t)c.n_heads * 128, F = (size_t)c.ffn_dim;
@@ -189,6 +189,10 @@ WsLayout ws_layout(const h3_block_config& c, int64_t S, int64_t T) {
   off = al256(off + (size_t)S * I * 2);
   L.x1 = off;
   off = al256(off + (size_t)S * D * 2);
+  L.sk_part = off;   // stream-K partial accumulators and flags of the residual GEMMs
+  off = al256(off + gemm_sk_part_bytes());
+  L.sk_flags = off;
+  off = al256(off + gemm_sk_flag_words() * 4);
   L.total = off;
   return L;
 }
@@ -217,8 +221,10 @@ h3_status run_adaln_chunks(const h3_block_config& c, const void* w_ada, const vo
   return cuda_st(launch_adaln_table(tm, tu, a, st));
 }
 
-h3_status run_silu(const h3_block_config& c, const float* t_cond, int T, void* u_scratch, cudaStream_t st) {
-  return cuda_st(launch_silu_rows(t_cond, T, c.cond_dim, static_cast<__nv_bfloat16*>(u_scratch), st));
+h3_status run_silu(const h3_block_config& c, const float* t_cond, int T, void* u_scratch, cudaStream_t st,
+                   uint32_t* zero_words = nullptr, int n_zero_words = 0) {
+  return cuda_st(launch_silu_rows(t_cond, T, c.cond_dim, static_cast<__nv_bfloat16*>(u_scratch), zero_words,
+                                  n_zero_words, st));
 }
 
 h3_status run_adaln_table(const h3_block_config& c, const void* w_ada, const void* b_ada, const float* t_cond,
@@ -306,11 +312,21 @@ h3_status run_attention(int S, int H, const void* q, const void* k, const void* 
   return cuda_st(launch_attention(tq, tk, tv, a, st));
 }
 
+// sk: stream-K scratch of the calling block (flags zeroed by its first
+// kernel); null for the stand-alone stage, which runs whole tiles only.
 h3_status run_resid_gemm(const h3_block_config& c, const h3_packed_meta& m, const void* table, int chunk,
                          const void* act, int K, const void* w, const void* b, const void* x, void* out,
-                         cudaStream_t st) {
+                         cudaStream_t st, SkScratch* sk = nullptr) {
   const int S = m.n_rows, D = c.dim;
-  const GemmPlan pl = gemm_plan(EPI_RESID, S, D, 0, 0);
+  GemmPlan pl = gemm_plan(EPI_RESID, S, D, 0, 0);
+  const int sk_lane = sk ? gemm_sk_lane(S, D, K, 256) : 0;
+  if (sk_lane > 0) {    // whole-width 256-column tiles, k-blocks shared out
+    pl = GemmPlan{};
+    pl.bn = 256;
+    pl.num_n = gemm_num_n(EPI_RESID, 256, D, 0, 0);
+    pl.b_rows = pl.b_box = gemm_b_box_rows(EPI_RESID, 256);
+    pl.a_box = 128;
+  }
   CUtensorMap tA, tB;
   if (!make_tmap_2d(&tA, act, S, K, K, (uint32_t)pl.a_box) || !make_tmap_2d(&tB, w, D, K, K, (uint32_t)pl.b_box))
     return H3_ERR_CUDA;
@@ -329,6 +345,14 @@ h3_status run_resid_gemm(const h3_block_config& c, const h3_packed_meta& m, cons
   a.T = m.n_timesteps;
   a.tag = m.token_tag;
   a.tidx = m.timestep_index;
+  if (sk_lane > 0) {
+    a.sk_lane = sk_lane;
+    a.sk_units = a.num_m * sk_lane;
+    a.sk_iters = (long long)a.num_n * a.num_k;
+    a.sk_part = sk->part;
+    a.sk_flags = sk->flags;
+    a.sk_epoch = ++sk->epoch;
+  }
   return cuda_st(launch_gemm(EPI_RESID, pl.bn, pl.mc, tA, tB, a, st));
 }
 
@@ -407,6 +431,7 @@ h3_status block_impl(const h3_block_config* cfg, const h3_block_weights* w, cons
   void* qkv = base + L.qkv;
   void* o = base + L.o;
   void* x1 = base + L.x1;
+  SkScratch sk{reinterpret_cast<float*>(base + L.sk_part), reinterpret_cast<uint32_t*>(base + L.sk_flags), 0};
   const int I = cfg->n_heads * 128;
   int stage = 0;
   auto mark = [&]() -> h3_status {
@@ -425,7 +450,7 @@ h3_status block_impl(const h3_block_config* cfg, const h3_block_weights* w, cons
   // the caller's stream; chunks 2-5 (two thirds of the weight stream) run on
   // the side stream on the SMs that the QKV GEMM's wave count leaves free,
   // and the caller's stream waits for them before the O projection.
-  s = run_silu(*cfg, meta->t_cond, T, u, st);
+  s = run_silu(*cfg, meta->t_cond, T, u, st, sk.flags, (int)gemm_sk_flag_words());
   if (s != H3_OK) return s;
   const int side_ctas = adaln_side_ctas(*cfg, S);
   cudaStream_t side = side_ctas > 0 ? side_stream() : nullptr;
@@ -469,10 +494,10 @@ h3_status block_impl(const h3_block_config* cfg, const h3_block_weights* w, cons
     H3_TRY(run_attention(S, cfg->n_heads, q, q + 128, q + 256, 3 * I, 384, o, nullptr, st));
   }
   if (side && cudaStreamWaitEvent(st, ev_b, 0) != cudaSuccess) return H3_ERR_CUDA;
-  H3_TRY(run_resid_gemm(*cfg, *meta, table, 2, o, I, w->w_o, w->b_o, x_in, x1, st));
+  H3_TRY(run_resid_gemm(*cfg, *meta, table, 2, o, I, w->w_o, w->b_o, x_in, x1, st, &sk));
   H3_TRY(run_modulate(*cfg, *meta, table, 1, x1, w->norm2_g, h, st));
   H3_TRY(run_ffn_up(*cfg, S, h, w->w_fc1, w->b_fc1, qkv, st));
-  H3_TRY(run_resid_gemm(*cfg, *meta, table, 5, qkv, cfg->ffn_dim, w->w_fc2, w->b_fc2, x1, x_out, st));
+  H3_TRY(run_resid_gemm(*cfg, *meta, table, 5, qkv, cfg->ffn_dim, w->w_fc2, w->b_fc2, x1, x_out, st, &sk));
 #undef H3_TRY
   return H3_OK;
 }
@@ -687,12 +712,13 @@ h3_status h3_refiner_forward(const h3_block_config* cfg, int32_t n_blocks, const
   void* qkv = base + L.qkv;
   void* o = base + L.o;
   void* x1 = base + L.x1;
+  SkScratch sk{reinterpret_cast<float*>(base + L.sk_part), reinterpret_cast<uint32_t*>(base + L.sk_flags), 0};
   int32_t* tag = reinterpret_cast<int32_t*>(base + L.total);
   int32_t* tidx = tag + n_rows;
   int32_t* pos = tidx + n_rows;
   const int S = n_rows, I = cfg->n_heads * 128;
-  if ((s = cuda_st(launch_refiner_setup(S, cfg->dim, static_cast<__nv_bfloat16*>(table), tag, tidx, pos,
-                                        stream))) != H3_OK)
+  if ((s = cuda_st(launch_refiner_setup(S, cfg->dim, static_cast<__nv_bfloat16*>(table), tag, tidx, pos, sk.flags,
+                                        (int)gemm_sk_flag_words(), stream))) != H3_OK)
     return s;
   const h3_packed_meta m{S, 1, tag, tidx, pos, nullptr};
   for (int b = 0; b < n_blocks; ++b) {
@@ -703,10 +729,11 @@ h3_status h3_refiner_forward(const h3_block_config* cfg, int32_t n_blocks, const
     if ((s = run_qkv(*cfg, m, h, wb.w_qkv, wb.b_qkv, wb.q_norm_g, wb.k_norm_g, qkv, stream)) != H3_OK) return s;
     if ((s = run_attention(S, cfg->n_heads, q, q + 128, q + 256, 3 * I, 384, o, nullptr, stream)) != H3_OK)
       return s;
-    if ((s = run_resid_gemm(*cfg, m, table, 2, o, I, wb.w_o, wb.b_o, xi, x1, stream)) != H3_OK) return s;
+    if ((s = run_resid_gemm(*cfg, m, table, 2, o, I, wb.w_o, wb.b_o, xi, x1, stream, &sk)) != H3_OK) return s;
     if ((s = run_modulate(*cfg, m, table, 1, x1, wb.norm2_g, h, stream)) != H3_OK) return s;
     if ((s = run_ffn_up(*cfg, S, h, wb.w_fc1, wb.b_fc1, qkv, stream)) != H3_OK) return s;
-    if ((s = run_resid_gemm(*cfg, m, table, 5, qkv, cfg->ffn_dim, wb.w_fc2, wb.b_fc2, x1, x_out, stream)) != H3_OK)
+    if ((s = run_resid_gemm(*cfg, m, table, 5, qkv, cfg->ffn_dim, wb.w_fc2, wb.b_fc2, x1, x_out, stream, &sk)) !=
+        H3_OK)
       return s;
   }
   if (final_norm_g)   // row-local, so in place on x_out

@@ -101,8 +101,37 @@ struct GemmArgs {
   // nw1 = 0 for uniform tiles of BN columns
   int b_rows;
   int nw1, ncnt1, nw2;
+  int l2_pf;             // k-blocks of weight L2 prefetch ahead of the loads (0: none); set by launch_gemm
+  // stream-K (sk_units > 0, pairs only): each 256-row tile has a lane of
+  // sk_lane CTA pairs; the lane's num_n column tiles x num_k k-blocks,
+  // column-tile-major, are cut into sk_lane equal runs.  A run that starts
+  // inside a tile writes that tile's partial accumulator to sk_part and sets
+  // its flags to sk_epoch; the pair whose run holds the tile's first k-block
+  // adds the partials (in k order) and runs the epilogue.
+  int sk_units;          // num_m * sk_lane
+  int sk_lane;           // pairs per 256-row tile
+  long long sk_iters;    // num_n * num_k, the k-blocks of one lane
+  float* sk_part;        // [sk_units][2 CTAs][BN/32 chunks][8 groups][128 rows][4] fp32
+  uint32_t* sk_flags;    // [sk_units][2 CTAs][4 row quadrants], zero before the first launch that uses them
+  uint32_t sk_epoch;     // nonzero, distinct for every launch between two zeroings
   uint32_t* err;
 };
+
+// Stream-K scratch of one GEMM launch inside a block call: partial
+// accumulators and flags (see GemmArgs), the flags zeroed by the first kernel
+// of the call.  epoch counts the launches that used them since.
+struct SkScratch {
+  float* part;
+  uint32_t* flags;
+  uint32_t epoch;
+};
+size_t gemm_sk_part_bytes();    // partial area for the largest stream-K launch on this GPU
+size_t gemm_sk_flag_words();    // flags for the largest stream-K launch on this GPU
+// CTA pairs per 256-row tile of a stream-K launch of this GEMM, 0 when whole
+// tiles per pair are at least as good.  H3_GEMM_SK=0 turns stream-K off, =1
+// forces it on whenever it is possible; H3_GEMM_SK_UNITS=<n> forces it with
+// n / row tiles pairs per row tile (at most one k-block per pair).
+int gemm_sk_lane(int M, int N, int K, int bn);
 
 // Column tiling of one GEMM launch.  Uniform: num_n tiles of bn columns.
 // Balanced (plain and residual epilogues, when one wave of uniform tiles
@@ -141,12 +170,14 @@ struct AdalnArgs {
   int D;                  // residual width
   int chunk_lo, chunk_hi; // compute the table chunks [chunk_lo, chunk_hi) of every modality
   int max_ctas;           // 0: one CTA per SM; otherwise at most this many
+  int l2_pf;              // stages of weight L2 prefetch ahead of the loads (0: none); set by the launcher
   const float* t_cond;    // [T][C]
   const __nv_bfloat16* bias;  // [NW] nullable
   __nv_bfloat16* out;     // [T][NW]
   uint32_t* err;
 };
-cudaError_t launch_silu_rows(const float* t_cond, int T, int C, __nv_bfloat16* u, cudaStream_t stream);
+cudaError_t launch_silu_rows(const float* t_cond, int T, int C, __nv_bfloat16* u, uint32_t* zero_words,
+                             int n_zero_words, cudaStream_t stream);
 cudaError_t launch_adaln_table(const CUtensorMap& tmW, const CUtensorMap& tmU, const AdalnArgs& a,
                                cudaStream_t stream);
 constexpr int kAdalnRows = 16;   // rows of the u scratch (T <= 16, zero padded)
@@ -201,6 +232,7 @@ cudaError_t launch_rope_qknorm(const CUtensorMap& tmq, const CUtensorMap& tmk, c
 
 // token refiner: identity AdaLN table [3][6][D] and text / timestep-0 / zero-position metadata
 cudaError_t launch_refiner_setup(int S, int D, __nv_bfloat16* table, int32_t* tag, int32_t* tidx, int32_t* pos,
+                                 uint32_t* zero_words, int n_zero_words,
                                  cudaStream_t st);
 
 // ---------------------------------------------------------------------------

@@ -58,7 +58,6 @@ struct GemmCfg {
   static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
   static constexpr int STAGES = (196608 / STAGE_BYTES) > 8 ? 8 : (196608 / STAGE_BYTES);   // 6, 7, 8
   static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + 256;
-  static constexpr int PREFETCH = 2 * STAGES;   // k-blocks of L2 prefetch ahead of the ring
 };
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
@@ -470,6 +469,157 @@ __device__ __forceinline__ void epi_qkv(const GemmArgs& a, uint32_t tacc, int m,
   }
 }
 
+// ---------------------------------------------------------------------------
+// work items: whole tiles (unit, unit + num_units, ...) or, with stream-K, the
+// tile pieces of this pair's run of k-blocks
+// ---------------------------------------------------------------------------
+struct WorkItem {
+  int tile, k0, k1;
+  bool owner;      // holds k-block 0 of the tile: finishes the tile
+};
+
+// Stream-K runs: one lane of sk_lane pairs per 256-row tile (unit = m *
+// sk_lane + j), all lanes walking the same column tiles and k-blocks at the
+// same time (weights shared across the row tiles in L2); pair j of a lane
+// takes k-blocks [j, j + 1) * sk_iters / sk_lane of the lane's num_n x num_k.
+__device__ __forceinline__ long long sk_start(const GemmArgs& a, int j) {
+  return (long long)j * a.sk_iters / a.sk_lane;
+}
+
+__device__ __forceinline__ bool work_item(const GemmArgs& a, int unit, int num_units, int num_tiles, int i,
+                                          WorkItem& w) {
+  if (a.sk_units == 0) {
+    w.tile = unit + i * num_units;
+    w.k0 = 0;
+    w.k1 = a.num_k;
+    w.owner = true;
+    return w.tile < num_tiles;
+  }
+  const int lane_m = unit / a.sk_lane, j = unit - lane_m * a.sk_lane;
+  const long long start = sk_start(a, j), end = sk_start(a, j + 1);
+  const int n = (int)(start / a.num_k) + i;
+  const long long tb = (long long)n * a.num_k;
+  if (tb >= end) return false;
+  w.tile = lane_m * a.num_n + n;     // m-major: (m, n) = (tile / num_n, tile % num_n)
+  w.k0 = i == 0 ? (int)(start - tb) : 0;
+  w.k1 = end - tb < a.num_k ? (int)(end - tb) : a.num_k;
+  w.owner = w.k0 == 0;
+  return w.k0 < w.k1;
+}
+
+__device__ __forceinline__ float* sk_slot(const GemmArgs& a, int unit, uint32_t rank, int nchunks) {
+  return a.sk_part + (size_t)(unit * 2 + (int)rank) * nchunks * (128 * 32);
+}
+// one flag per CTA and accumulator lane quadrant (epilogue warp)
+__device__ __forceinline__ uint32_t* sk_flag(const GemmArgs& a, int unit, uint32_t rank, int quad) {
+  return a.sk_flags + (unit * 2 + (int)rank) * 4 + quad;
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// A piece that does not hold k-block 0: this warp's 32 accumulator rows
+// (every 32-column chunk) to the pair's partial slot, then the warp's flag.
+template <int BN>
+__device__ __forceinline__ void sk_store_partial(const GemmArgs& a, uint32_t tacc, int unit, uint32_t rank,
+                                                 int quad, int row, int lane) {
+  constexpr int NCH = BN / 32;
+  float* slot = sk_slot(a, unit, rank, NCH);
+#pragma unroll 1
+  for (int c = 0; c < NCH; ++c) {
+    uint32_t r[32];
+    tmem_ld32(tacc + c * 32, r);
+    tmem_ld_wait(r);
+    // [chunk][16-byte group g][row]: one warp store covers 512 contiguous bytes
+    uint4* d = reinterpret_cast<uint4*>(slot + (size_t)c * (128 * 32)) + row;
+#pragma unroll
+    for (int g = 0; g < 8; ++g) d[g * 128] = make_uint4(r[4 * g], r[4 * g + 1], r[4 * g + 2], r[4 * g + 3]);
+  }
+  __syncwarp();
+  if (lane == 0) {
+    __threadfence();
+    st_release_u32(sk_flag(a, unit, rank, quad), a.sk_epoch);
+  }
+}
+
+// The owner of tile `tile`: wait for the partials of the runs of its lane
+// that start inside it (units unit+1, unit+2, ...; this warp's rows only) and
+// add them, in that order, to the accumulator in TMEM.  Returns false
+// (warp-uniform) when a wait gave up.
+template <int BN>
+__device__ __forceinline__ bool sk_fold_partials(const GemmArgs& a, uint32_t tacc, int unit, uint32_t rank,
+                                                 int quad, int row, int lane, int tile, volatile int* abort_v) {
+  constexpr int NCH = BN / 32;
+  static_assert(NCH % 2 == 0, "chunks are folded two at a time");
+  const int j = unit % a.sk_lane;
+  const long long tile_end = (long long)(tile % a.num_n + 1) * a.num_k;
+  int j_end = j + 1;
+  while (j_end < a.sk_lane && sk_start(a, j_end) < tile_end) ++j_end;
+  const int q_end = unit + (j_end - j);
+  if (q_end == unit + 1) return true;
+  int ok = 1;
+  if (lane == 0) {
+    for (int q = unit + 1; q < q_end && ok; ++q) {
+      const uint32_t* f = sk_flag(a, q, rank, quad);
+      if (ld_acquire_u32(f) == a.sk_epoch) continue;
+      const uint64_t t0 = globaltimer();
+      for (uint32_t i = 1;; ++i) {
+        if (ld_acquire_u32(f) == a.sk_epoch) break;
+        if ((i & 31u) == 0 && (*abort_v || globaltimer() - t0 > kWaitLimitNs)) {
+          *abort_v = 1;
+          ok = 0;
+          break;
+        }
+      }
+    }
+  }
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  if (!ok) return false;
+  // every lane acquires the flags it depends on before reading the partials
+  for (int q = unit + 1; q < q_end; ++q) (void)ld_acquire_u32(sk_flag(a, q, rank, quad));
+#pragma unroll 1
+  for (int q = unit + 1; q < q_end; ++q) {
+    const float* slot = sk_slot(a, q, rank, NCH);
+#pragma unroll 1
+    for (int c = 0; c < NCH; c += 2) {
+      float4 p[16];
+      const float4* s0 = reinterpret_cast<const float4*>(slot + (size_t)c * (128 * 32)) + row;
+      const float4* s1 = reinterpret_cast<const float4*>(slot + (size_t)(c + 1) * (128 * 32)) + row;
+#pragma unroll
+      for (int g = 0; g < 8; ++g) {
+        p[g] = __ldcg(s0 + g * 128);
+        p[8 + g] = __ldcg(s1 + g * 128);
+      }
+      uint32_t r0[32], r1[32];
+      tmem_ld32(tacc + c * 32, r0);
+      tmem_ld_wait(r0);
+      tmem_ld32(tacc + (c + 1) * 32, r1);
+      tmem_ld_wait(r1);
+#pragma unroll
+      for (int g = 0; g < 8; ++g) {
+        r0[4 * g] = __float_as_uint(__uint_as_float(r0[4 * g]) + p[g].x);
+        r0[4 * g + 1] = __float_as_uint(__uint_as_float(r0[4 * g + 1]) + p[g].y);
+        r0[4 * g + 2] = __float_as_uint(__uint_as_float(r0[4 * g + 2]) + p[g].z);
+        r0[4 * g + 3] = __float_as_uint(__uint_as_float(r0[4 * g + 3]) + p[g].w);
+        r1[4 * g] = __float_as_uint(__uint_as_float(r1[4 * g]) + p[8 + g].x);
+        r1[4 * g + 1] = __float_as_uint(__uint_as_float(r1[4 * g + 1]) + p[8 + g].y);
+        r1[4 * g + 2] = __float_as_uint(__uint_as_float(r1[4 * g + 2]) + p[8 + g].z);
+        r1[4 * g + 3] = __float_as_uint(__uint_as_float(r1[4 * g + 3]) + p[8 + g].w);
+      }
+      tmem_st32(tacc + c * 32, r0);
+      tmem_st32(tacc + (c + 1) * 32, r1);
+      tmem_st_wait();
+    }
+  }
+  return true;
+}
+
 template <int EPI, int BN>
 __device__ __forceinline__ void run_epilogue(const GemmArgs& a, uint32_t tacc, int m, int n_blk) {
   const bool valid = m < a.M;
@@ -529,6 +679,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   const uint16_t pair_mask = (uint16_t)(0x3u << lead);
   // tile `t` of this unit's walk -> (m_blk, n_blk) of this pair
   auto my_tile = [&](int t, int& m_blk, int& n_blk) {
+    if (args.sk_units > 0) {
+      m_blk = t / args.num_n;
+      n_blk = t - m_blk * args.num_n;
+      return;
+    }
     int mu, nu;
     tile_coords(t, num_mu, num_nu, mu, nu);
     m_blk = MC == 1 ? 2 * mu + (int)pic : mu;
@@ -552,11 +707,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     tma_prefetch_desc(&tmB);
     // weights are never written: pull this CTA's half of the first tile into
     // L2 while the previous kernel on the stream may still be running
-    if (unit < num_tiles) {
+    WorkItem w0;
+    if (work_item(args, unit, num_units, num_tiles, 0, w0)) {
       int m0, n0;
-      my_tile(unit, m0, n0);
+      my_tile(w0.tile, m0, n0);
       const int r0 = b_tile_row<EPI, BN>(args, n0, rank) + (MC == 1 ? (int)pic * (args.b_rows / 2) : 0);
-      for (int kb = 0; kb < C::STAGES + C::PREFETCH && kb < args.num_k; ++kb) tma_prefetch_l2(&tmB, kb * BK, r0);
+      for (int kb = w0.k0; kb < w0.k0 + C::STAGES + args.l2_pf && kb < w0.k1; ++kb)
+        tma_prefetch_l2(&tmB, kb * BK, r0);
     }
   }
   if (warp == 1) tmem_alloc_pair(tmem_slot, 512);
@@ -578,12 +735,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       const uint32_t full0 = mapa_shared(smem_u32(full), lead);   // this pair's even CTA's full[0]
       const uint32_t stage_tx = 2u * (uint32_t)(A_STAGE_BYTES + args.b_rows * BK * 2);   // both CTAs' boxes
       const uint16_t mc_mask = (uint16_t)((1u << rank) | (1u << (rank + 2)));   // same rank in both pairs
-      for (int tile = unit; tile < num_tiles && ok; tile += num_units) {
+      WorkItem w;
+      for (int i = 0; ok && work_item(args, unit, num_units, num_tiles, i, w); ++i) {
         int m_blk, n_blk;
-        my_tile(tile, m_blk, n_blk);
+        my_tile(w.tile, m_blk, n_blk);
         const int rb = b_tile_row<EPI, BN>(args, n_blk, rank) + (MC == 1 ? (int)pic * (args.b_rows / 2) : 0);
         const int ra = m_blk * 2 * BM + (int)rank * BM + (MC == 2 ? (int)pic * (BM / 2) : 0);
-        for (int kb = 0; kb < args.num_k; ++kb) {
+        for (int kb = w.k0; kb < w.k1; ++kb) {
           if (!mbar_wait_cluster(&empty[stage], phase ^ 1u, abort_v)) { ok = false; break; }
           if (leader) mbar_arrive_expect_tx(&full[stage], stage_tx);
           const uint32_t fb = full0 + (uint32_t)stage * 8u;
@@ -598,8 +756,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             tma_load_2d_pair(sB + stage * C::B_STAGE_BYTES, &tmB, fb, kb * BK, rb);
           last_phase[stage] = (int)phase;
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-          const int pk = kb + C::PREFETCH;
-          if (pk < args.num_k) tma_prefetch_l2(&tmB, pk * BK, rb);
+          const int pk = kb + args.l2_pf;
+          if (args.l2_pf > 0 && pk < w.k1) tma_prefetch_l2(&tmB, pk * BK, rb);
         }
       }
       if (ok) {
@@ -622,16 +780,17 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       uint32_t phase = 0;
       bool ok = true;
       int it = 0;
-      for (int tile = unit; tile < num_tiles && ok; tile += num_units, ++it) {
+      WorkItem w;
+      for (; ok && work_item(args, unit, num_units, num_tiles, it, w); ++it) {
         const int acc = it & 1;
         const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
         if (!mbar_wait_cluster(&acc_empty[acc], acc_phase ^ 1u, abort_v)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
         int m_blk, n_blk;
-        my_tile(tile, m_blk, n_blk);
+        my_tile(w.tile, m_blk, n_blk);
         const uint32_t idesc = idesc_bf16(2 * BM, n_tile<EPI, BN>(args, n_blk).w);
-        for (int kb = 0; kb < args.num_k; ++kb) {
+        for (int kb = w.k0; kb < w.k1; ++kb) {
           if (!mbar_wait_cluster(&full[stage], phase, abort_v)) { ok = false; break; }
           tc_fence_after();
           const uint32_t a0 = smem_u32(sA + stage * A_STAGE_BYTES);
@@ -639,7 +798,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
             mma_bf16_ss_pair(d_tmem, sdesc_kmajor(a0 + k * 32), sdesc_kmajor(b0 + k * 32), idesc,
-                             (kb | k) != 0 ? 1u : 0u);
+                             (kb != w.k0 || k != 0) ? 1u : 0u);
           }
           mma_commit_pair(&empty[stage], all_mask);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -659,18 +818,27 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     const int row = q * 32 + lane;
     const uint32_t acc_empty0 = mapa_shared(smem_u32(acc_empty), lead);
     int it = 0;
-    for (int tile = unit; tile < num_tiles; tile += num_units, ++it) {
+    WorkItem w;
+    for (; work_item(args, unit, num_units, num_tiles, it, w); ++it) {
       const int acc = it & 1;
       const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
       if (!__all_sync(0xffffffffu, mbar_wait_cluster(&acc_full[acc], acc_phase, abort_v))) break;
       tc_fence_after();
       int m_blk, n_blk;
-      my_tile(tile, m_blk, n_blk);
+      my_tile(w.tile, m_blk, n_blk);
       const uint32_t tacc = tmem_addr(tmem_base, (uint32_t)(q * 32), (uint32_t)(acc * BN));
-      run_epilogue<EPI, BN>(args, tacc, m_blk * 2 * BM + (int)rank * BM + row, n_blk);
+      bool done = true;
+      if (!w.owner) {
+        // stream-K piece without k-block 0: hand the partial to the owner
+        sk_store_partial<BN>(args, tacc, unit, rank, q, row, lane);
+      } else {
+        if (args.sk_units > 0) done = sk_fold_partials<BN>(args, tacc, unit, rank, q, row, lane, w.tile, abort_v);
+        if (done) run_epilogue<EPI, BN>(args, tacc, m_blk * 2 * BM + (int)rank * BM + row, n_blk);
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(acc_empty0 + (uint32_t)acc * 8u);
+      if (!done) break;
     }
   }
   tc_fence_before();
@@ -816,6 +984,45 @@ GemmPlan gemm_plan(int epi, int M, int N, int H, int F) {
   return p;
 }
 
+// Stream-K scratch for the largest launch: one slot of 256-column partial
+// accumulators and 8 flags per CTA pair that can be resident.
+size_t gemm_sk_part_bytes() { return (size_t)gemm_pair_slots() * 2 * 128 * 256 * sizeof(float); }
+size_t gemm_sk_flag_words() { return (size_t)gemm_pair_slots() * 8; }
+
+// Whole 256-column tiles run in waves of one tile per resident pair.  When
+// the last wave would leave more than a tenth of the pairs idle (a few
+// hundred rows: 505 rows x 5376 columns is 42 tiles for 76 pairs), each
+// 256-row tile gets a lane of floor(pairs / row tiles) pairs that share out
+// its column tiles' k-blocks, provided that keeps nine tenths of the pairs
+// busy and gives every pair at least 8 k-blocks.  Returns the pairs per lane.
+int gemm_sk_lane(int M, int N, int K, int bn) {
+  const char* env = getenv("H3_GEMM_SK");
+  if (env && env[0] == '0') return 0;
+  const bool force = env && env[0] == '1';
+  const int slots = gemm_pair_slots();
+  const int num_m = gemm_m_tiles(M);
+  const long long num_n = (N + bn - 1) / bn;
+  const long long lane_iters = num_n * (K / BK);
+  if (num_m > slots) return 0;
+  if (const char* u = getenv("H3_GEMM_SK_UNITS")) {
+    // pairs in all: any lane width from 1 up to one k-block per pair (every
+    // run nonempty: an owner waits for each later run that starts in its tile)
+    long long lane = atoi(u) / num_m;
+    if (lane > slots / num_m) lane = slots / num_m;
+    if (lane > lane_iters) lane = lane_iters;
+    if (lane >= 1) return (int)lane;
+  }
+  int lane = slots / num_m;
+  if ((long long)lane * 8 > lane_iters) lane = (int)(lane_iters / 8);
+  if (lane < 2) return 0;
+  if (force) return lane;
+  const long long tiles = (long long)num_m * num_n;
+  const long long waves = (tiles + slots - 1) / slots;
+  if (tiles * 10 >= waves * slots * 9) return 0;
+  if ((long long)num_m * lane * 10 < (long long)slots * 9) return 0;
+  return lane;
+}
+
 // Clusters of `cl` CTAs (2: pairs, 4: multicast pairs) resident at once.
 static int cluster_slots(int cl) {
   static int slots[64][2] = {{0}};
@@ -862,7 +1069,17 @@ static cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, co
 }
 
 cudaError_t launch_gemm(int epi, int bn, int mc, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                        const GemmArgs& a, cudaStream_t stream) {
+                        const GemmArgs& args, cudaStream_t stream) {
+  // Weight L2 prefetch distance in k-blocks.  Measured on GB300: with up to
+  // 16 row tiles (4096 rows) the TMA ring alone is faster by 1-5 %; at
+  // 15860 rows prefetching two rings ahead is faster by up to 7 %.
+  // H3_GEMM_L2PF=<k-blocks> overrides it.
+  const int stages = bn == 256 ? GemmCfg<256>::STAGES : (bn == 192 ? GemmCfg<192>::STAGES : GemmCfg<128>::STAGES);
+  GemmArgs a = args;
+  const char* pf = getenv("H3_GEMM_L2PF");
+  const int pf_default = a.num_m <= 16 ? 0 : 2 * stages;
+  a.l2_pf = pf ? atoi(pf) : pf_default;
+  if (a.l2_pf < 0 || a.l2_pf > 256) a.l2_pf = pf_default;
   const int cl = mc ? 4 : 2;
   const int units = mc == 1 ? ((a.num_m + 1) / 2) * a.num_n
                   : mc == 2 ? a.num_m * ((a.num_n + 1) / 2)
@@ -870,6 +1087,12 @@ cudaError_t launch_gemm(int epi, int bn, int mc, const CUtensorMap& tmA, const C
   const int slots = mc ? gemm_quad_slots() : gemm_pair_slots();
   int n_cl = units < slots ? units : slots;
   if (a.max_ctas > 0 && n_cl > a.max_ctas / cl) n_cl = a.max_ctas / cl > 0 ? a.max_ctas / cl : 1;
+  if (a.sk_units > 0) {
+    // every pair of a stream-K launch must be resident: an owner waits for
+    // the partials of later pairs
+    if (mc || a.sk_units > gemm_pair_slots()) return cudaErrorInvalidValue;
+    n_cl = a.sk_units;
+  }
   const int grid = cl * n_cl;
   const char* names[4] = {"plain", "qkv_qknorm_rope", "gated_residual", "swiglu"};
   cudaError_t e = cudaErrorInvalidValue;
@@ -893,12 +1116,12 @@ cudaError_t launch_gemm(int epi, int bn, int mc, const CUtensorMap& tmA, const C
   }
 #undef H3_GEMM_CASE
   if (e != cudaSuccess) return e;
-  const int stages = bn == 256 ? GemmCfg<256>::STAGES : (bn == 192 ? GemmCfg<192>::STAGES : GemmCfg<128>::STAGES);
   set_kernel_info("gemm_bf16_tc<%s,%d> tcgen05.mma.cta_group::2.kind::f16 pair-tile=%dx%dx%d stages=%d acc=f32 "
-                  "tmem=2x%d grid=%d (%s=%d of %d) tiles=%dx%d k_blocks=%d l2_prefetch=%d n-widths=%s%d,%d,%d",
+                  "tmem=2x%d grid=%d (%s=%d of %d) tiles=%dx%d k_blocks=%d l2_prefetch=%d stream-k=%d "
+                  "n-widths=%s%d,%d,%d",
                   names[epi], bn, 2 * BM, bn, BK, stages, bn, grid,
                   mc == 1 ? "weight-multicast quads" : (mc == 2 ? "activation-multicast quads" : "pairs"), n_cl,
-                  slots, a.num_m, a.num_n, a.num_k, 2 * stages, a.nw1 ? "balanced:" : "uniform:",
+                  slots, a.num_m, a.num_n, a.num_k, a.l2_pf, a.sk_units, a.nw1 ? "balanced:" : "uniform:",
                   a.nw1 ? a.nw1 : bn, a.ncnt1, a.nw2);
   return cudaGetLastError();
 }
@@ -914,14 +1137,16 @@ constexpr int AD_BN = 16;
 constexpr int AD_THREADS = 192;
 constexpr int AD_U_MAX_KB = 44;  // cond_dim <= 44 * 64 = 2816
 constexpr int AD_SMEM = 1024 + AD_U_MAX_KB * 2048 + AD_STAGES * AD_STAGE_BYTES + 256;
-constexpr int AD_PREFETCH = 2 * AD_STAGES;   // stages of L2 prefetch beyond the ring
 }  // namespace
 
-// u[t][k] = bf16(SiLU(t_cond[t][k])) in fp32 for t < T, zero for T <= t < 16.
+// u[t][k] = bf16(SiLU(t_cond[t][k])) in fp32 for t < T, zero for T <= t < 16;
+// also zeroes n_zero words (the stream-K flags of the block call it starts).
 __global__ void __launch_bounds__(256) silu_rows_kernel(const float* __restrict__ t_cond, int T, int C,
-                                                        __nv_bfloat16* __restrict__ u) {
+                                                        __nv_bfloat16* __restrict__ u, uint32_t* zero_words,
+                                                        int n_zero) {
   griddep_launch_dependents();
   griddep_wait();
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_zero; i += gridDim.x * blockDim.x) zero_words[i] = 0u;
   const int n = AD_BN * C;
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
     const int t = i / C;
@@ -989,7 +1214,7 @@ __global__ void __launch_bounds__(AD_THREADS, 1)
     // previous kernel (the SiLU rows) may still be running
     if ((int)blockIdx.x < num_tiles) {
       const int row0 = tile_row(blockIdx.x);
-      for (int kb = 0; kb < (AD_STAGES + AD_PREFETCH) * AD_KPS && kb < nkb; ++kb)
+      for (int kb = 0; kb < (AD_STAGES + args.l2_pf) * AD_KPS && kb < nkb; ++kb)
         tma_prefetch_l2(&tmW, kb * BK, row0);
     }
   }
@@ -1007,7 +1232,7 @@ __global__ void __launch_bounds__(AD_THREADS, 1)
       bool ok = true;
       for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
         const int row0 = tile_row(tile);
-        for (int kb = 0; kb < AD_PREFETCH * AD_KPS && kb < nkb; ++kb) tma_prefetch_l2(&tmW, kb * BK, row0);
+        for (int kb = 0; kb < args.l2_pf * AD_KPS && kb < nkb; ++kb) tma_prefetch_l2(&tmW, kb * BK, row0);
         for (int st = 0; st < nst; ++st) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_v)) { ok = false; break; }
           const int k0 = st * AD_KPS;
@@ -1018,8 +1243,8 @@ __global__ void __launch_bounds__(AD_THREADS, 1)
                         row0);
           last_phase[stage] = (int)phase;
           if (++stage == AD_STAGES) { stage = 0; phase ^= 1u; }
-          for (int b = 0; b < AD_KPS; ++b) {
-            const int pk = (st + AD_PREFETCH) * AD_KPS + b;
+          for (int b = 0; b < AD_KPS && args.l2_pf > 0; ++b) {
+            const int pk = (st + args.l2_pf) * AD_KPS + b;
             if (pk < nkb) tma_prefetch_l2(&tmW, pk * BK, row0);
           }
         }
@@ -1103,10 +1328,12 @@ __global__ void __launch_bounds__(AD_THREADS, 1)
   }
 }
 
-cudaError_t launch_silu_rows(const float* t_cond, int T, int C, __nv_bfloat16* u, cudaStream_t stream) {
+cudaError_t launch_silu_rows(const float* t_cond, int T, int C, __nv_bfloat16* u, uint32_t* zero_words,
+                             int n_zero_words, cudaStream_t stream) {
   const int n = AD_BN * C;
   const int blocks = (n + 255) / 256 < 1024 ? (n + 255) / 256 : 1024;
-  return launch_kernel(silu_rows_kernel, dim3(blocks), dim3(256), 0, stream, t_cond, T, C, u);
+  return launch_kernel(silu_rows_kernel, dim3(blocks), dim3(256), 0, stream, t_cond, T, C, u, zero_words,
+                       zero_words ? n_zero_words : 0);
 }
 
 cudaError_t launch_adaln_table(const CUtensorMap& tmW, const CUtensorMap& tmU, const AdalnArgs& a,
@@ -1124,15 +1351,24 @@ cudaError_t launch_adaln_table(const CUtensorMap& tmW, const CUtensorMap& tmU, c
       cluster = 2;
     }
   }
+  // Prefetching the weight stream into L2 ahead of the TMA loads measured
+  // slower on GB300 (6.2 against 6.6 TB/s over the full table, 35 against
+  // 31 us for chunks 0-1 at D = 5376): the ring alone keeps HBM busy.  Only
+  // the first tile's stages are prefetched, before the dependency wait.
+  // H3_ADALN_L2PF=<stages> turns the running prefetch on.
+  AdalnArgs a2 = a;
+  const char* pf = getenv("H3_ADALN_L2PF");
+  a2.l2_pf = pf ? atoi(pf) : 0;
+  if (a2.l2_pf < 0 || a2.l2_pf > 64) a2.l2_pf = 0;
   cudaError_t e = cudaFuncSetAttribute(adaln_table_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, AD_SMEM);
   if (e != cudaSuccess) return e;
   e = launch_kernel_cluster(adaln_table_kernel, dim3(grid), dim3(AD_THREADS), AD_SMEM, stream, cluster, tmW, tmU,
-                            a);
+                            a2);
   if (e != cudaSuccess) return e;
   set_kernel_info("adaln_table_kernel tcgen05.mma.cta_group::1.kind::f16 tile=%dx%dx%d stages=%dx%d acc=f32 "
                   "tmem=2x%d grid=%d cluster=%d tiles=%d chunks=[%d,%d) k_blocks=%d l2_prefetch=%d stages",
                   BM, AD_BN, BK, AD_STAGES, AD_KPS, AD_BN, grid, cluster, tiles, a.chunk_lo, a.chunk_hi, a.C / BK,
-                  AD_PREFETCH);
+                  a2.l2_pf);
   return cudaGetLastError();
 }
 

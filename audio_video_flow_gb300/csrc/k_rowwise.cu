@@ -327,9 +327,12 @@ cudaError_t launch_rope_qknorm(const CUtensorMap& tmq, const CUtensorMap& tmk, c
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) refiner_setup_kernel(int S, int D, __nv_bfloat16* __restrict__ table,
                                                             int32_t* __restrict__ tag, int32_t* __restrict__ tidx,
-                                                            int32_t* __restrict__ pos) {
+                                                            int32_t* __restrict__ pos, uint32_t* zero_words,
+                                                            int n_zero) {
   griddep_launch_dependents();
   griddep_wait();
+  // the stream-K flags of the call
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_zero; i += gridDim.x * blockDim.x) zero_words[i] = 0u;
   const int n_tab = 3 * 6 * D;
   const int n = n_tab + 5 * S;
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
@@ -346,11 +349,12 @@ __global__ void __launch_bounds__(256) refiner_setup_kernel(int S, int D, __nv_b
 }
 
 cudaError_t launch_refiner_setup(int S, int D, __nv_bfloat16* table, int32_t* tag, int32_t* tidx, int32_t* pos,
-                                 cudaStream_t st) {
+                                 uint32_t* zero_words, int n_zero_words, cudaStream_t st) {
   const long long n = 18LL * D + 5LL * S;
   int grid = (int)((n + 255) / 256);
   if (grid > 4 * num_sms()) grid = 4 * num_sms();
-  cudaError_t e = launch_kernel(refiner_setup_kernel, dim3(grid), dim3(256), 0, st, S, D, table, tag, tidx, pos);
+  cudaError_t e = launch_kernel(refiner_setup_kernel, dim3(grid), dim3(256), 0, st, S, D, table, tag, tidx, pos,
+                                zero_words, zero_words ? n_zero_words : 0);
   if (e != cudaSuccess) return e;
   set_kernel_info("refiner_setup_kernel identity-table rows=%d", S);
   return cudaGetLastError();
