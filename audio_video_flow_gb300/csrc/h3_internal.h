@@ -112,7 +112,7 @@ struct GemmArgs {
   int sk_lane;           // pairs per 256-row tile
   long long sk_iters;    // num_n * num_k, the k-blocks of one lane
   float* sk_part;        // [sk_units][2 CTAs][BN/32 chunks][8 groups][128 rows][4] fp32
-  uint32_t* sk_flags;    // [sk_units][2 CTAs][4 row quadrants], zero before the first launch that uses them
+  uint32_t* sk_flags;    // [sk_units][2 CTAs][4 row quadrants][2 column halves], zero before first use
   uint32_t sk_epoch;     // nonzero, distinct for every launch between two zeroings
   uint32_t* err;
 };

@@ -22,11 +22,15 @@
 // counted on the even CTA's barrier) and L2 prefetches further ahead; warp 1
 // of the even CTA issues the MMAs into one of two TMEM accumulators
 // (2 x BN columns) and releases ring stages to both CTAs with a multicast
-// commit; warps 2-5 of each CTA drain the other accumulator through
-// tcgen05.ld and run the epilogue.  BN (256, 192 or 128) is chosen per
-// launch to fill the SMs; it changes the tiling, never the reduction: every
-// output element is the same fixed sequence of 16-deep MMAs over K, so the
-// result does not depend on M, BN or the grid (no split-K).
+// commit; warps 2-9 of each CTA drain the other accumulator through
+// tcgen05.ld and run the epilogue, two warps per TMEM lane quadrant (warp w
+// reads lanes 32 (w % 4) ..), warps 2-5 on the first and 6-9 on the second
+// half of the tile's columns.  BN (256, 192 or 128) is chosen per launch to
+// fill the SMs; it changes the tiling, never the reduction: with whole tiles
+// every output element is the same fixed sequence of 16-deep MMAs over K, so
+// the result does not depend on M, BN or the grid.  Stream-K launches (the
+// residual GEMMs of a block when whole tiles would leave pairs idle) add
+// fp32 partial sums of k-ranges in a fixed order.
 //
 // adaln_table_kernel: the AdaLN projection.  Its M dimension is only T <= 16
 // timestep rows, so the GEMM runs transposed: the 18*D weight rows are the
@@ -48,7 +52,7 @@ namespace {
 
 constexpr int BM = 128, BK = 64;
 constexpr int A_STAGE_BYTES = BM * BK * 2;   // 16 KB
-constexpr int GEMM_THREADS = 192;
+constexpr int GEMM_THREADS = 320;   // producer, MMA issuer, 8 epilogue warps
 
 // Per CTA of a pair: its 128 rows of A and BN/2 rows of B per 64-deep k-block.
 template <int BN>
@@ -200,11 +204,21 @@ __device__ __forceinline__ void plain_chunk(const GemmArgs& a, uint32_t tc, int 
   }
 }
 
-__device__ __forceinline__ void epi_plain(const GemmArgs& a, uint32_t tacc, int m, bool valid, NTile t) {
-  int c = 0;
+// Column half `half` of a w-column tile: the first half takes the first
+// floor(w / 64) 32-column chunks, the second the other chunks and the
+// 16-column tail.
+__device__ __forceinline__ void half_range(int w, int half, int& c0, int& c1) {
+  const int mid = ((w >> 5) >> 1) << 5;
+  c0 = half ? mid : 0;
+  c1 = half ? w : mid;
+}
+
+__device__ __forceinline__ void epi_plain(const GemmArgs& a, uint32_t tacc, int m, bool valid, NTile t, int half) {
+  int c, c1;
+  half_range(t.w, half, c, c1);
 #pragma unroll 1
-  for (; c + 32 <= t.w; c += 32) plain_chunk<32>(a, tacc + c, m, valid, t.n0 + c);
-  if (c < t.w) plain_chunk<16>(a, tacc + c, m, valid, t.n0 + c);
+  for (; c + 32 <= c1; c += 32) plain_chunk<32>(a, tacc + c, m, valid, t.n0 + c);
+  if (c < c1) plain_chunk<16>(a, tacc + c, m, valid, t.n0 + c);
 }
 
 template <int NC>
@@ -236,7 +250,7 @@ __device__ __forceinline__ void resid_chunk(const GemmArgs& a, uint32_t tc, int 
   }
 }
 
-__device__ __forceinline__ void epi_resid(const GemmArgs& a, uint32_t tacc, int m, bool valid, NTile t) {
+__device__ __forceinline__ void epi_resid(const GemmArgs& a, uint32_t tacc, int m, bool valid, NTile t, int half) {
   const __nv_bfloat16* gate = nullptr;
   if (valid) {
     const int tg = a.tag[m], ti = a.tidx[m];
@@ -247,15 +261,17 @@ __device__ __forceinline__ void epi_resid(const GemmArgs& a, uint32_t tacc, int 
       gate = a.table + ((size_t)(ti * 3 + tg) * 6 + a.chunk) * a.D;
     }
   }
-  int c = 0;
+  int c, c1;
+  half_range(t.w, half, c, c1);
 #pragma unroll 1
-  for (; c + 32 <= t.w; c += 32) resid_chunk<32>(a, tacc + c, m, valid, gate, t.n0 + c);
-  if (c < t.w) resid_chunk<16>(a, tacc + c, m, valid, gate, t.n0 + c);
+  for (; c + 32 <= c1; c += 32) resid_chunk<32>(a, tacc + c, m, valid, gate, t.n0 + c);
+  if (c < c1) resid_chunk<16>(a, tacc + c, m, valid, gate, t.n0 + c);
 }
 
-__device__ __forceinline__ void epi_swiglu(const GemmArgs& a, uint32_t tacc, int m, bool valid, int n_blk) {
+__device__ __forceinline__ void epi_swiglu(const GemmArgs& a, uint32_t tacc, int m, bool valid, int n_blk,
+                                           int half) {
 #pragma unroll 1
-  for (int c = 0; c < 4; ++c) {
+  for (int c = 2 * half; c < 2 * half + 2; ++c) {
     uint32_t g[32], u[32];
     tmem_ld32(tacc + c * 32, g);
     tmem_ld32(tacc + 128 + c * 32, u);
@@ -335,94 +351,6 @@ __device__ __forceinline__ void epi_qk_part(const GemmArgs& a, uint32_t tpart, i
   }
 }
 
-// Q and K columns of head h together (q at tq, k at tk, 128 accumulator
-// columns each): the same per-head RMSNorm and rotation as epi_qk_part, with
-// each of the row's 48 rotation angles evaluated once for both parts.
-__device__ __forceinline__ void epi_qk_both(const GemmArgs& a, uint32_t tq, uint32_t tk, int m, bool valid, int h,
-                                            const float (&pos)[3]) {
-  const int cq = h * 384, ck = h * 384 + 128;   // output / weight column of channel 0 of q, k
-  float ssq = 0.f, ssk = 0.f;
-#pragma unroll 1
-  for (int c = 0; c < 4; ++c) {
-    uint32_t rq[16], rk[16], rq2[16], rk2[16];
-    tmem_ld16(tq + c * 32, rq);
-    tmem_ld16(tk + c * 32, rk);
-    tmem_ld_wait(rq, rk);
-    tmem_ld16(tq + c * 32 + 16, rq2);
-    tmem_ld16(tk + c * 32 + 16, rk2);
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const float vq = bf16_round(__uint_as_float(rq[j]) + bias_at(a.bias, cq + c * 32 + j));
-      const float vk = bf16_round(__uint_as_float(rk[j]) + bias_at(a.bias, ck + c * 32 + j));
-      ssq = __fmaf_rn(vq, vq, ssq);
-      ssk = __fmaf_rn(vk, vk, ssk);
-    }
-    tmem_ld_wait(rq2, rk2);
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const float vq = bf16_round(__uint_as_float(rq2[j]) + bias_at(a.bias, cq + c * 32 + 16 + j));
-      const float vk = bf16_round(__uint_as_float(rk2[j]) + bias_at(a.bias, ck + c * 32 + 16 + j));
-      ssq = __fmaf_rn(vq, vq, ssq);
-      ssk = __fmaf_rn(vk, vk, ssk);
-    }
-  }
-  const float invq = 1.0f / sqrtf(ssq * (1.0f / 128.0f) + a.eps);
-  const float invk = 1.0f / sqrtf(ssk * (1.0f / 128.0f) + a.eps);
-#pragma unroll 1
-  for (int band = 0; band < 3; ++band) {
-    const float p = band == 0 ? pos[0] : (band == 1 ? pos[1] : pos[2]);
-    float cs[16], sn[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) sincosf(p * a.omega[i], &sn[i], &cs[i]);
-#pragma unroll
-    for (int part = 0; part < 2; ++part) {
-      const uint32_t tp = part ? tk : tq;
-      const int cb = part ? ck : cq;
-      const float inv = part ? invk : invq;
-      const __nv_bfloat16* gain = part ? a.k_gain : a.q_gain;
-      uint32_t lo[16], hi[16];
-      tmem_ld16(tp + band * 16, lo);
-      tmem_ld16(tp + 48 + band * 16, hi);
-      tmem_ld_wait(lo, hi);
-      if (valid) {
-        float o1[16], o2[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int j = band * 16 + i;
-          const float v1 = bf16_round(__uint_as_float(lo[i]) + bias_at(a.bias, cb + j));
-          const float v2 = bf16_round(__uint_as_float(hi[i]) + bias_at(a.bias, cb + 48 + j));
-          const float x1 = bf16_round(v1 * inv * __bfloat162float(gain[j]));
-          const float x2 = bf16_round(v2 * inv * __bfloat162float(gain[48 + j]));
-          o1[i] = __fmaf_rn(x1, cs[i], -(x2 * sn[i]));
-          o2[i] = __fmaf_rn(x2, cs[i], x1 * sn[i]);
-        }
-        __nv_bfloat16* dst = a.out + (size_t)m * a.ldo + cb;
-        store16_bf16(dst + band * 16, o1);
-        store16_bf16(dst + 48 + band * 16, o2);
-      }
-    }
-  }
-#pragma unroll 1
-  for (int part = 0; part < 2; ++part) {
-    const uint32_t tp = part ? tk : tq;
-    const int cb = part ? ck : cq;
-    const float inv = part ? invk : invq;
-    const __nv_bfloat16* gain = part ? a.k_gain : a.q_gain;
-    uint32_t r[32];
-    tmem_ld32(tp + 96, r);
-    tmem_ld_wait(r);
-    if (valid) {
-      float v[32];
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const float x = bf16_round(__uint_as_float(r[j]) + bias_at(a.bias, cb + 96 + j));
-        v[j] = x * inv * __bfloat162float(gain[96 + j]);
-      }
-      store32_bf16(a.out + (size_t)m * a.ldo + cb + 96, v);
-    }
-  }
-}
-
 // V columns of one head (128 accumulator columns at tpart).
 __device__ __forceinline__ void epi_v_head(const GemmArgs& a, uint32_t tpart, int m, bool valid, int head) {
 #pragma unroll 1
@@ -441,7 +369,7 @@ __device__ __forceinline__ void epi_v_head(const GemmArgs& a, uint32_t tpart, in
 }
 
 template <int BN>
-__device__ __forceinline__ void epi_qkv(const GemmArgs& a, uint32_t tacc, int m, bool valid, int n_blk) {
+__device__ __forceinline__ void epi_qkv(const GemmArgs& a, uint32_t tacc, int m, bool valid, int n_blk, int half) {
   float pos[3] = {0.f, 0.f, 0.f};
   if (valid) {
 #pragma unroll
@@ -455,14 +383,11 @@ __device__ __forceinline__ void epi_qkv(const GemmArgs& a, uint32_t tacc, int m,
     }
   }
   if (BN == 256) {
-    if (n_blk < a.H) {
-      epi_qk_both(a, tacc, tacc + 128, m, valid, n_blk, pos);
-    } else {
-      const int p = n_blk - a.H;
-      epi_v_head(a, tacc, m, valid, 2 * p);
-      epi_v_head(a, tacc + 128, m, valid, 2 * p + 1);
-    }
-  } else {
+    // q | k of head n_blk (one part per column half), or v of heads 2p, 2p+1
+    if (n_blk < a.H) epi_qk_part(a, tacc + half * 128, m, valid, n_blk, half, pos);
+    else epi_v_head(a, tacc + half * 128, m, valid, 2 * (n_blk - a.H) + half);
+  } else if (half == 0) {
+    // one 128-column part: its norm needs all of it in one warp
     const int head = n_blk / 3, part = n_blk % 3;
     if (part < 2) epi_qk_part(a, tacc, m, valid, head, part, pos);
     else epi_v_head(a, tacc, m, valid, head);
@@ -510,9 +435,9 @@ __device__ __forceinline__ bool work_item(const GemmArgs& a, int unit, int num_u
 __device__ __forceinline__ float* sk_slot(const GemmArgs& a, int unit, uint32_t rank, int nchunks) {
   return a.sk_part + (size_t)(unit * 2 + (int)rank) * nchunks * (128 * 32);
 }
-// one flag per CTA and accumulator lane quadrant (epilogue warp)
-__device__ __forceinline__ uint32_t* sk_flag(const GemmArgs& a, int unit, uint32_t rank, int quad) {
-  return a.sk_flags + (unit * 2 + (int)rank) * 4 + quad;
+// one flag per CTA, accumulator lane quadrant and column half (epilogue warp)
+__device__ __forceinline__ uint32_t* sk_flag(const GemmArgs& a, int unit, uint32_t rank, int quad, int half) {
+  return a.sk_flags + ((unit * 2 + (int)rank) * 4 + quad) * 2 + half;
 }
 
 __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
@@ -525,14 +450,16 @@ __device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v) {
 }
 
 // A piece that does not hold k-block 0: this warp's 32 accumulator rows
-// (every 32-column chunk) to the pair's partial slot, then the warp's flag.
+// (the 32-column chunks of its column half) to the pair's partial slot, then
+// the warp's flag.
 template <int BN>
 __device__ __forceinline__ void sk_store_partial(const GemmArgs& a, uint32_t tacc, int unit, uint32_t rank,
-                                                 int quad, int row, int lane) {
+                                                 int quad, int half, int row, int lane) {
   constexpr int NCH = BN / 32;
   float* slot = sk_slot(a, unit, rank, NCH);
+  const int c_end = half ? NCH : NCH / 2;
 #pragma unroll 1
-  for (int c = 0; c < NCH; ++c) {
+  for (int c = half ? NCH / 2 : 0; c < c_end; ++c) {
     uint32_t r[32];
     tmem_ld32(tacc + c * 32, r);
     tmem_ld_wait(r);
@@ -544,7 +471,7 @@ __device__ __forceinline__ void sk_store_partial(const GemmArgs& a, uint32_t tac
   __syncwarp();
   if (lane == 0) {
     __threadfence();
-    st_release_u32(sk_flag(a, unit, rank, quad), a.sk_epoch);
+    st_release_u32(sk_flag(a, unit, rank, quad, half), a.sk_epoch);
   }
 }
 
@@ -554,9 +481,10 @@ __device__ __forceinline__ void sk_store_partial(const GemmArgs& a, uint32_t tac
 // (warp-uniform) when a wait gave up.
 template <int BN>
 __device__ __forceinline__ bool sk_fold_partials(const GemmArgs& a, uint32_t tacc, int unit, uint32_t rank,
-                                                 int quad, int row, int lane, int tile, volatile int* abort_v) {
+                                                 int quad, int half, int row, int lane, int tile,
+                                                 volatile int* abort_v) {
   constexpr int NCH = BN / 32;
-  static_assert(NCH % 2 == 0, "chunks are folded two at a time");
+  static_assert(NCH % 4 == 0, "each column half is folded two chunks at a time");
   const int j = unit % a.sk_lane;
   const long long tile_end = (long long)(tile % a.num_n + 1) * a.num_k;
   int j_end = j + 1;
@@ -566,7 +494,7 @@ __device__ __forceinline__ bool sk_fold_partials(const GemmArgs& a, uint32_t tac
   int ok = 1;
   if (lane == 0) {
     for (int q = unit + 1; q < q_end && ok; ++q) {
-      const uint32_t* f = sk_flag(a, q, rank, quad);
+      const uint32_t* f = sk_flag(a, q, rank, quad, half);
       if (ld_acquire_u32(f) == a.sk_epoch) continue;
       const uint64_t t0 = globaltimer();
       for (uint32_t i = 1;; ++i) {
@@ -582,12 +510,12 @@ __device__ __forceinline__ bool sk_fold_partials(const GemmArgs& a, uint32_t tac
   ok = __shfl_sync(0xffffffffu, ok, 0);
   if (!ok) return false;
   // every lane acquires the flags it depends on before reading the partials
-  for (int q = unit + 1; q < q_end; ++q) (void)ld_acquire_u32(sk_flag(a, q, rank, quad));
+  for (int q = unit + 1; q < q_end; ++q) (void)ld_acquire_u32(sk_flag(a, q, rank, quad, half));
 #pragma unroll 1
   for (int q = unit + 1; q < q_end; ++q) {
     const float* slot = sk_slot(a, q, rank, NCH);
 #pragma unroll 1
-    for (int c = 0; c < NCH; c += 2) {
+    for (int c = half ? NCH / 2 : 0; c < (half ? NCH : NCH / 2); c += 2) {
       float4 p[16];
       const float4* s0 = reinterpret_cast<const float4*>(slot + (size_t)c * (128 * 32)) + row;
       const float4* s1 = reinterpret_cast<const float4*>(slot + (size_t)(c + 1) * (128 * 32)) + row;
@@ -621,12 +549,12 @@ __device__ __forceinline__ bool sk_fold_partials(const GemmArgs& a, uint32_t tac
 }
 
 template <int EPI, int BN>
-__device__ __forceinline__ void run_epilogue(const GemmArgs& a, uint32_t tacc, int m, int n_blk) {
+__device__ __forceinline__ void run_epilogue(const GemmArgs& a, uint32_t tacc, int m, int n_blk, int half) {
   const bool valid = m < a.M;
-  if (EPI == EPI_PLAIN) epi_plain(a, tacc, m, valid, n_tile<EPI, BN>(a, n_blk));
-  if (EPI == EPI_RESID) epi_resid(a, tacc, m, valid, n_tile<EPI, BN>(a, n_blk));
-  if (EPI == EPI_SWIGLU) epi_swiglu(a, tacc, m, valid, n_blk);
-  if (EPI == EPI_QKV) epi_qkv<BN>(a, tacc, m, valid, n_blk);
+  if (EPI == EPI_PLAIN) epi_plain(a, tacc, m, valid, n_tile<EPI, BN>(a, n_blk), half);
+  if (EPI == EPI_RESID) epi_resid(a, tacc, m, valid, n_tile<EPI, BN>(a, n_blk), half);
+  if (EPI == EPI_SWIGLU) epi_swiglu(a, tacc, m, valid, n_blk, half);
+  if (EPI == EPI_QKV) epi_qkv<BN>(a, tacc, m, valid, n_blk, half);
 }
 
 }  // namespace
@@ -696,7 +624,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], 8);
+      mbar_init(&acc_empty[i], 16);   // 8 epilogue warps of each CTA
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -814,7 +742,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     __syncwarp();
   } else {
     // ---------------------------------------------------------- epilogue (both CTAs)
-    const int q = warp & 3;
+    const int q = warp & 3;              // TMEM lane quadrant
+    const int half = (warp - 2) >> 2;    // column half: warps 2-5 first, 6-9 second
     const int row = q * 32 + lane;
     const uint32_t acc_empty0 = mapa_shared(smem_u32(acc_empty), lead);
     int it = 0;
@@ -830,10 +759,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       bool done = true;
       if (!w.owner) {
         // stream-K piece without k-block 0: hand the partial to the owner
-        sk_store_partial<BN>(args, tacc, unit, rank, q, row, lane);
+        // (stream-K launches use 256-column tiles only)
+        if constexpr (BN == 256) sk_store_partial<BN>(args, tacc, unit, rank, q, half, row, lane);
       } else {
-        if (args.sk_units > 0) done = sk_fold_partials<BN>(args, tacc, unit, rank, q, row, lane, w.tile, abort_v);
-        if (done) run_epilogue<EPI, BN>(args, tacc, m_blk * 2 * BM + (int)rank * BM + row, n_blk);
+        if constexpr (BN == 256) {
+          if (args.sk_units > 0)
+            done = sk_fold_partials<BN>(args, tacc, unit, rank, q, half, row, lane, w.tile, abort_v);
+        }
+        if (done) run_epilogue<EPI, BN>(args, tacc, m_blk * 2 * BM + (int)rank * BM + row, n_blk, half);
       }
       tc_fence_before();
       __syncwarp();
@@ -985,9 +918,10 @@ GemmPlan gemm_plan(int epi, int M, int N, int H, int F) {
 }
 
 // Stream-K scratch for the largest launch: one slot of 256-column partial
-// accumulators and 8 flags per CTA pair that can be resident.
+// accumulators and 16 flags (CTA x lane quadrant x column half) per CTA pair
+// that can be resident.
 size_t gemm_sk_part_bytes() { return (size_t)gemm_pair_slots() * 2 * 128 * 256 * sizeof(float); }
-size_t gemm_sk_flag_words() { return (size_t)gemm_pair_slots() * 8; }
+size_t gemm_sk_flag_words() { return (size_t)gemm_pair_slots() * 16; }
 
 // Whole 256-column tiles run in waves of one tile per resident pair.  When
 // the last wave would leave more than a tenth of the pairs idle (a few
@@ -1090,7 +1024,7 @@ cudaError_t launch_gemm(int epi, int bn, int mc, const CUtensorMap& tmA, const C
   if (a.sk_units > 0) {
     // every pair of a stream-K launch must be resident: an owner waits for
     // the partials of later pairs
-    if (mc || a.sk_units > gemm_pair_slots()) return cudaErrorInvalidValue;
+    if (mc || bn != 256 || a.sk_units > gemm_pair_slots()) return cudaErrorInvalidValue;
     n_cl = a.sk_units;
   }
   const int grid = cl * n_cl;
