@@ -40,12 +40,15 @@ STAGES = ("adaln_table", "norm1_modulate", "qkv_qknorm_rope", "attention", "out_
 # kernel, from ncu captures of the current kernel build (profiles/
 # block505_launches.md, block1824_traffic.md, attn16384_traffic.md,
 # attention_attn4096.md), keyed "stage@workload"; absent when not captured.
+# At 505 rows QKV and FC1 take turns as the longest stage, so both are here.
 # Attention's DRAM traffic is reading q, k, v and writing o once (K/V re-reads
 # hit L2), so the 32,768- and 15,860-row values are the 16,384-row capture
 # scaled by the row count.
 TRAFFIC = {
-    "qkv_qknorm_rope@block505": 251573760,
-    "fc1_swiglu@block1824": 390174976,
+    "qkv_qknorm_rope@block505": 249717248,
+    "fc1_swiglu@block505": 332196096,
+    "qkv_qknorm_rope@block1824": 337300736,
+    "fc1_swiglu@block1824": 386801920,
     "attention@attn4096": 214684160,
     "attention@attn16384": 919471872,
     "attention@attn32768": 1838943744,

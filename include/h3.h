@@ -133,7 +133,14 @@ size_t h3_block_workspace_bytes(const h3_block_config *cfg, int32_t n_rows, int3
  * When D is a multiple of 128, the AdaLN chunks that norm1 does not read are
  * computed on a stream the library owns (one per device), overlapping the
  * QKV projection; the caller's stream waits for them before the O
- * projection, so the work stays ordered on the caller's stream. */
+ * projection, so the work stays ordered on the caller's stream.
+ * Reduction order: when whole 256-column tiles would leave SM pairs idle
+ * (a few hundred rows), the O and FC2 projections share each tile's K range
+ * out over several SM pairs and add the fp32 partial sums in k order
+ * (stream-K).  The split is fixed for a given row count and GPU, so repeated
+ * calls are bitwise equal, but it changes with the row count and the number
+ * of SMs; set H3_GEMM_SK=0 in the environment for one fixed MMA sequence per
+ * output element at every size (the RFC's strict order, section 4). */
 h3_status h3_block_forward(const h3_block_config *cfg, const h3_block_weights *w,
                            const h3_packed_meta *meta, const void *x_in, void *x_out,
                            void *workspace, size_t ws_bytes, cudaStream_t stream);
