@@ -328,18 +328,22 @@ def test_block_forward_505(h3):
 
 
 @pytest.mark.parametrize("name,units", [("ragged205", 2), ("ragged205", 7), ("d576", 5), ("d576", 76),
-                                        ("block505", 4), ("block505", 76)])
+                                        ("block505", 4), ("block505", 76), ("block505", 0)])
 def test_block_forward_stream_k(h3, name, units, monkeypatch):
     """The residual GEMMs of the block with their k-blocks shared out over
     `units` CTA pairs (stream-K, units / row tiles pairs per 256-row tile):
     runs that start inside a tile hand partial accumulators to the pair
     holding the tile's first k-block, which adds them in k order.  Against
-    the oracle, and bitwise repeatable."""
-    monkeypatch.setenv("H3_GEMM_SK_UNITS", str(units))
+    the oracle, and bitwise repeatable.  units = 0: stream-K off (the strict
+    reduction order), whole tiles only."""
+    if units:
+        monkeypatch.setenv("H3_GEMM_SK_UNITS", str(units))
+    else:
+        monkeypatch.setenv("H3_GEMM_SK", "0")
     c = get_case(name)
     y = run_block(h3, c)
     info = h3.h3_last_kernel_info()
-    assert "stream-k=0" not in info, info
+    assert ("stream-k=0" in info) == (units == 0), info
     if name == "block505":
         assert_close(to_np(y), c.ref["y"], f"block[{name}] stream-k {units}", CHAIN_MAX_E, CHAIN_MEAN_E)
     else:
