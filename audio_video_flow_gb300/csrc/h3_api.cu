@@ -277,8 +277,8 @@ h3_status run_qkv(const h3_block_config& c, const h3_packed_meta& m, const void*
   const int S = m.n_rows, D = c.dim, H = c.n_heads;
   const GemmPlan pl = gemm_plan(EPI_QKV, S, 3 * H * 128, H, 0);
   CUtensorMap tA, tB;
-  if (!make_tmap_2d(&tA, h, S, D, D, (uint32_t)pl.a_box) ||
-      !make_tmap_2d(&tB, w_qkv, (uint64_t)3 * H * 128, D, D, (uint32_t)pl.b_box))
+  if (!make_tmap_2d(&tA, h, S, D, D, 128) ||
+      !make_tmap_2d(&tB, w_qkv, (uint64_t)3 * H * 128, D, D, (uint32_t)pl.b_rows))
     return H3_ERR_CUDA;
   GemmArgs a{};
   gemm_common(a, S, D, pl.num_n);
@@ -293,7 +293,7 @@ h3_status run_qkv(const h3_block_config& c, const h3_packed_meta& m, const void*
   a.eps = c.eps;
   a.max_ctas = max_ctas;
   fill_omega(a.omega, c.rope_theta);
-  return cuda_st(launch_gemm(EPI_QKV, pl.bn, pl.mc, tA, tB, a, st));
+  return cuda_st(launch_gemm(EPI_QKV, pl.bn, tA, tB, a, st));
 }
 
 h3_status run_attention(int S, int H, const void* q, const void* k, const void* v, int64_t rs, int64_t hs,
@@ -324,11 +324,10 @@ h3_status run_resid_gemm(const h3_block_config& c, const h3_packed_meta& m, cons
     pl = GemmPlan{};
     pl.bn = 256;
     pl.num_n = gemm_num_n(EPI_RESID, 256, D, 0, 0);
-    pl.b_rows = pl.b_box = gemm_b_box_rows(EPI_RESID, 256);
-    pl.a_box = 128;
+    pl.b_rows = gemm_b_box_rows(EPI_RESID, 256);
   }
   CUtensorMap tA, tB;
-  if (!make_tmap_2d(&tA, act, S, K, K, (uint32_t)pl.a_box) || !make_tmap_2d(&tB, w, D, K, K, (uint32_t)pl.b_box))
+  if (!make_tmap_2d(&tA, act, S, K, K, 128) || !make_tmap_2d(&tB, w, D, K, K, (uint32_t)pl.b_rows))
     return H3_ERR_CUDA;
   GemmArgs a{};
   gemm_common(a, S, K, pl.num_n);
@@ -353,7 +352,7 @@ h3_status run_resid_gemm(const h3_block_config& c, const h3_packed_meta& m, cons
     a.sk_flags = sk->flags;
     a.sk_epoch = ++sk->epoch;
   }
-  return cuda_st(launch_gemm(EPI_RESID, pl.bn, pl.mc, tA, tB, a, st));
+  return cuda_st(launch_gemm(EPI_RESID, pl.bn, tA, tB, a, st));
 }
 
 h3_status run_ffn_up(const h3_block_config& c, int S, const void* h, const void* w1, const void* b1, void* out,
@@ -361,7 +360,7 @@ h3_status run_ffn_up(const h3_block_config& c, int S, const void* h, const void*
   const int D = c.dim, F = c.ffn_dim;
   const GemmPlan pl = gemm_plan(EPI_SWIGLU, S, 2 * F, 0, F);
   CUtensorMap tA, tB;
-  if (!make_tmap_2d(&tA, h, S, D, D, (uint32_t)pl.a_box) || !make_tmap_2d(&tB, w1, (uint64_t)2 * F, D, D, (uint32_t)pl.b_box))
+  if (!make_tmap_2d(&tA, h, S, D, D, 128) || !make_tmap_2d(&tB, w1, (uint64_t)2 * F, D, D, (uint32_t)pl.b_rows))
     return H3_ERR_CUDA;
   GemmArgs a{};
   gemm_common(a, S, D, pl.num_n);
@@ -370,7 +369,7 @@ h3_status run_ffn_up(const h3_block_config& c, int S, const void* h, const void*
   a.ldo = F;
   a.bias = static_cast<const __nv_bfloat16*>(b1);
   a.F = F;
-  return cuda_st(launch_gemm(EPI_SWIGLU, pl.bn, pl.mc, tA, tB, a, st));
+  return cuda_st(launch_gemm(EPI_SWIGLU, pl.bn, tA, tB, a, st));
 }
 
 h3_status check_block_weights(const h3_block_weights* w) {
@@ -396,13 +395,10 @@ int adaln_side_ctas(const h3_block_config& c, int S) {
   if (c.dim % 128) return 0;
   const int sms = num_sms(), H = c.n_heads, I = H * 128;
   const GemmPlan pl = gemm_plan(EPI_QKV, S, 3 * I, H, 0);
-  const int cl = pl.mc ? 4 : 2;
-  const int slots = pl.mc ? gemm_quad_slots() : gemm_pair_slots();
-  const long long units = pl.mc == 1 ? (long long)(gemm_m_tiles(S) / 2) * pl.num_n
-                        : pl.mc == 2 ? (long long)gemm_m_tiles(S) * (pl.num_n / 2)
-                                     : (long long)gemm_m_tiles(S) * pl.num_n;
-  const long long waves = (units + slots - 1) / slots;
-  const int need = cl * (int)((units + waves - 1) / waves);   // fewest CTAs (clusters x size) with the same wave count
+  const int slots = gemm_pair_slots();
+  const long long tiles = (long long)gemm_m_tiles(S) * pl.num_n;
+  const long long waves = (tiles + slots - 1) / slots;
+  const int need = 2 * (int)((tiles + waves - 1) / waves);   // fewest CTAs (pairs x 2) with the same wave count
   return sms - need >= 8 ? sms - need : 0;
 }
 
@@ -894,7 +890,7 @@ h3_status h3_linear(int32_t M, int32_t N, int32_t K, const void* x, const void* 
   if (!al16(x) || !al16(w) || !al16n(b) || !al16(y)) return H3_ERR_ALIGN;
   const GemmPlan pl = gemm_plan(EPI_PLAIN, M, N, 0, 0);
   CUtensorMap tA, tB;
-  if (!make_tmap_2d(&tA, x, M, K, K, (uint32_t)pl.a_box) || !make_tmap_2d(&tB, w, N, K, K, (uint32_t)pl.b_box))
+  if (!make_tmap_2d(&tA, x, M, K, K, 128) || !make_tmap_2d(&tB, w, N, K, K, (uint32_t)pl.b_rows))
     return H3_ERR_CUDA;
   GemmArgs a{};
   gemm_common(a, M, K, pl.num_n);
@@ -903,7 +899,7 @@ h3_status h3_linear(int32_t M, int32_t N, int32_t K, const void* x, const void* 
   a.ldo = N;
   a.bias = static_cast<const __nv_bfloat16*>(b);
   a.n_valid = N;
-  return cuda_st(launch_gemm(EPI_PLAIN, pl.bn, pl.mc, tA, tB, a, stream));
+  return cuda_st(launch_gemm(EPI_PLAIN, pl.bn, tA, tB, a, stream));
 }
 
 // ===========================================================================

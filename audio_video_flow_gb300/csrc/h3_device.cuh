@@ -300,17 +300,6 @@ __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* t
       "l"(reinterpret_cast<uint64_t>(tm)), "r"(bar_cluster), "r"(x), "r"(y)
       : "memory");
 }
-// The same load multicast to the CTAs of `cta_mask` (same shared offset in
-// each); each destination's bytes are counted on the mbarrier at bar_cluster's
-// offset in that destination's pair leader.
-__device__ __forceinline__ void tma_load_2d_pair_mc(void* dst, const CUtensorMap* tm, uint32_t bar_cluster,
-                                                    int32_t x, int32_t y, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster "
-      "[%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(tm)), "r"(bar_cluster), "r"(x), "r"(y), "h"(cta_mask)
-      : "memory");
-}
 // TMEM of a CTA pair: one warp of each CTA takes part in both calls.
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),

@@ -143,10 +143,6 @@ int gemm_sk_lane(int M, int N, int K, int bn);
 struct GemmPlan {
   int bn, num_n, b_rows;
   int nw1, ncnt1, nw2;
-  int mc;       // clusters of two pairs: 1 share the weight tile (two m-tiles),
-                // 2 share the activation tile (two column tiles), by multicast
-  int b_box;    // rows of the weight tensor map's box (b_rows, or half of it with mc 1)
-  int a_box;    // rows of the activation tensor map's box (128, or 64 with mc 2)
 };
 GemmPlan gemm_plan(int epi, int M, int N, int H, int F);
 // Tile width (256, 192 or 128 columns) for uniform tiles of a GEMM of M rows;
@@ -156,8 +152,7 @@ int gemm_num_n(int epi, int bn, int N, int H, int F);
 int gemm_b_box_rows(int epi, int bn);
 int gemm_m_tiles(int M);        // 256-row tiles (one per CTA pair)
 int gemm_pair_slots();          // CTA pairs that can be resident at once on this GPU
-int gemm_quad_slots();          // clusters of four CTAs (two pairs) resident at once
-cudaError_t launch_gemm(int epi, int bn, int mc, const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
+cudaError_t launch_gemm(int epi, int bn, const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
                         cudaStream_t stream);
 
 // AdaLN table: u = bf16(SiLU(t_cond)) into a [16][C] scratch (rows >= T zero),

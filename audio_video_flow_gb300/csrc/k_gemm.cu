@@ -40,7 +40,6 @@
 // resident N = 16 operand.  The kernel is bound by the weight stream from HBM.
 #include "h3_device.cuh"
 
-#include <string>
 #include "h3_internal.h"
 
 #include <cstdio>
@@ -559,16 +558,7 @@ __device__ __forceinline__ void run_epilogue(const GemmArgs& a, uint32_t tacc, i
 
 }  // namespace
 
-// MC = 1: clusters of four CTAs, two pairs on the two 256-row halves (m =
-// 2 mp, 2 mp + 1) of one column tile.  Each CTA loads one half of its weight
-// rows and multicasts it to the CTA with the same rank in the other pair, so
-// each SM fetches 16 KB of activations and BN/4 rows of weights per k-block.
-// A ring stage of a CTA is then written by both pairs: its release needs the
-// MMA commits of both pairs (empty barriers count 2, commits go to all four
-// CTAs).  Everything else (full barriers, accumulators, epilogue) stays per
-// pair.  Both pairs walk the same tiles and k-blocks, so their rings advance
-// together.
-template <int EPI, int BN, int MC>
+template <int EPI, int BN>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     gemm_bf16_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const GemmArgs args) {
@@ -589,22 +579,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 
   griddep_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t crank = cluster_ctarank();
-  const uint32_t rank = crank & 1u;                 // rank inside the CTA pair
-  const uint32_t pic = MC ? (crank >> 1) : 0u;      // pair inside the cluster
-  const uint32_t lead = crank & ~1u;                // cluster rank of this pair's even CTA
+  const uint32_t rank = cluster_ctarank();         // rank inside the CTA pair
   const bool leader = rank == 0;
-  constexpr int CL = MC ? 4 : 2;
+  constexpr int CL = 2;
   const int unit = (int)(blockIdx.x / CL), num_units = (int)(gridDim.x / CL);
-  // MC == 1: the cluster's two pairs take m-tiles 2u, 2u+1 of one column tile
-  // and share its weight tile; MC == 2: they take column tiles 2v, 2v+1 of one
-  // m-tile and share its activation tile.  Each pair loads half of the shared
-  // tile and multicasts it to the same rank of the other pair.
-  const int num_mu = MC == 1 ? (args.num_m + 1) / 2 : args.num_m;
-  const int num_nu = MC == 2 ? (args.num_n + 1) / 2 : args.num_n;
-  const int num_tiles = num_mu * num_nu;
-  const uint16_t all_mask = MC ? 0xF : 0x3;
-  const uint16_t pair_mask = (uint16_t)(0x3u << lead);
+  const int num_tiles = args.num_m * args.num_n;
+  const uint16_t pair_mask = 0x3;
   // tile `t` of this unit's walk -> (m_blk, n_blk) of this pair
   auto my_tile = [&](int t, int& m_blk, int& n_blk) {
     if (args.sk_units > 0) {
@@ -612,15 +592,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       n_blk = t - m_blk * args.num_n;
       return;
     }
-    int mu, nu;
-    tile_coords(t, num_mu, num_nu, mu, nu);
-    m_blk = MC == 1 ? 2 * mu + (int)pic : mu;
-    n_blk = MC == 2 ? 2 * nu + (int)pic : nu;
+    tile_coords(t, args.num_m, args.num_n, m_blk, n_blk);
   };
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], MC ? 2 : 1);
+      mbar_init(&empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&acc_full[i], 1);
@@ -639,7 +616,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     if (work_item(args, unit, num_units, num_tiles, 0, w0)) {
       int m0, n0;
       my_tile(w0.tile, m0, n0);
-      const int r0 = b_tile_row<EPI, BN>(args, n0, rank) + (MC == 1 ? (int)pic * (args.b_rows / 2) : 0);
+      const int r0 = b_tile_row<EPI, BN>(args, n0, rank);
       for (int kb = w0.k0; kb < w0.k0 + C::STAGES + args.l2_pf && kb < w0.k1; ++kb)
         tma_prefetch_l2(&tmB, kb * BK, r0);
     }
@@ -660,28 +637,20 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       int last_phase[STAGES];
       for (int s = 0; s < STAGES; ++s) last_phase[s] = -1;
       bool ok = true;
-      const uint32_t full0 = mapa_shared(smem_u32(full), lead);   // this pair's even CTA's full[0]
+      const uint32_t full0 = mapa_shared(smem_u32(full), 0);   // the even CTA's full[0]
       const uint32_t stage_tx = 2u * (uint32_t)(A_STAGE_BYTES + args.b_rows * BK * 2);   // both CTAs' boxes
-      const uint16_t mc_mask = (uint16_t)((1u << rank) | (1u << (rank + 2)));   // same rank in both pairs
       WorkItem w;
       for (int i = 0; ok && work_item(args, unit, num_units, num_tiles, i, w); ++i) {
         int m_blk, n_blk;
         my_tile(w.tile, m_blk, n_blk);
-        const int rb = b_tile_row<EPI, BN>(args, n_blk, rank) + (MC == 1 ? (int)pic * (args.b_rows / 2) : 0);
-        const int ra = m_blk * 2 * BM + (int)rank * BM + (MC == 2 ? (int)pic * (BM / 2) : 0);
+        const int rb = b_tile_row<EPI, BN>(args, n_blk, rank);
+        const int ra = m_blk * 2 * BM + (int)rank * BM;
         for (int kb = w.k0; kb < w.k1; ++kb) {
           if (!mbar_wait_cluster(&empty[stage], phase ^ 1u, abort_v)) { ok = false; break; }
           if (leader) mbar_arrive_expect_tx(&full[stage], stage_tx);
           const uint32_t fb = full0 + (uint32_t)stage * 8u;
-          if (MC == 2)
-            tma_load_2d_pair_mc(sA + stage * A_STAGE_BYTES + (int)pic * (BM / 2) * 128, &tmA, fb, kb * BK, ra, mc_mask);
-          else
-            tma_load_2d_pair(sA + stage * A_STAGE_BYTES, &tmA, fb, kb * BK, ra);
-          if (MC == 1)
-            tma_load_2d_pair_mc(sB + stage * C::B_STAGE_BYTES + (int)pic * (args.b_rows / 2) * 128, &tmB, fb, kb * BK, rb,
-                                mc_mask);
-          else
-            tma_load_2d_pair(sB + stage * C::B_STAGE_BYTES, &tmB, fb, kb * BK, rb);
+          tma_load_2d_pair(sA + stage * A_STAGE_BYTES, &tmA, fb, kb * BK, ra);
+          tma_load_2d_pair(sB + stage * C::B_STAGE_BYTES, &tmB, fb, kb * BK, rb);
           last_phase[stage] = (int)phase;
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
           const int pk = kb + args.l2_pf;
@@ -728,14 +697,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             mma_bf16_ss_pair(d_tmem, sdesc_kmajor(a0 + k * 32), sdesc_kmajor(b0 + k * 32), idesc,
                              (kb != w.k0 || k != 0) ? 1u : 0u);
           }
-          mma_commit_pair(&empty[stage], all_mask);
+          mma_commit_pair(&empty[stage], pair_mask);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
         mma_commit_pair(&acc_full[acc], pair_mask);
       }
       if (!ok) {  // all MMAs issued so far must finish before TMEM is released
-        mma_commit_pair(drain, (uint16_t)(1u << lead));
+        mma_commit_pair(drain, (uint16_t)1u);
         drain_wait(drain, 0);
       }
     }
@@ -745,7 +714,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     const int q = warp & 3;              // TMEM lane quadrant
     const int half = (warp - 2) >> 2;    // column half: warps 2-5 first, 6-9 second
     const int row = q * 32 + lane;
-    const uint32_t acc_empty0 = mapa_shared(smem_u32(acc_empty), lead);
+    const uint32_t acc_empty0 = mapa_shared(smem_u32(acc_empty), 0);
     int it = 0;
     WorkItem w;
     for (; work_item(args, unit, num_units, num_tiles, it, w); ++it) {
@@ -832,21 +801,13 @@ int gemm_choose_bn(int epi, int M, int N, int H, int F) {
   return best;
 }
 
-// Balanced column widths: every row of tiles gets `per_row` column tiles so
+// Balanced column widths: every 256-row tile gets `per_row` column tiles so
 // that all of them are resident at once, widths nw1 and nw1 - 16 (multiples
-// of 16).  mc as in GemmPlan.  Returns false when the uniform plan's wave
-// model is at least as good.
-static bool balance_columns(GemmPlan& p, int N, int num_m, int mc) {
-  const int slots = mc ? gemm_quad_slots() : gemm_pair_slots();
-  int per_row;
-  if (mc == 1) {
-    if (num_m % 2) return false;
-    per_row = slots / (num_m / 2);        // one row unit = two m-tiles
-  } else if (mc == 2) {
-    per_row = 2 * (slots / num_m);        // column tiles come in pairs
-  } else {
-    per_row = slots / num_m;
-  }
+// of 16).  Returns false when the uniform plan's wave model is at least as
+// good.
+static bool balance_columns(GemmPlan& p, int N, int num_m) {
+  const int slots = gemm_pair_slots();
+  const int per_row = slots / num_m;
   if (per_row < 1) return false;
   const int units = N / 16;
   const int u1 = (units + per_row - 1) / per_row;
@@ -855,10 +816,9 @@ static bool balance_columns(GemmPlan& p, int N, int num_m, int mc) {
   const int cnt1 = units - per_row * u2;       // cnt1 * u1 + (per_row - cnt1) * u2 == units
   const int cnt2 = per_row - cnt1;
   if (cnt1 < 1 || cnt1 > per_row) return false;
-  // wave model of the uniform (pair) plan against one wave of the balanced one
-  const int pair_slots = gemm_pair_slots();
+  // wave model of the uniform plan against one wave of the balanced one
   const long long u_tiles = (long long)num_m * p.num_n;
-  const long long u_waves = (u_tiles + pair_slots - 1) / pair_slots;
+  const long long u_waves = (u_tiles + slots - 1) / slots;
   const long long u_cost = u_waves * p.bn * 100 / (p.bn == 256 ? 100 : (p.bn == 192 ? 95 : 65));
   const long long b_cost = (long long)(16 * u1) * 100 / 95;
   if (b_cost >= u_cost) return false;
@@ -867,22 +827,7 @@ static bool balance_columns(GemmPlan& p, int N, int num_m, int mc) {
   p.nw2 = cnt2 > 0 ? 16 * u2 : 0;
   p.num_n = per_row;
   p.bn = p.nw1 <= 128 ? 128 : (p.nw1 <= 192 ? 192 : 256);
-  p.mc = mc;
-  // a weight half-box starts on a 1024-byte swizzle atom (8 weight rows), so
-  // with mc == 1 the CTA's box is rounded up to 16 rows; the extra rows go unused
-  p.b_rows = mc == 1 ? (p.nw1 / 2 + 15) / 16 * 16 : p.nw1 / 2;
-  p.b_box = mc == 1 ? p.b_rows / 2 : p.b_rows;
-  p.a_box = mc == 2 ? BM / 2 : BM;
-  return true;
-}
-
-// Uniform tiles with multicast: mc == 1 needs an even number of m-tiles,
-// mc == 2 an even number of column tiles.
-static bool uniform_mc(GemmPlan& p, int num_m, int mc) {
-  if (mc == 1 ? num_m % 2 != 0 : p.num_n % 2 != 0) return false;
-  p.mc = mc;
-  p.b_box = mc == 1 ? p.b_rows / 2 : p.b_rows;
-  p.a_box = mc == 2 ? BM / 2 : BM;
+  p.b_rows = p.nw1 / 2;
   return true;
 }
 
@@ -891,29 +836,9 @@ GemmPlan gemm_plan(int epi, int M, int N, int H, int F) {
   p.bn = gemm_choose_bn(epi, M, N, H, F);
   p.num_n = gemm_num_n(epi, p.bn, N, H, F);
   p.b_rows = gemm_b_box_rows(epi, p.bn);
-  p.b_box = p.b_rows;
-  p.a_box = BM;
-  const int num_m = gemm_m_tiles(M);
-  // Multicast (two pairs of a 4-CTA cluster sharing one operand tile) is a
-  // selectable mode, off by default: on GB300 only 36 such clusters fit (144
-  // of 152 SMs), and at 505-4096 rows it measured within a few percent of
-  // independent pairs either way, slower inside the block where the AdaLN
-  // side kernel fragments the SMs.  H3_GEMM_MC selects it: w / a weight /
-  // activation multicast on uniform tiles, bw / ba the same on balanced tiles.
-  const char* env = getenv("H3_GEMM_MC");
-  const std::string mode = env ? env : "";
-  const bool can_balance = (epi == EPI_PLAIN || epi == EPI_RESID) && !getenv("H3_GEMM_BN") && N % 16 == 0;
+  if ((epi != EPI_PLAIN && epi != EPI_RESID) || getenv("H3_GEMM_BN") || N % 16) return p;
   GemmPlan q = p;
-  if (mode == "w" || mode == "a") {
-    if (uniform_mc(q, num_m, mode == "w" ? 1 : 2)) return q;
-    return p;
-  }
-  if (mode == "bw" || mode == "ba") {
-    if (can_balance && balance_columns(q, N, num_m, mode == "bw" ? 1 : 2)) return q;
-    return p;
-  }
-  if (!can_balance) return p;
-  if (balance_columns(q, N, num_m, 0)) return q;
+  if (balance_columns(q, N, gemm_m_tiles(M))) return q;
   return p;
 }
 
@@ -957,53 +882,47 @@ int gemm_sk_lane(int M, int N, int K, int bn) {
   return lane;
 }
 
-// Clusters of `cl` CTAs (2: pairs, 4: multicast pairs) resident at once.
-static int cluster_slots(int cl) {
-  static int slots[64][2] = {{0}};
+// CTA pairs that can be resident at once.
+int gemm_pair_slots() {
+  static int slots[64] = {0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
-  const int k = cl == 4 ? 1 : 0;
-  if (!slots[dev][k]) {
+  if (!slots[dev]) {
     // every instance holds one CTA per SM; the largest shared-memory footprint bounds them all
     constexpr int smem = GemmCfg<192>::SMEM > GemmCfg<256>::SMEM ? GemmCfg<192>::SMEM : GemmCfg<256>::SMEM;
     int n = 0;
-    if (cudaFuncSetAttribute(gemm_bf16_tc<EPI_PLAIN, 192, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) ==
+    if (cudaFuncSetAttribute(gemm_bf16_tc<EPI_PLAIN, 192>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) ==
         cudaSuccess) {
       cudaLaunchConfig_t cfg = {};
-      cfg.gridDim = dim3(4 * 1024);
+      cfg.gridDim = dim3(2 * 1024);
       cfg.blockDim = dim3(GEMM_THREADS);
       cfg.dynamicSmemBytes = smem;
       cudaLaunchAttribute attr[1];
       attr[0].id = cudaLaunchAttributeClusterDimension;
-      attr[0].val.clusterDim.x = (unsigned)cl;
+      attr[0].val.clusterDim.x = 2;
       attr[0].val.clusterDim.y = 1;
       attr[0].val.clusterDim.z = 1;
       cfg.attrs = attr;
       cfg.numAttrs = 1;
-      if (cudaOccupancyMaxActiveClusters(&n, gemm_bf16_tc<EPI_PLAIN, 192, 0>, &cfg) != cudaSuccess) n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, gemm_bf16_tc<EPI_PLAIN, 192>, &cfg) != cudaSuccess) n = 0;
     }
     cudaGetLastError();
-    slots[dev][k] = n > 0 ? n : num_sms() / cl;
+    slots[dev] = n > 0 ? n : num_sms() / 2;
   }
-  return slots[dev][k];
+  return slots[dev];
 }
 
-int gemm_pair_slots() { return cluster_slots(2); }
-int gemm_quad_slots() { return cluster_slots(4); }
-
-template <int EPI, int BN, int MC>
+template <int EPI, int BN>
 static cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, int grid,
                               cudaStream_t stream) {
   constexpr int smem = GemmCfg<BN>::SMEM;
-  cudaError_t e =
-      cudaFuncSetAttribute(gemm_bf16_tc<EPI, BN, MC>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = cudaFuncSetAttribute(gemm_bf16_tc<EPI, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  return launch_kernel_cluster(gemm_bf16_tc<EPI, BN, MC>, dim3(grid), dim3(GEMM_THREADS), smem, stream,
-                               MC ? 4 : 2, tmA, tmB, a);
+  return launch_kernel_cluster(gemm_bf16_tc<EPI, BN>, dim3(grid), dim3(GEMM_THREADS), smem, stream, 2, tmA, tmB, a);
 }
 
-cudaError_t launch_gemm(int epi, int bn, int mc, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                        const GemmArgs& args, cudaStream_t stream) {
+cudaError_t launch_gemm(int epi, int bn, const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& args,
+                        cudaStream_t stream) {
   // Weight L2 prefetch distance in k-blocks.  Measured on GB300: with up to
   // 16 row tiles (4096 rows) the TMA ring alone is faster by 1-5 %; at
   // 15860 rows prefetching two rings ahead is faster by up to 7 %.
@@ -1014,27 +933,22 @@ cudaError_t launch_gemm(int epi, int bn, int mc, const CUtensorMap& tmA, const C
   const int pf_default = a.num_m <= 16 ? 0 : 2 * stages;
   a.l2_pf = pf ? atoi(pf) : pf_default;
   if (a.l2_pf < 0 || a.l2_pf > 256) a.l2_pf = pf_default;
-  const int cl = mc ? 4 : 2;
-  const int units = mc == 1 ? ((a.num_m + 1) / 2) * a.num_n
-                  : mc == 2 ? a.num_m * ((a.num_n + 1) / 2)
-                            : a.num_m * a.num_n;
-  const int slots = mc ? gemm_quad_slots() : gemm_pair_slots();
-  int n_cl = units < slots ? units : slots;
-  if (a.max_ctas > 0 && n_cl > a.max_ctas / cl) n_cl = a.max_ctas / cl > 0 ? a.max_ctas / cl : 1;
+  const int tiles = a.num_m * a.num_n;
+  const int slots = gemm_pair_slots();
+  int pairs = tiles < slots ? tiles : slots;
+  if (a.max_ctas > 0 && pairs > a.max_ctas / 2) pairs = a.max_ctas / 2 > 0 ? a.max_ctas / 2 : 1;
   if (a.sk_units > 0) {
     // every pair of a stream-K launch must be resident: an owner waits for
     // the partials of later pairs
-    if (mc || bn != 256 || a.sk_units > gemm_pair_slots()) return cudaErrorInvalidValue;
-    n_cl = a.sk_units;
+    if (bn != 256 || a.sk_units > slots) return cudaErrorInvalidValue;
+    pairs = a.sk_units;
   }
-  const int grid = cl * n_cl;
+  const int grid = 2 * pairs;
   const char* names[4] = {"plain", "qkv_qknorm_rope", "gated_residual", "swiglu"};
   cudaError_t e = cudaErrorInvalidValue;
-#define H3_GEMM_CASE(E, B)                                                                       \
-  case E * 1000 + B:                                                                             \
-    e = mc == 2   ? launch_one<E, B, 2>(tmA, tmB, a, grid, stream)                                 \
-        : mc == 1 ? launch_one<E, B, 1>(tmA, tmB, a, grid, stream)                                 \
-                  : launch_one<E, B, 0>(tmA, tmB, a, grid, stream);                                \
+#define H3_GEMM_CASE(E, B)                      \
+  case E * 1000 + B:                            \
+    e = launch_one<E, B>(tmA, tmB, a, grid, stream); \
     break;
   switch (epi * 1000 + bn) {
     H3_GEMM_CASE(EPI_PLAIN, 256)
@@ -1051,11 +965,9 @@ cudaError_t launch_gemm(int epi, int bn, int mc, const CUtensorMap& tmA, const C
 #undef H3_GEMM_CASE
   if (e != cudaSuccess) return e;
   set_kernel_info("gemm_bf16_tc<%s,%d> tcgen05.mma.cta_group::2.kind::f16 pair-tile=%dx%dx%d stages=%d acc=f32 "
-                  "tmem=2x%d grid=%d (%s=%d of %d) tiles=%dx%d k_blocks=%d l2_prefetch=%d stream-k=%d "
+                  "tmem=2x%d grid=%d (pairs=%d of %d) tiles=%dx%d k_blocks=%d l2_prefetch=%d stream-k=%d "
                   "n-widths=%s%d,%d,%d",
-                  names[epi], bn, 2 * BM, bn, BK, stages, bn, grid,
-                  mc == 1 ? "weight-multicast quads" : (mc == 2 ? "activation-multicast quads" : "pairs"), n_cl,
-                  slots, a.num_m, a.num_n, a.num_k, a.l2_pf, a.sk_units, a.nw1 ? "balanced:" : "uniform:",
+                  names[epi], bn, 2 * BM, bn, BK, stages, bn, grid, pairs, slots, a.num_m, a.num_n, a.num_k, a.l2_pf, a.sk_units, a.nw1 ? "balanced:" : "uniform:",
                   a.nw1 ? a.nw1 : bn, a.ncnt1, a.nw2);
   return cudaGetLastError();
 }

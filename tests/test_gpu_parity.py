@@ -108,7 +108,6 @@ def test_linear_balanced_column_tiles(h3, M, N, K):
     torch.cuda.synchronize()
     info = h3.h3_last_kernel_info()
     assert "balanced:" in info, info
-    assert "multicast" not in info, info
     assert_close(to_np(y), O.linear(to_np(x), to_np(w), to_np(b)), f"linear {M}x{N}x{K}")
 
 
@@ -232,68 +231,6 @@ def test_ffn_down_residual(h3, name, gemm_bn):
                             to_bf16(c.ref["x1"]), y)
     assert h3.h3_sync_check() == 0
     assert_close(to_np(y), c.ref["y"], f"ffn_down_residual[{name}]")
-
-
-@pytest.mark.parametrize("M,N,K", [(505, 2560, 192), (1024, 2928, 320)])
-@pytest.mark.parametrize("mode", ["w", "a", "bw", "ba"])
-def test_linear_multicast_modes(h3, M, N, K, mode, monkeypatch):
-    """h3_linear in each multicast mode.  N = 2560 at 505 rows gives balanced
-    80-column tiles: with weight multicast their 40-row half-boxes are rounded
-    up to 48 rows so that both halves start on a swizzle atom."""
-    monkeypatch.delenv("H3_GEMM_BN", raising=False)
-    monkeypatch.setenv("H3_GEMM_MC", mode)
-    g = torch.Generator().manual_seed(7)
-    x = torch.randn(M, K, generator=g).to(torch.bfloat16)
-    w = (torch.randn(N, K, generator=g) * 0.05).to(torch.bfloat16)
-    b = (torch.randn(N, generator=g) * 0.1).to(torch.bfloat16)
-    y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
-    h3.h3_linear(M, N, K, x.cuda(), w.cuda(), b.cuda(), y)
-    torch.cuda.synchronize()
-    assert "multicast" in h3.h3_last_kernel_info(), h3.h3_last_kernel_info()
-    assert_close(to_np(y), O.linear(to_np(x), to_np(w), to_np(b)), f"linear {M}x{N}x{K} mc={mode}")
-
-
-@pytest.mark.parametrize("mode", ["w", "a", "bw", "ba"])
-def test_gemm_multicast_modes(h3, mode, monkeypatch):
-    """Clusters of two CTA pairs that share one operand tile by TMA multicast:
-    the weight tile across two 256-row tiles (w) or the activation tile across
-    two column tiles (a), on uniform or balanced (b*) column tiles.  Every GEMM
-    of the block at 505 rows (two row tiles) in each mode against the oracle."""
-    monkeypatch.delenv("H3_GEMM_BN", raising=False)
-    monkeypatch.setenv("H3_GEMM_MC", mode)
-    c = get_case("block505")
-    H, D, F = c.w.shape.n_heads, c.w.shape.dim, c.w.shape.ffn_dim
-    kind = "weight-multicast" if mode.endswith("w") else "activation-multicast"
-    uniform = not mode.startswith("b")
-
-    out = torch.zeros(c.S, H, 3, 128, dtype=torch.bfloat16, device="cuda")
-    h3.h3_qkv_projection(c.cfg(h3), c.meta(h3), to_bf16(c.ref["h1"]), c.d_w["w_qkv"], None,
-                         c.d_w["q_norm_g"], c.d_w["k_norm_g"], out)
-    assert h3.h3_sync_check() == 0
-    assert (kind in h3.h3_last_kernel_info()) == uniform, h3.h3_last_kernel_info()
-    o = to_np(out)
-    for i, key in enumerate(("q", "k", "v")):
-        assert_close(o[:, :, i], c.ref[key], f"qkv.{key}[{mode}]")
-
-    x1 = torch.empty(c.S, D, dtype=torch.bfloat16, device="cuda")
-    h3.h3_out_projection(c.cfg(h3), c.meta(h3), table_tensor(c), to_bf16(c.ref["o"]), c.d_w["w_o"], None,
-                         c.d_x, x1)
-    assert h3.h3_sync_check() == 0
-    assert kind in h3.h3_last_kernel_info(), h3.h3_last_kernel_info()
-    assert_close(to_np(x1), c.ref["x1"], f"out_projection[{mode}]")
-
-    a = torch.empty(c.S, F, dtype=torch.bfloat16, device="cuda")
-    h3.h3_ffn_up_swiglu(c.cfg(h3), c.S, to_bf16(c.ref["h2"]), c.d_w["w_fc1"], None, a)
-    assert h3.h3_sync_check() == 0
-    assert (kind in h3.h3_last_kernel_info()) == uniform, h3.h3_last_kernel_info()
-    assert_close(to_np(a), c.ref["a"], f"ffn_up_swiglu[{mode}]")
-
-    y = torch.empty(c.S, D, dtype=torch.bfloat16, device="cuda")
-    h3.h3_ffn_down_residual(c.cfg(h3), c.meta(h3), table_tensor(c), to_bf16(c.ref["a"]), c.d_w["w_fc2"], None,
-                            to_bf16(c.ref["x1"]), y)
-    assert h3.h3_sync_check() == 0
-    assert kind in h3.h3_last_kernel_info(), h3.h3_last_kernel_info()
-    assert_close(to_np(y), c.ref["y"], f"ffn_down_residual[{mode}]")
 
 
 # ---------------------------------------------------------------------------
