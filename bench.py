@@ -45,8 +45,8 @@ STAGES = ("adaln_table", "norm1_modulate", "qkv_qknorm_rope", "attention", "out_
 # hit L2), so the 32,768- and 15,860-row values are the 16,384-row capture
 # scaled by the row count.
 TRAFFIC = {
-    "qkv_qknorm_rope@block505": 249717248,
-    "fc1_swiglu@block505": 332196096,
+    "qkv_qknorm_rope@block505": 249930496,
+    "fc1_swiglu@block505": 331703808,
     "qkv_qknorm_rope@block1824": 337300736,
     "fc1_swiglu@block1824": 386801920,
     "attention@attn4096": 214684160,
