@@ -19,10 +19,10 @@
 // own TMEM.  Per SM this moves 32 KB of operands per 64-deep k-block instead
 // of the 48 KB a 128 x 256 tile on one SM needs, and leaves room for a deeper
 // ring (6-8 stages).  Warp 0 of each CTA issues its TMA loads (completion
-// counted on the even CTA's barrier) and L2 prefetches further ahead; warp 1
-// of the even CTA issues the MMAs into one of two TMEM accumulators
-// (2 x BN columns) and releases ring stages to both CTAs with a multicast
-// commit; warps 2-9 of each CTA drain the other accumulator through
+// counted on the even CTA's barrier) and, above 16 row tiles, L2 prefetches
+// of the weights further ahead; warp 1 of the even CTA issues the MMAs into
+// one of two TMEM accumulators (2 x BN columns) and releases ring stages to
+// both CTAs with a multicast tcgen05.commit; warps 2-9 of each CTA drain the other accumulator through
 // tcgen05.ld and run the epilogue, two warps per TMEM lane quadrant (warp w
 // reads lanes 32 (w % 4) ..), warps 2-5 on the first and 6-9 on the second
 // half of the tile's columns.  BN (256, 192 or 128) is chosen per launch to
@@ -967,7 +967,8 @@ cudaError_t launch_gemm(int epi, int bn, const CUtensorMap& tmA, const CUtensorM
   set_kernel_info("gemm_bf16_tc<%s,%d> tcgen05.mma.cta_group::2.kind::f16 pair-tile=%dx%dx%d stages=%d acc=f32 "
                   "tmem=2x%d grid=%d (pairs=%d of %d) tiles=%dx%d k_blocks=%d l2_prefetch=%d stream-k=%d "
                   "n-widths=%s%d,%d,%d",
-                  names[epi], bn, 2 * BM, bn, BK, stages, bn, grid, pairs, slots, a.num_m, a.num_n, a.num_k, a.l2_pf, a.sk_units, a.nw1 ? "balanced:" : "uniform:",
+                  names[epi], bn, 2 * BM, bn, BK, stages, bn, grid, pairs, slots, a.num_m, a.num_n, a.num_k,
+                  a.l2_pf, a.sk_units, a.nw1 ? "balanced:" : "uniform:",
                   a.nw1 ? a.nw1 : bn, a.ncnt1, a.nw2);
   return cudaGetLastError();
 }
