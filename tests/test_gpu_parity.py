@@ -521,3 +521,44 @@ def test_attention_4096_sampled_rows(h3, attn4096, attn_qtiles):
         q, k = d["q"][rows[:16], h], d["k"][:, h]
         p_gpu = np.exp(q @ k.T / np.sqrt(128.0) - lse_np[h, rows[:16]][:, None])
         assert np.abs(p_gpu - O.attention_probs(q, k)).max() <= 1e-3
+
+
+# ---------------------------------------------------------------------------
+# attention core at 16,384 and 32,768 packed rows: the QK-norm + RoPE prologue
+# and attention exactly as the benchmark launches them, checked on every row
+# of the prologue and on sampled query rows of attention
+# ---------------------------------------------------------------------------
+
+@pytest.mark.slow
+@pytest.mark.parametrize("wl", ["attn16384", "attn32768"])
+def test_attention_core_full_size_sampled_rows(h3, wl):
+    w = hi.WORKLOADS[wl]
+    S, H = w.layout.n_rows, w.shape.n_heads
+    meta = hi.packed_metadata(w.layout, 1, 0)
+    ins = hi.attention_inputs(w.shape, S, 0)
+    q, k, v = O.qk_norm_rope(to_np(ins["qkv"]), meta["pos_thw"].numpy(), to_np(ins["q_norm_g"]),
+                             to_np(ins["k_norm_g"]))
+    cfg = h3.make_config(w.shape.dim, H, w.shape.ffn_dim, w.shape.cond_dim)
+    buf = ins["qkv"].cuda()
+    h3.h3_rope_qknorm(cfg, S, meta["pos_thw"].cuda(), buf[:, :, 0], buf[:, :, 1], H * 384, 384,
+                      ins["q_norm_g"].cuda(), ins["k_norm_g"].cuda())
+    o = torch.empty(S, H * 128, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(H, S, dtype=torch.float32, device="cuda")
+    h3.h3_attention(S, H, buf[:, :, 0], buf[:, :, 1], buf[:, :, 2], H * 384, 384, o, lse)
+    assert h3.h3_sync_check(timeout_ms=60000) == 0
+    got = to_np(buf)
+    assert_close(got[:, :, 0], q, f"{wl} rope.q")
+    assert_close(got[:, :, 1], k, f"{wl} rope.k")
+    # attention from the GPU's own q, k, v (bf16 after the prologue): the
+    # oracle's rounding of the prologue differs by at most an ulp in a few
+    # elements, which the prologue check above bounds
+    qg, kg, vg = got[:, :, 0], got[:, :, 1], got[:, :, 2]
+    rows = np.unique(np.concatenate([[0, 1, w.layout.n_text, S - w.layout.n_audio, S - 1],
+                                     np.random.default_rng(12).integers(0, S, 27)]))
+    ref = O.attention(qg, kg, vg, rows)
+    assert_close(to_np(o)[rows], ref, f"{wl} attention (sampled rows)")
+    lse_np = lse.cpu().numpy().astype(np.float64)
+    for h in range(0, H, 11):
+        qh, kh = qg[rows[:8], h], kg[:, h]
+        p_gpu = np.exp(qh @ kh.T / np.sqrt(128.0) - lse_np[h, rows[:8]][:, None])
+        assert np.abs(p_gpu - O.attention_probs(qh, kh)).max() <= 1e-3
