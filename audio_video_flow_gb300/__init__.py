@@ -67,6 +67,9 @@ def lib() -> ctypes.CDLL:
             "h3_block_workspace_bytes": (sz, [cfgp, i32, i32]),
             "h3_block_adaln_side_ctas": (i32, [cfgp, i32]),
             "h3_block_forward": (i32, [cfgp, wp, mp, vp, vp, vp, sz, vp]),
+            "h3_block_host_workspace_bytes": (sz, [cfgp, i32, i32]),
+            "h3_block_forward_host": (i32, [cfgp, wp, mp, vp, vp, vp, sz, vp]),
+            "h3_blocks_forward_host": (i32, [cfgp, i32, wp, mp, vp, vp, vp, sz, vp]),
             "h3_block_forward_profiled": (i32, [cfgp, wp, mp, vp, vp, vp, sz, vp, vp, i32]),
             "h3_blocks_forward": (i32, [cfgp, i32, wp, mp, vp, vp, vp, sz, vp]),
             "h3_adaln_table_workspace_bytes": (sz, [cfgp]),
@@ -161,7 +164,8 @@ def make_weights(w: Dict[str, object]) -> BlockWeights:
 
 
 def make_meta(token_tag, timestep_index, pos_thw, t_cond=None, n_timesteps: int = 0) -> PackedMeta:
-    """Struct of device pointers; it keeps the tensors alive while it lives."""
+    """Struct of the tensors' pointers (device ones, or host ones for
+    h3_block_forward_host); it keeps the tensors alive while it lives."""
     s = PackedMeta(int(token_tag.shape[0]), int(n_timesteps), _ptr(token_tag), _ptr(timestep_index),
                    _ptr(pos_thw), _ptr(t_cond))
     s._tensors = (token_tag, timestep_index, pos_thw, t_cond)
@@ -184,6 +188,27 @@ def h3_block_forward(cfg, weights, meta, x_in, x_out, workspace, stream=None) ->
     _check(lib().h3_block_forward(ctypes.byref(cfg), ctypes.byref(weights), ctypes.byref(meta), _ptr(x_in),
                                   _ptr(x_out), _ptr(workspace), workspace.numel() * workspace.element_size(),
                                   _stream(stream)), "h3_block_forward")
+
+
+def h3_block_host_workspace_bytes(cfg: BlockConfig, n_rows: int, n_timesteps: int) -> int:
+    return int(lib().h3_block_host_workspace_bytes(ctypes.byref(cfg), n_rows, n_timesteps))
+
+
+def h3_block_forward_host(cfg, weights, meta_host, x_host, y_host, workspace, stream=None) -> None:
+    """meta_host: make_meta() of host (preferably pinned) tensors; x_host,
+    y_host: host bf16 [S][D]; weights and workspace on the device."""
+    _check(lib().h3_block_forward_host(ctypes.byref(cfg), ctypes.byref(weights), ctypes.byref(meta_host),
+                                       _ptr(x_host), _ptr(y_host), _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(), _stream(stream)),
+           "h3_block_forward_host")
+
+
+def h3_blocks_forward_host(cfg, weights_list, meta_host, x_host, y_host, workspace, stream=None) -> None:
+    arr = (BlockWeights * len(weights_list))(*weights_list)
+    _check(lib().h3_blocks_forward_host(ctypes.byref(cfg), len(weights_list), arr, ctypes.byref(meta_host),
+                                        _ptr(x_host), _ptr(y_host), _ptr(workspace),
+                                        workspace.numel() * workspace.element_size(), _stream(stream)),
+           "h3_blocks_forward_host")
 
 
 def h3_block_forward_profiled(cfg, weights, meta, x_in, x_out, workspace, events, stream=None) -> None:

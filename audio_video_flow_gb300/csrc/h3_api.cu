@@ -566,6 +566,89 @@ h3_status h3_block_forward(const h3_block_config* cfg, const h3_block_weights* w
   return block_impl(cfg, w, meta, x_in, x_out, workspace, ws_bytes, stream, nullptr, 0);
 }
 
+// Staging for h3_block_forward_host, after the block workspace: x, y, the
+// three metadata arrays and t_cond.
+struct HostStaging {
+  size_t x, y, tag, tidx, pos, tcond, total;
+};
+HostStaging host_staging(const h3_block_config& c, int64_t S, int64_t T) {
+  HostStaging H{};
+  size_t off = ws_layout(c, S, T).total;
+  H.x = off;
+  off = al256(off + (size_t)S * c.dim * 2);
+  H.y = off;
+  off = al256(off + (size_t)S * c.dim * 2);
+  H.tag = off;
+  off = al256(off + (size_t)S * 4);
+  H.tidx = off;
+  off = al256(off + (size_t)S * 4);
+  H.pos = off;
+  off = al256(off + (size_t)S * 12);
+  H.tcond = off;
+  off = al256(off + (size_t)T * c.cond_dim * 4);
+  H.total = off;
+  return H;
+}
+
+size_t h3_block_host_workspace_bytes(const h3_block_config* cfg, int32_t n_rows, int32_t n_timesteps) {
+  if (check_cfg(cfg) != H3_OK || n_rows < 1 || n_timesteps < 1 || n_timesteps > 16) return 0;
+  return host_staging(*cfg, n_rows, n_timesteps).total;
+}
+
+// The blocks w[0 .. n_blocks) from and to host memory through the staging.
+static h3_status host_forward(const h3_block_config* cfg, int32_t n_blocks, const h3_block_weights* w,
+                              const h3_packed_meta* meta_host, const void* x_host, void* y_host, void* workspace,
+                              size_t ws_bytes, cudaStream_t stream) {
+  h3_status s = check_cfg(cfg);
+  if (s != H3_OK) return s;
+  if (!w) return H3_ERR_NULL;
+  if (n_blocks < 1) return H3_ERR_SHAPE;
+  if ((s = check_meta(meta_host, true)) != H3_OK) return s;
+  for (int b = 0; b < n_blocks; ++b)
+    if ((s = check_block_weights(&w[b])) != H3_OK) return s;
+  if (!x_host || !y_host || !workspace) return H3_ERR_NULL;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return H3_ERR_ALIGN;
+  const int S = meta_host->n_rows, T = meta_host->n_timesteps;
+  const HostStaging H = host_staging(*cfg, S, T);
+  if (ws_bytes < H.total) return H3_ERR_WORKSPACE;
+  uint8_t* base = static_cast<uint8_t*>(workspace);
+  const size_t xb = (size_t)S * cfg->dim * 2;
+  // one stream-ordered copy per host buffer
+  const struct {
+    size_t off;
+    const void* src;
+    size_t bytes;
+  } in[5] = {{H.x, x_host, xb},
+             {H.tag, meta_host->token_tag, (size_t)S * 4},
+             {H.tidx, meta_host->timestep_index, (size_t)S * 4},
+             {H.pos, meta_host->pos_thw, (size_t)S * 12},
+             {H.tcond, meta_host->t_cond, (size_t)T * cfg->cond_dim * 4}};
+  for (const auto& c : in)
+    if (cudaMemcpyAsync(base + c.off, c.src, c.bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+      return H3_ERR_CUDA;
+  const h3_packed_meta m{S, T, reinterpret_cast<const int32_t*>(base + H.tag),
+                         reinterpret_cast<const int32_t*>(base + H.tidx), reinterpret_cast<const int32_t*>(base + H.pos),
+                         reinterpret_cast<const float*>(base + H.tcond)};
+  for (int b = 0; b < n_blocks; ++b)
+    if ((s = block_impl(cfg, &w[b], &m, base + (b == 0 ? H.x : H.y), base + H.y, workspace, ws_bytes, stream,
+                        nullptr, 0)) != H3_OK)
+      return s;
+  return cudaMemcpyAsync(y_host, base + H.y, xb, cudaMemcpyDeviceToHost, stream) == cudaSuccess ? H3_OK
+                                                                                                : H3_ERR_CUDA;
+}
+
+h3_status h3_block_forward_host(const h3_block_config* cfg, const h3_block_weights* w,
+                                const h3_packed_meta* meta_host, const void* x_host, void* y_host, void* workspace,
+                                size_t ws_bytes, cudaStream_t stream) {
+  return host_forward(cfg, 1, w, meta_host, x_host, y_host, workspace, ws_bytes, stream);
+}
+
+h3_status h3_blocks_forward_host(const h3_block_config* cfg, int32_t n_blocks, const h3_block_weights* w,
+                                 const h3_packed_meta* meta_host, const void* x_host, void* y_host,
+                                 void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  return host_forward(cfg, n_blocks, w, meta_host, x_host, y_host, workspace, ws_bytes, stream);
+}
+
 h3_status h3_block_forward_profiled(const h3_block_config* cfg, const h3_block_weights* w,
                                     const h3_packed_meta* meta, const void* x_in, void* x_out, void* workspace,
                                     size_t ws_bytes, cudaStream_t stream, void* const* events,

@@ -675,24 +675,23 @@ def run_ours(args, ws_n: int, rank: int, local: int):
     tflops = units / (elapsed_ms * 1e-3) / 1e12
     tokens_per_s = ws_n * S * args.steps / (elapsed_ms * 1e-3)
 
-    # ---- end to end: pinned host inputs -> device, block(s), output -> host
+    # ---- end to end through the host-buffer entry point: pinned host input
+    # and metadata copied in, the block(s), the output copied back, all inside
+    # one h3_blocks_forward_host call per step
     e2e = None
     if not args.no_e2e:
         h_x = acts_c["x"].pin_memory()
         h_meta = {k: v.pin_memory() for k, v in meta_c.items()}
         h_tc = acts_c["t_cond"].pin_memory()
         h_y = torch.empty_like(acts_c["x"]).pin_memory()
+        meta_h = h3.make_meta(h_meta["token_tag"], h_meta["timestep_index"], h_meta["pos_thw"], h_tc, T)
+        ws_h = torch.empty(h3.h3_block_host_workspace_bytes(cfg, S, T), dtype=torch.uint8, device=dev)
         bi = h_x.numel() * 2 + h_tc.numel() * 4 + sum(v.numel() * 4 for v in h_meta.values())
         bo = h_y.numel() * 2
         n_e2e = max(3, min(args.steps, 200))
 
         def e2e_step():
-            x.copy_(h_x, non_blocking=True)
-            tc.copy_(h_tc, non_blocking=True)
-            for k in h_meta:
-                meta_d[k].copy_(h_meta[k], non_blocking=True)
-            step()
-            h_y.copy_(y, non_blocking=True)
+            h3.h3_blocks_forward_host(cfg, cw, meta_h, h_x, h_y, ws_h)
 
         for _ in range(3):
             e2e_step()

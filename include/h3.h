@@ -145,6 +145,28 @@ h3_status h3_block_forward(const h3_block_config *cfg, const h3_block_weights *w
                            const h3_packed_meta *meta, const void *x_in, void *x_out,
                            void *workspace, size_t ws_bytes, cudaStream_t stream);
 
+/* h3_block_forward from and to host memory, for callers whose activations
+ * live on the host: copies x_host (bf16 [S][D]) and the packed metadata that
+ * meta_host points to (token_tag, timestep_index, pos_thw, t_cond: host
+ * arrays of the sizes h3_packed_meta states) into staging space at the end
+ * of the workspace with one cudaMemcpyAsync each, runs the block there, and
+ * copies the result to y_host (bf16 [S][D]); x_host and y_host may be the
+ * same buffer.  Everything is ordered on `stream` and the call returns before
+ * the copies complete: synchronize the stream before reading y_host or
+ * reusing the inputs.  Host buffers should be page-locked (cudaHostAlloc or
+ * pinned), otherwise the copies are synchronous.  The weights stay device
+ * pointers.  Workspace: device, 256-byte aligned, at least
+ * h3_block_host_workspace_bytes (the block workspace plus the staging). */
+size_t h3_block_host_workspace_bytes(const h3_block_config *cfg, int32_t n_rows, int32_t n_timesteps);
+h3_status h3_block_forward_host(const h3_block_config *cfg, const h3_block_weights *w,
+                                const h3_packed_meta *meta_host, const void *x_host, void *y_host,
+                                void *workspace, size_t ws_bytes, cudaStream_t stream);
+/* The same for the chain w[0 .. n_blocks) of h3_blocks_forward: one copy in,
+ * the blocks in order on the device, one copy out. */
+h3_status h3_blocks_forward_host(const h3_block_config *cfg, int32_t n_blocks, const h3_block_weights *w,
+                                 const h3_packed_meta *meta_host, const void *x_host, void *y_host,
+                                 void *workspace, size_t ws_bytes, cudaStream_t stream);
+
 /* As h3_block_forward, recording cudaEvent_t events[k] on the stream after
  * launch stage k, for k = 0..min(n_events, 8)-1, stages in order: 0 AdaLN
  * table (the chunks on the caller's stream), 1 norm1/modulate, 2 QKV +

@@ -288,6 +288,32 @@ def test_block_forward_stream_k(h3, name, units, monkeypatch):
     assert torch.equal(y, run_block(h3, c))
 
 
+def test_block_forward_host_matches_device(h3):
+    """h3_block_forward_host (pinned host input, metadata and output, copies
+    ordered on the stream inside the call) gives the device call's output bit
+    for bit, also in place on the host buffer."""
+    c = get_case("ragged205")
+    y_dev = run_block(h3, c)
+    cfg = c.cfg(h3)
+    ws = torch.empty(h3.h3_block_host_workspace_bytes(cfg, c.S, c.T), dtype=torch.uint8, device="cuda")
+    assert ws.numel() > h3.h3_block_workspace_bytes(cfg, c.S, c.T)
+    md = {k: v.cpu().pin_memory() for k, v in c.d_meta.items()}
+    tc = c.d_tc.cpu().pin_memory()
+    meta_h = h3.make_meta(md["token_tag"], md["timestep_index"], md["pos_thw"], tc, c.T)
+    x_h = c.d_x.cpu().pin_memory()
+    y_h = torch.empty_like(x_h).pin_memory()
+    h3.h3_block_forward_host(cfg, h3.make_weights(c.d_w), meta_h, x_h, y_h, ws)
+    torch.cuda.synchronize()
+    assert h3.h3_sync_check() == 0
+    assert torch.equal(y_h, y_dev.cpu())
+    h3.h3_block_forward_host(cfg, h3.make_weights(c.d_w), meta_h, x_h, x_h, ws)   # in place
+    torch.cuda.synchronize()
+    assert torch.equal(x_h, y_dev.cpu())
+    small = torch.empty(h3.h3_block_workspace_bytes(cfg, c.S, c.T), dtype=torch.uint8, device="cuda")
+    with pytest.raises(h3.H3Error):
+        h3.h3_block_forward_host(cfg, h3.make_weights(c.d_w), meta_h, x_h, y_h, small)
+
+
 def test_block_repeatable_and_inplace(h3):
     """Control H-C0 (repeated call: bitwise equal), a fresh workspace, and
     x_out aliasing x_in."""
