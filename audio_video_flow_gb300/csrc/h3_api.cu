@@ -415,9 +415,24 @@ cudaStream_t side_stream() {
   return streams[dev];
 }
 
+// x_ready: when not null, an event the caller's stream waits for before the
+// first kernel that reads x_in (norm1); the AdaLN table does not read it.
+// A library-owned stream per device for the host-to-device copy of a block
+// input that overlaps the AdaLN table (joined by an event before norm1).
+cudaStream_t copy_stream() {
+  static cudaStream_t streams[kMaxDevicesApi] = {nullptr};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevicesApi) return nullptr;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!streams[dev] && cudaStreamCreateWithFlags(&streams[dev], cudaStreamNonBlocking) != cudaSuccess)
+    streams[dev] = nullptr;
+  return streams[dev];
+}
+
 h3_status block_impl(const h3_block_config* cfg, const h3_block_weights* w, const h3_packed_meta* meta,
                      const void* x_in, void* x_out, void* ws, size_t ws_bytes, cudaStream_t st,
-                     void* const* events, int n_events) {
+                     void* const* events, int n_events, cudaEvent_t x_ready = nullptr) {
   const int S = meta->n_rows, T = meta->n_timesteps;
   const WsLayout L = ws_layout(*cfg, S, T);
   uint8_t* base = static_cast<uint8_t*>(ws);
@@ -483,6 +498,7 @@ h3_status block_impl(const h3_block_config* cfg, const h3_block_weights* w, cons
     if ((s = run_adaln_chunks(*cfg, w->w_ada, w->b_ada, T, table, u, 0, 6, 0, st)) != H3_OK) return s;
   }
   if ((s = mark()) != H3_OK) return s;
+  if (x_ready && cudaStreamWaitEvent(st, x_ready, 0) != cudaSuccess) return H3_ERR_CUDA;
   H3_TRY(run_modulate(*cfg, *meta, table, 0, x_in, w->norm1_g, h, st));
   H3_TRY(run_qkv(*cfg, *meta, h, w->w_qkv, w->b_qkv, w->q_norm_g, w->k_norm_g, qkv, st, qkv_ctas));
   {
@@ -613,16 +629,36 @@ static h3_status host_forward(const h3_block_config* cfg, int32_t n_blocks, cons
   if (ws_bytes < H.total) return H3_ERR_WORKSPACE;
   uint8_t* base = static_cast<uint8_t*>(workspace);
   const size_t xb = (size_t)S * cfg->dim * 2;
-  // one stream-ordered copy per host buffer
+  // One copy per host buffer.  The metadata go first on the caller's
+  // stream; x goes on the library's copy stream, which starts after the
+  // caller's earlier work (that may still use the staging) and which norm1
+  // waits for, so that the copy overlaps the AdaLN table.
   const struct {
     size_t off;
     const void* src;
     size_t bytes;
-  } in[5] = {{H.x, x_host, xb},
-             {H.tag, meta_host->token_tag, (size_t)S * 4},
+  } in[4] = {{H.tag, meta_host->token_tag, (size_t)S * 4},
              {H.tidx, meta_host->timestep_index, (size_t)S * 4},
              {H.pos, meta_host->pos_thw, (size_t)S * 12},
              {H.tcond, meta_host->t_cond, (size_t)T * cfg->cond_dim * 4}};
+  struct EventGuard {
+    cudaEvent_t ev[2] = {nullptr, nullptr};
+    ~EventGuard() {
+      for (cudaEvent_t e : ev)
+        if (e) cudaEventDestroy(e);
+    }
+  } guard;
+  cudaStream_t cs = copy_stream();
+  if (cs) {
+    for (cudaEvent_t& e : guard.ev)
+      if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return H3_ERR_CUDA;
+    if (cudaEventRecord(guard.ev[0], stream) != cudaSuccess || cudaStreamWaitEvent(cs, guard.ev[0], 0) != cudaSuccess ||
+        cudaMemcpyAsync(base + H.x, x_host, xb, cudaMemcpyHostToDevice, cs) != cudaSuccess ||
+        cudaEventRecord(guard.ev[1], cs) != cudaSuccess)
+      return H3_ERR_CUDA;
+  } else if (cudaMemcpyAsync(base + H.x, x_host, xb, cudaMemcpyHostToDevice, stream) != cudaSuccess) {
+    return H3_ERR_CUDA;
+  }
   for (const auto& c : in)
     if (cudaMemcpyAsync(base + c.off, c.src, c.bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess)
       return H3_ERR_CUDA;
@@ -631,7 +667,7 @@ static h3_status host_forward(const h3_block_config* cfg, int32_t n_blocks, cons
                          reinterpret_cast<const float*>(base + H.tcond)};
   for (int b = 0; b < n_blocks; ++b)
     if ((s = block_impl(cfg, &w[b], &m, base + (b == 0 ? H.x : H.y), base + H.y, workspace, ws_bytes, stream,
-                        nullptr, 0)) != H3_OK)
+                        nullptr, 0, b == 0 ? guard.ev[1] : nullptr)) != H3_OK)
       return s;
   return cudaMemcpyAsync(y_host, base + H.y, xb, cudaMemcpyDeviceToHost, stream) == cudaSuccess ? H3_OK
                                                                                                 : H3_ERR_CUDA;

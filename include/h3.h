@@ -151,7 +151,9 @@ h3_status h3_block_forward(const h3_block_config *cfg, const h3_block_weights *w
  * arrays of the sizes h3_packed_meta states) into staging space at the end
  * of the workspace with one cudaMemcpyAsync each, runs the block there, and
  * copies the result to y_host (bf16 [S][D]); x_host and y_host may be the
- * same buffer.  Everything is ordered on `stream` and the call returns before
+ * same buffer.  The copy of x_host runs on a stream the library owns (one
+ * per device), after the caller's earlier work on `stream`, so that it
+ * overlaps the AdaLN table; the block waits for it before reading x.  Everything is ordered on `stream` and the call returns before
  * the copies complete: synchronize the stream before reading y_host or
  * reusing the inputs.  Host buffers should be page-locked (cudaHostAlloc or
  * pinned), otherwise the copies are synchronous.  The weights stay device
