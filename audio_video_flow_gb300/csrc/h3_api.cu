@@ -262,6 +262,25 @@ void gemm_set_plan(GemmArgs& a, const GemmPlan& p) {
   a.nw2 = p.nw2;
 }
 
+// Stream-K fields of a launch with sk_lane pairs per row tile (see GemmArgs).
+void gemm_set_sk(GemmArgs& a, int sk_lane, SkScratch* sk) {
+  a.sk_lane = sk_lane;
+  a.sk_units = a.num_m * sk_lane;
+  a.sk_iters = (long long)a.num_n * a.num_k;
+  a.sk_part = sk->part;
+  a.sk_flags = sk->flags;
+  a.sk_epoch = ++sk->epoch;
+}
+
+// The plan of a stream-K launch: whole-width 256-column tiles.
+GemmPlan sk_plan(int epi, int N, int H, int F) {
+  GemmPlan p{};
+  p.bn = 256;
+  p.num_n = gemm_num_n(epi, 256, N, H, F);
+  p.b_rows = gemm_b_box_rows(epi, 256);
+  return p;
+}
+
 void gemm_common(GemmArgs& a, int M, int K, int num_n) {
   a.M = M;
   a.K = K;
@@ -314,18 +333,15 @@ h3_status run_attention(int S, int H, const void* q, const void* k, const void* 
 
 // sk: stream-K scratch of the calling block (flags zeroed by its first
 // kernel); null for the stand-alone stage, which runs whole tiles only.
+// (The QKV and FC1 GEMMs run whole tiles: at 256 rows, where their last
+// wave is short, stream-K measured no faster over the refiner pass.)
 h3_status run_resid_gemm(const h3_block_config& c, const h3_packed_meta& m, const void* table, int chunk,
                          const void* act, int K, const void* w, const void* b, const void* x, void* out,
                          cudaStream_t st, SkScratch* sk = nullptr) {
   const int S = m.n_rows, D = c.dim;
   GemmPlan pl = gemm_plan(EPI_RESID, S, D, 0, 0);
-  const int sk_lane = sk ? gemm_sk_lane(S, D, K, 256) : 0;
-  if (sk_lane > 0) {    // whole-width 256-column tiles, k-blocks shared out
-    pl = GemmPlan{};
-    pl.bn = 256;
-    pl.num_n = gemm_num_n(EPI_RESID, 256, D, 0, 0);
-    pl.b_rows = gemm_b_box_rows(EPI_RESID, 256);
-  }
+  const int sk_lane = sk ? gemm_sk_lane(S, D, K, 256, 0) : 0;
+  if (sk_lane > 0) pl = sk_plan(EPI_RESID, D, 0, 0);   // whole-width tiles, k-blocks shared out
   CUtensorMap tA, tB;
   if (!make_tmap_2d(&tA, act, S, K, K, 128) || !make_tmap_2d(&tB, w, D, K, K, (uint32_t)pl.b_rows))
     return H3_ERR_CUDA;
@@ -344,14 +360,7 @@ h3_status run_resid_gemm(const h3_block_config& c, const h3_packed_meta& m, cons
   a.T = m.n_timesteps;
   a.tag = m.token_tag;
   a.tidx = m.timestep_index;
-  if (sk_lane > 0) {
-    a.sk_lane = sk_lane;
-    a.sk_units = a.num_m * sk_lane;
-    a.sk_iters = (long long)a.num_n * a.num_k;
-    a.sk_part = sk->part;
-    a.sk_flags = sk->flags;
-    a.sk_epoch = ++sk->epoch;
-  }
+  if (sk_lane > 0) gemm_set_sk(a, sk_lane, sk);
   return cuda_st(launch_gemm(EPI_RESID, pl.bn, tA, tB, a, st));
 }
 

@@ -127,11 +127,12 @@ struct SkScratch {
 };
 size_t gemm_sk_part_bytes();    // partial area for the largest stream-K launch on this GPU
 size_t gemm_sk_flag_words();    // flags for the largest stream-K launch on this GPU
-// CTA pairs per 256-row tile of a stream-K launch of this GEMM, 0 when whole
-// tiles per pair are at least as good.  H3_GEMM_SK=0 turns stream-K off, =1
+// CTA pairs per 256-row tile of a stream-K launch of this GEMM (on at most
+// max_pairs pairs when positive), 0 when whole tiles per pair are at least
+// as good.  H3_GEMM_SK=0 turns stream-K off, =1
 // forces it on whenever it is possible; H3_GEMM_SK_UNITS=<n> forces it with
 // n / row tiles pairs per row tile (at most one k-block per pair).
-int gemm_sk_lane(int M, int N, int K, int bn);
+int gemm_sk_lane(int M, int N, int K, int bn, int max_pairs);
 
 // Column tiling of one GEMM launch.  Uniform: num_n tiles of bn columns.
 // Balanced (plain and residual epilogues, when one wave of uniform tiles

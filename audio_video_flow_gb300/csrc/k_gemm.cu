@@ -448,17 +448,29 @@ __device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+// The i-th of the NCH/2 32-column accumulator chunks that the epilogue warps
+// of column half `half` read: the first or second half of the tile, except
+// for SwiGLU, where a half takes gate chunks and the value chunks paired with
+// them (chunk c of the gate columns with chunk c of the value columns).
+// Partial sums are stored and folded by the same warps that read them.
+template <int EPI, int NCH>
+__device__ __forceinline__ int sk_chunk(int half, int i) {
+  if (EPI == EPI_SWIGLU)
+    return i < NCH / 4 ? half * (NCH / 4) + i : NCH / 2 + half * (NCH / 4) + (i - NCH / 4);
+  return half * (NCH / 2) + i;
+}
+
 // A piece that does not hold k-block 0: this warp's 32 accumulator rows
 // (the 32-column chunks of its column half) to the pair's partial slot, then
 // the warp's flag.
-template <int BN>
+template <int EPI, int BN>
 __device__ __forceinline__ void sk_store_partial(const GemmArgs& a, uint32_t tacc, int unit, uint32_t rank,
                                                  int quad, int half, int row, int lane) {
   constexpr int NCH = BN / 32;
   float* slot = sk_slot(a, unit, rank, NCH);
-  const int c_end = half ? NCH : NCH / 2;
 #pragma unroll 1
-  for (int c = half ? NCH / 2 : 0; c < c_end; ++c) {
+  for (int i = 0; i < NCH / 2; ++i) {
+    const int c = sk_chunk<EPI, NCH>(half, i);
     uint32_t r[32];
     tmem_ld32(tacc + c * 32, r);
     tmem_ld_wait(r);
@@ -478,7 +490,7 @@ __device__ __forceinline__ void sk_store_partial(const GemmArgs& a, uint32_t tac
 // that start inside it (units unit+1, unit+2, ...; this warp's rows only) and
 // add them, in that order, to the accumulator in TMEM.  Returns false
 // (warp-uniform) when a wait gave up.
-template <int BN>
+template <int EPI, int BN>
 __device__ __forceinline__ bool sk_fold_partials(const GemmArgs& a, uint32_t tacc, int unit, uint32_t rank,
                                                  int quad, int half, int row, int lane, int tile,
                                                  volatile int* abort_v) {
@@ -514,7 +526,8 @@ __device__ __forceinline__ bool sk_fold_partials(const GemmArgs& a, uint32_t tac
   for (int q = unit + 1; q < q_end; ++q) {
     const float* slot = sk_slot(a, q, rank, NCH);
 #pragma unroll 1
-    for (int c = half ? NCH / 2 : 0; c < (half ? NCH : NCH / 2); c += 2) {
+    for (int i = 0; i < NCH / 2; i += 2) {
+      const int c = sk_chunk<EPI, NCH>(half, i);   // chunks c and c + 1 (pairs stay adjacent)
       float4 p[16];
       const float4* s0 = reinterpret_cast<const float4*>(slot + (size_t)c * (128 * 32)) + row;
       const float4* s1 = reinterpret_cast<const float4*>(slot + (size_t)(c + 1) * (128 * 32)) + row;
@@ -729,11 +742,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       if (!w.owner) {
         // stream-K piece without k-block 0: hand the partial to the owner
         // (stream-K launches use 256-column tiles only)
-        if constexpr (BN == 256) sk_store_partial<BN>(args, tacc, unit, rank, q, half, row, lane);
+        if constexpr (BN == 256) sk_store_partial<EPI, BN>(args, tacc, unit, rank, q, half, row, lane);
       } else {
         if constexpr (BN == 256) {
           if (args.sk_units > 0)
-            done = sk_fold_partials<BN>(args, tacc, unit, rank, q, half, row, lane, w.tile, abort_v);
+            done = sk_fold_partials<EPI, BN>(args, tacc, unit, rank, q, half, row, lane, w.tile, abort_v);
         }
         if (done) run_epilogue<EPI, BN>(args, tacc, m_blk * 2 * BM + (int)rank * BM + row, n_blk, half);
       }
@@ -848,17 +861,19 @@ GemmPlan gemm_plan(int epi, int M, int N, int H, int F) {
 size_t gemm_sk_part_bytes() { return (size_t)gemm_pair_slots() * 2 * 128 * 256 * sizeof(float); }
 size_t gemm_sk_flag_words() { return (size_t)gemm_pair_slots() * 16; }
 
-// Whole 256-column tiles run in waves of one tile per resident pair.  When
-// the last wave would leave more than a tenth of the pairs idle (a few
-// hundred rows: 505 rows x 5376 columns is 42 tiles for 76 pairs), each
+// Whole 256-column tiles run in waves of one tile per resident pair (at most
+// max_pairs when positive).  When the last wave would leave more than a
+// tenth of the pairs idle (a few hundred rows: 505 rows x 5376 columns is 42
+// tiles for 76 pairs; 256 rows x 21504 QKV columns 84), each
 // 256-row tile gets a lane of floor(pairs / row tiles) pairs that share out
 // its column tiles' k-blocks, provided that keeps nine tenths of the pairs
 // busy and gives every pair at least 8 k-blocks.  Returns the pairs per lane.
-int gemm_sk_lane(int M, int N, int K, int bn) {
+int gemm_sk_lane(int M, int N, int K, int bn, int max_pairs) {
   const char* env = getenv("H3_GEMM_SK");
   if (env && env[0] == '0') return 0;
   const bool force = env && env[0] == '1';
-  const int slots = gemm_pair_slots();
+  int slots = gemm_pair_slots();
+  if (max_pairs > 0 && max_pairs < slots) slots = max_pairs;
   const int num_m = gemm_m_tiles(M);
   const long long num_n = (N + bn - 1) / bn;
   const long long lane_iters = num_n * (K / BK);
