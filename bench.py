@@ -45,10 +45,10 @@ STAGES = ("adaln_table", "norm1_modulate", "qkv_qknorm_rope", "attention", "out_
 # hit L2), so the 32,768- and 15,860-row values are the 16,384-row capture
 # scaled by the row count.
 TRAFFIC = {
-    "qkv_qknorm_rope@block505": 249930496,
-    "fc1_swiglu@block505": 331703808,
-    "qkv_qknorm_rope@block1824": 337300736,
-    "fc1_swiglu@block1824": 386801920,
+    "qkv_qknorm_rope@block505": 252197120,
+    "fc1_swiglu@block505": 333102080,
+    "qkv_qknorm_rope@block1824": 331419648,
+    "fc1_swiglu@block1824": 377690368,
     "attention@attn4096": 214684160,
     "attention@attn16384": 919471872,
     "attention@attn32768": 1838943744,
