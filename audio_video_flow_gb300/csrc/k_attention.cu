@@ -522,24 +522,24 @@ __global__ void __launch_bounds__(AT2_THREADS, 1)
 #pragma unroll
       for (int e = 0; e < 8; ++e) mp[e] = -INFINITY;
       const bool full_tile = valid >= KV_TILE;
-#pragma unroll 1
-      for (int h2 = 0; h2 < 2; ++h2) {
-        uint32_t a[32], b[32];
-        tmem_ld32(s_base + (uint32_t)(h2 * 64), a);
-        tmem_ld32(s_base + (uint32_t)(h2 * 64 + 32), b);
-        tmem_ld_wait(a);
-        tmem_ld_wait(b);
+      {
+        // all 128 scores of the row requested before one wait
+        uint32_t r[4][32];
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) tmem_ld32(s_base + (uint32_t)(q4 * 32), r[q4]);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) tmem_ld_wait(r[q4]);
         if (full_tile) {
 #pragma unroll
-          for (int c = 0; c < 32; ++c)
-            mp[c & 7] = fmaxf(mp[c & 7], fmaxf(__uint_as_float(a[c]), __uint_as_float(b[c])));
+          for (int q4 = 0; q4 < 4; ++q4)
+#pragma unroll
+            for (int c = 0; c < 32; ++c) mp[c & 7] = fmaxf(mp[c & 7], __uint_as_float(r[q4][c]));
         } else {
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const float va = (h2 * 64 + c < valid) ? __uint_as_float(a[c]) : -INFINITY;
-            const float vb = (h2 * 64 + 32 + c < valid) ? __uint_as_float(b[c]) : -INFINITY;
-            mp[c & 7] = fmaxf(mp[c & 7], fmaxf(va, vb));
-          }
+          for (int q4 = 0; q4 < 4; ++q4)
+#pragma unroll
+            for (int c = 0; c < 32; ++c)
+              mp[c & 7] = fmaxf(mp[c & 7], (q4 * 32 + c < valid) ? __uint_as_float(r[q4][c]) : -INFINITY);
         }
       }
       const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),

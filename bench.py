@@ -49,10 +49,10 @@ TRAFFIC = {
     "fc1_swiglu@block505": 333102080,
     "qkv_qknorm_rope@block1824": 331419648,
     "fc1_swiglu@block1824": 377690368,
-    "attention@attn4096": 214684160,
-    "attention@attn16384": 919471872,
-    "attention@attn32768": 1838943744,
-    "attention@denoiser15860": 890064935,
+    "attention@attn4096": 212803072,
+    "attention@attn16384": 918654208,
+    "attention@attn32768": 1837308416,
+    "attention@denoiser15860": 889273422,
 }
 
 
