@@ -270,6 +270,12 @@ void gemm_set_sk(GemmArgs& a, int sk_lane, SkScratch* sk) {
   a.sk_part = sk->part;
   a.sk_flags = sk->flags;
   a.sk_epoch = ++sk->epoch;
+  // H3_SK_FLAG_TEST=1 (tests of the failure path only): owners wait for a
+  // flag value that no partial writer sets, so every owner's bounded wait
+  // runs out and the launch reports H3_ERR_TIMEOUT through h3_sync_check
+  // instead of producing its output; nothing traps or hangs.
+  const char* t = getenv("H3_SK_FLAG_TEST");
+  a.sk_wait = (t && t[0] == '1') ? (a.sk_epoch | 0x80000000u) : a.sk_epoch;
 }
 
 // The plan of a stream-K launch: whole-width 256-column tiles.

@@ -114,6 +114,7 @@ struct GemmArgs {
   float* sk_part;        // [sk_units][2 CTAs][BN/32 chunks][8 groups][128 rows][4] fp32
   uint32_t* sk_flags;    // [sk_units][2 CTAs][4 row quadrants][2 column halves], zero before first use
   uint32_t sk_epoch;     // nonzero, distinct for every launch between two zeroings
+  uint32_t sk_wait;      // the flag value owners wait for: sk_epoch (see gemm_set_sk for the test hook)
   uint32_t* err;
 };
 

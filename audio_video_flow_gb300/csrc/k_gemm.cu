@@ -506,10 +506,10 @@ __device__ __forceinline__ bool sk_fold_partials(const GemmArgs& a, uint32_t tac
   if (lane == 0) {
     for (int q = unit + 1; q < q_end && ok; ++q) {
       const uint32_t* f = sk_flag(a, q, rank, quad, half);
-      if (ld_acquire_u32(f) == a.sk_epoch) continue;
+      if (ld_acquire_u32(f) == a.sk_wait) continue;
       const uint64_t t0 = globaltimer();
       for (uint32_t i = 1;; ++i) {
-        if (ld_acquire_u32(f) == a.sk_epoch) break;
+        if (ld_acquire_u32(f) == a.sk_wait) break;
         if ((i & 31u) == 0 && (*abort_v || globaltimer() - t0 > kWaitLimitNs)) {
           *abort_v = 1;
           ok = 0;

@@ -314,6 +314,25 @@ def test_block_forward_host_matches_device(h3):
         h3.h3_block_forward_host(cfg, h3.make_weights(c.d_w), meta_h, x_h, y_h, small)
 
 
+def test_stream_k_lost_flags_time_out(h3, monkeypatch):
+    """The stream-K hand-off's failure path, without a GPU fault: with
+    H3_SK_FLAG_TEST=1 the owners wait for a flag value that nothing sets, so
+    their bounded waits (2 s) run out; the launch records a device timeout
+    that h3_sync_check reports as H3_ERR_TIMEOUT, and the next call on the
+    same context works and gives the normal result bit for bit."""
+    c = get_case("block505")          # O and FC2 run stream-K at 505 rows
+    y_ref = run_block(h3, c)
+    assert "stream-k=0" not in h3.h3_last_kernel_info()
+    monkeypatch.setenv("H3_SK_FLAG_TEST", "1")
+    cfg = c.cfg(h3)
+    ws = torch.empty(h3.h3_block_workspace_bytes(cfg, c.S, c.T), dtype=torch.uint8, device="cuda")
+    y = torch.empty_like(y_ref)
+    h3.h3_block_forward(cfg, h3.make_weights(c.d_w), c.meta(h3), c.d_x, y, ws)
+    assert h3.h3_sync_check(timeout_ms=60000) == h3.H3_ERR_TIMEOUT
+    monkeypatch.delenv("H3_SK_FLAG_TEST")
+    assert torch.equal(run_block(h3, c, ws=ws), y_ref)
+
+
 def test_block_repeatable_and_inplace(h3):
     """Control H-C0 (repeated call: bitwise equal), a fresh workspace, and
     x_out aliasing x_in."""
