@@ -45,8 +45,8 @@ STAGES = ("adaln_table", "norm1_modulate", "qkv_qknorm_rope", "attention", "out_
 # hit L2), so the 32,768- and 15,860-row values are the 16,384-row capture
 # scaled by the row count.
 TRAFFIC = {
-    "qkv_qknorm_rope@block505": 252197120,
-    "fc1_swiglu@block505": 333102080,
+    "qkv_qknorm_rope@block505": 252368128,
+    "fc1_swiglu@block505": 332998144,
     "qkv_qknorm_rope@block1824": 331419648,
     "fc1_swiglu@block1824": 377690368,
     "attention@attn4096": 212803072,
