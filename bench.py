@@ -47,8 +47,8 @@ STAGES = ("adaln_table", "norm1_modulate", "qkv_qknorm_rope", "attention", "out_
 TRAFFIC = {
     "qkv_qknorm_rope@block505": 252368128,
     "fc1_swiglu@block505": 332998144,
-    "qkv_qknorm_rope@block1824": 331419648,
-    "fc1_swiglu@block1824": 377690368,
+    "qkv_qknorm_rope@block1824": 330054656,
+    "fc1_swiglu@block1824": 377669888,
     "attention@attn4096": 212803072,
     "attention@attn16384": 918654208,
     "attention@attn32768": 1837308416,
