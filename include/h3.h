@@ -200,7 +200,7 @@ h3_status h3_blocks_forward(const h3_block_config *cfg, int32_t n_blocks,
                             cudaStream_t stream);
 
 /* The same chain captured once into a CUDA graph and replayed with one launch
- * (SURVEY "next" item 1: one graph per evaluation).  h3_blocks_graph_create
+ * (one graph per denoiser evaluation).  h3_blocks_graph_create
  * records the launches h3_blocks_forward would make for these arguments
  * (pointers and sizes are baked in; the buffers' contents are read at each
  * replay) and instantiates the graph; h3_graph_launch replays it on a
