@@ -379,6 +379,20 @@ def test_chain_two_blocks(h3):
     assert_close(to_np(y), ref, "two-block chain")
 
 
+@pytest.mark.parametrize("cond", [128, 2816])
+def test_block_maximum_table_sizes(h3, cond):
+    """The largest AdaLN table the kernels take: 16 timestep rows, and a
+    conditioning width of 2816 (the most the table kernel keeps resident in
+    shared memory), on a small block with every timestep row used."""
+    shape = hi.BlockShape(dim=512, n_heads=4, head_dim=128, ffn_dim=1536, cond_dim=cond)
+    w = hi.custom_workload(shape, n_text=9, video_grid=(2, 4, 5), n_audio=23, n_timesteps=16,
+                           name=f"maxtable{cond}")
+    c = Case(w)
+    assert set(np.unique(c.np_meta["timestep_index"])) <= set(range(16))
+    y = run_block(h3, c)
+    assert_close(to_np(y), c.ref["y"], f"block T=16 cond={cond}")
+
+
 def test_single_row_block(h3):
     w = hi.custom_workload(hi.TINY_SHAPE, n_text=1, video_grid=(0, 0, 0), n_audio=0, n_timesteps=1)
     c = Case(w)
