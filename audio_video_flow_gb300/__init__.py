@@ -102,6 +102,7 @@ def lib() -> ctypes.CDLL:
             "h3_sync_check": (i32, [vp, i32]),
             "h3_status_string": (c_char_p, [i32]),
             "h3_last_kernel_info": (i32, [ctypes.c_char_p, sz]),
+            "h3_last_error_site": (i32, [ctypes.c_char_p, sz]),
             "h3_version": (c_char_p, []),
         }
         for name, (res, args) in sig.items():
@@ -392,6 +393,14 @@ def h3_sync_check(stream=None, timeout_ms: int = 10000) -> int:
 def h3_last_kernel_info() -> str:
     buf = ctypes.create_string_buffer(512)
     lib().h3_last_kernel_info(buf, 512)
+    return buf.value.decode()
+
+
+def h3_last_error_site() -> str:
+    """Where the first device wait that ran out was (read by the last
+    h3_sync_check that returned H3_ERR_TIMEOUT), or "none"."""
+    buf = ctypes.create_string_buffer(128)
+    lib().h3_last_error_site(buf, 128)
     return buf.value.decode()
 
 

@@ -18,9 +18,10 @@
 
 namespace h3 {
 
-// Device error word: set by kernels on bad metadata or a wait that ran out,
-// read and cleared by h3_sync_check.
-__device__ uint32_t g_error_word = 0;
+// Device error words: [0] bits set by kernels on bad metadata or a wait that
+// ran out, [1] the site of the first wait that ran out; read and cleared by
+// h3_sync_check.
+__device__ uint32_t g_error_word[2] = {0u, 0u};
 
 namespace {
 thread_local char g_info[512] = "";
@@ -50,6 +51,27 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 }  // namespace
 
+namespace {
+char g_site[128] = "none";
+std::mutex g_site_mu;
+
+// Text of a site word (kernel id in the top byte; the low 24 bits are the
+// barrier's shared-memory byte offset / 8, or kSiteStreamKFlag).
+void note_error_site(uint32_t site) {
+  static const char* const names[] = {"unknown", "gemm", "attention-1q", "attention-2q", "adaln-table",
+                                      "rope-qknorm"};
+  const uint32_t k = site >> 24, lo = site & 0xFFFFFFu;
+  const char* kn = k < sizeof(names) / sizeof(names[0]) ? names[k] : "unknown";
+  std::lock_guard<std::mutex> lk(g_site_mu);
+  if (site == 0)
+    snprintf(g_site, sizeof(g_site), "timeout without a recorded site");
+  else if (lo == kSiteStreamKFlag)
+    snprintf(g_site, sizeof(g_site), "%s: stream-K partial-sum flag", kn);
+  else
+    snprintf(g_site, sizeof(g_site), "%s: mbarrier at shared offset %u", kn, lo * 8u);
+}
+}  // namespace
+
 void set_kernel_info(const char* fmt, ...) {
   va_list ap;
   va_start(ap, fmt);
@@ -73,6 +95,24 @@ int num_sms() {
     g_sms[d] = n > 0 ? n : 1;
   }
   return g_sms[d];
+}
+
+// If every TMEM kernel takes more than half of an SM's shared memory, no two
+// of them (the same kernel or two different ones) fit on one SM together.
+bool tmem_exclusive(int dyn_smem) {
+  static int per_sm[kMaxDevices] = {0}, reserved[kMaxDevices] = {0};
+  const int d = current_device();
+  if (!per_sm[d]) {
+    int p = 0, r = 0;
+    if (cudaDeviceGetAttribute(&p, cudaDevAttrMaxSharedMemoryPerMultiprocessor, d) != cudaSuccess ||
+        cudaDeviceGetAttribute(&r, cudaDevAttrReservedSharedMemoryPerBlock, d) != cudaSuccess || p <= 0) {
+      cudaGetLastError();
+      return false;
+    }
+    reserved[d] = r;
+    per_sm[d] = p;
+  }
+  return 2 * (dyn_smem + reserved[d]) > per_sm[d];
 }
 
 uint32_t* device_error_word() {
@@ -1209,13 +1249,17 @@ h3_status h3_sync_check(cudaStream_t stream, int32_t timeout_ms) {
   if (e != cudaSuccess) return H3_ERR_CUDA;
   uint32_t* p = device_error_word();
   if (!p) return H3_ERR_CUDA;
-  uint32_t bits = 0;
-  if (cudaMemcpy(&bits, p, sizeof(bits), cudaMemcpyDeviceToHost) != cudaSuccess) return H3_ERR_CUDA;
-  if (bits) {
-    if (cudaMemset(p, 0, sizeof(uint32_t)) != cudaSuccess) return H3_ERR_CUDA;
+  uint32_t words[2] = {0u, 0u};
+  if (cudaMemcpy(words, p, sizeof(words), cudaMemcpyDeviceToHost) != cudaSuccess) return H3_ERR_CUDA;
+  const uint32_t bits = words[0];
+  if (bits || words[1]) {
+    if (cudaMemset(p, 0, sizeof(words)) != cudaSuccess) return H3_ERR_CUDA;
     if (cudaDeviceSynchronize() != cudaSuccess) return H3_ERR_CUDA;
   }
-  if (bits & DEVERR_TIMEOUT) return H3_ERR_TIMEOUT;
+  if (bits & DEVERR_TIMEOUT) {
+    note_error_site(words[1]);
+    return H3_ERR_TIMEOUT;
+  }
   if (bits & DEVERR_INDEX) return H3_ERR_INDEX;
   return H3_OK;
 }
@@ -1233,6 +1277,13 @@ const char* h3_status_string(h3_status s) {
     case H3_ERR_WORKSPACE: return "workspace too small";
   }
   return "unknown status";
+}
+
+h3_status h3_last_error_site(char* buf, size_t len) {
+  if (!buf || len == 0) return H3_ERR_NULL;
+  std::lock_guard<std::mutex> lk(g_site_mu);
+  snprintf(buf, len, "%s", g_site);
+  return H3_OK;
 }
 
 h3_status h3_last_kernel_info(char* buf, size_t len) {

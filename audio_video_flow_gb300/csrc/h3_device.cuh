@@ -21,8 +21,32 @@ __device__ __forceinline__ void record_error(uint32_t* err, uint32_t bits) {
 }
 
 // Limit of one device-side wait.  A wait that runs out raises the CTA's abort
-// flag and returns false; the kernel records DEVERR_TIMEOUT before it exits.
+// flag, sets DEVERR_TIMEOUT in the device error word at once (with the site of
+// the first such wait) and returns false.  The kernels with bounded waits read
+// the TIMEOUT bit once, after griddepcontrol.wait and before they issue any
+// asynchronous copy or MMA, and skip their work when it is set: the bit is
+// sticky until h3_sync_check clears it, so one lost signal costs the launch
+// it happens in, not one wait limit per later launch.  (A wait already in
+// progress does not look at the bit: giving up early would leave TMA copies
+// and MMAs in flight that the drains after a real timeout can rely on having
+// finished.)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+// Kernel ids of the first timed-out wait (top byte of the site word).
+enum : uint32_t {
+  KID_GEMM = 1u, KID_ATTN_1Q = 2u, KID_ATTN_2Q = 3u, KID_ADALN = 4u, KID_ROPE = 5u,
+};
+// Low 24 bits of the site word for a wait that is not on an mbarrier.
+constexpr uint32_t kSiteStreamKFlag = 0xFFFFFFu;
+
+// What a bounded wait consults and where it reports: the CTA's abort flag in
+// shared memory, the device error word (err[0] bits, err[1] site of the first
+// timeout) and the kernel's id.
+struct WaitCtl {
+  volatile int* flag;
+  uint32_t* err;
+  uint32_t kernel;
+};
 
 __device__ __forceinline__ uint64_t globaltimer() {
   uint64_t t;
@@ -62,20 +86,37 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// True when a timeout has been recorded on the device since the last
+// h3_sync_check (read at kernel entry, after griddepcontrol.wait).
+__device__ __forceinline__ bool timeout_recorded(const uint32_t* err) {
+  return err && (*reinterpret_cast<const volatile uint32_t*>(err) & DEVERR_TIMEOUT);
+}
+
+// Slow-path check of a bounded wait (called every few polls): true when the
+// wait must give up, because another thread of the CTA gave up or because
+// this wait has now run for kWaitLimitNs (then the timeout and its site are
+// recorded).
+__device__ __forceinline__ bool wait_gives_up(const WaitCtl& c, uint64_t t0, uint32_t site_lo) {
+  if (*c.flag) return true;
+  if (globaltimer() - t0 > kWaitLimitNs) {
+    *c.flag = 1;
+    if (c.err) {
+      atomicOr(c.err, DEVERR_TIMEOUT);
+      atomicCAS(c.err + 1, 0u, (c.kernel << 24) | (site_lo & 0xFFFFFFu));
+    }
+    return true;
+  }
+  return false;
+}
+
 // Wait until the phase with the given parity has completed.  Bounded: gives up
-// after kWaitLimitNs (or as soon as another thread of the CTA has given up).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+// after kWaitLimitNs or as soon as another thread of the CTA has given up.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitCtl& c) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 31u) == 0) {
-      if (*abort_flag) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) {
-        *abort_flag = 1;
-        return false;
-      }
-    }
+    if ((i & 31u) == 0 && wait_gives_up(c, t0, smem_u32(bar) >> 3)) return false;
   }
 }
 
@@ -276,18 +317,12 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t pa
   return ok != 0;
 }
 // Bounded wait on a barrier that other CTAs of the cluster also arrive on.
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, const WaitCtl& c) {
   if (mbar_try_wait_cluster(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait_cluster(bar, parity)) return true;
-    if ((i & 31u) == 0) {
-      if (*abort_flag) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) {
-        *abort_flag = 1;
-        return false;
-      }
-    }
+    if ((i & 31u) == 0 && wait_gives_up(c, t0, smem_u32(bar) >> 3)) return false;
   }
 }
 // TMA load into this CTA's shared memory whose completion is counted on an

@@ -59,7 +59,32 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
                           Args&&... args) {
   return launch_kernel_cluster(kernel, grid, block, smem, stream, 1, static_cast<Args&&>(args)...);
 }
-uint32_t* device_error_word();   // device address of the error word (current device)
+// Device address of the error words of the current device: [0] the error
+// bits (DEVERR_*), [1] the site of the first timed-out wait (kernel id in the
+// top byte, the barrier's shared-memory offset / 8 or kSiteStreamKFlag below).
+uint32_t* device_error_word();
+
+// ---------------------------------------------------------------------------
+// TMEM exclusivity.  Every kernel that allocates tensor memory (the GEMM, both
+// attention kernels, the AdaLN table) allocates before griddepcontrol.wait,
+// so that the allocation overlaps the previous kernel's tail, and the
+// allocation blocks until the columns are free.  That is safe only while no
+// two such CTAs can be resident on one SM at the same time: a dependent CTA
+// holding TMEM on an SM where a primary CTA has started but not yet allocated
+// would wait for that primary grid forever.  The kernels keep it by their
+// shared-memory footprint: each takes more than half of an SM's shared
+// memory, so a second CTA of any of them cannot be placed beside it.  The
+// static checks below pin the footprints against the sm_100-family figure
+// (228 KB per SM, 1 KB reserved per CTA); tmem_exclusive() repeats the check
+// against the figures the device reports, once per device, and the launchers
+// refuse to launch when it fails.
+// ---------------------------------------------------------------------------
+constexpr int kSmemPerSm = 233472;
+constexpr int kSmemReservedPerCta = 1024;
+constexpr bool tmem_footprint_exclusive(int dyn_smem) {
+  return 2 * (dyn_smem + kSmemReservedPerCta) > kSmemPerSm;
+}
+bool tmem_exclusive(int dyn_smem);
 void set_kernel_info(const char* fmt, ...);
 
 // ---------------------------------------------------------------------------

@@ -97,9 +97,16 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   tc_fence_after();
   griddep_wait();
   const uint32_t tmem_base = *tmem_slot;   // S0: cols [0,128), S1: [128,256), O: [256,384)
-  volatile int* abort_v = abort_flag;
+  const WaitCtl abort_v{abort_flag, args.err, KID_ATTN_1Q};
 
-  if (warp == 0) {
+  // a wait of an earlier launch ran out (sticky until h3_sync_check): this
+  // launch skips its work, before any copy or MMA is issued
+  if (threadIdx.x == 0 && timeout_recorded(args.err)) *abort_flag = 1;
+  __syncthreads();
+  const bool skip = *abort_v.flag != 0;
+
+  if (skip) {
+  } else if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       bool ok = true;
@@ -299,7 +306,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (threadIdx.x == 0 && *abort_v) record_error(args.err, DEVERR_TIMEOUT);
+  if (threadIdx.x == 0 && *abort_v.flag) record_error(args.err, DEVERR_TIMEOUT);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, 512);
@@ -395,9 +402,16 @@ __global__ void __launch_bounds__(AT2_THREADS, 1)
   tc_fence_after();
   griddep_wait();
   const uint32_t tmem_base = *tmem_slot;
-  volatile int* abort_v = abort_flag;
+  const WaitCtl abort_v{abort_flag, args.err, KID_ATTN_2Q};
 
-  if (warp == 0) {
+  // a wait of an earlier launch ran out (sticky until h3_sync_check): this
+  // launch skips its work, before any copy or MMA is issued
+  if (threadIdx.x == 0 && timeout_recorded(args.err)) *abort_flag = 1;
+  __syncthreads();
+  const bool skip = *abort_v.flag != 0;
+
+  if (skip) {
+  } else if (warp == 0) {
     // ------------------------------------------------------------ producer of Q and K
     if (lane == 0) {
       bool ok = true;
@@ -634,7 +648,7 @@ __global__ void __launch_bounds__(AT2_THREADS, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (threadIdx.x == 0 && *abort_v) record_error(args.err, DEVERR_TIMEOUT);
+  if (threadIdx.x == 0 && *abort_v.flag) record_error(args.err, DEVERR_TIMEOUT);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, 512);
@@ -651,6 +665,9 @@ cudaError_t launch_attention(const CUtensorMap& tmQ, const CUtensorMap& tmK, con
     const int f = atoi(env);
     if (f == 1 || f == 2) qtiles = f;
   }
+  static_assert(tmem_footprint_exclusive(AT_SMEM) && tmem_footprint_exclusive(AT2_SMEM),
+                "an attention CTA must hold its SM's TMEM alone");
+  if (!tmem_exclusive(qtiles == 2 ? AT2_SMEM : AT_SMEM)) return cudaErrorNotSupported;
   cudaError_t e;
   if (qtiles == 2) {
     e = cudaFuncSetAttribute(attention_kernel_2q, cudaFuncAttributeMaxDynamicSharedMemorySize, AT2_SMEM);

@@ -493,7 +493,7 @@ __device__ __forceinline__ void sk_store_partial(const GemmArgs& a, uint32_t tac
 template <int EPI, int BN>
 __device__ __forceinline__ bool sk_fold_partials(const GemmArgs& a, uint32_t tacc, int unit, uint32_t rank,
                                                  int quad, int half, int row, int lane, int tile,
-                                                 volatile int* abort_v) {
+                                                 const WaitCtl& abort_v) {
   constexpr int NCH = BN / 32;
   static_assert(NCH % 4 == 0, "each column half is folded two chunks at a time");
   const int j = unit % a.sk_lane;
@@ -510,8 +510,7 @@ __device__ __forceinline__ bool sk_fold_partials(const GemmArgs& a, uint32_t tac
       const uint64_t t0 = globaltimer();
       for (uint32_t i = 1;; ++i) {
         if (ld_acquire_u32(f) == a.sk_wait) break;
-        if ((i & 31u) == 0 && (*abort_v || globaltimer() - t0 > kWaitLimitNs)) {
-          *abort_v = 1;
+        if ((i & 31u) == 0 && wait_gives_up(abort_v, t0, kSiteStreamKFlag)) {
           ok = 0;
           break;
         }
@@ -640,9 +639,16 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   tc_fence_after();
   griddep_wait();
   const uint32_t tmem_base = *tmem_slot;
-  volatile int* abort_v = abort_flag;
+  const WaitCtl abort_v{abort_flag, args.err, KID_GEMM};
 
-  if (warp == 0) {
+  // a wait of an earlier launch ran out (sticky until h3_sync_check): this
+  // launch skips its work, before any copy or MMA is issued
+  if (threadIdx.x == 0 && timeout_recorded(args.err)) *abort_flag = 1;
+  __syncthreads();
+  const bool skip = *abort_v.flag != 0;
+
+  if (skip) {
+  } else if (warp == 0) {
     // ---------------------------------------------------------- TMA producer (both CTAs)
     if (lane == 0) {
       int stage = 0;
@@ -759,7 +765,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   tc_fence_before();
   __syncthreads();
   cluster_sync();          // no CTA of the cluster still signals another's barriers or TMEM
-  if (threadIdx.x == 0 && *abort_v) record_error(args.err, DEVERR_TIMEOUT);
+  if (threadIdx.x == 0 && *abort_v.flag) record_error(args.err, DEVERR_TIMEOUT);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc_pair(tmem_base, 512);
@@ -931,6 +937,8 @@ template <int EPI, int BN>
 static cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, int grid,
                               cudaStream_t stream) {
   constexpr int smem = GemmCfg<BN>::SMEM;
+  static_assert(tmem_footprint_exclusive(smem), "a GEMM CTA must hold its SM's TMEM alone");
+  if (!tmem_exclusive(smem)) return cudaErrorNotSupported;
   cudaError_t e = cudaFuncSetAttribute(gemm_bf16_tc<EPI, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   return launch_kernel_cluster(gemm_bf16_tc<EPI, BN>, dim3(grid), dim3(GEMM_THREADS), smem, stream, 2, tmA, tmB, a);
@@ -1068,7 +1076,7 @@ __global__ void __launch_bounds__(AD_THREADS, 1)
     const int m = tile / tiles_per_mod;
     return m * 6 * args.D + args.chunk_lo * args.D + (tile - m * tiles_per_mod) * BM;
   };
-  volatile int* abort_v = abort_flag;
+  const WaitCtl abort_v{abort_flag, args.err, KID_ADALN};
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmW);
     tma_prefetch_desc(&tmU);
@@ -1082,7 +1090,14 @@ __global__ void __launch_bounds__(AD_THREADS, 1)
   }
   griddep_wait();
 
-  if (warp == 0) {
+  // a wait of an earlier launch ran out (sticky until h3_sync_check): this
+  // launch skips its work, before any copy or MMA is issued
+  if (threadIdx.x == 0 && timeout_recorded(args.err)) *abort_flag = 1;
+  __syncthreads();
+  const bool skip = *abort_v.flag != 0;
+
+  if (skip) {
+  } else if (warp == 0) {
     if (lane == 0) {
       // the resident N = 16 operand, one 2 KB box per 64 columns of K
       mbar_arrive_expect_tx(u_full, (uint32_t)nkb * 2048u);
@@ -1183,7 +1198,7 @@ __global__ void __launch_bounds__(AD_THREADS, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (threadIdx.x == 0 && *abort_v) record_error(args.err, DEVERR_TIMEOUT);
+  if (threadIdx.x == 0 && *abort_v.flag) record_error(args.err, DEVERR_TIMEOUT);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, 32);
@@ -1222,6 +1237,8 @@ cudaError_t launch_adaln_table(const CUtensorMap& tmW, const CUtensorMap& tmU, c
   const char* pf = getenv("H3_ADALN_L2PF");
   a2.l2_pf = pf ? atoi(pf) : 0;
   if (a2.l2_pf < 0 || a2.l2_pf > 64) a2.l2_pf = 0;
+  static_assert(tmem_footprint_exclusive(AD_SMEM), "an AdaLN-table CTA must hold its SM's TMEM alone");
+  if (!tmem_exclusive(AD_SMEM)) return cudaErrorNotSupported;
   cudaError_t e = cudaFuncSetAttribute(adaln_table_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, AD_SMEM);
   if (e != cudaSuccess) return e;
   e = launch_kernel_cluster(adaln_table_kernel, dim3(grid), dim3(AD_THREADS), AD_SMEM, stream, cluster, tmW, tmU,

@@ -157,9 +157,16 @@ __global__ void __launch_bounds__(ROPE_THREADS, 1)
   }
   __syncthreads();
   griddep_wait();
-  volatile int* abort_v = abort_flag;
+  const WaitCtl abort_v{abort_flag, a.err, KID_ROPE};
 
-  if (warp == 0) {
+  // a wait of an earlier launch ran out (sticky until h3_sync_check): this
+  // launch skips its work, before any copy or MMA is issued
+  if (threadIdx.x == 0 && timeout_recorded(a.err)) *abort_flag = 1;
+  __syncthreads();
+  const bool skip = *abort_v.flag != 0;
+
+  if (skip) {
+  } else if (warp == 0) {
     // ------------------------------------------------------------ producer
     int stage = 0;
     uint32_t phase = 0;
@@ -298,7 +305,7 @@ __global__ void __launch_bounds__(ROPE_THREADS, 1)
     }
   }
   __syncthreads();
-  if (threadIdx.x == 0 && *abort_v) record_error(a.err, DEVERR_TIMEOUT);
+  if (threadIdx.x == 0 && *abort_v.flag) record_error(a.err, DEVERR_TIMEOUT);
 }
 
 int rope_qknorm_smem_bytes(int H) { return rope_smem_bytes(rope_heads_per_unit(H)); }

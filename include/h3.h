@@ -23,11 +23,23 @@
  *     timestep index outside [0,T), a position outside [0, 2^24)) do not
  *     fault: the kernel records the error in a device error word, leaves the
  *     row's output unwritten and carries on.  h3_sync_check reads and clears
- *     that word.  A device-side wait that exceeds its time limit is recorded
- *     the same way (H3_ERR_TIMEOUT).
- *   - Results are deterministic: every reduction has a fixed order that does
- *     not depend on the row count, the launch geometry or the SM count (RFC
- *     section 4, numerical contract items 1-3).  There is no split-K.
+ *     that word.  A device-side wait that exceeds its time limit (2 s) is
+ *     recorded the same way (H3_ERR_TIMEOUT), together with the site of the
+ *     first such wait (h3_last_error_site).  The timeout bit is sticky: until
+ *     h3_sync_check clears it, every bounded wait of every library kernel on
+ *     that device gives up at its next poll, so one lost signal ends the
+ *     whole queue of work within about one time limit instead of costing one
+ *     limit per later launch.  Results of calls made in that window are
+ *     undefined; the status says so.
+ *   - Results are deterministic: a given call on a given GPU gives bitwise
+ *     the same output every time.  With H3_GEMM_SK=0 in the environment every
+ *     reduction has a fixed order that does not depend on the row count, the
+ *     launch geometry or the SM count (RFC section 4, numerical contract
+ *     items 1-3).  By default the block's O and FC2 projections run
+ *     stream-K where whole tiles would leave SM pairs idle: their fp32 partial
+ *     sums over k-ranges are added in k order, with split points fixed by the
+ *     row-tile count and the resident SM-pair count (recorded in
+ *     h3_last_kernel_info as stream-k=<pairs>).
  */
 #ifndef H3_H_
 #define H3_H_
@@ -482,6 +494,15 @@ const char *h3_status_string(h3_status s);
  * s5 h3_operator_trace): kernel id, tile shape, pipeline depth, accumulator
  * type, grid.  Writes a NUL-terminated string of at most len bytes. */
 h3_status h3_last_kernel_info(char *buf, size_t len);
+
+/* Where the first device-side wait that ran out was, as recorded on the
+ * device and read by the most recent h3_sync_check of this process that
+ * returned H3_ERR_TIMEOUT: "none", or the kernel ("gemm", "attention-1q",
+ * "attention-2q", "adaln-table", "rope-qknorm") and the wait (an mbarrier at
+ * a shared-memory byte offset, or a stream-K partial-sum flag).  Diagnostic
+ * only: the pages define no counterpart.  Writes a NUL-terminated string of
+ * at most len bytes; H3_ERR_NULL when buf is NULL or len is 0. */
+h3_status h3_last_error_site(char *buf, size_t len);
 
 /* Library version string. */
 const char *h3_version(void);

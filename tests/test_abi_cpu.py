@@ -81,6 +81,8 @@ def test_host_rejections_return_before_any_launch(lib):
     buf = ctypes.create_string_buffer(64)
     assert L.h3_last_kernel_info(None, 0) == h3.H3_ERR_NULL
     assert L.h3_last_kernel_info(buf, 64) == h3.H3_OK
+    assert L.h3_last_error_site(None, 0) == h3.H3_ERR_NULL
+    assert L.h3_last_error_site(buf, 64) == h3.H3_OK and buf.value == b"none"
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):

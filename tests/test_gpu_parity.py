@@ -7,6 +7,8 @@ end.  Sizes: the tiny H3-shaped block (72 rows: several tiles of every kernel
 but one M tile), a ragged small block (205 rows, odd head count: two M tiles, a
 ragged tail, a half-empty v tile), and the full-width 505-row block.
 """
+import time
+
 import numpy as np
 import pytest
 import torch
@@ -329,8 +331,24 @@ def test_stream_k_lost_flags_time_out(h3, monkeypatch):
     y = torch.empty_like(y_ref)
     h3.h3_block_forward(cfg, h3.make_weights(c.d_w), c.meta(h3), c.d_x, y, ws)
     assert h3.h3_sync_check(timeout_ms=60000) == h3.H3_ERR_TIMEOUT
+    assert h3.h3_last_error_site() == "gemm: stream-K partial-sum flag"
+    # The timeout bit is sticky until h3_sync_check: once the first launch with
+    # lost flags has given up (its waits run out after 2 s, some one after
+    # another), every later kernel of the queue reads the bit at entry and
+    # skips its work.  Without that, each of the eight stream-K launches of
+    # four blocks pays its own limits (26 s were measured before the entry
+    # check existed).
+    cw = [h3.make_weights(c.d_w)] * 4
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    h3.h3_blocks_forward(cfg, cw, c.meta(h3), c.d_x, y, ws)
+    assert h3.h3_sync_check(timeout_ms=60000) == h3.H3_ERR_TIMEOUT
+    elapsed = time.perf_counter() - t0
+    print(f"four blocks with lost stream-K flags: {elapsed:.1f} s until the timeout is reported")
+    assert elapsed < 10.0, f"four blocks with lost flags took {elapsed:.1f} s"
     monkeypatch.delenv("H3_SK_FLAG_TEST")
     assert torch.equal(run_block(h3, c, ws=ws), y_ref)
+    assert h3.h3_sync_check() == 0
 
 
 def test_block_repeatable_and_inplace(h3):
