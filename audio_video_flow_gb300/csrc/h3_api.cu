@@ -183,7 +183,7 @@ h3_status check_cfg(const h3_block_config* c) {
   if (!c) return H3_ERR_NULL;
   if (c->head_dim != 128 || c->rope_freqs_per_axis != 16 || c->rope_channels != 96) return H3_ERR_UNSUPPORTED;
   if (c->dim < 64 || c->dim % 64 || c->dim > 8192) return H3_ERR_UNSUPPORTED;
-  if (c->cond_dim < 64 || c->cond_dim % 64 || c->cond_dim > 2816) return H3_ERR_UNSUPPORTED;
+  if (c->cond_dim < 64 || c->cond_dim % 64 || c->cond_dim > kMaxCondDim) return H3_ERR_UNSUPPORTED;
   if (c->ffn_dim < 128 || c->ffn_dim % 128) return H3_ERR_UNSUPPORTED;
   if (c->n_heads < 1 || c->n_heads > 1024) return H3_ERR_UNSUPPORTED;
   if (!(c->eps > 0.0f) || !std::isfinite(c->eps)) return H3_ERR_SHAPE;
@@ -588,7 +588,7 @@ h3_status check_block_args(const h3_block_config* cfg, const h3_block_weights* w
 // Host code may not pass the array's name to a kernel (on the host it is only
 // a stand-in symbol): its device address is looked up once per device.
 // ---------------------------------------------------------------------------
-constexpr int kNoAllocMaxCond = 2816;
+constexpr int kNoAllocMaxCond = kMaxCondDim;   // every width the configuration check accepts
 void* g_noalloc_scratch[kMaxDevicesApi] = {nullptr};
 std::mutex g_noalloc_mu;
 

@@ -203,6 +203,11 @@ cudaError_t launch_silu_rows(const float* t_cond, int T, int C, __nv_bfloat16* u
 cudaError_t launch_adaln_table(const CUtensorMap& tmW, const CUtensorMap& tmU, const AdalnArgs& a,
                                cudaStream_t stream);
 constexpr int kAdalnRows = 16;   // rows of the u scratch (T <= 16, zero padded)
+// Widest AdaLN conditioning the library takes (the AdaLN-table kernel keeps
+// all of u in shared memory; the configuration check, that kernel's shared
+// memory plan and the no-allocation entry point's static scratch all derive
+// from this one value).
+constexpr int kMaxCondDim = 2816;
 
 // ---------------------------------------------------------------------------
 // attention (tcgen05 flash attention, one 128-row query tile per CTA)

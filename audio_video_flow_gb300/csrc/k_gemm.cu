@@ -1005,7 +1005,8 @@ constexpr int AD_STAGES = 4;
 constexpr int AD_STAGE_BYTES = AD_KPS * A_STAGE_BYTES;
 constexpr int AD_BN = 16;
 constexpr int AD_THREADS = 192;
-constexpr int AD_U_MAX_KB = 44;  // cond_dim <= 44 * 64 = 2816
+constexpr int AD_U_MAX_KB = kMaxCondDim / 64;  // 64-column blocks of u held in shared memory
+static_assert(AD_U_MAX_KB * 64 == kMaxCondDim, "the widest conditioning is a whole number of 64-column blocks");
 constexpr int AD_SMEM = 1024 + AD_U_MAX_KB * 2048 + AD_STAGES * AD_STAGE_BYTES + 256;
 }  // namespace
 
