@@ -333,6 +333,23 @@ constexpr int AT2_THREADS = 384;   // warp 0 TMA Q/K, warp 1 MMA, warp 2 TMA V, 
 constexpr int AT2_SMEM = 1024 + TILE_BYTES * (2 + KST + VST) + 512;
 constexpr float kRescaleThreshold = 8.0f;
 
+// 16 columns of 32-bit per lane: thread t of the warp writes lane (base + t).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_wait16(uint32_t (&r)[16]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                 "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+                 "+r"(r[14]), "+r"(r[15])::"memory");
+}
+
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -530,32 +547,29 @@ __global__ void __launch_bounds__(AT2_THREADS, 1)
       if (!mbar_wait(&s_full[t], (uint32_t)j & 1u, abort_v)) { ok = false; break; }
       tc_fence_after();
       const int valid = S - j * KV_TILE;     // keys of this tile that exist (>= 1)
-      // pass 1: row maximum
-      // eight independent partial maxima (fixed combination order)
+      // all 128 scores of the row, requested before one wait and kept in
+      // registers for both passes (keys past the end of the sequence are set
+      // to -inf: they take no part in the maximum and get probability 0)
+      uint32_t r[4][32];
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) tmem_ld32(s_base + (uint32_t)(q4 * 32), r[q4]);
+      tmem_ld_wait(r[0]);
+      if (valid < KV_TILE) {
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4)
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            if (q4 * 32 + c >= valid) r[q4][c] = __float_as_uint(-INFINITY);
+      }
+      // pass 1: row maximum, eight independent partial maxima (fixed
+      // combination order)
       float mp[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) mp[e] = -INFINITY;
-      const bool full_tile = valid >= KV_TILE;
-      {
-        // all 128 scores of the row requested before one wait
-        uint32_t r[4][32];
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) tmem_ld32(s_base + (uint32_t)(q4 * 32), r[q4]);
+      for (int q4 = 0; q4 < 4; ++q4)
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) tmem_ld_wait(r[q4]);
-        if (full_tile) {
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4)
-#pragma unroll
-            for (int c = 0; c < 32; ++c) mp[c & 7] = fmaxf(mp[c & 7], __uint_as_float(r[q4][c]));
-        } else {
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4)
-#pragma unroll
-            for (int c = 0; c < 32; ++c)
-              mp[c & 7] = fmaxf(mp[c & 7], (q4 * 32 + c < valid) ? __uint_as_float(r[q4][c]) : -INFINITY);
-        }
-      }
+        for (int c = 0; c < 32; ++c) mp[c & 7] = fmaxf(mp[c & 7], __uint_as_float(r[q4][c]));
       const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
                              fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
       const float m_tile = mx * sl2;
@@ -566,57 +580,43 @@ __global__ void __launch_bounds__(AT2_THREADS, 1)
         const float alpha = ex2_approx(m_used - m_new);   // 0 when m_used = -inf
         l_run *= alpha;
         if (j > 0) {
-          // O_t is final for tiles < j (the S_t(j) commit covers P_t V_{j-1})
+          // O_t is final for tiles < j (the S_t(j) commit covers P_t V_{j-1});
+          // 16 columns at a time, as the row's scores stay in registers
 #pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            uint32_t o[32];
-            tmem_ld32(o_base + (uint32_t)(c * 32), o);
-            tmem_ld_wait(o);
+          for (int c = 0; c < 8; ++c) {
+            uint32_t o[16];
+            tmem_ld16(o_base + (uint32_t)(c * 16), o);
+            tmem_ld_wait16(o);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tmem_st32(o_base + (uint32_t)(c * 32), o);
+            for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st16(o_base + (uint32_t)(c * 16), o);
           }
         }
         m_used = m_new;
       }
-      // pass 2: P = 2^(s * scale_log2 - m_used) as bf16 over the S columns
-      float sp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-      for (int h2 = 0; h2 < 2; ++h2) {
-        uint32_t a[32], b[32];
-        tmem_ld32(s_base + (uint32_t)(h2 * 64), a);
-        tmem_ld32(s_base + (uint32_t)(h2 * 64 + 32), b);
-        tmem_ld_wait(a);
-        tmem_ld_wait(b);
-        if (!full_tile) {   // keys past the end of the sequence get probability 0
+      // pass 2: P = 2^(s * scale_log2 - m_used) as bf16 over the S columns,
+      // two keys per packed fp32 FMA; eight partial sums (as float pairs)
+      const float2 sl2x2 = make_float2(sl2, sl2);
+      const float2 negm = make_float2(-m_used, -m_used);
+      float2 sp[4];
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            if (h2 * 64 + c >= valid) a[c] = __float_as_uint(-INFINITY);
-            if (h2 * 64 + 32 + c >= valid) b[c] = __float_as_uint(-INFINITY);
-          }
-        }
-        uint32_t pk[32];
+      for (int e = 0; e < 4; ++e) sp[e] = make_float2(0.0f, 0.0f);
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const float e0 = ex2_approx(__fmaf_rn(__uint_as_float(a[2 * c]), sl2, -m_used));
-          const float e1 = ex2_approx(__fmaf_rn(__uint_as_float(a[2 * c + 1]), sl2, -m_used));
-          sp[(2 * c) & 7] += e0;
-          sp[(2 * c + 1) & 7] += e1;
+      for (int q4 = 0; q4 < 4; ++q4) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {         // keys 32 q4 + 2c and 32 q4 + 2c + 1
+          const float2 z = __ffma2_rn(make_float2(__uint_as_float(r[q4][2 * c]), __uint_as_float(r[q4][2 * c + 1])),
+                                      sl2x2, negm);
+          const float e0 = ex2_approx(z.x), e1 = ex2_approx(z.y);
+          sp[c & 3] = __fadd2_rn(sp[c & 3], make_float2(e0, e1));
           pk[c] = pack_bf16x2(e0, e1);
         }
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const float e0 = ex2_approx(__fmaf_rn(__uint_as_float(b[2 * c]), sl2, -m_used));
-          const float e1 = ex2_approx(__fmaf_rn(__uint_as_float(b[2 * c + 1]), sl2, -m_used));
-          sp[(2 * c) & 7] += e0;
-          sp[(2 * c + 1) & 7] += e1;
-          pk[16 + c] = pack_bf16x2(e0, e1);
-        }
-        // keys [64 h2, 64 h2 + 64) -> packed columns [32 h2, 32 h2 + 32): only
-        // columns this thread has already read are overwritten
-        tmem_st32(s_base + (uint32_t)(h2 * 32), pk);
+        // keys [32 q4, 32 q4 + 32) -> packed columns [16 q4, 16 q4 + 16):
+        // their scores are already in registers
+        tmem_st16(s_base + (uint32_t)(q4 * 16), pk);
       }
-      l_run += ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
+      l_run += ((sp[0].x + sp[0].y) + (sp[1].x + sp[1].y)) + ((sp[2].x + sp[2].y) + (sp[3].x + sp[3].y));
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();

@@ -411,6 +411,59 @@ def test_block_maximum_table_sizes(h3, cond):
     assert_close(to_np(y), c.ref["y"], f"block T=16 cond={cond}")
 
 
+@pytest.mark.parametrize("layout", [(2, (1, 1, 3), 2), (5, (2, 4, 8), 60)], ids=["S7", "S129"])
+def test_block_odd_row_counts(h3, layout):
+    """Odd packed-row counts: 7 rows (one partial tile of every kernel, two
+    rows of each modality's segment) and 129 rows (one row past a 128-row
+    tile: a second, one-row tile in the GEMMs' A operand and in attention)."""
+    n_text, grid, n_audio = layout
+    w = hi.custom_workload(hi.TINY_SHAPE, n_text=n_text, video_grid=grid, n_audio=n_audio, n_timesteps=3,
+                           name=f"odd{n_text + grid[0] * grid[1] * grid[2] + n_audio}")
+    c = Case(w)
+    y = run_block(h3, c)
+    assert_close(to_np(y), c.ref["y"], f"block S={c.S}")
+
+
+def _large_positions(S, seed):
+    """Positions up to the largest the kernels accept (2^24 - 1 on every
+    axis): the extremes, values just below them, and random ones."""
+    rng = np.random.default_rng(seed)
+    top = (1 << 24) - 1
+    pos = rng.integers(0, 1 << 24, size=(S, 3)).astype(np.int32)
+    pos[:8] = [[top, top, top], [top - 1, 0, 5], [0, top, top - 2], [1 << 23, (1 << 23) + 1, top],
+               [top, 1, 2], [12345678, 7654321, 16000000], [0, 0, 0], [1, 1, 1]]
+    return pos
+
+
+@pytest.mark.parametrize("name", ["tiny72", "ragged205"])
+def test_rope_at_large_positions(h3, name):
+    """MM-RoPE at positions near the accepted maximum, where the fp32 angle is
+    large (up to 1.7e7 rad) and the sine and cosine depend on a full-range
+    argument reduction: the QKV epilogue and the standalone kernel against
+    the oracle's cosine and sine (fp64) of the same fp32 angle."""
+    c = get_case(name)
+    H = c.w.shape.n_heads
+    pos = _large_positions(c.S, 21)
+    d_pos = torch.from_numpy(pos).cuda()
+    m = c.d_meta
+    meta = h3.make_meta(m["token_tag"], m["timestep_index"], d_pos, c.d_tc, c.T)
+    q_ref, k_ref, _ = O.qk_norm_rope(c.ref["qkv"], pos, c.np_w["q_norm_g"], c.np_w["k_norm_g"])
+    out = torch.zeros(c.S, H, 3, 128, dtype=torch.bfloat16, device="cuda")
+    h3.h3_qkv_projection(c.cfg(h3), meta, to_bf16(c.ref["h1"]), c.d_w["w_qkv"], None,
+                         c.d_w["q_norm_g"], c.d_w["k_norm_g"], out)
+    assert h3.h3_sync_check() == 0
+    o = to_np(out)
+    assert_close(o[:, :, 0], q_ref, f"qkv epilogue q, large positions [{name}]")
+    assert_close(o[:, :, 1], k_ref, f"qkv epilogue k, large positions [{name}]")
+    buf = to_bf16(c.ref["qkv"].reshape(c.S, H, 3, 128))
+    h3.h3_rope_qknorm(c.cfg(h3), c.S, d_pos, buf[:, :, 0], buf[:, :, 1], H * 384, 384,
+                      c.d_w["q_norm_g"], c.d_w["k_norm_g"])
+    assert h3.h3_sync_check() == 0
+    o = to_np(buf)
+    assert_close(o[:, :, 0], q_ref, f"standalone q, large positions [{name}]")
+    assert_close(o[:, :, 1], k_ref, f"standalone k, large positions [{name}]")
+
+
 def test_single_row_block(h3):
     w = hi.custom_workload(hi.TINY_SHAPE, n_text=1, video_grid=(0, 0, 0), n_audio=0, n_timesteps=1)
     c = Case(w)
