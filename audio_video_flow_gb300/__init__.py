@@ -68,6 +68,8 @@ def lib() -> ctypes.CDLL:
             "h3_block_adaln_side_ctas": (i32, [cfgp, i32]),
             "h3_block_forward": (i32, [cfgp, wp, mp, vp, vp, vp, sz, vp]),
             "h3_block_host_workspace_bytes": (sz, [cfgp, i32, i32]),
+            "h3_blocks_host_workspace_bytes": (sz, [cfgp, i32, i32, i32]),
+            "h3_blocks_workspace_bytes": (sz, [cfgp, i32, i32, i32]),
             "h3_block_forward_host": (i32, [cfgp, wp, mp, vp, vp, vp, sz, vp]),
             "h3_blocks_forward_host": (i32, [cfgp, i32, wp, mp, vp, vp, vp, sz, vp]),
             "h3_block_forward_profiled": (i32, [cfgp, wp, mp, vp, vp, vp, sz, vp, vp, i32]),
@@ -193,6 +195,14 @@ def h3_block_forward(cfg, weights, meta, x_in, x_out, workspace, stream=None) ->
 
 def h3_block_host_workspace_bytes(cfg: BlockConfig, n_rows: int, n_timesteps: int) -> int:
     return int(lib().h3_block_host_workspace_bytes(ctypes.byref(cfg), n_rows, n_timesteps))
+
+
+def h3_blocks_workspace_bytes(cfg: BlockConfig, n_blocks: int, n_rows: int, n_timesteps: int) -> int:
+    return int(lib().h3_blocks_workspace_bytes(ctypes.byref(cfg), n_blocks, n_rows, n_timesteps))
+
+
+def h3_blocks_host_workspace_bytes(cfg: BlockConfig, n_blocks: int, n_rows: int, n_timesteps: int) -> int:
+    return int(lib().h3_blocks_host_workspace_bytes(ctypes.byref(cfg), n_blocks, n_rows, n_timesteps))
 
 
 def h3_block_forward_host(cfg, weights, meta_host, x_host, y_host, workspace, stream=None) -> None:

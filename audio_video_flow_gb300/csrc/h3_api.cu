@@ -310,6 +310,9 @@ void gemm_set_sk(GemmArgs& a, int sk_lane, SkScratch* sk) {
   a.sk_part = sk->part;
   a.sk_flags = sk->flags;
   a.sk_epoch = ++sk->epoch;
+  // H3_GEMM_L2HINT=0 turns the L2 eviction hints of stream-K launches off
+  const char* h = getenv("H3_GEMM_L2HINT");
+  a.l2_hint = (h && h[0] == '0') ? 0 : 1;
   // H3_SK_FLAG_TEST=1 (tests of the failure path only): owners wait for a
   // flag value that no partial writer sets, so every owner's bounded wait
   // runs out and the launch reports H3_ERR_TIMEOUT through h3_sync_check
@@ -451,6 +454,7 @@ int adaln_side_ctas(const h3_block_config& c, int S) {
   const int sms = num_sms(), H = c.n_heads, I = H * 128;
   const GemmPlan pl = gemm_plan(EPI_QKV, S, 3 * I, H, 0);
   const int slots = gemm_pair_slots();
+  if (slots < 1 || sms < 8) return 0;
   const long long tiles = (long long)gemm_m_tiles(S) * pl.num_n;
   const long long waves = (tiles + slots - 1) / slots;
   const int need = 2 * (int)((tiles + waves - 1) / waves);   // fewest CTAs (pairs x 2) with the same wave count
@@ -485,19 +489,24 @@ cudaStream_t copy_stream() {
   return streams[dev];
 }
 
+// table_pre: the block's AdaLN table computed beforehand (a chain's batched
+// tables); the block then starts at norm1.  sk_chain: stream-K scratch whose
+// flags the chain zeroed once and whose epoch runs on across its blocks.
 h3_status block_impl(const h3_block_config* cfg, const h3_block_weights* w, const h3_packed_meta* meta,
                      const void* x_in, void* x_out, void* ws, size_t ws_bytes, cudaStream_t st,
-                     void* const* events, int n_events, cudaEvent_t x_ready = nullptr) {
+                     void* const* events, int n_events, cudaEvent_t x_ready = nullptr,
+                     const void* table_pre = nullptr, SkScratch* sk_chain = nullptr) {
   const int S = meta->n_rows, T = meta->n_timesteps;
   const WsLayout L = ws_layout(*cfg, S, T);
   uint8_t* base = static_cast<uint8_t*>(ws);
   void* u = base + L.u;
-  void* table = base + L.table;
+  void* table = table_pre ? const_cast<void*>(table_pre) : base + L.table;
   void* h = base + L.h;
   void* qkv = base + L.qkv;
   void* o = base + L.o;
   void* x1 = base + L.x1;
-  SkScratch sk{reinterpret_cast<float*>(base + L.sk_part), reinterpret_cast<uint32_t*>(base + L.sk_flags), 0};
+  SkScratch sk_own{reinterpret_cast<float*>(base + L.sk_part), reinterpret_cast<uint32_t*>(base + L.sk_flags), 0};
+  SkScratch& sk = sk_chain ? *sk_chain : sk_own;
   const int I = cfg->n_heads * 128;
   int stage = 0;
   auto mark = [&]() -> h3_status {
@@ -516,25 +525,25 @@ h3_status block_impl(const h3_block_config* cfg, const h3_block_weights* w, cons
   // the caller's stream; chunks 2-5 (two thirds of the weight stream) run on
   // the side stream on the SMs that the QKV GEMM's wave count leaves free,
   // and the caller's stream waits for them before the O projection.
-  s = run_silu(*cfg, meta->t_cond, T, u, st, sk.flags, (int)gemm_sk_flag_words());
-  if (s != H3_OK) return s;
-  const int side_ctas = adaln_side_ctas(*cfg, S);
+  if (!table_pre) {
+    s = run_silu(*cfg, meta->t_cond, T, u, st, sk.flags, (int)gemm_sk_flag_words());
+    if (s != H3_OK) return s;
+  }
+  const int side_ctas = table_pre ? 0 : adaln_side_ctas(*cfg, S);
   cudaStream_t side = side_ctas > 0 ? side_stream() : nullptr;
   cudaEvent_t ev_a = nullptr, ev_b = nullptr;
-  if (side) {
-    if (cudaEventCreateWithFlags(&ev_a, cudaEventDisableTiming) != cudaSuccess) return H3_ERR_CUDA;
-    if (cudaEventCreateWithFlags(&ev_b, cudaEventDisableTiming) != cudaSuccess) {
-      cudaEventDestroy(ev_a);
-      return H3_ERR_CUDA;
-    }
-  }
   struct EventGuard {
-    cudaEvent_t a, b;
+    cudaEvent_t* e[2];
     ~EventGuard() {
-      if (a) cudaEventDestroy(a);
-      if (b) cudaEventDestroy(b);
+      for (cudaEvent_t* p : e)
+        if (*p) cudaEventDestroy(*p);
     }
-  } guard{ev_a, ev_b};
+  } guard{{&ev_a, &ev_b}};
+  if (side) {
+    if (cudaEventCreateWithFlags(&ev_a, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ev_b, cudaEventDisableTiming) != cudaSuccess)
+      return H3_ERR_CUDA;
+  }
   int qkv_ctas = 0;
   if (side) {
     qkv_ctas = num_sms() - side_ctas;
@@ -544,12 +553,15 @@ h3_status block_impl(const h3_block_config* cfg, const h3_block_weights* w, cons
     if (events && n_events > 8 && events[8] &&
         cudaEventRecord(static_cast<cudaEvent_t>(events[8]), side) != cudaSuccess)
       return H3_ERR_CUDA;
+    // (Launching the gate chunk on its own first, so that the O projection
+    // would not wait for chunks 3-5, measured slower at 505 rows: the QKV
+    // GEMM beside the two side launches took 133 instead of 102 us.)
     if ((s = run_adaln_chunks(*cfg, w->w_ada, w->b_ada, T, table, u, 2, 6, side_ctas, side)) != H3_OK) return s;
     if (events && n_events > 9 && events[9] &&
         cudaEventRecord(static_cast<cudaEvent_t>(events[9]), side) != cudaSuccess)
       return H3_ERR_CUDA;
     if (cudaEventRecord(ev_b, side) != cudaSuccess) return H3_ERR_CUDA;
-  } else {
+  } else if (!table_pre) {
     if ((s = run_adaln_chunks(*cfg, w->w_ada, w->b_ada, T, table, u, 0, 6, 0, st)) != H3_OK) return s;
   }
   if ((s = mark()) != H3_OK) return s;
@@ -566,6 +578,76 @@ h3_status block_impl(const h3_block_config* cfg, const h3_block_weights* w, cons
   H3_TRY(run_ffn_up(*cfg, S, h, w->w_fc1, w->b_fc1, qkv, st));
   H3_TRY(run_resid_gemm(*cfg, *meta, table, 5, qkv, cfg->ffn_dim, w->w_fc2, w->b_fc2, x1, x_out, st, &sk));
 #undef H3_TRY
+  return H3_OK;
+}
+
+// A chain computes the AdaLN tables of all its blocks up front, in one
+// launch per kAdalnBatch blocks, where a block would get no overlap from the
+// side stream (the QKV GEMM keeps every SM busy); the tables then follow the
+// block workspace.  Otherwise each block computes its own table.
+bool chain_batches_tables(const h3_block_config& c, int n_blocks, int S) {
+  return n_blocks > 1 && adaln_side_ctas(c, S) == 0;
+}
+size_t chain_table_bytes(const h3_block_config& c, int64_t T) { return al256((size_t)T * 18 * c.dim * 2); }
+size_t chain_ws_bytes(const h3_block_config& c, int n_blocks, int64_t S, int64_t T) {
+  size_t n = ws_layout(c, S, T).total;
+  if (chain_batches_tables(c, n_blocks, (int)S)) n += (size_t)n_blocks * chain_table_bytes(c, T);
+  return n;
+}
+
+// The blocks w[0 .. n_blocks) in order: x_in -> x_out (block b > 0 reads
+// x_out); x_ready as for block_impl (first block only).
+h3_status chain_impl(const h3_block_config* cfg, int n_blocks, const h3_block_weights* w,
+                     const h3_packed_meta* meta, const void* x_in, void* x_out, void* ws, size_t ws_bytes,
+                     cudaStream_t st, cudaEvent_t x_ready = nullptr) {
+  const int S = meta->n_rows, T = meta->n_timesteps;
+  if (!chain_batches_tables(*cfg, n_blocks, S)) {
+    for (int b = 0; b < n_blocks; ++b) {
+      h3_status s = block_impl(cfg, &w[b], meta, b == 0 ? x_in : x_out, x_out, ws, ws_bytes, st, nullptr, 0,
+                               b == 0 ? x_ready : nullptr);
+      if (s != H3_OK) return s;
+    }
+    return H3_OK;
+  }
+  const WsLayout L = ws_layout(*cfg, S, T);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  uint8_t* tables = base + L.total;
+  const size_t tb = chain_table_bytes(*cfg, T);
+  SkScratch sk{reinterpret_cast<float*>(base + L.sk_part), reinterpret_cast<uint32_t*>(base + L.sk_flags), 0};
+  // u = bf16(SiLU(t_cond)) once (the blocks share t_cond); the same launch
+  // zeroes the stream-K flags, whose epochs then run on across the chain
+  h3_status s = run_silu(*cfg, meta->t_cond, T, base + L.u, st, sk.flags, (int)gemm_sk_flag_words());
+  if (s != H3_OK) return s;
+  CUtensorMap tu;
+  if (!make_tmap_2d(&tu, base + L.u, kAdalnRows, (uint64_t)cfg->cond_dim, (uint64_t)cfg->cond_dim, kAdalnRows))
+    return H3_ERR_CUDA;
+  static thread_local AdalnBatchMaps maps;   // 8 KB: kept off the stack
+  for (int b0 = 0; b0 < n_blocks; b0 += kAdalnBatch) {
+    const int nb = n_blocks - b0 < kAdalnBatch ? n_blocks - b0 : kAdalnBatch;
+    for (int i = 0; i < nb; ++i) {
+      if (!make_tmap_2d(&maps.w[i], w[b0 + i].w_ada, (uint64_t)18 * cfg->dim, (uint64_t)cfg->cond_dim,
+                        (uint64_t)cfg->cond_dim, 128))
+        return H3_ERR_CUDA;
+      maps.bias[i] = static_cast<const __nv_bfloat16*>(w[b0 + i].b_ada);
+    }
+    AdalnArgs a{};
+    a.C = cfg->cond_dim;
+    a.T = T;
+    a.NW = 18 * cfg->dim;
+    a.D = cfg->dim;
+    a.chunk_lo = 0;
+    a.chunk_hi = 6;
+    a.out = reinterpret_cast<__nv_bfloat16*>(tables + (size_t)b0 * tb);
+    a.n_blocks = nb;
+    a.out_block_stride = tb / 2;
+    a.err = device_error_word();
+    if ((s = cuda_st(launch_adaln_tables_batched(maps, tu, a, st))) != H3_OK) return s;
+  }
+  for (int b = 0; b < n_blocks; ++b) {
+    s = block_impl(cfg, &w[b], meta, b == 0 ? x_in : x_out, x_out, ws, ws_bytes, st, nullptr, 0,
+                   b == 0 ? x_ready : nullptr, tables + (size_t)b * tb, &sk);
+    if (s != H3_OK) return s;
+  }
   return H3_OK;
 }
 
@@ -642,9 +724,9 @@ h3_status h3_block_forward(const h3_block_config* cfg, const h3_block_weights* w
 struct HostStaging {
   size_t x, y, tag, tidx, pos, tcond, total;
 };
-HostStaging host_staging(const h3_block_config& c, int64_t S, int64_t T) {
+HostStaging host_staging(const h3_block_config& c, int n_blocks, int64_t S, int64_t T) {
   HostStaging H{};
-  size_t off = ws_layout(c, S, T).total;
+  size_t off = chain_ws_bytes(c, n_blocks, S, T);
   H.x = off;
   off = al256(off + (size_t)S * c.dim * 2);
   H.y = off;
@@ -663,7 +745,18 @@ HostStaging host_staging(const h3_block_config& c, int64_t S, int64_t T) {
 
 size_t h3_block_host_workspace_bytes(const h3_block_config* cfg, int32_t n_rows, int32_t n_timesteps) {
   if (check_cfg(cfg) != H3_OK || n_rows < 1 || n_timesteps < 1 || n_timesteps > 16) return 0;
-  return host_staging(*cfg, n_rows, n_timesteps).total;
+  return host_staging(*cfg, 1, n_rows, n_timesteps).total;
+}
+
+size_t h3_blocks_host_workspace_bytes(const h3_block_config* cfg, int32_t n_blocks, int32_t n_rows,
+                                      int32_t n_timesteps) {
+  if (check_cfg(cfg) != H3_OK || n_blocks < 1 || n_rows < 1 || n_timesteps < 1 || n_timesteps > 16) return 0;
+  return host_staging(*cfg, n_blocks, n_rows, n_timesteps).total;
+}
+
+size_t h3_blocks_workspace_bytes(const h3_block_config* cfg, int32_t n_blocks, int32_t n_rows, int32_t n_timesteps) {
+  if (check_cfg(cfg) != H3_OK || n_blocks < 1 || n_rows < 1 || n_timesteps < 1 || n_timesteps > 16) return 0;
+  return chain_ws_bytes(*cfg, n_blocks, n_rows, n_timesteps);
 }
 
 // The blocks w[0 .. n_blocks) from and to host memory through the staging.
@@ -680,7 +773,7 @@ static h3_status host_forward(const h3_block_config* cfg, int32_t n_blocks, cons
   if (!x_host || !y_host || !workspace) return H3_ERR_NULL;
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return H3_ERR_ALIGN;
   const int S = meta_host->n_rows, T = meta_host->n_timesteps;
-  const HostStaging H = host_staging(*cfg, S, T);
+  const HostStaging H = host_staging(*cfg, n_blocks, S, T);
   if (ws_bytes < H.total) return H3_ERR_WORKSPACE;
   uint8_t* base = static_cast<uint8_t*>(workspace);
   const size_t xb = (size_t)S * cfg->dim * 2;
@@ -720,10 +813,9 @@ static h3_status host_forward(const h3_block_config* cfg, int32_t n_blocks, cons
   const h3_packed_meta m{S, T, reinterpret_cast<const int32_t*>(base + H.tag),
                          reinterpret_cast<const int32_t*>(base + H.tidx), reinterpret_cast<const int32_t*>(base + H.pos),
                          reinterpret_cast<const float*>(base + H.tcond)};
-  for (int b = 0; b < n_blocks; ++b)
-    if ((s = block_impl(cfg, &w[b], &m, base + (b == 0 ? H.x : H.y), base + H.y, workspace, ws_bytes, stream,
-                        nullptr, 0, b == 0 ? guard.ev[1] : nullptr)) != H3_OK)
-      return s;
+  if ((s = chain_impl(cfg, n_blocks, w, &m, base + H.x, base + H.y, workspace, ws_bytes, stream, guard.ev[1])) !=
+      H3_OK)
+    return s;
   return cudaMemcpyAsync(y_host, base + H.y, xb, cudaMemcpyDeviceToHost, stream) == cudaSuccess ? H3_OK
                                                                                                 : H3_ERR_CUDA;
 }
@@ -759,12 +851,8 @@ h3_status h3_blocks_forward(const h3_block_config* cfg, int32_t n_blocks, const 
     h3_status s = check_block_args(cfg, &w[b], meta, x_in, x_out, workspace, ws_bytes);
     if (s != H3_OK) return s;
   }
-  for (int b = 0; b < n_blocks; ++b) {
-    h3_status s = block_impl(cfg, &w[b], meta, b == 0 ? x_in : x_out, x_out, workspace, ws_bytes, stream,
-                             nullptr, 0);
-    if (s != H3_OK) return s;
-  }
-  return H3_OK;
+  if (ws_bytes < chain_ws_bytes(*cfg, n_blocks, meta->n_rows, meta->n_timesteps)) return H3_ERR_WORKSPACE;
+  return chain_impl(cfg, n_blocks, w, meta, x_in, x_out, workspace, ws_bytes, stream);
 }
 
 // ===========================================================================
@@ -786,6 +874,7 @@ h3_status h3_blocks_graph_create(const h3_block_config* cfg, int32_t n_blocks, c
     h3_status s = check_block_args(cfg, &w[b], meta, x_in, x_out, workspace, ws_bytes);
     if (s != H3_OK) return s;
   }
+  if (ws_bytes < chain_ws_bytes(*cfg, n_blocks, meta->n_rows, meta->n_timesteps)) return H3_ERR_WORKSPACE;
   cudaStream_t cap = nullptr;
   if (cudaStreamCreateWithFlags(&cap, cudaStreamNonBlocking) != cudaSuccess) return H3_ERR_CUDA;
   h3_status s = H3_OK;
@@ -793,8 +882,7 @@ h3_status h3_blocks_graph_create(const h3_block_config* cfg, int32_t n_blocks, c
     cudaStreamDestroy(cap);
     return H3_ERR_CUDA;
   }
-  for (int b = 0; b < n_blocks && s == H3_OK; ++b)
-    s = block_impl(cfg, &w[b], meta, b == 0 ? x_in : x_out, x_out, workspace, ws_bytes, cap, nullptr, 0);
+  s = chain_impl(cfg, n_blocks, w, meta, x_in, x_out, workspace, ws_bytes, cap);
   cudaGraph_t g = nullptr;
   const cudaError_t e_end = cudaStreamEndCapture(cap, &g);
   cudaStreamDestroy(cap);

@@ -127,6 +127,7 @@ struct GemmArgs {
   int b_rows;
   int nw1, ncnt1, nw2;
   int l2_pf;             // k-blocks of weight L2 prefetch ahead of the loads (0: none); set by launch_gemm
+  int l2_hint;           // 1: activation tiles loaded evict-last, weight tiles evict-first (set with stream-K)
   // stream-K (sk_units > 0, pairs only): each 256-row tile has a lane of
   // sk_lane CTA pairs; the lane's num_n column tiles x num_k k-blocks,
   // column-tile-major, are cut into sk_lane equal runs.  A run that starts
@@ -194,14 +195,28 @@ struct AdalnArgs {
   int max_ctas;           // 0: one CTA per SM; otherwise at most this many
   int l2_pf;              // stages of weight L2 prefetch ahead of the loads (0: none); set by the launcher
   const float* t_cond;    // [T][C]
-  const __nv_bfloat16* bias;  // [NW] nullable
-  __nv_bfloat16* out;     // [T][NW]
+  const __nv_bfloat16* bias;  // [NW] nullable (one block)
+  __nv_bfloat16* out;     // [T][NW] (block b of a batch at out + b * out_block_stride)
+  int n_blocks;           // blocks of a batched launch (1 otherwise)
+  size_t out_block_stride;  // elements between the tables of consecutive blocks
   uint32_t* err;
 };
+// Weight tensor maps and biases of the blocks of one batched AdaLN-table
+// launch (a kernel parameter; 64 maps are 8 KB).
+constexpr int kAdalnBatch = 64;
+template <int NM>
+struct AdalnMaps {
+  CUtensorMap w[NM];
+  const __nv_bfloat16* bias[NM];
+};
+using AdalnBatchMaps = AdalnMaps<kAdalnBatch>;
 cudaError_t launch_silu_rows(const float* t_cond, int T, int C, __nv_bfloat16* u, uint32_t* zero_words,
                              int n_zero_words, cudaStream_t stream);
 cudaError_t launch_adaln_table(const CUtensorMap& tmW, const CUtensorMap& tmU, const AdalnArgs& a,
                                cudaStream_t stream);
+// All chunks of the tables of a.n_blocks (<= kAdalnBatch) blocks in one launch.
+cudaError_t launch_adaln_tables_batched(const AdalnBatchMaps& maps, const CUtensorMap& tmU, const AdalnArgs& a,
+                                        cudaStream_t stream);
 constexpr int kAdalnRows = 16;   // rows of the u scratch (T <= 16, zero padded)
 // Widest AdaLN conditioning the library takes (the AdaLN-table kernel keeps
 // all of u in shared memory; the configuration check, that kernel's shared

@@ -658,6 +658,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       bool ok = true;
       const uint32_t full0 = mapa_shared(smem_u32(full), 0);   // the even CTA's full[0]
       const uint32_t stage_tx = 2u * (uint32_t)(A_STAGE_BYTES + args.b_rows * BK * 2);   // both CTAs' boxes
+      // stream-K: the activation rows are reused by every column tile of the
+      // lane while each weight k-block is used once per row tile at about the
+      // same time, so activations are kept in L2 ahead of the weight stream
+      const uint64_t pol_a = l2_policy_evict_last(), pol_b = l2_policy_evict_first();
       WorkItem w;
       for (int i = 0; ok && work_item(args, unit, num_units, num_tiles, i, w); ++i) {
         int m_blk, n_blk;
@@ -668,8 +672,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           if (!mbar_wait_cluster(&empty[stage], phase ^ 1u, abort_v)) { ok = false; break; }
           if (leader) mbar_arrive_expect_tx(&full[stage], stage_tx);
           const uint32_t fb = full0 + (uint32_t)stage * 8u;
-          tma_load_2d_pair(sA + stage * A_STAGE_BYTES, &tmA, fb, kb * BK, ra);
-          tma_load_2d_pair(sB + stage * C::B_STAGE_BYTES, &tmB, fb, kb * BK, rb);
+          if (args.l2_hint) {
+            tma_load_2d_pair_hint(sA + stage * A_STAGE_BYTES, &tmA, fb, kb * BK, ra, pol_a);
+            tma_load_2d_pair_hint(sB + stage * C::B_STAGE_BYTES, &tmB, fb, kb * BK, rb, pol_b);
+          } else {
+            tma_load_2d_pair(sA + stage * A_STAGE_BYTES, &tmA, fb, kb * BK, ra);
+            tma_load_2d_pair(sB + stage * C::B_STAGE_BYTES, &tmB, fb, kb * BK, rb);
+          }
           last_phase[stage] = (int)phase;
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
           const int pk = kb + args.l2_pf;
@@ -928,7 +937,7 @@ int gemm_pair_slots() {
       if (cudaOccupancyMaxActiveClusters(&n, gemm_bf16_tc<EPI_PLAIN, 192>, &cfg) != cudaSuccess) n = 0;
     }
     cudaGetLastError();
-    slots[dev] = n > 0 ? n : num_sms() / 2;
+    slots[dev] = n > 0 ? n : (num_sms() / 2 > 0 ? num_sms() / 2 : 1);
   }
   return slots[dev];
 }
@@ -989,9 +998,9 @@ cudaError_t launch_gemm(int epi, int bn, const CUtensorMap& tmA, const CUtensorM
   if (e != cudaSuccess) return e;
   set_kernel_info("gemm_bf16_tc<%s,%d> tcgen05.mma.cta_group::2.kind::f16 pair-tile=%dx%dx%d stages=%d acc=f32 "
                   "tmem=2x%d grid=%d (pairs=%d of %d) tiles=%dx%d k_blocks=%d l2_prefetch=%d stream-k=%d "
-                  "n-widths=%s%d,%d,%d",
+                  "l2-hint=%d n-widths=%s%d,%d,%d",
                   names[epi], bn, 2 * BM, bn, BK, stages, bn, grid, pairs, slots, a.num_m, a.num_n, a.num_k,
-                  a.l2_pf, a.sk_units, a.nw1 ? "balanced:" : "uniform:",
+                  a.l2_pf, a.sk_units, a.l2_hint, a.nw1 ? "balanced:" : "uniform:",
                   a.nw1 ? a.nw1 : bn, a.ncnt1, a.nw2);
   return cudaGetLastError();
 }
@@ -1030,8 +1039,12 @@ __global__ void __launch_bounds__(256) silu_rows_kernel(const float* __restrict_
   }
 }
 
+// NM = 1: one block's table (the weight map and bias in maps[0]); NM =
+// kAdalnBatch: the tables of args.n_blocks blocks, tile t of the launch being
+// tile t % (tiles per block) of block t / (tiles per block).
+template <int NM>
 __global__ void __launch_bounds__(AD_THREADS, 1)
-    adaln_table_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmU,
+    adaln_table_kernel(const __grid_constant__ AdalnMaps<NM> maps, const __grid_constant__ CUtensorMap tmU,
                        const AdalnArgs args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -1070,23 +1083,27 @@ __global__ void __launch_bounds__(AD_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  // tiles of chunks [chunk_lo, chunk_hi) of every modality
+  // tiles of chunks [chunk_lo, chunk_hi) of every modality, of every block
   const int tiles_per_mod = (args.chunk_hi - args.chunk_lo) * args.D / BM;
-  const int num_tiles = 3 * tiles_per_mod;
+  const int tiles_per_blk = 3 * tiles_per_mod;
+  const int num_tiles = tiles_per_blk * (NM == 1 ? 1 : args.n_blocks);
+  auto tile_blk = [&](int tile) { return NM == 1 ? 0 : tile / tiles_per_blk; };
   auto tile_row = [&](int tile) {
-    const int m = tile / tiles_per_mod;
-    return m * 6 * args.D + args.chunk_lo * args.D + (tile - m * tiles_per_mod) * BM;
+    const int lt = NM == 1 ? tile : tile % tiles_per_blk;
+    const int m = lt / tiles_per_mod;
+    return m * 6 * args.D + args.chunk_lo * args.D + (lt - m * tiles_per_mod) * BM;
   };
   const WaitCtl abort_v{abort_flag, args.err, KID_ADALN};
   if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tmW);
     tma_prefetch_desc(&tmU);
     // weights are never written: pull the first tile's into L2 while the
     // previous kernel (the SiLU rows) may still be running
     if ((int)blockIdx.x < num_tiles) {
+      const CUtensorMap* tw = &maps.w[tile_blk(blockIdx.x)];
+      tma_prefetch_desc(tw);
       const int row0 = tile_row(blockIdx.x);
       for (int kb = 0; kb < (AD_STAGES + args.l2_pf) * AD_KPS && kb < nkb; ++kb)
-        tma_prefetch_l2(&tmW, kb * BK, row0);
+        tma_prefetch_l2(tw, kb * BK, row0);
     }
   }
   griddep_wait();
@@ -1110,20 +1127,21 @@ __global__ void __launch_bounds__(AD_THREADS, 1)
       bool ok = true;
       for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
         const int row0 = tile_row(tile);
-        for (int kb = 0; kb < args.l2_pf * AD_KPS && kb < nkb; ++kb) tma_prefetch_l2(&tmW, kb * BK, row0);
+        const CUtensorMap* tw = &maps.w[tile_blk(tile)];
+        for (int kb = 0; kb < args.l2_pf * AD_KPS && kb < nkb; ++kb) tma_prefetch_l2(tw, kb * BK, row0);
         for (int st = 0; st < nst; ++st) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_v)) { ok = false; break; }
           const int k0 = st * AD_KPS;
           const int nb = nkb - k0 < AD_KPS ? nkb - k0 : AD_KPS;
           mbar_arrive_expect_tx(&full[stage], (uint32_t)(nb * A_STAGE_BYTES));
           for (int b = 0; b < nb; ++b)
-            tma_load_2d(sA + stage * AD_STAGE_BYTES + b * A_STAGE_BYTES, &tmW, &full[stage], (k0 + b) * BK,
+            tma_load_2d(sA + stage * AD_STAGE_BYTES + b * A_STAGE_BYTES, tw, &full[stage], (k0 + b) * BK,
                         row0);
           last_phase[stage] = (int)phase;
           if (++stage == AD_STAGES) { stage = 0; phase ^= 1u; }
           for (int b = 0; b < AD_KPS && args.l2_pf > 0; ++b) {
             const int pk = (st + args.l2_pf) * AD_KPS + b;
-            if (pk < nkb) tma_prefetch_l2(&tmW, pk * BK, row0);
+            if (pk < nkb) tma_prefetch_l2(tw, pk * BK, row0);
           }
         }
       }
@@ -1190,10 +1208,12 @@ __global__ void __launch_bounds__(AD_THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[acc]);
       const int n = tile_row(tile) + row;
-      const float b = bias_at(args.bias, n);
+      const int blk = tile_blk(tile);
+      const float b = bias_at(maps.bias[blk], n);
+      __nv_bfloat16* out = args.out + (size_t)blk * args.out_block_stride;
 #pragma unroll
       for (int t = 0; t < AD_BN; ++t) {
-        if (t < args.T) args.out[(size_t)t * args.NW + n] = __float2bfloat16_rn(__uint_as_float(r[t]) + b);
+        if (t < args.T) out[(size_t)t * args.NW + n] = __float2bfloat16_rn(__uint_as_float(r[t]) + b);
       }
     }
   }
@@ -1214,6 +1234,29 @@ cudaError_t launch_silu_rows(const float* t_cond, int T, int C, __nv_bfloat16* u
                        zero_words ? n_zero_words : 0);
 }
 
+static int adaln_l2_prefetch() {
+  // Prefetching the weight stream into L2 ahead of the TMA loads measured
+  // slower on GB300 (6.2 against 6.6 TB/s over the full table, 35 against
+  // 31 us for chunks 0-1 at D = 5376): the ring alone keeps HBM busy.  Only
+  // the first tile's stages are prefetched, before the dependency wait.
+  // H3_ADALN_L2PF=<stages> turns the running prefetch on.
+  const char* pf = getenv("H3_ADALN_L2PF");
+  const int v = pf ? atoi(pf) : 0;
+  return v < 0 || v > 64 ? 0 : v;
+}
+
+template <int NM>
+static cudaError_t launch_adaln_kernel(const AdalnMaps<NM>& maps, const CUtensorMap& tmU, const AdalnArgs& a,
+                                       int grid, int cluster, cudaStream_t stream) {
+  static_assert(tmem_footprint_exclusive(AD_SMEM), "an AdaLN-table CTA must hold its SM's TMEM alone");
+  if (!tmem_exclusive(AD_SMEM)) return cudaErrorNotSupported;
+  cudaError_t e =
+      cudaFuncSetAttribute(adaln_table_kernel<NM>, cudaFuncAttributeMaxDynamicSharedMemorySize, AD_SMEM);
+  if (e != cudaSuccess) return e;
+  return launch_kernel_cluster(adaln_table_kernel<NM>, dim3(grid), dim3(AD_THREADS), AD_SMEM, stream, cluster, maps,
+                               tmU, a);
+}
+
 cudaError_t launch_adaln_table(const CUtensorMap& tmW, const CUtensorMap& tmU, const AdalnArgs& a,
                                cudaStream_t stream) {
   const int tiles = 3 * (a.chunk_hi - a.chunk_lo) * a.D / BM;
@@ -1229,26 +1272,33 @@ cudaError_t launch_adaln_table(const CUtensorMap& tmW, const CUtensorMap& tmU, c
       cluster = 2;
     }
   }
-  // Prefetching the weight stream into L2 ahead of the TMA loads measured
-  // slower on GB300 (6.2 against 6.6 TB/s over the full table, 35 against
-  // 31 us for chunks 0-1 at D = 5376): the ring alone keeps HBM busy.  Only
-  // the first tile's stages are prefetched, before the dependency wait.
-  // H3_ADALN_L2PF=<stages> turns the running prefetch on.
   AdalnArgs a2 = a;
-  const char* pf = getenv("H3_ADALN_L2PF");
-  a2.l2_pf = pf ? atoi(pf) : 0;
-  if (a2.l2_pf < 0 || a2.l2_pf > 64) a2.l2_pf = 0;
-  static_assert(tmem_footprint_exclusive(AD_SMEM), "an AdaLN-table CTA must hold its SM's TMEM alone");
-  if (!tmem_exclusive(AD_SMEM)) return cudaErrorNotSupported;
-  cudaError_t e = cudaFuncSetAttribute(adaln_table_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, AD_SMEM);
-  if (e != cudaSuccess) return e;
-  e = launch_kernel_cluster(adaln_table_kernel, dim3(grid), dim3(AD_THREADS), AD_SMEM, stream, cluster, tmW, tmU,
-                            a2);
+  a2.l2_pf = adaln_l2_prefetch();
+  a2.n_blocks = 1;
+  AdalnMaps<1> maps;
+  maps.w[0] = tmW;
+  maps.bias[0] = a.bias;
+  cudaError_t e = launch_adaln_kernel(maps, tmU, a2, grid, cluster, stream);
   if (e != cudaSuccess) return e;
   set_kernel_info("adaln_table_kernel tcgen05.mma.cta_group::1.kind::f16 tile=%dx%dx%d stages=%dx%d acc=f32 "
                   "tmem=2x%d grid=%d cluster=%d tiles=%d chunks=[%d,%d) k_blocks=%d l2_prefetch=%d stages",
                   BM, AD_BN, BK, AD_STAGES, AD_KPS, AD_BN, grid, cluster, tiles, a.chunk_lo, a.chunk_hi, a.C / BK,
                   a2.l2_pf);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_adaln_tables_batched(const AdalnBatchMaps& maps, const CUtensorMap& tmU, const AdalnArgs& a,
+                                        cudaStream_t stream) {
+  if (a.n_blocks < 1 || a.n_blocks > kAdalnBatch) return cudaErrorInvalidValue;
+  const long long tiles = 3LL * (a.chunk_hi - a.chunk_lo) * a.D / BM * a.n_blocks;
+  const int grid = tiles < num_sms() ? (int)tiles : num_sms();
+  AdalnArgs a2 = a;
+  a2.l2_pf = adaln_l2_prefetch();
+  cudaError_t e = launch_adaln_kernel(maps, tmU, a2, grid, 1, stream);
+  if (e != cudaSuccess) return e;
+  set_kernel_info("adaln_table_kernel<batched> tcgen05.mma.cta_group::1.kind::f16 tile=%dx%dx%d stages=%dx%d "
+                  "acc=f32 tmem=2x%d grid=%d blocks=%d tiles=%lld k_blocks=%d", BM, AD_BN, BK, AD_STAGES, AD_KPS,
+                  AD_BN, grid, a.n_blocks, tiles, a.C / BK);
   return cudaGetLastError();
 }
 

@@ -146,18 +146,24 @@ __global__ void __launch_bounds__(1024) select_rows_kernel(int n, const int32_t*
 
 // ---------------------------------------------------------------------------
 // final AdaLN table: out[t][j] = SiLU(t_cond[t]) . w[j] + b[j], fp32, j < 2D.
-// Each CTA holds u = SiLU(t_cond) [T][C] in shared memory; each warp owns one
-// weight row at a time and streams it with 16-byte loads, four in flight per
-// lane (lane l takes float4 columns l + 32i), keeping T running sums that it
-// reduces over the warp with a fixed xor tree.  Many CTAs per SM keep enough
-// bytes in flight for HBM; the kernel is bound by the 2D x C fp32 weights.
+// Two CTAs per SM, each holding u = SiLU(t_cond) [T][C] in shared memory.  A
+// warp owns one weight row at a time and issues the whole row's 16-byte loads
+// before it multiplies (lane l takes float4 columns l + 32i, at most 22 per
+// lane for C <= 2816), so each resident warp keeps a full row (up to 11 KB) in
+// flight; the T running sums of a lane are reduced over the warp with a fixed
+// xor tree.  The kernel is bound by the 2D x C fp32 weights streamed once.
 // ---------------------------------------------------------------------------
 constexpr int FA_THREADS = 256;
+constexpr int FA_MAX_LOADS = kMaxCondDim / 4 / 32;   // float4 loads per lane per row
+static_assert(FA_MAX_LOADS * 4 * 32 == kMaxCondDim, "a lane's share of the widest row is whole float4s");
 
-__global__ void __launch_bounds__(FA_THREADS) final_adaln_kernel(const float* __restrict__ w,
-                                                                 const float* __restrict__ b,
-                                                                 const float* __restrict__ t_cond, int T, int C,
-                                                                 int rows, float* __restrict__ out) {
+// TT: timestep rows rounded up to a power of two (the unrolled sum loops
+// cover TT rows, so T = 1 compiles to one sum per lane)
+template <int TT>
+__global__ void __launch_bounds__(FA_THREADS, 2) final_adaln_kernel(const float* __restrict__ w,
+                                                                    const float* __restrict__ b,
+                                                                    const float* __restrict__ t_cond, int T, int C,
+                                                                    int rows, float* __restrict__ out) {
   extern __shared__ float u[];   // [T][C]
   griddep_launch_dependents();
   griddep_wait();
@@ -171,35 +177,33 @@ __global__ void __launch_bounds__(FA_THREADS) final_adaln_kernel(const float* __
   const int c4 = C >> 2;
   for (int j = blockIdx.x * nw + warp; j < rows; j += gridDim.x * nw) {
     const float4* wr = reinterpret_cast<const float4*>(w + (size_t)j * C);
-    float acc[16];
+    float4 wv[FA_MAX_LOADS];
 #pragma unroll
-    for (int t = 0; t < 16; ++t) acc[t] = 0.0f;
-    for (int k4 = lane; k4 < c4; k4 += 4 * 32) {
-      float4 wv[4];
+    for (int q = 0; q < FA_MAX_LOADS; ++q) {
+      const int kk = lane + q * 32;
+      wv[q] = kk < c4 ? __ldcs(wr + kk) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float acc[TT];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int kk = k4 + q * 32;
-        wv[q] = kk < c4 ? __ldg(wr + kk) : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
+    for (int t = 0; t < TT; ++t) acc[t] = 0.0f;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int kk = k4 + q * 32;
-        if (kk < c4) {
+    for (int q = 0; q < FA_MAX_LOADS; ++q) {
+      const int kk = lane + q * 32;
+      if (kk < c4) {
 #pragma unroll
-          for (int t = 0; t < 16; ++t) {
-            if (t < T) {
-              const float4 uv = reinterpret_cast<const float4*>(u + t * C)[kk];
-              acc[t] = __fmaf_rn(uv.x, wv[q].x, acc[t]);
-              acc[t] = __fmaf_rn(uv.y, wv[q].y, acc[t]);
-              acc[t] = __fmaf_rn(uv.z, wv[q].z, acc[t]);
-              acc[t] = __fmaf_rn(uv.w, wv[q].w, acc[t]);
-            }
+        for (int t = 0; t < TT; ++t) {
+          if (t < T) {
+            const float4 uv = reinterpret_cast<const float4*>(u + t * C)[kk];
+            acc[t] = __fmaf_rn(uv.x, wv[q].x, acc[t]);
+            acc[t] = __fmaf_rn(uv.y, wv[q].y, acc[t]);
+            acc[t] = __fmaf_rn(uv.z, wv[q].z, acc[t]);
+            acc[t] = __fmaf_rn(uv.w, wv[q].w, acc[t]);
           }
         }
       }
     }
 #pragma unroll
-    for (int t = 0; t < 16; ++t) {
+    for (int t = 0; t < TT; ++t) {
       if (t < T) {
         float a = acc[t];
 #pragma unroll
@@ -211,44 +215,81 @@ __global__ void __launch_bounds__(FA_THREADS) final_adaln_kernel(const float* __
 }
 
 // ---------------------------------------------------------------------------
-// Velocity head.  A CTA takes 64 selected rows and all P columns (P padded to
-// 16 * PT, PT in {2, 4, 6, 8}).  Phase 1: the inverse RMS of each row (fp32,
-// lane partial sums then a fixed xor tree).  Phase 2 walks D in 32-column
-// chunks: the modulated activations a[k][row] = (x * inv) * (1 + scale) +
-// shift and the head chunk w[k][p] are staged in shared memory (16-byte global
-// loads; the next chunk's loads are issued before the current chunk is
-// multiplied), and thread (ty, tx) keeps a 4-row x PT-column register tile,
-// reading 4 rows with one 16-byte and its PT columns with 8-byte shared loads
-// per k, and accumulating in k order.  Rows whose metadata is out of range are
-// reported and left unwritten.
+// Velocity head.  A cluster of OH_KS CTAs takes 128 selected rows and all P
+// columns (P padded to 16 * PT, PT in {2, 4, 6, 8}); CTA rank ks of the
+// cluster owns the ks-th of OH_KS contiguous ranges of the reduction axis D
+// (whole 32-column chunks).
+//   1. Each CTA sums the squares of its range of each row (lane partials in
+//      column order, fixed xor tree); after a cluster barrier every CTA adds
+//      the OH_KS partials in rank order and takes inv = 1/sqrt(ss/D + eps).
+//   2. Each CTA walks its range in 32-column chunks: the modulated
+//      activations a[k][row] = (x * inv) * (1 + scale) + shift and the head
+//      chunk w[k][p] are staged in shared memory (double-buffered; the next
+//      chunk's 16-byte global loads are in flight during the products), and
+//      thread (ty, tx) accumulates an 8-row x PT-column register tile in k
+//      order, reading its 8 rows with two 16-byte and its PT columns with
+//      8-byte shared loads per k.
+//   3. The partial tiles are left in shared memory; after a cluster barrier
+//      rank ks adds, for rows [16 ks, 16 ks + 16) of the tile, the OH_KS
+//      partials in rank order over distributed shared memory, adds the bias
+//      and writes the rows.
+// Every output is therefore the same fixed-order fp32 sum whatever the grid.
+// Rows whose metadata is out of range are reported and left unwritten.
 // ---------------------------------------------------------------------------
-constexpr int OH_ROWS = 64, OH_KC = 32, OH_THREADS = 256;
+constexpr int OH_ROWS = 128, OH_KC = 32, OH_THREADS = 256, OH_KS = 8;
 
 template <int PT>
-__global__ void __launch_bounds__(OH_THREADS) output_head_kernel(const OutputHeadArgs a) {
-  constexpr int PW = 16 * PT;        // padded head width
-  constexpr int WS = PW + 2;         // s_w row stride (even, 2 mod 32)
-  __shared__ __align__(16) float s_a[OH_KC][OH_ROWS];
-  __shared__ __align__(16) float s_w[OH_KC * WS];
+struct OhCfg {
+  static constexpr int PW = 16 * PT;                    // padded head width
+  static constexpr int WS = PW + 2;                     // s_w row stride (even, 2 mod 32)
+  static constexpr int A_FLOATS = OH_KC * OH_ROWS;      // one s_a buffer
+  static constexpr int W_FLOATS = OH_KC * WS;           // one s_w buffer
+  static constexpr int STAGE_FLOATS = 2 * (A_FLOATS + W_FLOATS);
+  static constexpr int TILE_FLOATS = OH_ROWS * PW;      // partial tile for the cluster reduction
+  static constexpr int FLOATS = STAGE_FLOATS > TILE_FLOATS ? STAGE_FLOATS : TILE_FLOATS;
+  static constexpr int SMEM = FLOATS * 4;
+  static constexpr int WSLOTS = (PW * (OH_KC / 4) + OH_THREADS - 1) / OH_THREADS;   // float4 per thread
+};
+
+__device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+template <int PT>
+__global__ void __launch_bounds__(OH_THREADS, 2) output_head_kernel(const OutputHeadArgs a) {
+  using Cf = OhCfg<PT>;
+  constexpr int PW = Cf::PW, WS = Cf::WS;
+  extern __shared__ __align__(16) float oh_smem[];
+  float* s_a = oh_smem;                          // [2][OH_KC][OH_ROWS]
+  float* s_w = oh_smem + 2 * Cf::A_FLOATS;       // [2][OH_KC][WS]
+  float* s_tile = oh_smem;                       // [OH_ROWS][PW] after the main loop
+  __shared__ float s_ss[OH_ROWS];                // this CTA's partial sums of squares
+  __shared__ __align__(16) float s_tab[2][16][2][OH_KC];   // shift / scale slices per timestep row
   __shared__ float s_inv[OH_ROWS];
   __shared__ int s_row[OH_ROWS], s_t[OH_ROWS];
   griddep_launch_dependents();
   griddep_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int i0 = blockIdx.x * OH_ROWS;
+  const int ks = (int)cluster_ctarank();
+  const int i0 = (blockIdx.x / OH_KS) * OH_ROWS;
   const int D = a.D, P = a.P;
+  const int nch = D / OH_KC;
+  const int c_lo = (ks * nch) / OH_KS, c_hi = ((ks + 1) * nch) / OH_KS;   // chunks of this CTA
+  const int k_lo = c_lo * OH_KC, k_hi = c_hi * OH_KC;
   if (threadIdx.x < OH_ROWS) {
     const int i = i0 + (int)threadIdx.x;
     int r = -1, t = 0;
     if (i < a.n_sel) {
       r = a.rows[i];
       if ((unsigned)r >= (unsigned)a.S) {
-        record_error(a.err, DEVERR_INDEX);
+        if (ks == 0) record_error(a.err, DEVERR_INDEX);
         r = -1;
       } else {
         t = a.tidx[r];
         if ((unsigned)t >= (unsigned)a.T) {
-          record_error(a.err, DEVERR_INDEX);
+          if (ks == 0) record_error(a.err, DEVERR_INDEX);
           r = -1;
           t = 0;
         }
@@ -258,13 +299,13 @@ __global__ void __launch_bounds__(OH_THREADS) output_head_kernel(const OutputHea
     s_t[threadIdx.x] = t;
   }
   __syncthreads();
-  // phase 1: inverse RMS, eight rows per warp
+  // 1. partial sums of squares over [k_lo, k_hi), sixteen rows per warp
   for (int rr = warp; rr < OH_ROWS; rr += OH_THREADS / 32) {
     const int r = s_row[rr];
     float ss = 0.0f;
     if (r >= 0) {
-      const uint4* xr = reinterpret_cast<const uint4*>(a.x + (size_t)r * D);
-      for (int c = lane; c < (D >> 3); c += 32) {
+      const uint4* xr = reinterpret_cast<const uint4*>(a.x + (size_t)r * D + k_lo);
+      for (int c = lane; c < ((k_hi - k_lo) >> 3); c += 32) {
         const uint4 q = xr[c];
         const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
@@ -277,24 +318,42 @@ __global__ void __launch_bounds__(OH_THREADS) output_head_kernel(const OutputHea
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    if (lane == 0) s_inv[rr] = 1.0f / sqrtf(ss / (float)D + a.eps);
+    if (lane == 0) s_ss[rr] = ss;
+  }
+  cluster_sync();
+  if (threadIdx.x < OH_ROWS) {
+    const uint32_t my = smem_u32(&s_ss[threadIdx.x]);
+    float ss = 0.0f;
+#pragma unroll
+    for (int q = 0; q < OH_KS; ++q) ss += ld_shared_cluster_f32(mapa_shared(my, (uint32_t)q));
+    s_inv[threadIdx.x] = 1.0f / sqrtf(ss / (float)D + a.eps);
   }
   __syncthreads();
 
-  // staging roles.  activations: row ar = tid / 4, columns ak..ak+7 of the chunk;
-  // head: float4 slots f = tid + 256 e over PW rows x 8 float4 (rows >= P are zero)
-  const int ar = threadIdx.x >> 2, ak = (threadIdx.x & 3) * 8;
+  // 2. staging roles.  activations: row ar = tid / 2, columns ak..ak+15 of the
+  // chunk; head: float4 slots f = tid + 256 e over PW rows x 8 float4 (rows >= P
+  // are zero)
+  const int ar = threadIdx.x >> 1, ak = (threadIdx.x & 1) * 16;
   const int my_row = s_row[ar];
   const float my_inv = s_inv[ar];
-  const float* tab = a.table + (size_t)s_t[ar] * 2 * D;
-  constexpr int WSLOTS = (PW * (OH_KC / 4) + OH_THREADS - 1) / OH_THREADS;
-  auto load_chunk = [&](int k0, uint4& xv, float4 (&sh)[2], float4 (&sc)[2], float4 (&wv)[WSLOTS]) {
+  const int my_t = s_t[ar];
+  constexpr int WSLOTS = Cf::WSLOTS;
+  // the table slice [T][shift, scale][32 columns] of a chunk: one float4 for
+  // each of the first 16 T threads, loaded two chunks ahead
+  const int tb_t = (int)threadIdx.x >> 4, tb_h = ((int)threadIdx.x >> 3) & 1, tb_q = (int)threadIdx.x & 7;
+  const bool tb_on = tb_t < a.T;
+  auto load_tab = [&](int k0) -> float4 {
+    return tb_on ? *reinterpret_cast<const float4*>(a.table + ((size_t)tb_t * 2 + tb_h) * D + k0 + tb_q * 4)
+                 : make_float4(0.f, 0.f, 0.f, 0.f);
+  };
+  auto put_tab = [&](int tbuf, const float4& tv) {
+    if (tb_on) *reinterpret_cast<float4*>(&s_tab[tbuf][tb_t][tb_h][tb_q * 4]) = tv;
+  };
+  auto load_chunk = [&](int k0, uint4 (&xv)[2], float4 (&wv)[WSLOTS]) {
     if (my_row >= 0) {
-      xv = *reinterpret_cast<const uint4*>(a.x + (size_t)my_row * D + k0 + ak);
-      sh[0] = *reinterpret_cast<const float4*>(tab + k0 + ak);
-      sh[1] = *reinterpret_cast<const float4*>(tab + k0 + ak + 4);
-      sc[0] = *reinterpret_cast<const float4*>(tab + D + k0 + ak);
-      sc[1] = *reinterpret_cast<const float4*>(tab + D + k0 + ak + 4);
+      const uint4* xp = reinterpret_cast<const uint4*>(a.x + (size_t)my_row * D + k0 + ak);
+      xv[0] = xp[0];
+      xv[1] = xp[1];
     }
 #pragma unroll
     for (int e = 0; e < WSLOTS; ++e) {
@@ -304,76 +363,111 @@ __global__ void __launch_bounds__(OH_THREADS) output_head_kernel(const OutputHea
                       : make_float4(0.f, 0.f, 0.f, 0.f);
     }
   };
-  auto store_chunk = [&](const uint4& xv, const float4 (&sh)[2], const float4 (&sc)[2],
-                         const float4 (&wv)[WSLOTS]) {
-    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-    const float shv[8] = {sh[0].x, sh[0].y, sh[0].z, sh[0].w, sh[1].x, sh[1].y, sh[1].z, sh[1].w};
-    const float scv[8] = {sc[0].x, sc[0].y, sc[0].z, sc[0].w, sc[1].x, sc[1].y, sc[1].z, sc[1].w};
+  auto store_chunk = [&](int buf, const uint4 (&xv)[2], const float4 (&wv)[WSLOTS]) {
+    float* sa = s_a + buf * Cf::A_FLOATS;
+    float* sw = s_w + buf * Cf::W_FLOATS;
+    const uint32_t xw[8] = {xv[0].x, xv[0].y, xv[0].z, xv[0].w, xv[1].x, xv[1].y, xv[1].z, xv[1].w};
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      float val = 0.0f;
+    for (int g = 0; g < 4; ++g) {
+      float4 sh = make_float4(0.f, 0.f, 0.f, 0.f), sc = sh;
       if (my_row >= 0) {
-        const float xvv = (e & 1) ? bf16_hi(xw[e >> 1]) : bf16_lo(xw[e >> 1]);
-        val = __fmaf_rn(xvv * my_inv, 1.0f + scv[e], shv[e]);
+        sh = *reinterpret_cast<const float4*>(&s_tab[buf][my_t][0][ak + 4 * g]);
+        sc = *reinterpret_cast<const float4*>(&s_tab[buf][my_t][1][ak + 4 * g]);
       }
-      s_a[ak + e][ar] = val;
+      const float shv[4] = {sh.x, sh.y, sh.z, sh.w};
+      const float scv[4] = {sc.x, sc.y, sc.z, sc.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int c = 4 * g + e;
+        float val = 0.0f;
+        if (my_row >= 0) {
+          const float xvv = (c & 1) ? bf16_hi(xw[c >> 1]) : bf16_lo(xw[c >> 1]);
+          val = __fmaf_rn(xvv * my_inv, 1.0f + scv[e], shv[e]);
+        }
+        sa[(ak + c) * OH_ROWS + ar] = val;
+      }
     }
 #pragma unroll
     for (int e = 0; e < WSLOTS; ++e) {
       const int f = (int)threadIdx.x + e * OH_THREADS;
       const int p = f / (OH_KC / 4), kq = f % (OH_KC / 4);
       if (p < PW) {
-        s_w[(kq * 4 + 0) * WS + p] = wv[e].x;
-        s_w[(kq * 4 + 1) * WS + p] = wv[e].y;
-        s_w[(kq * 4 + 2) * WS + p] = wv[e].z;
-        s_w[(kq * 4 + 3) * WS + p] = wv[e].w;
+        sw[(kq * 4 + 0) * WS + p] = wv[e].x;
+        sw[(kq * 4 + 1) * WS + p] = wv[e].y;
+        sw[(kq * 4 + 2) * WS + p] = wv[e].z;
+        sw[(kq * 4 + 3) * WS + p] = wv[e].w;
       }
     }
   };
 
-  const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;   // rows 4ty..4ty+3, columns PT tx..PT tx+PT-1
-  float acc[4][PT];
+  const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;   // rows 8ty..8ty+7, columns PT tx..PT tx+PT-1
+  float acc[8][PT];
 #pragma unroll
-  for (int r4 = 0; r4 < 4; ++r4)
+  for (int r8 = 0; r8 < 8; ++r8)
 #pragma unroll
-    for (int c = 0; c < PT; ++c) acc[r4][c] = 0.0f;
-  uint4 xv = make_uint4(0u, 0u, 0u, 0u);
-  float4 sh[2], sc[2], wv[WSLOTS];
-  load_chunk(0, xv, sh, sc, wv);
-  for (int k0 = 0; k0 < D; k0 += OH_KC) {
-    store_chunk(xv, sh, sc, wv);
-    __syncthreads();
-    if (k0 + OH_KC < D) load_chunk(k0 + OH_KC, xv, sh, sc, wv);   // in flight during the products
-#pragma unroll 8
+    for (int c = 0; c < PT; ++c) acc[r8][c] = 0.0f;
+  uint4 xv[2] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
+  float4 wv[WSLOTS];
+  float4 tv = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (k_lo < k_hi) put_tab(0, load_tab(k_lo));
+  if (k_lo + OH_KC < k_hi) put_tab(1, load_tab(k_lo + OH_KC));
+  __syncthreads();
+  if (k_lo < k_hi) {
+    load_chunk(k_lo, xv, wv);
+    store_chunk(0, xv, wv);
+  }
+  __syncthreads();
+  int buf = 0;
+  for (int k0 = k_lo; k0 < k_hi; k0 += OH_KC) {
+    const bool more = k0 + OH_KC < k_hi;
+    const bool more2 = k0 + 2 * OH_KC < k_hi;
+    if (more) load_chunk(k0 + OH_KC, xv, wv);   // in flight during the products
+    if (more2) tv = load_tab(k0 + 2 * OH_KC);
+    const float* sa = s_a + buf * Cf::A_FLOATS;
+    const float* sw = s_w + buf * Cf::W_FLOATS;
+#pragma unroll 2
     for (int kk = 0; kk < OH_KC; ++kk) {
-      const float4 av = *reinterpret_cast<const float4*>(&s_a[kk][ty * 4]);
+      const float4 a0 = *reinterpret_cast<const float4*>(&sa[kk * OH_ROWS + ty * 8]);
+      const float4 a1 = *reinterpret_cast<const float4*>(&sa[kk * OH_ROWS + ty * 8 + 4]);
       float w[PT];
 #pragma unroll
       for (int m = 0; m < PT / 2; ++m) {
-        const float2 w2 = *reinterpret_cast<const float2*>(&s_w[kk * WS + tx * PT + 2 * m]);
+        const float2 w2 = *reinterpret_cast<const float2*>(&sw[kk * WS + tx * PT + 2 * m]);
         w[2 * m] = w2.x;
         w[2 * m + 1] = w2.y;
       }
-      const float a4[4] = {av.x, av.y, av.z, av.w};
+      const float a8[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
 #pragma unroll
-      for (int r4 = 0; r4 < 4; ++r4)
+      for (int r8 = 0; r8 < 8; ++r8)
 #pragma unroll
-        for (int c = 0; c < PT; ++c) acc[r4][c] = __fmaf_rn(a4[r4], w[c], acc[r4][c]);
+        for (int c = 0; c < PT; ++c) acc[r8][c] = __fmaf_rn(a8[r8], w[c], acc[r8][c]);
     }
+    if (more) store_chunk(buf ^ 1, xv, wv);
+    // the table slice two chunks ahead goes where this chunk's was (last
+    // read by the staging before the previous barrier)
+    if (more2) put_tab(buf, tv);
     __syncthreads();
+    buf ^= 1;
   }
+
+  // 3. partial tile -> shared memory; rank ks reduces its 16 rows over the cluster
 #pragma unroll
-  for (int r4 = 0; r4 < 4; ++r4) {
-    const int rr = ty * 4 + r4;
+  for (int r8 = 0; r8 < 8; ++r8)
+#pragma unroll
+    for (int c = 0; c < PT; ++c) s_tile[(ty * 8 + r8) * PW + tx * PT + c] = acc[r8][c];
+  cluster_sync();
+  constexpr int SLICE = OH_ROWS / OH_KS;
+  for (int e = (int)threadIdx.x; e < SLICE * PW; e += OH_THREADS) {
+    const int rr = ks * SLICE + e / PW, p = e % PW;
+    if (p >= P) continue;
+    const uint32_t my = smem_u32(&s_tile[rr * PW + p]);
+    float v = 0.0f;
+#pragma unroll
+    for (int q = 0; q < OH_KS; ++q) v += ld_shared_cluster_f32(mapa_shared(my, (uint32_t)q));
     const int i = i0 + rr;
-    if (s_row[rr] >= 0 && i < a.n_sel) {
-#pragma unroll
-      for (int c = 0; c < PT; ++c) {
-        const int p = tx * PT + c;
-        if (p < P) a.out[(size_t)i * P + p] = acc[r4][c] + (a.b ? a.b[p] : 0.0f);
-      }
-    }
+    if (s_row[rr] >= 0 && i < a.n_sel) a.out[(size_t)i * P + p] = v + (a.b ? a.b[p] : 0.0f);
   }
+  cluster_sync();   // no CTA leaves while another still reads its shared memory
 }
 
 // ---------------------------------------------------------------------------
@@ -415,34 +509,53 @@ cudaError_t launch_select_rows(int n, const int32_t* tags, int tag, int32_t* row
   return cudaGetLastError();
 }
 
+template <int TT>
+static cudaError_t launch_fa(const float* w, const float* b, const float* t_cond, int T, int C, int rows, float* out,
+                             int grid, int smem, cudaStream_t st) {
+  cudaError_t e = cudaFuncSetAttribute(final_adaln_kernel<TT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  return launch_kernel(final_adaln_kernel<TT>, dim3(grid), dim3(FA_THREADS), (size_t)smem, st, w, b, t_cond, T, C,
+                       rows, out);
+}
+
 cudaError_t launch_final_adaln(const float* w, const float* b, const float* t_cond, int T, int C, int rows,
                                float* out, cudaStream_t st) {
   const int smem = T * C * (int)sizeof(float);
-  cudaError_t e = cudaFuncSetAttribute(final_adaln_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
   const int warps = FA_THREADS / 32;
   int grid = (rows + warps - 1) / warps;
-  if (grid > 8 * num_sms()) grid = 8 * num_sms();
-  e = launch_kernel(final_adaln_kernel, dim3(grid), dim3(FA_THREADS), (size_t)smem, st, w, b, t_cond, T, C, rows,
-                    out);
+  if (grid > 2 * num_sms()) grid = 2 * num_sms();   // two resident CTAs per SM, warps loop over rows
+  cudaError_t e;
+  if (T <= 1) e = launch_fa<1>(w, b, t_cond, T, C, rows, out, grid, smem, st);
+  else if (T <= 2) e = launch_fa<2>(w, b, t_cond, T, C, rows, out, grid, smem, st);
+  else if (T <= 4) e = launch_fa<4>(w, b, t_cond, T, C, rows, out, grid, smem, st);
+  else if (T <= 8) e = launch_fa<8>(w, b, t_cond, T, C, rows, out, grid, smem, st);
+  else e = launch_fa<16>(w, b, t_cond, T, C, rows, out, grid, smem, st);
   if (e != cudaSuccess) return e;
-  set_kernel_info("final_adaln_kernel fp32 warp-per-row T=%d C=%d rows=%d grid=%d", T, C, rows, grid);
+  set_kernel_info("final_adaln_kernel fp32 warp-per-row row-in-flight T=%d C=%d rows=%d grid=%d", T, C, rows, grid);
   return cudaGetLastError();
 }
 
+template <int PT>
+static cudaError_t launch_head(const OutputHeadArgs& a, int clusters, cudaStream_t st) {
+  constexpr int smem = OhCfg<PT>::SMEM;
+  cudaError_t e = cudaFuncSetAttribute(output_head_kernel<PT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  return launch_kernel_cluster(output_head_kernel<PT>, dim3(clusters * OH_KS), dim3(OH_THREADS), smem, st, OH_KS, a);
+}
+
 cudaError_t launch_output_head(const OutputHeadArgs& a, cudaStream_t st) {
-  const int grid = (a.n_sel + OH_ROWS - 1) / OH_ROWS;
+  const int clusters = (a.n_sel + OH_ROWS - 1) / OH_ROWS;
   const int pt = a.P <= 32 ? 2 : (a.P <= 64 ? 4 : (a.P <= 96 ? 6 : 8));
   cudaError_t e;
   switch (pt) {
-    case 2: e = launch_kernel(output_head_kernel<2>, dim3(grid), dim3(OH_THREADS), 0, st, a); break;
-    case 4: e = launch_kernel(output_head_kernel<4>, dim3(grid), dim3(OH_THREADS), 0, st, a); break;
-    case 6: e = launch_kernel(output_head_kernel<6>, dim3(grid), dim3(OH_THREADS), 0, st, a); break;
-    default: e = launch_kernel(output_head_kernel<8>, dim3(grid), dim3(OH_THREADS), 0, st, a); break;
+    case 2: e = launch_head<2>(a, clusters, st); break;
+    case 4: e = launch_head<4>(a, clusters, st); break;
+    case 6: e = launch_head<6>(a, clusters, st); break;
+    default: e = launch_head<8>(a, clusters, st); break;
   }
   if (e != cudaSuccess) return e;
-  set_kernel_info("output_head_kernel<%d> fp32 rows/cta=%d k_chunk=%d reg-tile=4x%d P=%d rows=%d", pt, OH_ROWS,
-                  OH_KC, pt, a.P, a.n_sel);
+  set_kernel_info("output_head_kernel<%d> fp32 rows/cluster=%d k-split=%d (cluster, rank-order sums) k_chunk=%d "
+                  "reg-tile=8x%d P=%d rows=%d", pt, OH_ROWS, OH_KS, OH_KC, pt, a.P, a.n_sel);
   return cudaGetLastError();
 }
 

@@ -176,7 +176,10 @@ h3_status h3_block_forward_host(const h3_block_config *cfg, const h3_block_weigh
                                 const h3_packed_meta *meta_host, const void *x_host, void *y_host,
                                 void *workspace, size_t ws_bytes, cudaStream_t stream);
 /* The same for the chain w[0 .. n_blocks) of h3_blocks_forward: one copy in,
- * the blocks in order on the device, one copy out. */
+ * the blocks in order on the device, one copy out.  Workspace: at least
+ * h3_blocks_host_workspace_bytes (the chain workspace plus the staging). */
+size_t h3_blocks_host_workspace_bytes(const h3_block_config *cfg, int32_t n_blocks, int32_t n_rows,
+                                      int32_t n_timesteps);
 h3_status h3_blocks_forward_host(const h3_block_config *cfg, int32_t n_blocks, const h3_block_weights *w,
                                  const h3_packed_meta *meta_host, const void *x_host, void *y_host,
                                  void *workspace, size_t ws_bytes, cudaStream_t stream);
@@ -204,8 +207,16 @@ int32_t h3_block_adaln_side_ctas(const h3_block_config *cfg, int32_t n_rows);
 /* A chain of n_blocks blocks (RFC s2 fingerprint row "Transformer layers"; s5
  * ws1_full_h3_transformer, without the refiner and heads): block b reads the
  * output of block b-1 and uses weights w[b] (a HOST array of n_blocks
- * structs of device pointers).  x_out may alias x_in.  Same workspace as one
- * block. */
+ * structs of device pointers).  x_out may alias x_in.  Where a single block
+ * would get no overlap for its AdaLN table (h3_block_adaln_side_ctas is 0,
+ * as for long documents), the chain computes the tables of all its blocks up
+ * front: one SiLU launch and one table launch per 64 blocks, streaming every
+ * block's AdaLN weights once, and each block then starts at norm1.  The
+ * tables are the same numbers either way.  Workspace: device, 256-byte
+ * aligned, at least h3_blocks_workspace_bytes (the block workspace, plus the
+ * chain's tables when it computes them up front); H3_ERR_WORKSPACE below. */
+size_t h3_blocks_workspace_bytes(const h3_block_config *cfg, int32_t n_blocks, int32_t n_rows,
+                                 int32_t n_timesteps);
 h3_status h3_blocks_forward(const h3_block_config *cfg, int32_t n_blocks,
                             const h3_block_weights *w, const h3_packed_meta *meta,
                             const void *x_in, void *x_out, void *workspace, size_t ws_bytes,

@@ -42,6 +42,14 @@ def test_workspace_bytes_and_config_validation(lib):
     assert at_least <= n < at_least + 8 * 256 + 256 * sk_per_pair
     assert h3.h3_block_workspace_bytes(cfg, 0, 12) == 0
     assert h3.h3_block_workspace_bytes(cfg, 10, 17) == 0
+    # a chain needs at least one block's workspace, at most that plus every
+    # block's table; its host variant adds the staging
+    nb = h3.h3_blocks_workspace_bytes(cfg, 50, 505, 12)
+    assert n <= nb <= n + 50 * (12 * 18 * D * 2 + 256)
+    assert h3.h3_blocks_workspace_bytes(cfg, 1, 505, 12) == n
+    assert h3.h3_blocks_host_workspace_bytes(cfg, 50, 505, 12) > nb
+    assert h3.h3_blocks_workspace_bytes(cfg, 0, 505, 12) == 0
+    assert h3.h3_blocks_host_workspace_bytes(cfg, 3, 505, 17) == 0
     for bad in [h3.make_config(5376, 56, 14336, 2688, head_dim=64),
                 h3.make_config(5376 + 32, 56, 14336, 2688),
                 h3.make_config(5376, 56, 14336 + 64, 2688),

@@ -115,7 +115,7 @@ def denoiser(h3):
     acts = hi.activations(shape, S, T, 0, device="cuda")
     wts = [hi.block_weights(shape, 0, b, device="cuda") for b in range(W.n_blocks)]
     cfg = h3.make_config(shape.dim, shape.n_heads, shape.ffn_dim, shape.cond_dim)
-    ws = torch.empty(h3.h3_block_workspace_bytes(cfg, S, T), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(h3.h3_blocks_workspace_bytes(cfg, W.n_blocks, S, T), dtype=torch.uint8, device="cuda")
     cw = [h3.make_weights(w) for w in wts]
     m = _meta(h3, meta, acts["t_cond"])
     yield {"meta": meta, "acts": acts, "wts": wts, "cfg": cfg, "ws": ws, "cw": cw, "m": m}
@@ -198,7 +198,7 @@ def test_tiny_chain_50_blocks(h3):
     meta_d = {k: v.cuda() for k, v in meta.items()}
     tc = acts["t_cond"].cuda()
     m = h3.make_meta(meta_d["token_tag"], meta_d["timestep_index"], meta_d["pos_thw"], tc, T)
-    ws = torch.empty(h3.h3_block_workspace_bytes(cfg, S, T), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(h3.h3_blocks_workspace_bytes(cfg, 50, S, T), dtype=torch.uint8, device="cuda")
     x = acts["x"].cuda()
     y = torch.empty_like(x)
     h3.h3_blocks_forward(cfg, cw, m, x, y, ws)

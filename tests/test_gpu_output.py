@@ -164,6 +164,32 @@ def test_output_heads(h3, wl):
         assert_close(v.cpu().numpy(), ref, f"head {m} {wl}", F32_MAX_E, F32_MEAN_E)
 
 
+@pytest.mark.parametrize("D,P,n_rows", [(512, 48, 300), (512, 128, 129), (640, 7, 77), (192, 96, 140)])
+def test_output_head_widths(h3, D, P, n_rows):
+    """Head widths of every register-tile variant (P up to 32, 64, 96, 128),
+    a residual width whose 32-column chunks do not split evenly over the eight
+    CTAs of a cluster (640: 20 chunks) or leave some of them without chunks
+    (192: 6 chunks), and row counts that end inside a 128-row block."""
+    shape = hi.BlockShape(dim=D, n_heads=1, head_dim=128, ffn_dim=256, cond_dim=128)
+    T = 3
+    g = torch.Generator().manual_seed(D + P)
+    x = (torch.randn(n_rows, D, generator=g)).to(torch.bfloat16)
+    tidx = torch.randint(0, T, (n_rows,), generator=g, dtype=torch.int32)
+    tab = (torch.randn(T, 2, D, generator=g) * 0.3).to(torch.float32)
+    w = (torch.randn(P, D, generator=g) * 0.02).to(torch.float32)
+    b = (torch.randn(P, generator=g) * 0.02).to(torch.float32)
+    sel = torch.sort(torch.randperm(n_rows, generator=g)[: (2 * n_rows) // 3]).values.to(torch.int32)
+    tags = torch.ones(n_rows, dtype=torch.int32)
+    tags[sel.long()] = OO.TAG_VIDEO
+    v = torch.full((sel.numel(), P), float("nan"), dtype=torch.float32, device="cuda")
+    h3.h3_output_head(_cfg(h3, shape), n_rows, sel.numel(), sel.cuda(), tidx.cuda(), T, x.cuda(), tab.cuda(),
+                      w.cuda(), b.cuda(), P, v)
+    assert h3.h3_sync_check() == 0
+    ref = OO.output_head(to_np(x), tags.numpy(), tidx.numpy(), OO.TAG_VIDEO, tab.numpy().astype(np.float64),
+                         w.numpy(), b.numpy())
+    assert_close(v.cpu().numpy(), ref, f"head D={D} P={P}", F32_MAX_E, F32_MEAN_E)
+
+
 def test_output_head_bad_timestep_is_reported(h3):
     w = hi.WORKLOADS["tiny72"]
     shape, S, T = w.shape, w.layout.n_rows, w.n_timesteps

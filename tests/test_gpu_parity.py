@@ -316,6 +316,66 @@ def test_block_forward_host_matches_device(h3):
         h3.h3_block_forward_host(cfg, h3.make_weights(c.d_w), meta_h, x_h, y_h, small)
 
 
+def _chain_case(name, nb, seed=0):
+    w = {"d576": D576}.get(name) or hi.WORKLOADS[name]
+    shape, S, T = w.shape, w.layout.n_rows, w.n_timesteps
+    meta = {k: v.cuda() for k, v in hi.packed_metadata(w.layout, T, seed).items()}
+    acts = hi.activations(shape, S, T, seed, device="cuda")
+    wts = [{k: (v.cuda() if v is not None else None) for k, v in hi.block_weights(shape, seed, b).items()}
+           for b in range(nb)]
+    return w, meta, acts, wts
+
+
+@pytest.mark.parametrize("name,nb", [("d576", 3), ("d576", 70), ("block1824", 2)])
+def test_chain_batched_tables_match_block_calls(h3, name, nb):
+    """Chains whose blocks get no side-stream overlap compute every block's
+    AdaLN table up front (one SiLU launch, one table launch per 64 blocks:
+    70 blocks take two), and at 1824 rows run stream-K residual GEMMs whose
+    flag epochs continue across the chain.  The chain must equal the blocks
+    called one by one bit for bit, through h3_blocks_forward, its CUDA graph
+    and the host-buffer call; a workspace without room for the tables is
+    refused."""
+    w, meta, acts, wts = _chain_case(name, nb)
+    shape, S, T = w.shape, w.layout.n_rows, w.n_timesteps
+    cfg = h3.make_config(shape.dim, shape.n_heads, shape.ffn_dim, shape.cond_dim)
+    assert h3.h3_block_adaln_side_ctas(cfg, S) == 0
+    cw = [h3.make_weights(x) for x in wts]
+    m = h3.make_meta(meta["token_tag"], meta["timestep_index"], meta["pos_thw"], acts["t_cond"], T)
+    nbytes = h3.h3_blocks_workspace_bytes(cfg, nb, S, T)
+    assert nbytes > h3.h3_block_workspace_bytes(cfg, S, T)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    x = acts["x"]
+    y_ref = x.clone()
+    for b in range(nb):
+        h3.h3_block_forward(cfg, cw[b], m, y_ref, y_ref, ws)
+    y = torch.empty_like(x)
+    h3.h3_blocks_forward(cfg, cw, m, x, y, ws)
+    assert h3.h3_sync_check() == 0
+    if name == "block1824":
+        assert "stream-k=0" not in h3.h3_last_kernel_info()
+    assert torch.equal(y, y_ref)
+    g = h3.BlocksGraph(cfg, cw, m, x, y, ws)
+    y.zero_()
+    g.launch()
+    assert h3.h3_sync_check() == 0
+    assert torch.equal(y, y_ref)
+    g.close()
+    wsh = torch.empty(h3.h3_blocks_host_workspace_bytes(cfg, nb, S, T), dtype=torch.uint8, device="cuda")
+    md = {k: v.cpu().pin_memory() for k, v in meta.items()}
+    tc = acts["t_cond"].cpu().pin_memory()
+    meta_h = h3.make_meta(md["token_tag"], md["timestep_index"], md["pos_thw"], tc, T)
+    x_h = x.cpu().pin_memory()
+    y_h = torch.empty_like(x_h).pin_memory()
+    h3.h3_blocks_forward_host(cfg, cw, meta_h, x_h, y_h, wsh)
+    torch.cuda.synchronize()
+    assert h3.h3_sync_check() == 0
+    assert torch.equal(y_h, y_ref.cpu())
+    small = torch.empty(h3.h3_block_workspace_bytes(cfg, S, T), dtype=torch.uint8, device="cuda")
+    with pytest.raises(h3.H3Error) as e:
+        h3.h3_blocks_forward(cfg, cw, m, x, y, small)
+    assert e.value.status == h3.H3_ERR_WORKSPACE
+
+
 def test_stream_k_lost_flags_time_out(h3, monkeypatch):
     """The stream-K hand-off's failure path, without a GPU fault: with
     H3_SK_FLAG_TEST=1 the owners wait for a flag value that nothing sets, so
@@ -339,6 +399,7 @@ def test_stream_k_lost_flags_time_out(h3, monkeypatch):
     # four blocks pays its own limits (26 s were measured before the entry
     # check existed).
     cw = [h3.make_weights(c.d_w)] * 4
+    ws = torch.empty(h3.h3_blocks_workspace_bytes(cfg, 4, c.S, c.T), dtype=torch.uint8, device="cuda")
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     h3.h3_blocks_forward(cfg, cw, c.meta(h3), c.d_x, y, ws)
@@ -384,7 +445,7 @@ def test_block_permutation_equivariance(h3):
 def test_chain_two_blocks(h3):
     c = get_case("tiny72")
     cfg = c.cfg(h3)
-    ws = torch.empty(h3.h3_block_workspace_bytes(cfg, c.S, c.T), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(h3.h3_blocks_workspace_bytes(cfg, 2, c.S, c.T), dtype=torch.uint8, device="cuda")
     y = torch.empty_like(c.d_x)
     wts = h3.make_weights(c.d_w)
     h3.h3_blocks_forward(cfg, [wts, wts], c.meta(h3), c.d_x, y, ws)
@@ -486,7 +547,7 @@ def test_blocks_graph_replay_matches_direct(h3, name, nb):
     cfg = h3.make_config(shape.dim, shape.n_heads, shape.ffn_dim, shape.cond_dim)
     cw = [h3.make_weights(x) for x in wts]
     m = h3.make_meta(meta["token_tag"], meta["timestep_index"], meta["pos_thw"], acts["t_cond"], T)
-    ws = torch.empty(h3.h3_block_workspace_bytes(cfg, S, T), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(h3.h3_blocks_workspace_bytes(cfg, nb, S, T), dtype=torch.uint8, device="cuda")
     x = acts["x"].clone()
     y_direct = torch.empty_like(x)
     h3.h3_blocks_forward(cfg, cw, m, x, y_direct, ws)
