@@ -70,6 +70,7 @@ def lib() -> ctypes.CDLL:
             "h3_block_host_workspace_bytes": (sz, [cfgp, i32, i32]),
             "h3_blocks_host_workspace_bytes": (sz, [cfgp, i32, i32, i32]),
             "h3_blocks_workspace_bytes": (sz, [cfgp, i32, i32, i32]),
+            "h3_blocks_kernel_count": (i32, [cfgp, i32, i32]),
             "h3_block_forward_host": (i32, [cfgp, wp, mp, vp, vp, vp, sz, vp]),
             "h3_blocks_forward_host": (i32, [cfgp, i32, wp, mp, vp, vp, vp, sz, vp]),
             "h3_block_forward_profiled": (i32, [cfgp, wp, mp, vp, vp, vp, sz, vp, vp, i32]),
@@ -181,6 +182,10 @@ def make_meta(token_tag, timestep_index, pos_thw, t_cond=None, n_timesteps: int 
 
 def h3_block_workspace_bytes(cfg: BlockConfig, n_rows: int, n_timesteps: int) -> int:
     return int(lib().h3_block_workspace_bytes(ctypes.byref(cfg), n_rows, n_timesteps))
+
+
+def h3_blocks_kernel_count(cfg: BlockConfig, n_blocks: int, n_rows: int) -> int:
+    return int(lib().h3_blocks_kernel_count(ctypes.byref(cfg), n_blocks, n_rows))
 
 
 def h3_block_adaln_side_ctas(cfg: BlockConfig, n_rows: int) -> int:

@@ -211,7 +211,8 @@ void fill_omega(float* omega, float theta) {
 size_t adaln_scratch_bytes(const h3_block_config& c) { return al256((size_t)kAdalnRows * c.cond_dim * 2); }
 
 struct WsLayout {
-  size_t u, table, h, qkv, o, x1, sk_part, sk_flags, total;
+  size_t u, table, h, qkv, o, x1, sk_part, sk_flags, nrm_cnt, nrm_part, total;
+  size_t zero_words;   // 32-bit words from sk_flags zeroed at the start of a block call
 };
 WsLayout ws_layout(const h3_block_config& c, int64_t S, int64_t T) {
   const size_t D = (size_t)c.dim, I = (size_t)c.n_heads * 128, F = (size_t)c.ffn_dim;
@@ -233,6 +234,14 @@ WsLayout ws_layout(const h3_block_config& c, int64_t S, int64_t T) {
   off = al256(off + gemm_sk_part_bytes());
   L.sk_flags = off;
   off = al256(off + gemm_sk_flag_words() * 4);
+  // fused-norm counters (one per 256-row tile, zeroed with the flags) and
+  // partial sums of squares (per row, two per 256-column tile)
+  const size_t m_tiles = (size_t)((S + 255) / 256), n_tiles = (D + 255) / 256;
+  L.nrm_cnt = off;
+  off = al256(off + m_tiles * 4);
+  L.zero_words = (L.nrm_cnt - L.sk_flags) / 4 + m_tiles;
+  L.nrm_part = off;
+  off = al256(off + m_tiles * 256 * 2 * n_tiles * 4);
   L.total = off;
   return L;
 }
@@ -384,9 +393,43 @@ h3_status run_attention(int S, int H, const void* q, const void* k, const void* 
 // kernel); null for the stand-alone stage, which runs whole tiles only.
 // (The QKV and FC1 GEMMs run whole tiles: at 256 rows, where their last
 // wave is short, stream-K measured no faster over the refiner pass.)
+// The norm + modulation a residual GEMM may emit as well (norm2 after the O
+// projection): the output h, its gain and table chunks.
+struct NormFuse {
+  void* h;
+  const void* gain;
+  int shift, scale;
+};
+
+// Fuse the following norm into a stream-K residual GEMM: off by default,
+// H3_NORM_FUSE=1 in the environment turns it on.  Measured on GB300 it loses:
+// the O projection waits for the last owner of each row tile before any row
+// can be normed, which costs more than the separate norm2 launch it saves
+// (505 rows: O 60.7 -> 75.6 us against norm2 8.6 -> 0; block 0.386 -> 0.398
+// ms; 1824 rows: 1.081 -> 1.122 ms).
+bool norm_fuse_enabled() {
+  const char* e = getenv("H3_NORM_FUSE");
+  return e && e[0] == '1';
+}
+
+// A stream-K residual GEMM with lanes of sk_lane pairs can carry the norm
+// when each pair's run spans few enough tiles (every epilogue warp keeps
+// the four tiles it may own).
+bool norm_fuse_fits(int sk_lane, int num_n, int num_k) {
+  return sk_lane > 0 && norm_fuse_enabled() && (long long)num_n * num_k / sk_lane / num_k + 2 <= 4;
+}
+
+// Whether the block's O projection carries norm2 at S rows on this device.
+bool o_norm_fused(const h3_block_config& c, int S) {
+  const int I = c.n_heads * 128;
+  return norm_fuse_fits(gemm_sk_lane(S, c.dim, I, 256, 0), (c.dim + 255) / 256, I / 64);
+}
+
 h3_status run_resid_gemm(const h3_block_config& c, const h3_packed_meta& m, const void* table, int chunk,
                          const void* act, int K, const void* w, const void* b, const void* x, void* out,
-                         cudaStream_t st, SkScratch* sk = nullptr) {
+                         cudaStream_t st, SkScratch* sk = nullptr, const NormFuse* nf = nullptr,
+                         bool* fused = nullptr) {
+  if (fused) *fused = false;
   const int S = m.n_rows, D = c.dim;
   GemmPlan pl = gemm_plan(EPI_RESID, S, D, 0, 0);
   const int sk_lane = sk ? gemm_sk_lane(S, D, K, 256, 0) : 0;
@@ -410,6 +453,18 @@ h3_status run_resid_gemm(const h3_block_config& c, const h3_packed_meta& m, cons
   a.tag = m.token_tag;
   a.tidx = m.timestep_index;
   if (sk_lane > 0) gemm_set_sk(a, sk_lane, sk);
+  // the fused norm needs every pair resident (stream-K) and runs of at most
+  // two whole tiles plus a partial piece (each warp keeps four owned tiles)
+  if (nf && sk->nrm_cnt && norm_fuse_fits(sk_lane, a.num_n, a.num_k)) {
+    a.nrm_h = static_cast<__nv_bfloat16*>(nf->h);
+    a.nrm_gain = static_cast<const __nv_bfloat16*>(nf->gain);
+    a.nrm_shift = nf->shift;
+    a.nrm_scale = nf->scale;
+    a.nrm_part = sk->nrm_part;
+    a.nrm_cnt = sk->nrm_cnt;
+    a.nrm_target = (++sk->nrm_launches) * 16u * (uint32_t)a.num_n;
+    if (fused) *fused = true;
+  }
   return cuda_st(launch_gemm(EPI_RESID, pl.bn, tA, tB, a, st));
 }
 
@@ -505,7 +560,8 @@ h3_status block_impl(const h3_block_config* cfg, const h3_block_weights* w, cons
   void* qkv = base + L.qkv;
   void* o = base + L.o;
   void* x1 = base + L.x1;
-  SkScratch sk_own{reinterpret_cast<float*>(base + L.sk_part), reinterpret_cast<uint32_t*>(base + L.sk_flags), 0};
+  SkScratch sk_own{reinterpret_cast<float*>(base + L.sk_part), reinterpret_cast<uint32_t*>(base + L.sk_flags), 0,
+                   reinterpret_cast<float*>(base + L.nrm_part), reinterpret_cast<uint32_t*>(base + L.nrm_cnt), 0};
   SkScratch& sk = sk_chain ? *sk_chain : sk_own;
   const int I = cfg->n_heads * 128;
   int stage = 0;
@@ -526,7 +582,7 @@ h3_status block_impl(const h3_block_config* cfg, const h3_block_weights* w, cons
   // the side stream on the SMs that the QKV GEMM's wave count leaves free,
   // and the caller's stream waits for them before the O projection.
   if (!table_pre) {
-    s = run_silu(*cfg, meta->t_cond, T, u, st, sk.flags, (int)gemm_sk_flag_words());
+    s = run_silu(*cfg, meta->t_cond, T, u, st, sk.flags, (int)L.zero_words);
     if (s != H3_OK) return s;
   }
   const int side_ctas = table_pre ? 0 : adaln_side_ctas(*cfg, S);
@@ -573,8 +629,16 @@ h3_status block_impl(const h3_block_config* cfg, const h3_block_weights* w, cons
     H3_TRY(run_attention(S, cfg->n_heads, q, q + 128, q + 256, 3 * I, 384, o, nullptr, st));
   }
   if (side && cudaStreamWaitEvent(st, ev_b, 0) != cudaSuccess) return H3_ERR_CUDA;
-  H3_TRY(run_resid_gemm(*cfg, *meta, table, 2, o, I, w->w_o, w->b_o, x_in, x1, st, &sk));
-  H3_TRY(run_modulate(*cfg, *meta, table, 1, x1, w->norm2_g, h, st));
+  // norm2 + modulation rides in the O projection's epilogue when that GEMM
+  // runs stream-K; otherwise it is its own kernel
+  bool fused = false;
+  const NormFuse nf{h, w->norm2_g, 3, 4};
+  H3_TRY(run_resid_gemm(*cfg, *meta, table, 2, o, I, w->w_o, w->b_o, x_in, x1, st, &sk, &nf, &fused));
+  if (fused) {
+    if ((s = mark()) != H3_OK) return s;
+  } else {
+    H3_TRY(run_modulate(*cfg, *meta, table, 1, x1, w->norm2_g, h, st));
+  }
   H3_TRY(run_ffn_up(*cfg, S, h, w->w_fc1, w->b_fc1, qkv, st));
   H3_TRY(run_resid_gemm(*cfg, *meta, table, 5, qkv, cfg->ffn_dim, w->w_fc2, w->b_fc2, x1, x_out, st, &sk));
 #undef H3_TRY
@@ -613,10 +677,12 @@ h3_status chain_impl(const h3_block_config* cfg, int n_blocks, const h3_block_we
   uint8_t* base = static_cast<uint8_t*>(ws);
   uint8_t* tables = base + L.total;
   const size_t tb = chain_table_bytes(*cfg, T);
-  SkScratch sk{reinterpret_cast<float*>(base + L.sk_part), reinterpret_cast<uint32_t*>(base + L.sk_flags), 0};
+  SkScratch sk{reinterpret_cast<float*>(base + L.sk_part), reinterpret_cast<uint32_t*>(base + L.sk_flags), 0,
+               reinterpret_cast<float*>(base + L.nrm_part), reinterpret_cast<uint32_t*>(base + L.nrm_cnt), 0};
   // u = bf16(SiLU(t_cond)) once (the blocks share t_cond); the same launch
-  // zeroes the stream-K flags, whose epochs then run on across the chain
-  h3_status s = run_silu(*cfg, meta->t_cond, T, base + L.u, st, sk.flags, (int)gemm_sk_flag_words());
+  // zeroes the stream-K flags and fused-norm counters, whose epochs and
+  // counts then run on across the chain
+  h3_status s = run_silu(*cfg, meta->t_cond, T, base + L.u, st, sk.flags, (int)L.zero_words);
   if (s != H3_OK) return s;
   CUtensorMap tu;
   if (!make_tmap_2d(&tu, base + L.u, kAdalnRows, (uint64_t)cfg->cond_dim, (uint64_t)cfg->cond_dim, kAdalnRows))
@@ -704,6 +770,16 @@ extern "C" {
 size_t h3_block_workspace_bytes(const h3_block_config* cfg, int32_t n_rows, int32_t n_timesteps) {
   if (check_cfg(cfg) != H3_OK || n_rows < 1 || n_timesteps < 1 || n_timesteps > 16) return 0;
   return ws_layout(*cfg, n_rows, n_timesteps).total;
+}
+
+int32_t h3_blocks_kernel_count(const h3_block_config* cfg, int32_t n_blocks, int32_t n_rows) {
+  if (check_cfg(cfg) != H3_OK || n_blocks < 1 || n_rows < 1) return 0;
+  const bool side = adaln_side_ctas(*cfg, n_rows) > 0;
+  const bool batched = chain_batches_tables(*cfg, n_blocks, n_rows);
+  // norm1, QKV, attention, O, norm2 (unless fused), FC1, FC2
+  const int stages = 7 - (o_norm_fused(*cfg, n_rows) ? 1 : 0);
+  if (batched) return 1 + (n_blocks + kAdalnBatch - 1) / kAdalnBatch + n_blocks * stages;
+  return n_blocks * (1 + (side ? 2 : 1) + stages);
 }
 
 int32_t h3_block_adaln_side_ctas(const h3_block_config* cfg, int32_t n_rows) {

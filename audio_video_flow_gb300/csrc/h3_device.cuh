@@ -38,6 +38,7 @@ enum : uint32_t {
 };
 // Low 24 bits of the site word for a wait that is not on an mbarrier.
 constexpr uint32_t kSiteStreamKFlag = 0xFFFFFFu;
+constexpr uint32_t kSiteNormCount = 0xFFFFFEu;   // a fused norm's row-tile count
 
 // What a bounded wait consults and where it reports: the CTA's abort flag in
 // shared memory, the device error word (err[0] bits, err[1] site of the first

@@ -141,6 +141,20 @@ struct GemmArgs {
   uint32_t* sk_flags;    // [sk_units][2 CTAs][4 row quadrants][2 column halves], zero before first use
   uint32_t sk_epoch;     // nonzero, distinct for every launch between two zeroings
   uint32_t sk_wait;      // the flag value owners wait for: sk_epoch (see gemm_set_sk for the test hook)
+  // RESID with the following RMSNorm + modulation fused (stream-K launches,
+  // where every pair is resident): each owner warp also stores, per row, the
+  // sum of squares of the bf16 outputs of its column half into nrm_part and
+  // counts itself in nrm_cnt[row tile]; after all its tiles, it waits until
+  // the row tile's count reaches nrm_target and writes
+  //   nrm_h = bf16((out * inv) * gain * (1 + table[scale]) + table[shift]),
+  //   inv = 1 / sqrt(sum of the row's partials in column order / D + eps),
+  // for the columns it owns.
+  __nv_bfloat16* nrm_h;           // [M][D], null when not fused
+  const __nv_bfloat16* nrm_gain;  // [D]
+  int nrm_shift, nrm_scale;       // table chunks of the modulation
+  float* nrm_part;                // [num_m * 256][2 * num_n]
+  uint32_t* nrm_cnt;              // [num_m], zeroed with the stream-K flags
+  uint32_t nrm_target;            // 16 * num_n arrivals per fused launch since that zeroing
   uint32_t* err;
 };
 
@@ -151,6 +165,9 @@ struct SkScratch {
   float* part;
   uint32_t* flags;
   uint32_t epoch;
+  float* nrm_part;        // fused-norm partial sums of squares (see GemmArgs)
+  uint32_t* nrm_cnt;      // fused-norm arrival counters, zeroed with the flags
+  uint32_t nrm_launches;  // fused launches since the zeroing
 };
 size_t gemm_sk_part_bytes();    // partial area for the largest stream-K launch on this GPU
 size_t gemm_sk_flag_words();    // flags for the largest stream-K launch on this GPU

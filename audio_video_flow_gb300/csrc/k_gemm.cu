@@ -220,9 +220,18 @@ __device__ __forceinline__ void epi_plain(const GemmArgs& a, uint32_t tacc, int 
   if (c < c1) plain_chunk<16>(a, tacc + c, m, valid, t.n0 + c);
 }
 
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 template <int NC>
 __device__ __forceinline__ void resid_chunk(const GemmArgs& a, uint32_t tc, int m, bool valid,
-                                            const __nv_bfloat16* gate, int n0) {
+                                            const __nv_bfloat16* gate, int n0, float& ss) {
   uint32_t r[32];
   tmem_ld_chunk<NC>(tc, r);
   if (valid && n0 < a.n_valid) {
@@ -243,13 +252,16 @@ __device__ __forceinline__ void resid_chunk(const GemmArgs& a, uint32_t tc, int 
         const float ylo = __fmaf_rn(bf16_lo(gw[e]), flo, bf16_lo(xw[e]));
         const float yhi = __fmaf_rn(bf16_hi(gw[e]), fhi, bf16_hi(xw[e]));
         ow[e] = pack_bf16x2(ylo, yhi);
+        ss = __fmaf_rn(bf16_lo(ow[e]), bf16_lo(ow[e]), ss);
+        ss = __fmaf_rn(bf16_hi(ow[e]), bf16_hi(ow[e]), ss);
       }
       dst[g] = make_uint4(ow[0], ow[1], ow[2], ow[3]);
     }
   }
 }
 
-__device__ __forceinline__ void epi_resid(const GemmArgs& a, uint32_t tacc, int m, bool valid, NTile t, int half) {
+__device__ __forceinline__ void epi_resid(const GemmArgs& a, uint32_t tacc, int m, bool valid, NTile t, int half,
+                                          int n_blk) {
   const __nv_bfloat16* gate = nullptr;
   if (valid) {
     const int tg = a.tag[m], ti = a.tidx[m];
@@ -262,9 +274,70 @@ __device__ __forceinline__ void epi_resid(const GemmArgs& a, uint32_t tacc, int 
   }
   int c, c1;
   half_range(t.w, half, c, c1);
+  float ss = 0.0f;
 #pragma unroll 1
-  for (; c + 32 <= c1; c += 32) resid_chunk<32>(a, tacc + c, m, valid, gate, t.n0 + c);
-  if (c < c1) resid_chunk<16>(a, tacc + c, m, valid, gate, t.n0 + c);
+  for (; c + 32 <= c1; c += 32) resid_chunk<32>(a, tacc + c, m, valid, gate, t.n0 + c, ss);
+  if (c < c1) resid_chunk<16>(a, tacc + c, m, valid, gate, t.n0 + c, ss);
+  if (a.nrm_h && m < a.M) a.nrm_part[(size_t)(2 * n_blk + half) * (a.num_m * 256) + m] = ss;
+}
+
+// The fused RMSNorm + modulation of one owned tile's column half for the 32
+// rows of this warp (see GemmArgs::nrm_h): waits until every owner warp of
+// the row tile has stored its partial sums; lane l then adds row (row0 + l)'s
+// partials in column order, and the warp walks the 32 rows with lane l on
+// columns 4l..4l+3 of the half (coalesced 8-byte loads and stores).
+__device__ __forceinline__ bool fused_norm(const GemmArgs& a, int m_blk, int n_blk, int row0, int half, int lane,
+                                           const WaitCtl& c) {
+  const uint32_t* cnt = a.nrm_cnt + m_blk;
+  if (ld_acquire_u32(cnt) < a.nrm_target) {
+    const uint64_t t0 = globaltimer();
+    for (uint32_t i = 1;; ++i) {
+      if (ld_acquire_u32(cnt) >= a.nrm_target) break;
+      if ((i & 31u) == 0 && wait_gives_up(c, t0, kSiteNormCount)) return false;
+    }
+  }
+  const int m = row0 + lane;
+  int trow = -1;
+  float inv = 0.0f;
+  if (m < a.M) {
+    const int tg = a.tag[m], ti = a.tidx[m];
+    if ((unsigned)tg <= 2u && (unsigned)ti < (unsigned)a.T) {   // bad rows are reported by the epilogue
+      trow = ti * 3 + tg;
+      const int mp = a.num_m * 256;
+      float ss = 0.0f;
+      for (int j = 0; j < 2 * a.num_n; ++j) ss += a.nrm_part[(size_t)j * mp + m];
+      inv = 1.0f / sqrtf(ss / (float)a.D + a.eps);
+    }
+  }
+  const NTile t = n_tile<EPI_RESID, 256>(a, n_blk);
+  int c0, c1;
+  half_range(t.w, half, c0, c1);
+  const int n = t.n0 + c0 + 4 * lane;
+  const bool on = 4 * lane < c1 - c0 && n < a.n_valid;
+  uint2 gv = make_uint2(0u, 0u);
+  if (on) gv = *reinterpret_cast<const uint2*>(a.nrm_gain + n);
+#pragma unroll 4
+  for (int r = 0; r < 32; ++r) {
+    const int tr = __shfl_sync(0xffffffffu, trow, r);
+    const float iv = __shfl_sync(0xffffffffu, inv, r);
+    if (tr < 0 || !on) continue;
+    const size_t mr = (size_t)(row0 + r);
+    const __nv_bfloat16* trp = a.table + (size_t)tr * 6 * a.D;
+    const uint2 xv = *reinterpret_cast<const uint2*>(a.out + mr * a.ldo + n);
+    const uint2 hv = *reinterpret_cast<const uint2*>(trp + (size_t)a.nrm_shift * a.D + n);
+    const uint2 sv = *reinterpret_cast<const uint2*>(trp + (size_t)a.nrm_scale * a.D + n);
+    const uint32_t xw[2] = {xv.x, xv.y}, gw[2] = {gv.x, gv.y}, hw[2] = {hv.x, hv.y}, sw[2] = {sv.x, sv.y};
+    uint32_t ow[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const float nlo = (bf16_lo(xw[e]) * iv) * bf16_lo(gw[e]);
+      const float nhi = (bf16_hi(xw[e]) * iv) * bf16_hi(gw[e]);
+      ow[e] = pack_bf16x2(__fmaf_rn(nlo, 1.0f + bf16_lo(sw[e]), bf16_lo(hw[e])),
+                          __fmaf_rn(nhi, 1.0f + bf16_hi(sw[e]), bf16_hi(hw[e])));
+    }
+    *reinterpret_cast<uint2*>(a.nrm_h + mr * a.D + n) = make_uint2(ow[0], ow[1]);
+  }
+  return true;
 }
 
 __device__ __forceinline__ void epi_swiglu(const GemmArgs& a, uint32_t tacc, int m, bool valid, int n_blk,
@@ -439,14 +512,6 @@ __device__ __forceinline__ uint32_t* sk_flag(const GemmArgs& a, int unit, uint32
   return a.sk_flags + ((unit * 2 + (int)rank) * 4 + quad) * 2 + half;
 }
 
-__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
 
 // The i-th of the NCH/2 32-column accumulator chunks that the epilogue warps
 // of column half `half` read: the first or second half of the tile, except
@@ -563,7 +628,7 @@ template <int EPI, int BN>
 __device__ __forceinline__ void run_epilogue(const GemmArgs& a, uint32_t tacc, int m, int n_blk, int half) {
   const bool valid = m < a.M;
   if (EPI == EPI_PLAIN) epi_plain(a, tacc, m, valid, n_tile<EPI, BN>(a, n_blk), half);
-  if (EPI == EPI_RESID) epi_resid(a, tacc, m, valid, n_tile<EPI, BN>(a, n_blk), half);
+  if (EPI == EPI_RESID) epi_resid(a, tacc, m, valid, n_tile<EPI, BN>(a, n_blk), half, n_blk);
   if (EPI == EPI_SWIGLU) epi_swiglu(a, tacc, m, valid, n_blk, half);
   if (EPI == EPI_QKV) epi_qkv<BN>(a, tacc, m, valid, n_blk, half);
 }
@@ -743,6 +808,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     const int half = (warp - 2) >> 2;    // column half: warps 2-5 first, 6-9 second
     const int row = q * 32 + lane;
     const uint32_t acc_empty0 = mapa_shared(smem_u32(acc_empty), 0);
+    // fused norm: the tiles this warp owned (a stream-K run holds at most a
+    // few whole tiles; a fourth and later one is not expected, see the host)
+    constexpr int kMaxOwned = 4;
+    int owned_m[kMaxOwned], owned_n[kMaxOwned], n_owned = 0;
     int it = 0;
     WorkItem w;
     for (; work_item(args, unit, num_units, num_tiles, it, w); ++it) {
@@ -764,11 +833,31 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             done = sk_fold_partials<EPI, BN>(args, tacc, unit, rank, q, half, row, lane, w.tile, abort_v);
         }
         if (done) run_epilogue<EPI, BN>(args, tacc, m_blk * 2 * BM + (int)rank * BM + row, n_blk, half);
+        if (EPI == EPI_RESID && done && args.nrm_h) {
+          // partial sums stored: count this warp for its row tile
+          __syncwarp();
+          if (lane == 0) {
+            __threadfence();
+            atomicAdd(args.nrm_cnt + m_blk, 1u);
+          }
+          if (n_owned < kMaxOwned) {
+            owned_m[n_owned] = m_blk;
+            owned_n[n_owned] = n_blk;
+          }
+          ++n_owned;
+        }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(acc_empty0 + (uint32_t)acc * 8u);
       if (!done) break;
+    }
+    if (EPI == EPI_RESID && args.nrm_h) {
+      if (n_owned > kMaxOwned) *abort_v.flag = 1;   // the host keeps runs shorter; never expected
+      for (int i = 0; i < n_owned && i < kMaxOwned && !*abort_v.flag; ++i)
+        if (!fused_norm(args, owned_m[i], owned_n[i], owned_m[i] * 2 * BM + (int)rank * BM + q * 32, half, lane,
+                        abort_v))
+          break;
     }
   }
   tc_fence_before();

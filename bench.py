@@ -33,19 +33,13 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "H3 block fwd TFLOP/s & packed tokens/s (bf16, 1 GB300); % of tensor/HBM roofline"
-def kernels_per_block(shape, S: int) -> int:
-    """SiLU rows, the AdaLN table (two launches when split: chunks 0-1 on the
-    caller's stream, chunks 2-5 on the side stream), the seven stage kernels."""
-    return 10 if adaln_split(shape, S) else 9
-
-
 def launches_per_step(shape, S: int, n_blocks: int) -> int:
-    """Kernels of one h3_blocks_forward call: a chain without side-stream
-    overlap computes all tables up front (one SiLU launch, one table launch
-    per 64 blocks) and each block then launches its seven stage kernels."""
-    if n_blocks > 1 and not adaln_split(shape, S):
-        return 1 + (n_blocks + 63) // 64 + 7 * n_blocks
-    return n_blocks * kernels_per_block(shape, S)
+    """Kernels one h3_blocks_forward call launches (the library's own count)."""
+    import audio_video_flow_gb300 as h3
+    cfg = h3.make_config(shape.dim, shape.n_heads, shape.ffn_dim, shape.cond_dim)
+    return h3.h3_blocks_kernel_count(cfg, n_blocks, S)
+
+
 STAGES = ("adaln_table", "norm1_modulate", "qkv_qknorm_rope", "attention", "out_proj_residual",
           "norm2_modulate", "fc1_swiglu", "fc2_residual")
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant

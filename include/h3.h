@@ -204,6 +204,16 @@ h3_status h3_block_forward_profiled(const h3_block_config *cfg, const h3_block_w
  * identical either way. */
 int32_t h3_block_adaln_side_ctas(const h3_block_config *cfg, int32_t n_rows);
 
+/* How many kernels one h3_blocks_forward call of n_blocks blocks over n_rows
+ * rows launches on the current device (h3_block_forward: n_blocks = 1); 0
+ * for invalid arguments.  Per block: the SiLU rows and the AdaLN table (two
+ * launches when split over the side stream), norm1, QKV, attention, O,
+ * norm2 (not launched when H3_NORM_FUSE=1 in the environment lets an O
+ * projection that runs stream-K carry it in its epilogue), FC1, FC2; a chain that computes its tables up front
+ * launches the SiLU rows once and one table kernel per 64 blocks instead.
+ * A scheduling detail (no counterpart on the pages). */
+int32_t h3_blocks_kernel_count(const h3_block_config *cfg, int32_t n_blocks, int32_t n_rows);
+
 /* A chain of n_blocks blocks (RFC s2 fingerprint row "Transformer layers"; s5
  * ws1_full_h3_transformer, without the refiner and heads): block b reads the
  * output of block b-1 and uses weights w[b] (a HOST array of n_blocks

@@ -290,6 +290,31 @@ def test_block_forward_stream_k(h3, name, units, monkeypatch):
     assert torch.equal(y, run_block(h3, c))
 
 
+@pytest.mark.parametrize("name,units", [("block505", None), ("d576", "12"), ("ragged205", "6")])
+def test_norm2_fused_into_out_projection(h3, name, units, monkeypatch):
+    """With H3_NORM_FUSE=1, where the O projection runs stream-K (every SM
+    pair resident), its epilogue also emits norm2 + modulation: each owner
+    warp stores per-row partial sums of squares of the bf16 residual, counts
+    itself for the row tile, and after its tiles normalises and modulates the
+    columns it owns; the separate norm2 kernel is not launched.  Against the
+    oracle, equal to the default (separate norm2) block within the bound,
+    bitwise repeatable, and one kernel fewer per block."""
+    if units:   # small blocks: stream-K forced over `units` pairs (one k-block or a few per run)
+        monkeypatch.setenv("H3_GEMM_SK_UNITS", units)
+    c = get_case(name)
+    cfg = c.cfg(h3)
+    sep_count = h3.h3_blocks_kernel_count(cfg, 1, c.S)
+    y_sep = run_block(h3, c)
+    monkeypatch.setenv("H3_NORM_FUSE", "1")     # off by default: measured slower
+    assert h3.h3_blocks_kernel_count(cfg, 1, c.S) == sep_count - 1
+    y = run_block(h3, c)
+    assert torch.equal(y, run_block(h3, c))
+    monkeypatch.delenv("H3_NORM_FUSE")
+    lim = (CHAIN_MAX_E, CHAIN_MEAN_E) if name == "block505" else (MAX_E, MEAN_E)
+    assert_close(to_np(y), c.ref["y"], f"block[{name}] norm2 fused", *lim)
+    assert_close(to_np(y), to_np(y_sep), f"block[{name}] fused vs separate norm2", *lim)
+
+
 def test_block_forward_host_matches_device(h3):
     """h3_block_forward_host (pinned host input, metadata and output, copies
     ordered on the stream inside the call) gives the device call's output bit
