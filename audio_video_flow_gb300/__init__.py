@@ -15,11 +15,14 @@ from ctypes import c_float, c_int32, c_int64, c_size_t, c_void_p, c_char_p
 from typing import Dict, Optional, Sequence
 
 PKG_DIR = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(PKG_DIR, "libh3.so")
+# H3_LIBRARY=bounds in the environment loads the bounds-checked build
+# (libh3_bounds.so: every checked global access first tests that it lies in
+# the buffer its call's arguments describe); otherwise the normal build.
+LIB_PATH = os.path.join(PKG_DIR, "libh3_bounds.so" if os.environ.get("H3_LIBRARY") == "bounds" else "libh3.so")
 HEADER = os.path.join(os.path.dirname(PKG_DIR), "include", "h3.h")
 
 H3_OK, H3_ERR_NULL, H3_ERR_SHAPE, H3_ERR_ALIGN, H3_ERR_UNSUPPORTED = 0, 1, 2, 3, 4
-H3_ERR_INDEX, H3_ERR_CUDA, H3_ERR_TIMEOUT, H3_ERR_WORKSPACE = 5, 6, 7, 8
+H3_ERR_INDEX, H3_ERR_CUDA, H3_ERR_TIMEOUT, H3_ERR_WORKSPACE, H3_ERR_BOUNDS = 5, 6, 7, 8, 9
 N_STAGES = 8
 STAGE_NAMES = ("adaln_table", "norm1_modulate", "qkv_qknorm_rope", "attention", "out_proj_residual",
                "norm2_modulate", "fc1_swiglu", "fc2_residual")
@@ -59,7 +62,7 @@ def lib() -> ctypes.CDLL:
     global _lib
     if _lib is None:
         if not os.path.exists(LIB_PATH):
-            raise RuntimeError(f"libh3.so is not built ({LIB_PATH}); run __graft_entry__.build()")
+            raise RuntimeError(f"{os.path.basename(LIB_PATH)} is not built ({LIB_PATH}); run __graft_entry__.build()")
         L = ctypes.CDLL(LIB_PATH)
         i32, sz, vp = c_int32, c_size_t, c_void_p
         cfgp, wp, mp = ctypes.POINTER(BlockConfig), ctypes.POINTER(BlockWeights), ctypes.POINTER(PackedMeta)

@@ -63,7 +63,9 @@ void note_error_site(uint32_t site) {
   const uint32_t k = site >> 24, lo = site & 0xFFFFFFu;
   const char* kn = k < sizeof(names) / sizeof(names[0]) ? names[k] : "unknown";
   std::lock_guard<std::mutex> lk(g_site_mu);
-  if (site == 0)
+  if (k & 0x80u)
+    snprintf(g_site, sizeof(g_site), "bounds: access site %u, element offset %u from the buffer", k & 0x7Fu, lo);
+  else if (site == 0)
     snprintf(g_site, sizeof(g_site), "timeout without a recorded site");
   else if (lo == kSiteStreamKFlag)
     snprintf(g_site, sizeof(g_site), "%s: stream-K partial-sum flag", kn);
@@ -298,6 +300,8 @@ h3_status run_modulate(const h3_block_config& c, const h3_packed_meta& m, const 
   a.chunk_scale = branch == 0 ? 1 : 4;
   a.tag = m.token_tag;
   a.tidx = m.timestep_index;
+  a.x_elems = a.h_elems = (size_t)m.n_rows * c.dim;
+  a.table_elems = (size_t)3 * m.n_timesteps * 6 * c.dim;
   a.eps = c.eps;
   a.h = static_cast<__nv_bfloat16*>(h);
   a.err = device_error_word();
@@ -384,6 +388,8 @@ h3_status run_attention(int S, int H, const void* q, const void* k, const void* 
   a.H = H;
   a.o = static_cast<__nv_bfloat16*>(o);
   a.lse = lse;
+  a.o_elems = (size_t)S * H * 128;
+  a.lse_elems = lse ? (size_t)H * S : 0;
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt(128.0));
   a.err = device_error_word();
   return cuda_st(launch_attention(tq, tk, tv, a, st));
@@ -1159,6 +1165,7 @@ h3_status h3_rope_qknorm(const h3_block_config* cfg, int32_t n_rows, const int32
   a.pos = pos_thw;
   a.eps = cfg->eps;
   fill_omega(a.omega, cfg->rope_theta);
+  a.qk_elems = (size_t)(n_rows - 1) * (size_t)row_stride_elems + (size_t)(a.H - 1) * (size_t)head_stride_elems + 128;
   a.err = device_error_word();
   CUtensorMap tq, tk;
   const uint32_t hb = (uint32_t)rope_qknorm_heads_per_unit(a.H);
@@ -1424,6 +1431,10 @@ h3_status h3_sync_check(cudaStream_t stream, int32_t timeout_ms) {
     note_error_site(words[1]);
     return H3_ERR_TIMEOUT;
   }
+  if (bits & DEVERR_BOUNDS) {
+    note_error_site(words[1]);
+    return H3_ERR_BOUNDS;
+  }
   if (bits & DEVERR_INDEX) return H3_ERR_INDEX;
   return H3_OK;
 }
@@ -1439,6 +1450,7 @@ const char* h3_status_string(h3_status s) {
     case H3_ERR_CUDA: return "CUDA runtime error";
     case H3_ERR_TIMEOUT: return "device wait or stream synchronisation timed out";
     case H3_ERR_WORKSPACE: return "workspace too small";
+    case H3_ERR_BOUNDS: return "bounds-checked build: a kernel access fell outside its buffer";
   }
   return "unknown status";
 }

@@ -14,6 +14,7 @@ namespace h3 {
 enum : uint32_t {
   DEVERR_INDEX = 1u,     // bad tag / timestep index / position
   DEVERR_TIMEOUT = 2u,   // an mbarrier wait gave up
+  DEVERR_BOUNDS = 4u,    // bounds-checked build: a global access outside its buffer
 };
 // The error word lives in global memory; kernels receive its address.
 __device__ __forceinline__ void record_error(uint32_t* err, uint32_t bits) {
@@ -57,6 +58,36 @@ __device__ __forceinline__ uint64_t globaltimer() {
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---------------------------------------------------------------------------
+// Bounds-checked build (compiled with H3_BOUNDS_CHECK=1): each checked global
+// access first tests that its n elements lie inside [base, base + extent),
+// the buffer the call's arguments describe.  An access outside is skipped and
+// reported: DEVERR_BOUNDS in the error word and, if it is the first report,
+// the site word 0x80 | site in the top byte with the element offset from the
+// base (low 24 bits, saturated).  The normal build compiles the test away.
+// ---------------------------------------------------------------------------
+#ifndef H3_BOUNDS_CHECK
+#define H3_BOUNDS_CHECK 0
+#endif
+template <typename T>
+__device__ __forceinline__ bool in_bounds(const T* base, size_t extent, const T* p, size_t n, uint32_t* err,
+                                          uint32_t site) {
+#if H3_BOUNDS_CHECK
+  if (base == nullptr || p < base || p + n > base + extent) {
+    if (err) {
+      atomicOr(err, DEVERR_BOUNDS);
+      const long long off = base ? (long long)(p - base) : 0;
+      const uint32_t lo = off < 0 ? 0xFFFFFFu : (off > 0xFFFFFE ? 0xFFFFFEu : (uint32_t)off);
+      atomicCAS(err + 1, 0u, ((0x80u | (site & 0x7Fu)) << 24) | lo);
+    }
+    return false;
+  }
+#else
+  (void)base; (void)extent; (void)p; (void)n; (void)err; (void)site;
+#endif
+  return true;
 }
 
 // ---------------------------------------------------------------------------

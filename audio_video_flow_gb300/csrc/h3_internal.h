@@ -155,6 +155,9 @@ struct GemmArgs {
   float* nrm_part;                // [num_m * 256][2 * num_n]
   uint32_t* nrm_cnt;              // [num_m], zeroed with the stream-K flags
   uint32_t nrm_target;            // 16 * num_n arrivals per fused launch since that zeroing
+  // extents (elements) for the bounds-checked build: out, resid, the AdaLN
+  // table, positions and the stream-K partial area
+  size_t out_elems, resid_elems, table_elems, pos_elems, sk_part_elems;
   uint32_t* err;
 };
 
@@ -249,6 +252,7 @@ struct AttnArgs {
   __nv_bfloat16* o;       // [S][H*128]
   float* lse;             // [H][S] or null
   float scale_log2;       // log2(e) / sqrt(128)
+  size_t o_elems, lse_elems;   // extents for the bounds-checked build
   uint32_t* err;
 };
 cudaError_t launch_attention(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
@@ -267,6 +271,7 @@ struct ModulateArgs {
   const int32_t* tidx;
   float eps;
   __nv_bfloat16* h;
+  size_t x_elems, table_elems, h_elems;   // extents for the bounds-checked build
   uint32_t* err;
 };
 cudaError_t launch_modulate(const ModulateArgs& a, cudaStream_t stream);
@@ -281,6 +286,7 @@ struct RopeArgs {
   const int32_t* pos;
   float eps;
   float omega[16];
+  size_t qk_elems;        // elements from q (or k) to the end of its last row, for the bounds-checked build
   uint32_t* err;
 };
 // q and k maps: 3-D [S][H][128] views with the caller's strides, box {128, heads per unit, 1}

@@ -289,7 +289,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         uint32_t o[32];
         tmem_ld32(lane_base + 256u + (uint32_t)(c * 32), o);
         tmem_ld_wait(o);
-        if (grow < S) {
+        if (grow < S && in_bounds<__nv_bfloat16>(args.o, args.o_elems,
+                                                 args.o + (size_t)grow * HD + head * 128 + c * 32, 32, args.err, 12)) {
           uint4* dst = reinterpret_cast<uint4*>(args.o + (size_t)grow * HD + head * 128 + c * 32);
 #pragma unroll
           for (int g = 0; g < 4; ++g) {
@@ -301,7 +302,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         }
       }
       if (args.lse != nullptr && grow < S)
-        args.lse[(size_t)head * S + grow] = (m_run + log2f(l_run)) * 0.69314718055994530942f;
+        if (in_bounds<float>(args.lse, args.lse_elems, args.lse + (size_t)head * S + grow, 1, args.err, 13))
+          args.lse[(size_t)head * S + grow] = (m_run + log2f(l_run)) * 0.69314718055994530942f;
     }
   }
   tc_fence_before();
@@ -631,7 +633,8 @@ __global__ void __launch_bounds__(AT2_THREADS, 1)
         uint32_t o[32];
         tmem_ld32(o_base + (uint32_t)(c * 32), o);
         tmem_ld_wait(o);
-        if (grow < S) {
+        if (grow < S && in_bounds<__nv_bfloat16>(args.o, args.o_elems,
+                                                 args.o + (size_t)grow * HD + head * 128 + c * 32, 32, args.err, 12)) {
           uint4* dst = reinterpret_cast<uint4*>(args.o + (size_t)grow * HD + head * 128 + c * 32);
 #pragma unroll
           for (int g = 0; g < 4; ++g) {
@@ -643,7 +646,8 @@ __global__ void __launch_bounds__(AT2_THREADS, 1)
         }
       }
       if (args.lse != nullptr && grow < S)
-        args.lse[(size_t)head * S + grow] = (m_used + log2f(l_run)) * 0.69314718055994530942f;
+        if (in_bounds<float>(args.lse, args.lse_elems, args.lse + (size_t)head * S + grow, 1, args.err, 13))
+          args.lse[(size_t)head * S + grow] = (m_used + log2f(l_run)) * 0.69314718055994530942f;
     }
   }
   tc_fence_before();

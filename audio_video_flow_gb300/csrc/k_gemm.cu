@@ -179,6 +179,11 @@ __device__ __forceinline__ void tmem_ld_chunk(uint32_t taddr, uint32_t (&r)[32])
   }
 }
 
+// bounds-checked build: n output elements at p inside the output buffer
+__device__ __forceinline__ bool out_ok(const GemmArgs& a, const __nv_bfloat16* p, int n, uint32_t site) {
+  return in_bounds<__nv_bfloat16>(a.out, a.out_elems, p, (size_t)n, a.err, site);
+}
+
 template <int NC>
 __device__ __forceinline__ void plain_chunk(const GemmArgs& a, uint32_t tc, int m, bool valid, int n0) {
   uint32_t r[32];
@@ -197,7 +202,7 @@ __device__ __forceinline__ void plain_chunk(const GemmArgs& a, uint32_t tc, int 
           const float hi = __uint_as_float(r[g * 8 + 2 * e + 1]) + bias_at(a.bias, n + 2 * e + 1);
           wp[e] = pack_bf16x2(lo, hi);
         }
-        *reinterpret_cast<uint4*>(dst + g * 8) = w;
+        if (out_ok(a, dst + g * 8, 8, 1)) *reinterpret_cast<uint4*>(dst + g * 8) = w;
       }
     }
   }
@@ -234,7 +239,10 @@ __device__ __forceinline__ void resid_chunk(const GemmArgs& a, uint32_t tc, int 
                                             const __nv_bfloat16* gate, int n0, float& ss) {
   uint32_t r[32];
   tmem_ld_chunk<NC>(tc, r);
-  if (valid && n0 < a.n_valid) {
+  if (valid && n0 < a.n_valid &&
+      in_bounds<__nv_bfloat16>(a.resid, a.resid_elems, a.resid + (size_t)m * a.ldr + n0, NC, a.err, 2) &&
+      in_bounds<__nv_bfloat16>(a.table, a.table_elems, gate + n0, NC, a.err, 3) &&
+      out_ok(a, a.out + (size_t)m * a.ldo + n0, NC, 4)) {
     const uint4* xs = reinterpret_cast<const uint4*>(a.resid + (size_t)m * a.ldr + n0);
     const uint4* gs = reinterpret_cast<const uint4*>(gate + n0);
     uint4* dst = reinterpret_cast<uint4*>(a.out + (size_t)m * a.ldo + n0);
@@ -358,7 +366,7 @@ __device__ __forceinline__ void epi_swiglu(const GemmArgs& a, uint32_t tacc, int
         const float uv = bf16_round(__uint_as_float(u[j]) + bias_at(a.bias, a.F + n0 + j));
         v[j] = (gv / (1.0f + expf(-gv))) * uv;
       }
-      store32_bf16(a.out + (size_t)m * a.ldo + n0, v);
+      if (out_ok(a, a.out + (size_t)m * a.ldo + n0, 32, 5)) store32_bf16(a.out + (size_t)m * a.ldo + n0, v);
     }
   }
 }
@@ -405,8 +413,8 @@ __device__ __forceinline__ void epi_qk_part(const GemmArgs& a, uint32_t tpart, i
         o2[i] = __fmaf_rn(x2, cs, x1 * sn);
       }
       __nv_bfloat16* dst = a.out + (size_t)m * a.ldo + cb;
-      store16_bf16(dst + band * 16, o1);
-      store16_bf16(dst + 48 + band * 16, o2);
+      if (out_ok(a, dst + band * 16, 16, 6)) store16_bf16(dst + band * 16, o1);
+      if (out_ok(a, dst + 48 + band * 16, 16, 7)) store16_bf16(dst + 48 + band * 16, o2);
     }
   }
   uint32_t r[32];
@@ -419,7 +427,7 @@ __device__ __forceinline__ void epi_qk_part(const GemmArgs& a, uint32_t tpart, i
       const float x = bf16_round(__uint_as_float(r[j]) + bias_at(a.bias, cb + 96 + j));
       v[j] = x * inv * __bfloat162float(gain[96 + j]);
     }
-    store32_bf16(a.out + (size_t)m * a.ldo + cb + 96, v);
+    if (out_ok(a, a.out + (size_t)m * a.ldo + cb + 96, 32, 8)) store32_bf16(a.out + (size_t)m * a.ldo + cb + 96, v);
   }
 }
 
@@ -435,7 +443,7 @@ __device__ __forceinline__ void epi_v_head(const GemmArgs& a, uint32_t tpart, in
       float v[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]) + bias_at(a.bias, cb + j);
-      store32_bf16(a.out + (size_t)m * a.ldo + cb, v);
+      if (out_ok(a, a.out + (size_t)m * a.ldo + cb, 32, 9)) store32_bf16(a.out + (size_t)m * a.ldo + cb, v);
     }
   }
 }
@@ -446,6 +454,10 @@ __device__ __forceinline__ void epi_qkv(const GemmArgs& a, uint32_t tacc, int m,
   if (valid) {
 #pragma unroll
     for (int ax = 0; ax < 3; ++ax) {
+      if (!in_bounds<int32_t>(a.pos, a.pos_elems, a.pos + (size_t)m * 3 + ax, 1, a.err, 18)) {
+        valid = false;
+        break;
+      }
       const int p = a.pos[(size_t)m * 3 + ax];
       if ((unsigned)p >= (1u << 24)) {
         record_error(a.err, DEVERR_INDEX);
@@ -541,8 +553,10 @@ __device__ __forceinline__ void sk_store_partial(const GemmArgs& a, uint32_t tac
     tmem_ld_wait(r);
     // [chunk][16-byte group g][row]: one warp store covers 512 contiguous bytes
     uint4* d = reinterpret_cast<uint4*>(slot + (size_t)c * (128 * 32)) + row;
+    if (in_bounds<float>(a.sk_part, a.sk_part_elems, slot + (size_t)c * (128 * 32), 128 * 32, a.err, 10)) {
 #pragma unroll
-    for (int g = 0; g < 8; ++g) d[g * 128] = make_uint4(r[4 * g], r[4 * g + 1], r[4 * g + 2], r[4 * g + 3]);
+      for (int g = 0; g < 8; ++g) d[g * 128] = make_uint4(r[4 * g], r[4 * g + 1], r[4 * g + 2], r[4 * g + 3]);
+    }
   }
   __syncwarp();
   if (lane == 0) {
@@ -589,6 +603,9 @@ __device__ __forceinline__ bool sk_fold_partials(const GemmArgs& a, uint32_t tac
 #pragma unroll 1
   for (int q = unit + 1; q < q_end; ++q) {
     const float* slot = sk_slot(a, q, rank, NCH);
+    // (an out-of-range slot is reported; the bounds-checked build then reads
+    // the first slot instead, so the warp's TMEM accesses stay uniform)
+    if (!in_bounds<float>(a.sk_part, a.sk_part_elems, slot, (size_t)NCH * 128 * 32, a.err, 11)) slot = a.sk_part;
 #pragma unroll 1
     for (int i = 0; i < NCH / 2; i += 2) {
       const int c = sk_chunk<EPI, NCH>(half, i);   // chunks c and c + 1 (pairs stay adjacent)
@@ -1050,6 +1067,12 @@ cudaError_t launch_gemm(int epi, int bn, const CUtensorMap& tmA, const CUtensorM
   // H3_GEMM_L2PF=<k-blocks> overrides it.
   const int stages = bn == 256 ? GemmCfg<256>::STAGES : (bn == 192 ? GemmCfg<192>::STAGES : GemmCfg<128>::STAGES);
   GemmArgs a = args;
+  // buffer extents implied by the arguments (checked by the bounds-checked build)
+  a.out_elems = (size_t)a.M * a.ldo;
+  a.resid_elems = a.resid ? (size_t)a.M * a.ldr : 0;
+  a.table_elems = a.table ? (size_t)3 * a.T * 6 * a.D : 0;
+  a.pos_elems = a.pos ? (size_t)3 * a.M : 0;
+  a.sk_part_elems = gemm_sk_part_bytes() / sizeof(float);
   const char* pf = getenv("H3_GEMM_L2PF");
   const int pf_default = a.num_m <= 16 ? 0 : 2 * stages;
   a.l2_pf = pf ? atoi(pf) : pf_default;

@@ -33,6 +33,11 @@ __global__ void __launch_bounds__(MOD_THREADS) modulate_kernel(const ModulateArg
     return;
   }
   const int nch = a.D >> 3;
+  const __nv_bfloat16* trow_chk = a.table + (size_t)(ti * 3 + tg) * 6 * a.D;
+  if (!in_bounds<__nv_bfloat16>(a.x, a.x_elems, a.x + (size_t)row * a.D, a.D, a.err, 14) ||
+      !in_bounds<__nv_bfloat16>(a.table, a.table_elems, trow_chk, (size_t)6 * a.D, a.err, 15) ||
+      !in_bounds<__nv_bfloat16>(a.h, a.h_elems, a.h + (size_t)row * a.D, a.D, a.err, 16))
+    return;
   const uint4* xr = reinterpret_cast<const uint4*>(a.x + (size_t)row * a.D);
   uint4 xv[MOD_MAXC];
   float ss = 0.0f;
@@ -293,9 +298,9 @@ __global__ void __launch_bounds__(ROPE_THREADS, 1)
               const float2 y = __ffma2_rn(n, cs2[e], __fmul2_rn(other, sn2[e]));
               outw[e] = pack_bf16x2(y.x, y.y);
             }
-            if (j == 0 || second)
-              *reinterpret_cast<uint4*>(gbase + (size_t)row * a.row_stride + (size_t)(h0 + hh[j]) * a.head_stride +
-                                        hl * 8) = make_uint4(outw[0], outw[1], outw[2], outw[3]);
+            __nv_bfloat16* gp = gbase + (size_t)row * a.row_stride + (size_t)(h0 + hh[j]) * a.head_stride + hl * 8;
+            if ((j == 0 || second) && in_bounds<__nv_bfloat16>(gbase, a.qk_elems, gp, 8, a.err, 17))
+              *reinterpret_cast<uint4*>(gp) = make_uint4(outw[0], outw[1], outw[2], outw[3]);
           }
         }
       }

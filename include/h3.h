@@ -61,7 +61,9 @@ typedef enum {
   H3_ERR_INDEX = 5,        /* the device saw a bad tag / timestep index / position */
   H3_ERR_CUDA = 6,         /* a CUDA runtime call failed */
   H3_ERR_TIMEOUT = 7,      /* a device-side wait or h3_sync_check timed out */
-  H3_ERR_WORKSPACE = 8     /* the workspace is smaller than required */
+  H3_ERR_WORKSPACE = 8,    /* the workspace is smaller than required */
+  H3_ERR_BOUNDS = 9        /* bounds-checked build only: a kernel's global access fell outside the
+                              buffer its call's arguments describe (skipped; h3_last_error_site) */
 } h3_status;
 
 /* Block widths (RFC s2, "Omni-Transformer fingerprint").  Supported:

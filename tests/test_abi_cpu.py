@@ -25,7 +25,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for s in range(9):
+    for s in range(10):
         assert h3.status_string(s)
     assert "closed" in h3.status_string(h3.H3_ERR_UNSUPPORTED)
     assert h3.h3_version().startswith("libh3")
