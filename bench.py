@@ -49,14 +49,14 @@ STAGES = ("adaln_table", "norm1_modulate", "qkv_qknorm_rope", "attention", "out_
 # reading q, k, v and writing o once (K/V re-reads hit L2), so the 32,768-
 # and 15,860-row values are the 16,384-row capture scaled by the row count.
 TRAFFIC = {
-    "qkv_qknorm_rope@block505": 252368128,
-    "fc1_swiglu@block505": 332998144,
-    "qkv_qknorm_rope@block1824": 330054656,
-    "fc1_swiglu@block1824": 377669888,
-    "attention@attn4096": 212803072,
-    "attention@attn16384": 918654208,
-    "attention@attn32768": 1837308416,
-    "attention@denoiser15860": 889273422,
+    "qkv_qknorm_rope@block505": 252609792,
+    "fc1_swiglu@block505": 333535232,
+    "qkv_qknorm_rope@block1824": 333443072,
+    "fc1_swiglu@block1824": 378129664,
+    "attention@attn4096": 213996544,
+    "attention@attn16384": 918765312,
+    "attention@attn32768": 1837530624,
+    "attention@denoiser15860": 889380972,
 }
 
 
