@@ -17,16 +17,28 @@
 namespace h3 {
 
 namespace {
-constexpr int MOD_THREADS = 256;
-constexpr int MOD_MAXC = 4;  // 16-byte chunks per thread: D <= 256 * 4 * 8 = 8192
+// The row's sum of squares follows one fixed tree whatever the CTA size: 256
+// virtual threads, virtual thread vt summing 16-byte chunks vt, vt + 256, ...
+// in order, a butterfly over each 32 virtual threads, then the eight warp
+// sums in order.  A CTA runs it with 256 threads (V = 1) for short documents,
+// where each row's latency matters most (505 rows: 8.6 us against 10.5 with
+// 128 threads), or with 128 threads holding two virtual threads each (V = 2)
+// for long ones, where smaller CTAs keep more rows, and so more bytes, in
+// flight per SM (15,860 rows: 75 -> 64 us, 67 -> 79 % of HBM).  Both give
+// the same bits.
+constexpr int MOD_VT = 256;                      // virtual threads per row
+constexpr int MOD_MAXC = 4;                      // chunks per virtual thread: D <= 256 * 4 * 8 = 8192
+constexpr int kModulateLongRows = 4096;
 }  // namespace
 
-__global__ void __launch_bounds__(MOD_THREADS) modulate_kernel(const ModulateArgs a) {
+template <int V>
+__global__ void __launch_bounds__(MOD_VT / V) modulate_kernel(const ModulateArgs a) {
+  constexpr int NT = MOD_VT / V;                 // real threads
   const int row = blockIdx.x;
   griddep_launch_dependents();
   griddep_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  __shared__ float red[MOD_THREADS / 32];
+  __shared__ float red[MOD_VT / 32];
   const int tg = a.tag[row], ti = a.tidx[row];
   if ((unsigned)tg > 2u || (unsigned)ti >= (unsigned)a.T) {
     if (threadIdx.x == 0) record_error(a.err, DEVERR_INDEX);
@@ -39,29 +51,37 @@ __global__ void __launch_bounds__(MOD_THREADS) modulate_kernel(const ModulateArg
       !in_bounds<__nv_bfloat16>(a.h, a.h_elems, a.h + (size_t)row * a.D, a.D, a.err, 16))
     return;
   const uint4* xr = reinterpret_cast<const uint4*>(a.x + (size_t)row * a.D);
-  uint4 xv[MOD_MAXC];
-  float ss = 0.0f;
+  uint4 xv[V][MOD_MAXC];
+  float ss[V];
 #pragma unroll
-  for (int i = 0; i < MOD_MAXC; ++i) {
-    const int c = threadIdx.x + i * MOD_THREADS;
-    if (c < nch) {
-      xv[i] = xr[c];
-      const uint32_t w[4] = {xv[i].x, xv[i].y, xv[i].z, xv[i].w};
+  for (int v = 0; v < V; ++v) {
+    ss[v] = 0.0f;
+    const int vt = threadIdx.x + v * NT;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float lo = bf16_lo(w[e]), hi = bf16_hi(w[e]);
-        ss = __fmaf_rn(lo, lo, ss);
-        ss = __fmaf_rn(hi, hi, ss);
+    for (int i = 0; i < MOD_MAXC; ++i) {
+      const int c = vt + i * MOD_VT;
+      if (c < nch) {
+        xv[v][i] = xr[c];
+        const uint32_t w[4] = {xv[v][i].x, xv[v][i].y, xv[v][i].z, xv[v][i].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float lo = bf16_lo(w[e]), hi = bf16_hi(w[e]);
+          ss[v] = __fmaf_rn(lo, lo, ss[v]);
+          ss[v] = __fmaf_rn(hi, hi, ss[v]);
+        }
       }
     }
   }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-  if (lane == 0) red[warp] = ss;
+  for (int v = 0; v < V; ++v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss[v] += __shfl_xor_sync(0xffffffffu, ss[v], o);
+    if (lane == 0) red[warp + v * (NT / 32)] = ss[v];
+  }
   __syncthreads();
   float tot = 0.0f;
 #pragma unroll
-  for (int w = 0; w < MOD_THREADS / 32; ++w) tot += red[w];
+  for (int w = 0; w < MOD_VT / 32; ++w) tot += red[w];
   const float inv = 1.0f / sqrtf(tot / (float)a.D + a.eps);
 
   const __nv_bfloat16* trow = a.table + (size_t)(ti * 3 + tg) * 6 * a.D;
@@ -70,32 +90,38 @@ __global__ void __launch_bounds__(MOD_THREADS) modulate_kernel(const ModulateArg
   const uint4* gp = reinterpret_cast<const uint4*>(a.gain);
   uint4* hp = reinterpret_cast<uint4*>(a.h + (size_t)row * a.D);
 #pragma unroll
-  for (int i = 0; i < MOD_MAXC; ++i) {
-    const int c = threadIdx.x + i * MOD_THREADS;
-    if (c < nch) {
-      const uint4 gv = gp[c], shv = shp[c], scv = scp[c];
-      const uint32_t xw[4] = {xv[i].x, xv[i].y, xv[i].z, xv[i].w};
-      const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
-      const uint32_t hw[4] = {shv.x, shv.y, shv.z, shv.w};
-      const uint32_t cw[4] = {scv.x, scv.y, scv.z, scv.w};
-      uint32_t ow[4];
+  for (int v = 0; v < V; ++v) {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float nlo = (bf16_lo(xw[e]) * inv) * bf16_lo(gw[e]);
-        const float nhi = (bf16_hi(xw[e]) * inv) * bf16_hi(gw[e]);
-        const float ylo = __fmaf_rn(nlo, 1.0f + bf16_lo(cw[e]), bf16_lo(hw[e]));
-        const float yhi = __fmaf_rn(nhi, 1.0f + bf16_hi(cw[e]), bf16_hi(hw[e]));
-        ow[e] = pack_bf16x2(ylo, yhi);
+    for (int i = 0; i < MOD_MAXC; ++i) {
+      const int c = threadIdx.x + v * NT + i * MOD_VT;
+      if (c < nch) {
+        const uint4 gv = gp[c], shv = shp[c], scv = scp[c];
+        const uint32_t xw[4] = {xv[v][i].x, xv[v][i].y, xv[v][i].z, xv[v][i].w};
+        const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+        const uint32_t hw[4] = {shv.x, shv.y, shv.z, shv.w};
+        const uint32_t cw[4] = {scv.x, scv.y, scv.z, scv.w};
+        uint32_t ow[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float nlo = (bf16_lo(xw[e]) * inv) * bf16_lo(gw[e]);
+          const float nhi = (bf16_hi(xw[e]) * inv) * bf16_hi(gw[e]);
+          const float ylo = __fmaf_rn(nlo, 1.0f + bf16_lo(cw[e]), bf16_lo(hw[e]));
+          const float yhi = __fmaf_rn(nhi, 1.0f + bf16_hi(cw[e]), bf16_hi(hw[e]));
+          ow[e] = pack_bf16x2(ylo, yhi);
+        }
+        hp[c] = make_uint4(ow[0], ow[1], ow[2], ow[3]);
       }
-      hp[c] = make_uint4(ow[0], ow[1], ow[2], ow[3]);
     }
   }
 }
 
 cudaError_t launch_modulate(const ModulateArgs& a, cudaStream_t stream) {
-  cudaError_t e = launch_kernel(modulate_kernel, dim3(a.S), dim3(MOD_THREADS), 0, stream, a);
+  const bool long_doc = a.S >= kModulateLongRows;
+  cudaError_t e = long_doc ? launch_kernel(modulate_kernel<2>, dim3(a.S), dim3(MOD_VT / 2), 0, stream, a)
+                           : launch_kernel(modulate_kernel<1>, dim3(a.S), dim3(MOD_VT), 0, stream, a);
   if (e != cudaSuccess) return e;
-  set_kernel_info("modulate_kernel rows=%d threads=%d vec=16B reduce=fixed-tree", a.S, MOD_THREADS);
+  set_kernel_info("modulate_kernel rows=%d threads=%d vec=16B reduce=fixed-tree(256)", a.S,
+                  long_doc ? MOD_VT / 2 : MOD_VT);
   return cudaGetLastError();
 }
 

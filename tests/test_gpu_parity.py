@@ -147,6 +147,34 @@ def gemm_bn(request, monkeypatch):
     return request.param
 
 
+@pytest.mark.parametrize("D", [512, 5376])
+def test_modulate_same_bits_for_long_and_short_documents(h3, D):
+    """Documents of 4096 rows and more run the norm + modulate kernel with
+    128-thread CTAs (two virtual threads each), shorter ones with 256; both
+    follow the same reduction tree, so a row gives the same bits in either."""
+    S_long, S_short, T = 4096, 505, 3
+    g = torch.Generator().manual_seed(D)
+    x = torch.randn(S_long, D, generator=g).to(torch.bfloat16).cuda()
+    gain = (1 + 0.1 * torch.randn(D, generator=g)).to(torch.bfloat16).cuda()
+    table = (0.3 * torch.randn(3 * T, 6, D, generator=g)).to(torch.bfloat16).cuda()
+    tag = torch.randint(0, 3, (S_long,), generator=g, dtype=torch.int32).cuda()
+    tidx = torch.randint(0, T, (S_long,), generator=g, dtype=torch.int32).cuda()
+    pos = torch.zeros(S_long, 3, dtype=torch.int32, device="cuda")
+    tc = torch.zeros(T, 256, dtype=torch.float32, device="cuda")
+    cfg = h3.make_config(D, 4, 1536, 256)
+    outs = []
+    for S in (S_long, S_short):
+        m = h3.make_meta(tag[:S], tidx[:S], pos[:S], tc, T)
+        h = torch.empty(S, D, dtype=torch.bfloat16, device="cuda")
+        h3.h3_adaln_modulate(cfg, m, table.reshape(T, -1), 1, x[:S], gain, h)
+        assert h3.h3_sync_check() == 0
+        outs.append(h)
+    assert torch.equal(outs[0][:S_short], outs[1])
+    mod = to_np(table)[(to_np(tidx) * 3 + to_np(tag)).astype(int)]
+    ref = O.rmsnorm_modulate(to_np(x), to_np(gain), mod[:, 3], mod[:, 4])
+    assert_close(to_np(outs[0]), ref, f"modulate D={D} S={S_long}")
+
+
 @pytest.mark.parametrize("name", CASE_NAMES)
 def test_qkv_projection(h3, name, gemm_bn):
     c = get_case(name)
