@@ -538,6 +538,17 @@ def test_block_odd_row_counts(h3, layout):
     assert_close(to_np(y), c.ref["y"], f"block S={c.S}")
 
 
+def test_block_maximum_width(h3):
+    """The widest residual the library takes (D = 8192: the norm kernels' 16-byte
+    chunks at their limit, 32 column tiles per GEMM row) on a short ragged
+    document with two heads."""
+    shape = hi.BlockShape(dim=8192, n_heads=2, head_dim=128, ffn_dim=256, cond_dim=128)
+    w = hi.custom_workload(shape, n_text=3, video_grid=(2, 2, 5), n_audio=14, n_timesteps=2, name="wide8192")
+    c = Case(w)
+    y = run_block(h3, c)
+    assert_close(to_np(y), c.ref["y"], "block D=8192")
+
+
 def _large_positions(S, seed):
     """Positions up to the largest the kernels accept (2^24 - 1 on every
     axis): the extremes, values just below them, and random ones."""
