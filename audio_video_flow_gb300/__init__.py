@@ -104,6 +104,7 @@ def lib() -> ctypes.CDLL:
             "h3_noise_mix": (i32, [c_int64, vp, vp, ctypes.c_float, vp, vp]),
             "h3_select_rows": (i32, [i32, vp, i32, vp, vp, vp]),
             "h3_final_adaln_table": (i32, [cfgp, vp, vp, vp, i32, vp, vp]),
+            "h3_final_adaln_tables": (i32, [cfgp, i32, vp, vp, vp, i32, vp, vp]),
             "h3_output_head": (i32, [cfgp, i32, i32, vp, vp, i32, vp, vp, vp, vp, i32, vp, vp]),
             "h3_sync_check": (i32, [vp, i32]),
             "h3_status_string": (c_char_p, [i32]),
@@ -394,6 +395,20 @@ def h3_select_rows(n_rows: int, token_tag, tag: int, rows, n_selected, stream=No
 def h3_final_adaln_table(cfg, w_fin, b_fin, t_cond, n_timesteps: int, table, stream=None) -> None:
     _check(lib().h3_final_adaln_table(ctypes.byref(cfg), _ptr(w_fin), _ptr(b_fin), _ptr(t_cond), n_timesteps,
                                       _ptr(table), _stream(stream)), "h3_final_adaln_table")
+
+
+def h3_final_adaln_tables(cfg, w_fin, b_fin, t_cond, n_timesteps: int, tables, stream=None) -> None:
+    """w_fin, b_fin (or None) and tables: sequences of the same length (the
+    modalities), passed as host arrays of device pointers."""
+    n = len(w_fin)
+    arr = ctypes.c_void_p * max(n, 1)
+    w_a = arr(*[_ptr(w) for w in w_fin])
+    b_a = None if b_fin is None else arr(*[_ptr(b) for b in b_fin])
+    t_a = arr(*[_ptr(t) for t in tables])
+    _check(lib().h3_final_adaln_tables(ctypes.byref(cfg), n, ctypes.cast(w_a, ctypes.c_void_p),
+                                       None if b_a is None else ctypes.cast(b_a, ctypes.c_void_p), _ptr(t_cond),
+                                       n_timesteps, ctypes.cast(t_a, ctypes.c_void_p), _stream(stream)),
+           "h3_final_adaln_tables")
 
 
 def h3_output_head(cfg, n_rows: int, n_sel: int, rows, timestep_index, n_timesteps: int, x, table, w_head, b_head,

@@ -1360,14 +1360,35 @@ h3_status h3_select_rows(int32_t n_rows, const int32_t* token_tag, int32_t tag, 
   return cuda_st(launch_select_rows(n_rows, token_tag, tag, rows, n_selected, stream));
 }
 
-h3_status h3_final_adaln_table(const h3_block_config* cfg, const float* w_fin, const float* b_fin,
-                               const float* t_cond, int32_t n_timesteps, float* table, cudaStream_t stream) {
+h3_status h3_final_adaln_tables(const h3_block_config* cfg, int32_t n_tables, const float* const* w_fin,
+                                const float* const* b_fin, const float* t_cond, int32_t n_timesteps,
+                                float* const* tables, cudaStream_t stream) {
   h3_status s = check_cfg(cfg);
   if (s != H3_OK) return s;
-  if (n_timesteps < 1 || n_timesteps > 16) return H3_ERR_UNSUPPORTED;
-  if (!w_fin || !t_cond || !table) return H3_ERR_NULL;
-  if (!al16(w_fin) || !al16(t_cond) || !al16n(b_fin) || !al16(table)) return H3_ERR_ALIGN;
-  return cuda_st(launch_final_adaln(w_fin, b_fin, t_cond, n_timesteps, cfg->cond_dim, 2 * cfg->dim, table, stream));
+  if (n_tables < 1 || n_tables > kFinalAdalnMaxTables || n_timesteps < 1 || n_timesteps > 16)
+    return H3_ERR_UNSUPPORTED;
+  if (!w_fin || !tables || !t_cond) return H3_ERR_NULL;
+  if (!al16(t_cond)) return H3_ERR_ALIGN;
+  FinalAdalnArgs a{};
+  a.n_tables = n_tables;
+  for (int m = 0; m < n_tables; ++m) {
+    if (!w_fin[m] || !tables[m]) return H3_ERR_NULL;
+    const float* bm = b_fin ? b_fin[m] : nullptr;
+    if (!al16(w_fin[m]) || !al16n(bm) || !al16(tables[m])) return H3_ERR_ALIGN;
+    a.w[m] = w_fin[m];
+    a.b[m] = bm;
+    a.out[m] = tables[m];
+  }
+  a.t_cond = t_cond;
+  a.T = n_timesteps;
+  a.C = cfg->cond_dim;
+  a.rows = 2 * cfg->dim;
+  return cuda_st(launch_final_adaln(a, stream));
+}
+
+h3_status h3_final_adaln_table(const h3_block_config* cfg, const float* w_fin, const float* b_fin,
+                               const float* t_cond, int32_t n_timesteps, float* table, cudaStream_t stream) {
+  return h3_final_adaln_tables(cfg, 1, &w_fin, &b_fin, t_cond, n_timesteps, &table, stream);
 }
 
 h3_status h3_output_head(const h3_block_config* cfg, int32_t n_rows, int32_t n_sel, const int32_t* rows,

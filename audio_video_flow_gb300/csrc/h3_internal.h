@@ -343,8 +343,16 @@ cudaError_t launch_ode_step(long long n, const float* xt, const float* v, float 
                             cudaStream_t st);
 cudaError_t launch_noise_mix(long long n, const float* x0, const float* noise, float t, float* out, cudaStream_t st);
 cudaError_t launch_select_rows(int n, const int32_t* tags, int tag, int32_t* rows, int32_t* count, cudaStream_t st);
-cudaError_t launch_final_adaln(const float* w, const float* b, const float* t_cond, int T, int C, int rows,
-                               float* out, cudaStream_t st);
+constexpr int kFinalAdalnMaxTables = 4;
+struct FinalAdalnArgs {
+  int n_tables;                               // 1 .. kFinalAdalnMaxTables
+  const float* w[kFinalAdalnMaxTables];       // [rows][C] each
+  const float* b[kFinalAdalnMaxTables];       // [rows] or null
+  float* out[kFinalAdalnMaxTables];           // [T][rows]
+  const float* t_cond;                        // [T][C]
+  int T, C, rows;                             // rows = 2D
+};
+cudaError_t launch_final_adaln(const FinalAdalnArgs& a, cudaStream_t st);
 cudaError_t launch_output_head(const OutputHeadArgs& a, cudaStream_t st);
 
 }  // namespace h3

@@ -145,59 +145,77 @@ __global__ void __launch_bounds__(1024) select_rows_kernel(int n, const int32_t*
 }
 
 // ---------------------------------------------------------------------------
-// final AdaLN table: out[t][j] = SiLU(t_cond[t]) . w[j] + b[j], fp32, j < 2D.
-// Two CTAs per SM, each holding u = SiLU(t_cond) [T][C] in shared memory.  A
-// warp owns one weight row at a time and issues the whole row's 16-byte loads
-// before it multiplies (lane l takes float4 columns l + 32i, at most 22 per
-// lane for C <= 2816), so each resident warp keeps a full row (up to 11 KB) in
-// flight; the T running sums of a lane are reduced over the warp with a fixed
-// xor tree.  The kernel is bound by the 2D x C fp32 weights streamed once.
+// final AdaLN table: out[t][j] = SiLU(t_cond[t]) . w[j] + b[j], fp32, j < 2D,
+// for one or more tables (the modalities) in one launch: weight row j of
+// table m is work unit m * 2D + j, so the modalities stream back to back
+// without a second launch's ramp.  Three CTAs per SM, each holding u = SiLU(t_cond) [T][C] in shared memory.
+// A warp owns one weight row at a time and issues the 16-byte loads of half
+// the row before it multiplies (lane l takes float4 columns l + 32i, at most
+// 11 per lane and half for C <= 2816), so each resident warp keeps half a
+// row (up to 5.5 KB) in flight; the lane's T running sums go on in column
+// order across the halves and are reduced over the warp with a fixed xor
+// tree.  Three CTAs of 256 threads fit in the registers with half rows (two
+// for T > 8): the
+// 10,752 rows of an H3 modality then take three rounds of the 3648 resident
+// warps (two CTAs and whole rows took five, the last 42 % full).  The
+// kernel is bound by the 2D x C fp32 weights streamed once.
 // ---------------------------------------------------------------------------
 constexpr int FA_THREADS = 256;
 constexpr int FA_MAX_LOADS = kMaxCondDim / 4 / 32;   // float4 loads per lane per row
+constexpr int FA_HALF_LOADS = FA_MAX_LOADS / 2;        // per half row
+// resident CTAs per SM: three, or two for the 16 running sums of T > 8
+// (which would not fit three CTAs' registers without spilling)
+__host__ __device__ constexpr int fa_ctas_per_sm(int TT) { return TT >= 16 ? 2 : 3; }
 static_assert(FA_MAX_LOADS * 4 * 32 == kMaxCondDim, "a lane's share of the widest row is whole float4s");
+static_assert(FA_HALF_LOADS * 2 == FA_MAX_LOADS, "the row splits into two equal halves");
 
 // TT: timestep rows rounded up to a power of two (the unrolled sum loops
 // cover TT rows, so T = 1 compiles to one sum per lane)
 template <int TT>
-__global__ void __launch_bounds__(FA_THREADS, 2) final_adaln_kernel(const float* __restrict__ w,
-                                                                    const float* __restrict__ b,
-                                                                    const float* __restrict__ t_cond, int T, int C,
-                                                                    int rows, float* __restrict__ out) {
+__global__ void __launch_bounds__(FA_THREADS, fa_ctas_per_sm(TT)) final_adaln_kernel(const __grid_constant__ FinalAdalnArgs a) {
   extern __shared__ float u[];   // [T][C]
   griddep_launch_dependents();
   griddep_wait();
+  const int T = a.T, C = a.C, rows = a.rows;
   for (int i = threadIdx.x; i < T * C; i += blockDim.x) {
-    const float x = t_cond[i];
+    const float x = a.t_cond[i];
     u[i] = x / (1.0f + expf(-x));
   }
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nw = blockDim.x >> 5;
   const int c4 = C >> 2;
-  for (int j = blockIdx.x * nw + warp; j < rows; j += gridDim.x * nw) {
-    const float4* wr = reinterpret_cast<const float4*>(w + (size_t)j * C);
-    float4 wv[FA_MAX_LOADS];
-#pragma unroll
-    for (int q = 0; q < FA_MAX_LOADS; ++q) {
-      const int kk = lane + q * 32;
-      wv[q] = kk < c4 ? __ldcs(wr + kk) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
+  for (int jm = blockIdx.x * nw + warp; jm < a.n_tables * rows; jm += gridDim.x * nw) {
+    const int m = jm / rows, j = jm - m * rows;   // table m, weight row j
+    const float* __restrict__ b = a.b[m];
+    float* __restrict__ out = a.out[m];
+    const float4* wr = reinterpret_cast<const float4*>(a.w[m] + (size_t)j * C);
     float acc[TT];
 #pragma unroll
     for (int t = 0; t < TT; ++t) acc[t] = 0.0f;
+    // the row in two halves (each lane's loads of a half in flight together),
+    // the sums running on in column order across them
 #pragma unroll
-    for (int q = 0; q < FA_MAX_LOADS; ++q) {
-      const int kk = lane + q * 32;
-      if (kk < c4) {
+    for (int h = 0; h < 2; ++h) {
+      float4 wv[FA_HALF_LOADS];
 #pragma unroll
-        for (int t = 0; t < TT; ++t) {
-          if (t < T) {
-            const float4 uv = reinterpret_cast<const float4*>(u + t * C)[kk];
-            acc[t] = __fmaf_rn(uv.x, wv[q].x, acc[t]);
-            acc[t] = __fmaf_rn(uv.y, wv[q].y, acc[t]);
-            acc[t] = __fmaf_rn(uv.z, wv[q].z, acc[t]);
-            acc[t] = __fmaf_rn(uv.w, wv[q].w, acc[t]);
+      for (int q = 0; q < FA_HALF_LOADS; ++q) {
+        const int kk = lane + (h * FA_HALF_LOADS + q) * 32;
+        wv[q] = kk < c4 ? __ldcs(wr + kk) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int q = 0; q < FA_HALF_LOADS; ++q) {
+        const int kk = lane + (h * FA_HALF_LOADS + q) * 32;
+        if (kk < c4) {
+#pragma unroll
+          for (int t = 0; t < TT; ++t) {
+            if (t < T) {
+              const float4 uv = reinterpret_cast<const float4*>(u + t * C)[kk];
+              acc[t] = __fmaf_rn(uv.x, wv[q].x, acc[t]);
+              acc[t] = __fmaf_rn(uv.y, wv[q].y, acc[t]);
+              acc[t] = __fmaf_rn(uv.z, wv[q].z, acc[t]);
+              acc[t] = __fmaf_rn(uv.w, wv[q].w, acc[t]);
+            }
           }
         }
       }
@@ -510,28 +528,29 @@ cudaError_t launch_select_rows(int n, const int32_t* tags, int tag, int32_t* row
 }
 
 template <int TT>
-static cudaError_t launch_fa(const float* w, const float* b, const float* t_cond, int T, int C, int rows, float* out,
-                             int grid, int smem, cudaStream_t st) {
+static cudaError_t launch_fa(const FinalAdalnArgs& a, int& grid, cudaStream_t st) {
+  const int smem = a.T * a.C * (int)sizeof(float);
+  const int warps = FA_THREADS / 32;
+  const long long units = (long long)a.n_tables * a.rows;
+  grid = (int)((units + warps - 1) / warps);
+  const int cap = fa_ctas_per_sm(TT) * num_sms();   // resident CTAs; warps loop over rows
+  if (grid > cap) grid = cap;
   cudaError_t e = cudaFuncSetAttribute(final_adaln_kernel<TT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  return launch_kernel(final_adaln_kernel<TT>, dim3(grid), dim3(FA_THREADS), (size_t)smem, st, w, b, t_cond, T, C,
-                       rows, out);
+  return launch_kernel(final_adaln_kernel<TT>, dim3(grid), dim3(FA_THREADS), (size_t)smem, st, a);
 }
 
-cudaError_t launch_final_adaln(const float* w, const float* b, const float* t_cond, int T, int C, int rows,
-                               float* out, cudaStream_t st) {
-  const int smem = T * C * (int)sizeof(float);
-  const int warps = FA_THREADS / 32;
-  int grid = (rows + warps - 1) / warps;
-  if (grid > 2 * num_sms()) grid = 2 * num_sms();   // two resident CTAs per SM, warps loop over rows
+cudaError_t launch_final_adaln(const FinalAdalnArgs& a, cudaStream_t st) {
+  int grid = 0;
   cudaError_t e;
-  if (T <= 1) e = launch_fa<1>(w, b, t_cond, T, C, rows, out, grid, smem, st);
-  else if (T <= 2) e = launch_fa<2>(w, b, t_cond, T, C, rows, out, grid, smem, st);
-  else if (T <= 4) e = launch_fa<4>(w, b, t_cond, T, C, rows, out, grid, smem, st);
-  else if (T <= 8) e = launch_fa<8>(w, b, t_cond, T, C, rows, out, grid, smem, st);
-  else e = launch_fa<16>(w, b, t_cond, T, C, rows, out, grid, smem, st);
+  if (a.T <= 1) e = launch_fa<1>(a, grid, st);
+  else if (a.T <= 2) e = launch_fa<2>(a, grid, st);
+  else if (a.T <= 4) e = launch_fa<4>(a, grid, st);
+  else if (a.T <= 8) e = launch_fa<8>(a, grid, st);
+  else e = launch_fa<16>(a, grid, st);
   if (e != cudaSuccess) return e;
-  set_kernel_info("final_adaln_kernel fp32 warp-per-row row-in-flight T=%d C=%d rows=%d grid=%d", T, C, rows, grid);
+  set_kernel_info("final_adaln_kernel fp32 warp-per-row half-rows-in-flight tables=%d T=%d C=%d rows=%d grid=%d",
+                  a.n_tables, a.T, a.C, a.rows, grid);
   return cudaGetLastError();
 }
 

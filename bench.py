@@ -349,8 +349,8 @@ def run_output_side(args, ws_n: int, rank: int, local: int):
         for m, tag, P, nr in mods:
             h3.h3_select_rows(S, meta["token_tag"], tag, rows[m], cnt[m])
         rec(1)
-        for m, tag, P, nr in mods:
-            h3.h3_final_adaln_table(cfg, ow[f"w_fin_{m}"], ow[f"b_fin_{m}"], acts["t_cond"], T, tab[m])
+        h3.h3_final_adaln_tables(cfg, [ow[f"w_fin_{m}"] for m, *_ in mods], [ow[f"b_fin_{m}"] for m, *_ in mods],
+                                 acts["t_cond"], T, [tab[m] for m, *_ in mods])   # both modalities, one launch
         rec(2)
         for m, tag, P, nr in mods:
             h3.h3_output_head(cfg, S, nr, rows[m], meta["timestep_index"], T, acts["x"], tab[m],
@@ -397,7 +397,7 @@ def run_output_side(args, ws_n: int, rank: int, local: int):
                    "video_rows": wl.layout.n_video, "audio_rows": wl.layout.n_audio, "dim": D, "cond": C,
                    "flop_per_step": head_flops, "l2": "inputs larger than L2: 231 MB of fp32 final-AdaLN "
                    "weights re-read every step", "parallelism": f"replicas x{ws_n}"},
-        "e2e": None, "gpu_launches": 8 * n,
+        "e2e": None, "gpu_launches": 7 * n,
         "roofline": {"kernel": "output_head", "bound": "alu", "achieved": round(head_tf, 2),
                      "peak": round(peak, 1), "unit": "TFLOP/s", "frac": round(head_tf / peak, 4),
                      "peak_source": "fp32 FMA lanes x 2 x max SM clock", "traffic": None},

@@ -486,6 +486,17 @@ h3_status h3_final_adaln_table(const h3_block_config *cfg, const float *w_fin, c
                                const float *t_cond, int32_t n_timesteps, float *table,
                                cudaStream_t stream);
 
+/* The final AdaLN tables of up to four modalities in one launch, their
+ * weights streamed back to back (the video and audio tables of an
+ * evaluation).  Table m is exactly what h3_final_adaln_table gives for
+ * w_fin[m], b_fin[m] and tables[m], bit for bit.  w_fin, b_fin and tables are
+ * HOST arrays of n_tables device pointers; b_fin may be NULL (no bias for
+ * any table) or hold NULL entries.  1 <= n_tables <= 4, else
+ * H3_ERR_UNSUPPORTED; a NULL weight or table pointer gives H3_ERR_NULL. */
+h3_status h3_final_adaln_tables(const h3_block_config *cfg, int32_t n_tables, const float *const *w_fin,
+                                const float *const *b_fin, const float *t_cond, int32_t n_timesteps,
+                                float *const *tables, cudaStream_t stream);
+
 /* Velocity head of one modality (RFC s5 video_output_projection_fp32 5376 ->
  * 96, audio_output_projection_fp32 5376 -> 32): for i < n_sel and r = rows[i],
  *   m = RMSNorm(x[r]) * (1 + table[tidx[r]][1]) + table[tidx[r]][0]

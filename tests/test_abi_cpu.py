@@ -86,6 +86,16 @@ def test_host_rejections_return_before_any_launch(lib):
     assert L.h3_adaln_table(ctypes.byref(cfg), 16, None, 16, 17, 16, 256, 1 << 20, None) == h3.H3_ERR_UNSUPPORTED
     assert L.h3_adaln_table(ctypes.byref(cfg), 16, None, 16, 4, 16, 256, 16, None) == h3.H3_ERR_WORKSPACE
     assert L.h3_adaln_table_workspace_bytes(ctypes.byref(cfg)) == 16 * 256 * 2
+    ptrs = (ctypes.c_void_p * 5)(16, 32, 48, 64, 80)
+    ptrs_null = (ctypes.c_void_p * 2)(16, None)
+    assert L.h3_final_adaln_tables(ctypes.byref(cfg), 0, ptrs, None, 16, 1, ptrs, None) == h3.H3_ERR_UNSUPPORTED
+    assert L.h3_final_adaln_tables(ctypes.byref(cfg), 5, ptrs, None, 16, 1, ptrs, None) == h3.H3_ERR_UNSUPPORTED
+    assert L.h3_final_adaln_tables(ctypes.byref(cfg), 2, ptrs, None, 16, 17, ptrs, None) == h3.H3_ERR_UNSUPPORTED
+    assert L.h3_final_adaln_tables(ctypes.byref(cfg), 2, None, None, 16, 1, ptrs, None) == h3.H3_ERR_NULL
+    assert L.h3_final_adaln_tables(ctypes.byref(cfg), 2, ptrs, None, 16, 1, ptrs_null, None) == h3.H3_ERR_NULL
+    assert L.h3_final_adaln_tables(ctypes.byref(cfg), 2, ptrs_null, None, 16, 1, ptrs, None) == h3.H3_ERR_NULL
+    ptrs_odd = (ctypes.c_void_p * 2)(16, 40)
+    assert L.h3_final_adaln_tables(ctypes.byref(cfg), 2, ptrs_odd, None, 16, 1, ptrs, None) == h3.H3_ERR_ALIGN
     buf = ctypes.create_string_buffer(64)
     assert L.h3_last_kernel_info(None, 0) == h3.H3_ERR_NULL
     assert L.h3_last_kernel_info(buf, 64) == h3.H3_OK

@@ -135,6 +135,34 @@ def test_final_adaln_table(h3, wl, T):
         assert_close(tab.cpu().numpy(), ref, f"final adaln {m} {wl}", F32_MAX_E, F32_MEAN_E)
 
 
+@pytest.mark.parametrize("wl,T", [("tiny72", 4), ("denoiser15860", 1), ("denoiser15860", 11)])
+def test_final_adaln_tables_in_one_launch(h3, wl, T):
+    """Both modalities' tables from one launch equal the per-modality calls
+    bit for bit (the same per-row sums), with and without biases; a single
+    table through the batched call is the single call."""
+    shape = hi.WORKLOADS[wl].shape
+    ow = hi.output_weights(shape, 0)
+    tc = hi.activations(shape, 1, T, 0)["t_cond"].cuda()
+    cfg = _cfg(h3, shape)
+    ws = [ow["w_fin_video"].cuda(), ow["w_fin_audio"].cuda()]
+    for bs in ([ow["b_fin_video"].cuda(), ow["b_fin_audio"].cuda()], None):
+        one = []
+        for m in range(2):
+            t = torch.empty(T, 2, shape.dim, dtype=torch.float32, device="cuda")
+            h3.h3_final_adaln_table(cfg, ws[m], None if bs is None else bs[m], tc, T, t)
+            one.append(t)
+        both = [torch.full((T, 2, shape.dim), float("nan"), dtype=torch.float32, device="cuda") for _ in range(2)]
+        h3.h3_final_adaln_tables(cfg, ws, bs, tc, T, both)
+        assert h3.h3_sync_check() == 0
+        assert "tables=2" in h3.h3_last_kernel_info()
+        for m in range(2):
+            assert torch.equal(both[m].view(torch.int32), one[m].view(torch.int32)), f"table {m}, bias {bs is not None}"
+    single = torch.empty(T, 2, shape.dim, dtype=torch.float32, device="cuda")
+    h3.h3_final_adaln_tables(cfg, ws[:1], None, tc, T, [single])
+    assert h3.h3_sync_check() == 0
+    assert torch.equal(single.view(torch.int32), one[0].view(torch.int32))
+
+
 @pytest.mark.parametrize("wl", ["tiny72", "ragged", "denoiser15860"])
 def test_output_heads(h3, wl):
     if wl == "ragged":
