@@ -63,6 +63,17 @@ struct GemmCfg {
   static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + 256;
 };
 
+// The gated-residual epilogue of 256-wide tiles stages each epilogue warp's
+// 32 rows x 64 columns (bf16, 4 KB) in shared memory after the barriers, so
+// that its global loads and stores move whole 128-byte lines.
+constexpr int EPI_STAGE_WARP_BYTES = 32 * 128;
+constexpr int EPI_STAGE_BYTES = 8 * EPI_STAGE_WARP_BYTES;
+template <int EPI, int BN>
+__host__ __device__ constexpr bool gemm_staged_resid() { return EPI == EPI_RESID && BN == 256; }
+template <int EPI, int BN>
+__host__ __device__ constexpr int gemm_smem() { return GemmCfg<BN>::SMEM + (gemm_staged_resid<EPI, BN>() ? EPI_STAGE_BYTES : 0); }
+static_assert(gemm_smem<EPI_RESID, 256>() <= 232448, "the staged epilogue fits the shared-memory limit");
+
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   const uint32_t s = smem_u32(p);
   return p + (((s + 1023u) & ~1023u) - s);
@@ -283,6 +294,120 @@ __device__ __forceinline__ void epi_resid(const GemmArgs& a, uint32_t tacc, int 
   int c, c1;
   half_range(t.w, half, c, c1);
   float ss = 0.0f;
+#pragma unroll 1
+  for (; c + 32 <= c1; c += 32) resid_chunk<32>(a, tacc + c, m, valid, gate, t.n0 + c, ss);
+  if (c < c1) resid_chunk<16>(a, tacc + c, m, valid, gate, t.n0 + c, ss);
+  if (a.nrm_h && m < a.M) a.nrm_part[(size_t)(2 * n_blk + half) * (a.num_m * 256) + m] = ss;
+}
+
+// The residual and gate rows of this warp's row and column half, asked
+// into L1 ahead of the epilogue (each lane its own row, 128-byte lines): the
+// owner of a stream-K tile issues them before it waits for the partials, so
+// the epilogue's loads hit L1 instead of paying an L2 round trip per chunk.
+__device__ __forceinline__ void prefetch_l1(const void* p) {
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
+__device__ __forceinline__ void epi_resid_prefetch(const GemmArgs& a, int m, NTile t, int half) {
+  if (m >= a.M) return;
+  const int tg = a.tag[m], ti = a.tidx[m];
+  if ((unsigned)tg > 2u || (unsigned)ti >= (unsigned)a.T) return;   // reported by the epilogue
+  const __nv_bfloat16* gate = a.table + ((size_t)(ti * 3 + tg) * 6 + a.chunk) * a.D;
+  int c, c1;
+  half_range(t.w, half, c, c1);
+  for (; c < c1; c += 64) {
+    const int n0 = t.n0 + c;
+    if (n0 >= a.n_valid) break;
+    prefetch_l1(a.resid + (size_t)m * a.ldr + n0);
+    prefetch_l1(gate + n0);
+  }
+}
+
+// Unit u (16 bytes) of row r of a warp's staging buffer (32 rows x 128
+// bytes) sits at unit u ^ (r & 7): one row per lane and eight lanes per row
+// both reach all 32 banks without conflict.
+__device__ __forceinline__ uint4* stage_unit(uint8_t* buf, int r, int u) {
+  return reinterpret_cast<uint4*>(buf + r * 128 + ((u ^ (r & 7)) << 4));
+}
+
+// The gated residual through the warp's staging buffer, 64 columns at a
+// time: the warp reads the residual rows as whole lines (eight lanes per row,
+// four rows per load), each lane combines its own row with its accumulator
+// row and gate exactly as resid_chunk does, and the warp writes the output
+// rows as whole lines.  Rows whose metadata is out of range are left
+// unwritten (their lanes vote them out).  Columns past the last full 64 go
+// through resid_chunk.
+__device__ __forceinline__ void epi_resid_staged(const GemmArgs& a, uint32_t tacc, int m, bool valid, NTile t,
+                                                 int half, int n_blk, uint8_t* buf) {
+  const int lane = (int)(threadIdx.x & 31u);
+  const int row0 = m - lane;
+  const __nv_bfloat16* gate = nullptr;
+  if (valid) {
+    const int tg = a.tag[m], ti = a.tidx[m];
+    if ((unsigned)tg > 2u || (unsigned)ti >= (unsigned)a.T) {
+      record_error(a.err, DEVERR_INDEX);
+      valid = false;
+    } else {
+      gate = a.table + ((size_t)(ti * 3 + tg) * 6 + a.chunk) * a.D;
+    }
+  }
+  int c, c1;
+  half_range(t.w, half, c, c1);
+  float ss = 0.0f;
+#pragma unroll 1
+  for (; c + 64 <= c1 && t.n0 + c + 64 <= a.n_valid; c += 64) {
+    const int n0 = t.n0 + c;
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+      const int r = it * 4 + (lane >> 3), u = lane & 7, gm = row0 + r;
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      const __nv_bfloat16* src = a.resid + (size_t)gm * a.ldr + n0 + u * 8;
+      if (gm < a.M && in_bounds<__nv_bfloat16>(a.resid, a.resid_elems, src, 8, a.err, 2))
+        v = *reinterpret_cast<const uint4*>(src);
+      *stage_unit(buf, r, u) = v;
+    }
+    uint32_t r0[32], r1[32];
+    tmem_ld32(tacc + c, r0);
+    tmem_ld_wait(r0);
+    tmem_ld32(tacc + c + 32, r1);
+    tmem_ld_wait(r1);
+    const bool ok = valid && in_bounds<__nv_bfloat16>(a.table, a.table_elems, gate + n0, 64, a.err, 3);
+    const unsigned ok_rows = __ballot_sync(0xffffffffu, ok);
+    __syncwarp();
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      uint4 ov = make_uint4(0u, 0u, 0u, 0u);
+      if (ok) {
+        const uint4 xv = *stage_unit(buf, lane, u);
+        const uint4 gv = *reinterpret_cast<const uint4*>(gate + n0 + u * 8);
+        const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+        const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+        uint32_t ow[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int j = u * 8 + 2 * e;   // column of the 64
+          const uint32_t acc_lo = j < 32 ? r0[j] : r1[j - 32];
+          const uint32_t acc_hi = j < 32 ? r0[j + 1] : r1[j - 31];
+          const float flo = bf16_round(__uint_as_float(acc_lo) + bias_at(a.bias, n0 + j));
+          const float fhi = bf16_round(__uint_as_float(acc_hi) + bias_at(a.bias, n0 + j + 1));
+          const float ylo = __fmaf_rn(bf16_lo(gw[e]), flo, bf16_lo(xw[e]));
+          const float yhi = __fmaf_rn(bf16_hi(gw[e]), fhi, bf16_hi(xw[e]));
+          ow[e] = pack_bf16x2(ylo, yhi);
+          ss = __fmaf_rn(bf16_lo(ow[e]), bf16_lo(ow[e]), ss);
+          ss = __fmaf_rn(bf16_hi(ow[e]), bf16_hi(ow[e]), ss);
+        }
+        ov = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+      }
+      *stage_unit(buf, lane, u) = ov;
+    }
+    __syncwarp();
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+      const int r = it * 4 + (lane >> 3), u = lane & 7, gm = row0 + r;
+      __nv_bfloat16* dst = a.out + (size_t)gm * a.ldo + n0 + u * 8;
+      if (((ok_rows >> r) & 1u) && out_ok(a, dst, 8, 4)) *reinterpret_cast<uint4*>(dst) = *stage_unit(buf, r, u);
+    }
+    __syncwarp();
+  }
 #pragma unroll 1
   for (; c + 32 <= c1; c += 32) resid_chunk<32>(a, tacc + c, m, valid, gate, t.n0 + c, ss);
   if (c < c1) resid_chunk<16>(a, tacc + c, m, valid, gate, t.n0 + c, ss);
@@ -642,10 +767,16 @@ __device__ __forceinline__ bool sk_fold_partials(const GemmArgs& a, uint32_t tac
 }
 
 template <int EPI, int BN>
-__device__ __forceinline__ void run_epilogue(const GemmArgs& a, uint32_t tacc, int m, int n_blk, int half) {
+__device__ __forceinline__ void run_epilogue(const GemmArgs& a, uint32_t tacc, int m, int n_blk, int half,
+                                             uint8_t* stage_buf) {
   const bool valid = m < a.M;
   if (EPI == EPI_PLAIN) epi_plain(a, tacc, m, valid, n_tile<EPI, BN>(a, n_blk), half);
-  if (EPI == EPI_RESID) epi_resid(a, tacc, m, valid, n_tile<EPI, BN>(a, n_blk), half, n_blk);
+  if (EPI == EPI_RESID) {
+    if constexpr (gemm_staged_resid<EPI, BN>())
+      epi_resid_staged(a, tacc, m, valid, n_tile<EPI, BN>(a, n_blk), half, n_blk, stage_buf);
+    else
+      epi_resid(a, tacc, m, valid, n_tile<EPI, BN>(a, n_blk), half, n_blk);
+  }
   if (EPI == EPI_SWIGLU) epi_swiglu(a, tacc, m, valid, n_blk, half);
   if (EPI == EPI_QKV) epi_qkv<BN>(a, tacc, m, valid, n_blk, half);
 }
@@ -670,6 +801,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   uint64_t* drain = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  uint8_t* stage_base = reinterpret_cast<uint8_t*>(bars) + 256;   // epilogue staging (staged residual tiles)
 
   griddep_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -846,10 +978,15 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         if constexpr (BN == 256) sk_store_partial<EPI, BN>(args, tacc, unit, rank, q, half, row, lane);
       } else {
         if constexpr (BN == 256) {
-          if (args.sk_units > 0)
+          if (args.sk_units > 0) {
+            if (EPI == EPI_RESID)
+              epi_resid_prefetch(args, m_blk * 2 * BM + (int)rank * BM + row, n_tile<EPI, BN>(args, n_blk), half);
             done = sk_fold_partials<EPI, BN>(args, tacc, unit, rank, q, half, row, lane, w.tile, abort_v);
+          }
         }
-        if (done) run_epilogue<EPI, BN>(args, tacc, m_blk * 2 * BM + (int)rank * BM + row, n_blk, half);
+        if (done)
+          run_epilogue<EPI, BN>(args, tacc, m_blk * 2 * BM + (int)rank * BM + row, n_blk, half,
+                                stage_base + (warp - 2) * EPI_STAGE_WARP_BYTES);
         if (EPI == EPI_RESID && done && args.nrm_h) {
           // partial sums stored: count this warp for its row tile
           __syncwarp();
@@ -1051,7 +1188,7 @@ int gemm_pair_slots() {
 template <int EPI, int BN>
 static cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, int grid,
                               cudaStream_t stream) {
-  constexpr int smem = GemmCfg<BN>::SMEM;
+  constexpr int smem = gemm_smem<EPI, BN>();
   static_assert(tmem_footprint_exclusive(smem), "a GEMM CTA must hold its SM's TMEM alone");
   if (!tmem_exclusive(smem)) return cudaErrorNotSupported;
   cudaError_t e = cudaFuncSetAttribute(gemm_bf16_tc<EPI, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
