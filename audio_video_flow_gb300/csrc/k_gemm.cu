@@ -63,15 +63,20 @@ struct GemmCfg {
   static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + 256;
 };
 
-// The gated-residual epilogue of 256-wide tiles stages each epilogue warp's
-// 32 rows x 64 columns (bf16, 4 KB) in shared memory after the barriers, so
-// that its global loads and stores move whole 128-byte lines.
+// The gated-residual and SwiGLU epilogues of 256-wide tiles stage each
+// epilogue warp's 32 rows x 64 columns (bf16, 4 KB) in shared memory after
+// the barriers, so that their global loads and stores move whole 128-byte
+// lines.
 constexpr int EPI_STAGE_WARP_BYTES = 32 * 128;
 constexpr int EPI_STAGE_BYTES = 8 * EPI_STAGE_WARP_BYTES;
 template <int EPI, int BN>
-__host__ __device__ constexpr bool gemm_staged_resid() { return EPI == EPI_RESID && BN == 256; }
+__host__ __device__ constexpr bool gemm_staged_epi() {
+  return BN == 256 && (EPI == EPI_RESID || EPI == EPI_SWIGLU);
+}
 template <int EPI, int BN>
-__host__ __device__ constexpr int gemm_smem() { return GemmCfg<BN>::SMEM + (gemm_staged_resid<EPI, BN>() ? EPI_STAGE_BYTES : 0); }
+__host__ __device__ constexpr int gemm_smem() {
+  return GemmCfg<BN>::SMEM + (gemm_staged_epi<EPI, BN>() ? EPI_STAGE_BYTES : 0);
+}
 static_assert(gemm_smem<EPI_RESID, 256>() <= 232448, "the staged epilogue fits the shared-memory limit");
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
@@ -412,6 +417,47 @@ __device__ __forceinline__ void epi_resid_staged(const GemmArgs& a, uint32_t tac
   for (; c + 32 <= c1; c += 32) resid_chunk<32>(a, tacc + c, m, valid, gate, t.n0 + c, ss);
   if (c < c1) resid_chunk<16>(a, tacc + c, m, valid, gate, t.n0 + c, ss);
   if (a.nrm_h && m < a.M) a.nrm_part[(size_t)(2 * n_blk + half) * (a.num_m * 256) + m] = ss;
+}
+
+// SwiGLU through the warp's staging buffer: the column half's 64 outputs of
+// this lane's row (computed exactly as epi_swiglu does) go to its staging
+// row, then the warp writes the 32 rows as whole lines.
+__device__ __forceinline__ void epi_swiglu_staged(const GemmArgs& a, uint32_t tacc, int m, bool valid, int n_blk,
+                                                  int half, uint8_t* buf) {
+  const int lane = (int)(threadIdx.x & 31u);
+  const int row0 = m - lane;
+  const int n0 = n_blk * 128 + half * 64;   // the half's first output column
+  const bool ok = valid && out_ok(a, a.out + (size_t)m * a.ldo + n0, 64, 5);
+  const unsigned ok_rows = __ballot_sync(0xffffffffu, ok);
+#pragma unroll 1
+  for (int cc = 0; cc < 2; ++cc) {
+    const int c = 2 * half + cc;
+    uint32_t g[32], u[32];
+    tmem_ld32(tacc + c * 32, g);
+    tmem_ld32(tacc + 128 + c * 32, u);
+    tmem_ld_wait(g);
+    tmem_ld_wait(u);
+    float v[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const float gv = bf16_round(__uint_as_float(g[j]) + bias_at(a.bias, n0 + cc * 32 + j));
+      const float uv = bf16_round(__uint_as_float(u[j]) + bias_at(a.bias, a.F + n0 + cc * 32 + j));
+      v[j] = ok ? (gv / (1.0f + expf(-gv))) * uv : 0.0f;
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      *stage_unit(buf, lane, cc * 4 + k) =
+          make_uint4(pack_bf16x2(v[8 * k + 0], v[8 * k + 1]), pack_bf16x2(v[8 * k + 2], v[8 * k + 3]),
+                     pack_bf16x2(v[8 * k + 4], v[8 * k + 5]), pack_bf16x2(v[8 * k + 6], v[8 * k + 7]));
+  }
+  __syncwarp();
+#pragma unroll
+  for (int it = 0; it < 8; ++it) {
+    const int r = it * 4 + (lane >> 3), un = lane & 7;
+    if ((ok_rows >> r) & 1u)
+      *reinterpret_cast<uint4*>(a.out + (size_t)(row0 + r) * a.ldo + n0 + un * 8) = *stage_unit(buf, r, un);
+  }
+  __syncwarp();
 }
 
 // The fused RMSNorm + modulation of one owned tile's column half for the 32
@@ -772,12 +818,17 @@ __device__ __forceinline__ void run_epilogue(const GemmArgs& a, uint32_t tacc, i
   const bool valid = m < a.M;
   if (EPI == EPI_PLAIN) epi_plain(a, tacc, m, valid, n_tile<EPI, BN>(a, n_blk), half);
   if (EPI == EPI_RESID) {
-    if constexpr (gemm_staged_resid<EPI, BN>())
+    if constexpr (gemm_staged_epi<EPI, BN>())
       epi_resid_staged(a, tacc, m, valid, n_tile<EPI, BN>(a, n_blk), half, n_blk, stage_buf);
     else
       epi_resid(a, tacc, m, valid, n_tile<EPI, BN>(a, n_blk), half, n_blk);
   }
-  if (EPI == EPI_SWIGLU) epi_swiglu(a, tacc, m, valid, n_blk, half);
+  if (EPI == EPI_SWIGLU) {
+    if constexpr (gemm_staged_epi<EPI, BN>())
+      epi_swiglu_staged(a, tacc, m, valid, n_blk, half, stage_buf);
+    else
+      epi_swiglu(a, tacc, m, valid, n_blk, half);
+  }
   if (EPI == EPI_QKV) epi_qkv<BN>(a, tacc, m, valid, n_blk, half);
 }
 
