@@ -419,9 +419,11 @@ __device__ __forceinline__ void epi_resid_staged(const GemmArgs& a, uint32_t tac
   if (a.nrm_h && m < a.M) a.nrm_part[(size_t)(2 * n_blk + half) * (a.num_m * 256) + m] = ss;
 }
 
-// SwiGLU through the warp's staging buffer: the column half's 64 outputs of
-// this lane's row (computed exactly as epi_swiglu does) go to its staging
-// row, then the warp writes the 32 rows as whole lines.
+// SwiGLU: gate columns g and value columns u of the tile (128 each; column
+// half `half` takes output columns 64 half .. 64 half + 63), out =
+// SiLU(bf16(g + b_g)) * bf16(u + b_u).  The 64 outputs of this lane's row go
+// to its row of the warp's staging buffer, then the warp writes the 32 rows
+// as whole lines.
 __device__ __forceinline__ void epi_swiglu_staged(const GemmArgs& a, uint32_t tacc, int m, bool valid, int n_blk,
                                                   int half, uint8_t* buf) {
   const int lane = (int)(threadIdx.x & 31u);
@@ -517,29 +519,6 @@ __device__ __forceinline__ bool fused_norm(const GemmArgs& a, int m_blk, int n_b
     *reinterpret_cast<uint2*>(a.nrm_h + mr * a.D + n) = make_uint2(ow[0], ow[1]);
   }
   return true;
-}
-
-__device__ __forceinline__ void epi_swiglu(const GemmArgs& a, uint32_t tacc, int m, bool valid, int n_blk,
-                                           int half) {
-#pragma unroll 1
-  for (int c = 2 * half; c < 2 * half + 2; ++c) {
-    uint32_t g[32], u[32];
-    tmem_ld32(tacc + c * 32, g);
-    tmem_ld32(tacc + 128 + c * 32, u);
-    tmem_ld_wait(g);
-    tmem_ld_wait(u);
-    const int n0 = n_blk * 128 + c * 32;
-    if (valid) {
-      float v[32];
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const float gv = bf16_round(__uint_as_float(g[j]) + bias_at(a.bias, n0 + j));
-        const float uv = bf16_round(__uint_as_float(u[j]) + bias_at(a.bias, a.F + n0 + j));
-        v[j] = (gv / (1.0f + expf(-gv))) * uv;
-      }
-      if (out_ok(a, a.out + (size_t)m * a.ldo + n0, 32, 5)) store32_bf16(a.out + (size_t)m * a.ldo + n0, v);
-    }
-  }
 }
 
 // Q or K columns of head h (128 accumulator columns at tpart): per-head
@@ -823,11 +802,9 @@ __device__ __forceinline__ void run_epilogue(const GemmArgs& a, uint32_t tacc, i
     else
       epi_resid(a, tacc, m, valid, n_tile<EPI, BN>(a, n_blk), half, n_blk);
   }
-  if (EPI == EPI_SWIGLU) {
-    if constexpr (gemm_staged_epi<EPI, BN>())
-      epi_swiglu_staged(a, tacc, m, valid, n_blk, half, stage_buf);
-    else
-      epi_swiglu(a, tacc, m, valid, n_blk, half);
+  if constexpr (EPI == EPI_SWIGLU) {
+    static_assert(gemm_staged_epi<EPI, BN>(), "SwiGLU tiles are 256 wide (128 gate + 128 value columns)");
+    epi_swiglu_staged(a, tacc, m, valid, n_blk, half, stage_buf);
   }
   if (EPI == EPI_QKV) epi_qkv<BN>(a, tacc, m, valid, n_blk, half);
 }
