@@ -244,6 +244,36 @@ def test_out_projection(h3, name, gemm_bn):
     assert_close(to_np(x1), c.ref["x1"], f"out_projection[{name}]")
 
 
+@pytest.mark.parametrize("name", ["ragged205", "block505"])
+def test_residual_epilogue_skips_rows_with_bad_metadata(h3, name, gemm_bn):
+    """The gated-residual epilogue leaves a row whose tag or timestep index is
+    out of range unwritten and reports it; every other row is the one the
+    good metadata give, bit for bit (256-wide tiles pass each warp's rows
+    through shared memory, and the rows of a warp there are written by other
+    lanes than the ones that checked them)."""
+    c = get_case(name)
+    D = c.w.shape.dim
+    o = to_bf16(c.ref["o"])
+    good = torch.empty(c.S, D, dtype=torch.bfloat16, device="cuda")
+    h3.h3_out_projection(c.cfg(h3), c.meta(h3), table_tensor(c), o, c.d_w["w_o"], None, c.d_x, good)
+    assert h3.h3_sync_check() == 0
+    tag = c.d_meta["token_tag"].clone()
+    tidx = c.d_meta["timestep_index"].clone()
+    bad_rows = [3, 37, c.S - 1]
+    tag[bad_rows[0]] = 7
+    tidx[bad_rows[1]] = c.T
+    tag[bad_rows[2]] = -1
+    meta = h3.make_meta(tag, tidx, c.d_meta["pos_thw"], c.d_tc, c.T)
+    y = torch.full((c.S, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    h3.h3_out_projection(c.cfg(h3), meta, table_tensor(c), o, c.d_w["w_o"], None, c.d_x, y)
+    assert h3.h3_sync_check() == h3.H3_ERR_INDEX
+    keep = torch.ones(c.S, dtype=torch.bool)
+    keep[bad_rows] = False
+    yc, gc = y.cpu(), good.cpu()
+    assert torch.isnan(yc[~keep].float()).all(), "a row with bad metadata was written"
+    assert torch.equal(yc[keep].view(torch.int16), gc[keep].view(torch.int16))
+
+
 @pytest.mark.parametrize("name", CASE_NAMES)
 def test_ffn_up_swiglu(h3, name):
     c = get_case(name)
