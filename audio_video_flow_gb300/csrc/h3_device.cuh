@@ -119,7 +119,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // True when a timeout has been recorded on the device since the last
-// h3_sync_check (read at kernel entry, after griddepcontrol.wait).
+// h3_sync_check.  Read in each kernel's prologue, before
+// griddepcontrol.wait, so the read overlaps the previous kernel: a launch
+// whose CTAs start after the timeout is recorded skips its work.
 __device__ __forceinline__ bool timeout_recorded(const uint32_t* err) {
   return err && (*reinterpret_cast<const volatile uint32_t*>(err) & DEVERR_TIMEOUT);
 }

@@ -83,7 +83,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     mbar_init(p_full, 4);
     mbar_init(o_done, 1);
     mbar_init(drain, 1);
-    *abort_flag = 0;
+    *abort_flag = timeout_recorded(args.err) ? 1 : 0;   // sticky timeout of an earlier launch
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -99,10 +99,9 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   const uint32_t tmem_base = *tmem_slot;   // S0: cols [0,128), S1: [128,256), O: [256,384)
   const WaitCtl abort_v{abort_flag, args.err, KID_ATTN_1Q};
 
-  // a wait of an earlier launch ran out (sticky until h3_sync_check): this
-  // launch skips its work, before any copy or MMA is issued
-  if (threadIdx.x == 0 && timeout_recorded(args.err)) *abort_flag = 1;
-  __syncthreads();
+  // a wait of an earlier launch ran out (sticky until h3_sync_check; read
+  // in the prologue, beside the previous kernel): this launch skips its
+  // work, before any copy or MMA is issued
   const bool skip = *abort_v.flag != 0;
 
   if (skip) {
@@ -407,7 +406,7 @@ __global__ void __launch_bounds__(AT2_THREADS, 1)
       mbar_init(&o_final[t], 1);
     }
     mbar_init(drain, 1);
-    *abort_flag = 0;
+    *abort_flag = timeout_recorded(args.err) ? 1 : 0;   // sticky timeout of an earlier launch
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -423,10 +422,9 @@ __global__ void __launch_bounds__(AT2_THREADS, 1)
   const uint32_t tmem_base = *tmem_slot;
   const WaitCtl abort_v{abort_flag, args.err, KID_ATTN_2Q};
 
-  // a wait of an earlier launch ran out (sticky until h3_sync_check): this
-  // launch skips its work, before any copy or MMA is issued
-  if (threadIdx.x == 0 && timeout_recorded(args.err)) *abort_flag = 1;
-  __syncthreads();
+  // a wait of an earlier launch ran out (sticky until h3_sync_check; read
+  // in the prologue, beside the previous kernel): this launch skips its
+  // work, before any copy or MMA is issued
   const bool skip = *abort_v.flag != 0;
 
   if (skip) {

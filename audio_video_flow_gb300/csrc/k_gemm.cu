@@ -858,7 +858,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       mbar_init(&acc_empty[i], 16);   // 8 epilogue warps of each CTA
     }
     mbar_init(drain, 1);
-    *abort_flag = 0;
+    *abort_flag = timeout_recorded(args.err) ? 1 : 0;   // sticky timeout of an earlier launch
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -883,10 +883,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   const uint32_t tmem_base = *tmem_slot;
   const WaitCtl abort_v{abort_flag, args.err, KID_GEMM};
 
-  // a wait of an earlier launch ran out (sticky until h3_sync_check): this
-  // launch skips its work, before any copy or MMA is issued
-  if (threadIdx.x == 0 && timeout_recorded(args.err)) *abort_flag = 1;
-  __syncthreads();
+  // a wait of an earlier launch ran out (sticky until h3_sync_check; read
+  // in the prologue, beside the previous kernel): this launch skips its
+  // work, before any copy or MMA is issued
   const bool skip = *abort_v.flag != 0;
 
   if (skip) {
@@ -1352,7 +1351,7 @@ __global__ void __launch_bounds__(AD_THREADS, 1)
     }
     mbar_init(u_full, 1);
     mbar_init(drain, 1);
-    *abort_flag = 0;
+    *abort_flag = timeout_recorded(args.err) ? 1 : 0;   // sticky timeout of an earlier launch
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(tmem_slot, 32);
@@ -1385,10 +1384,9 @@ __global__ void __launch_bounds__(AD_THREADS, 1)
   }
   griddep_wait();
 
-  // a wait of an earlier launch ran out (sticky until h3_sync_check): this
-  // launch skips its work, before any copy or MMA is issued
-  if (threadIdx.x == 0 && timeout_recorded(args.err)) *abort_flag = 1;
-  __syncthreads();
+  // a wait of an earlier launch ran out (sticky until h3_sync_check; read
+  // in the prologue, beside the previous kernel): this launch skips its
+  // work, before any copy or MMA is issued
   const bool skip = *abort_v.flag != 0;
 
   if (skip) {

@@ -179,7 +179,7 @@ __global__ void __launch_bounds__(ROPE_THREADS, 1)
       mbar_init(&full[st], 2);               // expect_tx arrival + angles-ready arrival
       mbar_init(&empty[st], ROPE_CWARPS);
     }
-    *abort_flag = 0;
+    *abort_flag = timeout_recorded(a.err) ? 1 : 0;   // sticky timeout of an earlier launch
     fence_mbar_init();
   }
   if (threadIdx.x == 32) {
@@ -190,10 +190,9 @@ __global__ void __launch_bounds__(ROPE_THREADS, 1)
   griddep_wait();
   const WaitCtl abort_v{abort_flag, a.err, KID_ROPE};
 
-  // a wait of an earlier launch ran out (sticky until h3_sync_check): this
-  // launch skips its work, before any copy or MMA is issued
-  if (threadIdx.x == 0 && timeout_recorded(a.err)) *abort_flag = 1;
-  __syncthreads();
+  // a wait of an earlier launch ran out (sticky until h3_sync_check; read
+  // in the prologue, beside the previous kernel): this launch skips its
+  // work, before any copy or MMA is issued
   const bool skip = *abort_v.flag != 0;
 
   if (skip) {

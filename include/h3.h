@@ -26,11 +26,11 @@
  *     that word.  A device-side wait that exceeds its time limit (2 s) is
  *     recorded the same way (H3_ERR_TIMEOUT), together with the site of the
  *     first such wait (h3_last_error_site).  The timeout bit is sticky: until
- *     h3_sync_check clears it, every bounded wait of every library kernel on
- *     that device gives up at its next poll, so one lost signal ends the
- *     whole queue of work within about one time limit instead of costing one
- *     limit per later launch.  Results of calls made in that window are
- *     undefined; the status says so.
+ *     h3_sync_check clears it, every library kernel whose CTAs start after
+ *     it is recorded skips its work (it reads the bit in its prologue), so
+ *     one lost signal ends the whole queue of work within about one time
+ *     limit instead of costing one limit per later launch.  Results of calls
+ *     made in that window are undefined; the status says so.
  *   - Results are deterministic: a given call on a given GPU gives bitwise
  *     the same output every time.  With H3_GEMM_SK=0 in the environment every
  *     reduction has a fixed order that does not depend on the row count, the
