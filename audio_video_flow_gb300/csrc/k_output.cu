@@ -233,13 +233,15 @@ __global__ void __launch_bounds__(FA_THREADS, fa_ctas_per_sm(TT)) final_adaln_ke
 }
 
 // ---------------------------------------------------------------------------
-// Velocity head.  A cluster of OH_KS CTAs takes 128 selected rows and all P
-// columns (P padded to 16 * PT, PT in {2, 4, 6, 8}); CTA rank ks of the
-// cluster owns the ks-th of OH_KS contiguous ranges of the reduction axis D
-// (whole 32-column chunks).
+// Velocity head.  A cluster of KS CTAs (KS in {1, 2, 4, 8}: the fewest that
+// give two CTAs per SM, else 8) takes 96 selected rows and all P columns (P
+// padded to 16 * PT, PT in {2, 4, 6, 8}); CTA rank ks of the cluster owns the
+// ks-th of KS contiguous ranges of the reduction axis D (whole 32-column
+// chunks).  The 14,580 video rows of an evaluation make 152 tiles in pairs:
+// 304 CTAs, one wave at two per SM.
 //   1. Each CTA sums the squares of its range of each row (lane partials in
-//      column order, fixed xor tree); after a cluster barrier every CTA adds
-//      the OH_KS partials in rank order and takes inv = 1/sqrt(ss/D + eps).
+//      column order, fixed xor tree); with KS > 1, after a cluster barrier,
+//      every CTA adds the KS partials in rank order; inv = 1/sqrt(ss/D + eps).
 //   2. Each CTA walks its range in 32-column chunks: the modulated
 //      activations a[k][row] = (x * inv) * (1 + scale) + shift and the head
 //      chunk w[k][p] are staged in shared memory (double-buffered; the next
@@ -247,14 +249,19 @@ __global__ void __launch_bounds__(FA_THREADS, fa_ctas_per_sm(TT)) final_adaln_ke
 //      thread (ty, tx) accumulates an 8-row x PT-column register tile in k
 //      order, reading its 8 rows with two 16-byte and its PT columns with
 //      8-byte shared loads per k.
-//   3. The partial tiles are left in shared memory; after a cluster barrier
-//      rank ks adds, for rows [16 ks, 16 ks + 16) of the tile, the OH_KS
-//      partials in rank order over distributed shared memory, adds the bias
-//      and writes the rows.
-// Every output is therefore the same fixed-order fp32 sum whatever the grid.
+//   3. With KS = 1 each thread adds the bias and writes its tile.  Otherwise
+//      the partial tiles are left in shared memory; after a cluster barrier
+//      rank ks adds, for its 96 / KS rows of the tile, the KS partials in
+//      rank order over distributed shared memory, adds the bias and writes
+//      the rows.
+// For a given row count every output is one fixed-order fp32 sum.
 // Rows whose metadata is out of range are reported and left unwritten.
 // ---------------------------------------------------------------------------
-constexpr int OH_ROWS = 128, OH_KC = 32, OH_THREADS = 256, OH_KS = 8;
+constexpr int OH_ROWS = 96, OH_KC = 32, OH_THREADS = 192, OH_MAX_KS = 8;
+static_assert(OH_ROWS == 8 * (OH_THREADS / 16), "16 column groups x 8-row groups cover the tile");
+static_assert(OH_THREADS == 2 * OH_ROWS, "two staging threads per row");
+static_assert(OH_ROWS % OH_MAX_KS == 0, "every k-split divides the rows");
+constexpr int OH_TSLOTS = (16 * 2 * (OH_KC / 4) + OH_THREADS - 1) / OH_THREADS;   // table float4 per thread
 
 template <int PT>
 struct OhCfg {
@@ -290,11 +297,12 @@ __global__ void __launch_bounds__(OH_THREADS, 2) output_head_kernel(const Output
   griddep_launch_dependents();
   griddep_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int KS = (int)cluster_nctarank();
   const int ks = (int)cluster_ctarank();
-  const int i0 = (blockIdx.x / OH_KS) * OH_ROWS;
+  const int i0 = (blockIdx.x / KS) * OH_ROWS;
   const int D = a.D, P = a.P;
   const int nch = D / OH_KC;
-  const int c_lo = (ks * nch) / OH_KS, c_hi = ((ks + 1) * nch) / OH_KS;   // chunks of this CTA
+  const int c_lo = (ks * nch) / KS, c_hi = ((ks + 1) * nch) / KS;   // chunks of this CTA
   const int k_lo = c_lo * OH_KC, k_hi = c_hi * OH_KC;
   if (threadIdx.x < OH_ROWS) {
     const int i = i0 + (int)threadIdx.x;
@@ -338,34 +346,46 @@ __global__ void __launch_bounds__(OH_THREADS, 2) output_head_kernel(const Output
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
     if (lane == 0) s_ss[rr] = ss;
   }
-  cluster_sync();
-  if (threadIdx.x < OH_ROWS) {
-    const uint32_t my = smem_u32(&s_ss[threadIdx.x]);
-    float ss = 0.0f;
-#pragma unroll
-    for (int q = 0; q < OH_KS; ++q) ss += ld_shared_cluster_f32(mapa_shared(my, (uint32_t)q));
-    s_inv[threadIdx.x] = 1.0f / sqrtf(ss / (float)D + a.eps);
+  if (KS > 1) {
+    cluster_sync();
+    if (threadIdx.x < OH_ROWS) {
+      const uint32_t my = smem_u32(&s_ss[threadIdx.x]);
+      float ss = 0.0f;
+      for (int q = 0; q < KS; ++q) ss += ld_shared_cluster_f32(mapa_shared(my, (uint32_t)q));
+      s_inv[threadIdx.x] = 1.0f / sqrtf(ss / (float)D + a.eps);
+    }
+  } else {
+    __syncthreads();
+    if (threadIdx.x < OH_ROWS) s_inv[threadIdx.x] = 1.0f / sqrtf(s_ss[threadIdx.x] / (float)D + a.eps);
   }
   __syncthreads();
 
   // 2. staging roles.  activations: row ar = tid / 2, columns ak..ak+15 of the
-  // chunk; head: float4 slots f = tid + 256 e over PW rows x 8 float4 (rows >= P
+  // chunk; head: float4 slots f = tid + 192 e over PW rows x 8 float4 (rows >= P
   // are zero)
   const int ar = threadIdx.x >> 1, ak = (threadIdx.x & 1) * 16;
   const int my_row = s_row[ar];
   const float my_inv = s_inv[ar];
   const int my_t = s_t[ar];
   constexpr int WSLOTS = Cf::WSLOTS;
-  // the table slice [T][shift, scale][32 columns] of a chunk: one float4 for
-  // each of the first 16 T threads, loaded two chunks ahead
-  const int tb_t = (int)threadIdx.x >> 4, tb_h = ((int)threadIdx.x >> 3) & 1, tb_q = (int)threadIdx.x & 7;
-  const bool tb_on = tb_t < a.T;
-  auto load_tab = [&](int k0) -> float4 {
-    return tb_on ? *reinterpret_cast<const float4*>(a.table + ((size_t)tb_t * 2 + tb_h) * D + k0 + tb_q * 4)
-                 : make_float4(0.f, 0.f, 0.f, 0.f);
+  // the table slice [T][shift, scale][32 columns] of a chunk: float4 slots
+  // f = tid + 192 e over 16 timestep rows x 2 x 8, loaded two chunks ahead
+  auto load_tab = [&](int k0, float4 (&tv)[OH_TSLOTS]) {
+#pragma unroll
+    for (int e = 0; e < OH_TSLOTS; ++e) {
+      const int f = (int)threadIdx.x + e * OH_THREADS;
+      const int tb_t = f >> 4, tb_h = (f >> 3) & 1, tb_q = f & 7;
+      tv[e] = tb_t < a.T ? *reinterpret_cast<const float4*>(a.table + ((size_t)tb_t * 2 + tb_h) * D + k0 + tb_q * 4)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
   };
-  auto put_tab = [&](int tbuf, const float4& tv) {
-    if (tb_on) *reinterpret_cast<float4*>(&s_tab[tbuf][tb_t][tb_h][tb_q * 4]) = tv;
+  auto put_tab = [&](int tbuf, const float4 (&tv)[OH_TSLOTS]) {
+#pragma unroll
+    for (int e = 0; e < OH_TSLOTS; ++e) {
+      const int f = (int)threadIdx.x + e * OH_THREADS;
+      const int tb_t = f >> 4, tb_h = (f >> 3) & 1, tb_q = f & 7;
+      if (tb_t < a.T) *reinterpret_cast<float4*>(&s_tab[tbuf][tb_t][tb_h][tb_q * 4]) = tv[e];
+    }
   };
   auto load_chunk = [&](int k0, uint4 (&xv)[2], float4 (&wv)[WSLOTS]) {
     if (my_row >= 0) {
@@ -426,9 +446,15 @@ __global__ void __launch_bounds__(OH_THREADS, 2) output_head_kernel(const Output
     for (int c = 0; c < PT; ++c) acc[r8][c] = 0.0f;
   uint4 xv[2] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
   float4 wv[WSLOTS];
-  float4 tv = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (k_lo < k_hi) put_tab(0, load_tab(k_lo));
-  if (k_lo + OH_KC < k_hi) put_tab(1, load_tab(k_lo + OH_KC));
+  float4 tv[OH_TSLOTS];
+  if (k_lo < k_hi) {
+    load_tab(k_lo, tv);
+    put_tab(0, tv);
+  }
+  if (k_lo + OH_KC < k_hi) {
+    load_tab(k_lo + OH_KC, tv);
+    put_tab(1, tv);
+  }
   __syncthreads();
   if (k_lo < k_hi) {
     load_chunk(k_lo, xv, wv);
@@ -440,7 +466,7 @@ __global__ void __launch_bounds__(OH_THREADS, 2) output_head_kernel(const Output
     const bool more = k0 + OH_KC < k_hi;
     const bool more2 = k0 + 2 * OH_KC < k_hi;
     if (more) load_chunk(k0 + OH_KC, xv, wv);   // in flight during the products
-    if (more2) tv = load_tab(k0 + 2 * OH_KC);
+    if (more2) load_tab(k0 + 2 * OH_KC, tv);
     const float* sa = s_a + buf * Cf::A_FLOATS;
     const float* sw = s_w + buf * Cf::W_FLOATS;
 #pragma unroll 2
@@ -468,20 +494,33 @@ __global__ void __launch_bounds__(OH_THREADS, 2) output_head_kernel(const Output
     buf ^= 1;
   }
 
-  // 3. partial tile -> shared memory; rank ks reduces its 16 rows over the cluster
+  // 3. the tile: straight out with KS = 1, else partial tiles to shared
+  // memory and rank ks reduces its 96 / KS rows over the cluster
+  if (KS == 1) {
+#pragma unroll
+    for (int r8 = 0; r8 < 8; ++r8) {
+      const int rr = ty * 8 + r8, i = i0 + rr;
+      if (s_row[rr] < 0 || i >= a.n_sel) continue;
+#pragma unroll
+      for (int c = 0; c < PT; ++c) {
+        const int p = tx * PT + c;
+        if (p < P) a.out[(size_t)i * P + p] = acc[r8][c] + (a.b ? a.b[p] : 0.0f);
+      }
+    }
+    return;
+  }
 #pragma unroll
   for (int r8 = 0; r8 < 8; ++r8)
 #pragma unroll
     for (int c = 0; c < PT; ++c) s_tile[(ty * 8 + r8) * PW + tx * PT + c] = acc[r8][c];
   cluster_sync();
-  constexpr int SLICE = OH_ROWS / OH_KS;
-  for (int e = (int)threadIdx.x; e < SLICE * PW; e += OH_THREADS) {
-    const int rr = ks * SLICE + e / PW, p = e % PW;
+  const int slice = OH_ROWS / KS;
+  for (int e = (int)threadIdx.x; e < slice * PW; e += OH_THREADS) {
+    const int rr = ks * slice + e / PW, p = e % PW;
     if (p >= P) continue;
     const uint32_t my = smem_u32(&s_tile[rr * PW + p]);
     float v = 0.0f;
-#pragma unroll
-    for (int q = 0; q < OH_KS; ++q) v += ld_shared_cluster_f32(mapa_shared(my, (uint32_t)q));
+    for (int q = 0; q < KS; ++q) v += ld_shared_cluster_f32(mapa_shared(my, (uint32_t)q));
     const int i = i0 + rr;
     if (s_row[rr] >= 0 && i < a.n_sel) a.out[(size_t)i * P + p] = v + (a.b ? a.b[p] : 0.0f);
   }
@@ -555,26 +594,37 @@ cudaError_t launch_final_adaln(const FinalAdalnArgs& a, cudaStream_t st) {
 }
 
 template <int PT>
-static cudaError_t launch_head(const OutputHeadArgs& a, int clusters, cudaStream_t st) {
+static cudaError_t launch_head(const OutputHeadArgs& a, int tiles, int ks, cudaStream_t st) {
   constexpr int smem = OhCfg<PT>::SMEM;
   cudaError_t e = cudaFuncSetAttribute(output_head_kernel<PT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  return launch_kernel_cluster(output_head_kernel<PT>, dim3(clusters * OH_KS), dim3(OH_THREADS), smem, st, OH_KS, a);
+  return launch_kernel_cluster(output_head_kernel<PT>, dim3(tiles * ks), dim3(OH_THREADS), smem, st, ks, a);
+}
+
+// The k-split: the fewest of 1, 2, 4, 8 CTAs per 96-row tile that give two
+// CTAs per SM (8 when none does).
+static int head_k_split(int tiles) {
+  const int target = 2 * num_sms();
+  const int options[] = {1, 2, 4, OH_MAX_KS};
+  for (int ks : options)
+    if ((long long)tiles * ks >= target) return ks;
+  return OH_MAX_KS;
 }
 
 cudaError_t launch_output_head(const OutputHeadArgs& a, cudaStream_t st) {
-  const int clusters = (a.n_sel + OH_ROWS - 1) / OH_ROWS;
+  const int tiles = (a.n_sel + OH_ROWS - 1) / OH_ROWS;
+  const int ks = head_k_split(tiles);
   const int pt = a.P <= 32 ? 2 : (a.P <= 64 ? 4 : (a.P <= 96 ? 6 : 8));
   cudaError_t e;
   switch (pt) {
-    case 2: e = launch_head<2>(a, clusters, st); break;
-    case 4: e = launch_head<4>(a, clusters, st); break;
-    case 6: e = launch_head<6>(a, clusters, st); break;
-    default: e = launch_head<8>(a, clusters, st); break;
+    case 2: e = launch_head<2>(a, tiles, ks, st); break;
+    case 4: e = launch_head<4>(a, tiles, ks, st); break;
+    case 6: e = launch_head<6>(a, tiles, ks, st); break;
+    default: e = launch_head<8>(a, tiles, ks, st); break;
   }
   if (e != cudaSuccess) return e;
-  set_kernel_info("output_head_kernel<%d> fp32 rows/cluster=%d k-split=%d (cluster, rank-order sums) k_chunk=%d "
-                  "reg-tile=8x%d P=%d rows=%d", pt, OH_ROWS, OH_KS, OH_KC, pt, a.P, a.n_sel);
+  set_kernel_info("output_head_kernel<%d> fp32 rows/tile=%d k-split=%d (cluster, rank-order sums) k_chunk=%d "
+                  "reg-tile=8x%d P=%d rows=%d", pt, OH_ROWS, ks, OH_KC, pt, a.P, a.n_sel);
   return cudaGetLastError();
 }
 

@@ -197,7 +197,7 @@ def test_output_head_widths(h3, D, P, n_rows):
     """Head widths of every register-tile variant (P up to 32, 64, 96, 128),
     a residual width whose 32-column chunks do not split evenly over the eight
     CTAs of a cluster (640: 20 chunks) or leave some of them without chunks
-    (192: 6 chunks), and row counts that end inside a 128-row block."""
+    (192: 6 chunks), and row counts that end inside a 96-row tile."""
     shape = hi.BlockShape(dim=D, n_heads=1, head_dim=128, ffn_dim=256, cond_dim=128)
     T = 3
     g = torch.Generator().manual_seed(D + P)
@@ -216,6 +216,37 @@ def test_output_head_widths(h3, D, P, n_rows):
     ref = OO.output_head(to_np(x), tags.numpy(), tidx.numpy(), OO.TAG_VIDEO, tab.numpy().astype(np.float64),
                          w.numpy(), b.numpy())
     assert_close(v.cpu().numpy(), ref, f"head D={D} P={P}", F32_MAX_E, F32_MEAN_E)
+
+
+@pytest.mark.parametrize("fill", [0.25, 0.6, 1.01, 2.02])
+def test_output_head_every_k_split(h3, fill):
+    """The k-split follows the row count (the fewest CTAs per 96-row tile
+    that give two per SM): selections from a quarter of that target up to
+    twice it take every split, 8, 4, 2 and 1 (the last one without a
+    cluster), each within the fp32 bound of the oracle."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    n_sel = int(fill * sms * 96) - 5
+    tiles = (n_sel + 95) // 96
+    want = next((k for k in (1, 2, 4) if tiles * k >= 2 * sms), 8)
+    D, P, T, n_rows = 320, 96, 2, n_sel + 37
+    g = torch.Generator().manual_seed(n_sel)
+    x = (torch.randn(n_rows, D, generator=g)).to(torch.bfloat16)
+    tidx = torch.randint(0, T, (n_rows,), generator=g, dtype=torch.int32)
+    tab = (torch.randn(T, 2, D, generator=g) * 0.3).to(torch.float32)
+    w = (torch.randn(P, D, generator=g) * 0.02).to(torch.float32)
+    b = (torch.randn(P, generator=g) * 0.02).to(torch.float32)
+    sel = torch.sort(torch.randperm(n_rows, generator=g)[:n_sel]).values.to(torch.int32)
+    tags = torch.ones(n_rows, dtype=torch.int32)
+    tags[sel.long()] = OO.TAG_VIDEO
+    shape = hi.BlockShape(dim=D, n_heads=1, head_dim=128, ffn_dim=256, cond_dim=128)
+    v = torch.full((n_sel, P), float("nan"), dtype=torch.float32, device="cuda")
+    h3.h3_output_head(_cfg(h3, shape), n_rows, n_sel, sel.cuda(), tidx.cuda(), T, x.cuda(), tab.cuda(), w.cuda(),
+                      b.cuda(), P, v)
+    assert h3.h3_sync_check() == 0
+    assert f"k-split={want} " in h3.h3_last_kernel_info()
+    ref = OO.output_head(to_np(x), tags.numpy(), tidx.numpy(), OO.TAG_VIDEO, tab.numpy().astype(np.float64),
+                         w.numpy(), b.numpy())
+    assert_close(v.cpu().numpy(), ref, f"head k-split {want}", F32_MAX_E, F32_MEAN_E)
 
 
 def test_output_head_bad_timestep_is_reported(h3):
