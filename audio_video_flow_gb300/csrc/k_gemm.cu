@@ -63,7 +63,7 @@ struct GemmCfg {
   static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + 256;
 };
 
-// The gated-residual and SwiGLU epilogues of 256-wide tiles stage each
+// The gated-residual, SwiGLU and QKV epilogues of 256-wide tiles stage each
 // epilogue warp's 32 rows x 64 columns (bf16, 4 KB) in shared memory after
 // the barriers, so that their global loads and stores move whole 128-byte
 // lines.
@@ -71,7 +71,7 @@ constexpr int EPI_STAGE_WARP_BYTES = 32 * 128;
 constexpr int EPI_STAGE_BYTES = 8 * EPI_STAGE_WARP_BYTES;
 template <int EPI, int BN>
 __host__ __device__ constexpr bool gemm_staged_epi() {
-  return BN == 256 && (EPI == EPI_RESID || EPI == EPI_SWIGLU);
+  return BN == 256 && (EPI == EPI_RESID || EPI == EPI_SWIGLU || EPI == EPI_QKV);
 }
 template <int EPI, int BN>
 __host__ __device__ constexpr int gemm_smem() {
@@ -598,8 +598,141 @@ __device__ __forceinline__ void epi_v_head(const GemmArgs& a, uint32_t tpart, in
   }
 }
 
+// The warp's staged 64 columns of its 32 rows out to columns [col, col + 64)
+// of each row whose bit is set in ok_rows, as whole lines.
+__device__ __forceinline__ void stage_flush64(const GemmArgs& a, uint8_t* buf, int row0, int col, unsigned ok_rows) {
+  const int lane = (int)(threadIdx.x & 31u);
+  __syncwarp();
+#pragma unroll
+  for (int it = 0; it < 8; ++it) {
+    const int r = it * 4 + (lane >> 3), u = lane & 7;
+    if ((ok_rows >> r) & 1u)
+      *reinterpret_cast<uint4*>(a.out + (size_t)(row0 + r) * a.ldo + col + u * 8) = *stage_unit(buf, r, u);
+  }
+  __syncwarp();
+}
+
+// Sixteen values as two staged 16-byte units of this lane's row.
+__device__ __forceinline__ void stage16(uint8_t* buf, int u0, const float (&v)[16]) {
+  const int lane = (int)(threadIdx.x & 31u);
+#pragma unroll
+  for (int g = 0; g < 2; ++g)
+    *stage_unit(buf, lane, u0 + g) =
+        make_uint4(pack_bf16x2(v[8 * g + 0], v[8 * g + 1]), pack_bf16x2(v[8 * g + 2], v[8 * g + 3]),
+                   pack_bf16x2(v[8 * g + 4], v[8 * g + 5]), pack_bf16x2(v[8 * g + 6], v[8 * g + 7]));
+}
+
+// epi_qk_part through the warp's staging buffer, in two passes of 64
+// channels: pass 1 holds the rotated channels 0..47 and their partners of
+// band t (48..63); the partners of bands h and w (64..95) wait in registers
+// as packed bf16 pairs while pass 1 is written, and join the normed
+// channels 96..127 in pass 2.  Same arithmetic as epi_qk_part.
+__device__ __forceinline__ void epi_qk_part_staged(const GemmArgs& a, uint32_t tpart, int m, bool valid, int h,
+                                                   int part, const float (&pos)[3], uint8_t* buf) {
+  const int lane = (int)(threadIdx.x & 31u);
+  const int row0 = m - lane;
+  const int cb = h * 384 + part * 128;       // output / weight column of channel 0
+  const __nv_bfloat16* gain = part ? a.k_gain : a.q_gain;
+  float ss = 0.f;
+#pragma unroll 1
+  for (int c = 0; c < 4; ++c) {
+    uint32_t r[32];
+    tmem_ld32(tpart + c * 32, r);
+    tmem_ld_wait(r);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const float v = bf16_round(__uint_as_float(r[j]) + bias_at(a.bias, cb + c * 32 + j));
+      ss = __fmaf_rn(v, v, ss);
+    }
+  }
+  const float inv = 1.0f / sqrtf(ss * (1.0f / 128.0f) + a.eps);
+  const bool ok = valid && out_ok(a, a.out + (size_t)m * a.ldo + cb, 128, 6);
+  const unsigned ok_rows = __ballot_sync(0xffffffffu, ok);
+  uint32_t hold[16];                         // channels 64..95, packed pairs
+#pragma unroll 1
+  for (int band = 0; band < 3; ++band) {
+    const float p = band == 0 ? pos[0] : (band == 1 ? pos[1] : pos[2]);
+    uint32_t lo[16], hi[16];
+    tmem_ld16(tpart + band * 16, lo);
+    tmem_ld16(tpart + 48 + band * 16, hi);
+    tmem_ld_wait(lo, hi);
+    float o1[16], o2[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int j = band * 16 + i;
+      float sn, cs;
+      sincosf(p * a.omega[i], &sn, &cs);
+      const float v1 = bf16_round(__uint_as_float(lo[i]) + bias_at(a.bias, cb + j));
+      const float v2 = bf16_round(__uint_as_float(hi[i]) + bias_at(a.bias, cb + 48 + j));
+      const float x1 = bf16_round(v1 * inv * __bfloat162float(gain[j]));
+      const float x2 = bf16_round(v2 * inv * __bfloat162float(gain[48 + j]));
+      o1[i] = __fmaf_rn(x1, cs, -(x2 * sn));
+      o2[i] = __fmaf_rn(x2, cs, x1 * sn);
+    }
+    stage16(buf, 2 * band, o1);              // channels 16 band .. 16 band + 15
+    if (band == 0) {
+      stage16(buf, 6, o2);                   // channels 48..63
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t w = pack_bf16x2(o2[2 * i], o2[2 * i + 1]);
+        if (band == 1) hold[i] = w; else hold[8 + i] = w;
+      }
+    }
+  }
+  stage_flush64(a, buf, row0, cb, ok_rows);
+#pragma unroll
+  for (int g = 0; g < 4; ++g)                 // channels 64..95
+    *stage_unit(buf, lane, g) = make_uint4(hold[4 * g], hold[4 * g + 1], hold[4 * g + 2], hold[4 * g + 3]);
+  uint32_t r[32];
+  tmem_ld32(tpart + 96, r);
+  tmem_ld_wait(r);
+  float v[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const float x = bf16_round(__uint_as_float(r[j]) + bias_at(a.bias, cb + 96 + j));
+    v[j] = x * inv * __bfloat162float(gain[96 + j]);
+  }
+#pragma unroll
+  for (int g = 0; g < 4; ++g)                 // channels 96..127
+    *stage_unit(buf, lane, 4 + g) =
+        make_uint4(pack_bf16x2(v[8 * g + 0], v[8 * g + 1]), pack_bf16x2(v[8 * g + 2], v[8 * g + 3]),
+                   pack_bf16x2(v[8 * g + 4], v[8 * g + 5]), pack_bf16x2(v[8 * g + 6], v[8 * g + 7]));
+  stage_flush64(a, buf, row0, cb + 64, ok_rows);
+}
+
+// epi_v_head through the warp's staging buffer, two 64-column passes.
+__device__ __forceinline__ void epi_v_head_staged(const GemmArgs& a, uint32_t tpart, int m, bool valid, int head,
+                                                  uint8_t* buf) {
+  const int lane = (int)(threadIdx.x & 31u);
+  const int row0 = m - lane;
+  const int cb = head * 384 + 256;
+  const bool ok = valid && head < a.H && out_ok(a, a.out + (size_t)m * a.ldo + cb, 128, 9);
+  const unsigned ok_rows = __ballot_sync(0xffffffffu, ok);
+#pragma unroll 1
+  for (int pass = 0; pass < 2; ++pass) {
+#pragma unroll 1
+    for (int cc = 0; cc < 2; ++cc) {
+      const int c = 2 * pass + cc;
+      uint32_t r[32];
+      tmem_ld32(tpart + c * 32, r);
+      tmem_ld_wait(r);
+      float v[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]) + bias_at(a.bias, cb + c * 32 + j);
+#pragma unroll
+      for (int g = 0; g < 4; ++g)
+        *stage_unit(buf, lane, cc * 4 + g) =
+            make_uint4(pack_bf16x2(v[8 * g + 0], v[8 * g + 1]), pack_bf16x2(v[8 * g + 2], v[8 * g + 3]),
+                       pack_bf16x2(v[8 * g + 4], v[8 * g + 5]), pack_bf16x2(v[8 * g + 6], v[8 * g + 7]));
+    }
+    stage_flush64(a, buf, row0, cb + 64 * pass, ok_rows);
+  }
+}
+
 template <int BN>
-__device__ __forceinline__ void epi_qkv(const GemmArgs& a, uint32_t tacc, int m, bool valid, int n_blk, int half) {
+__device__ __forceinline__ void epi_qkv(const GemmArgs& a, uint32_t tacc, int m, bool valid, int n_blk, int half,
+                                        uint8_t* stage_buf) {
   float pos[3] = {0.f, 0.f, 0.f};
   if (valid) {
 #pragma unroll
@@ -616,10 +749,10 @@ __device__ __forceinline__ void epi_qkv(const GemmArgs& a, uint32_t tacc, int m,
       pos[ax] = (float)p;
     }
   }
-  if (BN == 256) {
+  if constexpr (BN == 256) {
     // q | k of head n_blk (one part per column half), or v of heads 2p, 2p+1
-    if (n_blk < a.H) epi_qk_part(a, tacc + half * 128, m, valid, n_blk, half, pos);
-    else epi_v_head(a, tacc + half * 128, m, valid, 2 * (n_blk - a.H) + half);
+    if (n_blk < a.H) epi_qk_part_staged(a, tacc + half * 128, m, valid, n_blk, half, pos, stage_buf);
+    else epi_v_head_staged(a, tacc + half * 128, m, valid, 2 * (n_blk - a.H) + half, stage_buf);
   } else if (half == 0) {
     // one 128-column part: its norm needs all of it in one warp
     const int head = n_blk / 3, part = n_blk % 3;
@@ -806,7 +939,7 @@ __device__ __forceinline__ void run_epilogue(const GemmArgs& a, uint32_t tacc, i
     static_assert(gemm_staged_epi<EPI, BN>(), "SwiGLU tiles are 256 wide (128 gate + 128 value columns)");
     epi_swiglu_staged(a, tacc, m, valid, n_blk, half, stage_buf);
   }
-  if (EPI == EPI_QKV) epi_qkv<BN>(a, tacc, m, valid, n_blk, half);
+  if (EPI == EPI_QKV) epi_qkv<BN>(a, tacc, m, valid, n_blk, half, stage_buf);
 }
 
 }  // namespace
