@@ -626,22 +626,39 @@ __global__ void __launch_bounds__(AT2_THREADS, 1)
       tc_fence_after();
       const float inv_l = 1.0f / l_run;
       const int HD = args.H * 128;
+      // The normalised rows go out through the K ring, idle now (the
+      // o_final commit covers every S MMA, and no K load is left in flight):
+      // each warp stages its 32 rows x 128 channels (8 KB, 16-byte unit u of
+      // row r at unit u ^ (r & 7)), then two rows per store instruction
+      // leave as whole lines.
+      uint8_t* stg = sK + (size_t)(warp - 4) * 8192;
+      const int grow0 = grow - lane;
+      const bool row_ok = grow < S && in_bounds<__nv_bfloat16>(args.o, args.o_elems,
+                                                               args.o + (size_t)grow * HD + head * 128, 128, args.err,
+                                                               12);
+      const unsigned ok_rows = __ballot_sync(0xffffffffu, row_ok);
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         uint32_t o[32];
         tmem_ld32(o_base + (uint32_t)(c * 32), o);
         tmem_ld_wait(o);
-        if (grow < S && in_bounds<__nv_bfloat16>(args.o, args.o_elems,
-                                                 args.o + (size_t)grow * HD + head * 128 + c * 32, 32, args.err, 12)) {
-          uint4* dst = reinterpret_cast<uint4*>(args.o + (size_t)grow * HD + head * 128 + c * 32);
 #pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            dst[g] = make_uint4(pack_bf16x2(__uint_as_float(o[g * 8 + 0]) * inv_l, __uint_as_float(o[g * 8 + 1]) * inv_l),
-                                pack_bf16x2(__uint_as_float(o[g * 8 + 2]) * inv_l, __uint_as_float(o[g * 8 + 3]) * inv_l),
-                                pack_bf16x2(__uint_as_float(o[g * 8 + 4]) * inv_l, __uint_as_float(o[g * 8 + 5]) * inv_l),
-                                pack_bf16x2(__uint_as_float(o[g * 8 + 6]) * inv_l, __uint_as_float(o[g * 8 + 7]) * inv_l));
-          }
+        for (int g = 0; g < 4; ++g) {
+          const int u = c * 4 + g;
+          *reinterpret_cast<uint4*>(stg + lane * 256 + ((u ^ (lane & 7)) << 4)) =
+              make_uint4(pack_bf16x2(__uint_as_float(o[g * 8 + 0]) * inv_l, __uint_as_float(o[g * 8 + 1]) * inv_l),
+                         pack_bf16x2(__uint_as_float(o[g * 8 + 2]) * inv_l, __uint_as_float(o[g * 8 + 3]) * inv_l),
+                         pack_bf16x2(__uint_as_float(o[g * 8 + 4]) * inv_l, __uint_as_float(o[g * 8 + 5]) * inv_l),
+                         pack_bf16x2(__uint_as_float(o[g * 8 + 6]) * inv_l, __uint_as_float(o[g * 8 + 7]) * inv_l));
         }
+      }
+      __syncwarp();
+#pragma unroll 4
+      for (int it = 0; it < 16; ++it) {
+        const int r = it * 2 + (lane >> 4), u = lane & 15;
+        if ((ok_rows >> r) & 1u)
+          *reinterpret_cast<uint4*>(args.o + (size_t)(grow0 + r) * HD + head * 128 + u * 8) =
+              *reinterpret_cast<const uint4*>(stg + r * 256 + ((u ^ (r & 7)) << 4));
       }
       if (args.lse != nullptr && grow < S)
         if (in_bounds<float>(args.lse, args.lse_elems, args.lse + (size_t)head * S + grow, 1, args.err, 13))
