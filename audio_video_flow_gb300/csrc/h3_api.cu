@@ -506,7 +506,11 @@ h3_status check_block_weights(const h3_block_weights* w) {
   return H3_OK;
 }
 
-// SMs for the AdaLN chunks 2-5 on the side stream, 0 when the table is not
+// Table chunks of one block computed on the caller's stream when the rest
+// goes to the side stream: shift, scale and gate of the attention half.
+constexpr int kMainChunks = 3;
+
+// SMs for the AdaLN chunks 3-5 on the side stream, 0 when the table is not
 // split: the split needs D a multiple of 128 (whole chunks per weight tile)
 // and pays only when the QKV GEMM leaves at least 8 SMs free at its wave
 // count (short documents); otherwise every SM already has GEMM work.
@@ -582,11 +586,12 @@ h3_status block_impl(const h3_block_config* cfg, const h3_block_weights* w, cons
 #define H3_TRY(expr)            \
   if ((s = (expr)) != H3_OK) return s; \
   if ((s = mark()) != H3_OK) return s;
-  // Stage 0, the AdaLN table.  norm1 reads only chunks 0-1 (shift_msa,
-  // scale_msa); chunk 2 is first read by the O projection.  Chunks 0-1 run on
-  // the caller's stream; chunks 2-5 (two thirds of the weight stream) run on
-  // the side stream on the SMs that the QKV GEMM's wave count leaves free,
-  // and the caller's stream waits for them before the O projection.
+  // Stage 0, the AdaLN table.  norm1 reads chunks 0-1 (shift_msa,
+  // scale_msa) and the O projection chunk 2 (gate_msa); chunks 3-5 are first
+  // read by norm2.  Chunks 0-2 run on the caller's stream; chunks 3-5 (half
+  // of the weight stream) run on the side stream on the SMs that the QKV
+  // GEMM's wave count leaves free, and the caller's stream waits for them
+  // before norm2.
   if (!table_pre) {
     s = run_silu(*cfg, meta->t_cond, T, u, st, sk.flags, (int)L.zero_words);
     if (s != H3_OK) return s;
@@ -609,7 +614,7 @@ h3_status block_impl(const h3_block_config* cfg, const h3_block_weights* w, cons
   int qkv_ctas = 0;
   if (side) {
     qkv_ctas = num_sms() - side_ctas;
-    if ((s = run_adaln_chunks(*cfg, w->w_ada, w->b_ada, T, table, u, 0, 2, 0, st)) != H3_OK) return s;
+    if ((s = run_adaln_chunks(*cfg, w->w_ada, w->b_ada, T, table, u, 0, kMainChunks, 0, st)) != H3_OK) return s;
     if (cudaEventRecord(ev_a, st) != cudaSuccess || cudaStreamWaitEvent(side, ev_a, 0) != cudaSuccess)
       return H3_ERR_CUDA;
     if (events && n_events > 8 && events[8] &&
@@ -623,7 +628,8 @@ h3_status block_impl(const h3_block_config* cfg, const h3_block_weights* w, cons
     // GEMM's SMs, took 55 instead of 61 us, but the plain block took 0.408
     // instead of 0.387 ms: each cross-stream wait ends the programmatic
     // overlap of the kernel after it.)
-    if ((s = run_adaln_chunks(*cfg, w->w_ada, w->b_ada, T, table, u, 2, 6, side_ctas, side)) != H3_OK) return s;
+    if ((s = run_adaln_chunks(*cfg, w->w_ada, w->b_ada, T, table, u, kMainChunks, 6, side_ctas, side)) != H3_OK)
+      return s;
     if (events && n_events > 9 && events[9] &&
         cudaEventRecord(static_cast<cudaEvent_t>(events[9]), side) != cudaSuccess)
       return H3_ERR_CUDA;
@@ -639,15 +645,18 @@ h3_status block_impl(const h3_block_config* cfg, const h3_block_weights* w, cons
     const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(qkv);
     H3_TRY(run_attention(S, cfg->n_heads, q, q + 128, q + 256, 3 * I, 384, o, nullptr, st));
   }
-  if (side && cudaStreamWaitEvent(st, ev_b, 0) != cudaSuccess) return H3_ERR_CUDA;
   // norm2 + modulation rides in the O projection's epilogue when that GEMM
-  // runs stream-K; otherwise it is its own kernel
+  // runs stream-K and H3_NORM_FUSE is set (it then needs chunks 3-4 before
+  // the O projection); otherwise it is its own kernel
+  const bool may_fuse = norm_fuse_enabled();
+  if (side && may_fuse && cudaStreamWaitEvent(st, ev_b, 0) != cudaSuccess) return H3_ERR_CUDA;
   bool fused = false;
   const NormFuse nf{h, w->norm2_g, 3, 4};
   H3_TRY(run_resid_gemm(*cfg, *meta, table, 2, o, I, w->w_o, w->b_o, x_in, x1, st, &sk, &nf, &fused));
   if (fused) {
     if ((s = mark()) != H3_OK) return s;
   } else {
+    if (side && !may_fuse && cudaStreamWaitEvent(st, ev_b, 0) != cudaSuccess) return H3_ERR_CUDA;
     H3_TRY(run_modulate(*cfg, *meta, table, 1, x1, w->norm2_g, h, st));
   }
   H3_TRY(run_ffn_up(*cfg, S, h, w->w_fc1, w->b_fc1, qkv, st));

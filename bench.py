@@ -65,7 +65,7 @@ TRAFFIC = {
 # ---------------------------------------------------------------------------
 
 def adaln_split(shape, S: int) -> bool:
-    """True when the library computes AdaLN chunks 2-5 on its side stream."""
+    """True when the library computes AdaLN chunks 3-5 on its side stream."""
     import audio_video_flow_gb300 as h3
     cfg = h3.make_config(shape.dim, shape.n_heads, shape.ffn_dim, shape.cond_dim)
     return h3.h3_block_adaln_side_ctas(cfg, S) > 0
@@ -74,11 +74,11 @@ def adaln_split(shape, S: int) -> bool:
 def stage_work(shape, S: int, T: int, split: bool = False):
     """(flops, bytes) per stage of one block: the method's own dense work and
     the bytes each kernel must move at least once.  With the AdaLN split, the
-    critical-path stage covers chunks 0-1 and adaln_table_side chunks 2-5."""
+    critical-path stage covers chunks 0-2 and adaln_table_side chunks 3-5."""
     D, I, F, C = shape.dim, shape.n_heads * shape.head_dim, shape.ffn_dim, shape.cond_dim
     b = 2  # bf16
     ada = (2.0 * T * C * 18 * D, 18 * D * C * b + T * C * 4 + T * 18 * D * b)
-    frac = 2.0 / 6.0 if split else 1.0
+    frac = 3.0 / 6.0 if split else 1.0
     return {
         "adaln_table": (ada[0] * frac, ada[1] * frac),
         "adaln_table_side": (ada[0] * (1 - frac), ada[1] * (1 - frac)),
