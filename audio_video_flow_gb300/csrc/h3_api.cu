@@ -620,14 +620,13 @@ h3_status block_impl(const h3_block_config* cfg, const h3_block_weights* w, cons
     if (events && n_events > 8 && events[8] &&
         cudaEventRecord(static_cast<cudaEvent_t>(events[8]), side) != cudaSuccess)
       return H3_ERR_CUDA;
-    // (Launching the gate chunk on its own first, so that the O projection
-    // would not wait for chunks 3-5, measured slower at 505 rows: the QKV
-    // GEMM beside the two side launches took 133 instead of 102 us.  With
-    // chunks 3-5 launched after the QKV GEMM and without programmatic early
-    // start, the GEMM kept its 102 us and the O projection, capped at the
-    // GEMM's SMs, took 55 instead of 61 us, but the plain block took 0.408
-    // instead of 0.387 ms: each cross-stream wait ends the programmatic
-    // overlap of the kernel after it.)
+    // (Two side launches, the gate chunk first so that the O projection
+    // would wait for it alone, measured slower at 505 rows: the QKV GEMM
+    // beside them took 133 instead of 102 us.  With the second launched
+    // after the QKV GEMM and without programmatic early start, the GEMM
+    // kept its 102 us, but the plain block took 0.408 instead of 0.387 ms:
+    // each cross-stream wait ends the programmatic overlap of the kernel
+    // after it.  Hence one side launch, and the gate on this stream.)
     if ((s = run_adaln_chunks(*cfg, w->w_ada, w->b_ada, T, table, u, kMainChunks, 6, side_ctas, side)) != H3_OK)
       return s;
     if (events && n_events > 9 && events[9] &&
