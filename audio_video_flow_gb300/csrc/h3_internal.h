@@ -27,10 +27,13 @@ int num_sms();
 // the previous kernel on the stream finishes; it synchronises with
 // griddepcontrol.wait).  H3_NO_PDL=1 in the environment launches without it.
 bool pdl_enabled();
-// cluster_x > 1 launches clusters of cluster_x CTAs along x.
+// cluster_x > 1 launches clusters of cluster_x CTAs along x.  early = false
+// launches in plain stream order (griddepcontrol.wait then returns at once;
+// the kernel's own griddepcontrol.launch_dependents still lets the next
+// kernel start early).
 template <typename... KArgs, typename... Args>
-cudaError_t launch_kernel_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
-                                  int cluster_x, Args&&... args) {
+cudaError_t launch_kernel_ex(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                             int cluster_x, bool early, Args&&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
@@ -38,7 +41,7 @@ cudaError_t launch_kernel_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 bloc
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   int n = 0;
-  if (pdl_enabled()) {
+  if (early && pdl_enabled()) {
     attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[n].val.programmaticStreamSerializationAllowed = 1;
     ++n;
@@ -55,9 +58,14 @@ cudaError_t launch_kernel_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 bloc
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
 }
 template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                                  int cluster_x, Args&&... args) {
+  return launch_kernel_ex(kernel, grid, block, smem, stream, cluster_x, true, static_cast<Args&&>(args)...);
+}
+template <typename... KArgs, typename... Args>
 cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
                           Args&&... args) {
-  return launch_kernel_cluster(kernel, grid, block, smem, stream, 1, static_cast<Args&&>(args)...);
+  return launch_kernel_ex(kernel, grid, block, smem, stream, 1, true, static_cast<Args&&>(args)...);
 }
 // Device address of the error words of the current device: [0] the error
 // bits (DEVERR_*), [1] the site of the first timed-out wait (kernel id in the

@@ -677,6 +677,16 @@ __global__ void __launch_bounds__(AT2_THREADS, 1)
 // Two query tiles per CTA (measured faster at every length down to 505
 // rows); H3_ATTN_QTILES=1 in the environment selects the one-tile kernel
 // (tests cover both).
+//
+// A grid of one wave or less starts in plain stream order, not early beside
+// the kernel before it.  Measured with per-CTA clock stamps at 505 rows (112
+// CTAs): CTAs that started early and passed griddepcontrol.wait when the QKV
+// GEMM ended lived 19 us against 11.6 us.  The extra time fell on the code
+// that each CTA runs first (the first softmax step, the masked last one, the
+// output stores) and on the first MMAs.  The middle softmax steps ran at the
+// same speed either way.  The block took 368 instead of 374 us.  At three
+// waves (1824 rows) only the first wave starts early, and the two launch
+// modes measured the same.
 cudaError_t launch_attention(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                              const AttnArgs& a, cudaStream_t stream) {
   int qtiles = 2;
@@ -684,6 +694,8 @@ cudaError_t launch_attention(const CUtensorMap& tmQ, const CUtensorMap& tmK, con
     const int f = atoi(env);
     if (f == 1 || f == 2) qtiles = f;
   }
+  const long long ctas = (long long)(qtiles == 2 ? (a.S + 255) / 256 : (a.S + 127) / 128) * a.H;
+  const bool early = ctas > num_sms();
   static_assert(tmem_footprint_exclusive(AT_SMEM) && tmem_footprint_exclusive(AT2_SMEM),
                 "an attention CTA must hold its SM's TMEM alone");
   if (!tmem_exclusive(qtiles == 2 ? AT2_SMEM : AT_SMEM)) return cudaErrorNotSupported;
@@ -692,20 +704,21 @@ cudaError_t launch_attention(const CUtensorMap& tmQ, const CUtensorMap& tmK, con
     e = cudaFuncSetAttribute(attention_kernel_2q, cudaFuncAttributeMaxDynamicSharedMemorySize, AT2_SMEM);
     if (e != cudaSuccess) return e;
     const dim3 grid((unsigned)((a.S + 255) / 256), (unsigned)a.H);
-    e = launch_kernel(attention_kernel_2q, grid, dim3(AT2_THREADS), AT2_SMEM, stream, tmQ, tmK, tmV, a);
+    e = launch_kernel_ex(attention_kernel_2q, grid, dim3(AT2_THREADS), AT2_SMEM, stream, 1, early, tmQ, tmK, tmV, a);
     if (e != cudaSuccess) return e;
     set_kernel_info("attention_kernel_2q tcgen05.mma.cta_group::1.kind::f16 q_tiles=2x128 kv_tile=128 "
-                    "k_stages=%d v_stages=%d acc=f32 tmem=S_A,S_B,O_A,O_B P-in-TMEM lazy-rescale=%g grid=%ux%u",
-                    KST, VST, (double)kRescaleThreshold, grid.x, grid.y);
+                    "k_stages=%d v_stages=%d acc=f32 tmem=S_A,S_B,O_A,O_B P-in-TMEM lazy-rescale=%g grid=%ux%u "
+                    "early-start=%d",
+                    KST, VST, (double)kRescaleThreshold, grid.x, grid.y, early ? 1 : 0);
   } else {
     e = cudaFuncSetAttribute(attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, AT_SMEM);
     if (e != cudaSuccess) return e;
     const dim3 grid((unsigned)((a.S + 127) / 128), (unsigned)a.H);
-    e = launch_kernel(attention_kernel, grid, dim3(AT_THREADS), AT_SMEM, stream, tmQ, tmK, tmV, a);
+    e = launch_kernel_ex(attention_kernel, grid, dim3(AT_THREADS), AT_SMEM, stream, 1, early, tmQ, tmK, tmV, a);
     if (e != cudaSuccess) return e;
     set_kernel_info("attention_kernel tcgen05.mma.cta_group::1.kind::f16 q_tile=128 kv_tile=128 k_stages=%d "
-                    "v_stages=%d acc=f32 tmem=S0,S1,O softmax=fp32-online grid=%ux%u",
-                    KST, VST, grid.x, grid.y);
+                    "v_stages=%d acc=f32 tmem=S0,S1,O softmax=fp32-online grid=%ux%u early-start=%d",
+                    KST, VST, grid.x, grid.y, early ? 1 : 0);
   }
   return cudaGetLastError();
 }

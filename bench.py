@@ -49,14 +49,14 @@ STAGES = ("adaln_table", "norm1_modulate", "qkv_qknorm_rope", "attention", "out_
 # reading q, k, v and writing o once (K/V re-reads hit L2), so the 32,768-
 # and 15,860-row values are the 16,384-row capture scaled by the row count.
 TRAFFIC = {
-    "qkv_qknorm_rope@block505": 252609792,
-    "fc1_swiglu@block505": 333535232,
-    "qkv_qknorm_rope@block1824": 333443072,
-    "fc1_swiglu@block1824": 378129664,
-    "attention@attn4096": 213996544,
-    "attention@attn16384": 918765312,
-    "attention@attn32768": 1837530624,
-    "attention@denoiser15860": 889380972,
+    "qkv_qknorm_rope@block505": 252525312,
+    "fc1_swiglu@block505": 332613888,
+    "qkv_qknorm_rope@block1824": 328294144,
+    "fc1_swiglu@block1824": 378740736,
+    "attention@attn4096": 214936064,
+    "attention@attn16384": 921477120,
+    "attention@attn32768": 1842954240,
+    "attention@denoiser15860": 892006050,
 }
 
 
