@@ -233,8 +233,9 @@ __global__ void __launch_bounds__(FA_THREADS, fa_ctas_per_sm(TT)) final_adaln_ke
 }
 
 // ---------------------------------------------------------------------------
-// Velocity head.  A cluster of KS CTAs (KS in {1, 2, 4, 8}: the fewest that
-// give two CTAs per SM, else 8) takes 96 selected rows and all P columns (P
+// Velocity head.  A cluster of KS CTAs (KS in {1, 2, 4, 8, 16}: the fewest
+// that give two CTAs per SM, else 16 where the device runs clusters of 16,
+// else 8) takes 96 selected rows and all P columns (P
 // padded to 16 * PT, PT in {2, 4, 6, 8}); CTA rank ks of the cluster owns the
 // ks-th of KS contiguous ranges of the reduction axis D (whole 32-column
 // chunks).  The 14,580 video rows of an evaluation make 152 tiles in pairs:
@@ -257,7 +258,7 @@ __global__ void __launch_bounds__(FA_THREADS, fa_ctas_per_sm(TT)) final_adaln_ke
 // For a given row count every output is one fixed-order fp32 sum.
 // Rows whose metadata is out of range are reported and left unwritten.
 // ---------------------------------------------------------------------------
-constexpr int OH_ROWS = 96, OH_KC = 32, OH_THREADS = 192, OH_MAX_KS = 8;
+constexpr int OH_ROWS = 96, OH_KC = 32, OH_THREADS = 192, OH_MAX_KS = 16;
 static_assert(OH_ROWS == 8 * (OH_THREADS / 16), "16 column groups x 8-row groups cover the tile");
 static_assert(OH_THREADS == 2 * OH_ROWS, "two staging threads per row");
 static_assert(OH_ROWS % OH_MAX_KS == 0, "every k-split divides the rows");
@@ -593,27 +594,52 @@ cudaError_t launch_final_adaln(const FinalAdalnArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+// The k-split: the fewest of 1, 2, 4, 8 CTAs per 96-row tile that give two
+// CTAs per SM; when none does, 16 (a cluster size beyond the portable 8,
+// taken only where the device can hold such a cluster of this kernel), else
+// 8.  A short selection such as the 1024 audio rows (11 tiles) then walks 10
+// or 11 chunks of 32 columns per CTA instead of 21: its chunks are short, so
+// each waits for its global loads, and the time follows the chunk count.
 template <int PT>
-static cudaError_t launch_head(const OutputHeadArgs& a, int tiles, int ks, cudaStream_t st) {
+static cudaError_t launch_head(const OutputHeadArgs& a, int tiles, int& ks, cudaStream_t st) {
   constexpr int smem = OhCfg<PT>::SMEM;
   cudaError_t e = cudaFuncSetAttribute(output_head_kernel<PT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  return launch_kernel_cluster(output_head_kernel<PT>, dim3(tiles * ks), dim3(OH_THREADS), smem, st, ks, a);
-}
-
-// The k-split: the fewest of 1, 2, 4, 8 CTAs per 96-row tile that give two
-// CTAs per SM (8 when none does).
-static int head_k_split(int tiles) {
   const int target = 2 * num_sms();
-  const int options[] = {1, 2, 4, OH_MAX_KS};
-  for (int ks : options)
-    if ((long long)tiles * ks >= target) return ks;
-  return OH_MAX_KS;
+  ks = 0;
+  for (int k : {1, 2, 4, 8})
+    if (ks == 0 && (long long)tiles * k >= target) ks = k;
+  if (ks == 0) {
+    ks = 8;
+    if (cudaFuncSetAttribute(output_head_kernel<PT>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+        cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3((unsigned)(tiles * OH_MAX_KS));
+      cfg.blockDim = dim3(OH_THREADS);
+      cfg.dynamicSmemBytes = smem;
+      cfg.stream = st;
+      cudaLaunchAttribute attr;
+      attr.id = cudaLaunchAttributeClusterDimension;
+      attr.val.clusterDim.x = OH_MAX_KS;
+      attr.val.clusterDim.y = 1;
+      attr.val.clusterDim.z = 1;
+      cfg.attrs = &attr;
+      cfg.numAttrs = 1;
+      int clusters = 0;
+      if (cudaOccupancyMaxActiveClusters(&clusters, output_head_kernel<PT>, &cfg) == cudaSuccess && clusters >= 1)
+        ks = OH_MAX_KS;
+      else
+        (void)cudaGetLastError();   // the query's error is not this launch's
+    } else {
+      (void)cudaGetLastError();
+    }
+  }
+  return launch_kernel_cluster(output_head_kernel<PT>, dim3(tiles * ks), dim3(OH_THREADS), smem, st, ks, a);
 }
 
 cudaError_t launch_output_head(const OutputHeadArgs& a, cudaStream_t st) {
   const int tiles = (a.n_sel + OH_ROWS - 1) / OH_ROWS;
-  const int ks = head_k_split(tiles);
+  int ks = 0;
   const int pt = a.P <= 32 ? 2 : (a.P <= 64 ? 4 : (a.P <= 96 ? 6 : 8));
   cudaError_t e;
   switch (pt) {

@@ -218,16 +218,17 @@ def test_output_head_widths(h3, D, P, n_rows):
     assert_close(v.cpu().numpy(), ref, f"head D={D} P={P}", F32_MAX_E, F32_MEAN_E)
 
 
-@pytest.mark.parametrize("fill", [0.25, 0.6, 1.01, 2.02])
+@pytest.mark.parametrize("fill", [0.1, 0.25, 0.6, 1.01, 2.02])
 def test_output_head_every_k_split(h3, fill):
     """The k-split follows the row count (the fewest CTAs per 96-row tile
-    that give two per SM): selections from a quarter of that target up to
-    twice it take every split, 8, 4, 2 and 1 (the last one without a
-    cluster), each within the fp32 bound of the oracle."""
+    that give two per SM): selections from a tenth of that target up to
+    twice it take every split, 16, 8, 4, 2 and 1 (16 in a cluster beyond the
+    portable size, 1 without a cluster), each within the fp32 bound of the
+    oracle."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     n_sel = int(fill * sms * 96) - 5
     tiles = (n_sel + 95) // 96
-    want = next((k for k in (1, 2, 4) if tiles * k >= 2 * sms), 8)
+    want = next((k for k in (1, 2, 4, 8) if tiles * k >= 2 * sms), 16)
     D, P, T, n_rows = 320, 96, 2, n_sel + 37
     g = torch.Generator().manual_seed(n_sel)
     x = (torch.randn(n_rows, D, generator=g)).to(torch.bfloat16)
