@@ -233,6 +233,30 @@ def test_attention(h3, name, attn_qtiles):
         assert np.abs(p_gpu - p_ref).max() <= 1e-3, f"probabilities head {h}"
 
 
+@pytest.mark.parametrize("S,qtiles", [(256, "2"), (505, "2"), (505, "1"), (1824, "2")])
+def test_attention_start_mode_follows_wave_count(h3, S, qtiles, monkeypatch):
+    """A grid of at most one wave (CTAs <= SMs) starts in plain stream order,
+    since CTAs that start early beside the kernel before them measured slower.
+    A longer grid may start early.  The provenance string says which, and the
+    output is bitwise repeatable either way."""
+    monkeypatch.setenv("H3_ATTN_QTILES", qtiles)
+    H = 56
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    ctas = -(-S // (128 * int(qtiles))) * H
+    g = torch.Generator().manual_seed(S)
+    buf = torch.randn(S, H, 3, 128, generator=g).to(torch.bfloat16).cuda()
+    outs = []
+    for _ in range(2):
+        o = torch.empty(S, H * 128, dtype=torch.bfloat16, device="cuda")
+        h3.h3_attention(S, H, buf[:, :, 0], buf[:, :, 1], buf[:, :, 2], H * 384, 384, o, None)
+        assert h3.h3_sync_check() == 0
+        outs.append(o)
+    info = h3.h3_last_kernel_info()
+    assert f"early-start={1 if ctas > sms else 0}" in info, info
+    assert torch.equal(outs[0], outs[1])
+    assert torch.isfinite(outs[0].float()).all()
+
+
 @pytest.mark.parametrize("name", CASE_NAMES)
 def test_out_projection(h3, name, gemm_bn):
     c = get_case(name)
