@@ -315,17 +315,30 @@ void gemm_set_plan(GemmArgs& a, const GemmPlan& p) {
   a.nw2 = p.nw2;
 }
 
-// Stream-K fields of a launch with sk_lane pairs per row tile (see GemmArgs).
-void gemm_set_sk(GemmArgs& a, int sk_lane, SkScratch* sk) {
-  a.sk_lane = sk_lane;
-  a.sk_units = a.num_m * sk_lane;
-  a.sk_iters = (long long)a.num_n * a.num_k;
+// Stream-K fields of a launch with sk_lane pairs per row tile (see GemmArgs),
+// or, with tail_units > 0, of a launch whose first dp tiles run whole and
+// whose remaining tiles form one lane of tail_units pairs.
+void gemm_set_sk(GemmArgs& a, int sk_lane, SkScratch* sk, int tail_units = 0, int dp = 0) {
+  if (tail_units > 0) {
+    a.sk_tail = 1;
+    a.sk_dp = dp;
+    a.sk_lane = tail_units;
+    a.sk_units = tail_units;
+    a.sk_iters = ((long long)a.num_m * a.num_n - dp) * a.num_k;
+  } else {
+    a.sk_lane = sk_lane;
+    a.sk_units = a.num_m * sk_lane;
+    a.sk_iters = (long long)a.num_n * a.num_k;
+  }
   a.sk_part = sk->part;
   a.sk_flags = sk->flags;
   a.sk_epoch = ++sk->epoch;
-  // H3_GEMM_L2HINT=0 turns the L2 eviction hints of stream-K launches off
+  // H3_GEMM_L2HINT=0 turns the L2 eviction hints of stream-K launches off.
+  // They serve the lanes of short documents (every row tile's lane streams
+  // the same weight k-blocks while its pairs reread the activations); a tail
+  // launch walks whole tiles first, as a plain launch does, and loads plainly.
   const char* h = getenv("H3_GEMM_L2HINT");
-  a.l2_hint = (h && h[0] == '0') ? 0 : 1;
+  a.l2_hint = (tail_units > 0 || (h && h[0] == '0')) ? 0 : 1;
   // H3_SK_FLAG_TEST=1 (tests of the failure path only): owners wait for a
   // flag value that no partial writer sets, so every owner's bounded wait
   // runs out and the launch reports H3_ERR_TIMEOUT through h3_sync_check
@@ -438,8 +451,15 @@ h3_status run_resid_gemm(const h3_block_config& c, const h3_packed_meta& m, cons
   if (fused) *fused = false;
   const int S = m.n_rows, D = c.dim;
   GemmPlan pl = gemm_plan(EPI_RESID, S, D, 0, 0);
-  const int sk_lane = sk ? gemm_sk_lane(S, D, K, 256, 0) : 0;
-  if (sk_lane > 0) pl = sk_plan(EPI_RESID, D, 0, 0);   // whole-width tiles, k-blocks shared out
+  // stream-K: lanes of pairs per row tile for short documents; for long ones
+  // whole tiles with the last waves' k-blocks shared out over every pair
+  // (H3_GEMM_SK_TAIL=n forces the second form with n pairs)
+  int tail_units = 0, dp = -1;
+  if (sk) dp = gemm_sk_tail(S, D, K, 256, &tail_units);
+  const bool forced_tail = getenv("H3_GEMM_SK_TAIL") != nullptr;
+  const int sk_lane = (sk && !(forced_tail && dp >= 0)) ? gemm_sk_lane(S, D, K, 256, 0) : 0;
+  if (sk_lane > 0 || dp < 0) tail_units = 0;
+  if (sk_lane > 0 || tail_units > 0) pl = sk_plan(EPI_RESID, D, 0, 0);   // whole-width tiles, k-blocks shared out
   CUtensorMap tA, tB;
   if (!make_tmap_2d(&tA, act, S, K, K, 128) || !make_tmap_2d(&tB, w, D, K, K, (uint32_t)pl.b_rows))
     return H3_ERR_CUDA;
@@ -459,6 +479,7 @@ h3_status run_resid_gemm(const h3_block_config& c, const h3_packed_meta& m, cons
   a.tag = m.token_tag;
   a.tidx = m.timestep_index;
   if (sk_lane > 0) gemm_set_sk(a, sk_lane, sk);
+  else if (tail_units > 0) gemm_set_sk(a, 0, sk, tail_units, dp);
   // the fused norm needs every pair resident (stream-K) and runs of at most
   // two whole tiles plus a partial piece (each warp keeps four owned tiles)
   if (nf && sk->nrm_cnt && norm_fuse_fits(sk_lane, a.num_n, a.num_k)) {

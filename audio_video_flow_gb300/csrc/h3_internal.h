@@ -142,9 +142,16 @@ struct GemmArgs {
   // inside a tile writes that tile's partial accumulator to sk_part and sets
   // its flags to sk_epoch; the pair whose run holds the tile's first k-block
   // adds the partials (in k order) and runs the epilogue.
-  int sk_units;          // num_m * sk_lane
-  int sk_lane;           // pairs per 256-row tile
-  long long sk_iters;    // num_n * num_k, the k-blocks of one lane
+  // With sk_tail = 1 there is one lane instead, over all sk_units pairs:
+  // the first sk_dp tiles (a multiple of sk_units) run whole, tile u + i *
+  // sk_units on pair u as in a whole-tile launch, and the k-blocks of tiles
+  // [sk_dp, num_m * num_n) (in the whole-tile launch order) are cut into
+  // sk_units equal runs that follow them.
+  int sk_units;          // num_m * sk_lane, or the pairs of the one lane (sk_tail)
+  int sk_lane;           // pairs per 256-row tile (sk_tail: sk_units)
+  long long sk_iters;    // the k-blocks of one lane: num_n * num_k (sk_tail: the tail tiles' k-blocks)
+  int sk_tail;           // 1: whole tiles first, then one stream-K lane over the remaining tiles
+  int sk_dp;             // sk_tail: the tiles that run whole
   float* sk_part;        // [sk_units][2 CTAs][BN/32 chunks][8 groups][128 rows][4] fp32
   uint32_t* sk_flags;    // [sk_units][2 CTAs][4 row quadrants][2 column halves], zero before first use
   uint32_t sk_epoch;     // nonzero, distinct for every launch between two zeroings
@@ -188,6 +195,7 @@ size_t gemm_sk_flag_words();    // flags for the largest stream-K launch on this
 // forces it on whenever it is possible; H3_GEMM_SK_UNITS=<n> forces it with
 // n / row tiles pairs per row tile (at most one k-block per pair).
 int gemm_sk_lane(int M, int N, int K, int bn, int max_pairs);
+int gemm_sk_tail(int M, int N, int K, int bn, int* units);
 
 // Column tiling of one GEMM launch.  Uniform: num_n tiles of bn columns.
 // Balanced (plain and residual epilogues, when one wave of uniform tiles

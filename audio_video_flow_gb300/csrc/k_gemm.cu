@@ -768,6 +768,7 @@ __device__ __forceinline__ void epi_qkv(const GemmArgs& a, uint32_t tacc, int m,
 struct WorkItem {
   int tile, k0, k1;
   bool owner;      // holds k-block 0 of the tile: finishes the tile
+  bool sk;         // a stream-K piece (an owner then folds the partials of later runs)
 };
 
 // Stream-K runs: one lane of sk_lane pairs per 256-row tile (unit = m *
@@ -785,14 +786,36 @@ __device__ __forceinline__ bool work_item(const GemmArgs& a, int unit, int num_u
     w.k0 = 0;
     w.k1 = a.num_k;
     w.owner = true;
+    w.sk = false;
     return w.tile < num_tiles;
   }
-  const int lane_m = unit / a.sk_lane, j = unit - lane_m * a.sk_lane;
+  int j, base;
+  if (a.sk_tail) {
+    // whole tiles first (as in a whole-tile launch), then this pair's run of
+    // the one lane over the remaining tiles
+    const int n_dp = a.sk_dp / num_units;
+    if (i < n_dp) {
+      w.tile = unit + i * num_units;
+      w.k0 = 0;
+      w.k1 = a.num_k;
+      w.owner = true;
+      w.sk = false;
+      return true;
+    }
+    i -= n_dp;
+    j = unit;
+    base = a.sk_dp;
+  } else {
+    const int lane_m = unit / a.sk_lane;
+    j = unit - lane_m * a.sk_lane;
+    base = lane_m * a.num_n;         // m-major: (m, n) = (tile / num_n, tile % num_n)
+  }
   const long long start = sk_start(a, j), end = sk_start(a, j + 1);
   const int n = (int)(start / a.num_k) + i;
   const long long tb = (long long)n * a.num_k;
   if (tb >= end) return false;
-  w.tile = lane_m * a.num_n + n;     // m-major: (m, n) = (tile / num_n, tile % num_n)
+  w.tile = base + n;
+  w.sk = true;
   w.k0 = i == 0 ? (int)(start - tb) : 0;
   w.k1 = end - tb < a.num_k ? (int)(end - tb) : a.num_k;
   w.owner = w.k0 == 0;
@@ -859,7 +882,8 @@ __device__ __forceinline__ bool sk_fold_partials(const GemmArgs& a, uint32_t tac
   constexpr int NCH = BN / 32;
   static_assert(NCH % 4 == 0, "each column half is folded two chunks at a time");
   const int j = unit % a.sk_lane;
-  const long long tile_end = (long long)(tile % a.num_n + 1) * a.num_k;
+  const long long lane_tile = a.sk_tail ? tile - a.sk_dp : tile % a.num_n;   // the tile's place in the lane
+  const long long tile_end = (lane_tile + 1) * a.num_k;
   int j_end = j + 1;
   while (j_end < a.sk_lane && sk_start(a, j_end) < tile_end) ++j_end;
   const int q_end = unit + (j_end - j);
@@ -974,7 +998,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   const uint16_t pair_mask = 0x3;
   // tile `t` of this unit's walk -> (m_blk, n_blk) of this pair
   auto my_tile = [&](int t, int& m_blk, int& n_blk) {
-    if (args.sk_units > 0) {
+    if (args.sk_units > 0 && !args.sk_tail) {
       m_blk = t / args.num_n;
       n_blk = t - m_blk * args.num_n;
       return;
@@ -1138,7 +1162,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         if constexpr (BN == 256) sk_store_partial<EPI, BN>(args, tacc, unit, rank, q, half, row, lane);
       } else {
         if constexpr (BN == 256) {
-          if (args.sk_units > 0) {
+          if (args.sk_units > 0 && w.sk) {
             if (EPI == EPI_RESID)
               epi_resid_prefetch(args, m_blk * 2 * BM + (int)rank * BM + row, n_tile<EPI, BN>(args, n_blk), half);
             done = sk_fold_partials<EPI, BN>(args, tacc, unit, rank, q, half, row, lane, w.tile, abort_v);
@@ -1315,6 +1339,38 @@ int gemm_sk_lane(int M, int N, int K, int bn, int max_pairs) {
   return lane;
 }
 
+// Whole tiles, then stream-K over the tail: when whole 256-column tiles
+// take more than one wave and the last wave would leave more than a tenth of
+// the pairs idle (15,860 rows x 5376 columns: 1302 tiles, 17 waves of 76
+// pairs and 10 tiles), the tiles of every full wave but the last run whole,
+// and the rest (the last full wave and the partial one) are shared out over
+// all pairs as one stream-K lane, each pair's run following its whole tiles.
+// Returns the number of whole tiles (a multiple of *units), or -1 when the
+// split does not apply (it needs at least 8 k-blocks per pair in the tail).
+// H3_GEMM_SK=0 turns it off; H3_GEMM_SK_TAIL=n forces it with n pairs (tests).
+int gemm_sk_tail(int M, int N, int K, int bn, int* units) {
+  const char* env = getenv("H3_GEMM_SK");
+  if (env && env[0] == '0') return -1;
+  const long long tiles = (long long)gemm_m_tiles(M) * ((N + bn - 1) / bn);
+  const long long num_k = K / BK;
+  int slots = gemm_pair_slots();
+  const char* forced = getenv("H3_GEMM_SK_TAIL");
+  if (forced) {
+    const int f = atoi(forced);
+    if (f < 1 || f > slots) return -1;
+    slots = f;
+  } else {
+    if (slots < 1 || tiles <= slots) return -1;
+    const long long rem = tiles % slots;
+    if (rem == 0 || rem * 10 >= (long long)slots * 9) return -1;
+  }
+  const long long full = tiles / slots;
+  const long long dp = full > 0 ? (full - 1) * slots : 0;
+  if ((tiles - dp) * num_k < (forced ? 1LL : 8LL) * slots) return -1;
+  *units = slots;
+  return (int)dp;
+}
+
 // CTA pairs that can be resident at once.
 int gemm_pair_slots() {
   static int slots[64] = {0};
@@ -1407,9 +1463,9 @@ cudaError_t launch_gemm(int epi, int bn, const CUtensorMap& tmA, const CUtensorM
   if (e != cudaSuccess) return e;
   set_kernel_info("gemm_bf16_tc<%s,%d> tcgen05.mma.cta_group::2.kind::f16 pair-tile=%dx%dx%d stages=%d acc=f32 "
                   "tmem=2x%d grid=%d (pairs=%d of %d) tiles=%dx%d k_blocks=%d l2_prefetch=%d stream-k=%d "
-                  "l2-hint=%d n-widths=%s%d,%d,%d",
+                  "sk-whole-tiles=%d l2-hint=%d n-widths=%s%d,%d,%d",
                   names[epi], bn, 2 * BM, bn, BK, stages, bn, grid, pairs, slots, a.num_m, a.num_n, a.num_k,
-                  a.l2_pf, a.sk_units, a.l2_hint, a.nw1 ? "balanced:" : "uniform:",
+                  a.l2_pf, a.sk_units, a.sk_tail ? a.sk_dp : -1, a.l2_hint, a.nw1 ? "balanced:" : "uniform:",
                   a.nw1 ? a.nw1 : bn, a.ncnt1, a.nw2);
   return cudaGetLastError();
 }

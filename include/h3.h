@@ -39,7 +39,9 @@
  *     stream-K where whole tiles would leave SM pairs idle: their fp32 partial
  *     sums over k-ranges are added in k order, with split points fixed by the
  *     row-tile count and the resident SM-pair count (recorded in
- *     h3_last_kernel_info as stream-k=<pairs>).
+ *     h3_last_kernel_info as stream-k=<pairs>).  For long documents only the
+ *     tiles of the last waves are split that way; the others run whole
+ *     (sk-whole-tiles=<tiles> in the same record).
  */
 #ifndef H3_H_
 #define H3_H_

@@ -68,6 +68,11 @@ def test_denoiser_block0_sampled_rows(h3):
     y = torch.empty_like(x)
     h3.h3_block_forward(cfg, h3.make_weights(d_w), _meta(h3, meta_d, tc), x, y, ws)
     assert h3.h3_sync_check(timeout_ms=60000) == 0
+    # at this length the residual GEMMs run whole tiles and share the k-blocks
+    # of their last waves out over every pair (the sampled rows include rows
+    # of those tiles: the last row tiles, all columns)
+    info = h3.h3_last_kernel_info()
+    assert "stream-k=0" not in info and "sk-whole-tiles=-1" not in info, info
     got = to_np(y)[rows]
     mx, mn = errors(got, ref["y"])
     print(f"denoiser block 0, {rows.size} sampled rows: max_e={mx:.4f} mean_e={mn:.5f}")

@@ -372,6 +372,32 @@ def test_block_forward_stream_k(h3, name, units, monkeypatch):
     assert torch.equal(y, run_block(h3, c))
 
 
+@pytest.mark.parametrize("name,units", [("ragged205", 2), ("d576", 2), ("block505", 5), ("block505", 10),
+                                        ("block505", 76)])
+def test_block_forward_stream_k_tail(h3, name, units, monkeypatch):
+    """The residual GEMMs with whole tiles first and the rest shared out as
+    one stream-K lane over `units` pairs (the form long documents take when
+    their last wave is short, forced here on small shapes): every full wave
+    but the last runs whole tiles, and the remaining tiles' k-blocks are cut
+    into `units` runs whose partials are added in k order by the pair that
+    holds each tile's first k-block.  Against the oracle, and bitwise
+    repeatable."""
+    monkeypatch.setenv("H3_GEMM_SK_TAIL", str(units))
+    c = get_case(name)
+    y = run_block(h3, c)
+    info = h3.h3_last_kernel_info()
+    D = c.w.shape.dim
+    tiles = -(-c.S // 256) * -(-D // 256)
+    full = tiles // units
+    dp = (full - 1) * units if full > 0 else 0
+    assert f"stream-k={units} " in info and f"sk-whole-tiles={dp} " in info, info
+    if name == "block505":
+        assert_close(to_np(y), c.ref["y"], f"block[{name}] stream-k tail {units}", CHAIN_MAX_E, CHAIN_MEAN_E)
+    else:
+        assert_close(to_np(y), c.ref["y"], f"block[{name}] stream-k tail {units}")
+    assert torch.equal(y, run_block(h3, c))
+
+
 @pytest.mark.parametrize("name,units", [("block505", None), ("d576", "12"), ("ragged205", "6")])
 def test_norm2_fused_into_out_projection(h3, name, units, monkeypatch):
     """With H3_NORM_FUSE=1, where the O projection runs stream-K (every SM
