@@ -775,6 +775,9 @@ struct WorkItem {
 // sk_lane + j), all lanes walking the same column tiles and k-blocks at the
 // same time (weights shared across the row tiles in L2); pair j of a lane
 // takes k-blocks [j, j + 1) * sk_iters / sk_lane of the lane's num_n x num_k.
+// In the tail form (sk_tail) pair j first runs its whole tiles j + i *
+// sk_units of the first sk_dp tiles, then k-blocks [j, j + 1) * sk_iters /
+// sk_units of the one lane over the tiles that follow.
 __device__ __forceinline__ long long sk_start(const GemmArgs& a, int j) {
   return (long long)j * a.sk_iters / a.sk_lane;
 }
